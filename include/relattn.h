@@ -1,0 +1,150 @@
+/*
+ * relattn.h -- C ABI of the GB300 relative-attention forward library
+ *              (librelattn.so, built for sm_103a).
+ *
+ * The operation (page "SGLang and Miles Add Day-0 Support for Inkling",
+ * section "Attention with Relative Positional Embedding"): every query row
+ * carries a relative feature r_{t,h}; a learned projection P turns it into
+ * relative logits indexed by causal distance d,
+ *
+ *     rel_logits(t,h,d) = sum_c r[t,h,c] * P[c,d],          0 <= d < rel_extent,
+ *
+ * and the attention logit of query i, key j, head h is
+ *
+ *     l(i,j,h) = alpha * q_i . k_j + [0 <= i-j < rel_extent] * rel_logits(i,h,i-j).
+ *
+ * Future keys are masked; distances at or past rel_extent add no bias.
+ * Sliding-window layers (same section, paragraph "Attention layout") keep key
+ * j only when i - j < window.  Full layers may scale q and the relative logits
+ * by a length-dependent factor; the page gives no formula, and this library
+ * uses s(i) = max(1, ln(i+1)/ln(log_scale_base)), which multiplies the whole
+ * logit.  All layers are GQA with head size 128 (page "vLLM Day-0 support for
+ * TML Inkling", attention paragraph): query head h reads kv head
+ * h / (num_heads_q / num_heads_kv).
+ *
+ * Outputs: out = softmax-weighted sum of v (bf16) and the per-row natural-log
+ * logsumexp of the logits (fp32).
+ *
+ * Positions are bottom-right aligned: query row t of sequence b sits at
+ * position (Lk_b - Lq_b) + t, where Lq_b / Lk_b come from cu_seqlens_q / _k.
+ * Prefill has Lq_b == Lk_b; decode (<= 16 query rows, e.g. an MTP verify of 9
+ * positions) has Lq_b <= Lk_b and the rows are causal among themselves.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or synchronises; work is enqueued on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream) and returns immediately.
+ *   - Every function returns a relattn_status; nothing aborts or throws.
+ *     Argument errors are found on the host before any launch.  cu_seqlens
+ *     contents live on the device and are checked by the kernels: a sequence
+ *     with Lk < Lq or lengths above max_seqlen_* is skipped and recorded in a
+ *     device error word that relattn_get_device_error() reads.
+ *   - Layouts are row-major with the last dimension contiguous:
+ *       q   [total_q, num_heads_q,  128]        bf16
+ *       k,v [total_k, num_heads_kv, 128]        bf16
+ *       r   [total_q, num_heads_q,  r_dim]      bf16
+ *       P   [r_dim, rel_extent]                 bf16 (shared by all heads)
+ *       out [total_q, num_heads_q,  128]        bf16
+ *       lse [num_heads_q, total_q]              fp32
+ *     q, k, v, out must be 16-byte aligned.
+ */
+#ifndef RELATTN_H
+#define RELATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RELATTN_OK = 0,
+  RELATTN_ERR_INVALID_ARG = 1,  /* a pointer, size or flag is out of range      */
+  RELATTN_ERR_UNSUPPORTED = 2,  /* valid attention, but outside what is built   */
+  RELATTN_ERR_CUDA = 3,         /* a CUDA call or kernel launch failed          */
+  RELATTN_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up           */
+  RELATTN_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required   */
+  RELATTN_ERR_DEVICE_ARGS = 6   /* kernels found inconsistent cu_seqlens        */
+} relattn_status;
+
+typedef struct relattn_params {
+  const void *q;               /* bf16 [total_q, num_heads_q, 128]                  */
+  const void *k;               /* bf16 [total_k, num_heads_kv, 128]                 */
+  const void *v;               /* bf16 [total_k, num_heads_kv, 128]                 */
+  const void *r;               /* bf16 [total_q, num_heads_q, r_dim]                */
+  const void *P;               /* bf16 [r_dim, rel_extent]                          */
+  const int32_t *cu_seqlens_q; /* device int32 [batch+1], query rows per sequence    */
+  const int32_t *cu_seqlens_k; /* device int32 [batch+1], keys per sequence          */
+  int32_t batch;               /* number of sequences                                */
+  int32_t total_q;             /* cu_seqlens_q[batch] (host copy; sizes lse)         */
+  int32_t total_k;             /* cu_seqlens_k[batch] (host copy)                    */
+  int32_t max_seqlen_q;        /* upper bound on any Lq_b                            */
+  int32_t max_seqlen_k;        /* upper bound on any Lk_b                            */
+  int32_t num_heads_q;
+  int32_t num_heads_kv;        /* divides num_heads_q                                */
+  int32_t head_dim;            /* must be 128                                        */
+  int32_t r_dim;               /* 0..64 (0: no relative bias)                        */
+  int32_t rel_extent;          /* E >= 0: distances 0..E-1 carry bias                */
+  int32_t window;              /* <= 0: full attention; else keep 0 <= i-j < window  */
+  float alpha;                 /* logit scale, e.g. 1/sqrt(128)                      */
+  float log_scale_base;        /* <= 0: off; else > 1, s(i)=max(1,ln(i+1)/ln(base))  */
+  void *out;                   /* bf16 [total_q, num_heads_q, 128]                   */
+  float *lse;                  /* fp32 [num_heads_q, total_q], natural log           */
+  void *workspace;             /* decode split partials (device), may be NULL        */
+  size_t workspace_bytes;
+  int32_t num_splits;          /* decode: 0 = choose automatically                   */
+} relattn_params;
+
+/*
+ * Prefill / chunked prefill: any Lq_b <= Lk_b.  rows are grouped into 128-row
+ * query tiles per head; key tiles outside the causal / window range are
+ * skipped.  Needs no workspace.
+ */
+relattn_status relattn_prefill(const relattn_params *params, void *stream);
+
+/*
+ * Decode: max_seqlen_q <= 16 query rows per sequence against a long KV
+ * (page "vLLM Day-0 support for TML Inkling", FA4-with-sheared-bias paragraph:
+ * the KV range is cut into num_splits pieces chosen from batch and KV length).
+ * Each split writes a partial (out, lse) to the workspace and a combine kernel
+ * merges them by their logsumexp.  num_splits = 0 picks the split count; the
+ * chosen count is the one relattn_decode_workspace_size() sizes for.
+ */
+relattn_status relattn_decode(const relattn_params *params, void *stream);
+
+/* Workspace bytes relattn_decode needs for these params (0 when unsplit). */
+relattn_status relattn_decode_workspace_size(const relattn_params *params, size_t *bytes);
+
+/* The split count relattn_decode will use for these params. */
+relattn_status relattn_decode_num_splits(const relattn_params *params, int32_t *num_splits);
+
+/*
+ * Log-sum-exp combine of split partials (the decode combine step, exposed so
+ * partials from several KV shards can be merged):
+ *   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.
+ * o_part  fp32 [num_splits, rows, 128]   (normalised partial outputs)
+ * lse_part fp32 [num_splits, rows]        (-inf marks an empty partial)
+ * out bf16 [rows, 128]; lse fp32 with element (row) at lse[row_to_lse(row)]
+ * where rows are ordered (t, h) and lse is [num_heads, total_q]:
+ * row = t * num_heads + h  ->  lse[h * total_q + t].
+ */
+relattn_status relattn_combine(const float *o_part, const float *lse_part, int32_t num_splits,
+                               int32_t total_q, int32_t num_heads, void *out, float *lse,
+                               void *stream);
+
+/* Reads and clears the device error word (RELATTN_OK when clean).  Synchronises
+ * `stream` to read it. */
+relattn_status relattn_get_device_error(void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *relattn_status_string(relattn_status status);
+
+/* Library version, e.g. "relattn 0.1 sm_103a". */
+const char *relattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RELATTN_H */

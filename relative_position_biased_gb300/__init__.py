@@ -1,0 +1,222 @@
+"""GB300 relative-attention forward (Inkling-style relative position bias).
+
+A thin ctypes binding over ``librelattn.so`` (C ABI in ``include/relattn.h``).
+Functions named ``relattn_*`` mirror the C entry points one to one and only
+marshal arguments; ``prefill`` / ``decode`` are conveniences that also allocate
+``out`` / ``lse`` / workspace with torch (device memory is torch's job) before
+calling the same entry points.  Every step of the computation runs in the CUDA
+kernels; if the library is missing these functions raise -- there is no
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+from . import workloads  # noqa: F401  (seeded input generators)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librelattn.so")
+
+RELATTN_OK = 0
+STATUS_NAMES = {
+    0: "RELATTN_OK", 1: "RELATTN_ERR_INVALID_ARG", 2: "RELATTN_ERR_UNSUPPORTED",
+    3: "RELATTN_ERR_CUDA", 4: "RELATTN_ERR_TIMEOUT", 5: "RELATTN_ERR_WORKSPACE",
+    6: "RELATTN_ERR_DEVICE_ARGS",
+}
+EXPORTED = (
+    "relattn_prefill", "relattn_decode", "relattn_decode_workspace_size",
+    "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
+    "relattn_status_string", "relattn_version",
+)
+
+
+class RelattnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class RelattnParams(ctypes.Structure):
+    """Mirror of ``relattn_params`` (field order and types must match the header)."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("r", ctypes.c_void_p), ("P", ctypes.c_void_p),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("batch", ctypes.c_int32), ("total_q", ctypes.c_int32), ("total_k", ctypes.c_int32),
+        ("max_seqlen_q", ctypes.c_int32), ("max_seqlen_k", ctypes.c_int32),
+        ("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("r_dim", ctypes.c_int32), ("rel_extent", ctypes.c_int32),
+        ("window", ctypes.c_int32), ("alpha", ctypes.c_float), ("log_scale_base", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("num_splits", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    from .buildlib import build as _build
+    return _build(force=force)
+
+
+def _open(path: str):
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with relative_position_biased_gb300.build()")
+    return ctypes.CDLL(path)
+
+
+def load_library(path: Optional[str] = None):
+    """Load ``librelattn.so`` (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = _open(path or LIB_PATH)
+        P, vp = ctypes.POINTER(RelattnParams), ctypes.c_void_p
+        for name in ("relattn_prefill", "relattn_decode"):
+            f = getattr(lib, name)
+            f.argtypes, f.restype = [P, vp], ctypes.c_int
+        lib.relattn_decode_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        lib.relattn_decode_workspace_size.restype = ctypes.c_int
+        lib.relattn_decode_num_splits.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+        lib.relattn_decode_num_splits.restype = ctypes.c_int
+        lib.relattn_combine.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        vp, vp, vp]
+        lib.relattn_combine.restype = ctypes.c_int
+        lib.relattn_get_device_error.argtypes = [vp]
+        lib.relattn_get_device_error.restype = ctypes.c_int
+        lib.relattn_status_string.argtypes = [ctypes.c_int]
+        lib.relattn_status_string.restype = ctypes.c_char_p
+        lib.relattn_version.argtypes = []
+        lib.relattn_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != RELATTN_OK:
+        raise RelattnError(status, where)
+
+
+# ------------------------------------------------------------------ C mirrors
+
+def relattn_prefill(params: RelattnParams, stream: int = 0) -> int:
+    return load_library().relattn_prefill(ctypes.byref(params), ctypes.c_void_p(stream))
+
+
+def relattn_decode(params: RelattnParams, stream: int = 0) -> int:
+    return load_library().relattn_decode(ctypes.byref(params), ctypes.c_void_p(stream))
+
+
+def relattn_decode_workspace_size(params: RelattnParams) -> Tuple[int, int]:
+    n = ctypes.c_size_t(0)
+    st = load_library().relattn_decode_workspace_size(ctypes.byref(params), ctypes.byref(n))
+    return st, int(n.value)
+
+
+def relattn_decode_num_splits(params: RelattnParams) -> Tuple[int, int]:
+    n = ctypes.c_int32(0)
+    st = load_library().relattn_decode_num_splits(ctypes.byref(params), ctypes.byref(n))
+    return st, int(n.value)
+
+
+def relattn_combine(o_part: int, lse_part: int, num_splits: int, total_q: int, num_heads: int,
+                    out: int, lse: int, stream: int = 0) -> int:
+    return load_library().relattn_combine(o_part, lse_part, num_splits, total_q, num_heads,
+                                          out, lse, ctypes.c_void_p(stream))
+
+
+def relattn_get_device_error(stream: int = 0) -> int:
+    return load_library().relattn_get_device_error(ctypes.c_void_p(stream))
+
+
+def relattn_status_string(status: int) -> str:
+    return load_library().relattn_status_string(status).decode()
+
+
+def relattn_version() -> str:
+    return load_library().relattn_version().decode()
+
+
+# ------------------------------------------------------------------ torch conveniences
+
+def make_params(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int,
+                max_seqlen_k: int, alpha: float, window: int = 0, log_scale_base: float = 0.0,
+                out=None, lse=None, workspace=None, num_splits: int = 0,
+                total_q: Optional[int] = None, total_k: Optional[int] = None) -> RelattnParams:
+    """Fill a RelattnParams from torch tensors (pointers and sizes only)."""
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+    r_dim = int(r.shape[-1]) if r is not None and r.dim() == 3 else 0
+    E = int(P.shape[-1]) if P is not None and P.dim() == 2 else 0
+    return RelattnParams(
+        q=ptr(q), k=ptr(k), v=ptr(v), r=ptr(r), P=ptr(P),
+        cu_seqlens_q=ptr(cu_seqlens_q), cu_seqlens_k=ptr(cu_seqlens_k),
+        batch=int(cu_seqlens_q.numel()) - 1,
+        total_q=int(q.shape[0]) if total_q is None else int(total_q),
+        total_k=int(k.shape[0]) if total_k is None else int(total_k),
+        max_seqlen_q=int(max_seqlen_q), max_seqlen_k=int(max_seqlen_k),
+        num_heads_q=int(q.shape[1]), num_heads_kv=int(k.shape[1]), head_dim=int(q.shape[2]),
+        r_dim=r_dim, rel_extent=E, window=int(window), alpha=float(alpha),
+        log_scale_base=float(log_scale_base), out=ptr(out), lse=ptr(lse),
+        workspace=ptr(workspace),
+        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+        num_splits=int(num_splits))
+
+
+def _current_stream() -> int:
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _outputs(q, out, lse):
+    import torch
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[1], q.shape[0], dtype=torch.float32, device=q.device)
+    return out, lse
+
+
+def prefill(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int, max_seqlen_k: int,
+            alpha: float, window: int = 0, log_scale_base: float = 0.0, out=None, lse=None,
+            stream: Optional[int] = None):
+    """Relative-attention prefill on device tensors; returns (out, lse[Hq, Tq])."""
+    out, lse = _outputs(q, out, lse)
+    prm = make_params(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=max_seqlen_q,
+                      max_seqlen_k=max_seqlen_k, alpha=alpha, window=window,
+                      log_scale_base=log_scale_base, out=out, lse=lse)
+    _check(relattn_prefill(prm, _current_stream() if stream is None else stream), "relattn_prefill")
+    return out, lse
+
+
+def decode_workspace(params: RelattnParams, device):
+    import torch
+    st, nbytes = relattn_decode_workspace_size(params)
+    _check(st, "relattn_decode_workspace_size")
+    if nbytes == 0:
+        return None
+    return torch.empty((nbytes + 3) // 4, dtype=torch.float32, device=device)
+
+
+def decode(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int, max_seqlen_k: int,
+           alpha: float, window: int = 0, log_scale_base: float = 0.0, num_splits: int = 0,
+           out=None, lse=None, workspace=None, stream: Optional[int] = None):
+    """Split-KV decode (<= 16 query rows per sequence); returns (out, lse[Hq, Tq])."""
+    out, lse = _outputs(q, out, lse)
+    prm = make_params(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=max_seqlen_q,
+                      max_seqlen_k=max_seqlen_k, alpha=alpha, window=window,
+                      log_scale_base=log_scale_base, out=out, lse=lse, num_splits=num_splits)
+    if workspace is None:
+        workspace = decode_workspace(prm, q.device)
+    if workspace is not None:
+        prm.workspace = workspace.data_ptr()
+        prm.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(relattn_decode(prm, _current_stream() if stream is None else stream), "relattn_decode")
+    return out, lse

@@ -1,0 +1,263 @@
+// api.cu -- the C ABI (include/relattn.h): argument checks, split planning,
+// kernel dispatch.  No allocation, no synchronisation (except the explicit
+// relattn_get_device_error), no host fallback.
+#include <math.h>
+
+#include <mutex>
+
+#include "launch.h"
+
+using namespace relattn;
+
+namespace {
+
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_ptr[kMaxDevices];
+int g_sms[kMaxDevices];
+
+relattn_status device_state(int *dev_out, int **err_out, int *sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RELATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return RELATTN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return RELATTN_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int *>(p);
+    g_sms[dev] = sms;
+  }
+  if (dev_out) *dev_out = dev;
+  if (err_out) *err_out = g_err_ptr[dev];
+  if (sms_out) *sms_out = g_sms[dev];
+  return RELATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxRDim = 64;
+constexpr int kMaxDecodeRows = 16;
+
+relattn_status validate(const relattn_params *p, bool decode) {
+  if (!p) return RELATTN_ERR_INVALID_ARG;
+  if (p->head_dim != kHeadDim) return RELATTN_ERR_UNSUPPORTED;
+  if (p->num_heads_q <= 0 || p->num_heads_kv <= 0 || p->num_heads_q % p->num_heads_kv != 0)
+    return RELATTN_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->max_seqlen_q < 0 ||
+      p->max_seqlen_k < 0 || p->rel_extent < 0 || p->r_dim < 0)
+    return RELATTN_ERR_INVALID_ARG;
+  if (p->r_dim > kMaxRDim) return RELATTN_ERR_UNSUPPORTED;
+  if (!isfinite(p->alpha)) return RELATTN_ERR_INVALID_ARG;
+  if (!(p->log_scale_base <= 0.f || (p->log_scale_base > 1.f && isfinite(p->log_scale_base))))
+    return RELATTN_ERR_INVALID_ARG;
+  if (decode && p->max_seqlen_q > kMaxDecodeRows) return RELATTN_ERR_UNSUPPORTED;
+  if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
+  if (p->max_seqlen_q <= 0 || p->max_seqlen_k < p->max_seqlen_q) return RELATTN_ERR_INVALID_ARG;
+  if (!p->q || !p->k || !p->v || !p->out || !p->lse || !p->cu_seqlens_q || !p->cu_seqlens_k)
+    return RELATTN_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->out))
+    return RELATTN_ERR_INVALID_ARG;
+  if (p->r_dim > 0 && p->rel_extent > 0 && (!p->r || !p->P)) return RELATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(p->lse) & 3u) != 0) return RELATTN_ERR_INVALID_ARG;
+  return RELATTN_OK;
+}
+
+relattn_status make_args(const relattn_params *p, KernelArgs *a) {
+  int *err = nullptr;
+  relattn_status st = device_state(nullptr, &err, nullptr);
+  if (st != RELATTN_OK) return st;
+  KernelArgs &x = *a;
+  x = KernelArgs{};
+  x.q = static_cast<const __nv_bfloat16 *>(p->q);
+  x.k = static_cast<const __nv_bfloat16 *>(p->k);
+  x.v = static_cast<const __nv_bfloat16 *>(p->v);
+  x.r = static_cast<const __nv_bfloat16 *>(p->r);
+  x.P = static_cast<const __nv_bfloat16 *>(p->P);
+  x.cu_q = p->cu_seqlens_q;
+  x.cu_k = p->cu_seqlens_k;
+  x.out = static_cast<__nv_bfloat16 *>(p->out);
+  x.lse = p->lse;
+  x.err = err;
+  x.batch = p->batch;
+  x.total_q = p->total_q;
+  x.max_q = p->max_seqlen_q;
+  x.max_k = p->max_seqlen_k;
+  x.Hq = p->num_heads_q;
+  x.Hkv = p->num_heads_kv;
+  x.group = p->num_heads_q / p->num_heads_kv;
+  const bool bias = p->r_dim > 0 && p->rel_extent > 0;
+  x.rd = bias ? p->r_dim : 0;
+  x.rd_pad = bias ? (p->r_dim + 15) / 16 * 16 : 0;
+  x.E = bias ? p->rel_extent : 0;
+  x.window = p->window > 0 ? p->window : 0;
+  x.alpha_log2e = p->alpha * kLog2e;
+  x.inv_ln_base = p->log_scale_base > 1.f ? 1.f / logf(p->log_scale_base) : 0.f;
+  x.r_vec_ok = bias && (p->r_dim % 8 == 0) && aligned16(p->r);
+  x.p_vec_ok = bias && (p->rel_extent % 8 == 0) && aligned16(p->P);
+  x.num_splits = 1;
+  x.split_chunk = 0;
+  x.q_tiles = (p->max_seqlen_q + 127) / 128;
+  x.row_blocks = 1;
+  return RELATTN_OK;
+}
+
+struct DecodePlan {
+  int warps, row_blocks, splits, chunk;
+  size_t ws_bytes, lse_offset;
+};
+
+relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
+  int sms = 0;
+  relattn_status st = device_state(nullptr, nullptr, &sms);
+  if (st != RELATTN_OK) return st;
+  const int group = p->num_heads_q / p->num_heads_kv;
+  const int rows = p->max_seqlen_q * group;
+  plan->warps = decode_warps_for_rows(rows < 128 ? rows : 128);
+  const int m = plan->warps * 16;
+  plan->row_blocks = (rows + m - 1) / m;
+  const int tile = kDecodeKeyTile;
+  // keys any CTA of one (sequence, kv head) may visit, from an aligned start
+  long max_vis = p->max_seqlen_k;
+  if (p->window > 0) {
+    const long w = (long)p->window + p->max_seqlen_q - 1 + (tile - 1);
+    if (w < max_vis) max_vis = w;
+  }
+  if (max_vis < 1) max_vis = 1;
+  const long units = (long)p->batch * p->num_heads_kv * plan->row_blocks;
+  long splits = p->num_splits;
+  if (splits <= 0) {
+    const long target = 2L * sms;                       // about two waves of CTAs
+    splits = (target + units - 1) / units;
+    const long cap = (max_vis + 255) / 256;             // at least 256 keys per split
+    if (splits > cap) splits = cap;
+    if (splits < 1) splits = 1;
+  }
+  long chunk = (max_vis + splits - 1) / splits;
+  chunk = (chunk + tile - 1) / tile * tile;
+  splits = (max_vis + chunk - 1) / chunk;
+  if (splits > 65535) return RELATTN_ERR_UNSUPPORTED;
+  plan->splits = (int)splits;
+  plan->chunk = (int)chunk;
+  if (plan->splits > 1) {
+    const size_t rows_all = (size_t)p->total_q * p->num_heads_q;
+    const size_t o_bytes = (size_t)plan->splits * rows_all * kHeadDim * sizeof(float);
+    plan->lse_offset = (o_bytes + 255) / 256 * 256;
+    plan->ws_bytes = plan->lse_offset + (size_t)plan->splits * rows_all * sizeof(float);
+  } else {
+    plan->lse_offset = 0;
+    plan->ws_bytes = 0;
+  }
+  return RELATTN_OK;
+}
+
+relattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? RELATTN_OK : RELATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+relattn_status relattn_prefill(const relattn_params *p, void *stream) {
+  relattn_status st = validate(p, false);
+  if (st != RELATTN_OK) return st;
+  if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
+  KernelArgs a;
+  if ((st = make_args(p, &a)) != RELATTN_OK) return st;
+  return cuda_status(launch_prefill_mma(a, static_cast<cudaStream_t>(stream)));
+}
+
+relattn_status relattn_decode_workspace_size(const relattn_params *p, size_t *bytes) {
+  if (!bytes) return RELATTN_ERR_INVALID_ARG;
+  relattn_status st = validate(p, true);
+  if (st != RELATTN_OK) return st;
+  *bytes = 0;
+  if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
+  DecodePlan plan;
+  if ((st = plan_decode(p, &plan)) != RELATTN_OK) return st;
+  *bytes = plan.ws_bytes;
+  return RELATTN_OK;
+}
+
+relattn_status relattn_decode_num_splits(const relattn_params *p, int32_t *num_splits) {
+  if (!num_splits) return RELATTN_ERR_INVALID_ARG;
+  relattn_status st = validate(p, true);
+  if (st != RELATTN_OK) return st;
+  *num_splits = 1;
+  if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
+  DecodePlan plan;
+  if ((st = plan_decode(p, &plan)) != RELATTN_OK) return st;
+  *num_splits = plan.splits;
+  return RELATTN_OK;
+}
+
+relattn_status relattn_decode(const relattn_params *p, void *stream) {
+  relattn_status st = validate(p, true);
+  if (st != RELATTN_OK) return st;
+  if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
+  DecodePlan plan;
+  if ((st = plan_decode(p, &plan)) != RELATTN_OK) return st;
+  KernelArgs a;
+  if ((st = make_args(p, &a)) != RELATTN_OK) return st;
+  a.num_splits = plan.splits;
+  a.split_chunk = plan.chunk;
+  a.row_blocks = plan.row_blocks;
+  if (plan.splits > 1) {
+    if (!p->workspace || p->workspace_bytes < plan.ws_bytes || !aligned16(p->workspace))
+      return RELATTN_ERR_WORKSPACE;
+    a.o_part = static_cast<float *>(p->workspace);
+    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + plan.lse_offset);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = cuda_status(launch_decode_mma(a, plan.warps, s))) != RELATTN_OK) return st;
+  if (plan.splits > 1)
+    st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
+                                    p->num_heads_q, a.out, a.lse, s));
+  return st;
+}
+
+relattn_status relattn_combine(const float *o_part, const float *lse_part, int32_t num_splits,
+                               int32_t total_q, int32_t num_heads, void *out, float *lse,
+                               void *stream) {
+  if (num_splits <= 0 || total_q < 0 || num_heads <= 0) return RELATTN_ERR_INVALID_ARG;
+  if (total_q == 0) return RELATTN_OK;
+  if (!o_part || !lse_part || !out || !lse || !aligned16(o_part) || !aligned16(out))
+    return RELATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(o_part, lse_part, num_splits, total_q, num_heads,
+                                    static_cast<__nv_bfloat16 *>(out), lse,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+relattn_status relattn_get_device_error(void *stream) {
+  int *err = nullptr;
+  relattn_status st = device_state(nullptr, &err, nullptr);
+  if (st != RELATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RELATTN_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return RELATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RELATTN_ERR_CUDA;
+  if (host & kDevErrTimeout) return RELATTN_ERR_TIMEOUT;
+  if (host & kDevErrSeqlens) return RELATTN_ERR_DEVICE_ARGS;
+  return RELATTN_OK;
+}
+
+const char *relattn_status_string(relattn_status s) {
+  switch (s) {
+    case RELATTN_OK: return "RELATTN_OK";
+    case RELATTN_ERR_INVALID_ARG: return "RELATTN_ERR_INVALID_ARG";
+    case RELATTN_ERR_UNSUPPORTED: return "RELATTN_ERR_UNSUPPORTED";
+    case RELATTN_ERR_CUDA: return "RELATTN_ERR_CUDA";
+    case RELATTN_ERR_TIMEOUT: return "RELATTN_ERR_TIMEOUT";
+    case RELATTN_ERR_WORKSPACE: return "RELATTN_ERR_WORKSPACE";
+    case RELATTN_ERR_DEVICE_ARGS: return "RELATTN_ERR_DEVICE_ARGS";
+  }
+  return "RELATTN_ERR_UNKNOWN";
+}
+
+const char *relattn_version(void) { return "relattn 0.1 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,23 @@
+// launch.h -- internal launchers called by the C ABI layer (api.cu).
+#pragma once
+
+#include "common.cuh"
+
+namespace relattn {
+
+// Query rows per decode CTA for a given row count (max_seqlen_q * group).
+int decode_warps_for_rows(int rows);
+
+// Per-split key-chunk granularity (keys per tile) of the decode kernels.
+constexpr int kDecodeKeyTile = 64;
+
+size_t prefill_mma_smem_bytes(int rd_pad);
+size_t decode_mma_smem_bytes(int warps, int rd_pad);
+
+cudaError_t launch_prefill_mma(const KernelArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_mma(const KernelArgs &a, int warps, cudaStream_t stream);
+cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits,
+                           int total_q, int num_heads, __nv_bfloat16 *out, float *lse,
+                           cudaStream_t stream);
+
+}  // namespace relattn

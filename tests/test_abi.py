@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads,
+exports every symbol the header declares, and rejects bad arguments before
+touching the device."""
+import os
+import re
+
+import pytest
+import torch
+
+import relative_position_biased_gb300 as rpb
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rpb.build()
+    return rpb.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "relattn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(relattn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("relattn_prefill", "relattn_decode", "relattn_combine"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) <= set(rpb.EXPORTED)
+
+
+def test_struct_layout_matches_header(lib):
+    # 7 pointers, 11 int32, 2 floats, then out/lse/workspace, size_t, int32
+    off = {f[0]: getattr(rpb.RelattnParams, f[0]).offset for f in rpb.RelattnParams._fields_}
+    assert off["batch"] == 56 and off["alpha"] == 100 and off["out"] == 112
+    assert off["workspace_bytes"] == 136 and off["num_splits"] == 144
+
+
+def test_status_strings(lib):
+    for code, name in rpb.STATUS_NAMES.items():
+        assert rpb.relattn_status_string(code) == name
+    assert "sm_103a" in rpb.relattn_version()
+
+
+def _params(**over):
+    base = dict(q=256, k=256, v=256, r=256, P=256, cu_seqlens_q=256, cu_seqlens_k=256, batch=1,
+                total_q=8, total_k=8, max_seqlen_q=8, max_seqlen_k=8, num_heads_q=4,
+                num_heads_kv=2, head_dim=128, r_dim=32, rel_extent=64, window=0,
+                alpha=0.088, log_scale_base=0.0, out=256, lse=256, workspace=None,
+                workspace_bytes=0, num_splits=0)
+    base.update(over)
+    return rpb.RelattnParams(**base)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(head_dim=64), 2),
+    (dict(num_heads_q=3), 1),
+    (dict(num_heads_kv=0), 1),
+    (dict(r_dim=65), 2),
+    (dict(r_dim=-1), 1),
+    (dict(rel_extent=-1), 1),
+    (dict(log_scale_base=0.5), 1),
+    (dict(log_scale_base=1.0), 1),
+    (dict(alpha=float("nan")), 1),
+    (dict(q=None), 1),
+    (dict(lse=None), 1),
+    (dict(cu_seqlens_k=None), 1),
+    (dict(P=None), 1),
+    (dict(q=264), 1),            # not 16-byte aligned
+    (dict(out=258), 1),
+    (dict(max_seqlen_k=4), 1),   # below max_seqlen_q
+    (dict(batch=-1), 1),
+])
+def test_prefill_rejects_bad_arguments(lib, over, expect):
+    assert rpb.relattn_prefill(_params(**over)) == expect
+
+
+def test_decode_rejects_too_many_rows(lib):
+    assert rpb.relattn_decode(_params(max_seqlen_q=17, max_seqlen_k=100)) == 2
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert rpb.relattn_prefill(_params(batch=0, total_q=0)) == 0
+    assert rpb.relattn_decode(_params(total_q=0)) == 0
+
+
+def test_combine_rejects_bad_arguments(lib):
+    assert rpb.relattn_combine(0, 0, 0, 1, 1, 0, 0) == 1
+    assert rpb.relattn_combine(256, 256, 2, 4, 0, 256, 256) == 1
+    assert rpb.relattn_combine(264, 256, 2, 4, 2, 256, 256) == 1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        rpb._open(str(tmp_path / "librelattn.so"))
+
+
+def test_workload_generator_is_deterministic():
+    from relative_position_biased_gb300 import workloads as W
+    w = W.custom("det", [10, 3], [10, 3], 2, 1, 4, 8, seed=3)
+    a, b = W.make_inputs(w), W.make_inputs(w)
+    for k in a:
+        assert torch.equal(a[k], b[k])
+    assert a["q"].dtype == torch.bfloat16 and a["cu_seqlens_q"].tolist() == [0, 10, 13]

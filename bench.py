@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Benchmark of the relative-attention forward on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. prefill of the sliding-window workload (4 x 8192 tokens, Hq=16, Hkv=2,
+     window 4096, r_dim 64, E 1024) -- rel projection, QK^T, bias gather,
+     mask, online softmax, PV, epilogue;
+  2. split-KV decode + LSE combine of the long-context MTP verify
+     (9 query rows against 1,048,576 keys, log-scale);
+  3. split-KV decode + LSE combine of the batched decode
+     (64 sequences, 1 query row each, KV lengths U[1024, 32768]).
+`value` is the prefill throughput (TFLOP/s, algorithmic flops over the
+prefill kernel time); the decode HBM throughput (GB/s of visible K/V over the
+decode call time) is reported beside it.  L2 is flushed by a 256 MiB write
+before every timed kernel; the flush is outside the timed events.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (independent replicas, weak scaling); ranks meet only for the timing
+barrier and the max-over-ranks of the elapsed time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from relative_position_biased_gb300 import accounting as A  # noqa: E402
+from relative_position_biased_gb300 import workloads as W  # noqa: E402
+
+METRIC = "relattn prefill TFLOP/s & decode HBM GB/s at 1 GB300; % of roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "prefill": ["relative_position_biased_gb300/csrc/fwd_mma.cu",
+                "relative_position_biased_gb300/csrc/common.cuh"],
+    "decode": ["relative_position_biased_gb300/csrc/fwd_mma.cu",
+               "relative_position_biased_gb300/csrc/common.cuh"],
+}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def src_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_PATH):
+        return json.load(open(PEAKS_PATH)), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def load_traffic(kind: str):
+    """dram bytes per launch from a committed ncu summary, if it is current."""
+    try:
+        t = json.load(open(TRAFFIC_PATH)).get(kind)
+    except (OSError, ValueError):
+        return None
+    if not t or t.get("src_sha") != src_sha(kind):
+        return None
+    return t.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return ws, rank, local
+
+
+def init_dist(ws: int, local: int):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return dist
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+
+def step_workloads():
+    return {"prefill": W.swa_prefill(), "decode_long": W.decode_mtp_long(),
+            "decode_batched": W.decode_batched()}
+
+
+def _kw(w):
+    return dict(max_seqlen_q=max(w.q_lens), max_seqlen_k=max(w.k_lens), alpha=w.alpha,
+                window=w.window, log_scale_base=w.log_scale_base)
+
+
+ARG_ORDER = ("q", "k", "v", "r", "P", "cu_seqlens_q", "cu_seqlens_k")
+
+
+class Phase:
+    """One timed call of the library on device-resident inputs."""
+
+    def __init__(self, name, w, host_inputs, rpb):
+        self.name, self.w, self.rpb = name, w, rpb
+        self.host = host_inputs
+        self.dev = {k: v.cuda() for k, v in host_inputs.items()}
+        self.args = [self.dev[k] for k in ARG_ORDER]
+        self.out = torch.empty_like(self.dev["q"])
+        self.lse = torch.empty(self.dev["q"].shape[1], self.dev["q"].shape[0],
+                               dtype=torch.float32, device="cuda")
+        self.decode = w.is_decode
+        self.ws = None
+        self.launches = 1
+        if self.decode:
+            prm = rpb.make_params(*self.args, out=self.out, lse=self.lse, **_kw(w))
+            self.ws = rpb.decode_workspace(prm, "cuda")
+            st, splits = rpb.relattn_decode_num_splits(prm)
+            self.splits = splits
+            self.launches = 1 + (1 if splits > 1 else 0)
+        self.flops = A.flops(w)
+        self.bytes = A.kv_bytes(w)
+        io = A.io_bytes(w)
+        self.h2d, self.d2h = io["h2d"], io["d2h"]
+
+    def run(self, args=None, out=None, lse=None):
+        args = self.args if args is None else args
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
+        if self.decode:
+            self.rpb.decode(*args, out=out, lse=lse, workspace=self.ws, **_kw(self.w))
+        else:
+            self.rpb.prefill(*args, out=out, lse=lse, **_kw(self.w))
+
+
+def timed_steps(phases, steps, flush):
+    """Run `steps` steps; return per-phase lists of kernel times (ms)."""
+    stream = torch.cuda.current_stream()
+    times = {p.name: [] for p in phases}
+    events = []
+    for _ in range(steps):
+        for p in phases:
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            p.run()
+            b.record(stream)
+            events.append((p.name, a, b))
+    torch.cuda.synchronize()
+    for name, a, b in events:
+        times[name].append(a.elapsed_time(b))
+    return times
+
+
+def e2e_steps(phases, steps, flush):
+    """Same step with host buffers: pinned H2D of every input, the call, and a
+    D2H read of out and lse, all inside the timed events."""
+    stream = torch.cuda.current_stream()
+    pinned = {}
+    for p in phases:
+        pinned[p.name] = ({k: v.pin_memory() for k, v in p.host.items()},
+                          torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory(),
+                          torch.empty(p.lse.shape, dtype=p.lse.dtype).pin_memory())
+    staging = {p.name: {k: torch.empty_like(v) for k, v in p.dev.items()} for p in phases}
+    times = {p.name: [] for p in phases}
+    events = []
+    for _ in range(steps):
+        for p in phases:
+            hin, hout, hlse = pinned[p.name]
+            dst = staging[p.name]
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in ARG_ORDER:
+                dst[k].copy_(hin[k], non_blocking=True)
+            p.run(args=[dst[k] for k in ARG_ORDER])
+            hout.copy_(p.out, non_blocking=True)
+            hlse.copy_(p.lse, non_blocking=True)
+            b.record(stream)
+            events.append((p.name, a, b))
+    torch.cuda.synchronize()
+    for name, a, b in events:
+        times[name].append(a.elapsed_time(b))
+    return times
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def oracle_sample_rows(w, n_rows, seed=7):
+    rng = np.random.default_rng(seed)
+    total = sum(w.q_lens)
+    return np.sort(rng.choice(total, size=min(n_rows, total), replace=False)).astype(np.int64)
+
+
+def time_oracle(w, inp, rows):
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.forward(inp["q"], inp["k"], inp["v"], inp["r"], inp["P"], inp["cu_seqlens_q"],
+                   inp["cu_seqlens_k"], alpha=w.alpha, window=w.window,
+                   log_scale_base=w.log_scale_base, rows=rows)
+    dt = time.perf_counter() - t0
+    return dt, A.flops(w, rows), oracle.max_threads()
+
+
+def decode_rows_bytes(w, rows):
+    """K/V bytes the selected decode rows read (each row streams its visible keys)."""
+    return A.visible_pairs(w, rows) * w.Hkv * w.head_dim * 2 * 2 // max(1, len(rows))
+
+
+# ------------------------------------------------------------------ arms
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.swa_prefill()
+    inp = W.make_inputs(w)
+    rows = oracle_sample_rows(w, 64)
+    for _ in range(args.warmup):
+        time_oracle(w, inp, rows[:8])
+    dts, fl = [], 0
+    t_all0 = time.perf_counter()
+    for s in range(args.steps):
+        r = oracle_sample_rows(w, 64, seed=100 + s)
+        dt, f, cores = time_oracle(w, inp, r)
+        dts.append(dt)
+        fl += f
+    elapsed = sum(dts)
+    value = fl / elapsed / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": "64 random query rows x 16 heads per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps x 64 random query rows x 16 heads of {w.name}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_all0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(wl, host):
+    """Oracle on the host cores over a bounded sample of the prefill workload."""
+    w = wl["prefill"]
+    rows = oracle_sample_rows(w, 256)
+    dt, f, cores = time_oracle(w, host["prefill"], rows)
+    wd = wl["decode_long"]
+    drows = np.array([sum(wd.q_lens) - 1], dtype=np.int64)
+    ddt, _, _ = time_oracle(wd, host["decode_long"], drows)
+    return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"256 random query rows x 16 heads of {w.name} ({dt:.1f} s)",
+            "decode": {"value": decode_rows_bytes(wd, drows) / ddt / 1e9, "unit": "GB/s",
+                       "sample": f"1 query row x 16 heads of {wd.name} ({ddt:.1f} s)"}}
+
+
+def gpu_arm(args):
+    ws, rank, local = dist_env()
+    dist = init_dist(ws, local)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    torch.cuda.set_device(local if ws > 1 else 0)
+    import relative_position_biased_gb300 as rpb
+    rpb.build()
+    rpb.load_library()
+
+    wl = step_workloads()
+    if args.only:
+        wl = {args.only: wl[args.only]}
+    host = {k: W.make_inputs(w) for k, w in wl.items()}
+    names = ("prefill", "decode_long", "decode_batched")
+    if args.only:
+        return single_phase(args, Phase(args.only, wl[args.only], host[args.only], rpb))
+    phases = [Phase(k, wl[k], host[k], rpb) for k in names]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    for _ in range(args.warmup):
+        for p in phases:
+            p.run()
+    torch.cuda.synchronize()
+    if rpb.relattn_get_device_error() != 0:
+        raise SystemExit("device error word set during warm-up")
+
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = time.perf_counter()
+        times = timed_steps(phases, args.steps, flush)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(dist)
+    clocks = clk.summary()
+
+    e2e_t = e2e_steps(phases, max(1, min(args.steps, 5)), flush)
+    torch.cuda.synchronize()
+
+    pre, dl, db = phases
+    ms = {p.name: sum(times[p.name]) for p in phases}
+    step_ms = sum(ms.values()) / args.steps
+    pre_ms = max_over_ranks(ms["prefill"] / args.steps, dist)
+    dl_ms = max_over_ranks(ms["decode_long"] / args.steps, dist)
+    db_ms = max_over_ranks(ms["decode_batched"] / args.steps, dist)
+    step_ms = max_over_ranks(step_ms, dist)
+    value = ws * pre.flops / (pre_ms * 1e-3) / 1e12
+    peaks, peak_kind = load_peaks()
+    tf_peak = peaks["bf16_tflops"]
+    hbm_peak = peaks["hbm_gbs"]
+    pre_tf = pre.flops / (pre_ms * 1e-3) / 1e12
+    dl_gbs = dl.bytes / (dl_ms * 1e-3) / 1e9
+    db_gbs = db.bytes / (db_ms * 1e-3) / 1e9
+    e2e_pre = sum(e2e_t["prefill"]) / len(e2e_t["prefill"])
+    e2e_dl = sum(e2e_t["decode_long"]) / len(e2e_t["decode_long"])
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{pre.w.name} + {dl.w.name} + {db.w.name}",
+            "prefill": {"batch": pre.w.batch, "seq_len": pre.w.q_lens[0], "Hq": pre.w.Hq,
+                        "Hkv": pre.w.Hkv, "head_dim": 128, "r_dim": pre.w.r_dim,
+                        "rel_extent": pre.w.rel_extent, "window": pre.w.window,
+                        "flops": pre.flops},
+            "decode_long": {"q_rows": dl.w.q_lens[0], "kv_len": dl.w.k_lens[0],
+                            "log_scale_base": dl.w.log_scale_base, "kv_bytes": dl.bytes,
+                            "splits": dl.splits},
+            "decode_batched": {"batch": db.w.batch, "kv_lens": "U[1024,32768]",
+                               "kv_bytes": db.bytes, "splits": db.splits},
+            "l2": "flushed by a 256 MiB write before every timed call",
+            "parallelism": f"replicas x{ws}",
+        },
+        "phases_ms": {"prefill": pre_ms, "decode_long": dl_ms, "decode_batched": db_ms},
+        "roofline": {"bound": "tensor", "achieved": pre_tf, "peak": tf_peak,
+                     "unit": "TFLOP/s", "frac": pre_tf / tf_peak,
+                     "traffic": load_traffic("prefill"),
+                     "peak_source": f"{peak_kind} bf16 dense (burst)",
+                     "kernel": "relattn_fwd_mma_kernel<prefill>"},
+        "decode": {
+            "value": dl_gbs, "unit": "GB/s", "workload": dl.w.name,
+            "roofline": {"bound": "hbm", "achieved": dl_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": dl_gbs / hbm_peak, "frac_vs_8tbs": dl_gbs / 8000.0,
+                         "traffic": load_traffic("decode"),
+                         "peak_source": f"{peak_kind} HBM copy"},
+            "batched": {"value": db_gbs, "unit": "GB/s", "workload": db.w.name,
+                        "frac": db_gbs / hbm_peak},
+        },
+        "e2e": {"value": pre.flops / (e2e_pre * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": pre.h2d + dl.h2d + db.h2d,
+                "d2h_bytes_per_step": pre.d2h + dl.d2h + db.d2h,
+                "decode_value": dl.bytes / (e2e_dl * 1e-3) / 1e9, "decode_unit": "GB/s",
+                "path": "pinned host buffers -> H2D -> relattn_* C ABI -> D2H out+lse"},
+        "gpu_launches": args.steps * sum(p.launches for p in phases),
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, host)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def single_phase(args, p):
+    """One phase alone (used for profiling captures): warm-up, K timed calls."""
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        p.run()
+    torch.cuda.synchronize()
+    t = timed_steps([p], args.steps, flush)[p.name]
+    ms = sum(t) / len(t)
+    rate = (p.bytes / (ms * 1e-3) / 1e9, "GB/s") if p.decode else \
+        (p.flops / (ms * 1e-3) / 1e12, "TFLOP/s")
+    print(json.dumps({"phase": p.name, "workload": p.w.name, "ms": ms, "value": rate[0],
+                      "unit": rate[1], "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched"],
+                    help="time one phase alone (profiling captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -133,6 +133,32 @@ relattn_status relattn_combine(const float *o_part, const float *lse_part, int32
                                int32_t total_q, int32_t num_heads, void *out, float *lse,
                                void *stream);
 
+/*
+ * Decode without a caller workspace and without allocating.  (The Inkling
+ * pages have no counterpart to this; it is an integration convenience.)
+ *
+ * Same computation, arguments and results as relattn_decode, except that the
+ * split partials go to a fixed scratch array inside this library instead of
+ * params->workspace (which is ignored).  It is meant for callers that cannot
+ * call cudaMalloc where they run attention: engines that reserve all free
+ * device memory for their own pools up front, plugin hosts that offer no
+ * workspace hook, and latency-critical paths that cannot afford cudaMalloc's
+ * implicit device synchronisation.  Nothing is allocated or freed by the call.
+ *
+ * Limits and sharing:
+ *   - The scratch holds RELATTN_NOALLOC_SCRATCH_BYTES per device, for as long
+ *     as the library is loaded.  When relattn_decode_workspace_size() reports
+ *     more than that for these params, the call returns RELATTN_ERR_WORKSPACE
+ *     and launches nothing (pass a smaller num_splits, or use relattn_decode).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current).  Make that first call before any stream capture.
+ *   - Every call on a device shares the one array.  No contents need to carry
+ *     over between calls, but two calls whose kernels can overlap on the GPU
+ *     (unordered streams) race on it: order them, or use relattn_decode.
+ */
+#define RELATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+relattn_status relattn_decode_noalloc(const relattn_params *params, void *stream);
+
 /* Reads and clears the device error word (RELATTN_OK when clean).  Synchronises
  * `stream` to read it. */
 relattn_status relattn_get_device_error(void *stream);

@@ -29,8 +29,9 @@ STATUS_NAMES = {
 EXPORTED = (
     "relattn_prefill", "relattn_decode", "relattn_decode_workspace_size",
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
-    "relattn_status_string", "relattn_version",
+    "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
 
 class RelattnError(RuntimeError):
@@ -79,7 +80,7 @@ def load_library(path: Optional[str] = None):
             return _lib
         lib = _open(path or LIB_PATH)
         P, vp = ctypes.POINTER(RelattnParams), ctypes.c_void_p
-        for name in ("relattn_prefill", "relattn_decode"):
+        for name in ("relattn_prefill", "relattn_decode", "relattn_decode_noalloc"):
             f = getattr(lib, name)
             f.argtypes, f.restype = [P, vp], ctypes.c_int
         lib.relattn_decode_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
@@ -112,6 +113,11 @@ def relattn_prefill(params: RelattnParams, stream: int = 0) -> int:
 
 def relattn_decode(params: RelattnParams, stream: int = 0) -> int:
     return load_library().relattn_decode(ctypes.byref(params), ctypes.c_void_p(stream))
+
+
+def relattn_decode_noalloc(params: RelattnParams, stream: int = 0) -> int:
+    """Decode with the library's fixed scratch array; params.workspace is ignored."""
+    return load_library().relattn_decode_noalloc(ctypes.byref(params), ctypes.c_void_p(stream))
 
 
 def relattn_decode_workspace_size(params: RelattnParams) -> Tuple[int, int]:

@@ -45,7 +45,8 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
-    "prefill": ["relative_position_biased_gb300/csrc/fwd_mma.cu",
+    "prefill": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
+                "relative_position_biased_gb300/csrc/tc_common.cuh",
                 "relative_position_biased_gb300/csrc/common.cuh"],
     "decode": ["relative_position_biased_gb300/csrc/fwd_mma.cu",
                "relative_position_biased_gb300/csrc/common.cuh"],
@@ -433,7 +434,7 @@ def gpu_arm(args):
                      "unit": "TFLOP/s", "frac": pre_tf / tf_peak,
                      "traffic": load_traffic("prefill"),
                      "peak_source": f"{peak_kind} bf16 dense (burst)",
-                     "kernel": "relattn_fwd_mma_kernel<prefill>"},
+                     "kernel": "relattn_fwd_tc_prefill_kernel"},
         "decode": {
             "value": dl_gbs, "unit": "GB/s", "workload": dl.w.name,
             "roofline": {"bound": "hbm", "achieved": dl_gbs, "peak": hbm_peak, "unit": "GB/s",

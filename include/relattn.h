@@ -163,6 +163,11 @@ relattn_status relattn_decode_noalloc(const relattn_params *params, void *stream
  * `stream` to read it. */
 relattn_status relattn_get_device_error(void *stream);
 
+/* Raw device error word seen by the last relattn_get_device_error() call:
+ * bit 0 = inconsistent cu_seqlens, bit 1 = a bounded wait gave up, bits 8+ =
+ * the id of the wait that gave up first (diagnostics only). */
+int32_t relattn_last_device_error_word(void);
+
 /* Human-readable name of a status code (static string). */
 const char *relattn_status_string(relattn_status status);
 

@@ -30,6 +30,7 @@ EXPORTED = (
     "relattn_prefill", "relattn_decode", "relattn_decode_workspace_size",
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
+    "relattn_last_device_error_word",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -94,6 +95,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_get_device_error.restype = ctypes.c_int
         lib.relattn_status_string.argtypes = [ctypes.c_int]
         lib.relattn_status_string.restype = ctypes.c_char_p
+        lib.relattn_last_device_error_word.argtypes = []
+        lib.relattn_last_device_error_word.restype = ctypes.c_int32
         lib.relattn_version.argtypes = []
         lib.relattn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -140,6 +143,10 @@ def relattn_combine(o_part: int, lse_part: int, num_splits: int, total_q: int, n
 
 def relattn_get_device_error(stream: int = 0) -> int:
     return load_library().relattn_get_device_error(ctypes.c_void_p(stream))
+
+
+def relattn_last_device_error_word() -> int:
+    return int(load_library().relattn_last_device_error_word())
 
 
 def relattn_status_string(status: int) -> str:

@@ -17,6 +17,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_err_ptr[kMaxDevices];
 int g_sms[kMaxDevices];
+int g_last_error_word = 0;
 
 relattn_status device_state(int *dev_out, int **err_out, int *sms_out) {
   int dev = 0;
@@ -166,7 +167,9 @@ relattn_status relattn_prefill(const relattn_params *p, void *stream) {
   if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
   KernelArgs a;
   if ((st = make_args(p, &a)) != RELATTN_OK) return st;
-  return cuda_status(launch_prefill_mma(a, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (prefill_tc_supported(a, p->total_k)) return cuda_status(launch_prefill_tc(a, p->total_k, s));
+  return cuda_status(launch_prefill_mma(a, s));
 }
 
 relattn_status relattn_decode_workspace_size(const relattn_params *p, size_t *bytes) {
@@ -240,6 +243,7 @@ relattn_status relattn_get_device_error(void *stream) {
     return RELATTN_ERR_CUDA;
   if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return RELATTN_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return RELATTN_ERR_CUDA;
+  g_last_error_word = host;
   if (host & kDevErrTimeout) return RELATTN_ERR_TIMEOUT;
   if (host & kDevErrSeqlens) return RELATTN_ERR_DEVICE_ARGS;
   return RELATTN_OK;
@@ -259,5 +263,7 @@ const char *relattn_status_string(relattn_status s) {
 }
 
 const char *relattn_version(void) { return "relattn 0.1 sm_103a"; }
+
+int32_t relattn_last_device_error_word(void) { return g_last_error_word; }
 
 }  // extern "C"

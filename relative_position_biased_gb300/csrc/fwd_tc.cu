@@ -1,0 +1,572 @@
+// fwd_tc.cu -- relative-attention prefill on 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory, TMA-fed K/V).
+//
+// Same computation as the definition on the page "SGLang and Miles Add Day-0
+// Support for Inkling", section "Attention with Relative Positional
+// Embedding":  x(i,j) = s(i) * (alpha q_i.k_j + [0 <= i-j < E] r_i . P[:, i-j]),
+// online softmax, PV.
+//
+// One CTA = one query head x 128 query rows (TMEM lane a <-> row a), keys in
+// tiles of 64, visited from the diagonal backwards.  Warp roles:
+//   warp 0      TMA producer for K and V tiles (4-stage ring)
+//   warp 1      MMA issuer (one thread):  S = Q K^T (Q in TMEM),
+//               R_chunk = r P[:, 64c..64c+64) (both operands from shared
+//               memory), O += P V (P in TMEM)
+//   warp 2      TMEM allocator; producer of the P slices (plain loads into
+//               the 128-byte-swizzled layout)
+//   warps 4-7   softmax: thread a owns row a -- writes its q row to TMEM and
+//               its r row to the shared r tile, loads S from TMEM, adds the
+//               relative bias, masks edge tiles, keeps the running max/sum,
+//               writes P (bf16) back over S, rescales O when the max grows
+//               by more than 2^8, and writes out / lse at the end.
+//
+// Tensor memory (512 columns): Q [0,64) bf16, S0 [64,128), S1 [128,192),
+// O [192,320), R ring [320,512) = three 64-distance chunks of r.P.
+//
+// Relative bias without a sheared tensor: the R ring holds, for every row, the
+// relative logits of three consecutive 64-distance chunks.  Key tile at
+// offset D = i_0 - j_0 needs distances D-63 .. D+127 (chunks D/64-1 .. D/64+1);
+// walking tiles away from the diagonal needs one new chunk per tile.  Each
+// thread loads a 64-column window of its own row (one load shape for the
+// whole warp) and shifts it by its lane index with a 5-stage select network,
+// which turns "distance order" into "key order" in registers.
+//
+// Every wait is bounded; a timeout sets the device error word, the CTA drains
+// its own copies / MMAs with bounded waits, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace relattn {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128;          // query rows per CTA
+constexpr int BN = 64;           // keys per tile
+constexpr int KV_STAGES = 4;
+constexpr int P_STAGES = 2;
+constexpr int NTHREADS = 256;
+constexpr float kRescaleThreshold = 8.f;   // log2 units
+
+// TMEM columns
+constexpr uint32_t TM_Q = 0, TM_S0 = 64, TM_O = 192, TM_R = 320;
+
+// Shared memory layout (offsets from a 1024-aligned base)
+constexpr uint32_t SM_KV = 0;                                  // stages of K(16K) + V(16K)
+constexpr uint32_t KV_STAGE_BYTES = 32768;
+constexpr uint32_t SM_RT = SM_KV + KV_STAGES * KV_STAGE_BYTES;  // r tile 16K
+constexpr uint32_t SM_PS = SM_RT + 16384;                      // P slices 2 x 8K
+constexpr uint32_t SM_BAR = SM_PS + P_STAGES * 8192;
+// barriers (8 bytes each)
+constexpr int B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + KV_STAGES, B_PS_FULL = B_KV_EMPTY + KV_STAGES,
+              B_PS_EMPTY = B_PS_FULL + P_STAGES, B_RT_FULL = B_PS_EMPTY + P_STAGES,
+              B_Q_READY = B_RT_FULL + 1, B_S_FULL = B_Q_READY + 1, B_P_FULL = B_S_FULL + 2,
+              B_PV_DONE = B_P_FULL + 2, B_R_FULL = B_PV_DONE + 1, B_R_FREE = B_R_FULL + 3,
+              B_DRAIN = B_R_FREE + 1, B_COUNT = B_DRAIN + 1;
+constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
+constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
+constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
+constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;  // + alignment slack
+
+struct TcArgs {
+  KernelArgs a;
+  int has_bias;
+};
+
+__device__ __forceinline__ int floor_div64(int x) { return x >= 0 ? x >> 6 : -((63 - x) >> 6); }
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
+                              const __grid_constant__ CUtensorMap map_k,
+                              const __grid_constant__ CUtensorMap map_v) {
+  const KernelArgs &a = ta.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t sb = smem_addr(smem);
+  auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ------------------------------------------------------------ work item
+  const int q_tile = a.q_tiles - 1 - blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int cq = a.cu_q[b], ck = a.cu_k[b];
+  const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
+  if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) {
+    if (tid == 0) atomicOr(a.err, kDevErrSeqlens);
+    return;
+  }
+  const int row0 = q_tile * BM;
+  const int nrows = min(BM, Lq - row0);
+  if (nrows <= 0) return;
+  const int kv_head = h / a.group;
+  const int off = Lk - Lq;
+  const int p0 = off + row0, p_last = p0 + nrows - 1;
+  const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
+  // key tiles start at j0(n) = p0 + 64 - 64 n  (offset D(n) = p0 - j0 = 64 n - 64)
+  const int D_first = (p_last >= p0 + BN) ? -BN : 0;
+  const int ntiles = (p0 - j_lo - D_first + BN - 1) / BN + 1;
+  auto tile_D = [&](int n) { return D_first + BN * n; };
+  // band tiles (some distance < E) form a prefix of the tile order
+  int nband = 0;
+  if (ta.has_bias) {
+    nband = ntiles;
+    const int lim = a.E + BN - 1;  // band iff D - 63 < E
+    if (tile_D(ntiles - 1) >= lim) nband = (lim - D_first + BN - 1) / BN;
+    if (nband > ntiles) nband = ntiles;
+  }
+  const int c_first = floor_div64(tile_D(0)) + 1;             // newest chunk tile 0 needs
+  const int c_last = nband > 0 ? floor_div64(tile_D(nband - 1)) + 1 : -1;
+
+  // ------------------------------------------------------------ setup
+  if (tid == 0) {
+    for (int i = 0; i < KV_STAGES; ++i) {
+      mbar_init(bar(B_KV_FULL + i), 1);
+      mbar_init(bar(B_KV_EMPTY + i), 1);
+    }
+    for (int i = 0; i < P_STAGES; ++i) {
+      mbar_init(bar(B_PS_FULL + i), 1);
+      mbar_init(bar(B_PS_EMPTY + i), 1);
+    }
+    mbar_init(bar(B_RT_FULL), 128);
+    mbar_init(bar(B_Q_READY), 128);
+    mbar_init(bar(B_S_FULL + 0), 1);
+    mbar_init(bar(B_S_FULL + 1), 1);
+    mbar_init(bar(B_P_FULL + 0), 128);
+    mbar_init(bar(B_P_FULL + 1), 128);
+    mbar_init(bar(B_PV_DONE), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(bar(B_R_FULL + i), 1);
+    mbar_init(bar(B_R_FREE), 128);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(sb + SM_TMEM_SLOT, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
+
+  if (warp == 0) {
+    // ======================================================== K/V producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int n = 0; n < ntiles && !*abort_flag; ++n) {
+        const int st = n % KV_STAGES;
+        if (n >= KV_STAGES && !mbar_wait(bar(B_KV_EMPTY + st), ((n / KV_STAGES) - 1) & 1, abort_flag, 1))
+          break;
+        const int key = ck + p0 - tile_D(n);
+        const uint32_t dst = sb + SM_KV + st * KV_STAGE_BYTES;
+        mbar_arrive_expect_tx(bar(B_KV_FULL + st), KV_STAGE_BYTES);
+        tma_load_3d(dst, &map_k, 0, kv_head, key, bar(B_KV_FULL + st));
+        tma_load_3d(dst + 8192, &map_k, 64, kv_head, key, bar(B_KV_FULL + st));
+        tma_load_3d(dst + 16384, &map_v, 0, kv_head, key, bar(B_KV_FULL + st));
+        tma_load_3d(dst + 24576, &map_v, 64, kv_head, key, bar(B_KV_FULL + st));
+        issued = n + 1;
+      }
+      if (*abort_flag) {
+        // let our own copies land before the CTA goes away (bounded, not cut short by the abort)
+        volatile int keep_waiting = 0;
+        for (int n = max(0, issued - KV_STAGES); n < issued; ++n)
+          mbar_wait(bar(B_KV_FULL + n % KV_STAGES), (n / KV_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ======================================================== P-slice producer
+    // Chunk c = P[:, 64c, 64c+64) as rd_pad rows (channels) of 128 bytes in the
+    // 128-byte-swizzled layout the MMA descriptor expects; zero outside [0, E)
+    // and past r_dim.  Plain 16-byte loads (P is small and L2-resident).
+    if (nband > 0) {
+      const int c_hi = min(c_last, (a.E - 1) / BN);     // chunks past E stay zero-filled
+      for (int c = 0; c <= c_last; ++c) {
+        const int st = c & 1;
+        if (c >= P_STAGES) {
+          const bool w = mbar_wait(bar(B_PS_EMPTY + st), ((c >> 1) - 1) & 1, abort_flag, 3);
+          if (!__all_sync(0xffffffffu, w)) break;
+        }
+        uint8_t *dst = smem + SM_PS + st * 8192;
+        for (int idx = lane; idx < a.rd_pad * 8; idx += 32) {
+          const int ch = idx >> 3, j = idx & 7, col = BN * c + 8 * j;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (c <= c_hi && ch < a.rd && col < a.E)
+            v = *reinterpret_cast<const uint4 *>(a.P + (size_t)ch * a.E + col);
+          *reinterpret_cast<uint4 *>(dst + (ch >> 3) * 1024 + (ch & 7) * 128 +
+                                     ((j ^ (ch & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PS_FULL + st));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(BM, BN, 0, 0);       // S: Q(tmem) x K(smem, K-major)
+      const uint32_t id_o = idesc_bf16_f32(BM, 128, 0, 1);      // O: P(tmem) x V(smem, MN-major)
+      const uint32_t id_r = idesc_bf16_f32(BM, BN, 0, 1);       // R: r(smem) x P(smem, MN-major)
+      const int r_ksteps = a.rd_pad / 16;
+      bool ok = mbar_wait(bar(B_Q_READY), 0, abort_flag, 6);
+      tc_fence_after();
+      bool rt_ready = false;
+      auto issue_r = [&](int c) -> bool {
+        if (!rt_ready) {
+          if (!mbar_wait(bar(B_RT_FULL), 0, abort_flag, 7)) return false;
+          rt_ready = true;
+        }
+        const int st = c & 1;
+        if (!mbar_wait(bar(B_PS_FULL + st), (c >> 1) & 1, abort_flag, 8)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + TM_R + 64u * (uint32_t)(c % 3);
+        for (int k = 0; k < r_ksteps; ++k) {
+          const uint64_t ad = smem_desc_sw128(sb + SM_RT + 32u * k, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sb + SM_PS + st * 8192 + 2048u * k, 8192, 1024);
+          mma_ss(d, ad, bd, id_r, k > 0);
+        }
+        mma_commit(bar(B_R_FULL + c % 3));
+        mma_commit(bar(B_PS_EMPTY + st));
+        return true;
+      };
+      auto issue_s = [&](int n) -> bool {
+        const int st = n % KV_STAGES;
+        if (!mbar_wait(bar(B_KV_FULL + st), (n / KV_STAGES) & 1, abort_flag, 9)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + TM_S0 + 64u * (uint32_t)(n & 1);
+        const uint32_t kb = sb + SM_KV + st * KV_STAGE_BYTES;
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t bd = smem_desc_sw128(kb + (k >> 2) * 8192 + 32u * (k & 3), 16, 1024);
+          mma_ts(d, tmem + TM_Q + 8u * k, bd, id_s, k > 0);
+        }
+        mma_commit(bar(B_S_FULL + (n & 1)));
+        return true;
+      };
+      if (ok && nband > 0)
+        for (int c = 0; c <= c_first && ok; ++c) ok = issue_r(c);
+      if (ok) ok = issue_s(0);
+      for (int n = 0; n < ntiles && ok; ++n) {
+        if (n + 1 < ntiles && !(ok = issue_s(n + 1))) break;
+        if (n + 1 < nband) {
+          const int c = floor_div64(tile_D(n + 1)) + 1;
+          if (!(ok = mbar_wait(bar(B_R_FREE), n & 1, abort_flag, 10))) break;
+          if (c >= 0 && !(ok = issue_r(c))) break;
+        }
+        if (!(ok = mbar_wait(bar(B_P_FULL + (n & 1)), (n >> 1) & 1, abort_flag, 11))) break;
+        tc_fence_after();
+        const int st = n % KV_STAGES;
+        const uint32_t vb = sb + SM_KV + st * KV_STAGE_BYTES + 16384;
+        const uint32_t pa = tmem + TM_S0 + 64u * (uint32_t)(n & 1);
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t bd = smem_desc_sw128(vb + 2048u * k, 8192, 1024);
+          mma_ts(tmem + TM_O, pa + 8u * k, bd, id_o, (n > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_PV_DONE));
+        mma_commit(bar(B_KV_EMPTY + st));
+      }
+      // drain: every MMA issued above has finished before TMEM is released
+      mma_commit(bar(B_DRAIN));
+      volatile int keep_waiting = 0;
+      mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 12, 400000000ll);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ======================================================== softmax
+    const int a_row = tid - 128;                 // 0..127 == TMEM lane
+    const int wq = warp - 4;                     // lane quarter
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    const int t_row = row0 + min(a_row, nrows - 1);
+    const int pos = p0 + a_row;                  // padding rows only compute garbage
+    const float sc = log_scale(min(pos, p_last), a.inv_ln_base);
+    const float cqk = a.alpha_log2e * sc, cbias = kLog2e * sc;
+
+    // Q row -> TMEM (bf16 pairs)
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim);
+      uint32_t r[32];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = src[half * 8 + i];
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_base + TM_Q + 32u * half, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_Q_READY));
+    }
+    // r row -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
+    if (nband > 0) {
+      const __nv_bfloat16 *rsrc = a.r + ((size_t)(cq + t_row) * a.Hq + h) * a.rd;
+      uint8_t *rrow = smem + SM_RT + (a_row >> 3) * 1024 + (a_row & 7) * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (8 * j < a.rd) v = *reinterpret_cast<const uint4 *>(rsrc + 8 * j);
+        *reinterpret_cast<uint4 *>(rrow + ((j ^ (a_row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_RT_FULL));
+    }
+
+    // every lane of a softmax warp takes the same branch after a wait, so the
+    // warp-collective tcgen05 loads / stores that follow see a converged warp
+    auto warp_wait = [&](uint32_t br, uint32_t parity, int site) -> bool {
+      const bool r = mbar_wait(br, parity, abort_flag, site);
+      return __all_sync(0xffffffffu, r);
+    };
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int n = 0; n < ntiles; ++n) {
+      const uint32_t sbuf = tmem + lane_base + TM_S0 + 64u * (uint32_t)(n & 1);
+      if (!(ok = warp_wait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1, 13))) break;
+      tc_fence_after();
+      float s[64];
+      {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(sbuf, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
+        tmem_ld32(sbuf + 32, r);
+        tmem_wait_ld(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
+      }
+      const int D = tile_D(n);
+      const int j0 = p0 - D;
+      if (n < nband) {
+        // wait for the newest chunk this tile needs (older ones were awaited before)
+        if (n == 0) {
+          for (int c = 0; c <= c_first && ok; ++c)
+            ok = warp_wait(bar(B_R_FULL + c % 3), (c / 3) & 1, 14);
+        } else {
+          const int c = floor_div64(D) + 1;
+          if (c >= 0) ok = warp_wait(bar(B_R_FULL + c % 3), (c / 3) & 1, 15);
+        }
+        if (!ok) break;
+        tc_fence_after();
+        const int sh = 31 - lane;  // per-thread shift of the distance window
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          // distances D + a - (32 g + u), u in [0, 32): window [base, base + 64)
+          const int base = D + 32 * wq - 32 * g - 32;
+          float z[64];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int d0 = base + 32 * hh;
+            if (d0 >= 0) {
+              const int c = d0 >> 6;
+              uint32_t r[32];
+              __syncwarp();
+              tmem_ld32(tmem + lane_base + TM_R + 64u * (uint32_t)(c % 3) + (uint32_t)(d0 & 63), r);
+              tmem_wait_ld(r);
+              // reversed: z[63 - i] = window[i]
+#pragma unroll
+              for (int i = 0; i < 32; ++i) z[63 - (32 * hh + i)] = __uint_as_float(r[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) z[63 - (32 * hh + i)] = 0.f;
+            }
+          }
+          // y[u] = z[u + sh]: shift left by sh with a select network
+#pragma unroll
+          for (int i = 0; i < 47; ++i) z[i] = (sh & 16) ? z[i + 16] : z[i];
+#pragma unroll
+          for (int i = 0; i < 39; ++i) z[i] = (sh & 8) ? z[i + 8] : z[i];
+#pragma unroll
+          for (int i = 0; i < 35; ++i) z[i] = (sh & 4) ? z[i + 4] : z[i];
+#pragma unroll
+          for (int i = 0; i < 33; ++i) z[i] = (sh & 2) ? z[i + 2] : z[i];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) z[i] = (sh & 1) ? z[i + 1] : z[i];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) s[32 * g + u] = fmaf(s[32 * g + u], cqk, z[u] * cbias);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_R_FREE));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] *= cqk;
+      }
+      const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int j = j0 + i;
+          const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
+          s[i] = vis ? s[i] : -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+      float corr = 1.f;
+      bool rescale_o = false;
+      if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
+        const float m_new = fmaxf(m_ref, mx);
+        corr = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+        rescale_o = (n > 0) && (m_ref != -INFINITY);
+        l *= corr;
+        m_ref = m_new;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      {
+        uint32_t pk[32];
+        float rs = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float e0 = fast_exp2(s[2 * i] - m_use), e1 = fast_exp2(s[2 * i + 1] - m_use);
+          rs += e0 + e1;
+          pk[i] = pack_bf16x2(e0, e1);
+        }
+        l += rs;
+        __syncwarp();
+        tmem_st32(sbuf, pk);
+      }
+      if (n > 0) {
+        if (!(ok = warp_wait(bar(B_PV_DONE), (n - 1) & 1, 16))) break;
+        tc_fence_after();
+      }
+      // TMEM loads / stores are warp-collective: the whole warp rescales its 32
+      // rows when any of them needs it (rows that do not are scaled by 1)
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        const float cf = rescale_o ? corr : 1.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_base + TM_O + 32u * c, r);
+          tmem_wait_ld(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * cf);
+          __syncwarp();
+          tmem_st32(tmem + lane_base + TM_O + 32u * c, r);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL + (n & 1)));
+    }
+    // ---- epilogue
+    if (ok && ntiles > 0) ok = warp_wait(bar(B_PV_DONE), (ntiles - 1) & 1, 17);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = a_row < nrows;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *dst = a.out + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_base + TM_O + 32u * c, r);
+        tmem_wait_ld(r);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]) * inv, __uint_as_float(r[8 * i + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
+            *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * i) = v;
+          }
+        }
+      }
+      if (valid)
+        a.lse[(size_t)h * a.total_q + cq + t_row] =
+            l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+            const cuuint64_t *strides, const cuuint32_t *box) {
+  auto fn = get_encoder();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const KernelArgs &a, int total_k) {
+  auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!get_encoder()) return false;
+  if (!al(a.k) || !al(a.v) || !al(a.q) || !al(a.out)) return false;
+  if (a.rd > 0) {
+    if (a.rd % 8 != 0 || a.E % 8 != 0 || a.rd > 64 || !al(a.r) || !al(a.P)) return false;
+  }
+  if (total_k < BN) return false;   // K/V boxes stay inside the tensor
+  return true;
+}
+
+cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {
+  TcArgs ta;
+  ta.a = a;
+  ta.has_bias = a.rd > 0 && a.E > 0;
+  CUtensorMap mk, mv;
+  {
+    cuuint64_t dims[3] = {128, (cuuint64_t)a.Hkv, (cuuint64_t)total_k};
+    cuuint64_t strides[2] = {256, (cuuint64_t)a.Hkv * 256};
+    cuuint32_t box[3] = {64, 1, BN};
+    if (!encode(&mk, a.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode(&mv, a.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_prefill_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(a.q_tiles, a.Hq, a.batch);
+  relattn_fwd_tc_prefill_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace relattn

@@ -15,6 +15,11 @@ size_t prefill_mma_smem_bytes(int rd_pad);
 size_t decode_mma_smem_bytes(int warps, int rd_pad);
 
 cudaError_t launch_prefill_mma(const KernelArgs &a, cudaStream_t stream);
+
+// tcgen05 / TMA prefill: needs 16-byte aligned q/k/v/out, r_dim % 8 == 0 and
+// rel_extent % 8 == 0 (TMA strides), r_dim <= 64.
+bool prefill_tc_supported(const KernelArgs &a, int total_k);
+cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream);
 cudaError_t launch_decode_mma(const KernelArgs &a, int warps, cudaStream_t stream);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits,
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,

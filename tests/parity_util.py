@@ -27,7 +27,7 @@ def run_gpu(w: W.Workload, inp, *, decode=None, num_splits=0, stream=None):
         out, lse = rpb.prefill(*args, **kw)
     torch.cuda.synchronize()
     st = rpb.relattn_get_device_error()
-    assert st == rpb.RELATTN_OK, rpb.STATUS_NAMES.get(st, st)
+    assert st == rpb.RELATTN_OK, (rpb.STATUS_NAMES.get(st, st), hex(rpb.relattn_last_device_error_word()))
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 

@@ -14,11 +14,13 @@
 //               memory), O += P V (P in TMEM)
 //   warp 2      TMEM allocator; producer of the P slices (plain loads into
 //               the 128-byte-swizzled layout)
-//   warps 4-7   softmax: thread a owns row a -- writes its q row to TMEM and
-//               its r row to the shared r tile, loads S from TMEM, adds the
-//               relative bias, masks edge tiles, keeps the running max/sum,
-//               writes P (bf16) back over S, rescales O when the max grows
-//               by more than 2^8, and writes out / lse at the end.
+//   warps 4-11  softmax, two warpgroups: row a is owned by one thread of each
+//               (TMEM lane a); warpgroup wg takes keys [32 wg, 32 wg + 32) of
+//               every tile.  They write the q / r rows, load S from TMEM, add
+//               the relative bias, mask edge tiles, agree on the running row
+//               max through shared memory, write P (bf16) back over S, rescale
+//               their half of O when the max grows by more than 2^8, and write
+//               out / lse at the end.
 //
 // Tensor memory (512 columns): Q [0,64) bf16, S0 [64,128), S1 [128,192),
 // O [192,320), R ring [320,512) = three 64-distance chunks of r.P.
@@ -46,8 +48,8 @@ using namespace tc;
 constexpr int BM = 128;          // query rows per CTA
 constexpr int BN = 64;           // keys per tile
 constexpr int KV_STAGES = 4;
-constexpr int P_STAGES = 2;
-constexpr int NTHREADS = 256;
+constexpr int P_STAGES = 4;
+constexpr int NTHREADS = 384;
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 // TMEM columns
@@ -63,11 +65,12 @@ constexpr uint32_t SM_BAR = SM_PS + P_STAGES * 8192;
 constexpr int B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + KV_STAGES, B_PS_FULL = B_KV_EMPTY + KV_STAGES,
               B_PS_EMPTY = B_PS_FULL + P_STAGES, B_RT_FULL = B_PS_EMPTY + P_STAGES,
               B_Q_READY = B_RT_FULL + 1, B_S_FULL = B_Q_READY + 1, B_P_FULL = B_S_FULL + 2,
-              B_PV_DONE = B_P_FULL + 2, B_R_FULL = B_PV_DONE + 1, B_R_FREE = B_R_FULL + 3,
-              B_DRAIN = B_R_FREE + 1, B_COUNT = B_DRAIN + 1;
+              B_PV_DONE = B_P_FULL + 2, B_R_FULL = B_PV_DONE + 2, B_R_FREE = B_R_FULL + 3,
+              B_DRAIN = B_R_FREE + 1, B_XCH = B_DRAIN + 1, B_COUNT = B_XCH + 4;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
-constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
+constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row-max exchange [2][2][128] f32
+constexpr uint32_t SM_TOTAL = SM_XCH + 2 * 2 * 128 * 4;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;  // + alignment slack
 
 struct TcArgs {
@@ -132,16 +135,18 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       mbar_init(bar(B_PS_FULL + i), 1);
       mbar_init(bar(B_PS_EMPTY + i), 1);
     }
-    mbar_init(bar(B_RT_FULL), 128);
-    mbar_init(bar(B_Q_READY), 128);
+    mbar_init(bar(B_RT_FULL), 256);
+    mbar_init(bar(B_Q_READY), 256);
     mbar_init(bar(B_S_FULL + 0), 1);
     mbar_init(bar(B_S_FULL + 1), 1);
-    mbar_init(bar(B_P_FULL + 0), 128);
-    mbar_init(bar(B_P_FULL + 1), 128);
-    mbar_init(bar(B_PV_DONE), 1);
+    mbar_init(bar(B_P_FULL + 0), 256);
+    mbar_init(bar(B_P_FULL + 1), 256);
+    mbar_init(bar(B_PV_DONE + 0), 1);
+    mbar_init(bar(B_PV_DONE + 1), 1);
     for (int i = 0; i < 3; ++i) mbar_init(bar(B_R_FULL + i), 1);
-    mbar_init(bar(B_R_FREE), 128);
+    mbar_init(bar(B_R_FREE), 256);
     mbar_init(bar(B_DRAIN), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(B_XCH + i), 64);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -191,19 +196,28 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
     if (nband > 0) {
       const int c_hi = min(c_last, (a.E - 1) / BN);     // chunks past E stay zero-filled
       for (int c = 0; c <= c_last; ++c) {
-        const int st = c & 1;
+        const int st = c % P_STAGES;
         if (c >= P_STAGES) {
-          const bool w = mbar_wait(bar(B_PS_EMPTY + st), ((c >> 1) - 1) & 1, abort_flag, 3);
+          const bool w = mbar_wait(bar(B_PS_EMPTY + st), ((c / P_STAGES) - 1) & 1, abort_flag, 3);
           if (!__all_sync(0xffffffffu, w)) break;
         }
         uint8_t *dst = smem + SM_PS + st * 8192;
-        for (int idx = lane; idx < a.rd_pad * 8; idx += 32) {
-          const int ch = idx >> 3, j = idx & 7, col = BN * c + 8 * j;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (c <= c_hi && ch < a.rd && col < a.E)
-            v = *reinterpret_cast<const uint4 *>(a.P + (size_t)ch * a.E + col);
-          *reinterpret_cast<uint4 *>(dst + (ch >> 3) * 1024 + (ch & 7) * 128 +
-                                     ((j ^ (ch & 7)) << 4)) = v;
+        // up to 64 channels x 8 sixteen-byte pieces = 16 per lane: issue every
+        // load before the first store so the L2 round trips overlap
+        uint4 v[16];
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+          const int idx = lane + 32 * it, ch = idx >> 3, j = idx & 7, col = BN * c + 8 * j;
+          v[it] = make_uint4(0u, 0u, 0u, 0u);
+          if (idx < a.rd_pad * 8 && c <= c_hi && ch < a.rd && col < a.E)
+            v[it] = *reinterpret_cast<const uint4 *>(a.P + (size_t)ch * a.E + col);
+        }
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+          const int idx = lane + 32 * it, ch = idx >> 3, j = idx & 7;
+          if (idx < a.rd_pad * 8)
+            *reinterpret_cast<uint4 *>(dst + (ch >> 3) * 1024 + (ch & 7) * 128 +
+                                       ((j ^ (ch & 7)) << 4)) = v[it];
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -218,6 +232,11 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       const uint32_t id_o = idesc_bf16_f32(BM, 128, 0, 1);      // O: P(tmem) x V(smem, MN-major)
       const uint32_t id_r = idesc_bf16_f32(BM, BN, 0, 1);       // R: r(smem) x P(smem, MN-major)
       const int r_ksteps = a.rd_pad / 16;
+      // descriptor bases; per k-step / stage only the 16-byte address field moves
+      const uint64_t kd0 = smem_desc_sw128(sb + SM_KV, 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(sb + SM_KV + 16384, 8192, 1024);
+      const uint64_t rd0 = smem_desc_sw128(sb + SM_RT, 16, 1024);
+      const uint64_t pd0 = smem_desc_sw128(sb + SM_PS, 8192, 1024);
       bool ok = mbar_wait(bar(B_Q_READY), 0, abort_flag, 6);
       tc_fence_after();
       bool rt_ready = false;
@@ -226,15 +245,15 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
           if (!mbar_wait(bar(B_RT_FULL), 0, abort_flag, 7)) return false;
           rt_ready = true;
         }
-        const int st = c & 1;
-        if (!mbar_wait(bar(B_PS_FULL + st), (c >> 1) & 1, abort_flag, 8)) return false;
+        const int st = c % P_STAGES;
+        if (!mbar_wait(bar(B_PS_FULL + st), (c / P_STAGES) & 1, abort_flag, 8)) return false;
         tc_fence_after();
         const uint32_t d = tmem + TM_R + 64u * (uint32_t)(c % 3);
-        for (int k = 0; k < r_ksteps; ++k) {
-          const uint64_t ad = smem_desc_sw128(sb + SM_RT + 32u * k, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sb + SM_PS + st * 8192 + 2048u * k, 8192, 1024);
-          mma_ss(d, ad, bd, id_r, k > 0);
-        }
+        const uint64_t pd = pd0 + (uint64_t)((st * 8192) >> 4);
+        mma_ss_c<0>(d, rd0, pd, id_r);
+        if (r_ksteps > 1) mma_ss_c<1>(d, rd0 + 2, pd + 128, id_r);
+        if (r_ksteps > 2) mma_ss_c<1>(d, rd0 + 4, pd + 256, id_r);
+        if (r_ksteps > 3) mma_ss_c<1>(d, rd0 + 6, pd + 384, id_r);
         mma_commit(bar(B_R_FULL + c % 3));
         mma_commit(bar(B_PS_EMPTY + st));
         return true;
@@ -244,11 +263,17 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
         if (!mbar_wait(bar(B_KV_FULL + st), (n / KV_STAGES) & 1, abort_flag, 9)) return false;
         tc_fence_after();
         const uint32_t d = tmem + TM_S0 + 64u * (uint32_t)(n & 1);
-        const uint32_t kb = sb + SM_KV + st * KV_STAGE_BYTES;
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t bd = smem_desc_sw128(kb + (k >> 2) * 8192 + 32u * (k & 3), 16, 1024);
-          mma_ts(d, tmem + TM_Q + 8u * k, bd, id_s, k > 0);
-        }
+        const uint64_t kd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
+        const uint32_t qa = tmem + TM_Q;
+        // k-step k: box k/4 (+8 KB), 32 bytes per step inside the 128-byte row
+        mma_ts_c<0>(d, qa + 0, kd + 0, id_s);
+        mma_ts_c<1>(d, qa + 8, kd + 2, id_s);
+        mma_ts_c<1>(d, qa + 16, kd + 4, id_s);
+        mma_ts_c<1>(d, qa + 24, kd + 6, id_s);
+        mma_ts_c<1>(d, qa + 32, kd + 512, id_s);
+        mma_ts_c<1>(d, qa + 40, kd + 514, id_s);
+        mma_ts_c<1>(d, qa + 48, kd + 516, id_s);
+        mma_ts_c<1>(d, qa + 56, kd + 518, id_s);
         mma_commit(bar(B_S_FULL + (n & 1)));
         return true;
       };
@@ -265,13 +290,15 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
         if (!(ok = mbar_wait(bar(B_P_FULL + (n & 1)), (n >> 1) & 1, abort_flag, 11))) break;
         tc_fence_after();
         const int st = n % KV_STAGES;
-        const uint32_t vb = sb + SM_KV + st * KV_STAGE_BYTES + 16384;
+        const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
         const uint32_t pa = tmem + TM_S0 + 64u * (uint32_t)(n & 1);
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t bd = smem_desc_sw128(vb + 2048u * k, 8192, 1024);
-          mma_ts(tmem + TM_O, pa + 8u * k, bd, id_o, (n > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(B_PV_DONE));
+        // k-step k = 16 keys = 2048 bytes of the MN-major V tile
+        if (n > 0) mma_ts_c<1>(tmem + TM_O, pa + 0, vd + 0, id_o);
+        else mma_ts_c<0>(tmem + TM_O, pa + 0, vd + 0, id_o);
+        mma_ts_c<1>(tmem + TM_O, pa + 8, vd + 128, id_o);
+        mma_ts_c<1>(tmem + TM_O, pa + 16, vd + 256, id_o);
+        mma_ts_c<1>(tmem + TM_O, pa + 24, vd + 384, id_o);
+        mma_commit(bar(B_PV_DONE + (n & 1)));
         mma_commit(bar(B_KV_EMPTY + st));
       }
       // drain: every MMA issued above has finished before TMEM is released
@@ -282,37 +309,43 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
     __syncwarp();
   } else if (warp >= 4) {
     // ======================================================== softmax
-    const int a_row = tid - 128;                 // 0..127 == TMEM lane
-    const int wq = warp - 4;                     // lane quarter
+    // Two warpgroups share the 128 rows: warpgroup wg handles keys
+    // [32 wg, 32 wg + 32) of every 64-key tile (and O / output columns
+    // [64 wg, 64 wg + 64)).  The two threads of a row agree on the running max
+    // through a shared-memory exchange guarded by a per-lane-quarter mbarrier.
+    const int wg = (warp - 4) >> 2;
+    const int wq = warp & 3;                     // lane quarter (TMEM lanes 32 wq ..)
+    const int a_row = 32 * wq + lane;            // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const int t_row = row0 + min(a_row, nrows - 1);
     const int pos = p0 + a_row;                  // padding rows only compute garbage
     const float sc = log_scale(min(pos, p_last), a.inv_ln_base);
     const float cqk = a.alpha_log2e * sc, cbias = kLog2e * sc;
+    float *xbuf = reinterpret_cast<float *>(smem + SM_XCH);   // [2 parity][2 wg][128]
 
-    // Q row -> TMEM (bf16 pairs)
+    // q row half -> TMEM columns [32 wg, 32 wg + 32) (bf16 pairs)
     {
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim);
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          a.q + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim + 64 * wg);
       uint32_t r[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = src[half * 8 + i];
-          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_base + TM_Q + 32u * half, r);
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = src[i];
+        r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
       }
+      __syncwarp();
+      tmem_st32(tmem + lane_base + TM_Q + 32u * wg, r);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_Q_READY));
     }
-    // r row -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
+    // r row half -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
     if (nband > 0) {
       const __nv_bfloat16 *rsrc = a.r + ((size_t)(cq + t_row) * a.Hq + h) * a.rd;
       uint8_t *rrow = smem + SM_RT + (a_row >> 3) * 1024 + (a_row & 7) * 128;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = 4 * wg + jj;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (8 * j < a.rd) v = *reinterpret_cast<const uint4 *>(rsrc + 8 * j);
         *reinterpret_cast<uint4 *>(rrow + ((j ^ (a_row & 7)) << 4)) = v;
@@ -327,29 +360,19 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       const bool r = mbar_wait(br, parity, abort_flag, site);
       return __all_sync(0xffffffffu, r);
     };
+    auto r_addr = [&](int d0) {  // TMEM address of distances d0 .. d0+31 (d0 >= 0)
+      return tmem + lane_base + TM_R + 64u * (uint32_t)((d0 >> 6) % 3) + (uint32_t)(d0 & 63);
+    };
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
       const uint32_t sbuf = tmem + lane_base + TM_S0 + 64u * (uint32_t)(n & 1);
       if (!(ok = warp_wait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1, 13))) break;
-      tc_fence_after();
-      float s[64];
-      {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(sbuf, r);
-        tmem_wait_ld(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(r[i]);
-        tmem_ld32(sbuf + 32, r);
-        tmem_wait_ld(r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(r[i]);
-      }
       const int D = tile_D(n);
       const int j0 = p0 - D;
-      if (n < nband) {
-        // wait for the newest chunk this tile needs (older ones were awaited before)
+      const bool band = n < nband;
+      if (band) {
+        // the newest chunk this tile needs (older ones were awaited before)
         if (n == 0) {
           for (int c = 0; c <= c_first && ok; ++c)
             ok = warp_wait(bar(B_R_FULL + c % 3), (c / 3) & 1, 14);
@@ -358,62 +381,70 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
           if (c >= 0) ok = warp_wait(bar(B_R_FULL + c % 3), (c / 3) & 1, 15);
         }
         if (!ok) break;
-        tc_fence_after();
-        const int sh = 31 - lane;  // per-thread shift of the distance window
+      }
+      tc_fence_after();
+      // distances D + a - (32 wg + u), u in [0, 32): window [base, base + 64)
+      const int base = D + 32 * wq - 32 * wg - 32;
+      uint32_t sr[32], w0[32], w1[32];
+      __syncwarp();
+      tmem_ld32(sbuf + 32u * wg, sr);
+      if (band) {
+        if (base >= 0) tmem_ld32(r_addr(base), w0);
+        if (base + 32 >= 0) tmem_ld32(r_addr(base + 32), w1);
+      }
+      tmem_wait_ld(sr);
+      reg_dep(w0);
+      reg_dep(w1);
+      float x[32];
+      if (band) {
+        // z[63 - i] = window[i]; the thread of lane t needs window[32 + t - u]
+        float z[64];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          // distances D + a - (32 g + u), u in [0, 32): window [base, base + 64)
-          const int base = D + 32 * wq - 32 * g - 32;
-          float z[64];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int d0 = base + 32 * hh;
-            if (d0 >= 0) {
-              const int c = d0 >> 6;
-              uint32_t r[32];
-              __syncwarp();
-              tmem_ld32(tmem + lane_base + TM_R + 64u * (uint32_t)(c % 3) + (uint32_t)(d0 & 63), r);
-              tmem_wait_ld(r);
-              // reversed: z[63 - i] = window[i]
-#pragma unroll
-              for (int i = 0; i < 32; ++i) z[63 - (32 * hh + i)] = __uint_as_float(r[i]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) z[63 - (32 * hh + i)] = 0.f;
-            }
-          }
-          // y[u] = z[u + sh]: shift left by sh with a select network
-#pragma unroll
-          for (int i = 0; i < 47; ++i) z[i] = (sh & 16) ? z[i + 16] : z[i];
-#pragma unroll
-          for (int i = 0; i < 39; ++i) z[i] = (sh & 8) ? z[i + 8] : z[i];
-#pragma unroll
-          for (int i = 0; i < 35; ++i) z[i] = (sh & 4) ? z[i + 4] : z[i];
-#pragma unroll
-          for (int i = 0; i < 33; ++i) z[i] = (sh & 2) ? z[i + 2] : z[i];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = (sh & 1) ? z[i + 1] : z[i];
-#pragma unroll
-          for (int u = 0; u < 32; ++u) s[32 * g + u] = fmaf(s[32 * g + u], cqk, z[u] * cbias);
+        for (int i = 0; i < 32; ++i) {
+          z[63 - i] = base >= 0 ? __uint_as_float(w0[i]) : 0.f;
+          z[31 - i] = base + 32 >= 0 ? __uint_as_float(w1[i]) : 0.f;
         }
         tc_fence_before();
         mbar_arrive(bar(B_R_FREE));
+        // y[u] = z[u + sh], sh = 31 - lane: shift with a select network
+        const int sh = 31 - lane;
+#pragma unroll
+        for (int i = 0; i < 47; ++i) z[i] = (sh & 16) ? z[i + 16] : z[i];
+#pragma unroll
+        for (int i = 0; i < 39; ++i) z[i] = (sh & 8) ? z[i + 8] : z[i];
+#pragma unroll
+        for (int i = 0; i < 35; ++i) z[i] = (sh & 4) ? z[i + 4] : z[i];
+#pragma unroll
+        for (int i = 0; i < 33; ++i) z[i] = (sh & 2) ? z[i + 2] : z[i];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = (sh & 1) ? z[i + 1] : z[i];
+#pragma unroll
+        for (int u = 0; u < 32; u += 2)
+          ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
+                z[u] * cbias, z[u + 1] * cbias);
       } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] *= cqk;
+        for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(sr[u]) * cqk;
       }
       const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
       if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int j = j0 + i;
+        for (int i = 0; i < 32; ++i) {
+          const int j = j0 + 32 * wg + i;
           const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
-          s[i] = vis ? s[i] : -INFINITY;
+          x[i] = vis ? x[i] : -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      float mloc = fmax3(x[0], x[1], x[2]);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 3; i < 31; i += 2) mloc = fmax3(mloc, x[i], x[i + 1]);
+      mloc = fmaxf(mloc, x[31]);
+      // agree on the row max with the other warpgroup
+      float *xb = xbuf + (n & 1) * 256;
+      xb[wg * 128 + a_row] = mloc;
+      mbar_arrive(bar(B_XCH + wq));
+      if (!(ok = warp_wait(bar(B_XCH + wq), n & 1, 18))) break;
+      const float mx = fmaxf(mloc, xb[(1 - wg) * 128 + a_row]);
       float corr = 1.f;
       bool rescale_o = false;
       if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
@@ -425,36 +456,41 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       {
-        uint32_t pk[32];
-        float rs = 0.f;
+        uint32_t pk[16];
+        float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float e0 = fast_exp2(s[2 * i] - m_use), e1 = fast_exp2(s[2 * i + 1] - m_use);
-          rs += e0 + e1;
+        for (int i = 0; i < 16; ++i) {
+          const float e0 = fast_exp2(x[2 * i] - m_use), e1 = fast_exp2(x[2 * i + 1] - m_use);
+          rs0 += e0;
+          rs1 += e1;
           pk[i] = pack_bf16x2(e0, e1);
         }
-        l += rs;
+        l += rs0 + rs1;
         __syncwarp();
-        tmem_st32(sbuf, pk);
+        tmem_st16(sbuf + 16u * wg, pk);   // P (bf16 pairs) over S columns [16 wg, 16 wg + 16)
       }
-      if (n > 0) {
-        if (!(ok = warp_wait(bar(B_PV_DONE), (n - 1) & 1, 16))) break;
-        tc_fence_after();
-      }
+      // O is only touched when some row of this warp needs a rescale; then PV(n-1)
+      // must have landed first.  Otherwise PV(n) simply queues behind PV(n-1)
+      // on the tensor core.  (PV completions alternate between two barriers by
+      // tile parity; S(n) landing implies PV(n-2) did, so each wait is for the
+      // next phase of its barrier and never ambiguous.)
       // TMEM loads / stores are warp-collective: the whole warp rescales its 32
       // rows when any of them needs it (rows that do not are scaled by 1)
       if (__any_sync(0xffffffffu, rescale_o)) {
+        if (!(ok = warp_wait(bar(B_PV_DONE + ((n - 1) & 1)), ((n - 1) >> 1) & 1, 16))) break;
+        tc_fence_after();
         const float cf = rescale_o ? corr : 1.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
+          const uint32_t oaddr = tmem + lane_base + TM_O + 64u * wg + 32u * c;
           __syncwarp();
-          tmem_ld32(tmem + lane_base + TM_O + 32u * c, r);
+          tmem_ld32(oaddr, r);
           tmem_wait_ld(r);
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * cf);
           __syncwarp();
-          tmem_st32(tmem + lane_base + TM_O + 32u * c, r);
+          tmem_st32(oaddr, r);
         }
       }
       tmem_wait_st();
@@ -462,17 +498,26 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       mbar_arrive(bar(B_P_FULL + (n & 1)));
     }
     // ---- epilogue
-    if (ok && ntiles > 0) ok = warp_wait(bar(B_PV_DONE), (ntiles - 1) & 1, 17);
+    if (ok && ntiles > 0)
+      ok = warp_wait(bar(B_PV_DONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 17);
     if (ok) {
+      // total row sum over both key halves
+      float *xb = xbuf + (ntiles & 1) * 256;
+      xb[wg * 128 + a_row] = l;
+      mbar_arrive(bar(B_XCH + wq));
+      ok = warp_wait(bar(B_XCH + wq), ntiles & 1, 19);
+    }
+    if (ok) {
+      const float lt = l + xbuf[(ntiles & 1) * 256 + (1 - wg) * 128 + a_row];
       tc_fence_after();
       const bool valid = a_row < nrows;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *dst = a.out + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16 *dst = a.out + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim + 64 * wg;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
         __syncwarp();
-        tmem_ld32(tmem + lane_base + TM_O + 32u * c, r);
+        tmem_ld32(tmem + lane_base + TM_O + 64u * wg + 32u * c, r);
         tmem_wait_ld(r);
         if (valid) {
 #pragma unroll
@@ -486,9 +531,9 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
           }
         }
       }
-      if (valid)
+      if (valid && wg == 0)
         a.lse[(size_t)h * a.total_q + cq + t_row] =
-            l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+            lt > 0.f ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
     }
   }
 

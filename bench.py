@@ -48,8 +48,10 @@ KERNEL_SOURCES = {
     "prefill": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
                 "relative_position_biased_gb300/csrc/tc_common.cuh",
                 "relative_position_biased_gb300/csrc/common.cuh"],
-    "decode": ["relative_position_biased_gb300/csrc/fwd_mma.cu",
-               "relative_position_biased_gb300/csrc/common.cuh"],
+    "decode": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
+               "relative_position_biased_gb300/csrc/tc_common.cuh",
+               "relative_position_biased_gb300/csrc/common.cuh",
+               "relative_position_biased_gb300/csrc/combine.cu"],
 }
 L2_FLUSH_BYTES = 256 << 20
 

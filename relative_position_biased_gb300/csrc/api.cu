@@ -107,6 +107,7 @@ relattn_status make_args(const relattn_params *p, KernelArgs *a) {
 }
 
 struct DecodePlan {
+  bool tc;               // tcgen05 kernel (else the warp-MMA kernel)
   int warps, row_blocks, splits, chunk;
   size_t ws_bytes, lse_offset;
 };
@@ -117,8 +118,11 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
   if (st != RELATTN_OK) return st;
   const int group = p->num_heads_q / p->num_heads_kv;
   const int rows = p->max_seqlen_q * group;
+  KernelArgs probe;
+  if ((st = make_args(p, &probe)) != RELATTN_OK) return st;
+  plan->tc = tc_supported(probe, p->total_k);
   plan->warps = decode_warps_for_rows(rows < 128 ? rows : 128);
-  const int m = plan->warps * 16;
+  const int m = plan->tc ? kTcDecodeRows : plan->warps * 16;
   plan->row_blocks = (rows + m - 1) / m;
   const int tile = kDecodeKeyTile;
   // keys any CTA of one (sequence, kv head) may visit, from an aligned start
@@ -168,7 +172,7 @@ relattn_status relattn_prefill(const relattn_params *p, void *stream) {
   KernelArgs a;
   if ((st = make_args(p, &a)) != RELATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (prefill_tc_supported(a, p->total_k)) return cuda_status(launch_prefill_tc(a, p->total_k, s));
+  if (tc_supported(a, p->total_k)) return cuda_status(launch_prefill_tc(a, p->total_k, s));
   return cuda_status(launch_prefill_mma(a, s));
 }
 
@@ -214,7 +218,9 @@ relattn_status relattn_decode(const relattn_params *p, void *stream) {
     a.lse_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + plan.lse_offset);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if ((st = cuda_status(launch_decode_mma(a, plan.warps, s))) != RELATTN_OK) return st;
+  st = plan.tc ? cuda_status(launch_decode_tc(a, p->total_k, s))
+               : cuda_status(launch_decode_mma(a, plan.warps, s));
+  if (st != RELATTN_OK) return st;
   if (plan.splits > 1)
     st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
                                     p->num_heads_q, a.out, a.lse, s));

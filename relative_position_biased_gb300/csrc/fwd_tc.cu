@@ -80,8 +80,9 @@ struct TcArgs {
 
 __device__ __forceinline__ int floor_div64(int x) { return x >= 0 ? x >> 6 : -((63 - x) >> 6); }
 
+template <bool DECODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
-relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
+relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
                               const __grid_constant__ CUtensorMap map_k,
                               const __grid_constant__ CUtensorMap map_v) {
   const KernelArgs &a = ta.a;
@@ -95,35 +96,73 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ------------------------------------------------------------ work item
-  const int q_tile = a.q_tiles - 1 - blockIdx.x;
-  const int h = blockIdx.y, b = blockIdx.z;
+  // prefill: one query head x 128 consecutive rows.  decode: 128 rows of the
+  // (token, head-in-group) list of one kv head, and one split of its keys.
+  int b, kv_head, row0, nrows, split = 0, h_fixed = 0;
+  if constexpr (DECODE) {
+    split = blockIdx.x;
+    kv_head = blockIdx.y / a.row_blocks;
+    row0 = (blockIdx.y % a.row_blocks) * BM;
+    b = blockIdx.z;
+  } else {
+    h_fixed = blockIdx.y;
+    kv_head = h_fixed / a.group;
+    row0 = (a.q_tiles - 1 - blockIdx.x) * BM;   // longest-running tiles first
+    b = blockIdx.z;
+  }
   const int cq = a.cu_q[b], ck = a.cu_k[b];
   const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
   if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) {
     if (tid == 0) atomicOr(a.err, kDevErrSeqlens);
     return;
   }
-  const int row0 = q_tile * BM;
-  const int nrows = min(BM, Lq - row0);
+  nrows = min(BM, (DECODE ? Lq * a.group : Lq) - row0);
   if (nrows <= 0) return;
-  const int kv_head = h / a.group;
   const int off = Lk - Lq;
-  const int p0 = off + row0, p_last = p0 + nrows - 1;
+  // row (local, clamped to the last valid one) -> token t and query head
+  auto row_t = [&](int rl) {
+    const int x = row0 + min(rl, nrows - 1);
+    return DECODE ? x / a.group : x;
+  };
+  auto row_h = [&](int rl) {
+    const int x = row0 + min(rl, nrows - 1);
+    return DECODE ? kv_head * a.group + x % a.group : h_fixed;
+  };
+  const int p0 = off + row_t(0), p_last = off + row_t(nrows - 1);
   const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
-  // key tiles start at j0(n) = p0 + 64 - 64 n  (offset D(n) = p0 - j0 = 64 n - 64)
-  const int D_first = (p_last >= p0 + BN) ? -BN : 0;
-  const int ntiles = (p0 - j_lo - D_first + BN - 1) / BN + 1;
+  // distance offset D(n) = p0 - j0(n) of the key tile processed n-th (from the
+  // diagonal backwards); rows sit at p0 + delta, delta <= span
+  int ntiles, D_first, span;
+  if constexpr (DECODE) {
+    const int kbase = j_lo & ~(BN - 1);
+    const int kbeg = kbase + split * a.split_chunk;
+    const int kend = min(p_last + 1, kbeg + a.split_chunk);
+    ntiles = kend > kbeg ? (kend - kbeg + BN - 1) / BN : 0;
+    D_first = p0 - (kbeg + (ntiles - 1) * BN);
+    span = p_last - p0;
+  } else {
+    // key tiles start at j0(n) = p0 + 64 - 64 n  (D = 64 n - 64), or one tile
+    // later when every row of the block sits in the first 64 positions
+    D_first = (p_last >= p0 + BN) ? -BN : 0;
+    ntiles = (p0 - j_lo - D_first + BN - 1) / BN + 1;
+    span = BM - 1;   // padding rows reuse the pattern of full tiles
+  }
   auto tile_D = [&](int n) { return D_first + BN * n; };
   // band tiles (some distance < E) form a prefix of the tile order
   int nband = 0;
-  if (ta.has_bias) {
-    nband = ntiles;
+  if (ta.has_bias && ntiles > 0) {
     const int lim = a.E + BN - 1;  // band iff D - 63 < E
-    if (tile_D(ntiles - 1) >= lim) nband = (lim - D_first + BN - 1) / BN;
+    nband = tile_D(ntiles - 1) < lim ? ntiles : max(0, (lim - D_first + BN - 1) / BN);
     if (nband > ntiles) nband = ntiles;
   }
-  const int c_first = floor_div64(tile_D(0)) + 1;             // newest chunk tile 0 needs
-  const int c_last = nband > 0 ? floor_div64(tile_D(nband - 1)) + 1 : -1;
+  // newest 64-distance chunk of r.P a tile needs (one more per tile)
+  auto c_new = [&](int n) { return floor_div64(tile_D(n) + span); };
+  const int c_first = c_new(0);
+  const int c_last = nband > 0 ? c_new(nband - 1) : -1;
+  // first chunk computed: the oldest one tile 0 reads (a decode split far from
+  // the diagonal starts deep in the band).  Chunk c uses ring slot / P stage /
+  // barrier phase counted from c_start.
+  const int c_start = nband > 0 ? max(0, floor_div64(tile_D(0) - (BN - 1))) : 0;
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
@@ -171,7 +210,7 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
         const int st = n % KV_STAGES;
         if (n >= KV_STAGES && !mbar_wait(bar(B_KV_EMPTY + st), ((n / KV_STAGES) - 1) & 1, abort_flag, 1))
           break;
-        const int key = ck + p0 - tile_D(n);
+        const int key = ck + p0 - tile_D(n);   // may be < 0: the tile reads zeros there
         const uint32_t dst = sb + SM_KV + st * KV_STAGE_BYTES;
         mbar_arrive_expect_tx(bar(B_KV_FULL + st), KV_STAGE_BYTES);
         tma_load_3d(dst, &map_k, 0, kv_head, key, bar(B_KV_FULL + st));
@@ -195,10 +234,11 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
     // and past r_dim.  Plain 16-byte loads (P is small and L2-resident).
     if (nband > 0) {
       const int c_hi = min(c_last, (a.E - 1) / BN);     // chunks past E stay zero-filled
-      for (int c = 0; c <= c_last; ++c) {
-        const int st = c % P_STAGES;
-        if (c >= P_STAGES) {
-          const bool w = mbar_wait(bar(B_PS_EMPTY + st), ((c / P_STAGES) - 1) & 1, abort_flag, 3);
+      for (int c = c_start; c <= c_last; ++c) {
+        const int o = c - c_start;
+        const int st = o % P_STAGES;
+        if (o >= P_STAGES) {
+          const bool w = mbar_wait(bar(B_PS_EMPTY + st), ((o / P_STAGES) - 1) & 1, abort_flag, 3);
           if (!__all_sync(0xffffffffu, w)) break;
         }
         uint8_t *dst = smem + SM_PS + st * 8192;
@@ -245,16 +285,17 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
           if (!mbar_wait(bar(B_RT_FULL), 0, abort_flag, 7)) return false;
           rt_ready = true;
         }
-        const int st = c % P_STAGES;
-        if (!mbar_wait(bar(B_PS_FULL + st), (c / P_STAGES) & 1, abort_flag, 8)) return false;
+        const int o = c - c_start;
+        const int st = o % P_STAGES;
+        if (!mbar_wait(bar(B_PS_FULL + st), (o / P_STAGES) & 1, abort_flag, 8)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + TM_R + 64u * (uint32_t)(c % 3);
+        const uint32_t d = tmem + TM_R + 64u * (uint32_t)(o % 3);
         const uint64_t pd = pd0 + (uint64_t)((st * 8192) >> 4);
         mma_ss_c<0>(d, rd0, pd, id_r);
         if (r_ksteps > 1) mma_ss_c<1>(d, rd0 + 2, pd + 128, id_r);
         if (r_ksteps > 2) mma_ss_c<1>(d, rd0 + 4, pd + 256, id_r);
         if (r_ksteps > 3) mma_ss_c<1>(d, rd0 + 6, pd + 384, id_r);
-        mma_commit(bar(B_R_FULL + c % 3));
+        mma_commit(bar(B_R_FULL + o % 3));
         mma_commit(bar(B_PS_EMPTY + st));
         return true;
       };
@@ -278,12 +319,12 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
         return true;
       };
       if (ok && nband > 0)
-        for (int c = 0; c <= c_first && ok; ++c) ok = issue_r(c);
-      if (ok) ok = issue_s(0);
+        for (int c = c_start; c <= c_first && ok; ++c) ok = issue_r(c);
+      if (ok && ntiles > 0) ok = issue_s(0);   // an empty decode split issues nothing
       for (int n = 0; n < ntiles && ok; ++n) {
         if (n + 1 < ntiles && !(ok = issue_s(n + 1))) break;
         if (n + 1 < nband) {
-          const int c = floor_div64(tile_D(n + 1)) + 1;
+          const int c = c_new(n + 1);
           if (!(ok = mbar_wait(bar(B_R_FREE), n & 1, abort_flag, 10))) break;
           if (c >= 0 && !(ok = issue_r(c))) break;
         }
@@ -317,8 +358,12 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
     const int wq = warp & 3;                     // lane quarter (TMEM lanes 32 wq ..)
     const int a_row = 32 * wq + lane;            // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    const int t_row = row0 + min(a_row, nrows - 1);
-    const int pos = p0 + a_row;                  // padding rows only compute garbage
+    const int t_row = row_t(a_row), h_row = row_h(a_row);
+    // position of this row; prefill padding rows (a_row >= nrows) continue the
+    // diagonal pattern and only compute garbage that is never stored
+    const int pos = DECODE ? off + t_row : p0 + a_row;
+    const int delta = pos - p0;                  // 0 .. span
+    const int delta_w = DECODE ? off + row_t(32 * wq) - p0 : 32 * wq;   // first row of the warp
     const float sc = log_scale(min(pos, p_last), a.inv_ln_base);
     const float cqk = a.alpha_log2e * sc, cbias = kLog2e * sc;
     float *xbuf = reinterpret_cast<float *>(smem + SM_XCH);   // [2 parity][2 wg][128]
@@ -326,7 +371,7 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
     // q row half -> TMEM columns [32 wg, 32 wg + 32) (bf16 pairs)
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(
-          a.q + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim + 64 * wg);
+          a.q + ((size_t)(cq + t_row) * a.Hq + h_row) * kHeadDim + 64 * wg);
       uint32_t r[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -341,7 +386,7 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
     }
     // r row half -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
     if (nband > 0) {
-      const __nv_bfloat16 *rsrc = a.r + ((size_t)(cq + t_row) * a.Hq + h) * a.rd;
+      const __nv_bfloat16 *rsrc = a.r + ((size_t)(cq + t_row) * a.Hq + h_row) * a.rd;
       uint8_t *rrow = smem + SM_RT + (a_row >> 3) * 1024 + (a_row & 7) * 128;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
@@ -360,9 +405,11 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       const bool r = mbar_wait(br, parity, abort_flag, site);
       return __all_sync(0xffffffffu, r);
     };
-    auto r_addr = [&](int d0) {  // TMEM address of distances d0 .. d0+31 (d0 >= 0)
-      return tmem + lane_base + TM_R + 64u * (uint32_t)((d0 >> 6) % 3) + (uint32_t)(d0 & 63);
+    // TMEM address of distances d0 .. d0+31; valid for chunks >= c_start
+    auto r_addr = [&](int d0) {
+      return tmem + lane_base + TM_R + 64u * (uint32_t)(((d0 >> 6) - c_start) % 3) + (uint32_t)(d0 & 63);
     };
+    const int d_min = BN * c_start;   // smaller distances were never computed (not needed)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
@@ -374,59 +421,111 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       if (band) {
         // the newest chunk this tile needs (older ones were awaited before)
         if (n == 0) {
-          for (int c = 0; c <= c_first && ok; ++c)
-            ok = warp_wait(bar(B_R_FULL + c % 3), (c / 3) & 1, 14);
+          for (int c = c_start; c <= c_first && ok; ++c)
+            ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 14);
         } else {
-          const int c = floor_div64(D) + 1;
-          if (c >= 0) ok = warp_wait(bar(B_R_FULL + c % 3), (c / 3) & 1, 15);
+          const int c = c_new(n);
+          if (c >= c_start) ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 15);
         }
         if (!ok) break;
       }
       tc_fence_after();
-      // distances D + a - (32 wg + u), u in [0, 32): window [base, base + 64)
-      const int base = D + 32 * wq - 32 * wg - 32;
-      uint32_t sr[32], w0[32], w1[32];
+      uint32_t sr[32];
       __syncwarp();
       tmem_ld32(sbuf + 32u * wg, sr);
-      if (band) {
-        if (base >= 0) tmem_ld32(r_addr(base), w0);
-        if (base + 32 >= 0) tmem_ld32(r_addr(base + 32), w1);
-      }
-      tmem_wait_ld(sr);
-      reg_dep(w0);
-      reg_dep(w1);
       float x[32];
-      if (band) {
-        // z[63 - i] = window[i]; the thread of lane t needs window[32 + t - u]
-        float z[64];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          z[63 - i] = base >= 0 ? __uint_as_float(w0[i]) : 0.f;
-          z[31 - i] = base + 32 >= 0 ? __uint_as_float(w1[i]) : 0.f;
+      if constexpr (!DECODE) {
+        // distances D + a - (32 wg + u), u in [0, 32): window [base, base + 64),
+        // base a multiple of 32 (D is a multiple of 64 here)
+        const int base = D + 32 * wq - 32 * wg - 32;
+        uint32_t w0[32], w1[32];
+        if (band) {
+          if (base >= d_min) tmem_ld32(r_addr(base), w0);
+          if (base + 32 >= d_min) tmem_ld32(r_addr(base + 32), w1);
         }
-        tc_fence_before();
-        mbar_arrive(bar(B_R_FREE));
-        // y[u] = z[u + sh], sh = 31 - lane: shift with a select network
-        const int sh = 31 - lane;
+        tmem_wait_ld(sr);
+        reg_dep(w0);
+        reg_dep(w1);
+        if (band) {
+          // z[63 - i] = window[i]; the thread of lane t needs window[32 + t - u]
+          float z[64];
 #pragma unroll
-        for (int i = 0; i < 47; ++i) z[i] = (sh & 16) ? z[i + 16] : z[i];
+          for (int i = 0; i < 32; ++i) {
+            z[63 - i] = base >= d_min ? __uint_as_float(w0[i]) : 0.f;
+            z[31 - i] = base + 32 >= d_min ? __uint_as_float(w1[i]) : 0.f;
+          }
+          tc_fence_before();
+          mbar_arrive(bar(B_R_FREE));
+          // y[u] = z[u + sh], sh = 31 - lane: shift with a select network
+          const int sh = 31 - lane;
 #pragma unroll
-        for (int i = 0; i < 39; ++i) z[i] = (sh & 8) ? z[i + 8] : z[i];
+          for (int i = 0; i < 47; ++i) z[i] = (sh & 16) ? z[i + 16] : z[i];
 #pragma unroll
-        for (int i = 0; i < 35; ++i) z[i] = (sh & 4) ? z[i + 4] : z[i];
+          for (int i = 0; i < 39; ++i) z[i] = (sh & 8) ? z[i + 8] : z[i];
 #pragma unroll
-        for (int i = 0; i < 33; ++i) z[i] = (sh & 2) ? z[i + 2] : z[i];
+          for (int i = 0; i < 35; ++i) z[i] = (sh & 4) ? z[i + 4] : z[i];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = (sh & 1) ? z[i + 1] : z[i];
+          for (int i = 0; i < 33; ++i) z[i] = (sh & 2) ? z[i + 2] : z[i];
 #pragma unroll
-        for (int u = 0; u < 32; u += 2)
-          ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
-                z[u] * cbias, z[u + 1] * cbias);
+          for (int i = 0; i < 32; ++i) z[i] = (sh & 1) ? z[i + 1] : z[i];
+#pragma unroll
+          for (int u = 0; u < 32; u += 2)
+            ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
+                  z[u] * cbias, z[u + 1] * cbias);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(sr[u]) * cqk;
+        }
       } else {
+        tmem_wait_ld(sr);
+        if (band) {
+          // rows of a warp span at most 16 positions: distances
+          // D + delta - (32 wg + u) lie in a 96-wide window [bal, bal + 96)
+          // starting at a multiple of 32
+          const int lo = D + delta_w - 32 * wg - 31;
+          const int bal = lo & ~31;
+          float z[96];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(sr[u]) * cqk;
+          for (int hh = 0; hh < 3; ++hh) {
+            uint32_t w[32];
+            const int d0 = bal + 32 * hh;
+            if (d0 >= d_min) {
+              __syncwarp();
+              tmem_ld32(r_addr(d0), w);
+              tmem_wait_ld(w);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[95 - (32 * hh + i)] = d0 >= d_min ? __uint_as_float(w[i]) : 0.f;
+          }
+          tc_fence_before();
+          mbar_arrive(bar(B_R_FREE));
+          // y[u] = window[i0 - u] = z[95 - i0 + u] with 95 - i0 in [18, 64]
+          const int i0 = D + delta - 32 * wg - bal;
+          const int sh = 95 - i0 - 18;
+          float* zz = z + 18;   // 78 entries
+#pragma unroll
+          for (int i = 0; i < 46; ++i) zz[i] = (sh & 32) ? zz[i + 32] : zz[i];
+#pragma unroll
+          for (int i = 0; i < 47; ++i) zz[i] = (sh & 16) ? zz[i + 16] : zz[i];
+#pragma unroll
+          for (int i = 0; i < 39; ++i) zz[i] = (sh & 8) ? zz[i + 8] : zz[i];
+#pragma unroll
+          for (int i = 0; i < 35; ++i) zz[i] = (sh & 4) ? zz[i + 4] : zz[i];
+#pragma unroll
+          for (int i = 0; i < 33; ++i) zz[i] = (sh & 2) ? zz[i + 2] : zz[i];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) zz[i] = (sh & 1) ? zz[i + 1] : zz[i];
+#pragma unroll
+          for (int u = 0; u < 32; u += 2)
+            ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
+                  zz[u] * cbias, zz[u + 1] * cbias);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(sr[u]) * cqk;
+        }
       }
       const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+      (void)delta;
       if (need_mask) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -512,14 +611,30 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
       tc_fence_after();
       const bool valid = a_row < nrows;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      __nv_bfloat16 *dst = a.out + ((size_t)(cq + t_row) * a.Hq + h) * kHeadDim + 64 * wg;
+      const float row_lse = lt > 0.f ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
+      const size_t qrow = (size_t)(cq + t_row) * a.Hq + h_row;
+      // decode with several splits leaves fp32 partials for the combine kernel
+      const bool partial = DECODE && a.num_splits > 1;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tmem + lane_base + TM_O + 64u * wg + 32u * c, r);
-        tmem_wait_ld(r);
-        if (valid) {
+        if (ntiles > 0) {
+          __syncwarp();
+          tmem_ld32(tmem + lane_base + TM_O + 64u * wg + 32u * c, r);
+          tmem_wait_ld(r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;   // an empty split contributes nothing
+        }
+        if (valid && partial) {
+          float *dst = a.o_part + ((size_t)split * a.total_q * a.Hq + qrow) * kHeadDim + 64 * wg + 32 * c;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float4 *>(dst + 4 * i) =
+                make_float4(__uint_as_float(r[4 * i]) * inv, __uint_as_float(r[4 * i + 1]) * inv,
+                            __uint_as_float(r[4 * i + 2]) * inv, __uint_as_float(r[4 * i + 3]) * inv);
+        } else if (valid) {
+          __nv_bfloat16 *dst = a.out + qrow * kHeadDim + 64 * wg + 32 * c;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 v;
@@ -527,13 +642,14 @@ relattn_fwd_tc_prefill_kernel(const __grid_constant__ TcArgs ta,
             v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]) * inv, __uint_as_float(r[8 * i + 3]) * inv);
             v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]) * inv, __uint_as_float(r[8 * i + 5]) * inv);
             v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]) * inv, __uint_as_float(r[8 * i + 7]) * inv);
-            *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * i) = v;
+            *reinterpret_cast<uint4 *>(dst + 8 * i) = v;
           }
         }
       }
-      if (valid && wg == 0)
-        a.lse[(size_t)h * a.total_q + cq + t_row] =
-            lt > 0.f ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
+      if (valid && wg == 0) {
+        if (partial) a.lse_part[(size_t)split * a.total_q * a.Hq + qrow] = row_lse;
+        else a.lse[(size_t)h_row * a.total_q + cq + t_row] = row_lse;
+      }
     }
   }
 
@@ -577,7 +693,7 @@ bool encode(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
 
 }  // namespace
 
-bool prefill_tc_supported(const KernelArgs &a, int total_k) {
+bool tc_supported(const KernelArgs &a, int total_k) {
   auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (!get_encoder()) return false;
   if (!al(a.k) || !al(a.v) || !al(a.q) || !al(a.out)) return false;
@@ -588,7 +704,10 @@ bool prefill_tc_supported(const KernelArgs &a, int total_k) {
   return true;
 }
 
-cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {
+namespace {
+
+template <bool DECODE>
+cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t stream) {
   TcArgs ta;
   ta.a = a;
   ta.has_bias = a.rd > 0 && a.E > 0;
@@ -604,14 +723,23 @@ cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t str
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_prefill_kernel,
+    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_kernel<DECODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  dim3 grid(a.q_tiles, a.Hq, a.batch);
-  relattn_fwd_tc_prefill_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv);
+  relattn_fwd_tc_kernel<DECODE><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {
+  return launch_tc<false>(a, total_k, dim3(a.q_tiles, a.Hq, a.batch), stream);
+}
+
+cudaError_t launch_decode_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {
+  return launch_tc<true>(a, total_k, dim3(a.num_splits, a.Hkv * a.row_blocks, a.batch), stream);
 }
 
 }  // namespace relattn

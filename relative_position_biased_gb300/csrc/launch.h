@@ -16,10 +16,14 @@ size_t decode_mma_smem_bytes(int warps, int rd_pad);
 
 cudaError_t launch_prefill_mma(const KernelArgs &a, cudaStream_t stream);
 
-// tcgen05 / TMA prefill: needs 16-byte aligned q/k/v/out, r_dim % 8 == 0 and
-// rel_extent % 8 == 0 (TMA strides), r_dim <= 64.
-bool prefill_tc_supported(const KernelArgs &a, int total_k);
+// tcgen05 / TMA kernels: need 16-byte aligned q/k/v/out (and r/P), r_dim % 8 == 0,
+// rel_extent % 8 == 0, r_dim <= 64 and at least one 64-key tile of K/V.
+bool tc_supported(const KernelArgs &a, int total_k);
 cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream);
+// decode on the same kernel: 128 rows of (token, head-in-group) per CTA; grid
+// (num_splits, Hkv * row_blocks, batch); partials when num_splits > 1.
+constexpr int kTcDecodeRows = 128;
+cudaError_t launch_decode_tc(const KernelArgs &a, int total_k, cudaStream_t stream);
 cudaError_t launch_decode_mma(const KernelArgs &a, int warps, cudaStream_t stream);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits,
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,

@@ -124,7 +124,7 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
   plan->warps = decode_warps_for_rows(rows < 128 ? rows : 128);
   const int m = plan->tc ? kTcDecodeRows : plan->warps * 16;
   plan->row_blocks = (rows + m - 1) / m;
-  const int tile = kDecodeKeyTile;
+  const int tile = plan->tc ? kTcKeyTile : kDecodeKeyTile;
   // keys any CTA of one (sequence, kv head) may visit, from an aligned start
   long max_vis = p->max_seqlen_k;
   if (p->window > 0) {

@@ -1,37 +1,47 @@
-// fwd_tc.cu -- relative-attention prefill on 5th-generation tensor cores
-// (tcgen05.mma, accumulators in tensor memory, TMA-fed K/V).
+// fwd_tc.cu -- relative-attention forward on 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory, TMA-fed K/V), prefill and
+// split-KV decode.
 //
 // Same computation as the definition on the page "SGLang and Miles Add Day-0
 // Support for Inkling", section "Attention with Relative Positional
 // Embedding":  x(i,j) = s(i) * (alpha q_i.k_j + [0 <= i-j < E] r_i . P[:, i-j]),
 // online softmax, PV.
 //
-// One CTA = one query head x 128 query rows (TMEM lane a <-> row a), keys in
-// tiles of 64, visited from the diagonal backwards.  Warp roles:
-//   warp 0      TMA producer for K and V tiles (4-stage ring)
+// One CTA = 128 query rows (TMEM lane a <-> row a): prefill takes one query
+// head x 128 consecutive rows; decode takes 128 rows of the (token,
+// head-in-group) list of one kv head and one split of its keys.  Keys come in
+// 128-key tiles (one TMA stage), visited from the diagonal backwards.  Tiles
+// inside the relative-bias band are processed as two 64-key half steps (the
+// upper half first); the rest as one 128-key step.  Warp roles:
+//   warp 0      TMA producer for K tiles (3-stage ring of 128 keys)
+//   warp 3      TMA producer for V tiles (2-stage ring); K and V stages are
+//               freed separately (K once its S MMAs are done, V after PV)
 //   warp 1      MMA issuer (one thread):  S = Q K^T (Q in TMEM),
 //               R_chunk = r P[:, 64c..64c+64) (both operands from shared
 //               memory), O += P V (P in TMEM)
 //   warp 2      TMEM allocator; producer of the P slices (plain loads into
 //               the 128-byte-swizzled layout)
 //   warps 4-11  softmax, two warpgroups: row a is owned by one thread of each
-//               (TMEM lane a); warpgroup wg takes keys [32 wg, 32 wg + 32) of
-//               every tile.  They write the q / r rows, load S from TMEM, add
-//               the relative bias, mask edge tiles, agree on the running row
-//               max through shared memory, write P (bf16) back over S, rescale
-//               their half of O when the max grows by more than 2^8, and write
-//               out / lse at the end.
+//               (TMEM lane a); warpgroup wg takes the lower / upper half of
+//               every step's keys.  They write the q / r rows, load S from
+//               TMEM, add the relative bias, mask edge tiles, agree on the
+//               running row max through shared memory, write P (bf16) back
+//               over S, rescale their half of O when the max grows by more
+//               than 2^8, and write out / lse (or decode partials) at the end.
 //
-// Tensor memory (512 columns): Q [0,64) bf16, S0 [64,128), S1 [128,192),
-// O [192,320), R ring [320,512) = three 64-distance chunks of r.P.
+// Tensor memory (512 columns): Q [0,64) bf16 and O [64,192) always.  During
+// the band: half-step S buffers H0 [192,256), H1 [256,320) and the R ring
+// [320,512) (three 64-distance chunks of r.P).  After the band: full-step S
+// buffers S0 [192,320), S1 [320,448).  The switch happens once per CTA: the
+// first full step's S is issued only after the last half step's P is in.
 //
-// Relative bias without a sheared tensor: the R ring holds, for every row, the
-// relative logits of three consecutive 64-distance chunks.  Key tile at
-// offset D = i_0 - j_0 needs distances D-63 .. D+127 (chunks D/64-1 .. D/64+1);
-// walking tiles away from the diagonal needs one new chunk per tile.  Each
-// thread loads a 64-column window of its own row (one load shape for the
-// whole warp) and shifts it by its lane index with a 5-stage select network,
-// which turns "distance order" into "key order" in registers.
+// Relative bias without a sheared tensor: a 64-key half step at offset
+// D = i_0 - j_0 needs distances D-63 .. D+span (span = rows' position spread),
+// i.e. at most three consecutive 64-distance chunks; walking away from the
+// diagonal needs one new chunk per half step.  Each thread loads a window of
+// its own row of R (one load shape for the whole warp) and shifts it by its
+// lane's offset with a select network, which turns "distance order" into
+// "key order" in registers.
 //
 // Every wait is bounded; a timeout sets the device error word, the CTA drains
 // its own copies / MMAs with bounded waits, frees TMEM and exits.
@@ -46,32 +56,38 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128;          // query rows per CTA
-constexpr int BN = 64;           // keys per tile
-constexpr int KV_STAGES = 4;
+constexpr int BN = kTcKeyTile;   // keys per tile / TMA stage (128)
+constexpr int HN = 64;           // keys per half step (bias band); also the r.P chunk width
+constexpr int K_STAGES = 3, V_STAGES = 2;
 constexpr int P_STAGES = 4;
 constexpr int NTHREADS = 384;
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 // TMEM columns
-constexpr uint32_t TM_Q = 0, TM_S0 = 64, TM_O = 192, TM_R = 320;
+constexpr uint32_t TM_Q = 0, TM_O = 64, TM_H = 192, TM_R = 320, TM_S = 192;
 
-// Shared memory layout (offsets from a 1024-aligned base)
-constexpr uint32_t SM_KV = 0;                                  // stages of K(16K) + V(16K)
-constexpr uint32_t KV_STAGE_BYTES = 32768;
-constexpr uint32_t SM_RT = SM_KV + KV_STAGES * KV_STAGE_BYTES;  // r tile 16K
-constexpr uint32_t SM_PS = SM_RT + 16384;                      // P slices 2 x 8K
+// Shared memory layout (offsets from a 1024-aligned base).  A K or V stage
+// holds two 16 KB boxes [64 dims x 128 keys] (128-byte rows).
+constexpr uint32_t KV_BOX_BYTES = 16384;
+constexpr uint32_t KV_STAGE_BYTES = 2 * KV_BOX_BYTES;
+constexpr uint32_t SM_K = 0;
+constexpr uint32_t SM_V = SM_K + K_STAGES * KV_STAGE_BYTES;
+constexpr uint32_t SM_RT = SM_V + V_STAGES * KV_STAGE_BYTES;    // r tile 16K
+constexpr uint32_t SM_PS = SM_RT + 16384;                      // P slices 4 x 8K
 constexpr uint32_t SM_BAR = SM_PS + P_STAGES * 8192;
-// barriers (8 bytes each)
-constexpr int B_KV_FULL = 0, B_KV_EMPTY = B_KV_FULL + KV_STAGES, B_PS_FULL = B_KV_EMPTY + KV_STAGES,
+// barriers (8 bytes each); S_FULL / P_FULL / PV_DONE: [0,1] half steps, [2,3] full steps
+constexpr int B_K_FULL = 0, B_K_EMPTY = B_K_FULL + K_STAGES, B_V_FULL = B_K_EMPTY + K_STAGES,
+              B_V_EMPTY = B_V_FULL + V_STAGES, B_PS_FULL = B_V_EMPTY + V_STAGES,
               B_PS_EMPTY = B_PS_FULL + P_STAGES, B_RT_FULL = B_PS_EMPTY + P_STAGES,
-              B_Q_READY = B_RT_FULL + 1, B_S_FULL = B_Q_READY + 1, B_P_FULL = B_S_FULL + 2,
-              B_PV_DONE = B_P_FULL + 2, B_R_FULL = B_PV_DONE + 2, B_R_FREE = B_R_FULL + 3,
+              B_Q_READY = B_RT_FULL + 1, B_S_FULL = B_Q_READY + 1, B_P_FULL = B_S_FULL + 4,
+              B_PV_DONE = B_P_FULL + 4, B_R_FULL = B_PV_DONE + 4, B_R_FREE = B_R_FULL + 3,
               B_DRAIN = B_R_FREE + 1, B_XCH = B_DRAIN + 1, B_COUNT = B_XCH + 4;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
-constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row-max exchange [2][2][128] f32
+constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row exchange [2][2][128] f32
 constexpr uint32_t SM_TOTAL = SM_XCH + 2 * 2 * 128 * 4;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct TcArgs {
   KernelArgs a;
@@ -80,11 +96,35 @@ struct TcArgs {
 
 __device__ __forceinline__ int floor_div64(int x) { return x >= 0 ? x >> 6 : -((63 - x) >> 6); }
 
+// exp2(x - m) of one step's keys for this thread: returns the sum, packs bf16 pairs
+template <int NX>
+__device__ __forceinline__ float exp_pack(const float (&x)[NX], float m_use, uint32_t (&pk)[NX / 2]) {
+  float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < NX / 2; ++i) {
+    const float e0 = fast_exp2(x[2 * i] - m_use), e1 = fast_exp2(x[2 * i + 1] - m_use);
+    rs0 += e0;
+    rs1 += e1;
+    pk[i] = pack_bf16x2(e0, e1);
+  }
+  return rs0 + rs1;
+}
+
+// row max of NX values (three-input max)
+template <int NX>
+__device__ __forceinline__ float row_max(const float (&x)[NX]) {
+  float m = fmax3(x[0], x[1], x[2]);
+#pragma unroll
+  for (int i = 3; i + 1 < NX; i += 2) m = fmax3(m, x[i], x[i + 1]);
+  if constexpr ((NX - 3) % 2 == 1) m = fmaxf(m, x[NX - 1]);
+  return m;
+}
+
 template <bool DECODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
-                              const __grid_constant__ CUtensorMap map_k,
-                              const __grid_constant__ CUtensorMap map_v) {
+                      const __grid_constant__ CUtensorMap map_k,
+                      const __grid_constant__ CUtensorMap map_v) {
   const KernelArgs &a = ta.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -96,8 +136,6 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ------------------------------------------------------------ work item
-  // prefill: one query head x 128 consecutive rows.  decode: 128 rows of the
-  // (token, head-in-group) list of one kv head, and one split of its keys.
   int b, kv_head, row0, nrows, split = 0, h_fixed = 0;
   if constexpr (DECODE) {
     split = blockIdx.x;
@@ -130,45 +168,55 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   };
   const int p0 = off + row_t(0), p_last = off + row_t(nrows - 1);
   const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
-  // distance offset D(n) = p0 - j0(n) of the key tile processed n-th (from the
-  // diagonal backwards); rows sit at p0 + delta, delta <= span
-  int ntiles, D_first, span;
+  // 128-key tiles from the diagonal backwards: tile t starts at key
+  // p0 - D(t); the rows sit at positions p0 + delta, 0 <= delta <= span
+  int ntiles, Dt0, span;
   if constexpr (DECODE) {
     const int kbase = j_lo & ~(BN - 1);
     const int kbeg = kbase + split * a.split_chunk;
     const int kend = min(p_last + 1, kbeg + a.split_chunk);
     ntiles = kend > kbeg ? (kend - kbeg + BN - 1) / BN : 0;
-    D_first = p0 - (kbeg + (ntiles - 1) * BN);
+    Dt0 = p0 - (kbeg + (ntiles - 1) * BN);
     span = p_last - p0;
   } else {
-    // key tiles start at j0(n) = p0 + 64 - 64 n  (D = 64 n - 64), or one tile
-    // later when every row of the block sits in the first 64 positions
-    D_first = (p_last >= p0 + BN) ? -BN : 0;
-    ntiles = (p0 - j_lo - D_first + BN - 1) / BN + 1;
+    Dt0 = 0;                                   // tile 0 = keys [p0, p0 + 127]
+    ntiles = (p0 - j_lo + BN - 1) / BN + 1;
     span = BM - 1;   // padding rows reuse the pattern of full tiles
   }
-  auto tile_D = [&](int n) { return D_first + BN * n; };
+  auto tile_D = [&](int t) { return Dt0 + BN * t; };
   // band tiles (some distance < E) form a prefix of the tile order
-  int nband = 0;
+  int nb_tiles = 0;
   if (ta.has_bias && ntiles > 0) {
-    const int lim = a.E + BN - 1;  // band iff D - 63 < E
-    nband = tile_D(ntiles - 1) < lim ? ntiles : max(0, (lim - D_first + BN - 1) / BN);
-    if (nband > ntiles) nband = ntiles;
+    const int lim = a.E + BN - 1;              // band iff D - 127 < E
+    nb_tiles = tile_D(ntiles - 1) < lim ? ntiles : max(0, (lim - Dt0 + BN - 1) / BN);
+    if (nb_tiles > ntiles) nb_tiles = ntiles;
   }
-  // newest 64-distance chunk of r.P a tile needs (one more per tile)
-  auto c_new = [&](int n) { return floor_div64(tile_D(n) + span); };
-  const int c_first = c_new(0);
-  const int c_last = nband > 0 ? c_new(nband - 1) : -1;
-  // first chunk computed: the oldest one tile 0 reads (a decode split far from
+  const int s2 = 2 * nb_tiles;                  // first full step
+  const int nsteps = s2 + (ntiles - nb_tiles);
+  auto step_tile = [&](int s) { return s < s2 ? s >> 1 : nb_tiles + (s - s2); };
+  auto step_kh = [&](int s) { return (s < s2 && (s & 1) == 0) ? HN : 0; };   // first key in the tile
+  auto step_D = [&](int s) { return tile_D(step_tile(s)) - step_kh(s); };
+  // barrier / buffer of a step: half steps alternate 0,1; full steps 2,3
+  auto step_kind = [&](int s) { return s < s2 ? (s & 1) : 2 + ((s - s2) & 1); };
+  auto step_phase = [&](int s) { return s < s2 ? (s >> 1) & 1 : ((s - s2) >> 1) & 1; };
+  // newest r.P chunk (64 distances) a half step needs: one more per half step
+  auto c_new = [&](int s) { return floor_div64(step_D(s) + span); };
+  const int c_first = s2 > 0 ? c_new(0) : -1;
+  const int c_last = s2 > 0 ? c_new(s2 - 1) : -1;
+  // first chunk computed: the oldest one step 0 reads (a decode split far from
   // the diagonal starts deep in the band).  Chunk c uses ring slot / P stage /
   // barrier phase counted from c_start.
-  const int c_start = nband > 0 ? max(0, floor_div64(tile_D(0) - (BN - 1))) : 0;
+  const int c_start = s2 > 0 ? max(0, floor_div64(step_D(0) - (HN - 1))) : 0;
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
-    for (int i = 0; i < KV_STAGES; ++i) {
-      mbar_init(bar(B_KV_FULL + i), 1);
-      mbar_init(bar(B_KV_EMPTY + i), 1);
+    for (int i = 0; i < K_STAGES; ++i) {
+      mbar_init(bar(B_K_FULL + i), 1);
+      mbar_init(bar(B_K_EMPTY + i), 1);
+    }
+    for (int i = 0; i < V_STAGES; ++i) {
+      mbar_init(bar(B_V_FULL + i), 1);
+      mbar_init(bar(B_V_EMPTY + i), 1);
     }
     for (int i = 0; i < P_STAGES; ++i) {
       mbar_init(bar(B_PS_FULL + i), 1);
@@ -176,12 +224,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     }
     mbar_init(bar(B_RT_FULL), 256);
     mbar_init(bar(B_Q_READY), 256);
-    mbar_init(bar(B_S_FULL + 0), 1);
-    mbar_init(bar(B_S_FULL + 1), 1);
-    mbar_init(bar(B_P_FULL + 0), 256);
-    mbar_init(bar(B_P_FULL + 1), 256);
-    mbar_init(bar(B_PV_DONE + 0), 1);
-    mbar_init(bar(B_PV_DONE + 1), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_S_FULL + i), 1);
+      mbar_init(bar(B_P_FULL + i), 256);
+      mbar_init(bar(B_PV_DONE + i), 1);
+    }
     for (int i = 0; i < 3; ++i) mbar_init(bar(B_R_FULL + i), 1);
     mbar_init(bar(B_R_FREE), 256);
     mbar_init(bar(B_DRAIN), 1);
@@ -193,37 +240,39 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     tmem_alloc(sb + SM_TMEM_SLOT, 512);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&map_k);
-    prefetch_tmap(&map_v);
-  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&map_k);
+  if (warp == 3 && lane == 0) prefetch_tmap(&map_v);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
-
-  if (warp == 0) {
-    // ======================================================== K/V producer
+  if (warp == 0 || warp == 3) {
+    // ======================================================== K / V producers
     if (lane == 0) {
+      const bool is_k = warp == 0;
+      const int nst = is_k ? K_STAGES : V_STAGES;
+      const int b_full = is_k ? B_K_FULL : B_V_FULL, b_empty = is_k ? B_K_EMPTY : B_V_EMPTY;
+      const uint32_t base = sb + (is_k ? SM_K : SM_V);
+      const CUtensorMap *map = is_k ? &map_k : &map_v;
       int issued = 0;
-      for (int n = 0; n < ntiles && !*abort_flag; ++n) {
-        const int st = n % KV_STAGES;
-        if (n >= KV_STAGES && !mbar_wait(bar(B_KV_EMPTY + st), ((n / KV_STAGES) - 1) & 1, abort_flag, 1))
-          break;
-        const int key = ck + p0 - tile_D(n);   // may be < 0: the tile reads zeros there
-        const uint32_t dst = sb + SM_KV + st * KV_STAGE_BYTES;
-        mbar_arrive_expect_tx(bar(B_KV_FULL + st), KV_STAGE_BYTES);
-        tma_load_3d(dst, &map_k, 0, kv_head, key, bar(B_KV_FULL + st));
-        tma_load_3d(dst + 8192, &map_k, 64, kv_head, key, bar(B_KV_FULL + st));
-        tma_load_3d(dst + 16384, &map_v, 0, kv_head, key, bar(B_KV_FULL + st));
-        tma_load_3d(dst + 24576, &map_v, 64, kv_head, key, bar(B_KV_FULL + st));
-        issued = n + 1;
+      for (int t = 0, st = 0, ph = 0; t < ntiles && !*abort_flag; ++t) {
+        if (t >= nst && !mbar_wait(bar(b_empty + st), ph ^ 1, abort_flag, is_k ? 1 : 4)) break;
+        const int key = ck + p0 - tile_D(t);   // may be < 0: the tile reads zeros there
+        const uint32_t dst = base + st * KV_STAGE_BYTES;
+        mbar_arrive_expect_tx(bar(b_full + st), KV_STAGE_BYTES);
+        tma_load_3d(dst, map, 0, kv_head, key, bar(b_full + st));
+        tma_load_3d(dst + KV_BOX_BYTES, map, 64, kv_head, key, bar(b_full + st));
+        issued = t + 1;
+        if (++st == nst) {
+          st = 0;
+          ph ^= 1;
+        }
       }
       if (*abort_flag) {
         // let our own copies land before the CTA goes away (bounded, not cut short by the abort)
         volatile int keep_waiting = 0;
-        for (int n = max(0, issued - KV_STAGES); n < issued; ++n)
-          mbar_wait(bar(B_KV_FULL + n % KV_STAGES), (n / KV_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+        for (int t = max(0, issued - nst); t < issued; ++t)
+          mbar_wait(bar(b_full + t % nst), (t / nst) & 1, &keep_waiting, 2, 400000000ll);
       }
     }
     __syncwarp();
@@ -232,8 +281,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     // Chunk c = P[:, 64c, 64c+64) as rd_pad rows (channels) of 128 bytes in the
     // 128-byte-swizzled layout the MMA descriptor expects; zero outside [0, E)
     // and past r_dim.  Plain 16-byte loads (P is small and L2-resident).
-    if (nband > 0) {
-      const int c_hi = min(c_last, (a.E - 1) / BN);     // chunks past E stay zero-filled
+    if (s2 > 0) {
+      const int c_hi = min(c_last, (a.E - 1) / HN);     // chunks past E stay zero-filled
       for (int c = c_start; c <= c_last; ++c) {
         const int o = c - c_start;
         const int st = o % P_STAGES;
@@ -242,22 +291,26 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           if (!__all_sync(0xffffffffu, w)) break;
         }
         uint8_t *dst = smem + SM_PS + st * 8192;
-        // up to 64 channels x 8 sixteen-byte pieces = 16 per lane: issue every
-        // load before the first store so the L2 round trips overlap
-        uint4 v[16];
+        // up to 64 channels x 8 sixteen-byte pieces = 16 per lane, in two
+        // rounds of 8: every load of a round is issued before its first store
+        // so the L2 round trips overlap
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          const int idx = lane + 32 * it, ch = idx >> 3, j = idx & 7, col = BN * c + 8 * j;
-          v[it] = make_uint4(0u, 0u, 0u, 0u);
-          if (idx < a.rd_pad * 8 && c <= c_hi && ch < a.rd && col < a.E)
-            v[it] = *reinterpret_cast<const uint4 *>(a.P + (size_t)ch * a.E + col);
-        }
+        for (int half = 0; half < 2; ++half) {
+          uint4 v[8];
 #pragma unroll
-        for (int it = 0; it < 16; ++it) {
-          const int idx = lane + 32 * it, ch = idx >> 3, j = idx & 7;
-          if (idx < a.rd_pad * 8)
-            *reinterpret_cast<uint4 *>(dst + (ch >> 3) * 1024 + (ch & 7) * 128 +
-                                       ((j ^ (ch & 7)) << 4)) = v[it];
+          for (int it = 0; it < 8; ++it) {
+            const int idx = lane + 32 * (8 * half + it), ch = idx >> 3, j = idx & 7, col = HN * c + 8 * j;
+            v[it] = make_uint4(0u, 0u, 0u, 0u);
+            if (idx < a.rd_pad * 8 && c <= c_hi && ch < a.rd && col < a.E)
+              v[it] = *reinterpret_cast<const uint4 *>(a.P + (size_t)ch * a.E + col);
+          }
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int idx = lane + 32 * (8 * half + it), ch = idx >> 3, j = idx & 7;
+            if (idx < a.rd_pad * 8)
+              *reinterpret_cast<uint4 *>(dst + (ch >> 3) * 1024 + (ch & 7) * 128 +
+                                         ((j ^ (ch & 7)) << 4)) = v[it];
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -268,13 +321,16 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   } else if (warp == 1) {
     // ======================================================== MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(BM, BN, 0, 0);       // S: Q(tmem) x K(smem, K-major)
+      const uint32_t id_h = idesc_bf16_f32(BM, HN, 0, 0);       // half S: Q(tmem) x K(smem, K-major)
+      const uint32_t id_f = idesc_bf16_f32(BM, BN, 0, 0);       // full S
       const uint32_t id_o = idesc_bf16_f32(BM, 128, 0, 1);      // O: P(tmem) x V(smem, MN-major)
-      const uint32_t id_r = idesc_bf16_f32(BM, BN, 0, 1);       // R: r(smem) x P(smem, MN-major)
+      const uint32_t id_r = idesc_bf16_f32(BM, HN, 0, 1);       // R: r(smem) x P(smem, MN-major)
       const int r_ksteps = a.rd_pad / 16;
-      // descriptor bases; per k-step / stage only the 16-byte address field moves
-      const uint64_t kd0 = smem_desc_sw128(sb + SM_KV, 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(sb + SM_KV + 16384, 8192, 1024);
+      // descriptor bases; per k-step / stage / half only the 16-byte address
+      // field moves: +2 per 32 bytes of a 128-byte row, +1024 per 16 KB box,
+      // +8 per key row, +128 per 16 V rows
+      const uint64_t kd0 = smem_desc_sw128(sb + SM_K, 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(sb + SM_V, KV_BOX_BYTES, 1024);
       const uint64_t rd0 = smem_desc_sw128(sb + SM_RT, 16, 1024);
       const uint64_t pd0 = smem_desc_sw128(sb + SM_PS, 8192, 1024);
       bool ok = mbar_wait(bar(B_Q_READY), 0, abort_flag, 6);
@@ -299,48 +355,85 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         mma_commit(bar(B_PS_EMPTY + st));
         return true;
       };
-      auto issue_s = [&](int n) -> bool {
-        const int st = n % KV_STAGES;
-        if (!mbar_wait(bar(B_KV_FULL + st), (n / KV_STAGES) & 1, abort_flag, 9)) return false;
+      auto issue_s = [&](int s) -> bool {
+        const int t = step_tile(s), st = t % K_STAGES;
+        if (!mbar_wait(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + TM_S0 + 64u * (uint32_t)(n & 1);
-        const uint64_t kd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
         const uint32_t qa = tmem + TM_Q;
-        // k-step k: box k/4 (+8 KB), 32 bytes per step inside the 128-byte row
-        mma_ts_c<0>(d, qa + 0, kd + 0, id_s);
-        mma_ts_c<1>(d, qa + 8, kd + 2, id_s);
-        mma_ts_c<1>(d, qa + 16, kd + 4, id_s);
-        mma_ts_c<1>(d, qa + 24, kd + 6, id_s);
-        mma_ts_c<1>(d, qa + 32, kd + 512, id_s);
-        mma_ts_c<1>(d, qa + 40, kd + 514, id_s);
-        mma_ts_c<1>(d, qa + 48, kd + 516, id_s);
-        mma_ts_c<1>(d, qa + 56, kd + 518, id_s);
-        mma_commit(bar(B_S_FULL + (n & 1)));
+        const uint64_t kd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
+        // k-step k: dims 16k..16k+15 -> box k/4, 32 bytes per step inside the row
+        if (s < s2) {
+          const uint32_t d = tmem + TM_H + 64u * (uint32_t)(s & 1);
+          mma_ts_c<0>(d, qa + 0, kd + 0, id_h);
+          mma_ts_c<1>(d, qa + 8, kd + 2, id_h);
+          mma_ts_c<1>(d, qa + 16, kd + 4, id_h);
+          mma_ts_c<1>(d, qa + 24, kd + 6, id_h);
+          mma_ts_c<1>(d, qa + 32, kd + 1024, id_h);
+          mma_ts_c<1>(d, qa + 40, kd + 1026, id_h);
+          mma_ts_c<1>(d, qa + 48, kd + 1028, id_h);
+          mma_ts_c<1>(d, qa + 56, kd + 1030, id_h);
+        } else {
+          const uint32_t d = tmem + TM_S + 128u * (uint32_t)((s - s2) & 1);
+          mma_ts_c<0>(d, qa + 0, kd + 0, id_f);
+          mma_ts_c<1>(d, qa + 8, kd + 2, id_f);
+          mma_ts_c<1>(d, qa + 16, kd + 4, id_f);
+          mma_ts_c<1>(d, qa + 24, kd + 6, id_f);
+          mma_ts_c<1>(d, qa + 32, kd + 1024, id_f);
+          mma_ts_c<1>(d, qa + 40, kd + 1026, id_f);
+          mma_ts_c<1>(d, qa + 48, kd + 1028, id_f);
+          mma_ts_c<1>(d, qa + 56, kd + 1030, id_f);
+        }
+        mma_commit(bar(B_S_FULL + step_kind(s)));
+        if (step_kh(s) == 0) mma_commit(bar(B_K_EMPTY + st));   // last S of its tile
         return true;
       };
-      if (ok && nband > 0)
-        for (int c = c_start; c <= c_first && ok; ++c) ok = issue_r(c);
-      if (ok && ntiles > 0) ok = issue_s(0);   // an empty decode split issues nothing
-      for (int n = 0; n < ntiles && ok; ++n) {
-        if (n + 1 < ntiles && !(ok = issue_s(n + 1))) break;
-        if (n + 1 < nband) {
-          const int c = c_new(n + 1);
-          if (!(ok = mbar_wait(bar(B_R_FREE), n & 1, abort_flag, 10))) break;
-          if (c >= 0 && !(ok = issue_r(c))) break;
-        }
-        if (!(ok = mbar_wait(bar(B_P_FULL + (n & 1)), (n >> 1) & 1, abort_flag, 11))) break;
+      // O += P V; k-step k = 16 keys = 2048 bytes of the MN-major V tile
+      auto issue_pv = [&](int s) -> bool {
+        const int t = step_tile(s), st = t % V_STAGES;
+        if (!mbar_wait(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5)) return false;
         tc_fence_after();
-        const int st = n % KV_STAGES;
-        const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
-        const uint32_t pa = tmem + TM_S0 + 64u * (uint32_t)(n & 1);
-        // k-step k = 16 keys = 2048 bytes of the MN-major V tile
-        if (n > 0) mma_ts_c<1>(tmem + TM_O, pa + 0, vd + 0, id_o);
-        else mma_ts_c<0>(tmem + TM_O, pa + 0, vd + 0, id_o);
-        mma_ts_c<1>(tmem + TM_O, pa + 8, vd + 128, id_o);
-        mma_ts_c<1>(tmem + TM_O, pa + 16, vd + 256, id_o);
-        mma_ts_c<1>(tmem + TM_O, pa + 24, vd + 384, id_o);
-        mma_commit(bar(B_PV_DONE + (n & 1)));
-        mma_commit(bar(B_KV_EMPTY + st));
+        const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
+        const uint32_t o = tmem + TM_O;
+        if (s < s2) {
+          const uint32_t pa = tmem + TM_H + 64u * (uint32_t)(s & 1);
+          if (s > 0) mma_ts_c<1>(o, pa + 0, vd + 0, id_o);
+          else mma_ts_c<0>(o, pa + 0, vd + 0, id_o);
+          mma_ts_c<1>(o, pa + 8, vd + 128, id_o);
+          mma_ts_c<1>(o, pa + 16, vd + 256, id_o);
+          mma_ts_c<1>(o, pa + 24, vd + 384, id_o);
+        } else {
+          const uint32_t pa = tmem + TM_S + 128u * (uint32_t)((s - s2) & 1);
+          if (s > 0) mma_ts_c<1>(o, pa + 0, vd + 0, id_o);
+          else mma_ts_c<0>(o, pa + 0, vd + 0, id_o);
+          mma_ts_c<1>(o, pa + 8, vd + 128, id_o);
+          mma_ts_c<1>(o, pa + 16, vd + 256, id_o);
+          mma_ts_c<1>(o, pa + 24, vd + 384, id_o);
+          mma_ts_c<1>(o, pa + 32, vd + 512, id_o);
+          mma_ts_c<1>(o, pa + 40, vd + 640, id_o);
+          mma_ts_c<1>(o, pa + 48, vd + 768, id_o);
+          mma_ts_c<1>(o, pa + 56, vd + 896, id_o);
+        }
+        mma_commit(bar(B_PV_DONE + step_kind(s)));
+        if (step_kh(s) == 0) mma_commit(bar(B_V_EMPTY + st));   // last PV of its tile
+        return true;
+      };
+      if (ok && s2 > 0)
+        for (int c = c_start; c <= c_first && ok; ++c) ok = issue_r(c);
+      if (ok && nsteps > 0) ok = issue_s(0);   // an empty decode split issues nothing
+      for (int s = 0; s < nsteps && ok; ++s) {
+        // the first full step's S buffer overlaps the half-step buffers and the
+        // R ring: it is issued only once the last half step's P is in
+        const bool switch_next = (s + 1 == s2) && (s2 < nsteps);
+        if (!switch_next && s + 1 < nsteps && !(ok = issue_s(s + 1))) break;
+        if (s + 1 < s2) {
+          const int c = c_new(s + 1);
+          if (!(ok = mbar_wait(bar(B_R_FREE), s & 1, abort_flag, 10))) break;
+          if (c >= c_start && !(ok = issue_r(c))) break;
+        }
+        if (!(ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11))) break;
+        tc_fence_after();
+        if (!(ok = issue_pv(s))) break;
+        if (switch_next && !(ok = issue_s(s + 1))) break;
       }
       // drain: every MMA issued above has finished before TMEM is released
       mma_commit(bar(B_DRAIN));
@@ -350,10 +443,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     __syncwarp();
   } else if (warp >= 4) {
     // ======================================================== softmax
-    // Two warpgroups share the 128 rows: warpgroup wg handles keys
-    // [32 wg, 32 wg + 32) of every 64-key tile (and O / output columns
-    // [64 wg, 64 wg + 64)).  The two threads of a row agree on the running max
-    // through a shared-memory exchange guarded by a per-lane-quarter mbarrier.
+    // Two warpgroups share the 128 rows: warpgroup wg handles the wg-th half of
+    // every step's keys and O / output columns [64 wg, 64 wg + 64).  The two
+    // threads of a row agree on the running max through a shared-memory
+    // exchange guarded by a per-lane-quarter mbarrier.
     const int wg = (warp - 4) >> 2;
     const int wq = warp & 3;                     // lane quarter (TMEM lanes 32 wq ..)
     const int a_row = 32 * wq + lane;            // row == TMEM lane
@@ -385,7 +478,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       mbar_arrive(bar(B_Q_READY));
     }
     // r row half -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
-    if (nband > 0) {
+    if (s2 > 0) {
       const __nv_bfloat16 *rsrc = a.r + ((size_t)(cq + t_row) * a.Hq + h_row) * a.rd;
       uint8_t *rrow = smem + SM_RT + (a_row >> 3) * 1024 + (a_row & 7) * 128;
 #pragma unroll
@@ -409,44 +502,61 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     auto r_addr = [&](int d0) {
       return tmem + lane_base + TM_R + 64u * (uint32_t)(((d0 >> 6) - c_start) % 3) + (uint32_t)(d0 & 63);
     };
-    const int d_min = BN * c_start;   // smaller distances were never computed (not needed)
+    const int d_min = HN * c_start;   // smaller distances were never computed (not needed)
+    // combine this thread's max with the other warpgroup's for the same row
+    // (buffer and barrier phase by step parity)
+    auto exchange = [&](int s, float v, bool &okx) -> float {
+      float *xb = xbuf + (s & 1) * 256;
+      xb[wg * 128 + a_row] = v;
+      mbar_arrive(bar(B_XCH + wq));
+      okx = warp_wait(bar(B_XCH + wq), s & 1, 18);
+      return xb[(1 - wg) * 128 + a_row];
+    };
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int n = 0; n < ntiles; ++n) {
-      const uint32_t sbuf = tmem + lane_base + TM_S0 + 64u * (uint32_t)(n & 1);
-      if (!(ok = warp_wait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1, 13))) break;
-      const int D = tile_D(n);
-      const int j0 = p0 - D;
-      const bool band = n < nband;
-      if (band) {
-        // the newest chunk this tile needs (older ones were awaited before)
-        if (n == 0) {
+    for (int s = 0; s < nsteps; ++s) {
+      if (!(ok = warp_wait(bar(B_S_FULL + step_kind(s)), step_phase(s), 13))) break;
+      const int D = step_D(s);
+      const int j0 = p0 - D;                     // first key of this step
+      float corr = 1.f;
+      bool rescale_o = false;
+      // running-max update shared by both step shapes
+      auto update_max = [&](float mx) {
+        if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
+          const float m_new = fmaxf(m_ref, mx);
+          corr = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
+          rescale_o = (s > 0) && (m_ref != -INFINITY);
+          l *= corr;
+          m_ref = m_new;
+        }
+      };
+      if (s < s2) {
+        // ---------------- half step: 32 keys per thread, relative bias
+        const uint32_t sbuf = tmem + lane_base + TM_H + 64u * (uint32_t)(s & 1);
+        // the newest chunk this step needs (older ones were awaited before)
+        if (s == 0) {
           for (int c = c_start; c <= c_first && ok; ++c)
             ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 14);
         } else {
-          const int c = c_new(n);
+          const int c = c_new(s);
           if (c >= c_start) ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 15);
         }
         if (!ok) break;
-      }
-      tc_fence_after();
-      uint32_t sr[32];
-      __syncwarp();
-      tmem_ld32(sbuf + 32u * wg, sr);
-      float x[32];
-      if constexpr (!DECODE) {
-        // distances D + a - (32 wg + u), u in [0, 32): window [base, base + 64),
-        // base a multiple of 32 (D is a multiple of 64 here)
-        const int base = D + 32 * wq - 32 * wg - 32;
-        uint32_t w0[32], w1[32];
-        if (band) {
+        tc_fence_after();
+        uint32_t sr[32];
+        __syncwarp();
+        tmem_ld32(sbuf + 32u * wg, sr);
+        float x[32];
+        if constexpr (!DECODE) {
+          // distances D + a - (32 wg + u), u in [0, 32): window [base, base + 64),
+          // base a multiple of 32 (D is a multiple of 64 here)
+          const int base = D + 32 * wq - 32 * wg - 32;
+          uint32_t w0[32], w1[32];
           if (base >= d_min) tmem_ld32(r_addr(base), w0);
           if (base + 32 >= d_min) tmem_ld32(r_addr(base + 32), w1);
-        }
-        tmem_wait_ld(sr);
-        reg_dep(w0);
-        reg_dep(w1);
-        if (band) {
+          tmem_wait_ld(sr);
+          reg_dep(w0);
+          reg_dep(w1);
           // z[63 - i] = window[i]; the thread of lane t needs window[32 + t - u]
           float z[64];
 #pragma unroll
@@ -473,12 +583,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
                   z[u] * cbias, z[u + 1] * cbias);
         } else {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(sr[u]) * cqk;
-        }
-      } else {
-        tmem_wait_ld(sr);
-        if (band) {
+          tmem_wait_ld(sr);
           // rows of a warp span at most 16 positions: distances
           // D + delta - (32 wg + u) lie in a 96-wide window [bal, bal + 96)
           // starting at a multiple of 32
@@ -502,7 +607,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           // y[u] = window[i0 - u] = z[95 - i0 + u] with 95 - i0 in [18, 64]
           const int i0 = D + delta - 32 * wg - bal;
           const int sh = 95 - i0 - 18;
-          float* zz = z + 18;   // 78 entries
+          float *zz = z + 18;   // 78 entries
 #pragma unroll
           for (int i = 0; i < 46; ++i) zz[i] = (sh & 32) ? zz[i + 32] : zz[i];
 #pragma unroll
@@ -519,64 +624,68 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           for (int u = 0; u < 32; u += 2)
             ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
                   zz[u] * cbias, zz[u + 1] * cbias);
-        } else {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) x[u] = __uint_as_float(sr[u]) * cqk;
         }
-      }
-      const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
-      (void)delta;
-      if (need_mask) {
+        const bool need_mask = (j0 + HN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+        if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int j = j0 + 32 * wg + i;
-          const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
-          x[i] = vis ? x[i] : -INFINITY;
+          for (int i = 0; i < 32; ++i) {
+            const int j = j0 + 32 * wg + i;
+            const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
+            x[i] = vis ? x[i] : -INFINITY;
+          }
         }
-      }
-      float mloc = fmax3(x[0], x[1], x[2]);
-#pragma unroll
-      for (int i = 3; i < 31; i += 2) mloc = fmax3(mloc, x[i], x[i + 1]);
-      mloc = fmaxf(mloc, x[31]);
-      // agree on the row max with the other warpgroup
-      float *xb = xbuf + (n & 1) * 256;
-      xb[wg * 128 + a_row] = mloc;
-      mbar_arrive(bar(B_XCH + wq));
-      if (!(ok = warp_wait(bar(B_XCH + wq), n & 1, 18))) break;
-      const float mx = fmaxf(mloc, xb[(1 - wg) * 128 + a_row]);
-      float corr = 1.f;
-      bool rescale_o = false;
-      if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
-        const float m_new = fmaxf(m_ref, mx);
-        corr = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
-        rescale_o = (n > 0) && (m_ref != -INFINITY);
-        l *= corr;
-        m_ref = m_new;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      {
+        const float mloc = row_max(x);
+        const float mo = exchange(s, mloc, ok);
+        if (!ok) break;
+        update_max(fmaxf(mloc, mo));
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[16];
-        float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float e0 = fast_exp2(x[2 * i] - m_use), e1 = fast_exp2(x[2 * i + 1] - m_use);
-          rs0 += e0;
-          rs1 += e1;
-          pk[i] = pack_bf16x2(e0, e1);
-        }
-        l += rs0 + rs1;
+        l += exp_pack(x, m_use, pk);
         __syncwarp();
         tmem_st16(sbuf + 16u * wg, pk);   // P (bf16 pairs) over S columns [16 wg, 16 wg + 16)
+      } else {
+        // ---------------- full step: 64 keys per thread, no bias
+        const uint32_t sbuf = tmem + lane_base + TM_S + 128u * (uint32_t)((s - s2) & 1);
+        tc_fence_after();
+        uint32_t sr0[32], sr1[32];
+        __syncwarp();
+        tmem_ld32(sbuf + 64u * wg, sr0);
+        tmem_ld32(sbuf + 64u * wg + 32u, sr1);
+        tmem_wait_ld(sr0);
+        reg_dep(sr1);
+        float x[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(sr0[i]) * cqk;
+          x[32 + i] = __uint_as_float(sr1[i]) * cqk;
+        }
+        const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const int j = j0 + 64 * wg + i;
+            const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
+            x[i] = vis ? x[i] : -INFINITY;
+          }
+        }
+        const float mloc = row_max(x);
+        const float mo = exchange(s, mloc, ok);
+        if (!ok) break;
+        update_max(fmaxf(mloc, mo));
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        uint32_t pk[32];
+        l += exp_pack(x, m_use, pk);
+        __syncwarp();
+        tmem_st32(sbuf + 32u * wg, pk);   // P (bf16 pairs) over S columns [32 wg, 32 wg + 32)
       }
-      // O is only touched when some row of this warp needs a rescale; then PV(n-1)
-      // must have landed first.  Otherwise PV(n) simply queues behind PV(n-1)
-      // on the tensor core.  (PV completions alternate between two barriers by
-      // tile parity; S(n) landing implies PV(n-2) did, so each wait is for the
-      // next phase of its barrier and never ambiguous.)
+      // O is only touched when some row of this warp needs a rescale; then
+      // PV(s-1) must have landed first.  Otherwise PV(s) simply queues behind
+      // PV(s-1) on the tensor core.  (S(s) landing implies PV(s-2) did, so the
+      // wait is for the next phase of its barrier and never ambiguous.)
       // TMEM loads / stores are warp-collective: the whole warp rescales its 32
       // rows when any of them needs it (rows that do not are scaled by 1)
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (!(ok = warp_wait(bar(B_PV_DONE + ((n - 1) & 1)), ((n - 1) >> 1) & 1, 16))) break;
+        if (!(ok = warp_wait(bar(B_PV_DONE + step_kind(s - 1)), step_phase(s - 1), 16))) break;
         tc_fence_after();
         const float cf = rescale_o ? corr : 1.f;
 #pragma unroll
@@ -594,20 +703,16 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_P_FULL + (n & 1)));
+      mbar_arrive(bar(B_P_FULL + step_kind(s)));
     }
+    (void)delta;
     // ---- epilogue
-    if (ok && ntiles > 0)
-      ok = warp_wait(bar(B_PV_DONE + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1, 17);
+    if (ok && nsteps > 0)
+      ok = warp_wait(bar(B_PV_DONE + step_kind(nsteps - 1)), step_phase(nsteps - 1), 17);
+    float l_other = 0.f;
+    if (ok) l_other = exchange(nsteps, l, ok);   // total row sum over both key halves
     if (ok) {
-      // total row sum over both key halves
-      float *xb = xbuf + (ntiles & 1) * 256;
-      xb[wg * 128 + a_row] = l;
-      mbar_arrive(bar(B_XCH + wq));
-      ok = warp_wait(bar(B_XCH + wq), ntiles & 1, 19);
-    }
-    if (ok) {
-      const float lt = l + xbuf[(ntiles & 1) * 256 + (1 - wg) * 128 + a_row];
+      const float lt = l + l_other;
       tc_fence_after();
       const bool valid = a_row < nrows;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -618,7 +723,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        if (ntiles > 0) {
+        if (nsteps > 0) {
           __syncwarp();
           tmem_ld32(tmem + lane_base + TM_O + 64u * wg + 32u * c, r);
           tmem_wait_ld(r);

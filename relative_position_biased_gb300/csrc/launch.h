@@ -17,7 +17,9 @@ size_t decode_mma_smem_bytes(int warps, int rd_pad);
 cudaError_t launch_prefill_mma(const KernelArgs &a, cudaStream_t stream);
 
 // tcgen05 / TMA kernels: need 16-byte aligned q/k/v/out (and r/P), r_dim % 8 == 0,
-// rel_extent % 8 == 0, r_dim <= 64 and at least one 64-key tile of K/V.
+// rel_extent % 8 == 0, r_dim <= 64 and at least one 128-key tile of K/V.
+// Their key tiles (and decode split chunks) are kTcKeyTile keys.
+constexpr int kTcKeyTile = 128;
 bool tc_supported(const KernelArgs &a, int total_k);
 cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream);
 // decode on the same kernel: 128 rows of (token, head-in-group) per CTA; grid

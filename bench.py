@@ -12,7 +12,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
 `value` is the prefill throughput (TFLOP/s, algorithmic flops over the
 prefill kernel time); the decode HBM throughput (GB/s of visible K/V over the
 decode call time) is reported beside it.  L2 is flushed by a 256 MiB write
-before every timed kernel; the flush is outside the timed events.
+before every timed kernel; the flush is outside the timed events.  Before the
+flush the stream is held busy for about half a millisecond, so the host has
+queued the timed call (argument marshalling, tensor-map encoding, launch)
+before the device reaches it: the device-timed window holds device work only.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
@@ -54,6 +57,7 @@ KERNEL_SOURCES = {
                "relative_position_biased_gb300/csrc/combine.cu"],
 }
 L2_FLUSH_BYTES = 256 << 20
+HOLD_CYCLES = 1_000_000   # device-side hold before each timed call (~0.5 ms)
 
 
 def src_sha(kind: str) -> str:
@@ -226,6 +230,7 @@ def timed_steps(phases, steps, flush):
     events = []
     for _ in range(steps):
         for p in phases:
+            torch.cuda._sleep(HOLD_CYCLES)
             flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)

@@ -132,18 +132,23 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
     if (w < max_vis) max_vis = w;
   }
   if (max_vis < 1) max_vis = 1;
-  const long units = (long)p->batch * p->num_heads_kv * plan->row_blocks;
-  long splits = p->num_splits;
-  if (splits <= 0) {
-    const long target = 2L * sms;                       // about two waves of CTAs
-    splits = (target + units - 1) / units;
-    const long cap = (max_vis + 255) / 256;             // at least 256 keys per split
-    if (splits > cap) splits = cap;
-    if (splits < 1) splits = 1;
+  long chunk;
+  if (p->num_splits > 0) {
+    chunk = (max_vis + p->num_splits - 1) / p->num_splits;
+  } else {
+    // keys all CTAs visit together (each sequence sees at most max_vis of its
+    // keys), cut into about two waves of CTAs; splits past a short sequence's
+    // keys exit at once, so variable lengths still spread evenly
+    long seq_keys = (long)p->total_k;
+    if ((long)p->batch * max_vis < seq_keys) seq_keys = (long)p->batch * max_vis;
+    const long work = seq_keys * p->num_heads_kv * plan->row_blocks;
+    const long target = 2L * sms;
+    chunk = (work + target - 1) / target;
+    if (chunk < 256) chunk = 256;                       // at least 256 keys per split
   }
-  long chunk = (max_vis + splits - 1) / splits;
   chunk = (chunk + tile - 1) / tile * tile;
-  splits = (max_vis + chunk - 1) / chunk;
+  if (chunk > (max_vis + tile - 1) / tile * tile) chunk = (max_vis + tile - 1) / tile * tile;
+  long splits = (max_vis + chunk - 1) / chunk;
   if (splits > 65535) return RELATTN_ERR_UNSUPPORTED;
   plan->splits = (int)splits;
   plan->chunk = (int)chunk;

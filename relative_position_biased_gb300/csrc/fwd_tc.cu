@@ -96,28 +96,81 @@ struct TcArgs {
 
 __device__ __forceinline__ int floor_div64(int x) { return x >= 0 ? x >> 6 : -((63 - x) >> 6); }
 
-// exp2(x - m) of one step's keys for this thread: returns the sum, packs bf16 pairs
+// 2^y0, 2^y1 on the FMA pipe (relieves the MUFU unit): y = n + f with
+// n = rint(y) taken from the low mantissa bits of y + 1.5 * 2^23, f in
+// [-1/2, 1/2]; 2^f by a cubic fitted here for least maximum relative error on
+// that interval (7.5e-5, below the bf16 rounding of P), then n is added into
+// the exponent field.  y is clamped at -125 so the result stays a normal
+// number: masked lanes (y = -inf) give 2^-125 where the MUFU path gives 0.
+__device__ __forceinline__ void exp2_poly2(float y0, float y1, float &e0, float &e1) {
+  constexpr float kRound = 12582912.f;   // 1.5 * 2^23
+  y0 = fmaxf(y0, -125.f);
+  y1 = fmaxf(y1, -125.f);
+  float t0, t1, n0, n1, f0, f1, p0, p1;
+  ffma2(t0, t1, y0, y1, 1.f, 1.f, kRound, kRound);
+  ffma2(n0, n1, t0, t1, 1.f, 1.f, -kRound, -kRound);
+  ffma2(f0, f1, n0, n1, -1.f, -1.f, y0, y1);
+  ffma2(p0, p1, f0, f1, 0.05517605f, 0.05517605f, 0.24261150f, 0.24261150f);
+  ffma2(p0, p1, p0, p1, f0, f1, 0.69326019f, 0.69326019f);
+  ffma2(p0, p1, p0, p1, f0, f1, 0.99992806f, 0.99992806f);
+  e0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  e1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+}
+
+// P of one step's keys for this thread: e = 2^(x c - m) (x raw scores, c > 0),
+// packed to bf16 pairs; returns the sum.  Every fourth pair goes through the
+// FMA-pipe exponential, the rest through MUFU ex2.
+template <int NX>
+__device__ __forceinline__ float exp_pack_raw(const float (&x)[NX], float c, float m_use,
+                                              uint32_t (&pk)[NX / 2]) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < NX / 2; ++i) {
+    float y0, y1, e0, e1;
+    ffma2(y0, y1, x[2 * i], x[2 * i + 1], c, c, -m_use, -m_use);
+    if ((i & 3) == 3) {
+      exp2_poly2(y0, y1, e0, e1);
+    } else {
+      e0 = fast_exp2(y0);
+      e1 = fast_exp2(y1);
+    }
+    acc[i & 3] += e0 + e1;
+    pk[i] = pack_bf16x2(e0, e1);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// P of one step's keys from already scaled logits: e = 2^(x - m)
 template <int NX>
 __device__ __forceinline__ float exp_pack(const float (&x)[NX], float m_use, uint32_t (&pk)[NX / 2]) {
-  float rs0 = 0.f, rs1 = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < NX / 2; ++i) {
     const float e0 = fast_exp2(x[2 * i] - m_use), e1 = fast_exp2(x[2 * i + 1] - m_use);
-    rs0 += e0;
-    rs1 += e1;
+    acc[i & 3] += e0 + e1;
     pk[i] = pack_bf16x2(e0, e1);
   }
-  return rs0 + rs1;
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-// row max of NX values (three-input max)
-template <int NX>
-__device__ __forceinline__ float row_max(const float (&x)[NX]) {
-  float m = fmax3(x[0], x[1], x[2]);
+// max of N values as a tree of three-input maxima (short dependency chains)
+template <int N>
+__device__ __forceinline__ float row_max(const float (&x)[N]) {
+  if constexpr (N == 1) {
+    return x[0];
+  } else if constexpr (N == 2) {
+    return fmaxf(x[0], x[1]);
+  } else {
+    constexpr int M = (N + 2) / 3;
+    float t[M];
 #pragma unroll
-  for (int i = 3; i + 1 < NX; i += 2) m = fmax3(m, x[i], x[i + 1]);
-  if constexpr ((NX - 3) % 2 == 1) m = fmaxf(m, x[NX - 1]);
-  return m;
+    for (int k = 0; k < M; ++k) {
+      if (3 * k + 2 < N) t[k] = fmax3(x[3 * k], x[3 * k + 1], x[3 * k + 2]);
+      else if (3 * k + 1 < N) t[k] = fmaxf(x[3 * k], x[3 * k + 1]);
+      else t[k] = x[3 * k];
+    }
+    return row_max(t);
+  }
 }
 
 template <bool DECODE>
@@ -458,7 +511,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     const int delta = pos - p0;                  // 0 .. span
     const int delta_w = DECODE ? off + row_t(32 * wq) - p0 : 32 * wq;   // first row of the warp
     const float sc = log_scale(min(pos, p_last), a.inv_ln_base);
-    const float cqk = a.alpha_log2e * sc, cbias = kLog2e * sc;
+    // scores are scaled by cqk > 0: a negative alpha flips the sign of q
+    // instead (exact in bf16), so a row max of raw scores is a max of logits
+    const bool q_neg = a.alpha_log2e < 0.f;
+    const float cqk = fmaxf(fabsf(a.alpha_log2e) * sc, 1e-30f), cbias = kLog2e * sc;
     float *xbuf = reinterpret_cast<float *>(smem + SM_XCH);   // [2 parity][2 wg][128]
 
     // q row half -> TMEM columns [32 wg, 32 wg + 32) (bf16 pairs)
@@ -470,6 +526,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       for (int i = 0; i < 8; ++i) {
         const uint4 v = src[i];
         r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+      }
+      if (q_neg) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] ^= 0x80008000u;
       }
       __syncwarp();
       tmem_st32(tmem + lane_base + TM_Q + 32u * wg, r);
@@ -653,11 +713,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         tmem_ld32(sbuf + 64u * wg + 32u, sr1);
         tmem_wait_ld(sr0);
         reg_dep(sr1);
-        float x[64];
+        float x[64];   // raw scores; the scale is applied inside the exponent
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(sr0[i]) * cqk;
-          x[32 + i] = __uint_as_float(sr1[i]) * cqk;
+          x[i] = __uint_as_float(sr0[i]);
+          x[32 + i] = __uint_as_float(sr1[i]);
         }
         const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
         if (need_mask) {
@@ -668,13 +728,13 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             x[i] = vis ? x[i] : -INFINITY;
           }
         }
-        const float mloc = row_max(x);
+        const float mloc = row_max(x) * cqk;
         const float mo = exchange(s, mloc, ok);
         if (!ok) break;
         update_max(fmaxf(mloc, mo));
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[32];
-        l += exp_pack(x, m_use, pk);
+        l += exp_pack_raw(x, cqk, m_use, pk);
         __syncwarp();
         tmem_st32(sbuf + 32u * wg, pk);   // P (bf16 pairs) over S columns [32 wg, 32 wg + 32)
       }

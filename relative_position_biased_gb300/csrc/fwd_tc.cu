@@ -12,15 +12,18 @@
 // head-in-group) list of one kv head and one split of its keys.  Keys come in
 // 128-key tiles (one TMA stage), visited from the diagonal backwards.  Tiles
 // inside the relative-bias band are processed as two 64-key half steps (the
-// upper half first); the rest as one 128-key step.  Warp roles:
-//   warp 0      TMA producer for K tiles (3-stage ring of 128 keys)
-//   warp 3      TMA producer for V tiles (2-stage ring); K and V stages are
-//               freed separately (K once its S MMAs are done, V after PV)
-//   warp 1      MMA issuer (one thread):  S = Q K^T (Q in TMEM),
-//               R_chunk = r P[:, 64c..64c+64) (both operands from shared
-//               memory), O += P V (P in TMEM)
-//   warp 2      TMEM allocator; producer of the P slices (plain loads into
-//               the 128-byte-swizzled layout)
+// upper half first); the rest as one 128-key step.  Warp roles (12 warps,
+// one support and two softmax warps per SM sub-partition; the support warps
+// hand registers to the softmax warps: 64 vs 216 per thread):
+//   warp 0      TMA producer (one thread) of K tiles (2-stage ring of 128
+//               keys), V tiles (3-stage ring) and P slices P[:, 64c..64c+64)
+//               (4 stages), in the order the MMA issuer consumes them; K and
+//               V stages are freed separately (K once its S MMAs are done, V
+//               after PV)
+//   warp 1      TMEM allocator; MMA issuer (one thread):  S = Q K^T (Q in
+//               TMEM), R_chunk = r P_slice (both operands from shared memory),
+//               O += P V (P in TMEM)
+//   warps 2-3   idle
 //   warps 4-11  softmax, two warpgroups: row a is owned by one thread of each
 //               (TMEM lane a); warpgroup wg takes the lower / upper half of
 //               every step's keys.  They write the q / r rows, load S from
@@ -31,9 +34,12 @@
 //
 // Tensor memory (512 columns): Q [0,64) bf16 and O [64,192) always.  During
 // the band: half-step S buffers H0 [192,256), H1 [256,320) and the R ring
-// [320,512) (three 64-distance chunks of r.P).  After the band: full-step S
-// buffers S0 [192,320), S1 [320,448).  The switch happens once per CTA: the
-// first full step's S is issued only after the last half step's P is in.
+// [320,512) (three 64-distance chunks of r.P); a half step's P (bf16) is
+// written over its S.  After the band: full-step S buffers S0 [192,320),
+// S1 [320,448) and one P buffer [448,512), so an S buffer is free as soon as
+// the softmax has read it and S(s+2) is computed while step s is in the
+// softmax.  The switch happens once per CTA: the first full steps' S are
+// issued only after the last half step's P is in.
 //
 // Relative bias without a sheared tensor: a 64-key half step at offset
 // D = i_0 - j_0 needs distances D-63 .. D+span (span = rows' position spread),
@@ -58,13 +64,17 @@ using namespace tc;
 constexpr int BM = 128;          // query rows per CTA
 constexpr int BN = kTcKeyTile;   // keys per tile / TMA stage (128)
 constexpr int HN = 64;           // keys per half step (bias band); also the r.P chunk width
-constexpr int K_STAGES = 3, V_STAGES = 2;
+constexpr int K_STAGES = 2, V_STAGES = 3;
 constexpr int P_STAGES = 4;
 constexpr int NTHREADS = 384;
+// registers per thread: 168 at launch; the support warpgroup drops to 64 and
+// the two softmax warpgroups rise to 216 (4 x 32 x 64 + 8 x 32 x 216 <= 384 x 168)
+constexpr uint32_t kRegsSupport = 64, kRegsSoftmax = 216;
+static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= NTHREADS * 168, "register split");
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 // TMEM columns
-constexpr uint32_t TM_Q = 0, TM_O = 64, TM_H = 192, TM_R = 320, TM_S = 192;
+constexpr uint32_t TM_Q = 0, TM_O = 64, TM_H = 192, TM_R = 320, TM_S = 192, TM_P = 448;
 
 // Shared memory layout (offsets from a 1024-aligned base).  A K or V stage
 // holds two 16 KB boxes [64 dims x 128 keys] (128-byte rows).
@@ -75,13 +85,18 @@ constexpr uint32_t SM_V = SM_K + K_STAGES * KV_STAGE_BYTES;
 constexpr uint32_t SM_RT = SM_V + V_STAGES * KV_STAGE_BYTES;    // r tile 16K
 constexpr uint32_t SM_PS = SM_RT + 16384;                      // P slices 4 x 8K
 constexpr uint32_t SM_BAR = SM_PS + P_STAGES * 8192;
-// barriers (8 bytes each); S_FULL / P_FULL / PV_DONE: [0,1] half steps, [2,3] full steps
+// barriers (8 bytes each); S_FULL: [0,1] half steps, [2,3] full steps;
+// P_FULL: [0,1] half steps; full steps: S_READ, and per warpgroup w P_HALF
+// [2w, 2w+1] and PV_F [2w, 2w+1] by step parity.  PV_SW / PV_TAIL are
+// committed once each (see the MMA issuer).
 constexpr int B_K_FULL = 0, B_K_EMPTY = B_K_FULL + K_STAGES, B_V_FULL = B_K_EMPTY + K_STAGES,
               B_V_EMPTY = B_V_FULL + V_STAGES, B_PS_FULL = B_V_EMPTY + V_STAGES,
               B_PS_EMPTY = B_PS_FULL + P_STAGES, B_RT_FULL = B_PS_EMPTY + P_STAGES,
               B_Q_READY = B_RT_FULL + 1, B_S_FULL = B_Q_READY + 1, B_P_FULL = B_S_FULL + 4,
-              B_PV_DONE = B_P_FULL + 4, B_R_FULL = B_PV_DONE + 4, B_R_FREE = B_R_FULL + 3,
-              B_DRAIN = B_R_FREE + 1, B_XCH = B_DRAIN + 1, B_COUNT = B_XCH + 4;
+              B_PV_SW = B_P_FULL + 4, B_PV_TAIL = B_PV_SW + 1, B_R_FULL = B_PV_TAIL + 2,
+              B_R_FREE = B_R_FULL + 3, B_S_READ = B_R_FREE + 1, B_PV_F = B_S_READ + 2,
+              B_P_HALF = B_PV_F + 4,
+              B_DRAIN = B_P_HALF + 4, B_XCH = B_DRAIN + 1, B_COUNT = B_XCH + 4;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
 constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row exchange [2][2][128] f32
@@ -96,30 +111,9 @@ struct TcArgs {
 
 __device__ __forceinline__ int floor_div64(int x) { return x >= 0 ? x >> 6 : -((63 - x) >> 6); }
 
-// 2^y0, 2^y1 on the FMA pipe (relieves the MUFU unit): y = n + f with
-// n = rint(y) taken from the low mantissa bits of y + 1.5 * 2^23, f in
-// [-1/2, 1/2]; 2^f by a cubic fitted here for least maximum relative error on
-// that interval (7.5e-5, below the bf16 rounding of P), then n is added into
-// the exponent field.  y is clamped at -125 so the result stays a normal
-// number: masked lanes (y = -inf) give 2^-125 where the MUFU path gives 0.
-__device__ __forceinline__ void exp2_poly2(float y0, float y1, float &e0, float &e1) {
-  constexpr float kRound = 12582912.f;   // 1.5 * 2^23
-  y0 = fmaxf(y0, -125.f);
-  y1 = fmaxf(y1, -125.f);
-  float t0, t1, n0, n1, f0, f1, p0, p1;
-  ffma2(t0, t1, y0, y1, 1.f, 1.f, kRound, kRound);
-  ffma2(n0, n1, t0, t1, 1.f, 1.f, -kRound, -kRound);
-  ffma2(f0, f1, n0, n1, -1.f, -1.f, y0, y1);
-  ffma2(p0, p1, f0, f1, 0.05517605f, 0.05517605f, 0.24261150f, 0.24261150f);
-  ffma2(p0, p1, p0, p1, f0, f1, 0.69326019f, 0.69326019f);
-  ffma2(p0, p1, p0, p1, f0, f1, 0.99992806f, 0.99992806f);
-  e0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  e1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
-}
-
 // P of one step's keys for this thread: e = 2^(x c - m) (x raw scores, c > 0),
-// packed to bf16 pairs; returns the sum.  Every fourth pair goes through the
-// FMA-pipe exponential, the rest through MUFU ex2.
+// packed to bf16 pairs; returns the sum.  All exponentials go to MUFU: the FMA
+// pipe is what the MMA-issuing warp competes for on its sub-partition.
 template <int NX>
 __device__ __forceinline__ float exp_pack_raw(const float (&x)[NX], float c, float m_use,
                                               uint32_t (&pk)[NX / 2]) {
@@ -128,13 +122,9 @@ __device__ __forceinline__ float exp_pack_raw(const float (&x)[NX], float c, flo
   for (int i = 0; i < NX / 2; ++i) {
     float y0, y1, e0, e1;
     ffma2(y0, y1, x[2 * i], x[2 * i + 1], c, c, -m_use, -m_use);
-    if ((i & 3) == 3) {
-      exp2_poly2(y0, y1, e0, e1);
-    } else {
-      e0 = fast_exp2(y0);
-      e1 = fast_exp2(y1);
-    }
-    acc[i & 3] += e0 + e1;
+    e0 = fast_exp2(y0);
+    e1 = fast_exp2(y1);
+    ffma2(acc[2 * (i & 1)], acc[2 * (i & 1) + 1], e0, e1, 1.f, 1.f, acc[2 * (i & 1)], acc[2 * (i & 1) + 1]);
     pk[i] = pack_bf16x2(e0, e1);
   }
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -177,7 +167,8 @@ template <bool DECODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
                       const __grid_constant__ CUtensorMap map_k,
-                      const __grid_constant__ CUtensorMap map_v) {
+                      const __grid_constant__ CUtensorMap map_v,
+                      const __grid_constant__ CUtensorMap map_p) {
   const KernelArgs &a = ta.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -280,7 +271,14 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(B_S_FULL + i), 1);
       mbar_init(bar(B_P_FULL + i), 256);
-      mbar_init(bar(B_PV_DONE + i), 1);
+    }
+    mbar_init(bar(B_PV_SW), 1);
+    mbar_init(bar(B_PV_TAIL), 1);
+    mbar_init(bar(B_PV_TAIL + 1), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bar(B_S_READ + i), 256);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(B_PV_F + i), 1);
+      mbar_init(bar(B_P_HALF + i), 128);
     }
     for (int i = 0; i < 3; ++i) mbar_init(bar(B_R_FULL + i), 1);
     mbar_init(bar(B_R_FREE), 256);
@@ -289,85 +287,75 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(sb + SM_TMEM_SLOT, 512);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&map_k);
-  if (warp == 3 && lane == 0) prefetch_tmap(&map_v);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+    if (ta.has_bias) prefetch_tmap(&map_p);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
-  if (warp == 0 || warp == 3) {
-    // ======================================================== K / V producers
+  if (warp < 4) {
+  regs_dec<kRegsSupport>();
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    // Per tile t: the P slices its half steps need (band tiles), then K(t),
+    // then V(t) -- the order the MMA issuer consumes them, so a wait here only
+    // ever depends on work issued before it.  A P slice is P[0:r_dim, 64c ..
+    // 64c + 64) in the 128-byte-swizzled layout (columns past E read as 0;
+    // rows r_dim .. rd_pad stay at the zeros the softmax warps put there).
     if (lane == 0) {
-      const bool is_k = warp == 0;
-      const int nst = is_k ? K_STAGES : V_STAGES;
-      const int b_full = is_k ? B_K_FULL : B_V_FULL, b_empty = is_k ? B_K_EMPTY : B_V_EMPTY;
-      const uint32_t base = sb + (is_k ? SM_K : SM_V);
-      const CUtensorMap *map = is_k ? &map_k : &map_v;
-      int issued = 0;
-      for (int t = 0, st = 0, ph = 0; t < ntiles && !*abort_flag; ++t) {
-        if (t >= nst && !mbar_wait(bar(b_empty + st), ph ^ 1, abort_flag, is_k ? 1 : 4)) break;
+      const uint32_t p_bytes = 128u * (uint32_t)a.rd;
+      int kst = 0, kph = 0, vst = 0, vph = 0;
+      int issued_k = 0, issued_v = 0, c_next = c_start;
+      bool run = true;
+      for (int t = 0; t < ntiles && run && !*abort_flag; ++t) {
+        if (t < nb_tiles) {
+          const int c_need = c_new(2 * t + 1);   // newest chunk of the tile's second half step
+          for (; c_next <= c_need; ++c_next) {
+            const int o = c_next - c_start, st = o % P_STAGES;
+            if (o >= P_STAGES && !(run = mbar_wait(bar(B_PS_EMPTY + st), ((o / P_STAGES) - 1) & 1, abort_flag, 3)))
+              break;
+            mbar_arrive_expect_tx(bar(B_PS_FULL + st), p_bytes);
+            tma_load_2d(sb + SM_PS + st * 8192, &map_p, HN * c_next, 0, bar(B_PS_FULL + st));
+          }
+          if (!run) break;
+        }
         const int key = ck + p0 - tile_D(t);   // may be < 0: the tile reads zeros there
-        const uint32_t dst = base + st * KV_STAGE_BYTES;
-        mbar_arrive_expect_tx(bar(b_full + st), KV_STAGE_BYTES);
-        tma_load_3d(dst, map, 0, kv_head, key, bar(b_full + st));
-        tma_load_3d(dst + KV_BOX_BYTES, map, 64, kv_head, key, bar(b_full + st));
-        issued = t + 1;
-        if (++st == nst) {
-          st = 0;
-          ph ^= 1;
+        if (t >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
+        {
+          const uint32_t dst = sb + SM_K + kst * KV_STAGE_BYTES;
+          mbar_arrive_expect_tx(bar(B_K_FULL + kst), KV_STAGE_BYTES);
+          tma_load_3d(dst, &map_k, 0, kv_head, key, bar(B_K_FULL + kst));
+          tma_load_3d(dst + KV_BOX_BYTES, &map_k, 64, kv_head, key, bar(B_K_FULL + kst));
+          issued_k = t + 1;
+          if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
+        }
+        if (t >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
+        {
+          const uint32_t dst = sb + SM_V + vst * KV_STAGE_BYTES;
+          mbar_arrive_expect_tx(bar(B_V_FULL + vst), KV_STAGE_BYTES);
+          tma_load_3d(dst, &map_v, 0, kv_head, key, bar(B_V_FULL + vst));
+          tma_load_3d(dst + KV_BOX_BYTES, &map_v, 64, kv_head, key, bar(B_V_FULL + vst));
+          issued_v = t + 1;
+          if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
         }
       }
       if (*abort_flag) {
         // let our own copies land before the CTA goes away (bounded, not cut short by the abort)
         volatile int keep_waiting = 0;
-        for (int t = max(0, issued - nst); t < issued; ++t)
-          mbar_wait(bar(b_full + t % nst), (t / nst) & 1, &keep_waiting, 2, 400000000ll);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ======================================================== P-slice producer
-    // Chunk c = P[:, 64c, 64c+64) as rd_pad rows (channels) of 128 bytes in the
-    // 128-byte-swizzled layout the MMA descriptor expects; zero outside [0, E)
-    // and past r_dim.  Plain 16-byte loads (P is small and L2-resident).
-    if (s2 > 0) {
-      const int c_hi = min(c_last, (a.E - 1) / HN);     // chunks past E stay zero-filled
-      for (int c = c_start; c <= c_last; ++c) {
-        const int o = c - c_start;
-        const int st = o % P_STAGES;
-        if (o >= P_STAGES) {
-          const bool w = mbar_wait(bar(B_PS_EMPTY + st), ((o / P_STAGES) - 1) & 1, abort_flag, 3);
-          if (!__all_sync(0xffffffffu, w)) break;
-        }
-        uint8_t *dst = smem + SM_PS + st * 8192;
-        // up to 64 channels x 8 sixteen-byte pieces = 16 per lane, in two
-        // rounds of 8: every load of a round is issued before its first store
-        // so the L2 round trips overlap
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4 v[8];
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int idx = lane + 32 * (8 * half + it), ch = idx >> 3, j = idx & 7, col = HN * c + 8 * j;
-            v[it] = make_uint4(0u, 0u, 0u, 0u);
-            if (idx < a.rd_pad * 8 && c <= c_hi && ch < a.rd && col < a.E)
-              v[it] = *reinterpret_cast<const uint4 *>(a.P + (size_t)ch * a.E + col);
-          }
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int idx = lane + 32 * (8 * half + it), ch = idx >> 3, j = idx & 7;
-            if (idx < a.rd_pad * 8)
-              *reinterpret_cast<uint4 *>(dst + (ch >> 3) * 1024 + (ch & 7) * 128 +
-                                         ((j ^ (ch & 7)) << 4)) = v[it];
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PS_FULL + st));
+        for (int t = max(0, issued_k - K_STAGES); t < issued_k; ++t)
+          mbar_wait(bar(B_K_FULL + t % K_STAGES), (t / K_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+        for (int t = max(0, issued_v - V_STAGES); t < issued_v; ++t)
+          mbar_wait(bar(B_V_FULL + t % V_STAGES), (t / V_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+        const int issued_p = c_next - c_start;
+        for (int o = max(0, issued_p - P_STAGES); o < issued_p; ++o)
+          mbar_wait(bar(B_PS_FULL + o % P_STAGES), (o / P_STAGES) & 1, &keep_waiting, 2, 400000000ll);
       }
     }
     __syncwarp();
@@ -404,8 +392,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         if (r_ksteps > 1) mma_ss_c<1>(d, rd0 + 2, pd + 128, id_r);
         if (r_ksteps > 2) mma_ss_c<1>(d, rd0 + 4, pd + 256, id_r);
         if (r_ksteps > 3) mma_ss_c<1>(d, rd0 + 6, pd + 384, id_r);
-        mma_commit(bar(B_R_FULL + o % 3));
-        mma_commit(bar(B_PS_EMPTY + st));
+        mma_commit(bar(B_R_FULL + o % 3));   // its landing also frees P stage st (softmax arrives)
         return true;
       };
       auto issue_s = [&](int s) -> bool {
@@ -436,8 +423,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           mma_ts_c<1>(d, qa + 48, kd + 1028, id_f);
           mma_ts_c<1>(d, qa + 56, kd + 1030, id_f);
         }
+        // one commit per S group: its landing also tells the softmax warps that
+        // the K stage was read (for the tile's last S) and that every MMA
+        // issued before it, PV(s - 2) included, has finished
         mma_commit(bar(B_S_FULL + step_kind(s)));
-        if (step_kh(s) == 0) mma_commit(bar(B_K_EMPTY + st));   // last S of its tile
         return true;
       };
       // O += P V; k-step k = 16 keys = 2048 bytes of the MN-major V tile
@@ -455,38 +444,66 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           mma_ts_c<1>(o, pa + 16, vd + 256, id_o);
           mma_ts_c<1>(o, pa + 24, vd + 384, id_o);
         } else {
-          const uint32_t pa = tmem + TM_S + 128u * (uint32_t)((s - s2) & 1);
-          if (s > 0) mma_ts_c<1>(o, pa + 0, vd + 0, id_o);
-          else mma_ts_c<0>(o, pa + 0, vd + 0, id_o);
-          mma_ts_c<1>(o, pa + 8, vd + 128, id_o);
-          mma_ts_c<1>(o, pa + 16, vd + 256, id_o);
-          mma_ts_c<1>(o, pa + 24, vd + 384, id_o);
-          mma_ts_c<1>(o, pa + 32, vd + 512, id_o);
-          mma_ts_c<1>(o, pa + 40, vd + 640, id_o);
-          mma_ts_c<1>(o, pa + 48, vd + 768, id_o);
-          mma_ts_c<1>(o, pa + 56, vd + 896, id_o);
+          // two halves, one per warpgroup's P (keys 0..63 / 64..127), each
+          // issued as soon as that warpgroup's P is in
+          const int par = (s - s2) & 1, ph = ((s - s2) >> 1) & 1;
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(bar(B_P_HALF + 2 * h + par), ph, abort_flag, 11)) return false;
+            tc_fence_after();
+            const uint32_t pa = tmem + TM_P + 32u * h;
+            const uint64_t vh = vd + 512 * h;
+            if (s > 0 || h > 0) mma_ts_c<1>(o, pa + 0, vh + 0, id_o);
+            else mma_ts_c<0>(o, pa + 0, vh + 0, id_o);
+            mma_ts_c<1>(o, pa + 8, vh + 128, id_o);
+            mma_ts_c<1>(o, pa + 16, vh + 256, id_o);
+            mma_ts_c<1>(o, pa + 24, vh + 384, id_o);
+            // this half of the P buffer is free again once this lands
+            mma_commit(bar(B_PV_F + 2 * h + par));
+          }
         }
-        mma_commit(bar(B_PV_DONE + step_kind(s)));
-        if (step_kh(s) == 0) mma_commit(bar(B_V_EMPTY + st));   // last PV of its tile
+        // In the band, PV(s) completion is learnt from the landing of S(s + 2)
+        // (or S(s + 1) for an O rescale at step s + 1); commits only where no
+        // such S follows without waiting for P: the last two steps, and the step
+        // before the first full step (whose S is issued after the last half
+        // step's PV).  Full steps commit PV_F above.
+        if (s == nsteps - 2) mma_commit(bar(B_PV_TAIL));
+        if (s == nsteps - 1) mma_commit(bar(B_PV_TAIL + 1));
+        if (s2 < nsteps && s == s2 - 2) mma_commit(bar(B_PV_SW));
         return true;
       };
       if (ok && s2 > 0)
         for (int c = c_start; c <= c_first && ok; ++c) ok = issue_r(c);
       if (ok && nsteps > 0) ok = issue_s(0);   // an empty decode split issues nothing
+      if (ok && s2 == 0 && nsteps > 1) ok = issue_s(1);   // full steps keep two S in flight
       for (int s = 0; s < nsteps && ok; ++s) {
-        // the first full step's S buffer overlaps the half-step buffers and the
-        // R ring: it is issued only once the last half step's P is in
-        const bool switch_next = (s + 1 == s2) && (s2 < nsteps);
-        if (!switch_next && s + 1 < nsteps && !(ok = issue_s(s + 1))) break;
-        if (s + 1 < s2) {
-          const int c = c_new(s + 1);
-          if (!(ok = mbar_wait(bar(B_R_FREE), s & 1, abort_flag, 10))) break;
-          if (c >= c_start && !(ok = issue_r(c))) break;
+        if (s < s2) {
+          // ---- half step: S(s+1) ahead of PV(s).  The first full steps' S
+          // buffers overlap the half-step buffers and the R ring: they are
+          // issued only once the last half step's P is in.
+          const bool switch_next = (s + 1 == s2) && (s2 < nsteps);
+          if (!switch_next && s + 1 < nsteps && !(ok = issue_s(s + 1))) break;
+          if (s + 1 < s2) {
+            const int c = c_new(s + 1);
+            if (!(ok = mbar_wait(bar(B_R_FREE), s & 1, abort_flag, 10))) break;
+            if (c >= c_start && !(ok = issue_r(c))) break;
+          }
+          if (!(ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11))) break;
+          tc_fence_after();
+          if (!(ok = issue_pv(s))) break;
+          if (switch_next) {
+            if (!(ok = issue_s(s + 1))) break;
+            if (s + 2 < nsteps && !(ok = issue_s(s + 2))) break;
+          }
+        } else {
+          // ---- full step: S(s+2) into the buffer of S(s) as soon as the
+          // softmax has read it, then PV(s)
+          if (s + 2 < nsteps) {
+            if (!(ok = mbar_wait(bar(B_S_READ + ((s - s2) & 1)), ((s - s2) >> 1) & 1, abort_flag, 19))) break;
+            tc_fence_after();
+            if (!(ok = issue_s(s + 2))) break;
+          }
+          if (!(ok = issue_pv(s))) break;   // waits for each warpgroup's P half
         }
-        if (!(ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11))) break;
-        tc_fence_after();
-        if (!(ok = issue_pv(s))) break;
-        if (switch_next && !(ok = issue_s(s + 1))) break;
       }
       // drain: every MMA issued above has finished before TMEM is released
       mma_commit(bar(B_DRAIN));
@@ -494,7 +511,9 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 12, 400000000ll);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ======================================================== softmax
     // Two warpgroups share the 128 rows: warpgroup wg handles the wg-th half of
     // every step's keys and O / output columns [64 wg, 64 wg + 64).  The two
@@ -502,6 +521,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     // exchange guarded by a per-lane-quarter mbarrier.
     const int wg = (warp - 4) >> 2;
     const int wq = warp & 3;                     // lane quarter (TMEM lanes 32 wq ..)
+    const bool leader = warp == 4 && lane == 0;  // releases K / V / P stages
     const int a_row = 32 * wq + lane;            // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const int t_row = row_t(a_row), h_row = row_h(a_row);
@@ -548,6 +568,15 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         if (8 * j < a.rd) v = *reinterpret_cast<const uint4 *>(rsrc + 8 * j);
         *reinterpret_cast<uint4 *>(rrow + ((j ^ (a_row & 7)) << 4)) = v;
       }
+      // P-slice rows r_dim .. rd_pad of every stage are zero (the TMA box
+      // covers r_dim rows); written once, before the first R MMA
+      const int zero_chunks = (a.rd_pad - a.rd) * 8 * P_STAGES;
+      for (int i = a_row + 128 * wg; i < zero_chunks; i += 256) {
+        const int st = i / ((a.rd_pad - a.rd) * 8), rem = i % ((a.rd_pad - a.rd) * 8);
+        const int ch = a.rd + (rem >> 3), j = rem & 7;
+        *reinterpret_cast<uint4 *>(smem + SM_PS + st * 8192 + (ch >> 3) * 1024 + (ch & 7) * 128 + j * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
       fence_proxy_async_smem();
       mbar_arrive(bar(B_RT_FULL));
     }
@@ -576,6 +605,14 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
       if (!(ok = warp_wait(bar(B_S_FULL + step_kind(s)), step_phase(s), 13))) break;
+      if (leader) {
+        // S(s) landed: the K stage of its tile is read (last S of the tile)
+        if (step_kh(s) == 0) mbar_arrive(bar(B_K_EMPTY + step_tile(s) % K_STAGES));
+        // (S(s) is issued after PV(s-2) while s - 2 is a half step; full steps
+        // release their V stage after waiting for PV_F instead)
+        if (s >= 2 && s - 2 < s2 && step_kh(s - 2) == 0)
+          mbar_arrive(bar(B_V_EMPTY + step_tile(s - 2) % V_STAGES));
+      }
       const int D = step_D(s);
       const int j0 = p0 - D;                     // first key of this step
       float corr = 1.f;
@@ -594,12 +631,18 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         // ---------------- half step: 32 keys per thread, relative bias
         const uint32_t sbuf = tmem + lane_base + TM_H + 64u * (uint32_t)(s & 1);
         // the newest chunk this step needs (older ones were awaited before)
+        // (chunk c landed: its P stage may be refilled)
         if (s == 0) {
-          for (int c = c_start; c <= c_first && ok; ++c)
+          for (int c = c_start; c <= c_first && ok; ++c) {
             ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 14);
+            if (ok && leader) mbar_arrive(bar(B_PS_EMPTY + (c - c_start) % P_STAGES));
+          }
         } else {
           const int c = c_new(s);
-          if (c >= c_start) ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 15);
+          if (c >= c_start) {
+            ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 15);
+            if (ok && leader) mbar_arrive(bar(B_PS_EMPTY + (c - c_start) % P_STAGES));
+          }
         }
         if (!ok) break;
         tc_fence_after();
@@ -705,14 +748,21 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         tmem_st16(sbuf + 16u * wg, pk);   // P (bf16 pairs) over S columns [16 wg, 16 wg + 16)
       } else {
         // ---------------- full step: 64 keys per thread, no bias
+        // Each thread also reads the other warpgroup's half of its row to take
+        // the full row max itself (bit-identical in both warpgroups), so the
+        // two warpgroups never meet.  Once S(s) is read, the MMA issuer may
+        // compute S(s+2) into its buffer; P goes to the separate P buffer as
+        // soon as PV(s-1) has consumed the previous P.
         const uint32_t sbuf = tmem + lane_base + TM_S + 128u * (uint32_t)((s - s2) & 1);
         tc_fence_after();
-        uint32_t sr0[32], sr1[32];
+        uint32_t sr0[32], sr1[32], so[32];
         __syncwarp();
         tmem_ld32(sbuf + 64u * wg, sr0);
         tmem_ld32(sbuf + 64u * wg + 32u, sr1);
+        tmem_ld32(sbuf + 64u * (1 - wg), so);
         tmem_wait_ld(sr0);
         reg_dep(sr1);
+        reg_dep(so);
         float x[64];   // raw scores; the scale is applied inside the exponent
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -720,32 +770,68 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           x[32 + i] = __uint_as_float(sr1[i]);
         }
         const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+        auto visible = [&](int j) { return j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window); };
+        float mo;
+        {
+          float y[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(so[i]);
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = visible(j0 + 64 * (1 - wg) + i) ? y[i] : -INFINITY;
+          }
+          mo = row_max(y);
+          __syncwarp();
+          tmem_ld32(sbuf + 64u * (1 - wg) + 32u, so);
+          tmem_wait_ld(so);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(so[i]);
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = visible(j0 + 64 * (1 - wg) + 32 + i) ? y[i] : -INFINITY;
+          }
+          mo = fmaxf(mo, row_max(y));
+        }
+        // this thread has read all of S(s): its buffer may take S(s+2)
+        tc_fence_before();
+        mbar_arrive(bar(B_S_READ + ((s - s2) & 1)));
         if (need_mask) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const int j = j0 + 64 * wg + i;
-            const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
-            x[i] = vis ? x[i] : -INFINITY;
-          }
+          for (int i = 0; i < 64; ++i) x[i] = visible(j0 + 64 * wg + i) ? x[i] : -INFINITY;
         }
-        const float mloc = row_max(x) * cqk;
-        const float mo = exchange(s, mloc, ok);
-        if (!ok) break;
-        update_max(fmaxf(mloc, mo));
+        update_max(fmaxf(row_max(x), mo) * cqk);
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[32];
         l += exp_pack_raw(x, cqk, m_use, pk);
+        if (s > s2) {
+          // this warpgroup's half of PV(s-1) has consumed its half of the P
+          // buffer; the second half (issued last) also frees the V stage
+          if (!(ok = warp_wait(bar(B_PV_F + 2 * wg + ((s - 1 - s2) & 1)), ((s - 1 - s2) >> 1) & 1, 18))) break;
+          if (wg == 1 && warp == 8 && lane == 0) mbar_arrive(bar(B_V_EMPTY + step_tile(s - 1) % V_STAGES));
+        }
+        tc_fence_after();
         __syncwarp();
-        tmem_st32(sbuf + 32u * wg, pk);   // P (bf16 pairs) over S columns [32 wg, 32 wg + 32)
+        tmem_st32(tmem + lane_base + TM_P + 32u * wg, pk);   // P (bf16 pairs), keys [64 wg, 64 wg + 64)
       }
       // O is only touched when some row of this warp needs a rescale; then
       // PV(s-1) must have landed first.  Otherwise PV(s) simply queues behind
-      // PV(s-1) on the tensor core.  (S(s) landing implies PV(s-2) did, so the
-      // wait is for the next phase of its barrier and never ambiguous.)
+      // PV(s-1) on the tensor core.  Full steps have waited for PV(s-1) above
+      // (the first full step: S(s2) was issued after PV(s2-1)).  In the band
+      // PV(s-1) is known done when S(s+1) lands (issued after it without
+      // waiting for P(s)); where S(s+1) does not exist or waits for P(s) (the
+      // switch to full steps), by its own commit.
       // TMEM loads / stores are warp-collective: the whole warp rescales its 32
       // rows when any of them needs it (rows that do not are scaled by 1)
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (!(ok = warp_wait(bar(B_PV_DONE + step_kind(s - 1)), step_phase(s - 1), 16))) break;
+        if (s < s2) {
+          if (s + 1 >= nsteps) ok = warp_wait(bar(B_PV_TAIL), 0, 16);       // after PV(nsteps - 2)
+          else if (s + 1 == s2) ok = warp_wait(bar(B_PV_SW), 0, 16);        // after PV(s2 - 2)
+          else ok = warp_wait(bar(B_S_FULL + step_kind(s + 1)), step_phase(s + 1), 16);
+          if (!ok) break;
+        } else if (s > s2 && wg == 0) {
+          // both halves of PV(s-1) write every O column: wait for the second
+          if (!(ok = warp_wait(bar(B_PV_F + 2 + ((s - 1 - s2) & 1)), ((s - 1 - s2) >> 1) & 1, 16))) break;
+        }
         tc_fence_after();
         const float cf = rescale_o ? corr : 1.f;
 #pragma unroll
@@ -763,14 +849,15 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_P_FULL + step_kind(s)));
+      if (s < s2) mbar_arrive(bar(B_P_FULL + step_kind(s)));
+      else mbar_arrive(bar(B_P_HALF + 2 * wg + ((s - s2) & 1)));
     }
     (void)delta;
     // ---- epilogue
-    if (ok && nsteps > 0)
-      ok = warp_wait(bar(B_PV_DONE + step_kind(nsteps - 1)), step_phase(nsteps - 1), 17);
+    if (ok && nsteps > 0) ok = warp_wait(bar(B_PV_TAIL + 1), 0, 17);
     float l_other = 0.f;
-    if (ok) l_other = exchange(nsteps, l, ok);   // total row sum over both key halves
+    // total row sum over both key halves (exchange number s2: one per half step)
+    if (ok) l_other = exchange(s2, l, ok);
     if (ok) {
       const float lt = l + l_other;
       tc_fence_after();
@@ -823,7 +910,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
-  if (warp == 2) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -862,8 +949,9 @@ bool tc_supported(const KernelArgs &a, int total_k) {
   auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (!get_encoder()) return false;
   if (!al(a.k) || !al(a.v) || !al(a.q) || !al(a.out)) return false;
-  if (a.rd > 0) {
-    if (a.rd % 8 != 0 || a.E % 8 != 0 || a.rd > 64 || !al(a.r) || !al(a.P)) return false;
+  if (a.rd > 0 && a.E > 0) {
+    // P slices are TMA boxes of 64 distances: rel_extent >= 64, rows of 16 bytes
+    if (a.rd % 8 != 0 || a.E % 8 != 0 || a.rd > 64 || a.E < HN || !al(a.r) || !al(a.P)) return false;
   }
   if (total_k < BN) return false;   // K/V boxes stay inside the tensor
   return true;
@@ -876,13 +964,23 @@ cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t 
   TcArgs ta;
   ta.a = a;
   ta.has_bias = a.rd > 0 && a.E > 0;
-  CUtensorMap mk, mv;
+  CUtensorMap mk, mv, mp;
   {
     cuuint64_t dims[3] = {128, (cuuint64_t)a.Hkv, (cuuint64_t)total_k};
     cuuint64_t strides[2] = {256, (cuuint64_t)a.Hkv * 256};
     cuuint32_t box[3] = {64, 1, BN};
     if (!encode(&mk, a.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (!encode(&mv, a.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  if (ta.has_bias) {
+    // P [r_dim, E]: box of 64 distances x r_dim channels (x offsets are
+    // multiples of 64 elements, i.e. of 128 bytes)
+    cuuint64_t dims[2] = {(cuuint64_t)a.E, (cuuint64_t)a.rd};
+    cuuint64_t strides[1] = {(cuuint64_t)a.E * 2};
+    cuuint32_t box[2] = {(cuuint32_t)HN, (cuuint32_t)a.rd};
+    if (!encode(&mp, a.P, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
+    mp = mk;   // unused
   }
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -893,7 +991,7 @@ cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  relattn_fwd_tc_kernel<DECODE><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv);
+  relattn_fwd_tc_kernel<DECODE><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv, mp);
   return cudaGetLastError();
 }
 

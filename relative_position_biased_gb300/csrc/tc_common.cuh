@@ -49,17 +49,30 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Wait until the phase with `parity` has completed.  The wait is bounded by
-// SM clock cycles (about a second at GB300 clocks for the default): after
-// `limit_cycles`, or as soon as another thread of the CTA raised `*abort`, it
-// gives up, raises `*abort` (= site id, for diagnosis) and returns false.
-// Callers inside a warp-collective region make the result warp-uniform.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with `parity` has completed, polling (the waits on
+// the critical path are short; a suspended thread wakes later than a polling
+// one).  The wait is bounded by SM clock cycles (about a second at GB300
+// clocks for the default): after `limit_cycles`, or as soon as another thread
+// of the CTA raised `*abort`, it gives up, raises `*abort` (= site id, for
+// diagnosis) and returns false.  Callers inside a warp-collective region make
+// the result warp-uniform.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int site, long long limit_cycles = 2000000000ll) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit_cycles) {
       *abort = site;
@@ -170,6 +183,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 // Orders every later use of r after the preceding (ordered) tcgen05.wait::ld.
+// Per-warpgroup register budget (setmaxnreg, executed by every warp of the
+// warpgroup): .dec returns registers to the CTA's pool, .inc waits for them.
+// The budgets of all warpgroups must add up to at most the launch's
+// threads x registers-per-thread.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 __device__ __forceinline__ void reg_dep(uint32_t (&r)[32]) {
   asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),

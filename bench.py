@@ -309,13 +309,15 @@ def reference_arm(args):
         return 0
     w = W.swa_prefill()
     inp = W.make_inputs(w)
-    rows = oracle_sample_rows(w, 64)
+    # each step: a sample of query rows sized to about a second of oracle work
+    cal = oracle_sample_rows(w, 64, seed=3)
     for _ in range(args.warmup):
-        time_oracle(w, inp, rows[:8])
+        cdt, _, _ = time_oracle(w, inp, cal)
+    n_step = int(min(sum(w.q_lens), max(64, 64 * 1.0 / max(cdt, 1e-3))))
     dts, fl = [], 0
     t_all0 = time.perf_counter()
     for s in range(args.steps):
-        r = oracle_sample_rows(w, 64, seed=100 + s)
+        r = oracle_sample_rows(w, n_step, seed=100 + s)
         dt, f, cores = time_oracle(w, inp, r)
         dts.append(dt)
         fl += f
@@ -326,9 +328,9 @@ def reference_arm(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample": "64 random query rows x 16 heads per step"},
+        "config": {"workload": w.name, "sample": f"{n_step} random query rows x {w.Hq} heads per step"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} steps x 64 random query rows x 16 heads of {w.name}"},
+                         "sample": f"{args.steps} steps x {n_step} random query rows x {w.Hq} heads of {w.name}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s": time.perf_counter() - t_all0,
@@ -337,18 +339,25 @@ def reference_arm(args):
     return 0
 
 
+CPU_SAMPLE_SECONDS = 10.0   # oracle work for the cpu_baseline (bounded sample)
+
+
 def cpu_baseline(wl, host):
-    """Oracle on the host cores over a bounded sample of the prefill workload."""
+    """Oracle on the host cores over a bounded sample of the prefill workload:
+    a short calibration sizes the sample to about CPU_SAMPLE_SECONDS."""
     w = wl["prefill"]
-    rows = oracle_sample_rows(w, 256)
+    cal = oracle_sample_rows(w, 128, seed=3)
+    cdt, _, _ = time_oracle(w, host["prefill"], cal)
+    n = int(min(sum(w.q_lens), max(128, 128 * CPU_SAMPLE_SECONDS / max(cdt, 1e-3))))
+    rows = oracle_sample_rows(w, n)
     dt, f, cores = time_oracle(w, host["prefill"], rows)
     wd = wl["decode_long"]
-    drows = np.array([sum(wd.q_lens) - 1], dtype=np.int64)
+    drows = np.arange(sum(wd.q_lens), dtype=np.int64)   # every MTP row
     ddt, _, _ = time_oracle(wd, host["decode_long"], drows)
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"256 random query rows x 16 heads of {w.name} ({dt:.1f} s)",
+            "sample": f"{n} random query rows x {w.Hq} heads of {w.name} ({dt:.1f} s)",
             "decode": {"value": decode_rows_bytes(wd, drows) / ddt / 1e9, "unit": "GB/s",
-                       "sample": f"1 query row x 16 heads of {wd.name} ({ddt:.1f} s)"}}
+                       "sample": f"all {len(drows)} query rows x {wd.Hq} heads of {wd.name} ({ddt:.1f} s)"}}
 
 
 def gpu_arm(args):
@@ -441,7 +450,7 @@ def gpu_arm(args):
                      "unit": "TFLOP/s", "frac": pre_tf / tf_peak,
                      "traffic": load_traffic("prefill"),
                      "peak_source": f"{peak_kind} bf16 dense (burst)",
-                     "kernel": "relattn_fwd_tc_prefill_kernel"},
+                     "kernel": "relattn_fwd_tc_kernel<prefill>"},
         "decode": {
             "value": dl_gbs, "unit": "GB/s", "workload": dl.w.name,
             "roofline": {"bound": "hbm", "achieved": dl_gbs, "peak": hbm_peak, "unit": "GB/s",

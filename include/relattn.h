@@ -168,6 +168,17 @@ relattn_status relattn_get_device_error(void *stream);
  * the id of the wait that gave up first (diagnostics only). */
 int32_t relattn_last_device_error_word(void);
 
+/* Test hook for the failure path; not for production use, and with no
+ * counterpart on the pages.  With tile >= 0, every later launch of the
+ * tensor-core kernels leaves key tile `tile` (the tile-th 128-key tile a CTA
+ * visits) unloaded, so the wait of the MMA issuer on it runs out after its
+ * bounded limit (about a second): the CTA gives up, drains its own copies and
+ * MMAs, frees its tensor memory and exits, and relattn_get_device_error()
+ * then returns RELATTN_ERR_TIMEOUT (outputs of affected rows are undefined).
+ * tile = -1 restores normal operation; tile < -1 -> RELATTN_ERR_INVALID_ARG.
+ * Process-wide; not thread-safe against concurrent launches. */
+relattn_status relattn_test_skip_k_tile(int32_t tile);
+
 /* Human-readable name of a status code (static string). */
 const char *relattn_status_string(relattn_status status);
 

@@ -21,6 +21,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librelattn.so")
 
 RELATTN_OK = 0
+RELATTN_ERR_TIMEOUT = 4
 STATUS_NAMES = {
     0: "RELATTN_OK", 1: "RELATTN_ERR_INVALID_ARG", 2: "RELATTN_ERR_UNSUPPORTED",
     3: "RELATTN_ERR_CUDA", 4: "RELATTN_ERR_TIMEOUT", 5: "RELATTN_ERR_WORKSPACE",
@@ -30,7 +31,7 @@ EXPORTED = (
     "relattn_prefill", "relattn_decode", "relattn_decode_workspace_size",
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
-    "relattn_last_device_error_word",
+    "relattn_last_device_error_word", "relattn_test_skip_k_tile",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -97,6 +98,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_status_string.restype = ctypes.c_char_p
         lib.relattn_last_device_error_word.argtypes = []
         lib.relattn_last_device_error_word.restype = ctypes.c_int32
+        lib.relattn_test_skip_k_tile.argtypes = [ctypes.c_int32]
+        lib.relattn_test_skip_k_tile.restype = ctypes.c_int
         lib.relattn_version.argtypes = []
         lib.relattn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -147,6 +150,11 @@ def relattn_get_device_error(stream: int = 0) -> int:
 
 def relattn_last_device_error_word() -> int:
     return int(load_library().relattn_last_device_error_word())
+
+
+def relattn_test_skip_k_tile(tile: int) -> int:
+    """Test hook: later tensor-core launches never load key tile ``tile`` (-1: off)."""
+    return int(load_library().relattn_test_skip_k_tile(int(tile)))
 
 
 def relattn_status_string(status: int) -> str:

@@ -12,6 +12,8 @@ using namespace relattn;
 namespace {
 
 __device__ int g_device_error;
+// test hook (relattn_test_skip_k_tile): K tile the tcgen05 producer never loads
+int g_test_skip_k_tile = -1;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -98,6 +100,7 @@ relattn_status make_args(const relattn_params *p, KernelArgs *a) {
   x.alpha_log2e = p->alpha * kLog2e;
   x.inv_ln_base = p->log_scale_base > 1.f ? 1.f / logf(p->log_scale_base) : 0.f;
   x.r_vec_ok = bias && (p->r_dim % 8 == 0) && aligned16(p->r);
+  x.test_skip_k_tile = g_test_skip_k_tile;
   x.p_vec_ok = bias && (p->rel_extent % 8 == 0) && aligned16(p->P);
   x.num_splits = 1;
   x.split_chunk = 0;
@@ -276,5 +279,11 @@ const char *relattn_status_string(relattn_status s) {
 const char *relattn_version(void) { return "relattn 0.1 sm_103a"; }
 
 int32_t relattn_last_device_error_word(void) { return g_last_error_word; }
+
+relattn_status relattn_test_skip_k_tile(int32_t tile) {
+  if (tile < -1) return RELATTN_ERR_INVALID_ARG;
+  g_test_skip_k_tile = tile;
+  return RELATTN_OK;
+}
 
 }  // extern "C"

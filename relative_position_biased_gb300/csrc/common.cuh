@@ -38,6 +38,7 @@ struct KernelArgs {
   int q_tiles;                   // prefill: query tiles per (sequence, head)
   int row_blocks;                // decode: 128-row blocks per (sequence, kv head)
   int r_vec_ok, p_vec_ok;        // 16-byte vector loads allowed for r / P
+  int test_skip_k_tile;          // test hook (tcgen05 kernels): never load this K tile; -1 = off
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -300,6 +300,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
+  // TMA copies issued by the producer thread (to drain them if the CTA gives up)
+  int issued_k = 0, issued_v = 0, issued_p = 0;
   if (warp < 4) {
   regs_dec<kRegsSupport>();
   if (warp == 0) {
@@ -312,7 +314,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     if (lane == 0) {
       const uint32_t p_bytes = 128u * (uint32_t)a.rd;
       int kst = 0, kph = 0, vst = 0, vph = 0;
-      int issued_k = 0, issued_v = 0, c_next = c_start;
+      int c_next = c_start;
       bool run = true;
       for (int t = 0; t < ntiles && run && !*abort_flag; ++t) {
         if (t < nb_tiles) {
@@ -323,19 +325,20 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
               break;
             mbar_arrive_expect_tx(bar(B_PS_FULL + st), p_bytes);
             tma_load_2d(sb + SM_PS + st * 8192, &map_p, HN * c_next, 0, bar(B_PS_FULL + st));
+            issued_p = c_next - c_start + 1;
           }
           if (!run) break;
         }
         const int key = ck + p0 - tile_D(t);   // may be < 0: the tile reads zeros there
         if (t >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
-        {
+        if (t != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
           const uint32_t dst = sb + SM_K + kst * KV_STAGE_BYTES;
           mbar_arrive_expect_tx(bar(B_K_FULL + kst), KV_STAGE_BYTES);
           tma_load_3d(dst, &map_k, 0, kv_head, key, bar(B_K_FULL + kst));
           tma_load_3d(dst + KV_BOX_BYTES, &map_k, 64, kv_head, key, bar(B_K_FULL + kst));
-          issued_k = t + 1;
-          if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
         }
+        issued_k = t + 1;
+        if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
         if (t >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
         {
           const uint32_t dst = sb + SM_V + vst * KV_STAGE_BYTES;
@@ -345,17 +348,6 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           issued_v = t + 1;
           if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
         }
-      }
-      if (*abort_flag) {
-        // let our own copies land before the CTA goes away (bounded, not cut short by the abort)
-        volatile int keep_waiting = 0;
-        for (int t = max(0, issued_k - K_STAGES); t < issued_k; ++t)
-          mbar_wait(bar(B_K_FULL + t % K_STAGES), (t / K_STAGES) & 1, &keep_waiting, 2, 400000000ll);
-        for (int t = max(0, issued_v - V_STAGES); t < issued_v; ++t)
-          mbar_wait(bar(B_V_FULL + t % V_STAGES), (t / V_STAGES) & 1, &keep_waiting, 2, 400000000ll);
-        const int issued_p = c_next - c_start;
-        for (int o = max(0, issued_p - P_STAGES); o < issued_p; ++o)
-          mbar_wait(bar(B_PS_FULL + o % P_STAGES), (o / P_STAGES) & 1, &keep_waiting, 2, 400000000ll);
       }
     }
     __syncwarp();
@@ -910,6 +902,18 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // the CTA gave up: let the producer's own copies land before shared memory
+    // goes away (bounded waits, not cut short by the abort)
+    volatile int keep_waiting = 0;
+    for (int t = max(0, issued_k - K_STAGES); t < issued_k; ++t)
+      if (t != a.test_skip_k_tile)
+        mbar_wait(bar(B_K_FULL + t % K_STAGES), (t / K_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+    for (int t = max(0, issued_v - V_STAGES); t < issued_v; ++t)
+      mbar_wait(bar(B_V_FULL + t % V_STAGES), (t / V_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+    for (int o = max(0, issued_p - P_STAGES); o < issued_p; ++o)
+      mbar_wait(bar(B_PS_FULL + o % P_STAGES), (o / P_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -1,0 +1,46 @@
+"""Failure path of the tensor-core kernels, without faulting the GPU.
+
+A test hook makes the TMA producer leave one key tile unloaded, so the MMA
+issuer's wait on it (bounded by its clock limit, about a second) runs out.
+The CTA must give up cleanly: drain its own copies and MMAs, free its tensor
+memory and exit; the host then reads RELATTN_ERR_TIMEOUT from the device
+error word, and the context stays usable for the next, normal call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import relative_position_biased_gb300 as rpb
+from relative_position_biased_gb300 import workloads as W
+
+from tests.parity_util import compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_gives_up_and_context_recovers(oracle_mod):
+    # 384 tokens, no bias: the tensor-core path; the CTAs of the last two
+    # query tiles visit 2 and 3 key tiles, so key tile 1 is on their path
+    w = W.custom("fail_t384", [384], [384], 2, 1, 0, 64)
+    inp = W.make_inputs(w)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    args = [dev[k] for k in ("q", "k", "v", "r", "P", "cu_seqlens_q", "cu_seqlens_k")]
+    kw = dict(max_seqlen_q=384, max_seqlen_k=384, alpha=w.alpha, window=0, log_scale_base=0.0)
+    assert rpb.relattn_get_device_error() == rpb.RELATTN_OK   # start clean
+    assert rpb.relattn_test_skip_k_tile(1) == rpb.RELATTN_OK
+    try:
+        rpb.prefill(*args, **kw)          # the launch itself succeeds
+        torch.cuda.synchronize()          # and the CTAs finish (no hang)
+        st = rpb.relattn_get_device_error()
+        word = rpb.relattn_last_device_error_word()
+    finally:
+        rpb.relattn_test_skip_k_tile(-1)
+    assert st == rpb.RELATTN_ERR_TIMEOUT, (rpb.STATUS_NAMES.get(st, st), hex(word))
+    assert word & 2 and (word >> 8) > 0
+    # the same call, hook off: correct results on the same context
+    compare(w, inp, run_gpu(w, inp))
+
+
+def test_skip_hook_rejects_bad_tile():
+    assert rpb.relattn_test_skip_k_tile(-2) != rpb.RELATTN_OK
+    assert rpb.relattn_test_skip_k_tile(-1) == rpb.RELATTN_OK

@@ -130,19 +130,6 @@ __device__ __forceinline__ float exp_pack_raw(const float (&x)[NX], float c, flo
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-// P of one step's keys from already scaled logits: e = 2^(x - m)
-template <int NX>
-__device__ __forceinline__ float exp_pack(const float (&x)[NX], float m_use, uint32_t (&pk)[NX / 2]) {
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < NX / 2; ++i) {
-    const float e0 = fast_exp2(x[2 * i] - m_use), e1 = fast_exp2(x[2 * i + 1] - m_use);
-    acc[i & 3] += e0 + e1;
-    pk[i] = pack_bf16x2(e0, e1);
-  }
-  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
-}
-
 // max of N values as a tree of three-input maxima (short dependency chains)
 template <int N>
 __device__ __forceinline__ float row_max(const float (&x)[N]) {
@@ -527,6 +514,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     // instead (exact in bf16), so a row max of raw scores is a max of logits
     const bool q_neg = a.alpha_log2e < 0.f;
     const float cqk = fmaxf(fabsf(a.alpha_log2e) * sc, 1e-30f), cbias = kLog2e * sc;
+    // band steps form t = |alpha| S + bias and apply cbias inside the exponent
+    const float qk_over_bias = cqk / cbias;
     float *xbuf = reinterpret_cast<float *>(smem + SM_XCH);   // [2 parity][2 wg][128]
 
     // q row half -> TMEM columns [32 wg, 32 wg + 32) (bf16 pairs)
@@ -652,12 +641,22 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           tmem_wait_ld(sr);
           reg_dep(w0);
           reg_dep(w1);
+          // distances below the first computed chunk are not needed: zeros
+          // (warp-uniform; only near the start of a decode split's band)
+          if (base < d_min) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w0[i] = 0u;
+          }
+          if (base + 32 < d_min) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w1[i] = 0u;
+          }
           // z[63 - i] = window[i]; the thread of lane t needs window[32 + t - u]
           float z[64];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            z[63 - i] = base >= d_min ? __uint_as_float(w0[i]) : 0.f;
-            z[31 - i] = base + 32 >= d_min ? __uint_as_float(w1[i]) : 0.f;
+            z[63 - i] = __uint_as_float(w0[i]);
+            z[31 - i] = __uint_as_float(w1[i]);
           }
           tc_fence_before();
           mbar_arrive(bar(B_R_FREE));
@@ -675,8 +674,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           for (int i = 0; i < 32; ++i) z[i] = (sh & 1) ? z[i + 1] : z[i];
 #pragma unroll
           for (int u = 0; u < 32; u += 2)
-            ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
-                  z[u] * cbias, z[u + 1] * cbias);
+            ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), qk_over_bias,
+                  qk_over_bias, z[u], z[u + 1]);
         } else {
           tmem_wait_ld(sr);
           // rows of a warp span at most 16 positions: distances
@@ -717,8 +716,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           for (int i = 0; i < 32; ++i) zz[i] = (sh & 1) ? zz[i + 1] : zz[i];
 #pragma unroll
           for (int u = 0; u < 32; u += 2)
-            ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), cqk, cqk,
-                  zz[u] * cbias, zz[u + 1] * cbias);
+            ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), qk_over_bias,
+                  qk_over_bias, zz[u], zz[u + 1]);
         }
         const bool need_mask = (j0 + HN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
         if (need_mask) {
@@ -729,13 +728,14 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             x[i] = vis ? x[i] : -INFINITY;
           }
         }
-        const float mloc = row_max(x);
+        // x holds t = |alpha| S + bias; the logit in log2 units is t * cbias
+        const float mloc = row_max(x) * cbias;
         const float mo = exchange(s, mloc, ok);
         if (!ok) break;
         update_max(fmaxf(mloc, mo));
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[16];
-        l += exp_pack(x, m_use, pk);
+        l += exp_pack_raw(x, cbias, m_use, pk);
         __syncwarp();
         tmem_st16(sbuf + 16u * wg, pk);   // P (bf16 pairs) over S columns [16 wg, 16 wg + 16)
       } else {

@@ -171,7 +171,7 @@ int32_t relattn_last_device_error_word(void);
 /* Test hook for the failure path; not for production use, and with no
  * counterpart on the pages.  With tile >= 0, every later launch of the
  * tensor-core kernels leaves key tile `tile` (the tile-th 128-key tile a CTA
- * visits) unloaded, so the wait of the MMA issuer on it runs out after its
+ * of that kernel visits) unloaded, so the wait of the MMA issuer on it runs out after its
  * bounded limit (about a second): the CTA gives up, drains its own copies and
  * MMAs, frees its tensor memory and exits, and relattn_get_device_error()
  * then returns RELATTN_ERR_TIMEOUT (outputs of affected rows are undefined).

@@ -180,7 +180,22 @@ relattn_status relattn_prefill(const relattn_params *p, void *stream) {
   KernelArgs a;
   if ((st = make_args(p, &a)) != RELATTN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (tc_supported(a, p->total_k)) return cuda_status(launch_prefill_tc(a, p->total_k, s));
+  if (tc_supported(a, p->total_k)) {
+    if (tc_main_supported(a, p->total_q, p->total_k)) {
+      // the bias band on the bias kernel (out / lse normalised over the band),
+      // then every other key tile on the two-head main kernel, which starts
+      // from that state
+      if (a.rd > 0 && a.E > 0) {
+        a.band_only = 1;
+        cudaError_t e = launch_prefill_tc(a, p->total_k, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        a.band_only = 0;
+        a.init_from_out = 1;
+      }
+      return cuda_status(launch_prefill_tc_main(a, p->total_k, s));
+    }
+    return cuda_status(launch_prefill_tc(a, p->total_k, s));
+  }
   return cuda_status(launch_prefill_mma(a, s));
 }
 

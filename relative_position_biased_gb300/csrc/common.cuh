@@ -39,6 +39,8 @@ struct KernelArgs {
   int row_blocks;                // decode: 128-row blocks per (sequence, kv head)
   int r_vec_ok, p_vec_ok;        // 16-byte vector loads allowed for r / P
   int test_skip_k_tile;          // test hook (tcgen05 kernels): never load this K tile; -1 = off
+  int band_only;                 // prefill, bias kernel: only the key tiles of the bias band
+  int init_from_out;             // prefill, main kernel: start from the band's out / lse
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

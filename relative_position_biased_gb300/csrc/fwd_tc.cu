@@ -222,6 +222,9 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     nb_tiles = tile_D(ntiles - 1) < lim ? ntiles : max(0, (lim - Dt0 + BN - 1) / BN);
     if (nb_tiles > ntiles) nb_tiles = ntiles;
   }
+  // prefill split in two kernels: this one takes only the band, and leaves
+  // out / lse normalised over the band's keys for the main kernel to continue
+  if (!DECODE && a.band_only && nb_tiles > 0) ntiles = nb_tiles;
   const int s2 = 2 * nb_tiles;                  // first full step
   const int nsteps = s2 + (ntiles - nb_tiles);
   auto step_tile = [&](int s) { return s < s2 ? s >> 1 : nb_tiles + (s - s2); };

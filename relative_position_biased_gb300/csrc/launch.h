@@ -22,6 +22,12 @@ cudaError_t launch_prefill_mma(const KernelArgs &a, cudaStream_t stream);
 constexpr int kTcKeyTile = 128;
 bool tc_supported(const KernelArgs &a, int total_k);
 cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream);
+// Prefill past the bias band (fwd_tc_main.cu): two query heads of one GQA
+// group per CTA; needs an even group size, alpha > 0 and at least 128 query
+// rows and keys.  With init_from_out it continues from the band kernel's
+// out / lse (launched first with band_only).
+bool tc_main_supported(const KernelArgs &a, int total_q, int total_k);
+cudaError_t launch_prefill_tc_main(const KernelArgs &a, int total_k, cudaStream_t stream);
 // decode on the same kernel: 128 rows of (token, head-in-group) per CTA; grid
 // (num_splits, Hkv * row_blocks, batch); partials when num_splits > 1.
 constexpr int kTcDecodeRows = 128;

@@ -159,6 +159,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// Loads of 32 columns straight into floats x[OFF .. OFF + 32) of a larger
+// register array (keeps the scores in one array, no integer copy).
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&x)[N]) {
+  static_assert(OFF + 32 <= N, "range");
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+               : "=f"(x[OFF + 0]), "=f"(x[OFF + 1]), "=f"(x[OFF + 2]), "=f"(x[OFF + 3]), "=f"(x[OFF + 4]), "=f"(x[OFF + 5]), "=f"(x[OFF + 6]), "=f"(x[OFF + 7]), "=f"(x[OFF + 8]), "=f"(x[OFF + 9]), "=f"(x[OFF + 10]), "=f"(x[OFF + 11]), "=f"(x[OFF + 12]), "=f"(x[OFF + 13]), "=f"(x[OFF + 14]), "=f"(x[OFF + 15]), "=f"(x[OFF + 16]), "=f"(x[OFF + 17]), "=f"(x[OFF + 18]), "=f"(x[OFF + 19]), "=f"(x[OFF + 20]), "=f"(x[OFF + 21]), "=f"(x[OFF + 22]), "=f"(x[OFF + 23]), "=f"(x[OFF + 24]), "=f"(x[OFF + 25]), "=f"(x[OFF + 26]), "=f"(x[OFF + 27]), "=f"(x[OFF + 28]), "=f"(x[OFF + 29]), "=f"(x[OFF + 30]), "=f"(x[OFF + 31])
+               : "r"(taddr));
+}
+// tcgen05.wait::ld that also orders the use of x[OFF .. OFF + 32)
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_wait_ld_f(float (&x)[N]) {
+  static_assert(OFF + 32 <= N, "range");
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+f"(x[OFF + 0]), "+f"(x[OFF + 1]), "+f"(x[OFF + 2]), "+f"(x[OFF + 3]), "+f"(x[OFF + 4]), "+f"(x[OFF + 5]), "+f"(x[OFF + 6]), "+f"(x[OFF + 7]), "+f"(x[OFF + 8]), "+f"(x[OFF + 9]), "+f"(x[OFF + 10]), "+f"(x[OFF + 11]), "+f"(x[OFF + 12]), "+f"(x[OFF + 13]), "+f"(x[OFF + 14]), "+f"(x[OFF + 15]), "+f"(x[OFF + 16]), "+f"(x[OFF + 17]), "+f"(x[OFF + 18]), "+f"(x[OFF + 19]), "+f"(x[OFF + 20]), "+f"(x[OFF + 21]), "+f"(x[OFF + 22]), "+f"(x[OFF + 23]), "+f"(x[OFF + 24]), "+f"(x[OFF + 25]), "+f"(x[OFF + 26]), "+f"(x[OFF + 27]), "+f"(x[OFF + 28]), "+f"(x[OFF + 29]), "+f"(x[OFF + 30]), "+f"(x[OFF + 31])
+               :
+               : "memory");
+}
+// register dependency only (no instruction) for x[OFF .. OFF + 32)
+template <int OFF, int N>
+__device__ __forceinline__ void reg_dep_f(float (&x)[N]) {
+  static_assert(OFF + 32 <= N, "range");
+  asm volatile("" : "+f"(x[OFF + 0]), "+f"(x[OFF + 1]), "+f"(x[OFF + 2]), "+f"(x[OFF + 3]), "+f"(x[OFF + 4]), "+f"(x[OFF + 5]), "+f"(x[OFF + 6]), "+f"(x[OFF + 7]), "+f"(x[OFF + 8]), "+f"(x[OFF + 9]), "+f"(x[OFF + 10]), "+f"(x[OFF + 11]), "+f"(x[OFF + 12]), "+f"(x[OFF + 13]), "+f"(x[OFF + 14]), "+f"(x[OFF + 15]), "+f"(x[OFF + 16]), "+f"(x[OFF + 17]), "+f"(x[OFF + 18]), "+f"(x[OFF + 19]), "+f"(x[OFF + 20]), "+f"(x[OFF + 21]), "+f"(x[OFF + 22]), "+f"(x[OFF + 23]), "+f"(x[OFF + 24]), "+f"(x[OFF + 25]), "+f"(x[OFF + 26]), "+f"(x[OFF + 27]), "+f"(x[OFF + 28]), "+f"(x[OFF + 29]), "+f"(x[OFF + 30]), "+f"(x[OFF + 31]));
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "

@@ -49,6 +49,7 @@ TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "prefill": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
+                "relative_position_biased_gb300/csrc/fwd_tc_main.cu",
                 "relative_position_biased_gb300/csrc/tc_common.cuh",
                 "relative_position_biased_gb300/csrc/common.cuh"],
     "decode": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
@@ -201,7 +202,8 @@ class Phase:
                                dtype=torch.float32, device="cuda")
         self.decode = w.is_decode
         self.ws = None
-        self.launches = 1
+        # prefill with a bias band: the band kernel, then the main kernel
+        self.launches = 2 if (w.r_dim > 0 and w.rel_extent > 0) else 1
         if self.decode:
             prm = rpb.make_params(*self.args, out=self.out, lse=self.lse, **_kw(w))
             self.ws = rpb.decode_workspace(prm, "cuda")
@@ -450,7 +452,8 @@ def gpu_arm(args):
                      "unit": "TFLOP/s", "frac": pre_tf / tf_peak,
                      "traffic": load_traffic("prefill"),
                      "peak_source": f"{peak_kind} bf16 dense (burst)",
-                     "kernel": "relattn_fwd_tc_kernel<prefill>"},
+                     "kernel": "relattn_fwd_tc_kernel<prefill, band> + relattn_fwd_tc_main_kernel "
+                               "(the two launches of one prefill call)"},
         "decode": {
             "value": dl_gbs, "unit": "GB/s", "workload": dl.w.name,
             "roofline": {"bound": "hbm", "achieved": dl_gbs, "peak": hbm_peak, "unit": "GB/s",

@@ -724,12 +724,12 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         }
         const bool need_mask = (j0 + HN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
         if (need_mask) {
+          // visible keys of this row: one range [kmin, kmax] of this thread's keys
+          const int jb = j0 + 32 * wg;
+          const int kmax = pos - jb;
+          const int kmin = max(-jb, a.window > 0 ? pos - a.window + 1 - jb : 0);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int j = j0 + 32 * wg + i;
-            const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
-            x[i] = vis ? x[i] : -INFINITY;
-          }
+          for (int i = 0; i < 32; ++i) x[i] = (i >= kmin && i <= kmax) ? x[i] : -INFINITY;
         }
         // x holds t = |alpha| S + bias; the logit in log2 units is t * cbias
         const float mloc = row_max(x) * cbias;
@@ -765,7 +765,9 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           x[32 + i] = __uint_as_float(sr1[i]);
         }
         const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
-        auto visible = [&](int j) { return j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window); };
+        // visible keys of this row: one range of key indices; kmin / kmax relative to j0
+        const int kmax = pos - j0;
+        const int kmin = max(-j0, a.window > 0 ? pos - a.window + 1 - j0 : 0);
         float mo;
         {
           float y[32];
@@ -773,7 +775,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(so[i]);
           if (need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) y[i] = visible(j0 + 64 * (1 - wg) + i) ? y[i] : -INFINITY;
+            for (int i = 0; i < 32; ++i) {
+              const int k = 64 * (1 - wg) + i;
+              y[i] = (k >= kmin && k <= kmax) ? y[i] : -INFINITY;
+            }
           }
           mo = row_max(y);
           __syncwarp();
@@ -783,7 +788,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(so[i]);
           if (need_mask) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) y[i] = visible(j0 + 64 * (1 - wg) + 32 + i) ? y[i] : -INFINITY;
+            for (int i = 0; i < 32; ++i) {
+              const int k = 64 * (1 - wg) + 32 + i;
+              y[i] = (k >= kmin && k <= kmax) ? y[i] : -INFINITY;
+            }
           }
           mo = fmaxf(mo, row_max(y));
         }
@@ -792,7 +800,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         mbar_arrive(bar(B_S_READ + ((s - s2) & 1)));
         if (need_mask) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) x[i] = visible(j0 + 64 * wg + i) ? x[i] : -INFINITY;
+          for (int i = 0; i < 64; ++i) {
+            const int k = 64 * wg + i;
+            x[i] = (k >= kmin && k <= kmax) ? x[i] : -INFINITY;
+          }
         }
         update_max(fmaxf(row_max(x), mo) * cqk);
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;

@@ -321,12 +321,11 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
       const int j0 = p0 - BN * t;
       const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
       if (need_mask) {
+        // visible keys of this row are one range [kmin, kmax] of the tile
+        const int kmax = pos - j0;
+        const int kmin = max(-j0, a.window > 0 ? pos - a.window + 1 - j0 : 0);
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
-          const int j = j0 + k;
-          const bool vis = j <= pos && j >= 0 && (a.window <= 0 || pos - j < a.window);
-          x[k] = vis ? x[k] : -INFINITY;
-        }
+        for (int k = 0; k < 128; ++k) x[k] = (k >= kmin && k <= kmax) ? x[k] : -INFINITY;
       }
       const float mx = row_max(x) * cqk;
       float corr = 1.f;

@@ -70,8 +70,8 @@ relattn_status validate(const relattn_params *p, bool decode) {
 }
 
 relattn_status make_args(const relattn_params *p, KernelArgs *a) {
-  int *err = nullptr;
-  relattn_status st = device_state(nullptr, &err, nullptr);
+  int *err = nullptr, sms = 0;
+  relattn_status st = device_state(nullptr, &err, &sms);
   if (st != RELATTN_OK) return st;
   KernelArgs &x = *a;
   x = KernelArgs{};
@@ -106,6 +106,7 @@ relattn_status make_args(const relattn_params *p, KernelArgs *a) {
   x.split_chunk = 0;
   x.q_tiles = (p->max_seqlen_q + 127) / 128;
   x.row_blocks = 1;
+  x.sms = sms;
   return RELATTN_OK;
 }
 

@@ -7,26 +7,34 @@
 // Embedding":  x(i,j) = s(i) * (alpha q_i.k_j + [0 <= i-j < E] r_i . P[:, i-j]),
 // online softmax, PV.
 //
-// One CTA = 128 query rows (TMEM lane a <-> row a): prefill takes one query
-// head x 128 consecutive rows; decode takes 128 rows of the (token,
-// head-in-group) list of one kv head and one split of its keys.  Keys come in
+// A work item = 128 query rows (TMEM lane a <-> row a): prefill takes one
+// query head x 128 consecutive rows; decode takes 128 rows of the (token,
+// head-in-group) list of one kv head and one split of its keys.  Decode and
+// the one-launch prefill run one item per CTA; the bias band of the
+// two-launch prefill runs one CTA per SM that walks the items, its barrier
+// phases and stage rings running on from item to item, so the next item's
+// loads and first MMAs overlap the current item's epilogue.  Keys come in
 // 128-key tiles (one TMA stage), visited from the diagonal backwards.  Tiles
 // inside the relative-bias band are processed as two 64-key half steps (the
 // upper half first); the rest as one 128-key step.  Warp roles (12 warps,
 // one support and two softmax warps per SM sub-partition; the support warps
-// hand registers to the softmax warps: 64 vs 216 per thread):
+// hand registers to the softmax warps: 80 vs 208 per thread):
 //   warp 0      TMA producer (one thread) of K tiles (2-stage ring of 128
 //               keys), V tiles (3-stage ring) and P slices P[:, 64c..64c+64)
 //               (4 stages), in the order the MMA issuer consumes them; K and
 //               V stages are freed separately (K once its S MMAs are done, V
-//               after PV)
+//               after PV).  In the band-only prefill it also loads each
+//               item's q rows (into a K-ring slot ahead of the item's tiles)
+//               and r rows (into the r tile)
 //   warp 1      TMEM allocator; MMA issuer (one thread):  S = Q K^T (Q in
-//               TMEM), R_chunk = r P_slice (both operands from shared memory),
-//               O += P V (P in TMEM)
+//               TMEM; in the band-only prefill copied there from its K-ring
+//               slot with tcgen05.cp), R_chunk = r P_slice (both operands from
+//               shared memory), O += P V (P in TMEM)
 //   warps 2-3   idle
 //   warps 4-11  softmax, two warpgroups: row a is owned by one thread of each
 //               (TMEM lane a); warpgroup wg takes the lower / upper half of
-//               every step's keys.  They write the q / r rows, load S from
+//               every step's keys.  They write the q / r rows (unless the
+//               producer brings them), load S from
 //               TMEM, add the relative bias, mask edge tiles, agree on the
 //               running row max through shared memory, write P (bf16) back
 //               over S, rescale their half of O when the max grows by more
@@ -67,9 +75,9 @@ constexpr int HN = 64;           // keys per half step (bias band); also the r.P
 constexpr int K_STAGES = 2, V_STAGES = 3;
 constexpr int P_STAGES = 4;
 constexpr int NTHREADS = 384;
-// registers per thread: 168 at launch; the support warpgroup drops to 64 and
-// the two softmax warpgroups rise to 216 (4 x 32 x 64 + 8 x 32 x 216 <= 384 x 168)
-constexpr uint32_t kRegsSupport = 64, kRegsSoftmax = 216;
+// registers per thread: 168 at launch; the support warpgroup drops to 80 and
+// the two softmax warpgroups rise to 208 (4 x 32 x 80 + 8 x 32 x 208 <= 384 x 168)
+constexpr uint32_t kRegsSupport = 80, kRegsSoftmax = 208;
 static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= NTHREADS * 168, "register split");
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
@@ -96,7 +104,8 @@ constexpr int B_K_FULL = 0, B_K_EMPTY = B_K_FULL + K_STAGES, B_V_FULL = B_K_EMPT
               B_PV_SW = B_P_FULL + 4, B_PV_TAIL = B_PV_SW + 1, B_R_FULL = B_PV_TAIL + 2,
               B_R_FREE = B_R_FULL + 3, B_S_READ = B_R_FREE + 1, B_PV_F = B_S_READ + 2,
               B_P_HALF = B_PV_F + 4,
-              B_DRAIN = B_P_HALF + 4, B_XCH = B_DRAIN + 1, B_COUNT = B_XCH + 4;
+              B_DRAIN = B_P_HALF + 4, B_XCH = B_DRAIN + 1, B_RT_EMPTY = B_XCH + 4,
+              B_COUNT = B_RT_EMPTY + 1;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
 constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row exchange [2][2][128] f32
@@ -107,6 +116,10 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 struct TcArgs {
   KernelArgs a;
   int has_bias;
+  // prefill, bias band alone: the q and r rows of an item come by TMA (q
+  // into a K-ring slot, copied to TMEM by the MMA issuer; r straight into
+  // the r tile), so a CTA's next item starts without the softmax warps
+  int stage_tma;
 };
 
 __device__ __forceinline__ int floor_div64(int x) { return x >= 0 ? x >> 6 : -((63 - x) >> 6); }
@@ -150,12 +163,22 @@ __device__ __forceinline__ float row_max(const float (&x)[N]) {
   }
 }
 
+// One unit of work: 128 query rows and the key tiles they visit.
+struct Item {
+  int b, kv_head, row0, nrows, split, h_fixed;
+  int cq, ck, off, p0, p_last;
+  int ntiles, Dt0, span, nb_tiles, s2, nsteps;
+  int c_start, c_first, c_last;   // r.P chunks of the band (s2 > 0)
+};
+
 template <bool DECODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
                       const __grid_constant__ CUtensorMap map_k,
                       const __grid_constant__ CUtensorMap map_v,
-                      const __grid_constant__ CUtensorMap map_p) {
+                      const __grid_constant__ CUtensorMap map_p,
+                      const __grid_constant__ CUtensorMap map_q,
+                      const __grid_constant__ CUtensorMap map_r) {
   const KernelArgs &a = ta.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -166,81 +189,119 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ------------------------------------------------------------ work item
-  int b, kv_head, row0, nrows, split = 0, h_fixed = 0;
-  if constexpr (DECODE) {
-    split = blockIdx.x;
-    kv_head = blockIdx.y / a.row_blocks;
-    row0 = (blockIdx.y % a.row_blocks) * BM;
-    b = blockIdx.z;
-  } else {
-    h_fixed = blockIdx.y;
-    kv_head = h_fixed / a.group;
-    row0 = (a.q_tiles - 1 - blockIdx.x) * BM;   // longest-running tiles first
-    b = blockIdx.z;
-  }
-  const int cq = a.cu_q[b], ck = a.cu_k[b];
-  const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
-  if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) {
-    if (tid == 0) atomicOr(a.err, kDevErrSeqlens);
-    return;
-  }
-  nrows = min(BM, (DECODE ? Lq * a.group : Lq) - row0);
-  if (nrows <= 0) return;
-  const int off = Lk - Lq;
+  // ------------------------------------------------------------ work items
+  // Decode: one item per CTA (a split of one kv head's row block).  Prefill:
+  // items are (row tile, sequence, head), row tiles from the last (longest
+  // running) backwards; CTA x takes items x, x + gridDim.x, ...  Every role
+  // walks the same list, and the barrier phases run on across items.
+  Item I{};
+  const int n_items = DECODE ? 1 : a.q_tiles * a.Hq * a.batch;
+  const int item0 = DECODE ? 0 : (int)blockIdx.x, item_step = DECODE ? 1 : (int)gridDim.x;
+  // work of the items before the current one, for barrier phases / stages
+  int hb = 0, fb = 0, tb = 0, ob = 0;     // half steps, full steps, key tiles, r.P chunks
+  // K-ring slots: the item's q rows take one ahead of its key tiles (TMA staging)
+  const int q_slot = (!DECODE && ta.stage_tma) ? 1 : 0;
+  int kb = 0;
+  auto kslot = [&](int t) { return kb + q_slot + t; };
+  int n_it = 0, n_rt = 0;                   // items; items with a band (r tile)
+  int n_tail0 = 0, n_tail1 = 0, n_sw = 0;   // PV_TAIL[0/1] and PV_SW commits
   // row (local, clamped to the last valid one) -> token t and query head
   auto row_t = [&](int rl) {
-    const int x = row0 + min(rl, nrows - 1);
+    const int x = I.row0 + min(rl, I.nrows - 1);
     return DECODE ? x / a.group : x;
   };
   auto row_h = [&](int rl) {
-    const int x = row0 + min(rl, nrows - 1);
-    return DECODE ? kv_head * a.group + x % a.group : h_fixed;
+    const int x = I.row0 + min(rl, I.nrows - 1);
+    return DECODE ? I.kv_head * a.group + x % a.group : I.h_fixed;
   };
-  const int p0 = off + row_t(0), p_last = off + row_t(nrows - 1);
-  const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
-  // 128-key tiles from the diagonal backwards: tile t starts at key
-  // p0 - D(t); the rows sit at positions p0 + delta, 0 <= delta <= span
-  int ntiles, Dt0, span;
-  if constexpr (DECODE) {
-    const int kbase = j_lo & ~(BN - 1);
-    const int kbeg = kbase + split * a.split_chunk;
-    const int kend = min(p_last + 1, kbeg + a.split_chunk);
-    ntiles = kend > kbeg ? (kend - kbeg + BN - 1) / BN : 0;
-    Dt0 = p0 - (kbeg + (ntiles - 1) * BN);
-    span = p_last - p0;
-  } else {
-    Dt0 = 0;                                   // tile 0 = keys [p0, p0 + 127]
-    ntiles = (p0 - j_lo + BN - 1) / BN + 1;
-    span = BM - 1;   // padding rows reuse the pattern of full tiles
-  }
-  auto tile_D = [&](int t) { return Dt0 + BN * t; };
-  // band tiles (some distance < E) form a prefix of the tile order
-  int nb_tiles = 0;
-  if (ta.has_bias && ntiles > 0) {
-    const int lim = a.E + BN - 1;              // band iff D - 127 < E
-    nb_tiles = tile_D(ntiles - 1) < lim ? ntiles : max(0, (lim - Dt0 + BN - 1) / BN);
-    if (nb_tiles > ntiles) nb_tiles = ntiles;
-  }
-  // prefill split in two kernels: this one takes only the band, and leaves
-  // out / lse normalised over the band's keys for the main kernel to continue
-  if (!DECODE && a.band_only && nb_tiles > 0) ntiles = nb_tiles;
-  const int s2 = 2 * nb_tiles;                  // first full step
-  const int nsteps = s2 + (ntiles - nb_tiles);
-  auto step_tile = [&](int s) { return s < s2 ? s >> 1 : nb_tiles + (s - s2); };
-  auto step_kh = [&](int s) { return (s < s2 && (s & 1) == 0) ? HN : 0; };   // first key in the tile
+  auto tile_D = [&](int t) { return I.Dt0 + BN * t; };
+  auto step_tile = [&](int s) { return s < I.s2 ? s >> 1 : I.nb_tiles + (s - I.s2); };
+  auto step_kh = [&](int s) { return (s < I.s2 && (s & 1) == 0) ? HN : 0; };   // first key in the tile
   auto step_D = [&](int s) { return tile_D(step_tile(s)) - step_kh(s); };
-  // barrier / buffer of a step: half steps alternate 0,1; full steps 2,3
-  auto step_kind = [&](int s) { return s < s2 ? (s & 1) : 2 + ((s - s2) & 1); };
-  auto step_phase = [&](int s) { return s < s2 ? (s >> 1) & 1 : ((s - s2) >> 1) & 1; };
+  // barrier / buffer of a step: half steps alternate 0,1; full steps 2,3 (the
+  // half-step count of an item is even, so half steps keep their parity)
+  auto step_kind = [&](int s) { return s < I.s2 ? (s & 1) : 2 + ((fb + s - I.s2) & 1); };
+  auto step_phase = [&](int s) { return s < I.s2 ? ((hb + s) >> 1) & 1 : ((fb + s - I.s2) >> 1) & 1; };
+  // full-step index across items (S_READ / P_HALF / PV_F parity and phase)
+  auto full_idx = [&](int s) { return fb + s - I.s2; };
   // newest r.P chunk (64 distances) a half step needs: one more per half step
-  auto c_new = [&](int s) { return floor_div64(step_D(s) + span); };
-  const int c_first = s2 > 0 ? c_new(0) : -1;
-  const int c_last = s2 > 0 ? c_new(s2 - 1) : -1;
-  // first chunk computed: the oldest one step 0 reads (a decode split far from
-  // the diagonal starts deep in the band).  Chunk c uses ring slot / P stage /
-  // barrier phase counted from c_start.
-  const int c_start = s2 > 0 ? max(0, floor_div64(step_D(0) - (HN - 1))) : 0;
+  auto c_new = [&](int s) { return floor_div64(step_D(s) + I.span); };
+  // chunk c of the current item: ring slot / P stage / barrier phase index
+  auto chunk_idx = [&](int c) { return ob + (c - I.c_start); };
+  // 1 = work to do, 0 = nothing (row tile past the sequence, empty split),
+  // -1 = inconsistent sequence lengths (reported by the caller, item skipped)
+  auto load_item = [&](int idx) -> int {
+    if constexpr (DECODE) {
+      I.split = blockIdx.x;
+      I.kv_head = blockIdx.y / a.row_blocks;
+      I.row0 = (blockIdx.y % a.row_blocks) * BM;
+      I.b = blockIdx.z;
+      I.h_fixed = 0;
+    } else {
+      const int per_x = a.Hq * a.batch;
+      const int xi = idx / per_x, rem = idx - xi * per_x;
+      I.b = rem / a.Hq;
+      I.h_fixed = rem - I.b * a.Hq;
+      I.split = 0;
+      I.kv_head = I.h_fixed / a.group;
+      I.row0 = (a.q_tiles - 1 - xi) * BM;
+    }
+    I.cq = a.cu_q[I.b];
+    I.ck = a.cu_k[I.b];
+    const int Lq = a.cu_q[I.b + 1] - I.cq, Lk = a.cu_k[I.b + 1] - I.ck;
+    if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) return -1;
+    I.nrows = min(BM, (DECODE ? Lq * a.group : Lq) - I.row0);
+    if (I.nrows <= 0) return 0;
+    I.off = Lk - Lq;
+    I.p0 = I.off + row_t(0);
+    I.p_last = I.off + row_t(I.nrows - 1);
+    const int j_lo = a.window > 0 ? max(0, I.p0 - a.window + 1) : 0;
+    // 128-key tiles from the diagonal backwards: tile t starts at key
+    // p0 - D(t); the rows sit at positions p0 + delta, 0 <= delta <= span
+    if constexpr (DECODE) {
+      const int kbase = j_lo & ~(BN - 1);
+      const int kbeg = kbase + I.split * a.split_chunk;
+      const int kend = min(I.p_last + 1, kbeg + a.split_chunk);
+      I.ntiles = kend > kbeg ? (kend - kbeg + BN - 1) / BN : 0;
+      I.Dt0 = I.p0 - (kbeg + (I.ntiles - 1) * BN);
+      I.span = I.p_last - I.p0;
+    } else {
+      I.Dt0 = 0;                                   // tile 0 = keys [p0, p0 + 127]
+      I.ntiles = (I.p0 - j_lo + BN - 1) / BN + 1;
+      I.span = BM - 1;   // padding rows reuse the pattern of full tiles
+    }
+    // band tiles (some distance < E) form a prefix of the tile order
+    I.nb_tiles = 0;
+    if (ta.has_bias && I.ntiles > 0) {
+      const int lim = a.E + BN - 1;              // band iff D - 127 < E
+      I.nb_tiles = tile_D(I.ntiles - 1) < lim ? I.ntiles : max(0, (lim - I.Dt0 + BN - 1) / BN);
+      if (I.nb_tiles > I.ntiles) I.nb_tiles = I.ntiles;
+    }
+    // prefill split in two kernels: this one takes only the band, and leaves
+    // out / lse normalised over the band's keys for the main kernel to continue
+    if (!DECODE && a.band_only && I.nb_tiles > 0) I.ntiles = I.nb_tiles;
+    I.s2 = 2 * I.nb_tiles;                         // first full step
+    I.nsteps = I.s2 + (I.ntiles - I.nb_tiles);
+    I.c_first = I.s2 > 0 ? c_new(0) : -1;
+    I.c_last = I.s2 > 0 ? c_new(I.s2 - 1) : -1;
+    // first chunk computed: the oldest one step 0 reads (a decode split far
+    // from the diagonal starts deep in the band)
+    I.c_start = I.s2 > 0 ? max(0, floor_div64(step_D(0) - (HN - 1))) : 0;
+    return 1;
+  };
+  // after an item: advance the cross-item counters (every role, same values)
+  auto finish_item = [&]() {
+    hb += I.s2;
+    fb += I.nsteps - I.s2;
+    tb += I.ntiles;
+    kb += I.ntiles + q_slot;
+    ob += I.s2 > 0 ? I.c_last - I.c_start + 1 : 0;
+    n_tail0 += I.nsteps >= 2;
+    n_tail1 += I.nsteps >= 1;
+    n_sw += (I.s2 > 0 && I.s2 < I.nsteps);
+    n_rt += I.s2 > 0;
+    ++n_it;
+  };
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
@@ -256,7 +317,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       mbar_init(bar(B_PS_FULL + i), 1);
       mbar_init(bar(B_PS_EMPTY + i), 1);
     }
-    mbar_init(bar(B_RT_FULL), 256);
+    mbar_init(bar(B_RT_FULL), q_slot ? 1 : 256);
+    mbar_init(bar(B_RT_EMPTY), 1);
     mbar_init(bar(B_Q_READY), 256);
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(B_S_FULL + i), 1);
@@ -285,13 +347,17 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     prefetch_tmap(&map_k);
     prefetch_tmap(&map_v);
     if (ta.has_bias) prefetch_tmap(&map_p);
+    if (q_slot) {
+      prefetch_tmap(&map_q);
+      prefetch_tmap(&map_r);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
   // TMA copies issued by the producer thread (to drain them if the CTA gives up)
-  int issued_k = 0, issued_v = 0, issued_p = 0;
+  int issued_k = 0, issued_v = 0, issued_p = 0, issued_rt = 0;
   if (warp < 4) {
   regs_dec<kRegsSupport>();
   if (warp == 0) {
@@ -301,43 +367,72 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     // ever depends on work issued before it.  A P slice is P[0:r_dim, 64c ..
     // 64c + 64) in the 128-byte-swizzled layout (columns past E read as 0;
     // rows r_dim .. rd_pad stay at the zeros the softmax warps put there).
+    // The stage rings run on across items, so the next item's tiles load
+    // while the current one finishes.
     if (lane == 0) {
       const uint32_t p_bytes = 128u * (uint32_t)a.rd;
       int kst = 0, kph = 0, vst = 0, vph = 0;
-      int c_next = c_start;
       bool run = true;
-      for (int t = 0; t < ntiles && run && !*abort_flag; ++t) {
-        if (t < nb_tiles) {
-          const int c_need = c_new(2 * t + 1);   // newest chunk of the tile's second half step
-          for (; c_next <= c_need; ++c_next) {
-            const int o = c_next - c_start, st = o % P_STAGES;
-            if (o >= P_STAGES && !(run = mbar_wait(bar(B_PS_EMPTY + st), ((o / P_STAGES) - 1) & 1, abort_flag, 3)))
-              break;
-            mbar_arrive_expect_tx(bar(B_PS_FULL + st), p_bytes);
-            tma_load_2d(sb + SM_PS + st * 8192, &map_p, HN * c_next, 0, bar(B_PS_FULL + st));
-            issued_p = c_next - c_start + 1;
+      for (int idx = item0; idx < n_items && run; idx += item_step) {
+        const int li = load_item(idx);
+        if (li < 0) atomicOr(a.err, kDevErrSeqlens);
+        if (li <= 0) continue;
+        if (q_slot) {
+          // r rows -> r tile, once the previous item's r.P chunks are done
+          if (I.s2 > 0) {
+            if (n_rt > 0 && !(run = mbar_wait(bar(B_RT_EMPTY), (n_rt - 1) & 1, abort_flag, 20))) break;
+            mbar_arrive_expect_tx(bar(B_RT_FULL), 16384u);
+            tma_load_3d(sb + SM_RT, &map_r, 0, I.h_fixed, I.cq + I.row0, bar(B_RT_FULL));
+            issued_rt = n_rt + 1;
           }
-          if (!run) break;
-        }
-        const int key = ck + p0 - tile_D(t);   // may be < 0: the tile reads zeros there
-        if (t >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
-        if (t != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
+          // q rows -> the item's first K-ring slot (rows past the sequence
+          // read other rows or zeros: padding rows, never stored)
+          if (kb >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
           const uint32_t dst = sb + SM_K + kst * KV_STAGE_BYTES;
           mbar_arrive_expect_tx(bar(B_K_FULL + kst), KV_STAGE_BYTES);
-          tma_load_3d(dst, &map_k, 0, kv_head, key, bar(B_K_FULL + kst));
-          tma_load_3d(dst + KV_BOX_BYTES, &map_k, 64, kv_head, key, bar(B_K_FULL + kst));
+          tma_load_3d(dst, &map_q, 0, I.h_fixed, I.cq + I.row0, bar(B_K_FULL + kst));
+          tma_load_3d(dst + KV_BOX_BYTES, &map_q, 64, I.h_fixed, I.cq + I.row0, bar(B_K_FULL + kst));
+          issued_k = kb + 1;
+          if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
         }
-        issued_k = t + 1;
-        if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
-        if (t >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
-        {
-          const uint32_t dst = sb + SM_V + vst * KV_STAGE_BYTES;
-          mbar_arrive_expect_tx(bar(B_V_FULL + vst), KV_STAGE_BYTES);
-          tma_load_3d(dst, &map_v, 0, kv_head, key, bar(B_V_FULL + vst));
-          tma_load_3d(dst + KV_BOX_BYTES, &map_v, 64, kv_head, key, bar(B_V_FULL + vst));
-          issued_v = t + 1;
-          if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
+        int c_next = I.c_start;
+        for (int t = 0; t < I.ntiles && run && !*abort_flag; ++t) {
+          if (t < I.nb_tiles) {
+            const int c_need = c_new(2 * t + 1);   // newest chunk of the tile's second half step
+            for (; c_next <= c_need; ++c_next) {
+              const int o = chunk_idx(c_next), st = o % P_STAGES;
+              if (o >= P_STAGES &&
+                  !(run = mbar_wait(bar(B_PS_EMPTY + st), ((o / P_STAGES) - 1) & 1, abort_flag, 3)))
+                break;
+              mbar_arrive_expect_tx(bar(B_PS_FULL + st), p_bytes);
+              tma_load_2d(sb + SM_PS + st * 8192, &map_p, HN * c_next, 0, bar(B_PS_FULL + st));
+              issued_p = o + 1;
+            }
+            if (!run) break;
+          }
+          const int tg = tb + t, kg = kslot(t);        // V / K ring index across items
+          const int key = I.ck + I.p0 - tile_D(t);     // may be < 0: the tile reads zeros there
+          if (kg >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
+          if (kg != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
+            const uint32_t dst = sb + SM_K + kst * KV_STAGE_BYTES;
+            mbar_arrive_expect_tx(bar(B_K_FULL + kst), KV_STAGE_BYTES);
+            tma_load_3d(dst, &map_k, 0, I.kv_head, key, bar(B_K_FULL + kst));
+            tma_load_3d(dst + KV_BOX_BYTES, &map_k, 64, I.kv_head, key, bar(B_K_FULL + kst));
+          }
+          issued_k = kg + 1;
+          if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
+          if (tg >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
+          {
+            const uint32_t dst = sb + SM_V + vst * KV_STAGE_BYTES;
+            mbar_arrive_expect_tx(bar(B_V_FULL + vst), KV_STAGE_BYTES);
+            tma_load_3d(dst, &map_v, 0, I.kv_head, key, bar(B_V_FULL + vst));
+            tma_load_3d(dst + KV_BOX_BYTES, &map_v, 64, I.kv_head, key, bar(B_V_FULL + vst));
+            issued_v = tg + 1;
+            if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
+          }
         }
+        if (*abort_flag) run = false;
+        finish_item();
       }
     }
     __syncwarp();
@@ -356,15 +451,14 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       const uint64_t vd0 = smem_desc_sw128(sb + SM_V, KV_BOX_BYTES, 1024);
       const uint64_t rd0 = smem_desc_sw128(sb + SM_RT, 16, 1024);
       const uint64_t pd0 = smem_desc_sw128(sb + SM_PS, 8192, 1024);
-      bool ok = mbar_wait(bar(B_Q_READY), 0, abort_flag, 6);
-      tc_fence_after();
+      bool ok = true;
       bool rt_ready = false;
       auto issue_r = [&](int c) -> bool {
         if (!rt_ready) {
-          if (!mbar_wait(bar(B_RT_FULL), 0, abort_flag, 7)) return false;
+          if (!mbar_wait(bar(B_RT_FULL), n_rt & 1, abort_flag, 7)) return false;
           rt_ready = true;
         }
-        const int o = c - c_start;
+        const int o = chunk_idx(c);
         const int st = o % P_STAGES;
         if (!mbar_wait(bar(B_PS_FULL + st), (o / P_STAGES) & 1, abort_flag, 8)) return false;
         tc_fence_after();
@@ -374,17 +468,19 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         if (r_ksteps > 1) mma_ss_c<1>(d, rd0 + 2, pd + 128, id_r);
         if (r_ksteps > 2) mma_ss_c<1>(d, rd0 + 4, pd + 256, id_r);
         if (r_ksteps > 3) mma_ss_c<1>(d, rd0 + 6, pd + 384, id_r);
-        mma_commit(bar(B_R_FULL + o % 3));   // its landing also frees P stage st (softmax arrives)
+        mma_commit(bar(B_R_FULL + o % 3));
+        // the item's last chunk: once it lands the r tile may take the next item's rows
+        if (q_slot && c == I.c_last) mma_commit(bar(B_RT_EMPTY));   // its landing also frees P stage st (softmax arrives)
         return true;
       };
       auto issue_s = [&](int s) -> bool {
-        const int t = step_tile(s), st = t % K_STAGES;
+        const int t = kslot(step_tile(s)), st = t % K_STAGES;
         if (!mbar_wait(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9)) return false;
         tc_fence_after();
         const uint32_t qa = tmem + TM_Q;
         const uint64_t kd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
         // k-step k: dims 16k..16k+15 -> box k/4, 32 bytes per step inside the row
-        if (s < s2) {
+        if (s < I.s2) {
           const uint32_t d = tmem + TM_H + 64u * (uint32_t)(s & 1);
           mma_ts_c<0>(d, qa + 0, kd + 0, id_h);
           mma_ts_c<1>(d, qa + 8, kd + 2, id_h);
@@ -395,7 +491,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           mma_ts_c<1>(d, qa + 48, kd + 1028, id_h);
           mma_ts_c<1>(d, qa + 56, kd + 1030, id_h);
         } else {
-          const uint32_t d = tmem + TM_S + 128u * (uint32_t)((s - s2) & 1);
+          const uint32_t d = tmem + TM_S + 128u * (uint32_t)(full_idx(s) & 1);
           mma_ts_c<0>(d, qa + 0, kd + 0, id_f);
           mma_ts_c<1>(d, qa + 8, kd + 2, id_f);
           mma_ts_c<1>(d, qa + 16, kd + 4, id_f);
@@ -413,12 +509,12 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       };
       // O += P V; k-step k = 16 keys = 2048 bytes of the MN-major V tile
       auto issue_pv = [&](int s) -> bool {
-        const int t = step_tile(s), st = t % V_STAGES;
+        const int t = tb + step_tile(s), st = t % V_STAGES;
         if (!mbar_wait(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5)) return false;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
         const uint32_t o = tmem + TM_O;
-        if (s < s2) {
+        if (s < I.s2) {
           const uint32_t pa = tmem + TM_H + 64u * (uint32_t)(s & 1);
           if (s > 0) mma_ts_c<1>(o, pa + 0, vd + 0, id_o);
           else mma_ts_c<0>(o, pa + 0, vd + 0, id_o);
@@ -428,7 +524,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         } else {
           // two halves, one per warpgroup's P (keys 0..63 / 64..127), each
           // issued as soon as that warpgroup's P is in
-          const int par = (s - s2) & 1, ph = ((s - s2) >> 1) & 1;
+          const int par = full_idx(s) & 1, ph = (full_idx(s) >> 1) & 1;
           for (int h = 0; h < 2; ++h) {
             if (!mbar_wait(bar(B_P_HALF + 2 * h + par), ph, abort_flag, 11)) return false;
             tc_fence_after();
@@ -448,44 +544,74 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         // such S follows without waiting for P: the last two steps, and the step
         // before the first full step (whose S is issued after the last half
         // step's PV).  Full steps commit PV_F above.
-        if (s == nsteps - 2) mma_commit(bar(B_PV_TAIL));
-        if (s == nsteps - 1) mma_commit(bar(B_PV_TAIL + 1));
-        if (s2 < nsteps && s == s2 - 2) mma_commit(bar(B_PV_SW));
+        if (s == I.nsteps - 2) mma_commit(bar(B_PV_TAIL));
+        if (s == I.nsteps - 1) mma_commit(bar(B_PV_TAIL + 1));
+        if (I.s2 < I.nsteps && s == I.s2 - 2) mma_commit(bar(B_PV_SW));
         return true;
       };
-      if (ok && s2 > 0)
-        for (int c = c_start; c <= c_first && ok; ++c) ok = issue_r(c);
-      if (ok && nsteps > 0) ok = issue_s(0);   // an empty decode split issues nothing
-      if (ok && s2 == 0 && nsteps > 1) ok = issue_s(1);   // full steps keep two S in flight
-      for (int s = 0; s < nsteps && ok; ++s) {
-        if (s < s2) {
+      for (int idx = item0; idx < n_items && ok; idx += item_step) {
+      if (load_item(idx) <= 0) continue;
+      // the item's q (TMEM) and r (shared) rows are in: everything of the
+      // previous item that read them has finished (its S / R landings were
+      // awaited by the softmax warps first)
+      if (q_slot) {
+        // the item's q rows: K-ring slot -> TMEM (after every S MMA of the
+        // previous item, in issue order), then the slot is free again
+        const int st = kb % K_STAGES;
+        ok = mbar_wait(bar(B_K_FULL + st), (kb / K_STAGES) & 1, abort_flag, 6);
+        tc_fence_after();
+        const uint64_t qd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
+        if (ok) {
+          tmem_cp_128x256b(tmem + TM_Q + 0, qd + 0);
+          tmem_cp_128x256b(tmem + TM_Q + 8, qd + 2);
+          tmem_cp_128x256b(tmem + TM_Q + 16, qd + 4);
+          tmem_cp_128x256b(tmem + TM_Q + 24, qd + 6);
+          tmem_cp_128x256b(tmem + TM_Q + 32, qd + 1024);
+          tmem_cp_128x256b(tmem + TM_Q + 40, qd + 1026);
+          tmem_cp_128x256b(tmem + TM_Q + 48, qd + 1028);
+          tmem_cp_128x256b(tmem + TM_Q + 56, qd + 1030);
+          mma_commit(bar(B_K_EMPTY + st));
+        }
+      } else {
+        ok = mbar_wait(bar(B_Q_READY), n_it & 1, abort_flag, 6);
+        tc_fence_after();
+      }
+      rt_ready = false;
+      if (ok && I.s2 > 0)
+        for (int c = I.c_start; c <= I.c_first && ok; ++c) ok = issue_r(c);
+      if (ok && I.nsteps > 0) ok = issue_s(0);   // an empty decode split issues nothing
+      if (ok && I.s2 == 0 && I.nsteps > 1) ok = issue_s(1);   // full steps keep two S in flight
+      for (int s = 0; s < I.nsteps && ok; ++s) {
+        if (s < I.s2) {
           // ---- half step: S(s+1) ahead of PV(s).  The first full steps' S
           // buffers overlap the half-step buffers and the R ring: they are
           // issued only once the last half step's P is in.
-          const bool switch_next = (s + 1 == s2) && (s2 < nsteps);
-          if (!switch_next && s + 1 < nsteps && !(ok = issue_s(s + 1))) break;
-          if (s + 1 < s2) {
+          const bool switch_next = (s + 1 == I.s2) && (I.s2 < I.nsteps);
+          if (!switch_next && s + 1 < I.nsteps && !(ok = issue_s(s + 1))) break;
+          if (s + 1 < I.s2) {
             const int c = c_new(s + 1);
-            if (!(ok = mbar_wait(bar(B_R_FREE), s & 1, abort_flag, 10))) break;
-            if (c >= c_start && !(ok = issue_r(c))) break;
+            if (!(ok = mbar_wait(bar(B_R_FREE), (hb + s) & 1, abort_flag, 10))) break;
+            if (c >= I.c_start && !(ok = issue_r(c))) break;
           }
           if (!(ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11))) break;
           tc_fence_after();
           if (!(ok = issue_pv(s))) break;
           if (switch_next) {
             if (!(ok = issue_s(s + 1))) break;
-            if (s + 2 < nsteps && !(ok = issue_s(s + 2))) break;
+            if (s + 2 < I.nsteps && !(ok = issue_s(s + 2))) break;
           }
         } else {
           // ---- full step: S(s+2) into the buffer of S(s) as soon as the
           // softmax has read it, then PV(s)
-          if (s + 2 < nsteps) {
-            if (!(ok = mbar_wait(bar(B_S_READ + ((s - s2) & 1)), ((s - s2) >> 1) & 1, abort_flag, 19))) break;
+          if (s + 2 < I.nsteps) {
+            if (!(ok = mbar_wait(bar(B_S_READ + (full_idx(s) & 1)), (full_idx(s) >> 1) & 1, abort_flag, 19))) break;
             tc_fence_after();
             if (!(ok = issue_s(s + 2))) break;
           }
           if (!(ok = issue_pv(s))) break;   // waits for each warpgroup's P half
         }
+      }
+      finish_item();
       }
       // drain: every MMA issued above has finished before TMEM is released
       mma_commit(bar(B_DRAIN));
@@ -506,99 +632,118 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     const bool leader = warp == 4 && lane == 0;  // releases K / V / P stages
     const int a_row = 32 * wq + lane;            // row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    const int t_row = row_t(a_row), h_row = row_h(a_row);
-    // position of this row; prefill padding rows (a_row >= nrows) continue the
-    // diagonal pattern and only compute garbage that is never stored
-    const int pos = DECODE ? off + t_row : p0 + a_row;
-    const int delta = pos - p0;                  // 0 .. span
-    const int delta_w = DECODE ? off + row_t(32 * wq) - p0 : 32 * wq;   // first row of the warp
-    const float sc = log_scale(min(pos, p_last), a.inv_ln_base);
     // scores are scaled by cqk > 0: a negative alpha flips the sign of q
     // instead (exact in bf16), so a row max of raw scores is a max of logits
     const bool q_neg = a.alpha_log2e < 0.f;
-    const float cqk = fmaxf(fabsf(a.alpha_log2e) * sc, 1e-30f), cbias = kLog2e * sc;
-    // band steps form t = |alpha| S + bias and apply cbias inside the exponent
-    const float qk_over_bias = cqk / cbias;
     float *xbuf = reinterpret_cast<float *>(smem + SM_XCH);   // [2 parity][2 wg][128]
-
-    // q row half -> TMEM columns [32 wg, 32 wg + 32) (bf16 pairs)
-    {
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-          a.q + ((size_t)(cq + t_row) * a.Hq + h_row) * kHeadDim + 64 * wg);
-      uint32_t r[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 v = src[i];
-        r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-      }
-      if (q_neg) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] ^= 0x80008000u;
-      }
-      __syncwarp();
-      tmem_st32(tmem + lane_base + TM_Q + 32u * wg, r);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(B_Q_READY));
-    }
-    // r row half -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
-    if (s2 > 0) {
-      const __nv_bfloat16 *rsrc = a.r + ((size_t)(cq + t_row) * a.Hq + h_row) * a.rd;
-      uint8_t *rrow = smem + SM_RT + (a_row >> 3) * 1024 + (a_row & 7) * 128;
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = 4 * wg + jj;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (8 * j < a.rd) v = *reinterpret_cast<const uint4 *>(rsrc + 8 * j);
-        *reinterpret_cast<uint4 *>(rrow + ((j ^ (a_row & 7)) << 4)) = v;
-      }
-      // P-slice rows r_dim .. rd_pad of every stage are zero (the TMA box
-      // covers r_dim rows); written once, before the first R MMA
-      const int zero_chunks = (a.rd_pad - a.rd) * 8 * P_STAGES;
-      for (int i = a_row + 128 * wg; i < zero_chunks; i += 256) {
-        const int st = i / ((a.rd_pad - a.rd) * 8), rem = i % ((a.rd_pad - a.rd) * 8);
-        const int ch = a.rd + (rem >> 3), j = rem & 7;
-        *reinterpret_cast<uint4 *>(smem + SM_PS + st * 8192 + (ch >> 3) * 1024 + (ch & 7) * 128 + j * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(B_RT_FULL));
-    }
-
     // every lane of a softmax warp takes the same branch after a wait, so the
     // warp-collective tcgen05 loads / stores that follow see a converged warp
     auto warp_wait = [&](uint32_t br, uint32_t parity, int site) -> bool {
       const bool r = mbar_wait(br, parity, abort_flag, site);
       return __all_sync(0xffffffffu, r);
     };
-    // TMEM address of distances d0 .. d0+31; valid for chunks >= c_start
-    auto r_addr = [&](int d0) {
-      return tmem + lane_base + TM_R + 64u * (uint32_t)(((d0 >> 6) - c_start) % 3) + (uint32_t)(d0 & 63);
-    };
-    const int d_min = HN * c_start;   // smaller distances were never computed (not needed)
-    // combine this thread's max with the other warpgroup's for the same row
-    // (buffer and barrier phase by step parity)
-    auto exchange = [&](int s, float v, bool &okx) -> float {
-      float *xb = xbuf + (s & 1) * 256;
+    // combine this thread's value with the other warpgroup's for the same row
+    // (buffer and barrier phase by the parity of the exchange count)
+    int n_xch = 0;
+    auto exchange = [&](float v, bool &okx) -> float {
+      float *xb = xbuf + (n_xch & 1) * 256;
       xb[wg * 128 + a_row] = v;
       mbar_arrive(bar(B_XCH + wq));
-      okx = warp_wait(bar(B_XCH + wq), s & 1, 18);
+      okx = warp_wait(bar(B_XCH + wq), n_xch & 1, 18);
+      ++n_xch;
       return xb[(1 - wg) * 128 + a_row];
     };
-    float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int s = 0; s < nsteps; ++s) {
+    int idx = item0;
+    // the next item with work (every role walks the same list)
+    auto next_item = [&]() -> bool {
+      for (; idx < n_items; idx += item_step)
+        if (load_item(idx) > 0) {
+          idx += item_step;
+          return true;
+        }
+      return false;
+    };
+    // the current item's q and r rows; once they are in, the MMA issuer may
+    // start the item
+    auto stage_item = [&]() {
+      const int t_row = row_t(a_row), h_row = row_h(a_row);
+      // q row half -> TMEM columns [32 wg, 32 wg + 32) (bf16 pairs)
+      {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            a.q + ((size_t)(I.cq + t_row) * a.Hq + h_row) * kHeadDim + 64 * wg);
+        uint32_t r[32];
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = src[i];
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        if (q_neg) {
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] ^= 0x80008000u;
+        }
+        __syncwarp();
+        tmem_st32(tmem + lane_base + TM_Q + 32u * wg, r);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_Q_READY));
+      }
+      // r row half -> shared r tile (row a, 128-byte swizzle; zero past r_dim)
+      if (I.s2 > 0) {
+        const __nv_bfloat16 *rsrc = a.r + ((size_t)(I.cq + t_row) * a.Hq + h_row) * a.rd;
+        uint8_t *rrow = smem + SM_RT + (a_row >> 3) * 1024 + (a_row & 7) * 128;
+  #pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * wg + jj;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (8 * j < a.rd) v = *reinterpret_cast<const uint4 *>(rsrc + 8 * j);
+          *reinterpret_cast<uint4 *>(rrow + ((j ^ (a_row & 7)) << 4)) = v;
+        }
+        // P-slice rows r_dim .. rd_pad of every stage are zero (the TMA box
+        // covers r_dim rows); written once, before the first R MMA
+        const int zero_chunks = n_rt == 0 ? (a.rd_pad - a.rd) * 8 * P_STAGES : 0;
+        for (int i = a_row + 128 * wg; i < zero_chunks; i += 256) {
+          const int st = i / ((a.rd_pad - a.rd) * 8), rem = i % ((a.rd_pad - a.rd) * 8);
+          const int ch = a.rd + (rem >> 3), j = rem & 7;
+          *reinterpret_cast<uint4 *>(smem + SM_PS + st * 8192 + (ch >> 3) * 1024 + (ch & 7) * 128 + j * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(B_RT_FULL));
+      }
+    };
+    bool have = next_item();
+    if (have && !q_slot) stage_item();
+    while (have && ok) {
+    const int t_row = row_t(a_row), h_row = row_h(a_row);
+    // position of this row; prefill padding rows (a_row >= nrows) continue the
+    // diagonal pattern and only compute garbage that is never stored
+    const int pos = DECODE ? I.off + t_row : I.p0 + a_row;
+    const int delta = pos - I.p0;                // 0 .. span
+    const int delta_w = DECODE ? I.off + row_t(32 * wq) - I.p0 : 32 * wq;   // first row of the warp
+    const float sc = log_scale(min(pos, I.p_last), a.inv_ln_base);
+    const float cqk = fmaxf(fabsf(a.alpha_log2e) * sc, 1e-30f), cbias = kLog2e * sc;
+    // band steps form t = |alpha| S + bias and apply cbias inside the exponent
+    const float qk_over_bias = cqk / cbias;
+
+    // TMEM address of distances d0 .. d0+31; valid for chunks >= c_start
+    auto r_addr = [&](int d0) {
+      return tmem + lane_base + TM_R + 64u * (uint32_t)(chunk_idx(d0 >> 6) % 3) + (uint32_t)(d0 & 63);
+    };
+    const int d_min = HN * I.c_start;   // smaller distances were never computed (not needed)
+    float m_ref = -INFINITY, l = 0.f;
+    for (int s = 0; s < I.nsteps; ++s) {
       if (!(ok = warp_wait(bar(B_S_FULL + step_kind(s)), step_phase(s), 13))) break;
       if (leader) {
         // S(s) landed: the K stage of its tile is read (last S of the tile)
-        if (step_kh(s) == 0) mbar_arrive(bar(B_K_EMPTY + step_tile(s) % K_STAGES));
+        if (step_kh(s) == 0) mbar_arrive(bar(B_K_EMPTY + kslot(step_tile(s)) % K_STAGES));
         // (S(s) is issued after PV(s-2) while s - 2 is a half step; full steps
         // release their V stage after waiting for PV_F instead)
-        if (s >= 2 && s - 2 < s2 && step_kh(s - 2) == 0)
-          mbar_arrive(bar(B_V_EMPTY + step_tile(s - 2) % V_STAGES));
+        if (s >= 2 && s - 2 < I.s2 && step_kh(s - 2) == 0)
+          mbar_arrive(bar(B_V_EMPTY + (tb + step_tile(s - 2)) % V_STAGES));
       }
       const int D = step_D(s);
-      const int j0 = p0 - D;                     // first key of this step
+      const int j0 = I.p0 - D;                   // first key of this step
       float corr = 1.f;
       bool rescale_o = false;
       // running-max update shared by both step shapes
@@ -611,21 +756,21 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           m_ref = m_new;
         }
       };
-      if (s < s2) {
+      if (s < I.s2) {
         // ---------------- half step: 32 keys per thread, relative bias
         const uint32_t sbuf = tmem + lane_base + TM_H + 64u * (uint32_t)(s & 1);
         // the newest chunk this step needs (older ones were awaited before)
         // (chunk c landed: its P stage may be refilled)
         if (s == 0) {
-          for (int c = c_start; c <= c_first && ok; ++c) {
-            ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 14);
-            if (ok && leader) mbar_arrive(bar(B_PS_EMPTY + (c - c_start) % P_STAGES));
+          for (int c = I.c_start; c <= I.c_first && ok; ++c) {
+            ok = warp_wait(bar(B_R_FULL + chunk_idx(c) % 3), (chunk_idx(c) / 3) & 1, 14);
+            if (ok && leader) mbar_arrive(bar(B_PS_EMPTY + chunk_idx(c) % P_STAGES));
           }
         } else {
           const int c = c_new(s);
-          if (c >= c_start) {
-            ok = warp_wait(bar(B_R_FULL + (c - c_start) % 3), ((c - c_start) / 3) & 1, 15);
-            if (ok && leader) mbar_arrive(bar(B_PS_EMPTY + (c - c_start) % P_STAGES));
+          if (c >= I.c_start) {
+            ok = warp_wait(bar(B_R_FULL + chunk_idx(c) % 3), (chunk_idx(c) / 3) & 1, 15);
+            if (ok && leader) mbar_arrive(bar(B_PS_EMPTY + chunk_idx(c) % P_STAGES));
           }
         }
         if (!ok) break;
@@ -722,7 +867,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             ffma2(x[u], x[u + 1], __uint_as_float(sr[u]), __uint_as_float(sr[u + 1]), qk_over_bias,
                   qk_over_bias, zz[u], zz[u + 1]);
         }
-        const bool need_mask = (j0 + HN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+        const bool need_mask =
+            (j0 + HN - 1 > I.p0) || (a.window > 0 && j0 < I.p_last - a.window + 1) || (j0 < 0);
         if (need_mask) {
           // visible keys of this row: one range [kmin, kmax] of this thread's keys
           const int jb = j0 + 32 * wg;
@@ -733,7 +879,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         }
         // x holds t = |alpha| S + bias; the logit in log2 units is t * cbias
         const float mloc = row_max(x) * cbias;
-        const float mo = exchange(s, mloc, ok);
+        const float mo = exchange(mloc, ok);
         if (!ok) break;
         update_max(fmaxf(mloc, mo));
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
@@ -748,7 +894,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         // two warpgroups never meet.  Once S(s) is read, the MMA issuer may
         // compute S(s+2) into its buffer; P goes to the separate P buffer as
         // soon as PV(s-1) has consumed the previous P.
-        const uint32_t sbuf = tmem + lane_base + TM_S + 128u * (uint32_t)((s - s2) & 1);
+        const uint32_t sbuf = tmem + lane_base + TM_S + 128u * (uint32_t)(full_idx(s) & 1);
         tc_fence_after();
         uint32_t sr0[32], sr1[32], so[32];
         __syncwarp();
@@ -764,7 +910,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           x[i] = __uint_as_float(sr0[i]);
           x[32 + i] = __uint_as_float(sr1[i]);
         }
-        const bool need_mask = (j0 + BN - 1 > p0) || (a.window > 0 && j0 < p_last - a.window + 1) || (j0 < 0);
+        const bool need_mask =
+            (j0 + BN - 1 > I.p0) || (a.window > 0 && j0 < I.p_last - a.window + 1) || (j0 < 0);
         // visible keys of this row: one range of key indices; kmin / kmax relative to j0
         const int kmax = pos - j0;
         const int kmin = max(-j0, a.window > 0 ? pos - a.window + 1 - j0 : 0);
@@ -797,7 +944,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         }
         // this thread has read all of S(s): its buffer may take S(s+2)
         tc_fence_before();
-        mbar_arrive(bar(B_S_READ + ((s - s2) & 1)));
+        mbar_arrive(bar(B_S_READ + (full_idx(s) & 1)));
         if (need_mask) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
@@ -809,11 +956,13 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         uint32_t pk[32];
         l += exp_pack_raw(x, cqk, m_use, pk);
-        if (s > s2) {
+        if (s > I.s2) {
           // this warpgroup's half of PV(s-1) has consumed its half of the P
           // buffer; the second half (issued last) also frees the V stage
-          if (!(ok = warp_wait(bar(B_PV_F + 2 * wg + ((s - 1 - s2) & 1)), ((s - 1 - s2) >> 1) & 1, 18))) break;
-          if (wg == 1 && warp == 8 && lane == 0) mbar_arrive(bar(B_V_EMPTY + step_tile(s - 1) % V_STAGES));
+          if (!(ok = warp_wait(bar(B_PV_F + 2 * wg + (full_idx(s - 1) & 1)), (full_idx(s - 1) >> 1) & 1, 18)))
+            break;
+          if (wg == 1 && warp == 8 && lane == 0)
+            mbar_arrive(bar(B_V_EMPTY + (tb + step_tile(s - 1)) % V_STAGES));
         }
         tc_fence_after();
         __syncwarp();
@@ -829,14 +978,14 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       // TMEM loads / stores are warp-collective: the whole warp rescales its 32
       // rows when any of them needs it (rows that do not are scaled by 1)
       if (__any_sync(0xffffffffu, rescale_o)) {
-        if (s < s2) {
-          if (s + 1 >= nsteps) ok = warp_wait(bar(B_PV_TAIL), 0, 16);       // after PV(nsteps - 2)
-          else if (s + 1 == s2) ok = warp_wait(bar(B_PV_SW), 0, 16);        // after PV(s2 - 2)
+        if (s < I.s2) {
+          if (s + 1 >= I.nsteps) ok = warp_wait(bar(B_PV_TAIL), n_tail0 & 1, 16);   // after PV(nsteps - 2)
+          else if (s + 1 == I.s2) ok = warp_wait(bar(B_PV_SW), n_sw & 1, 16);       // after PV(s2 - 2)
           else ok = warp_wait(bar(B_S_FULL + step_kind(s + 1)), step_phase(s + 1), 16);
           if (!ok) break;
-        } else if (s > s2 && wg == 0) {
+        } else if (s > I.s2 && wg == 0) {
           // both halves of PV(s-1) write every O column: wait for the second
-          if (!(ok = warp_wait(bar(B_PV_F + 2 + ((s - 1 - s2) & 1)), ((s - 1 - s2) >> 1) & 1, 16))) break;
+          if (!(ok = warp_wait(bar(B_PV_F + 2 + (full_idx(s - 1) & 1)), (full_idx(s - 1) >> 1) & 1, 16))) break;
         }
         tc_fence_after();
         const float cf = rescale_o ? corr : 1.f;
@@ -855,28 +1004,38 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       }
       tmem_wait_st();
       tc_fence_before();
-      if (s < s2) mbar_arrive(bar(B_P_FULL + step_kind(s)));
-      else mbar_arrive(bar(B_P_HALF + 2 * wg + ((s - s2) & 1)));
+      if (s < I.s2) mbar_arrive(bar(B_P_FULL + step_kind(s)));
+      else mbar_arrive(bar(B_P_HALF + 2 * wg + (full_idx(s) & 1)));
     }
     (void)delta;
-    // ---- epilogue
-    if (ok && nsteps > 0) ok = warp_wait(bar(B_PV_TAIL + 1), 0, 17);
+    // ---- epilogue.  The next item's q / r rows go in first: its first MMAs
+    // (r.P chunks, S) run while this item's output is written.
+    const int nsteps_e = I.nsteps, tail_par = n_tail1 & 1, v_last = (tb + I.ntiles - 1) % V_STAGES;
+    const bool valid = a_row < I.nrows;
+    const size_t qrow = (size_t)(I.cq + t_row) * a.Hq + h_row;
+    // decode with several splits leaves fp32 partials for the combine kernel
+    const bool partial = DECODE && a.num_splits > 1;
+    const size_t part_row = (size_t)I.split * a.total_q * a.Hq + qrow;
+    const size_t lse_at = (size_t)h_row * a.total_q + I.cq + t_row;
+    finish_item();
+    have = ok && next_item();
+    if (have && !q_slot) stage_item();
+    if (ok && nsteps_e > 0) ok = warp_wait(bar(B_PV_TAIL + 1), tail_par, 17);
+    // PV of the last step has landed: the last tile's V stage is free (the
+    // steps release every earlier one)
+    if (ok && leader && nsteps_e > 0) mbar_arrive(bar(B_V_EMPTY + v_last));
     float l_other = 0.f;
-    // total row sum over both key halves (exchange number s2: one per half step)
-    if (ok) l_other = exchange(s2, l, ok);
+    // total row sum over both key halves
+    if (ok) l_other = exchange(l, ok);
     if (ok) {
       const float lt = l + l_other;
       tc_fence_after();
-      const bool valid = a_row < nrows;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const float row_lse = lt > 0.f ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
-      const size_t qrow = (size_t)(cq + t_row) * a.Hq + h_row;
-      // decode with several splits leaves fp32 partials for the combine kernel
-      const bool partial = DECODE && a.num_splits > 1;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        if (nsteps > 0) {
+        if (nsteps_e > 0) {
           __syncwarp();
           tmem_ld32(tmem + lane_base + TM_O + 64u * wg + 32u * c, r);
           tmem_wait_ld(r);
@@ -885,7 +1044,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           for (int i = 0; i < 32; ++i) r[i] = 0u;   // an empty split contributes nothing
         }
         if (valid && partial) {
-          float *dst = a.o_part + ((size_t)split * a.total_q * a.Hq + qrow) * kHeadDim + 64 * wg + 32 * c;
+          float *dst = a.o_part + part_row * kHeadDim + 64 * wg + 32 * c;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             *reinterpret_cast<float4 *>(dst + 4 * i) =
@@ -905,9 +1064,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         }
       }
       if (valid && wg == 0) {
-        if (partial) a.lse_part[(size_t)split * a.total_q * a.Hq + qrow] = row_lse;
-        else a.lse[(size_t)h_row * a.total_q + cq + t_row] = row_lse;
+        if (partial) a.lse_part[part_row] = row_lse;
+        else a.lse[lse_at] = row_lse;
       }
+    }
     }
   }
 
@@ -927,6 +1087,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       mbar_wait(bar(B_V_FULL + t % V_STAGES), (t / V_STAGES) & 1, &keep_waiting, 2, 400000000ll);
     for (int o = max(0, issued_p - P_STAGES); o < issued_p; ++o)
       mbar_wait(bar(B_PS_FULL + o % P_STAGES), (o / P_STAGES) & 1, &keep_waiting, 2, 400000000ll);
+    if (issued_rt > 0)
+      mbar_wait(bar(B_RT_FULL), (issued_rt - 1) & 1, &keep_waiting, 2, 400000000ll);
   }
   if (warp == 1) {
     tc_fence_after();
@@ -1000,6 +1162,22 @@ cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t 
   } else {
     mp = mk;   // unused
   }
+  // prefill, bias band alone, alpha > 0, r_dim a multiple of 16 (no padding
+  // channels): q and r rows by TMA.  q [total_q, Hq, 128] in boxes of 64
+  // dims x 128 rows; r [total_q, Hq, r_dim] in one box of 64 channels x 128
+  // rows (channels past r_dim read as 0)
+  CUtensorMap mq = mk, mr = mk;
+  ta.stage_tma = !DECODE && a.band_only && ta.has_bias && a.alpha_log2e > 0.f && a.rd == a.rd_pad &&
+                 a.rd <= 64 && a.total_q >= BM;
+  if (ta.stage_tma) {
+    cuuint64_t dq[3] = {128, (cuuint64_t)a.Hq, (cuuint64_t)a.total_q};
+    cuuint64_t sq[2] = {256, (cuuint64_t)a.Hq * 256};
+    cuuint32_t bq[3] = {64, 1, BM};
+    cuuint64_t dr[3] = {(cuuint64_t)a.rd, (cuuint64_t)a.Hq, (cuuint64_t)a.total_q};
+    cuuint64_t sr[2] = {(cuuint64_t)a.rd * 2, (cuuint64_t)a.Hq * a.rd * 2};
+    cuuint32_t br[3] = {64, 1, BM};
+    if (!encode(&mq, a.q, 3, dq, sq, bq) || !encode(&mr, a.r, 3, dr, sr, br)) ta.stage_tma = 0;
+  }
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1009,14 +1187,21 @@ cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  relattn_fwd_tc_kernel<DECODE><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv, mp);
+  relattn_fwd_tc_kernel<DECODE><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv, mp, mq, mr);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {
-  return launch_tc<false>(a, total_k, dim3(a.q_tiles, a.Hq, a.batch), stream);
+  // one item per CTA, except for the bias band alone: then one CTA per SM
+  // walks the items (no per-CTA set-up, and the next item's tiles load while
+  // the current one finishes)
+  const long items = (long)a.q_tiles * a.Hq * a.batch;
+  if (items <= 0) return cudaSuccess;
+  const long ctas = a.band_only && a.sms > 0 && items > a.sms ? (long)a.sms : items;
+  if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
+  return launch_tc<false>(a, total_k, dim3((unsigned)ctas, 1, 1), stream);
 }
 
 cudaError_t launch_decode_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {

@@ -18,7 +18,7 @@
 // inside the relative-bias band are processed as two 64-key half steps (the
 // upper half first); the rest as one 128-key step.  Warp roles (12 warps,
 // one support and two softmax warps per SM sub-partition; the support warps
-// hand registers to the softmax warps: 80 vs 208 per thread):
+// hand registers to the softmax warps: 88 vs 208 per thread):
 //   warp 0      TMA producer (one thread) of K tiles (2-stage ring of 128
 //               keys), V tiles (3-stage ring) and P slices P[:, 64c..64c+64)
 //               (4 stages), in the order the MMA issuer consumes them; K and
@@ -75,9 +75,9 @@ constexpr int HN = 64;           // keys per half step (bias band); also the r.P
 constexpr int K_STAGES = 2, V_STAGES = 3;
 constexpr int P_STAGES = 4;
 constexpr int NTHREADS = 384;
-// registers per thread: 168 at launch; the support warpgroup drops to 80 and
-// the two softmax warpgroups rise to 208 (4 x 32 x 80 + 8 x 32 x 208 <= 384 x 168)
-constexpr uint32_t kRegsSupport = 80, kRegsSoftmax = 208;
+// registers per thread: 168 at launch; the support warpgroup drops to 88 and
+// the two softmax warpgroups rise to 208 (4 x 32 x 88 + 8 x 32 x 208 = 384 x 168)
+constexpr uint32_t kRegsSupport = 88, kRegsSoftmax = 208;
 static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= NTHREADS * 168, "register split");
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
@@ -109,7 +109,11 @@ constexpr int B_K_FULL = 0, B_K_EMPTY = B_K_FULL + K_STAGES, B_V_FULL = B_K_EMPT
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
 constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row exchange [2][2][128] f32
-constexpr uint32_t SM_TOTAL = SM_XCH + 2 * 2 * 128 * 4;
+// cu_seqlens_q / _k of up to kCuCache sequences, read once per CTA (the
+// persistent CTAs look them up for every item)
+constexpr int kCuCache = 64;
+constexpr uint32_t SM_CU = SM_XCH + 2 * 2 * 128 * 4;            // [2][kCuCache + 1] int
+constexpr uint32_t SM_TOTAL = SM_CU + 2 * (kCuCache + 1) * 4;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -186,6 +190,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   const uint32_t sb = smem_addr(smem);
   auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);
+  int *cu_s = reinterpret_cast<int *>(smem + SM_CU);   // filled before the set-up barrier
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -199,10 +204,12 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   const int item0 = DECODE ? 0 : (int)blockIdx.x, item_step = DECODE ? 1 : (int)gridDim.x;
   // work of the items before the current one, for barrier phases / stages
   int hb = 0, fb = 0, tb = 0, ob = 0;     // half steps, full steps, key tiles, r.P chunks
-  // K-ring slots: the item's q rows take one ahead of its key tiles (TMA staging)
+  // V-ring slots: the item's q rows take one ahead of its value tiles (TMA
+  // staging; the V ring is the deeper one, so the next item's first K tiles
+  // are not held up)
   const int q_slot = (!DECODE && ta.stage_tma) ? 1 : 0;
-  int kb = 0;
-  auto kslot = [&](int t) { return kb + q_slot + t; };
+  int vb = 0;
+  auto vslot = [&](int t) { return vb + q_slot + t; };
   int n_it = 0, n_rt = 0;                   // items; items with a band (r tile)
   int n_tail0 = 0, n_tail1 = 0, n_sw = 0;   // PV_TAIL[0/1] and PV_SW commits
   // row (local, clamped to the last valid one) -> token t and query head
@@ -246,9 +253,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       I.kv_head = I.h_fixed / a.group;
       I.row0 = (a.q_tiles - 1 - xi) * BM;
     }
-    I.cq = a.cu_q[I.b];
-    I.ck = a.cu_k[I.b];
-    const int Lq = a.cu_q[I.b + 1] - I.cq, Lk = a.cu_k[I.b + 1] - I.ck;
+    const int *cuq = a.batch <= kCuCache ? cu_s : a.cu_q;
+    const int *cuk = a.batch <= kCuCache ? cu_s + kCuCache + 1 : a.cu_k;
+    I.cq = cuq[I.b];
+    I.ck = cuk[I.b];
+    const int Lq = cuq[I.b + 1] - I.cq, Lk = cuk[I.b + 1] - I.ck;
     if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) return -1;
     I.nrows = min(BM, (DECODE ? Lq * a.group : Lq) - I.row0);
     if (I.nrows <= 0) return 0;
@@ -294,7 +303,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     hb += I.s2;
     fb += I.nsteps - I.s2;
     tb += I.ntiles;
-    kb += I.ntiles + q_slot;
+    vb += I.ntiles + q_slot;
     ob += I.s2 > 0 ? I.c_last - I.c_start + 1 : 0;
     n_tail0 += I.nsteps >= 2;
     n_tail1 += I.nsteps >= 1;
@@ -343,6 +352,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     tmem_alloc(sb + SM_TMEM_SLOT, 512);
     tmem_relinquish();
   }
+  if (a.batch <= kCuCache && tid >= 128 && tid < 128 + 2 * (a.batch + 1)) {
+    const int i = tid - 128;
+    cu_s[i <= a.batch ? i : kCuCache + 1 + (i - a.batch - 1)] =
+        i <= a.batch ? a.cu_q[i] : a.cu_k[i - a.batch - 1];
+  }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_k);
     prefetch_tmap(&map_v);
@@ -378,6 +392,16 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         if (li < 0) atomicOr(a.err, kDevErrSeqlens);
         if (li <= 0) continue;
         if (q_slot) {
+          // q rows -> the item's first V-ring slot (rows past the sequence
+          // read other rows or zeros: padding rows, never stored); first,
+          // since the r tile waits for the previous item's last r.P chunk
+          if (vb >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
+          const uint32_t dst = sb + SM_V + vst * KV_STAGE_BYTES;
+          mbar_arrive_expect_tx(bar(B_V_FULL + vst), KV_STAGE_BYTES);
+          tma_load_3d(dst, &map_q, 0, I.h_fixed, I.cq + I.row0, bar(B_V_FULL + vst));
+          tma_load_3d(dst + KV_BOX_BYTES, &map_q, 64, I.h_fixed, I.cq + I.row0, bar(B_V_FULL + vst));
+          issued_v = vb + 1;
+          if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
           // r rows -> r tile, once the previous item's r.P chunks are done
           if (I.s2 > 0) {
             if (n_rt > 0 && !(run = mbar_wait(bar(B_RT_EMPTY), (n_rt - 1) & 1, abort_flag, 20))) break;
@@ -385,15 +409,6 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             tma_load_3d(sb + SM_RT, &map_r, 0, I.h_fixed, I.cq + I.row0, bar(B_RT_FULL));
             issued_rt = n_rt + 1;
           }
-          // q rows -> the item's first K-ring slot (rows past the sequence
-          // read other rows or zeros: padding rows, never stored)
-          if (kb >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
-          const uint32_t dst = sb + SM_K + kst * KV_STAGE_BYTES;
-          mbar_arrive_expect_tx(bar(B_K_FULL + kst), KV_STAGE_BYTES);
-          tma_load_3d(dst, &map_q, 0, I.h_fixed, I.cq + I.row0, bar(B_K_FULL + kst));
-          tma_load_3d(dst + KV_BOX_BYTES, &map_q, 64, I.h_fixed, I.cq + I.row0, bar(B_K_FULL + kst));
-          issued_k = kb + 1;
-          if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
         }
         int c_next = I.c_start;
         for (int t = 0; t < I.ntiles && run && !*abort_flag; ++t) {
@@ -410,7 +425,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             }
             if (!run) break;
           }
-          const int tg = tb + t, kg = kslot(t);        // V / K ring index across items
+          const int kg = tb + t, vg = vslot(t);        // K / V ring index across items
           const int key = I.ck + I.p0 - tile_D(t);     // may be < 0: the tile reads zeros there
           if (kg >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
           if (kg != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
@@ -421,13 +436,13 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           }
           issued_k = kg + 1;
           if (++kst == K_STAGES) { kst = 0; kph ^= 1; }
-          if (tg >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
+          if (vg >= V_STAGES && !(run = mbar_wait(bar(B_V_EMPTY + vst), vph ^ 1, abort_flag, 4))) break;
           {
             const uint32_t dst = sb + SM_V + vst * KV_STAGE_BYTES;
             mbar_arrive_expect_tx(bar(B_V_FULL + vst), KV_STAGE_BYTES);
             tma_load_3d(dst, &map_v, 0, I.kv_head, key, bar(B_V_FULL + vst));
             tma_load_3d(dst + KV_BOX_BYTES, &map_v, 64, I.kv_head, key, bar(B_V_FULL + vst));
-            issued_v = tg + 1;
+            issued_v = vg + 1;
             if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
           }
         }
@@ -474,7 +489,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         return true;
       };
       auto issue_s = [&](int s) -> bool {
-        const int t = kslot(step_tile(s)), st = t % K_STAGES;
+        const int t = tb + step_tile(s), st = t % K_STAGES;
         if (!mbar_wait(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9)) return false;
         tc_fence_after();
         const uint32_t qa = tmem + TM_Q;
@@ -509,7 +524,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       };
       // O += P V; k-step k = 16 keys = 2048 bytes of the MN-major V tile
       auto issue_pv = [&](int s) -> bool {
-        const int t = tb + step_tile(s), st = t % V_STAGES;
+        const int t = vslot(step_tile(s)), st = t % V_STAGES;
         if (!mbar_wait(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5)) return false;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
@@ -555,12 +570,13 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       // previous item that read them has finished (its S / R landings were
       // awaited by the softmax warps first)
       if (q_slot) {
-        // the item's q rows: K-ring slot -> TMEM (after every S MMA of the
+        // the item's q rows: V-ring slot -> TMEM (after every S MMA of the
         // previous item, in issue order), then the slot is free again
-        const int st = kb % K_STAGES;
-        ok = mbar_wait(bar(B_K_FULL + st), (kb / K_STAGES) & 1, abort_flag, 6);
+        const int st = vb % V_STAGES;
+        ok = mbar_wait(bar(B_V_FULL + st), (vb / V_STAGES) & 1, abort_flag, 6);
         tc_fence_after();
-        const uint64_t qd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4);
+        // same 128-byte-swizzled K-major layout as a K tile
+        const uint64_t qd = kd0 + (uint64_t)((SM_V - SM_K + st * KV_STAGE_BYTES) >> 4);
         if (ok) {
           tmem_cp_128x256b(tmem + TM_Q + 0, qd + 0);
           tmem_cp_128x256b(tmem + TM_Q + 8, qd + 2);
@@ -570,7 +586,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           tmem_cp_128x256b(tmem + TM_Q + 40, qd + 1026);
           tmem_cp_128x256b(tmem + TM_Q + 48, qd + 1028);
           tmem_cp_128x256b(tmem + TM_Q + 56, qd + 1030);
-          mma_commit(bar(B_K_EMPTY + st));
+          mma_commit(bar(B_V_EMPTY + st));
         }
       } else {
         ok = mbar_wait(bar(B_Q_READY), n_it & 1, abort_flag, 6);
@@ -736,11 +752,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       if (!(ok = warp_wait(bar(B_S_FULL + step_kind(s)), step_phase(s), 13))) break;
       if (leader) {
         // S(s) landed: the K stage of its tile is read (last S of the tile)
-        if (step_kh(s) == 0) mbar_arrive(bar(B_K_EMPTY + kslot(step_tile(s)) % K_STAGES));
+        if (step_kh(s) == 0) mbar_arrive(bar(B_K_EMPTY + (tb + step_tile(s)) % K_STAGES));
         // (S(s) is issued after PV(s-2) while s - 2 is a half step; full steps
         // release their V stage after waiting for PV_F instead)
         if (s >= 2 && s - 2 < I.s2 && step_kh(s - 2) == 0)
-          mbar_arrive(bar(B_V_EMPTY + (tb + step_tile(s - 2)) % V_STAGES));
+          mbar_arrive(bar(B_V_EMPTY + vslot(step_tile(s - 2)) % V_STAGES));
       }
       const int D = step_D(s);
       const int j0 = I.p0 - D;                   // first key of this step
@@ -962,7 +978,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           if (!(ok = warp_wait(bar(B_PV_F + 2 * wg + (full_idx(s - 1) & 1)), (full_idx(s - 1) >> 1) & 1, 18)))
             break;
           if (wg == 1 && warp == 8 && lane == 0)
-            mbar_arrive(bar(B_V_EMPTY + (tb + step_tile(s - 1)) % V_STAGES));
+            mbar_arrive(bar(B_V_EMPTY + vslot(step_tile(s - 1)) % V_STAGES));
         }
         tc_fence_after();
         __syncwarp();
@@ -1010,7 +1026,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     (void)delta;
     // ---- epilogue.  The next item's q / r rows go in first: its first MMAs
     // (r.P chunks, S) run while this item's output is written.
-    const int nsteps_e = I.nsteps, tail_par = n_tail1 & 1, v_last = (tb + I.ntiles - 1) % V_STAGES;
+    const int nsteps_e = I.nsteps, tail_par = n_tail1 & 1, v_last = vslot(I.ntiles - 1) % V_STAGES;
     const bool valid = a_row < I.nrows;
     const size_t qrow = (size_t)(I.cq + t_row) * a.Hq + h_row;
     // decode with several splits leaves fp32 partials for the combine kernel

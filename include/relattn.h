@@ -179,6 +179,15 @@ int32_t relattn_last_device_error_word(void);
  * Process-wide; not thread-safe against concurrent launches. */
 relattn_status relattn_test_skip_k_tile(int32_t tile);
 
+/* Test hook; not for production use, and with no counterpart on the pages.
+ * The bias-band launch of the two-launch prefill runs one CTA per SM, each
+ * walking several work items (128 query rows of one head); with n > 0 it
+ * runs at most n CTAs instead, so that small problems also take the paths
+ * where a CTA moves from item to item.  Results are unchanged (only the
+ * speed).  n = 0 restores the default; n < 0 -> RELATTN_ERR_INVALID_ARG.
+ * Process-wide; not thread-safe against concurrent launches. */
+relattn_status relattn_test_band_ctas(int32_t n);
+
 /* Human-readable name of a status code (static string). */
 const char *relattn_status_string(relattn_status status);
 

@@ -31,7 +31,7 @@ EXPORTED = (
     "relattn_prefill", "relattn_decode", "relattn_decode_workspace_size",
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
-    "relattn_last_device_error_word", "relattn_test_skip_k_tile",
+    "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -100,6 +100,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_last_device_error_word.restype = ctypes.c_int32
         lib.relattn_test_skip_k_tile.argtypes = [ctypes.c_int32]
         lib.relattn_test_skip_k_tile.restype = ctypes.c_int
+        lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
+        lib.relattn_test_band_ctas.restype = ctypes.c_int
         lib.relattn_version.argtypes = []
         lib.relattn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -155,6 +157,11 @@ def relattn_last_device_error_word() -> int:
 def relattn_test_skip_k_tile(tile: int) -> int:
     """Test hook: later tensor-core launches never load key tile ``tile`` (-1: off)."""
     return int(load_library().relattn_test_skip_k_tile(int(tile)))
+
+
+def relattn_test_band_ctas(n: int) -> int:
+    """Test hook: at most ``n`` CTAs for the persistent bias-band launch (0: one per SM)."""
+    return int(load_library().relattn_test_band_ctas(int(n)))
 
 
 def relattn_status_string(status: int) -> str:

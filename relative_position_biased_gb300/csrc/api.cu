@@ -14,6 +14,8 @@ namespace {
 __device__ int g_device_error;
 // test hook (relattn_test_skip_k_tile): K tile the tcgen05 producer never loads
 int g_test_skip_k_tile = -1;
+// test hook (relattn_test_band_ctas): CTA cap of the persistent band launch
+int g_test_band_ctas = 0;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -106,7 +108,7 @@ relattn_status make_args(const relattn_params *p, KernelArgs *a) {
   x.split_chunk = 0;
   x.q_tiles = (p->max_seqlen_q + 127) / 128;
   x.row_blocks = 1;
-  x.sms = sms;
+  x.sms = g_test_band_ctas > 0 ? g_test_band_ctas : sms;
   return RELATTN_OK;
 }
 
@@ -299,6 +301,12 @@ int32_t relattn_last_device_error_word(void) { return g_last_error_word; }
 relattn_status relattn_test_skip_k_tile(int32_t tile) {
   if (tile < -1) return RELATTN_ERR_INVALID_ARG;
   g_test_skip_k_tile = tile;
+  return RELATTN_OK;
+}
+
+relattn_status relattn_test_band_ctas(int32_t n) {
+  if (n < 0) return RELATTN_ERR_INVALID_ARG;
+  g_test_band_ctas = n;
   return RELATTN_OK;
 }
 

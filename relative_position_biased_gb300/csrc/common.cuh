@@ -41,7 +41,7 @@ struct KernelArgs {
   int test_skip_k_tile;          // test hook (tcgen05 kernels): never load this K tile; -1 = off
   int band_only;                 // prefill, bias kernel: only the key tiles of the bias band
   int init_from_out;             // prefill, main kernel: start from the band's out / lse
-  int sms;                       // streaming multiprocessors of the device
+  int sms;                       // CTAs of a persistent launch: the SM count (or a test cap)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -80,6 +80,51 @@ def test_chunked_prefill_bottom_right():
     _check(W.custom("chunked_win", [130], [1000], 4, 2, 32, 64, window=256))
 
 
+# ------------------------------------------------- persistent bias-band launch
+# The two-launch prefill (bias band, then the rest) runs its band launch with
+# one CTA per SM, each walking several (row tile, sequence, head) items.  The
+# test hook caps the CTA count so that small cases take the item-to-item paths
+# (stage rings and barrier phases carried over, the next item's q / r rows
+# staged during the previous item's epilogue).
+
+@pytest.fixture
+def band_ctas():
+    import relative_position_biased_gb300 as rpb
+
+    def set_cap(n):
+        assert rpb.relattn_test_band_ctas(n) == 0
+
+    yield set_cap
+    rpb.relattn_test_band_ctas(0)
+
+
+@pytest.mark.parametrize("ctas", [1, 3])
+def test_band_ctas_walk_many_items(band_ctas, ctas):
+    """Items with different band lengths (short, empty and ragged sequences) in one CTA."""
+    band_ctas(ctas)
+    lens = [333, 77, 520, 1, 129, 0, 256]
+    _check(W.custom(f"persist{ctas}", lens, lens, 4, 2, 32, 104))
+
+
+def test_band_ctas_rows_staged_by_softmax(band_ctas):
+    """r_dim 40 (not a multiple of 16): the softmax warps stage the q / r rows."""
+    band_ctas(2)
+    _check(W.custom("persist_rd40", [300, 200], [300, 200], 4, 2, 40, 200, window=250))
+
+
+def test_band_ctas_log_scale_chunked(band_ctas):
+    band_ctas(2)
+    _check(W.custom("persist_ls", [130, 260], [400, 300], 4, 2, 64, 128, log_scale_base=16.0))
+
+
+@pytest.mark.parametrize("ctas", [0, 2])
+def test_band_many_sequences(band_ctas, ctas):
+    """More sequences than the per-CTA copy of the sequence offsets holds (64)."""
+    band_ctas(ctas)
+    lens = np.random.default_rng(7).integers(1, 150, size=70).tolist()
+    _check(W.custom(f"many_seqs{ctas}", lens, lens, 2, 1, 16, 64))
+
+
 def test_single_key_rows_exact():
     """window = 1: every row sees only itself, so out is v exactly."""
     w = W.custom("win1", [200], [200], 4, 2, 32, 64, window=1)

@@ -18,7 +18,7 @@
 // inside the relative-bias band are processed as two 64-key half steps (the
 // upper half first); the rest as one 128-key step.  Warp roles (12 warps,
 // one support and two softmax warps per SM sub-partition; the support warps
-// hand registers to the softmax warps: 88 vs 208 per thread):
+// hand registers to the softmax warps in prefill: 88 vs 208 per thread):
 //   warp 0      TMA producer (one thread) of K tiles (2-stage ring of 128
 //               keys), V tiles (3-stage ring) and P slices P[:, 64c..64c+64)
 //               (4 stages), in the order the MMA issuer consumes them; K and
@@ -75,8 +75,10 @@ constexpr int HN = 64;           // keys per half step (bias band); also the r.P
 constexpr int K_STAGES = 2, V_STAGES = 3;
 constexpr int P_STAGES = 4;
 constexpr int NTHREADS = 384;
-// registers per thread: 168 at launch; the support warpgroup drops to 88 and
-// the two softmax warpgroups rise to 208 (4 x 32 x 88 + 8 x 32 x 208 = 384 x 168)
+// registers per thread: 168 at launch.  Prefill: the support warpgroup drops
+// to 88 and the two softmax warpgroups rise to 208 (4 x 32 x 88 + 8 x 32 x 208
+// = 384 x 168).  Decode keeps 168 everywhere (it fits without spills, and
+// measured faster).
 constexpr uint32_t kRegsSupport = 88, kRegsSoftmax = 208;
 static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= NTHREADS * 168, "register split");
 constexpr float kRescaleThreshold = 8.f;   // log2 units
@@ -373,7 +375,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   // TMA copies issued by the producer thread (to drain them if the CTA gives up)
   int issued_k = 0, issued_v = 0, issued_p = 0, issued_rt = 0;
   if (warp < 4) {
-  regs_dec<kRegsSupport>();
+  if constexpr (!DECODE) regs_dec<kRegsSupport>();
   if (warp == 0) {
     // ======================================================== TMA producer
     // Per tile t: the P slices its half steps need (band tiles), then K(t),
@@ -637,7 +639,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     __syncwarp();
   }
   } else {
-    regs_inc<kRegsSoftmax>();
+    if constexpr (!DECODE) regs_inc<kRegsSoftmax>();
     // ======================================================== softmax
     // Two warpgroups share the 128 rows: warpgroup wg handles the wg-th half of
     // every step's keys and O / output columns [64 wg, 64 wg + 64).  The two

@@ -39,8 +39,8 @@ constexpr int BM = 128, BN = kTcKeyTile;
 constexpr int K_STAGES = 2, V_STAGES = 3;
 constexpr int NTHREADS = 384;
 constexpr float kRescaleThreshold = 8.f;   // log2 units
-constexpr uint32_t kRegsSupport = 56, kRegsSoftmax = 224;
-static_assert(128 * kRegsSupport + 256 * kRegsSoftmax <= NTHREADS * 168, "register split");
+// Every warp keeps the 168 registers of the launch: the softmax warps fit
+// (no spills), and moving registers to them with setmaxnreg measured slower.
 
 constexpr uint32_t TM_O = 0, TM_S = 256;   // O_w at 128 w, S_w at 256 + 128 w
 
@@ -155,7 +155,6 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
   bool q_issued = false;
 
   if (warp < 4) {
-    regs_dec<kRegsSupport>();
     if (warp == 0) {
       // ====================================================== TMA producer
       if (lane == 0) {
@@ -249,7 +248,6 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
       __syncwarp();
     }
   } else {
-    regs_inc<kRegsSoftmax>();
     // ======================================================== softmax
     const int w = (warp - 4) >> 2;               // head h0 + w
     const int wq = warp & 3;                     // lane quarter (TMEM lanes 32 wq ..)

@@ -115,7 +115,8 @@ constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row exchange [
 // persistent CTAs look them up for every item)
 constexpr int kCuCache = 64;
 constexpr uint32_t SM_CU = SM_XCH + 2 * 2 * 128 * 4;            // [2][kCuCache + 1] int
-constexpr uint32_t SM_TOTAL = SM_CU + 2 * (kCuCache + 1) * 4;
+constexpr uint32_t SM_QLOADS = SM_CU + 2 * (kCuCache + 1) * 4;   // q staging loads issued
+constexpr uint32_t SM_TOTAL = SM_QLOADS + 8;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -193,6 +194,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);
   int *cu_s = reinterpret_cast<int *>(smem + SM_CU);   // filled before the set-up barrier
+  volatile int *q_loads = reinterpret_cast<volatile int *>(smem + SM_QLOADS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -348,6 +350,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     mbar_init(bar(B_DRAIN), 1);
     for (int i = 0; i < 4; ++i) mbar_init(bar(B_XCH + i), 64);
     *abort_flag = 0;
+    *q_loads = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -403,6 +406,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           tma_load_3d(dst, &map_q, 0, I.h_fixed, I.cq + I.row0, bar(B_V_FULL + vst));
           tma_load_3d(dst + KV_BOX_BYTES, &map_q, 64, I.h_fixed, I.cq + I.row0, bar(B_V_FULL + vst));
           issued_v = vb + 1;
+          *q_loads = n_it + 1;   // q rows of this CTA's first n_it + 1 items are on their way
           if (++vst == V_STAGES) { vst = 0; vph ^= 1; }
           // r rows -> r tile, once the previous item's r.P chunks are done
           if (I.s2 > 0) {
@@ -470,6 +474,26 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       const uint64_t pd0 = smem_desc_sw128(sb + SM_PS, 8192, 1024);
       bool ok = true;
       bool rt_ready = false;
+      // q rows of an item: V-ring slot vq -> TMEM (eight 128x256b copies, in
+      // the same 128-byte-swizzled K-major layout as a K tile), then the slot
+      // is free again.  Every S MMA that read the previous q has landed.
+      auto copy_q = [&](int vq) -> bool {
+        const int st = vq % V_STAGES;
+        if (!mbar_wait(bar(B_V_FULL + st), (vq / V_STAGES) & 1, abort_flag, 6)) return false;
+        tc_fence_after();
+        const uint64_t qd = kd0 + (uint64_t)((SM_V - SM_K + st * KV_STAGE_BYTES) >> 4);
+        tmem_cp_128x256b(tmem + TM_Q + 0, qd + 0);
+        tmem_cp_128x256b(tmem + TM_Q + 8, qd + 2);
+        tmem_cp_128x256b(tmem + TM_Q + 16, qd + 4);
+        tmem_cp_128x256b(tmem + TM_Q + 24, qd + 6);
+        tmem_cp_128x256b(tmem + TM_Q + 32, qd + 1024);
+        tmem_cp_128x256b(tmem + TM_Q + 40, qd + 1026);
+        tmem_cp_128x256b(tmem + TM_Q + 48, qd + 1028);
+        tmem_cp_128x256b(tmem + TM_Q + 56, qd + 1030);
+        mma_commit(bar(B_V_EMPTY + st));
+        return true;
+      };
+      bool q_in = false;   // the current item's q rows are already in TMEM
       auto issue_r = [&](int c) -> bool {
         if (!rt_ready) {
           if (!mbar_wait(bar(B_RT_FULL), n_rt & 1, abort_flag, 7)) return false;
@@ -572,24 +596,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       // previous item that read them has finished (its S / R landings were
       // awaited by the softmax warps first)
       if (q_slot) {
-        // the item's q rows: V-ring slot -> TMEM (after every S MMA of the
-        // previous item, in issue order), then the slot is free again
-        const int st = vb % V_STAGES;
-        ok = mbar_wait(bar(B_V_FULL + st), (vb / V_STAGES) & 1, abort_flag, 6);
-        tc_fence_after();
-        // same 128-byte-swizzled K-major layout as a K tile
-        const uint64_t qd = kd0 + (uint64_t)((SM_V - SM_K + st * KV_STAGE_BYTES) >> 4);
-        if (ok) {
-          tmem_cp_128x256b(tmem + TM_Q + 0, qd + 0);
-          tmem_cp_128x256b(tmem + TM_Q + 8, qd + 2);
-          tmem_cp_128x256b(tmem + TM_Q + 16, qd + 4);
-          tmem_cp_128x256b(tmem + TM_Q + 24, qd + 6);
-          tmem_cp_128x256b(tmem + TM_Q + 32, qd + 1024);
-          tmem_cp_128x256b(tmem + TM_Q + 40, qd + 1026);
-          tmem_cp_128x256b(tmem + TM_Q + 48, qd + 1028);
-          tmem_cp_128x256b(tmem + TM_Q + 56, qd + 1030);
-          mma_commit(bar(B_V_EMPTY + st));
-        }
+        // the item's q rows, unless they went in during the previous item's
+        // last step
+        if (q_in) q_in = false;
+        else ok = copy_q(vb);
       } else {
         ok = mbar_wait(bar(B_Q_READY), n_it & 1, abort_flag, 6);
         tc_fence_after();
@@ -599,7 +609,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         for (int c = I.c_start; c <= I.c_first && ok; ++c) ok = issue_r(c);
       if (ok && I.nsteps > 0) ok = issue_s(0);   // an empty decode split issues nothing
       if (ok && I.s2 == 0 && I.nsteps > 1) ok = issue_s(1);   // full steps keep two S in flight
-      for (int s = 0; s < I.nsteps && ok; ++s) {
+      // with TMA-staged q rows (band only: every step a half step) the last
+      // step comes after the loop
+      const int s_loop = q_slot ? I.nsteps - 1 : I.nsteps;
+      for (int s = 0; s < s_loop && ok; ++s) {
         if (s < I.s2) {
           // ---- half step: S(s+1) ahead of PV(s).  The first full steps' S
           // buffers overlap the half-step buffers and the R ring: they are
@@ -628,6 +641,21 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           }
           if (!(ok = issue_pv(s))) break;   // waits for each warpgroup's P half
         }
+      }
+      if (q_slot && ok && I.nsteps > 0) {
+        const int s = I.nsteps - 1;
+        // once the last S has landed nothing reads q: the next item's q rows
+        // go in now, ahead of this step's PV (if the producer has issued them
+        // already; else at the next item's start)
+        if (*q_loads > n_it + 1) {
+          ok = mbar_wait(bar(B_S_FULL + step_kind(s)), step_phase(s), abort_flag, 13);
+          tc_fence_after();
+          if (ok) ok = copy_q(vb + I.ntiles + q_slot);
+          q_in = ok;
+        }
+        if (ok) ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11);
+        tc_fence_after();
+        if (ok) ok = issue_pv(s);
       }
       finish_item();
       }

@@ -143,12 +143,15 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
     chunk = (max_vis + p->num_splits - 1) / p->num_splits;
   } else {
     // keys all CTAs visit together (each sequence sees at most max_vis of its
-    // keys), cut into about two waves of CTAs; splits past a short sequence's
-    // keys exit at once, so variable lengths still spread evenly
+    // keys), cut into one wave of CTAs when there are few (sequence, kv head,
+    // row block) units -- long sequences split evenly, one CTA per SM -- and
+    // into about two waves otherwise, where splits past a short sequence's
+    // keys exit at once and the second wave evens out variable lengths
     long seq_keys = (long)p->total_k;
     if ((long)p->batch * max_vis < seq_keys) seq_keys = (long)p->batch * max_vis;
+    const long units = (long)p->batch * p->num_heads_kv * plan->row_blocks;
     const long work = seq_keys * p->num_heads_kv * plan->row_blocks;
-    const long target = 2L * sms;
+    const long target = (2 * units <= sms ? 1L : 2L) * sms;
     chunk = (work + target - 1) / target;
     if (chunk < 256) chunk = 256;                       // at least 256 keys per split
   }

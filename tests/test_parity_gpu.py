@@ -125,6 +125,13 @@ def test_band_many_sequences(band_ctas, ctas):
     _check(W.custom(f"many_seqs{ctas}", lens, lens, 2, 1, 16, 64))
 
 
+@pytest.mark.parametrize("alpha", [-0.0883883, 0.0, 0.5])
+def test_prefill_alpha(alpha):
+    """alpha < 0 (the score sign is folded into q; one-launch path), alpha = 0
+    (the logits are the bias alone) and a large alpha (steep softmax, O rescales)."""
+    _check(W.custom(f"alpha{alpha}", [300, 130], [300, 130], 4, 2, 32, 200, alpha=alpha))
+
+
 def test_single_key_rows_exact():
     """window = 1: every row sees only itself, so out is v exactly."""
     w = W.custom("win1", [200], [200], 4, 2, 32, 64, window=1)
@@ -147,6 +154,11 @@ def test_decode_splits(Lq, splits):
 def test_decode_window(window):
     ks = [700, 1500, 300]
     _check(W.custom(f"decw{window}", [9] * 3, ks, 8, 2, 32, 128, window=window), decode=True)
+
+
+@pytest.mark.parametrize("alpha", [-0.0883883, 0.0, 0.5])
+def test_decode_alpha(alpha):
+    _check(W.custom(f"dalpha{alpha}", [9, 1], [3000, 800], 16, 2, 32, 256, alpha=alpha), decode=True)
 
 
 def test_decode_log_scale_and_gqa1():

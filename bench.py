@@ -11,7 +11,10 @@ One step = one pass of the whole hot path over one batch of synthetic input:
      (64 sequences, 1 query row each, KV lengths U[1024, 32768]).
 `value` is the prefill throughput (TFLOP/s, algorithmic flops over the
 prefill kernel time); the decode HBM throughput (GB/s of visible K/V over the
-decode call time) is reported beside it.  L2 is flushed by a 256 MiB write
+decode call time) is reported beside it.  The attention prologue of the
+prefill chunk (ShortConv of k / v, RMSNorm of q / k, KV-cache write, conv
+state) is timed after the step, on its own, and reported under `prologue`
+in GB/s of the bytes it must move.  L2 is flushed by a 256 MiB write
 before every timed kernel; the flush is outside the timed events.  Before the
 flush the stream is held busy for about half a millisecond, so the host has
 queued the timed call (argument marshalling, tensor-map encoding, launch)
@@ -64,6 +67,8 @@ KERNEL_SOURCES = {
                "relative_position_biased_gb300/csrc/tc_common.cuh",
                "relative_position_biased_gb300/csrc/common.cuh",
                "relative_position_biased_gb300/csrc/combine.cu"],
+    "prologue": ["relative_position_biased_gb300/csrc/prologue.cu",
+                 "relative_position_biased_gb300/csrc/common.cuh"],
 }
 L2_FLUSH_BYTES = 256 << 20
 HOLD_CYCLES = 1_000_000   # device-side hold before each timed call (~0.5 ms)
@@ -231,6 +236,33 @@ class Phase:
             self.rpb.decode(*args, out=out, lse=lse, workspace=self.ws, **_kw(self.w))
         else:
             self.rpb.prefill(*args, out=out, lse=lse, **_kw(self.w))
+
+
+class ProloguePhase:
+    """The attention prologue over the prefill workload's chunk rows: ShortConv
+    of k / v, RMSNorm of q / k, cache write and conv state out (the sequences
+    start with the chunk, so no state in)."""
+
+    def __init__(self, w, rpb):
+        self.name, self.w, self.rpb = "prologue", w, rpb
+        self.decode = True   # reported in GB/s
+        self.host = W.make_prologue_inputs(w)
+        d = {k: v.cuda() for k, v in self.host.items()}
+        self.dev = d
+        Tk = sum(w.k_lens)
+        self.k_cache = torch.empty(Tk, w.Hkv, 128, dtype=torch.bfloat16, device="cuda")
+        self.v_cache = torch.empty_like(self.k_cache)
+        self.q_out = torch.empty_like(d["q"])
+        self.state = tuple(torch.empty(w.batch, 3, w.Hkv * 128, dtype=torch.bfloat16,
+                                       device="cuda") for _ in range(2))
+        self.launches = 2   # rows kernel + state kernel
+        self.bytes = A.prologue_bytes(w, state_in=False, state_out=True)
+
+    def run(self):
+        d = self.dev
+        self.rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"],
+                          d["norm_k"], d["cu_seqlens_q"], d["cu_seqlens_k"], self.k_cache,
+                          self.v_cache, q_out=self.q_out, conv_state_out=self.state)
 
 
 def timed_steps(phases, steps, flush):
@@ -426,7 +458,19 @@ def cpu_baseline(wl, host):
     wd = wl["decode_long"]
     drows = np.arange(sum(wd.q_lens), dtype=np.int64)   # every MTP row
     ddt, _, _ = time_oracle(wd, host["decode_long"], drows)
+    # the prologue oracle over the first sequence of the prefill chunk
+    from oracle import prologue as OP
+    wp = W.custom("prologue_sample", w.q_lens[:1], w.k_lens[:1], w.Hq, w.Hkv, 0, 0)
+    pin = W.make_prologue_inputs(wp)
+    t0 = time.perf_counter()
+    OP.prologue(pin["q"], pin["k"], pin["v"], pin["conv_k"], pin["conv_v"], pin["norm_q"],
+                pin["norm_k"], pin["cu_seqlens_q"], pin["cu_seqlens_k"])
+    pdt = time.perf_counter() - t0
+    pro = {"value": A.prologue_bytes(wp) / pdt / 1e9, "unit": "GB/s",
+           "sample": f"one {wp.q_lens[0]}-row sequence x ({w.Hq} q + 2x{w.Hkv} kv) heads "
+                     f"({pdt:.1f} s)"}
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "prologue": pro,
             "sample": f"{n} random query rows x {w.Hq} heads of {w.name} ({dt:.1f} s)",
             "decode": {"value": decode_rows_bytes(wd, drows) / ddt / 1e9, "unit": "GB/s",
                        "sample": f"all {len(drows)} query rows x {wd.Hq} heads of {wd.name} ({ddt:.1f} s)"}}
@@ -443,6 +487,8 @@ def gpu_arm(args):
     rpb.load_library()
 
     wl = step_workloads()
+    if args.only == "prologue":
+        return single_phase(args, ProloguePhase(wl["prefill"], rpb))
     if args.only:
         wl = {args.only: wl[args.only]}
     host = {k: W.make_inputs(w) for k, w in wl.items()}
@@ -469,6 +515,16 @@ def gpu_arm(args):
     barrier(dist)
     clocks = clk.summary()
 
+    # the attention prologue of the prefill chunk, timed on its own
+    pro = ProloguePhase(wl["prefill"], rpb)
+    for _ in range(args.warmup):
+        pro.run()
+    torch.cuda.synchronize()
+    pro_t = timed_steps([pro], args.steps, flush)["prologue"]
+    torch.cuda.synchronize()
+    if rpb.relattn_get_device_error() != 0:
+        raise SystemExit("device error word set by the prologue")
+
     e2e_t = e2e_steps(phases, max(1, min(args.steps, 5)), flush)
     torch.cuda.synchronize()
     e2e_steps_pipe = max(4, min(args.steps, 8))
@@ -481,6 +537,8 @@ def gpu_arm(args):
     dl_ms = max_over_ranks(ms["decode_long"] / args.steps, dist)
     db_ms = max_over_ranks(ms["decode_batched"] / args.steps, dist)
     step_ms = max_over_ranks(step_ms, dist)
+    pro_ms = max_over_ranks(sum(pro_t) / len(pro_t), dist)
+    pro_gbs = pro.bytes / (pro_ms * 1e-3) / 1e9
     value = ws * pre.flops / (pre_ms * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
     tf_peak = peaks["bf16_tflops"]
@@ -539,6 +597,13 @@ def gpu_arm(args):
             "batched": {"value": db_gbs, "unit": "GB/s", "workload": db.w.name,
                         "frac": db_gbs / hbm_peak},
         },
+        "prologue": {
+            "value": ws * pro_gbs, "unit": "GB/s", "ms": pro_ms, "workload": pre.w.name,
+            "what": "ShortConv k/v + RMSNorm q/k + KV-cache write + conv state out",
+            "bytes": pro.bytes, "launches": args.steps * pro.launches,
+            "roofline": {"bound": "hbm", "achieved": pro_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": pro_gbs / hbm_peak, "traffic": load_traffic("prologue"),
+                         "peak_source": f"{peak_kind} HBM copy"}},
         "e2e": {"value": ws * pre.flops / (e2e_pre * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": pre.h2d + dl.h2d + db.h2d,
                 "d2h_bytes_per_step": pre.d2h + dl.d2h + db.d2h,
@@ -580,7 +645,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched"],
+    ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched", "prologue"],
                     help="time one phase alone (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:

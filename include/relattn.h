@@ -168,6 +168,69 @@ relattn_status relattn_get_device_error(void *stream);
  * the id of the wait that gave up first (diagnostics only). */
 int32_t relattn_last_device_error_word(void);
 
+/*
+ * Attention prologue: the step right before the attention forward (page
+ * "SGLang and Miles Add Day-0 Support for Inkling", section "ShortConv
+ * Optimization", paragraph "KV ShortConv + QK-norm + KV store"), for one
+ * chunk of new rows of packed sequences:
+ *   - K and V each go through ShortConv (section "Short Convolution"), a
+ *     per-channel causal filter with W = 4 taps and the input added back:
+ *         y[t,c] = x[t,c] + sum_{d=0}^{3} w[c,d] * x[t-d,c],
+ *     channel c = kv_head * 128 + dim, taps over the sequence's rows;
+ *   - Q and the convolved K are RMS-normalised per token and head over the
+ *     128 dims: x * rsqrt(mean(x^2) + eps) * gamma (one gamma of 128 values
+ *     for q, one for k, shared by the heads -- the pages give no detail);
+ *   - the normalised K and the convolved V are written to the KV cache rows
+ *     the attention reads: chunk row t of sequence b goes to cache row
+ *     cu_seqlens_k[b] + (Lk_b - Lq_b) + t (the chunk is the sequence's tail).
+ * Inputs before the chunk's first row come from conv_state_in[b] (the 3
+ * pre-convolution inputs that precede it, oldest first), or are zero when
+ * conv_state_in is NULL (the sequence starts with the chunk).  When
+ * conv_state_out is not NULL it receives the last 3 pre-convolution inputs
+ * of each sequence up to the chunk's end (earlier ones from the state in, or
+ * zero); it must not overlap conv_state_in.  q_out may be q itself (in
+ * place) but must not partly overlap it; the caches must not overlap k or v.
+ * Cache rows outside the chunk's rows are left untouched.  Arithmetic in
+ * fp32, every output rounded once to bf16.
+ *
+ * Errors: RELATTN_ERR_UNSUPPORTED for head_dim != 128;
+ * RELATTN_ERR_INVALID_ARG for a NULL required pointer (all but the four
+ * states, when batch > 0), negative sizes, num_heads_kv not dividing
+ * num_heads_q, q / k / v / q_out / caches / states not 8-byte aligned,
+ * conv and norm weights not 16-byte aligned, eps not a finite number > 0.
+ * cu_seqlens contents are checked on the device: a row outside its
+ * sequence, Lq_b > Lk_b, or cache rows outside [0, total_k) skip the row and
+ * record RELATTN_ERR_DEVICE_ARGS for relattn_get_device_error().  Nothing is
+ * allocated; the call only enqueues work on `stream`.
+ */
+typedef struct relattn_prologue_params {
+  const void *q;               /* bf16 [total_q, num_heads_q, 128] (pre-norm)          */
+  const void *k;               /* bf16 [total_q, num_heads_kv, 128] (pre-conv)         */
+  const void *v;               /* bf16 [total_q, num_heads_kv, 128] (pre-conv)         */
+  const float *conv_k;         /* fp32 [num_heads_kv * 128, 4]: w[c, d], d = lag       */
+  const float *conv_v;         /* fp32 [num_heads_kv * 128, 4]                         */
+  const float *norm_q;         /* fp32 [128]                                           */
+  const float *norm_k;         /* fp32 [128]                                           */
+  float eps;                   /* > 0, e.g. 1e-6                                       */
+  const int32_t *cu_seqlens_q; /* device int32 [batch+1]: the chunk's rows             */
+  const int32_t *cu_seqlens_k; /* device int32 [batch+1]: cache rows per sequence      */
+  int32_t batch;
+  int32_t total_q;             /* cu_seqlens_q[batch] (host copy)                      */
+  int32_t total_k;             /* cu_seqlens_k[batch] (host copy)                      */
+  int32_t num_heads_q;
+  int32_t num_heads_kv;
+  int32_t head_dim;            /* must be 128                                          */
+  void *q_out;                 /* bf16 [total_q, num_heads_q, 128]; may equal q        */
+  void *k_cache;               /* bf16 [total_k, num_heads_kv, 128]                    */
+  void *v_cache;               /* bf16 [total_k, num_heads_kv, 128]                    */
+  const void *conv_state_in_k; /* bf16 [batch, 3, num_heads_kv * 128] or NULL          */
+  const void *conv_state_in_v;
+  void *conv_state_out_k;      /* bf16 [batch, 3, num_heads_kv * 128] or NULL          */
+  void *conv_state_out_v;
+} relattn_prologue_params;
+
+relattn_status relattn_prologue(const relattn_prologue_params *params, void *stream);
+
 /* Test hook for the failure path; not for production use, and with no
  * counterpart on the pages.  With tile >= 0, every later launch of the
  * tensor-core kernels leaves key tile `tile` (the tile-th 128-key tile a CTA

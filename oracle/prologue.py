@@ -82,8 +82,8 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
     v = _f64(v)
     cq = np.asarray(_f64(cu_seqlens_q), dtype=np.int64)
     ck = np.asarray(_f64(cu_seqlens_k), dtype=np.int64)
-    Tq, Hkv = k.shape[0], k.shape[1]
-    C = Hkv * k.shape[2]
+    Tq, Hkv, D = k.shape
+    C = Hkv * D
     B = len(cq) - 1
     q_out = rms_norm(q, norm_q, eps)
     k_rows = np.zeros_like(k)
@@ -98,8 +98,8 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
         st_v = None if state_v is None else _f64(state_v)[b]
         yk, sk[b] = short_conv(k[a:e].reshape(Lq, C), conv_k, st_k)
         yv, sv[b] = short_conv(v[a:e].reshape(Lq, C), conv_v, st_v)
-        k_rows[a:e] = rms_norm(yk.reshape(Lq, Hkv, -1), norm_k, eps)
-        v_rows[a:e] = yv.reshape(Lq, Hkv, -1)
+        k_rows[a:e] = rms_norm(yk.reshape(Lq, Hkv, D), norm_k, eps)
+        v_rows[a:e] = yv.reshape(Lq, Hkv, D)
         rows[a:e] = ck[b] + (Lk - Lq) + np.arange(Lq)
     return {"q_out": q_out, "k_rows": k_rows, "v_rows": v_rows, "cache_rows": rows,
             "state_k": sk, "state_v": sv}

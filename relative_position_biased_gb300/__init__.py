@@ -32,6 +32,7 @@ EXPORTED = (
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
     "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
+    "relattn_prologue",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -56,6 +57,22 @@ class RelattnParams(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("num_splits", ctypes.c_int32),
+    ]
+
+
+class RelattnPrologueParams(ctypes.Structure):
+    """Mirror of ``relattn_prologue_params`` (field order and types must match the header)."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("conv_k", ctypes.c_void_p), ("conv_v", ctypes.c_void_p),
+        ("norm_q", ctypes.c_void_p), ("norm_k", ctypes.c_void_p), ("eps", ctypes.c_float),
+        ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+        ("batch", ctypes.c_int32), ("total_q", ctypes.c_int32), ("total_k", ctypes.c_int32),
+        ("num_heads_q", ctypes.c_int32), ("num_heads_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("q_out", ctypes.c_void_p), ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("conv_state_in_k", ctypes.c_void_p), ("conv_state_in_v", ctypes.c_void_p),
+        ("conv_state_out_k", ctypes.c_void_p), ("conv_state_out_v", ctypes.c_void_p),
     ]
 
 
@@ -102,6 +119,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_test_skip_k_tile.restype = ctypes.c_int
         lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
         lib.relattn_test_band_ctas.restype = ctypes.c_int
+        lib.relattn_prologue.argtypes = [ctypes.POINTER(RelattnPrologueParams), vp]
+        lib.relattn_prologue.restype = ctypes.c_int
         lib.relattn_version.argtypes = []
         lib.relattn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -166,6 +185,10 @@ def relattn_test_band_ctas(n: int) -> int:
 
 def relattn_status_string(status: int) -> str:
     return load_library().relattn_status_string(status).decode()
+
+
+def relattn_prologue(params: RelattnPrologueParams, stream: int = 0) -> int:
+    return load_library().relattn_prologue(ctypes.byref(params), ctypes.c_void_p(stream))
 
 
 def relattn_version() -> str:
@@ -248,3 +271,36 @@ def decode(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int, max_
         prm.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(relattn_decode(prm, _current_stream() if stream is None else stream), "relattn_decode")
     return out, lse
+
+
+def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k, k_cache,
+             v_cache, *, eps: float = 1e-6, q_out=None, conv_state_in=None,
+             conv_state_out=None, total_k: Optional[int] = None, stream: Optional[int] = None):
+    """ShortConv + Q/K RMSNorm + KV-cache write for one chunk, on device tensors.
+
+    ``conv_state_in`` / ``conv_state_out`` are ``(k_state, v_state)`` pairs of
+    bf16 [batch, 3, Hkv*128] tensors, or None.  Writes ``k_cache`` / ``v_cache``
+    rows in place and returns ``q_out`` (a new tensor unless given; pass
+    ``q_out=q`` to normalise in place).
+    """
+    import torch
+    if q_out is None:
+        q_out = torch.empty_like(q)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+    sin = conv_state_in if conv_state_in is not None else (None, None)
+    sout = conv_state_out if conv_state_out is not None else (None, None)
+    prm = RelattnPrologueParams(
+        q=ptr(q), k=ptr(k), v=ptr(v), conv_k=ptr(conv_k), conv_v=ptr(conv_v),
+        norm_q=ptr(norm_q), norm_k=ptr(norm_k), eps=float(eps),
+        cu_seqlens_q=ptr(cu_seqlens_q), cu_seqlens_k=ptr(cu_seqlens_k),
+        batch=int(cu_seqlens_q.numel()) - 1, total_q=int(q.shape[0]),
+        total_k=int(k_cache.shape[0]) if total_k is None else int(total_k),
+        num_heads_q=int(q.shape[1]), num_heads_kv=int(k.shape[1]), head_dim=int(q.shape[2]),
+        q_out=ptr(q_out), k_cache=ptr(k_cache), v_cache=ptr(v_cache),
+        conv_state_in_k=ptr(sin[0]), conv_state_in_v=ptr(sin[1]),
+        conv_state_out_k=ptr(sout[0]), conv_state_out_v=ptr(sout[1]))
+    _check(relattn_prologue(prm, _current_stream() if stream is None else stream),
+           "relattn_prologue")
+    return q_out

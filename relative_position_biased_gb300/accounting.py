@@ -72,3 +72,15 @@ def io_bytes(w: Workload) -> dict:
                w.r_dim * w.rel_extent) + 2 * 4 * (w.batch + 1)
     out = 2 * Tq * w.Hq * D + 4 * Tq * w.Hq
     return {"h2d": inp, "d2h": out}
+
+
+def prologue_bytes(w: Workload, state_in: bool = False, state_out: bool = True) -> int:
+    """Bytes the attention prologue must move for the chunk rows of ``w``:
+    read q, k, v once and write q_out and the k / v cache rows once (bf16),
+    read the conv taps and norm weights (fp32) once, and the conv states.
+    The earlier rows a conv tap reads again are not counted."""
+    Tq, D, C = sum(w.q_lens), w.head_dim, w.Hkv * w.head_dim
+    rows = 2 * 2 * Tq * (w.Hq + 2 * w.Hkv) * D
+    weights = 4 * (2 * C * 4 + 2 * D)
+    state = 2 * 2 * w.batch * 3 * C
+    return rows + weights + (state if state_in else 0) + (state if state_out else 0)

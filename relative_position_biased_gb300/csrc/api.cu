@@ -175,6 +175,53 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
 
 relattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? RELATTN_OK : RELATTN_ERR_CUDA; }
 
+bool aligned(const void *p, uintptr_t bytes) {
+  return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+
+// [a, a + na) and [b, b + nb) share a byte
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+relattn_status validate_prologue(const relattn_prologue_params *p) {
+  if (!p) return RELATTN_ERR_INVALID_ARG;
+  if (p->head_dim != kHeadDim) return RELATTN_ERR_UNSUPPORTED;
+  if (p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->num_heads_q <= 0 ||
+      p->num_heads_kv <= 0 || p->num_heads_q % p->num_heads_kv != 0)
+    return RELATTN_ERR_INVALID_ARG;
+  if (!(isfinite(p->eps) && p->eps > 0.f)) return RELATTN_ERR_INVALID_ARG;
+  if (p->batch == 0) return RELATTN_OK;
+  const void *need8[] = {p->q, p->k, p->v, p->q_out, p->k_cache, p->v_cache};
+  for (const void *x : need8)
+    if (!x || !aligned(x, 8)) return RELATTN_ERR_INVALID_ARG;
+  const void *need16[] = {p->conv_k, p->conv_v, p->norm_q, p->norm_k};
+  for (const void *x : need16)
+    if (!x || !aligned(x, 16)) return RELATTN_ERR_INVALID_ARG;
+  if (!p->cu_seqlens_q || !p->cu_seqlens_k) return RELATTN_ERR_INVALID_ARG;
+  const void *states[] = {p->conv_state_in_k, p->conv_state_in_v, p->conv_state_out_k,
+                          p->conv_state_out_v};
+  for (const void *x : states)
+    if (x && !aligned(x, 8)) return RELATTN_ERR_INVALID_ARG;
+  const size_t row = (size_t)kHeadDim * 2;
+  const size_t q_bytes = (size_t)p->total_q * p->num_heads_q * row;
+  const size_t kv_bytes = (size_t)p->total_q * p->num_heads_kv * row;
+  const size_t cache_bytes = (size_t)p->total_k * p->num_heads_kv * row;
+  const size_t state_bytes = (size_t)p->batch * 3 * p->num_heads_kv * row;
+  if (p->q_out != p->q && overlaps(p->q_out, q_bytes, p->q, q_bytes)) return RELATTN_ERR_INVALID_ARG;
+  const void *kv_in[] = {p->k, p->v};
+  for (const void *x : kv_in)
+    if (overlaps(p->k_cache, cache_bytes, x, kv_bytes) || overlaps(p->v_cache, cache_bytes, x, kv_bytes))
+      return RELATTN_ERR_INVALID_ARG;
+  const void *outs[] = {p->conv_state_out_k, p->conv_state_out_v};
+  for (const void *o : outs)
+    if (o && (overlaps(o, state_bytes, p->conv_state_in_k, p->conv_state_in_k ? state_bytes : 0) ||
+              overlaps(o, state_bytes, p->conv_state_in_v, p->conv_state_in_v ? state_bytes : 0)))
+      return RELATTN_ERR_INVALID_ARG;
+  return RELATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -266,6 +313,16 @@ relattn_status relattn_combine(const float *o_part, const float *lse_part, int32
   return cuda_status(launch_combine(o_part, lse_part, num_splits, total_q, num_heads,
                                     static_cast<__nv_bfloat16 *>(out), lse,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+relattn_status relattn_prologue(const relattn_prologue_params *p, void *stream) {
+  relattn_status st = validate_prologue(p);
+  if (st != RELATTN_OK) return st;
+  if (p->batch == 0) return RELATTN_OK;
+  int *err = nullptr;
+  int sms = 0;
+  if ((st = device_state(nullptr, &err, &sms)) != RELATTN_OK) return st;
+  return cuda_status(launch_prologue(p, err, sms, static_cast<cudaStream_t>(stream)));
 }
 
 relattn_status relattn_get_device_error(void *stream) {

@@ -37,4 +37,9 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_s
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,
                            cudaStream_t stream);
 
+// attention prologue (prologue.cu): ShortConv + Q/K RMSNorm + KV-cache rows;
+// err = the device error word, sms = the SM count (sizes the grid).
+cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms,
+                            cudaStream_t stream);
+
 }  // namespace relattn

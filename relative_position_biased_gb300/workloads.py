@@ -123,6 +123,52 @@ def make_inputs(w: Workload, device: Optional[str] = None) -> Dict[str, torch.Te
     return out
 
 
+def make_prologue_inputs(w: Workload, with_state: bool = False,
+                         device: Optional[str] = None) -> Dict[str, torch.Tensor]:
+    """Draw the inputs of the attention prologue for the chunk rows of ``w``.
+
+    Recipe: ``torch.Generator('cpu').manual_seed(w.seed)``; draw, in this order,
+    (1) the lengths if ``w`` drew them, (2) q [Tq,Hq,D], (3) k, (4) v
+    [Tq,Hkv,D], all N(0, 1) rounded to bf16 (the pre-norm / pre-conv
+    projections of the chunk's rows); (5) conv_k, (6) conv_v [Hkv*D, 4] fp32
+    ~ N(0, 0.3^2) (taps of the order of a uniform(-1/sqrt(4), 1/sqrt(4))
+    initialisation); (7) norm_q, (8) norm_k [D] fp32 ~ 1 + N(0, 0.1^2);
+    then, with ``with_state``, (9) state_k, (10) state_v [B,3,Hkv*D] ~ N(0, 1)
+    in bf16.  Also returns cu_seqlens_q / cu_seqlens_k (int32, [B+1]).
+    """
+    gen = torch.Generator().manual_seed(w.seed)
+    if w.len_draw:
+        lo, hi, n = w.len_draw
+        _uniform_lengths(gen, n, lo, hi)
+    Tq, D, C = sum(w.q_lens), w.head_dim, w.Hkv * w.head_dim
+
+    def normal(*shape, std=1.0, mean=0.0, bf16=True):
+        x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        if mean != 0.0:
+            x.add_(mean)
+        return x.to(torch.bfloat16) if bf16 else x
+
+    out = {
+        "q": normal(Tq, w.Hq, D),
+        "k": normal(Tq, w.Hkv, D),
+        "v": normal(Tq, w.Hkv, D),
+        "conv_k": normal(C, 4, std=0.3, bf16=False),
+        "conv_v": normal(C, 4, std=0.3, bf16=False),
+        "norm_q": normal(D, std=0.1, mean=1.0, bf16=False),
+        "norm_k": normal(D, std=0.1, mean=1.0, bf16=False),
+        "cu_seqlens_q": cu_seqlens(w.q_lens),
+        "cu_seqlens_k": cu_seqlens(w.k_lens),
+    }
+    if with_state:
+        out["state_k"] = normal(w.batch, 3, C)
+        out["state_v"] = normal(w.batch, 3, C)
+    if device is not None:
+        out = {k: v.to(device) for k, v in out.items()}
+    return out
+
+
 def cu_seqlens(lens) -> torch.Tensor:
     c = [0]
     for n in lens:

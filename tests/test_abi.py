@@ -95,6 +95,52 @@ def test_combine_rejects_bad_arguments(lib):
     assert rpb.relattn_combine(264, 256, 2, 4, 2, 256, 256) == 1
 
 
+def _prologue_params(**over):
+    # fake, well separated addresses: every check fails before the device is touched
+    names = ("q", "k", "v", "conv_k", "conv_v", "norm_q", "norm_k", "cu_seqlens_q",
+             "cu_seqlens_k", "q_out", "k_cache", "v_cache")
+    base = {n: (i + 1) << 20 for i, n in enumerate(names)}
+    base.update(eps=1e-6, batch=1, total_q=8, total_k=16, num_heads_q=4, num_heads_kv=2,
+                head_dim=128)
+    base.update(over)
+    return rpb.RelattnPrologueParams(**base)
+
+
+def test_prologue_struct_layout_matches_header(lib):
+    off = {f[0]: getattr(rpb.RelattnPrologueParams, f[0]).offset
+           for f in rpb.RelattnPrologueParams._fields_}
+    # 7 pointers, a float, 2 pointers, 6 int32, then 7 pointers
+    assert off["eps"] == 56 and off["cu_seqlens_q"] == 64 and off["batch"] == 80
+    assert off["q_out"] == 104 and off["conv_state_out_v"] == 152
+    assert rpb.ctypes.sizeof(rpb.RelattnPrologueParams) == 160
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(head_dim=64), 2),
+    (dict(num_heads_q=3), 1),
+    (dict(num_heads_kv=0), 1),
+    (dict(total_q=-1), 1),
+    (dict(eps=0.0), 1),
+    (dict(eps=float("inf")), 1),
+    (dict(q=None), 1),
+    (dict(k_cache=None), 1),
+    (dict(norm_k=None), 1),
+    (dict(cu_seqlens_k=None), 1),
+    (dict(q=(1 << 20) + 4), 1),                    # not 8-byte aligned
+    (dict(conv_v=(5 << 20) + 8), 1),               # weights not 16-byte aligned
+    (dict(conv_state_out_k=(20 << 20) + 2), 1),
+    (dict(q_out=(1 << 20) + 256), 1),              # q_out partly overlaps q
+    (dict(k_cache=(2 << 20) + 512), 1),            # cache overlaps k
+    (dict(conv_state_in_k=30 << 20, conv_state_out_v=(30 << 20) + 512), 1),
+])
+def test_prologue_rejects_bad_arguments(lib, over, expect):
+    assert rpb.relattn_prologue(_prologue_params(**over)) == expect
+
+
+def test_prologue_empty_batch_is_a_no_op(lib):
+    assert rpb.relattn_prologue(_prologue_params(batch=0, q=None)) == 0
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         rpb._open(str(tmp_path / "librelattn.so"))

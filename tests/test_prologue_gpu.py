@@ -1,0 +1,211 @@
+"""Attention prologue on the GPU (ShortConv + Q/K RMSNorm + KV-cache rows)
+against the fp64 prologue oracle, through the C ABI.
+
+Tolerance: the kernel computes in fp32 from the same bf16 inputs and fp32
+weights and rounds once to bf16 (half an ulp: 2^-9 relative), so every output
+must satisfy |gpu - ref| <= 2^-8 |ref| + 1e-5, and at least 99.9% of them must
+be exactly the round-to-nearest bf16 of the fp64 value (the rest sit within
+fp32 error of a rounding tie).  The conv state is a copy of bf16 inputs and
+must match bit for bit; cache rows outside the chunk must keep their contents.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests.conftest import gpu_available
+from relative_position_biased_gb300 import workloads as W
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
+
+SENTINEL = 3.0   # what the cache holds before the call (exact in bf16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import relative_position_biased_gb300 as rpb
+    rpb.build()
+    rpb.load_library()
+
+
+def _w(q_lens, k_lens=None, Hq=16, Hkv=2, seed=0):
+    k_lens = q_lens if k_lens is None else k_lens
+    return W.custom("prologue", q_lens, k_lens, Hq, Hkv, 0, 0, seed=seed)
+
+
+def run_gpu(w, inp, *, with_state_in, with_state_out=True, in_place=False):
+    import relative_position_biased_gb300 as rpb
+    d = {k: v.cuda() for k, v in inp.items()}
+    Tk = sum(w.k_lens)
+    kc = torch.full((Tk, w.Hkv, 128), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, SENTINEL)
+    s_in = (d["state_k"], d["state_v"]) if with_state_in else None
+    s_out = None
+    if with_state_out:
+        s_out = (torch.full((w.batch, 3, w.Hkv * 128), SENTINEL, dtype=torch.bfloat16,
+                            device="cuda"),
+                 torch.full((w.batch, 3, w.Hkv * 128), SENTINEL, dtype=torch.bfloat16,
+                            device="cuda"))
+    q_out = rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"],
+                         d["norm_k"], d["cu_seqlens_q"], d["cu_seqlens_k"], kc, vc,
+                         q_out=d["q"] if in_place else None, conv_state_in=s_in,
+                         conv_state_out=s_out)
+    torch.cuda.synchronize()
+    st = rpb.relattn_get_device_error()
+    assert st == rpb.RELATTN_OK, rpb.STATUS_NAMES.get(st, st)
+    if in_place:
+        assert q_out.data_ptr() == d["q"].data_ptr()
+    res = {"q_out": q_out.cpu(), "k_cache": kc.cpu(), "v_cache": vc.cpu()}
+    if s_out is not None:
+        res["state_k"], res["state_v"] = s_out[0].cpu(), s_out[1].cpu()
+    return res
+
+
+def run_oracle(inp, with_state_in):
+    from oracle import prologue as OP
+    return OP.prologue(inp["q"], inp["k"], inp["v"], inp["conv_k"], inp["conv_v"],
+                       inp["norm_q"], inp["norm_k"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                       eps=1e-6, state_k=inp["state_k"] if with_state_in else None,
+                       state_v=inp["state_v"] if with_state_in else None)
+
+
+def assert_rounded(gpu_bf16, ref, what):
+    g = gpu_bf16.float().double().numpy()
+    err = np.abs(g - ref)
+    bad = err > 2.0 ** -8 * np.abs(ref) + 1e-5
+    assert not bad.any(), (what, int(bad.sum()), float(err.max()))
+    if ref.size:
+        rn = torch.from_numpy(ref).float().bfloat16().float().double().numpy()
+        frac = float(np.mean(rn == g))
+        assert frac >= 0.999, (what, frac)
+
+
+def check(w, *, with_state_in=False, with_state_out=True, in_place=False):
+    inp = W.make_prologue_inputs(w, with_state=True)
+    got = run_gpu(w, inp, with_state_in=with_state_in, with_state_out=with_state_out,
+                  in_place=in_place)
+    ref = run_oracle(inp, with_state_in)
+    assert_rounded(got["q_out"], ref["q_out"], "q_out")
+    rows = ref["cache_rows"]
+    Tk = sum(w.k_lens)
+    untouched = np.ones(Tk, dtype=bool)
+    untouched[rows] = False
+    for name, key in (("k_cache", "k_rows"), ("v_cache", "v_rows")):
+        c = got[name]
+        assert_rounded(c[torch.from_numpy(rows)], ref[key], name)
+        assert bool((c[torch.from_numpy(untouched)] == SENTINEL).all()), name + " rows outside the chunk"
+    if with_state_out:
+        for key in ("state_k", "state_v"):
+            np.testing.assert_array_equal(got[key].float().double().numpy(), ref[key], err_msg=key)
+    return got, ref
+
+
+# ------------------------------------------------------------------ prefill chunks
+
+def test_prefill_packed_ragged():
+    check(_w([1, 2, 3, 5, 64, 200, 131]))
+
+
+def test_prefill_single_long_sequence():
+    check(_w([2048], Hq=8, Hkv=1))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (4, 4), (16, 2), (12, 3), (64, 8)])
+def test_head_layouts(Hq, Hkv):
+    check(_w([37, 5, 90], Hq=Hq, Hkv=Hkv, seed=Hq + Hkv))
+
+
+def test_q_out_in_place():
+    check(_w([17, 40]), in_place=True)
+
+
+def test_without_state_out():
+    check(_w([9, 4]), with_state_out=False)
+
+
+# ------------------------------------------------------------------ chunks after a prefix
+
+def test_chunk_after_prefix_with_state():
+    # each chunk is the tail of a longer cached sequence
+    check(_w([1, 7, 64, 3], [10, 7, 500, 4]), with_state_in=True)
+
+
+def test_decode_one_row_per_sequence():
+    gen = np.random.default_rng(3)
+    k_lens = [int(x) for x in gen.integers(1, 5000, 64)]
+    check(_w([1] * 64, k_lens), with_state_in=True)
+
+
+def test_mtp_verify_rows():
+    check(_w([9, 9, 9], [9, 1000, 77]), with_state_in=True)
+
+
+def test_empty_chunks_keep_the_state():
+    got, ref = check(_w([0, 5, 0, 2], [4, 9, 0, 2]), with_state_in=True)
+    inp = W.make_prologue_inputs(_w([0, 5, 0, 2], [4, 9, 0, 2]), with_state=True)
+    for b in (0, 2):   # no new rows: the state passes through
+        assert torch.equal(got["state_k"][b], inp["state_k"][b])
+
+
+def test_chunked_equals_whole_bit_for_bit():
+    """Two chunks with the state carried on the GPU give the same cache and
+    q_out bits as one pass over the whole sequences."""
+    import relative_position_biased_gb300 as rpb
+    lens, cut = [300, 45], [100, 44]
+    w = _w(lens)
+    inp = {k: v.cuda() for k, v in W.make_prologue_inputs(w).items()}
+    base = W.cu_seqlens(lens).tolist()
+
+    def cache(rows):
+        return torch.full((rows, 2, 128), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    kw, vw = cache(base[-1]), cache(base[-1])
+    qw = rpb.prologue(inp["q"], inp["k"], inp["v"], inp["conv_k"], inp["conv_v"], inp["norm_q"],
+                      inp["norm_k"], inp["cu_seqlens_q"], inp["cu_seqlens_k"], kw, vw)
+    kc, vc, qc = cache(base[-1]), cache(base[-1]), torch.empty_like(qw)
+    st = [torch.empty(2, 3, 256, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    chunks = [([0, 0], cut), (cut, [n - c for n, c in zip(lens, cut)])]
+    for i, (start, part) in enumerate(chunks):
+        idx = torch.cat([torch.arange(base[b] + start[b], base[b] + start[b] + part[b])
+                         for b in range(2)]).cuda()
+        # the chunk is the tail of a sequence of start + part rows, in a cache
+        # of its own; its rows are then put where the whole pass put them
+        upto = [s + n for s, n in zip(start, part)]
+        ko = W.cu_seqlens(upto).tolist()
+        kk, vv = cache(ko[-1]), cache(ko[-1])
+        s_in = None if i == 0 else (st[0].clone(), st[1].clone())
+        q = rpb.prologue(inp["q"][idx], inp["k"][idx], inp["v"][idx], inp["conv_k"],
+                         inp["conv_v"], inp["norm_q"], inp["norm_k"],
+                         W.cu_seqlens(part).cuda(), W.cu_seqlens(upto).cuda(), kk, vv,
+                         conv_state_in=s_in, conv_state_out=(st[0], st[1]))
+        qc[idx] = q
+        for b in range(2):
+            g0 = base[b] + start[b]
+            kc[g0: g0 + part[b]] = kk[ko[b] + start[b]: ko[b + 1]]
+            vc[g0: g0 + part[b]] = vv[ko[b] + start[b]: ko[b + 1]]
+    torch.cuda.synchronize()
+    assert rpb.relattn_get_device_error() == rpb.RELATTN_OK
+    assert torch.equal(kc, kw) and torch.equal(vc, vw) and torch.equal(qc, qw)
+
+
+# ------------------------------------------------------------------ errors and sizes
+
+def test_inconsistent_cu_seqlens_are_reported_and_skipped():
+    import relative_position_biased_gb300 as rpb
+    w = _w([4, 6], [4, 6])
+    inp = {k: v.cuda() for k, v in W.make_prologue_inputs(w).items()}
+    bad_k = torch.tensor([0, 4, 8], dtype=torch.int32, device="cuda")   # sequence 1: Lk 4 < Lq 6
+    kc = torch.full((10, 2, 128), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, SENTINEL)
+    rpb.prologue(inp["q"], inp["k"], inp["v"], inp["conv_k"], inp["conv_v"], inp["norm_q"],
+                 inp["norm_k"], inp["cu_seqlens_q"], bad_k, kc, vc, total_k=10)
+    torch.cuda.synchronize()
+    assert rpb.relattn_get_device_error() == 6          # RELATTN_ERR_DEVICE_ARGS
+    assert rpb.relattn_get_device_error() == rpb.RELATTN_OK   # the word was cleared
+    assert bool((kc[4:] == SENTINEL).all()) and bool((vc[4:] == SENTINEL).all())
+    assert not bool((kc[:4] == SENTINEL).all())          # sequence 0 was written
+
+
+@pytest.mark.slow
+def test_full_size_swa_prefill_chunk():
+    """The 4 x 8192 packed prefill chunk (16 q heads, 2 kv heads) in one call."""
+    check(_w([8192] * 4), with_state_in=False)

@@ -138,3 +138,16 @@ def test_v_is_only_convolved_and_q_only_normalised():
     np.testing.assert_allclose(out["k_rows"], k / np.sqrt(ms + 1e-6) * gk, rtol=1e-12)
     msq = np.mean(q * q, axis=-1, keepdims=True)
     np.testing.assert_allclose(out["q_out"], q / np.sqrt(msq + 1e-6) * gq, rtol=1e-12)
+
+
+def test_empty_chunk_passes_the_state_through():
+    rng = np.random.default_rng(8)
+    q, k, v, wk, wv, gq, gk = _chunk_inputs(rng, [0, 3])
+    sk = _rand(rng, 2, P.W - 1, 2 * 128)
+    sv = _rand(rng, 2, P.W - 1, 2 * 128)
+    out = P.prologue(q, k, v, wk, wv, gq, gk, [0, 0, 3], [0, 5, 8], state_k=sk, state_v=sv)
+    np.testing.assert_array_equal(out["state_k"][0], sk[0])
+    np.testing.assert_array_equal(out["state_v"][0], sv[0])
+    # the other sequence's state is its last 3 inputs
+    np.testing.assert_array_equal(out["state_k"][1], k.reshape(3, -1))
+    np.testing.assert_array_equal(out["cache_rows"], [5, 6, 7])

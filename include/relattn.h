@@ -196,8 +196,8 @@ int32_t relattn_last_device_error_word(void);
  * Errors: RELATTN_ERR_UNSUPPORTED for head_dim != 128;
  * RELATTN_ERR_INVALID_ARG for a NULL required pointer (all but the four
  * states, when batch > 0), negative sizes, num_heads_kv not dividing
- * num_heads_q, q / k / v / q_out / caches / states not 8-byte aligned,
- * conv and norm weights not 16-byte aligned, eps not a finite number > 0.
+ * num_heads_q, q / k / v / q_out / caches / states / conv and norm weights
+ * not 16-byte aligned, eps not a finite number > 0.
  * cu_seqlens contents are checked on the device: a row outside its
  * sequence, Lq_b > Lk_b, or cache rows outside [0, total_k) skip the row and
  * record RELATTN_ERR_DEVICE_ARGS for relattn_get_device_error().  Nothing is

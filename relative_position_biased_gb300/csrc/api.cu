@@ -193,17 +193,15 @@ relattn_status validate_prologue(const relattn_prologue_params *p) {
     return RELATTN_ERR_INVALID_ARG;
   if (!(isfinite(p->eps) && p->eps > 0.f)) return RELATTN_ERR_INVALID_ARG;
   if (p->batch == 0) return RELATTN_OK;
-  const void *need8[] = {p->q, p->k, p->v, p->q_out, p->k_cache, p->v_cache};
-  for (const void *x : need8)
-    if (!x || !aligned(x, 8)) return RELATTN_ERR_INVALID_ARG;
-  const void *need16[] = {p->conv_k, p->conv_v, p->norm_q, p->norm_k};
-  for (const void *x : need16)
+  const void *need[] = {p->q,      p->k,      p->v,      p->q_out, p->k_cache,
+                        p->v_cache, p->conv_k, p->conv_v, p->norm_q, p->norm_k};
+  for (const void *x : need)
     if (!x || !aligned(x, 16)) return RELATTN_ERR_INVALID_ARG;
   if (!p->cu_seqlens_q || !p->cu_seqlens_k) return RELATTN_ERR_INVALID_ARG;
   const void *states[] = {p->conv_state_in_k, p->conv_state_in_v, p->conv_state_out_k,
                           p->conv_state_out_v};
   for (const void *x : states)
-    if (x && !aligned(x, 8)) return RELATTN_ERR_INVALID_ARG;
+    if (x && !aligned(x, 16)) return RELATTN_ERR_INVALID_ARG;
   const size_t row = (size_t)kHeadDim * 2;
   const size_t q_bytes = (size_t)p->total_q * p->num_heads_q * row;
   const size_t kv_bytes = (size_t)p->total_q * p->num_heads_kv * row;

@@ -8,12 +8,20 @@
 // K / V convolution, the Q / K RMSNorm and the cache write into one kernel.
 //
 // HBM bound: each (token, head) row of q, k and v is read once and written
-// once (the three earlier rows a conv tap reads were just read by nearby
-// warps, so they come from L2).  A warp takes 4 consecutive rows of the
-// (token, slot) order -- slots are the q heads, then the k heads, then the v
-// heads of a token -- and each lane 4 dims (8-byte accesses, 256 contiguous
-// bytes per row); all loads of the 4 rows are issued before any arithmetic.
+// once.  The main kernel is persistent: a CTA walks tiles of T consecutive
+// chunk tokens; one thread streams each tile's q, k and v slabs (plus the 3
+// k / v rows before the tile, the conv halo) into a 2-stage shared-memory
+// ring with bulk async copies tracked by mbarriers, so the next tile is in
+// flight while the CTA computes the current one from shared memory.  A
+// half-warp takes one 128-dim row (8 dims per lane, 16-byte accesses);
+// outputs go straight from registers to global memory.  Every wait is
+// bounded; a timeout sets the device error word and the CTA drains its own
+// copies before it exits.
+//
+// The register-only kernel below it (one warp per 4 rows, every tap read from
+// global memory) serves head counts whose tile does not fit in shared memory.
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace relattn {
 namespace {
@@ -159,30 +167,336 @@ relattn_prologue_kernel(const PrologueArgs a) {
 }
 
 // conv state after the chunk: the last 3 pre-convolution inputs of each
-// sequence (from the chunk, else from the state before it, else zero)
-__global__ void __launch_bounds__(kPrologueThreads)
-relattn_prologue_state_kernel(const PrologueArgs a) {
-  const int C = a.Hkv * kHeadDim;
-  const long n = (long)a.batch * (kTaps - 1) * (C / 4);
-  for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < 2 * n; e += (long)gridDim.x * blockDim.x) {
+// sequence (from the chunk, else from the state before it, else zero); raw
+// bf16 copies, 8 bytes a thread, over [first, ...) with the given stride
+__device__ __forceinline__ void state_out_pass(const PrologueArgs &a, long first, long stride) {
+  const int C4 = a.Hkv * kHeadDim / 4;
+  const long n = (long)a.batch * (kTaps - 1) * C4;
+  for (long e = first; e < 2 * n; e += stride) {
     const bool is_k = e < n;
     const long f = is_k ? e : e - n;
-    const int c4 = (int)(f % (C / 4)), jb = (int)(f / (C / 4));
+    const int c4 = (int)(f % C4), jb = (int)(f / C4);
     const int j = jb % (kTaps - 1), b = jb / (kTaps - 1);
+    __nv_bfloat16 *dst = is_k ? a.state_out_k : a.state_out_v;
+    if (dst == nullptr) continue;
     const int cq = a.cu_q[b], Lq = a.cu_q[b + 1] - cq;
     if (cq < 0 || Lq < 0 || a.cu_q[b + 1] > a.total_q) {
       atomicOr(a.err, kDevErrSeqlens);
       continue;
     }
     const int p = Lq - (kTaps - 1) + j;                   // chunk row of state slot j
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
     const __nv_bfloat16 *src = is_k ? a.k : a.v;
     const __nv_bfloat16 *st = is_k ? a.state_in_k : a.state_in_v;
-    if (p >= 0) load4(src + (size_t)(cq + p) * C + 4 * c4, x);
-    else if (st != nullptr) load4(st + ((size_t)b * (kTaps - 1) + (kTaps - 1 + p)) * C + 4 * c4, x);
-    __nv_bfloat16 *dst = is_k ? a.state_out_k : a.state_out_v;
-    if (dst != nullptr) store4(dst + ((size_t)b * (kTaps - 1) + j) * C + 4 * c4, x);
+    uint2 u = make_uint2(0u, 0u);
+    if (p >= 0) u = *reinterpret_cast<const uint2 *>(src + (size_t)(cq + p) * 4 * C4 + 4 * c4);
+    else if (st != nullptr)
+      u = *reinterpret_cast<const uint2 *>(st + ((size_t)b * (kTaps - 1) + (kTaps - 1 + p)) * 4 * C4 + 4 * c4);
+    *reinterpret_cast<uint2 *>(dst + ((size_t)b * (kTaps - 1) + j) * 4 * C4 + 4 * c4) = u;
   }
+}
+
+__global__ void __launch_bounds__(kPrologueThreads)
+relattn_prologue_state_kernel(const PrologueArgs a) {
+  state_out_pass(a, (long)blockIdx.x * blockDim.x + threadIdx.x, (long)gridDim.x * blockDim.x);
+}
+
+// ------------------------------------------------------------------ staged kernel
+
+constexpr int kConsumerWarps = 8;         // the row math
+constexpr int kStagedThreads = 32 * (kConsumerWarps + 1);   // + the producer warp
+constexpr int kStages = 2;
+constexpr int kHalo = kTaps - 1;          // k / v rows before a tile that its taps read
+constexpr int kMaxTileTokens = 32;        // (the producer warp's lanes fill the token info)
+// shared memory: full / empty mbarriers, the abort flag, per-stage token info,
+// the conv taps, then the stages
+constexpr uint32_t kFullBarOffset = 0, kEmptyBarOffset = 64, kAbortOffset = 128;
+constexpr uint32_t kInfoOffset = 256;
+constexpr uint32_t kWeightOffset = (kInfoOffset + kStages * kMaxTileTokens * 16 + 127) / 128 * 128;
+constexpr uint32_t kTargetStageBytes = 40u << 10;
+constexpr size_t kPrologueMaxSmem = 227u << 10;
+static_assert(kStages <= 8, "barrier slots");
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
+  x[0] = __uint_as_float(u.x << 16);
+  x[1] = __uint_as_float(u.x & 0xffff0000u);
+  x[2] = __uint_as_float(u.y << 16);
+  x[3] = __uint_as_float(u.y & 0xffff0000u);
+  x[4] = __uint_as_float(u.z << 16);
+  x[5] = __uint_as_float(u.z & 0xffff0000u);
+  x[6] = __uint_as_float(u.w << 16);
+  x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
+  uint4 u;
+  u.x = pack_bf16x2(y[0], y[1]);
+  u.y = pack_bf16x2(y[2], y[3]);
+  u.z = pack_bf16x2(y[4], y[5]);
+  u.w = pack_bf16x2(y[6], y[7]);
+  return u;
+}
+
+// y *= g / rms(y) over one 128-dim row held by a half-warp (8 dims a lane)
+__device__ __forceinline__ void rms_norm_half(float (&y)[8], const float (&g)[8], float eps,
+                                              unsigned hmask) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(y[i], y[i], ss);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(hmask, ss, o);
+  const float inv = rsqrtf(ss * (1.f / kHeadDim) + eps);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) y[i] *= inv * g[i];
+}
+
+// Two rows at once, one per register set (their reductions interleave):
+// y *= g / rms(y) where the row is normalised (norm0 / norm1), untouched
+// otherwise.  A half-warp holds a 128-dim row, 8 dims a lane.
+__device__ __forceinline__ void rms_norm_half2(float (&y0)[8], float (&y1)[8], const float (&g0)[8],
+                                               const float (&g1)[8], bool norm0, bool norm1,
+                                               float eps, unsigned hmask) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    s0 = fmaf(y0[i], y0[i], s0);
+    s1 = fmaf(y1[i], y1[i], s1);
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    s0 += __shfl_xor_sync(hmask, s0, o);
+    s1 += __shfl_xor_sync(hmask, s1, o);
+  }
+  const float inv0 = norm0 ? rsqrtf(s0 * (1.f / kHeadDim) + eps) : 1.f;
+  const float inv1 = norm1 ? rsqrtf(s1 * (1.f / kHeadDim) + eps) : 1.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    y0[i] *= norm0 ? inv0 * g0[i] : 1.f;
+    y1[i] *= norm1 ? inv1 * g1[i] : 1.f;
+  }
+}
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!tc::mbar_test_wait(bar, parity))
+    if (clock64() - t0 > 200000000ll) return false;
+  return true;
+}
+
+// One k / v row of a tile, loaded: the 4 conv inputs of the lane's 8 dims.
+struct KvRow {
+  float x[kTaps][8];
+  const float *w;           // the lane's taps in shared memory: w[d * C + i], dims i < 8
+  __nv_bfloat16 *dst;       // the lane's 8 dims of the cache row
+  bool is_k, live;
+};
+
+// Warp-specialised: the producer warp walks the CTA's tiles (tile n in stage
+// n % kStages), fills the stage's token info and issues the tile's bulk
+// copies once the 8 consumer warps have released the stage; each consumer
+// warp waits for the stage, does its share of the rows and releases it.  No
+// block-wide barrier inside the loop.  Stage layout: q [T][Hq][128], then k
+// and v [T + 3][Hkv][128] each (row j of k / v is token t0 - 3 + j).  Token
+// info: {row in the sequence's chunk, cache row - token, ok, sequence}.
+__global__ void __launch_bounds__(kStagedThreads, 2)
+relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kAbortOffset);
+  int4 *info_all = reinterpret_cast<int4 *>(smem + kInfoOffset);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Hq = a.Hq, Hkv = a.Hkv;
+  constexpr uint32_t kRow = kHeadDim * 2;   // bytes of a row
+  const uint32_t q_region = (uint32_t)T * Hq * kRow;
+  const uint32_t kv_region = (uint32_t)(T + kHalo) * Hkv * kRow;
+  const uint32_t stage_bytes = q_region + 2 * kv_region;
+  const int C = Hkv * kHeadDim;
+  const uint32_t stage0 = kWeightOffset + 2u * kTaps * C * 4;
+  const int tiles = (a.total_q + T - 1) / T;
+  auto full = [&](int st) { return sbase + kFullBarOffset + 8u * st; };
+  auto empty = [&](int st) { return sbase + kEmptyBarOffset + 8u * st; };
+
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      tc::mbar_init(full(st), 1);
+      tc::mbar_init(empty(st), kConsumerWarps);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  // conv taps, transposed to tap-major so a half-warp reads 512 contiguous bytes a tap
+  float *wsm = reinterpret_cast<float *>(smem + kWeightOffset);
+  for (int e = tid; e < 2 * C; e += kStagedThreads) {
+    const int kind = e >= C, c = e - kind * C;
+    const float4 w = __ldg(reinterpret_cast<const float4 *>((kind ? a.conv_v : a.conv_k) + (size_t)c * kTaps));
+    float *dst = wsm + (size_t)kind * kTaps * C + c;
+    dst[0] = w.x;
+    dst[C] = w.y;
+    dst[2 * C] = w.z;
+    dst[3 * C] = w.w;
+  }
+  __syncthreads();
+
+  int issued = 0;                   // (producer) tiles whose copies were issued
+  if (warp == kConsumerWarps) {
+    // ======================================================== producer warp
+    for (int n = 0;; ++n) {
+      const int tile = (int)blockIdx.x + n * (int)gridDim.x;
+      if (tile >= tiles) break;
+      const int st = n % kStages;
+      if (n >= kStages) {           // the consumers released tile n - kStages
+        bool ok = true;
+        if (lane == 0) ok = tc::mbar_wait(empty(st), ((n / kStages) - 1) & 1, abort_flag, 2);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      const int t0 = tile * T, nt = min(T, a.total_q - t0);
+      if (lane < nt) {
+        const int t = t0 + lane;
+        const int b = seq_of(a.cu_q, a.batch, t);
+        const int cq = a.cu_q[b], ck = a.cu_k[b];
+        const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
+        const int pos = t - cq;
+        const bool ok = pos >= 0 && pos < Lq && Lk >= Lq && ck >= 0 && a.cu_k[b + 1] <= a.total_k;
+        if (!ok) atomicOr(a.err, kDevErrSeqlens);
+        info_all[st * kMaxTileTokens + lane] = make_int4(pos, ck + (Lk - Lq) - cq, ok ? 1 : 0, b);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const int t1 = t0 + nt, h0 = max(0, t0 - kHalo);
+        const uint32_t qb = (uint32_t)nt * Hq * kRow;
+        const uint32_t kvb = (uint32_t)(t1 - h0) * Hkv * kRow;
+        const uint32_t kv_dst = (uint32_t)(h0 - (t0 - kHalo)) * Hkv * kRow;
+        const uint32_t dst = sbase + stage0 + (uint32_t)st * stage_bytes;
+        tc::mbar_arrive_expect_tx(full(st), qb + 2 * kvb);
+        bulk_load(dst, a.q + (size_t)t0 * Hq * kHeadDim, qb, full(st));
+        bulk_load(dst + q_region + kv_dst, a.k + (size_t)h0 * Hkv * kHeadDim, kvb, full(st));
+        bulk_load(dst + q_region + kv_region + kv_dst, a.v + (size_t)h0 * Hkv * kHeadDim, kvb,
+                  full(st));
+      }
+      ++issued;
+    }
+  } else {
+    // ======================================================== consumer warps
+    // a half-warp takes a row, lane hl of it dims 8hl .. 8hl+7
+    const int hw = tid >> 4, hl = tid & 15, dim = 8 * hl;
+    const unsigned hmask = 0xffffu << (lane & 16);
+    constexpr int kHalves = 2 * kConsumerWarps;
+    float gq[8], gk[8];
+    {
+      const float4 *pq = reinterpret_cast<const float4 *>(a.norm_q + dim);
+      const float4 *pk = reinterpret_cast<const float4 *>(a.norm_k + dim);
+      const float4 q0 = __ldg(pq), q1 = __ldg(pq + 1), k0 = __ldg(pk), k1 = __ldg(pk + 1);
+      gq[0] = q0.x; gq[1] = q0.y; gq[2] = q0.z; gq[3] = q0.w;
+      gq[4] = q1.x; gq[5] = q1.y; gq[6] = q1.z; gq[7] = q1.w;
+      gk[0] = k0.x; gk[1] = k0.y; gk[2] = k0.z; gk[3] = k0.w;
+      gk[4] = k1.x; gk[5] = k1.y; gk[6] = k1.z; gk[7] = k1.w;
+    }
+    int n = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++n) {
+      const int st = n % kStages;
+      const bool ok = tc::mbar_wait(full(st), (n / kStages) & 1, abort_flag, 1);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int t0 = tile * T, nt = min(T, a.total_q - t0);
+      const uint8_t *sq = smem + stage0 + (size_t)st * stage_bytes;
+      const uint8_t *skv = sq + q_region;
+      const int4 *info = info_all + st * kMaxTileTokens;
+
+      // ---- q rows: the tile's q slab is the rows t0*Hq .. (t0+nt)*Hq of q;
+      // two rows per half-warp and pass (the second re-reads the first's row
+      // when it is past the end, and is not stored)
+      const int q_rows = nt * Hq;
+      for (int r0 = hw; r0 < q_rows; r0 += 2 * kHalves) {
+        const int r1 = r0 + kHalves;
+        const bool two = r1 < q_rows;
+        float y0[8], y1[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sq + (size_t)r0 * kRow + 16 * hl), y0);
+        unpack8(*reinterpret_cast<const uint4 *>(sq + (size_t)(two ? r1 : r0) * kRow + 16 * hl), y1);
+        rms_norm_half2(y0, y1, gq, gq, true, true, a.eps, hmask);
+        __nv_bfloat16 *o = a.q_out + (size_t)t0 * Hq * kHeadDim + dim;
+        *reinterpret_cast<uint4 *>(o + (size_t)r0 * kHeadDim) = pack8(y0);
+        if (two) *reinterpret_cast<uint4 *>(o + (size_t)r1 * kHeadDim) = pack8(y1);
+      }
+
+      // ---- k / v rows, order (token, k heads, v heads)
+      const int kv_rows = nt * 2 * Hkv;
+      auto load_kv = [&](int r, KvRow &R) {
+        const int tt = r / (2 * Hkv), rem = r - tt * 2 * Hkv;
+        R.is_k = rem < Hkv;
+        const int h = R.is_k ? rem : rem - Hkv;
+        const int4 in = info[tt];
+        R.live = in.z != 0;
+        const int pos = in.x;
+        // row tt + 3 - d of the stage's k (or v) block is token t - d
+        const uint8_t *src = skv + (R.is_k ? 0u : kv_region) + ((size_t)(tt + kHalo) * Hkv + h) * kRow + 16 * hl;
+#pragma unroll
+        for (int d = 0; d < kTaps; ++d)
+          unpack8(*reinterpret_cast<const uint4 *>(src - (size_t)d * Hkv * kRow), R.x[d]);
+        if (R.live && pos < kHalo) {
+          // taps before the chunk: the conv state, or zero (the stage rows
+          // there belong to another sequence, or were never loaded)
+          const __nv_bfloat16 *state = R.is_k ? a.state_in_k : a.state_in_v;
+#pragma unroll
+          for (int d = 1; d < kTaps; ++d) {
+            if (pos - d >= 0) continue;
+            if (state != nullptr) {
+              unpack8(*reinterpret_cast<const uint4 *>(
+                          state + ((size_t)in.w * kHalo + (kHalo + pos - d)) * Hkv * kHeadDim +
+                          (size_t)h * kHeadDim + dim),
+                      R.x[d]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) R.x[d][i] = 0.f;
+            }
+          }
+        }
+        R.w = wsm + (R.is_k ? 0 : kTaps * C) + h * kHeadDim + dim;
+        R.dst = (R.is_k ? a.k_cache : a.v_cache) +
+                ((size_t)(t0 + tt + in.y) * Hkv + h) * kHeadDim + dim;
+      };
+      auto conv = [&](const KvRow &R, float (&y)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = R.x[0][i];   // the input added back
+#pragma unroll
+        for (int d = 0; d < kTaps; ++d) {
+          const float4 w0 = *reinterpret_cast<const float4 *>(R.w + d * C);
+          const float4 w1 = *reinterpret_cast<const float4 *>(R.w + d * C + 4);
+          const float wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) y[i] = fmaf(wd[i], R.x[d][i], y[i]);
+        }
+      };
+      for (int r = hw; r < kv_rows; r += kHalves) {
+        KvRow A;
+        load_kv(r, A);
+        float y[8];
+        conv(A, y);
+        if (A.is_k) rms_norm_half(y, gk, a.eps, hmask);
+        if (A.live) *reinterpret_cast<uint4 *>(A.dst) = pack8(y);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty(st));   // this warp is done with the stage
+    }
+  }
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == kConsumerWarps && lane == 0) {
+      atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+      // copies still in flight: those of the last kStages tiles issued
+      for (int m = max(0, issued - kStages); m < issued; ++m)
+        drain_wait(full(m % kStages), (m / kStages) & 1);
+    }
+    return;
+  }
+  // the conv state after the chunk, spread over the grid
+  if (a.state_out_k != nullptr || a.state_out_v != nullptr)
+    state_out_pass(a, (long)blockIdx.x * blockDim.x + tid, (long)gridDim.x * blockDim.x);
 }
 
 }  // namespace
@@ -213,6 +527,33 @@ cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms,
   a.state_out_v = static_cast<__nv_bfloat16 *>(p->conv_state_out_v);
   a.err = err;
   const long rows = (long)a.total_q * (a.Hq + 2 * a.Hkv);
+  // staged kernel: tokens per tile so that a stage holds about kTargetStageBytes
+  const uint32_t tok_bytes = (uint32_t)(a.Hq + 2 * a.Hkv) * kHeadDim * 2;
+  int T = (int)(kTargetStageBytes / tok_bytes);
+  T = T < 1 ? 1 : (T > kMaxTileTokens ? kMaxTileTokens : T);
+  const size_t stage_bytes = (size_t)T * a.Hq * kHeadDim * 2 + 2 * (size_t)(T + kHalo) * a.Hkv * kHeadDim * 2;
+  const size_t smem = kWeightOffset + 2 * kTaps * (size_t)a.Hkv * kHeadDim * 4 + kStages * stage_bytes;
+  if (rows > 0 && smem <= kPrologueMaxSmem) {
+    static bool attr_set[64] = {false};   // the attribute is set once per device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(relattn_prologue_staged_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kPrologueMaxSmem);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, relattn_prologue_staged_kernel, kStagedThreads, smem);
+    if (e != cudaSuccess) return e;
+    const long tiles = (a.total_q + T - 1) / T;
+    long grid = (long)(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    if (grid > tiles) grid = tiles;
+    relattn_prologue_staged_kernel<<<(unsigned)grid, kStagedThreads, smem, stream>>>(a, T);
+    return cudaGetLastError();   // (it also writes the conv state)
+  }
   if (rows > 0) {
     const long per_block = (long)(kPrologueThreads / 32) * kRowsPerWarp;
     long blocks = (rows + per_block - 1) / per_block;

@@ -126,9 +126,10 @@ def test_prologue_struct_layout_matches_header(lib):
     (dict(k_cache=None), 1),
     (dict(norm_k=None), 1),
     (dict(cu_seqlens_k=None), 1),
-    (dict(q=(1 << 20) + 4), 1),                    # not 8-byte aligned
-    (dict(conv_v=(5 << 20) + 8), 1),               # weights not 16-byte aligned
-    (dict(conv_state_out_k=(20 << 20) + 2), 1),
+    (dict(q=(1 << 20) + 8), 1),                    # not 16-byte aligned
+    (dict(v_cache=(12 << 20) + 8), 1),
+    (dict(conv_v=(5 << 20) + 8), 1),
+    (dict(conv_state_out_k=(20 << 20) + 8), 1),
     (dict(q_out=(1 << 20) + 256), 1),              # q_out partly overlaps q
     (dict(k_cache=(2 << 20) + 512), 1),            # cache overlaps k
     (dict(conv_state_in_k=30 << 20, conv_state_out_v=(30 << 20) + 512), 1),

@@ -115,6 +115,16 @@ def test_head_layouts(Hq, Hkv):
     check(_w([37, 5, 90], Hq=Hq, Hkv=Hkv, seed=Hq + Hkv))
 
 
+def test_tiles_reuse_the_ring():
+    # about 2 tiles per CTA: the 2-stage ring wraps and the phases flip
+    check(_w([3000, 2000, 1]))
+
+
+def test_wide_heads_take_the_register_kernel():
+    # a token of 512 q heads does not fit a 2-stage tile in shared memory
+    check(_w([5, 3], Hq=512, Hkv=1), with_state_in=True)
+
+
 def test_q_out_in_place():
     check(_w([17, 40]), in_place=True)
 

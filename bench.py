@@ -68,6 +68,7 @@ KERNEL_SOURCES = {
                "relative_position_biased_gb300/csrc/common.cuh",
                "relative_position_biased_gb300/csrc/combine.cu"],
     "prologue": ["relative_position_biased_gb300/csrc/prologue.cu",
+                 "relative_position_biased_gb300/csrc/tc_common.cuh",
                  "relative_position_biased_gb300/csrc/common.cuh"],
 }
 L2_FLUSH_BYTES = 256 << 20

@@ -8,18 +8,20 @@
 // K / V convolution, the Q / K RMSNorm and the cache write into one kernel.
 //
 // HBM bound: each (token, head) row of q, k and v is read once and written
-// once.  The main kernel is persistent: a CTA walks tiles of T consecutive
-// chunk tokens; one thread streams each tile's q, k and v slabs (plus the 3
-// k / v rows before the tile, the conv halo) into a 2-stage shared-memory
-// ring with bulk async copies tracked by mbarriers, so the next tile is in
-// flight while the CTA computes the current one from shared memory.  A
-// half-warp takes one 128-dim row (8 dims per lane, 16-byte accesses);
-// outputs go straight from registers to global memory.  Every wait is
-// bounded; a timeout sets the device error word and the CTA drains its own
-// copies before it exits.
+// once.  The main kernel is persistent and warp-specialised: a CTA walks
+// tiles of T consecutive chunk tokens (about 40 KB of q, k and v); a producer
+// warp streams each tile's q, k and v slabs (plus the 3 k / v rows before the
+// tile, the conv halo) into a 2-stage shared-memory ring with bulk async
+// copies tracked by full / empty mbarriers, and 8 consumer warps compute the
+// rows from shared memory, a half-warp per 128-dim row (8 dims a lane,
+// 16-byte accesses), storing straight from registers.  The conv taps sit in
+// shared memory, tap-major.  Every wait is bounded; a timeout sets the device
+// error word and the CTA drains its own copies before it exits.  The same
+// launch writes the conv state after its tiles.
 //
-// The register-only kernel below it (one warp per 4 rows, every tap read from
-// global memory) serves head counts whose tile does not fit in shared memory.
+// The register-only kernel (one warp per 4 rows, every tap read from global
+// memory) and the separate state kernel serve head counts whose tile does
+// not fit in shared memory.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -216,12 +218,31 @@ constexpr uint32_t kTargetStageBytes = 40u << 10;
 constexpr size_t kPrologueMaxSmem = 227u << 10;
 static_assert(kStages <= 8, "barrier slots");
 
+// global -> shared bulk copy completing on an mbarrier (16-byte aligned
+// addresses, a multiple of 16 bytes)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
                                           uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Bounded wait on an mbarrier phase that suspends the thread between probes
+// (the consumer warps wait here for most of a stage's copy, and a suspended
+// warp leaves the issue slots to the others).  Gives up after about a second
+// of SM clocks or when another thread raised *abort, setting *abort = site.
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                           int site) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (tc::mbar_try_wait(bar, parity, 100000u)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > 2000000000ll) {
+      *abort = site;
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ void unpack8(const uint4 u, float (&x)[8]) {
@@ -258,10 +279,8 @@ __device__ __forceinline__ void rms_norm_half(float (&y)[8], const float (&g)[8]
 }
 
 // Two rows at once, one per register set (their reductions interleave):
-// y *= g / rms(y) where the row is normalised (norm0 / norm1), untouched
-// otherwise.  A half-warp holds a 128-dim row, 8 dims a lane.
-__device__ __forceinline__ void rms_norm_half2(float (&y0)[8], float (&y1)[8], const float (&g0)[8],
-                                               const float (&g1)[8], bool norm0, bool norm1,
+// y *= g / rms(y) for each.
+__device__ __forceinline__ void rms_norm_half2(float (&y0)[8], float (&y1)[8], const float (&g)[8],
                                                float eps, unsigned hmask) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -274,12 +293,12 @@ __device__ __forceinline__ void rms_norm_half2(float (&y0)[8], float (&y1)[8], c
     s0 += __shfl_xor_sync(hmask, s0, o);
     s1 += __shfl_xor_sync(hmask, s1, o);
   }
-  const float inv0 = norm0 ? rsqrtf(s0 * (1.f / kHeadDim) + eps) : 1.f;
-  const float inv1 = norm1 ? rsqrtf(s1 * (1.f / kHeadDim) + eps) : 1.f;
+  const float inv0 = rsqrtf(s0 * (1.f / kHeadDim) + eps);
+  const float inv1 = rsqrtf(s1 * (1.f / kHeadDim) + eps);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    y0[i] *= norm0 ? inv0 * g0[i] : 1.f;
-    y1[i] *= norm1 ? inv1 * g1[i] : 1.f;
+    y0[i] *= inv0 * g[i];
+    y1[i] *= inv1 * g[i];
   }
 }
 
@@ -353,7 +372,7 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
       const int st = n % kStages;
       if (n >= kStages) {           // the consumers released tile n - kStages
         bool ok = true;
-        if (lane == 0) ok = tc::mbar_wait(empty(st), ((n / kStages) - 1) & 1, abort_flag, 2);
+        if (lane == 0) ok = stage_wait(empty(st), ((n / kStages) - 1) & 1, abort_flag, 2);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
       const int t0 = tile * T, nt = min(T, a.total_q - t0);
@@ -401,7 +420,7 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
     int n = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++n) {
       const int st = n % kStages;
-      const bool ok = tc::mbar_wait(full(st), (n / kStages) & 1, abort_flag, 1);
+      const bool ok = stage_wait(full(st), (n / kStages) & 1, abort_flag, 1);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int t0 = tile * T, nt = min(T, a.total_q - t0);
       const uint8_t *sq = smem + stage0 + (size_t)st * stage_bytes;
@@ -418,7 +437,7 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
         float y0[8], y1[8];
         unpack8(*reinterpret_cast<const uint4 *>(sq + (size_t)r0 * kRow + 16 * hl), y0);
         unpack8(*reinterpret_cast<const uint4 *>(sq + (size_t)(two ? r1 : r0) * kRow + 16 * hl), y1);
-        rms_norm_half2(y0, y1, gq, gq, true, true, a.eps, hmask);
+        rms_norm_half2(y0, y1, gq, a.eps, hmask);
         __nv_bfloat16 *o = a.q_out + (size_t)t0 * Hq * kHeadDim + dim;
         *reinterpret_cast<uint4 *>(o + (size_t)r0 * kHeadDim) = pack8(y0);
         if (two) *reinterpret_cast<uint4 *>(o + (size_t)r1 * kHeadDim) = pack8(y1);

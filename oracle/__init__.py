@@ -1,8 +1,9 @@
 """fp64 CPU oracle for Inkling relative attention -- TEST INFRASTRUCTURE ONLY.
 
-The arithmetic lives in ``relattn_oracle.c`` (plain C, fp64, one row at a time,
-two-pass softmax); this module compiles it with gcc and marshals arrays through
-ctypes.  It shares nothing with the CUDA library.  Only the test suite,
+The arithmetic lives in ``relattn_oracle.c`` (the forward: plain C, fp64, one
+row at a time, two-pass softmax) and ``relattn_oracle_bwd.c`` (the backward:
+the chain rule through that softmax, with P frozen); this module compiles them
+with gcc and marshals arrays through ctypes.  It shares nothing with the CUDA library.  Only the test suite,
 ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference arm
 may import it; the product path never does.
 
@@ -20,7 +21,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "relattn_oracle.c")
+_SRCS = [os.path.join(_HERE, "relattn_oracle.c"), os.path.join(_HERE, "relattn_oracle_bwd.c")]
 _LIB = os.path.join(_HERE, "librelattn_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -31,11 +32,11 @@ F64, BF16 = 0, 1
 def build(force: bool = False) -> str:
     """Compile the oracle into ``oracle/librelattn_oracle.so`` (gcc, OpenMP)."""
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(s) for s in _SRCS)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O3", "-fopenmp", "-shared", "-fPIC", "-std=c11",
-           "-o", tmp, _SRC, "-lm"]
+           "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB
@@ -55,6 +56,10 @@ def _load():
             lib.relattn_oracle_forward.argtypes = [
                 ci, vp, vp, vp, vp, vp, i32p, i32p, ci, ci, ci, ci, ci, ci, ci,
                 cd, cd, i64p, ctypes.c_int64, f64p, f64p, ci]
+            lib.relattn_oracle_backward.restype = ctypes.c_int
+            lib.relattn_oracle_backward.argtypes = [
+                ci, vp, vp, vp, vp, vp, vp, i32p, i32p, ci, ci, ci, ci, ci, ci, ci,
+                cd, cd, f64p, f64p, f64p, f64p, ci]
             lib.relattn_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -129,3 +134,47 @@ def forward(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, *, alpha: float,
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return out, lse
+
+
+def backward(q, k, v, r, P, dout, cu_seqlens_q, cu_seqlens_k, *, alpha: float,
+             window: int = 0, log_scale_base: float = 0.0, threads: int = 0):
+    """Gradients of sum(dout * out) in fp64, with P frozen.
+
+    Inputs as for ``forward`` plus dout [Tq,Hq,D] (same kind).  Returns
+    (dq [Tq,Hq,D], dk [Tk,Hkv,D], dv [Tk,Hkv,D], dr [Tq,Hq,r_dim]) float64.
+    """
+    lib = _load()
+    arrs = [_as_input(x) for x in (q, k, v, r, P, dout)]
+    kinds = {a[1] for a in arrs}
+    if len(kinds) != 1:
+        raise TypeError("oracle inputs must all be bf16 or all be float")
+    dtype = kinds.pop()
+    qa, ka, va, ra, Pa, da = (a[0] for a in arrs)
+    Tq, Hq, D = qa.shape
+    Tk, Hkv, _ = ka.shape
+    if da.shape != qa.shape or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    r_dim = ra.shape[2] if ra.ndim == 3 else 0
+    if Pa.ndim != 2 or Pa.shape[0] != r_dim:
+        raise ValueError("P must be [r_dim, E]")
+    E = Pa.shape[1]
+    cq = np.ascontiguousarray(np.asarray(
+        cu_seqlens_q.cpu() if hasattr(cu_seqlens_q, "cpu") else cu_seqlens_q), dtype=np.int32)
+    ck = np.ascontiguousarray(np.asarray(
+        cu_seqlens_k.cpu() if hasattr(cu_seqlens_k, "cpu") else cu_seqlens_k), dtype=np.int32)
+    B = cq.shape[0] - 1
+    dq = np.zeros((Tq, Hq, D))
+    dk = np.zeros((Tk, Hkv, D))
+    dv = np.zeros((Tk, Hkv, D))
+    dr = np.zeros((Tq, Hq, r_dim))
+    f64p = ctypes.POINTER(ctypes.c_double)
+    rc = lib.relattn_oracle_backward(
+        dtype, qa.ctypes.data, ka.ctypes.data, va.ctypes.data, ra.ctypes.data,
+        Pa.ctypes.data, da.ctypes.data, cq.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        ck.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), B, Hq, Hkv, D, r_dim, E,
+        int(window), float(alpha), float(log_scale_base), dq.ctypes.data_as(f64p),
+        dk.ctypes.data_as(f64p), dv.ctypes.data_as(f64p), dr.ctypes.data_as(f64p),
+        int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return dq, dk, dv, dr

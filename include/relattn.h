@@ -169,6 +169,46 @@ relattn_status relattn_get_device_error(void *stream);
 int32_t relattn_last_device_error_word(void);
 
 /*
+ * Backward pass (page "SGLang and Miles Add Day-0 Support for Inkling",
+ * section "Customized Efficient Kernels for Train-Inference Consistency",
+ * paragraph "Relative attention": the training side differentiates through
+ * the attention scores and r while P stays frozen).  Given the forward's
+ * inputs, its saved out / lse and the upstream gradient dout, it writes the
+ * gradients of sum(dout * out):
+ *   dq [total_q, Hq, 128], dk / dv [total_k, Hkv, 128], dr [total_q, Hq, r_dim]
+ * (bf16; dk / dv summed over the query heads of each GQA group; no gradient
+ * for P).  With D_i = dout_i . out_i and dl = p (dout_i . v_j - D_i):
+ * dq_i = s_i alpha sum_j dl k_j, dk_j = sum_i s_i alpha dl q_i,
+ * dv_j = sum_i p dout_i, dr_i = s_i sum_j dl P[:, i-j] over 0 <= i-j < E.
+ * The softmax weights are recomputed from lse (fp32 arithmetic, bf16 MMA
+ * operands).  Every key row of dk / dv is written (zero when no query sees
+ * it); dq / dr rows of every query row are written.
+ *
+ * Layouts and conventions are the forward's (fwd.*); fwd.out and fwd.lse are
+ * read, fwd.workspace / fwd.num_splits are ignored.  The workspace (device,
+ * 16-byte aligned) holds D: at least relattn_backward_workspace_size() bytes.
+ * Requirements: every pointer 16-byte aligned, r_dim a multiple of 8 (0..64).
+ * Errors: RELATTN_ERR_INVALID_ARG (NULL or unaligned pointers, bad sizes),
+ * RELATTN_ERR_UNSUPPORTED (head_dim != 128, r_dim not a multiple of 8 or
+ * above 64), RELATTN_ERR_WORKSPACE (workspace missing or too small);
+ * inconsistent cu_seqlens contents skip the sequence and record
+ * RELATTN_ERR_DEVICE_ARGS for relattn_get_device_error().
+ */
+typedef struct relattn_bwd_params {
+  relattn_params fwd;          /* the forward call; fwd.out / fwd.lse are inputs here */
+  const void *dout;            /* bf16 [total_q, num_heads_q, 128]                  */
+  void *dq;                    /* bf16 [total_q, num_heads_q, 128]                  */
+  void *dk;                    /* bf16 [total_k, num_heads_kv, 128]                 */
+  void *dv;                    /* bf16 [total_k, num_heads_kv, 128]                 */
+  void *dr;                    /* bf16 [total_q, num_heads_q, r_dim]; NULL if r_dim == 0 */
+  void *workspace;             /* device, >= relattn_backward_workspace_size bytes  */
+  size_t workspace_bytes;
+} relattn_bwd_params;
+
+relattn_status relattn_backward_workspace_size(const relattn_bwd_params *params, size_t *bytes);
+relattn_status relattn_backward(const relattn_bwd_params *params, void *stream);
+
+/*
  * Attention prologue: the step right before the attention forward (page
  * "SGLang and Miles Add Day-0 Support for Inkling", section "ShortConv
  * Optimization", paragraph "KV ShortConv + QK-norm + KV store"), for one

@@ -32,7 +32,7 @@ EXPORTED = (
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
     "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
-    "relattn_prologue",
+    "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -57,6 +57,15 @@ class RelattnParams(ctypes.Structure):
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("num_splits", ctypes.c_int32),
+    ]
+
+
+class RelattnBwdParams(ctypes.Structure):
+    """Mirror of ``relattn_bwd_params`` (field order and types must match the header)."""
+    _fields_ = [
+        ("fwd", RelattnParams), ("dout", ctypes.c_void_p), ("dq", ctypes.c_void_p),
+        ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p), ("dr", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -119,6 +128,11 @@ def load_library(path: Optional[str] = None):
         lib.relattn_test_skip_k_tile.restype = ctypes.c_int
         lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
         lib.relattn_test_band_ctas.restype = ctypes.c_int
+        BP = ctypes.POINTER(RelattnBwdParams)
+        lib.relattn_backward.argtypes = [BP, vp]
+        lib.relattn_backward.restype = ctypes.c_int
+        lib.relattn_backward_workspace_size.argtypes = [BP, ctypes.POINTER(ctypes.c_size_t)]
+        lib.relattn_backward_workspace_size.restype = ctypes.c_int
         lib.relattn_prologue.argtypes = [ctypes.POINTER(RelattnPrologueParams), vp]
         lib.relattn_prologue.restype = ctypes.c_int
         lib.relattn_version.argtypes = []
@@ -185,6 +199,16 @@ def relattn_test_band_ctas(n: int) -> int:
 
 def relattn_status_string(status: int) -> str:
     return load_library().relattn_status_string(status).decode()
+
+
+def relattn_backward(params: RelattnBwdParams, stream: int = 0) -> int:
+    return load_library().relattn_backward(ctypes.byref(params), ctypes.c_void_p(stream))
+
+
+def relattn_backward_workspace_size(params: RelattnBwdParams) -> Tuple[int, int]:
+    n = ctypes.c_size_t(0)
+    st = load_library().relattn_backward_workspace_size(ctypes.byref(params), ctypes.byref(n))
+    return st, int(n.value)
 
 
 def relattn_prologue(params: RelattnPrologueParams, stream: int = 0) -> int:
@@ -304,3 +328,33 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
     _check(relattn_prologue(prm, _current_stream() if stream is None else stream),
            "relattn_prologue")
     return q_out
+
+
+def backward(q, k, v, r, P, out, lse, dout, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int,
+             max_seqlen_k: int, alpha: float, window: int = 0, log_scale_base: float = 0.0,
+             dq=None, dk=None, dv=None, dr=None, workspace=None, stream: Optional[int] = None):
+    """Gradients of sum(dout * out) w.r.t. q, k, v and r (P frozen), from the
+    forward's inputs and its saved out / lse.  Returns (dq, dk, dv, dr); dr is
+    None when r has no channels."""
+    import torch
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    r_dim = int(r.shape[-1]) if r is not None and r.dim() == 3 else 0
+    if dr is None and r_dim > 0:
+        dr = torch.empty_like(r)
+    prm = RelattnBwdParams(
+        fwd=make_params(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, max_seqlen_q=max_seqlen_q,
+                        max_seqlen_k=max_seqlen_k, alpha=alpha, window=window,
+                        log_scale_base=log_scale_base, out=out, lse=lse),
+        dout=dout.data_ptr(), dq=dq.data_ptr(), dk=dk.data_ptr(), dv=dv.data_ptr(),
+        dr=None if dr is None else dr.data_ptr())
+    if workspace is None:
+        st, nbytes = relattn_backward_workspace_size(prm)
+        _check(st, "relattn_backward_workspace_size")
+        workspace = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device=q.device)
+    prm.workspace = workspace.data_ptr()
+    prm.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(relattn_backward(prm, _current_stream() if stream is None else stream),
+           "relattn_backward")
+    return dq, dk, dv, dr

@@ -185,6 +185,30 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
+size_t backward_workspace_bytes(const relattn_params &f) {
+  return ((size_t)f.num_heads_q * f.total_q * sizeof(float) + 255) / 256 * 256;
+}
+
+relattn_status validate_backward(const relattn_bwd_params *p) {
+  if (!p) return RELATTN_ERR_INVALID_ARG;
+  const relattn_params &f = p->fwd;
+  relattn_status st = validate(&f, false);
+  if (st != RELATTN_OK) return st;
+  if (f.r_dim % 8 != 0) return RELATTN_ERR_UNSUPPORTED;
+  if (f.batch == 0) return RELATTN_OK;
+  if (f.total_k > 0 && (!p->dk || !p->dv || !aligned16(p->dk) || !aligned16(p->dv)))
+    return RELATTN_ERR_INVALID_ARG;
+  if (f.total_q == 0) return RELATTN_OK;
+  if (!p->dout || !p->dq || !aligned16(p->dout) || !aligned16(p->dq) || !aligned16(f.lse))
+    return RELATTN_ERR_INVALID_ARG;
+  if (f.r_dim > 0 && (!p->dr || !aligned16(p->dr))) return RELATTN_ERR_INVALID_ARG;
+  if (f.r_dim > 0 && f.rel_extent > 0 && (!aligned16(f.r) || !aligned16(f.P)))
+    return RELATTN_ERR_INVALID_ARG;
+  if (!p->workspace || !aligned16(p->workspace) || p->workspace_bytes < backward_workspace_bytes(f))
+    return RELATTN_ERR_WORKSPACE;
+  return RELATTN_OK;
+}
+
 relattn_status validate_prologue(const relattn_prologue_params *p) {
   if (!p) return RELATTN_ERR_INVALID_ARG;
   if (p->head_dim != kHeadDim) return RELATTN_ERR_UNSUPPORTED;
@@ -311,6 +335,67 @@ relattn_status relattn_combine(const float *o_part, const float *lse_part, int32
   return cuda_status(launch_combine(o_part, lse_part, num_splits, total_q, num_heads,
                                     static_cast<__nv_bfloat16 *>(out), lse,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+relattn_status relattn_backward_workspace_size(const relattn_bwd_params *p, size_t *bytes) {
+  if (!bytes || !p) return RELATTN_ERR_INVALID_ARG;
+  relattn_status st = validate(&p->fwd, false);
+  if (st != RELATTN_OK) return st;
+  *bytes = backward_workspace_bytes(p->fwd);
+  return RELATTN_OK;
+}
+
+relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
+  relattn_status st = validate_backward(p);
+  if (st != RELATTN_OK) return st;
+  const relattn_params &f = p->fwd;
+  if (f.batch == 0) return RELATTN_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f.total_q == 0) {   // no query sees any key: the key gradients are zero
+    const size_t n = (size_t)f.total_k * f.num_heads_kv * kHeadDim * 2;
+    if (n == 0) return RELATTN_OK;
+    if (cudaMemsetAsync(p->dk, 0, n, s) != cudaSuccess) return RELATTN_ERR_CUDA;
+    return cudaMemsetAsync(p->dv, 0, n, s) == cudaSuccess ? RELATTN_OK : RELATTN_ERR_CUDA;
+  }
+  int *err = nullptr, sms = 0;
+  if ((st = device_state(nullptr, &err, &sms)) != RELATTN_OK) return st;
+  BwdArgs a{};
+  a.q = static_cast<const __nv_bfloat16 *>(f.q);
+  a.k = static_cast<const __nv_bfloat16 *>(f.k);
+  a.v = static_cast<const __nv_bfloat16 *>(f.v);
+  a.r = static_cast<const __nv_bfloat16 *>(f.r);
+  a.P = static_cast<const __nv_bfloat16 *>(f.P);
+  a.out = static_cast<const __nv_bfloat16 *>(f.out);
+  a.dout = static_cast<const __nv_bfloat16 *>(p->dout);
+  a.lse = f.lse;
+  a.cu_q = f.cu_seqlens_q;
+  a.cu_k = f.cu_seqlens_k;
+  a.dq = static_cast<__nv_bfloat16 *>(p->dq);
+  a.dk = static_cast<__nv_bfloat16 *>(p->dk);
+  a.dv = static_cast<__nv_bfloat16 *>(p->dv);
+  a.dr = f.r_dim > 0 ? static_cast<__nv_bfloat16 *>(p->dr) : nullptr;
+  a.Dsum = static_cast<float *>(p->workspace);
+  a.err = err;
+  a.batch = f.batch;
+  a.total_q = f.total_q;
+  a.total_k = f.total_k;
+  a.max_q = f.max_seqlen_q;
+  a.max_k = f.max_seqlen_k;
+  a.Hq = f.num_heads_q;
+  a.Hkv = f.num_heads_kv;
+  a.group = f.num_heads_q / f.num_heads_kv;
+  const bool bias = f.r_dim > 0 && f.rel_extent > 0;
+  a.rd = f.r_dim;
+  a.rd_pad = bias ? (f.r_dim + 15) / 16 * 16 : 0;
+  a.E = bias ? f.rel_extent : 0;
+  a.window = f.window > 0 ? f.window : 0;
+  a.alpha = f.alpha;
+  a.alpha_log2e = f.alpha * kLog2e;
+  a.inv_ln_base = f.log_scale_base > 1.f ? 1.f / logf(f.log_scale_base) : 0.f;
+  a.p_vec_ok = bias && f.rel_extent % 8 == 0;
+  a.q_tiles = (f.max_seqlen_q + 63) / 64;
+  a.k_tiles = (f.max_seqlen_k + 63) / 64;
+  return cuda_status(launch_backward(a, sms, s));
 }
 
 relattn_status relattn_prologue(const relattn_prologue_params *p, void *stream) {

@@ -37,6 +37,24 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_s
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,
                            cudaStream_t stream);
 
+// Backward pass (bwd_mma.cu): gradients of sum(dout * out) w.r.t. q, k, v, r.
+struct BwdArgs {
+  const __nv_bfloat16 *q, *k, *v, *r, *P, *out, *dout;
+  const float *lse;            // [Hq, Tq] natural log (the forward's)
+  const int32_t *cu_q, *cu_k;
+  __nv_bfloat16 *dq, *dk, *dv, *dr;   // dr may be null (no bias)
+  float *Dsum;                 // workspace [Hq, Tq]: dout . out
+  int *err;
+  int batch, total_q, total_k, max_q, max_k, Hq, Hkv, group;
+  int rd, rd_pad, E, window;
+  float alpha, alpha_log2e, inv_ln_base;
+  int p_vec_ok;                // 16-byte vector loads of P allowed (E % 8 == 0)
+  int q_tiles, k_tiles;        // 64-row / 64-key tiles per sequence (max)
+};
+size_t bwd_dq_smem_bytes(int rd_pad);
+size_t bwd_dkdv_smem_bytes(int rd_pad);
+cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream);
+
 // attention prologue (prologue.cu): ShortConv + Q/K RMSNorm + KV-cache rows;
 // err = the device error word, sms = the SM count (sizes the grid).
 cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms,

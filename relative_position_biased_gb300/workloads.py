@@ -89,11 +89,14 @@ def decode_mtp_long(seed: int = 0, kv_len: int = 1 << 20) -> Workload:
                     log_scale_base=65536.0, seed=seed)
 
 
-def make_inputs(w: Workload, device: Optional[str] = None) -> Dict[str, torch.Tensor]:
+def make_inputs(w: Workload, device: Optional[str] = None,
+                with_dout: bool = False) -> Dict[str, torch.Tensor]:
     """Draw q, k, v, r, P for workload ``w`` (CPU bf16 unless ``device`` given).
 
     Returns dict with q [Tq,Hq,D], k/v [Tk,Hkv,D], r [Tq,Hq,r_dim], P [r_dim,E]
-    (bf16) and cu_seqlens_q / cu_seqlens_k (int32, [B+1]).
+    (bf16) and cu_seqlens_q / cu_seqlens_k (int32, [B+1]).  With ``with_dout``
+    a step (7) draws the upstream gradient dout [Tq,Hq,D] ~ N(0, 1) in bf16
+    (after P, so the other tensors are unchanged).
     """
     gen = torch.Generator().manual_seed(w.seed)
     if w.len_draw:
@@ -118,6 +121,8 @@ def make_inputs(w: Workload, device: Optional[str] = None) -> Dict[str, torch.Te
         "cu_seqlens_q": cu_seqlens(w.q_lens),
         "cu_seqlens_k": cu_seqlens(w.k_lens),
     }
+    if with_dout:
+        out["dout"] = normal(Tq, w.Hq, D)
     if device is not None:
         out = {k: v.to(device) for k, v in out.items()}
     return out

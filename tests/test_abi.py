@@ -95,6 +95,45 @@ def test_combine_rejects_bad_arguments(lib):
     assert rpb.relattn_combine(264, 256, 2, 4, 2, 256, 256) == 1
 
 
+def _bwd_params(fwd=None, **over):
+    base = dict(dout=1 << 22, dq=2 << 22, dk=3 << 22, dv=4 << 22, dr=5 << 22,
+                workspace=6 << 22, workspace_bytes=1 << 20)
+    base.update(over)
+    return rpb.RelattnBwdParams(fwd=fwd if fwd is not None else _params(), **base)
+
+
+def test_backward_struct_layout_matches_header(lib):
+    off = {f[0]: getattr(rpb.RelattnBwdParams, f[0]).offset for f in rpb.RelattnBwdParams._fields_}
+    assert off["dout"] == rpb.ctypes.sizeof(rpb.RelattnParams) == 152
+    assert off["workspace_bytes"] == 200 and rpb.ctypes.sizeof(rpb.RelattnBwdParams) == 208
+
+
+def test_backward_workspace_size(lib):
+    st, n = rpb.relattn_backward_workspace_size(_bwd_params())
+    assert st == 0 and n == 256            # 4 heads x 8 rows x 4 bytes, rounded up to 256
+    st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(total_q=1000)))
+    assert st == 0 and n == 16128
+
+
+@pytest.mark.parametrize("over,fwd_over,expect", [
+    (dict(dq=None), {}, 1),
+    (dict(dk=None), {}, 1),
+    (dict(dout=(1 << 22) + 8), {}, 1),      # not 16-byte aligned
+    (dict(dr=None), {}, 1),                 # r_dim 32 needs dr
+    (dict(workspace=None), {}, 5),
+    (dict(workspace_bytes=64), {}, 5),
+    (dict(), dict(r_dim=12), 2),            # r_dim not a multiple of 8
+    (dict(), dict(head_dim=64), 2),
+    (dict(), dict(lse=256 + 4), 1),         # lse not 16-byte aligned
+])
+def test_backward_rejects_bad_arguments(lib, over, fwd_over, expect):
+    assert rpb.relattn_backward(_bwd_params(fwd=_params(**fwd_over), **over)) == expect
+
+
+def test_backward_empty_batch_is_a_no_op(lib):
+    assert rpb.relattn_backward(_bwd_params(fwd=_params(batch=0, total_q=0), dq=None)) == 0
+
+
 def _prologue_params(**over):
     # fake, well separated addresses: every check fails before the device is touched
     names = ("q", "k", "v", "conv_k", "conv_v", "norm_q", "norm_k", "cu_seqlens_q",

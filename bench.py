@@ -14,7 +14,10 @@ prefill kernel time); the decode HBM throughput (GB/s of visible K/V over the
 decode call time) is reported beside it.  The attention prologue of the
 prefill chunk (ShortConv of k / v, RMSNorm of q / k, KV-cache write, conv
 state) is timed after the step, on its own, and reported under `prologue`
-in GB/s of the bytes it must move.  L2 is flushed by a 256 MiB write
+in GB/s of the bytes it must move; the backward of the prefill (dq, dk, dv,
+dr from the saved out / lse) likewise under `backward`, in TFLOP/s of its
+algorithmic flops (five 128-deep products per visible pair and head, plus
+dr in the bias band).  L2 is flushed by a 256 MiB write
 before every timed kernel; the flush is outside the timed events.  Before the
 flush the stream is held busy for about half a millisecond, so the host has
 queued the timed call (argument marshalling, tensor-map encoding, launch)
@@ -67,6 +70,8 @@ KERNEL_SOURCES = {
                "relative_position_biased_gb300/csrc/tc_common.cuh",
                "relative_position_biased_gb300/csrc/common.cuh",
                "relative_position_biased_gb300/csrc/combine.cu"],
+    "backward": ["relative_position_biased_gb300/csrc/bwd_mma.cu",
+                 "relative_position_biased_gb300/csrc/common.cuh"],
     "prologue": ["relative_position_biased_gb300/csrc/prologue.cu",
                  "relative_position_biased_gb300/csrc/tc_common.cuh",
                  "relative_position_biased_gb300/csrc/common.cuh"],
@@ -264,6 +269,33 @@ class ProloguePhase:
         self.rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"],
                           d["norm_k"], d["cu_seqlens_q"], d["cu_seqlens_k"], self.k_cache,
                           self.v_cache, q_out=self.q_out, conv_state_out=self.state)
+
+
+class BackwardPhase:
+    """The backward of the prefill workload: gradients of sum(dout * out)
+    w.r.t. q, k, v, r from the forward's saved out / lse (computed once,
+    outside the timing)."""
+
+    def __init__(self, w, rpb):
+        self.name, self.w, self.rpb = "backward", w, rpb
+        self.decode = False   # reported in TFLOP/s
+        host = W.make_inputs(w, with_dout=True)
+        d = {k: v.cuda() for k, v in host.items()}
+        self.d = d
+        self.args = [d[k] for k in ARG_ORDER]
+        self.out, self.lse = rpb.prefill(*self.args, **_kw(w))
+        self.dq, self.dk, self.dv = (torch.empty_like(d["q"]), torch.empty_like(d["k"]),
+                                     torch.empty_like(d["v"]))
+        self.dr = torch.empty_like(d["r"])
+        self.ws = torch.empty(sum(w.q_lens) * w.Hq + 64, dtype=torch.float32, device="cuda")
+        self.launches = 3    # D, dq / dr, dk / dv
+        self.flops = A.bwd_flops(w)
+
+    def run(self):
+        a = self.args
+        self.rpb.backward(a[0], a[1], a[2], a[3], a[4], self.out, self.lse, self.d["dout"],
+                          a[5], a[6], dq=self.dq, dk=self.dk, dv=self.dv, dr=self.dr,
+                          workspace=self.ws, **_kw(self.w))
 
 
 def timed_steps(phases, steps, flush):
@@ -470,8 +502,22 @@ def cpu_baseline(wl, host):
     pro = {"value": A.prologue_bytes(wp) / pdt / 1e9, "unit": "GB/s",
            "sample": f"one {wp.q_lens[0]}-row sequence x ({w.Hq} q + 2x{w.Hkv} kv) heads "
                      f"({pdt:.1f} s)"}
+    # the backward oracle over the last 64 rows of the first sequence (a
+    # chunk at the end of its 8,192 keys)
+    import oracle
+    T0 = w.q_lens[0]
+    wb = W.custom("bwd_sample", [64], [T0], w.Hq, w.Hkv, w.r_dim, w.rel_extent, window=w.window)
+    bin_ = W.make_inputs(w, with_dout=True)
+    sl = slice(T0 - 64, T0)
+    t0 = time.perf_counter()
+    oracle.backward(bin_["q"][sl], bin_["k"][:T0], bin_["v"][:T0], bin_["r"][sl], bin_["P"],
+                    bin_["dout"][sl], [0, 64], [0, T0], alpha=w.alpha, window=w.window)
+    bdt = time.perf_counter() - t0
+    bwd = {"value": A.bwd_flops(wb) / bdt / 1e12, "unit": "TFLOP/s",
+           "sample": f"the last 64 rows x {w.Hq} heads of one {T0}-token sequence ({bdt:.1f} s, "
+                     f"{w.Hkv} threads: one task per kv head)"}
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "prologue": pro,
+            "prologue": pro, "backward": bwd,
             "sample": f"{n} random query rows x {w.Hq} heads of {w.name} ({dt:.1f} s)",
             "decode": {"value": decode_rows_bytes(wd, drows) / ddt / 1e9, "unit": "GB/s",
                        "sample": f"all {len(drows)} query rows x {wd.Hq} heads of {wd.name} ({ddt:.1f} s)"}}
@@ -490,6 +536,8 @@ def gpu_arm(args):
     wl = step_workloads()
     if args.only == "prologue":
         return single_phase(args, ProloguePhase(wl["prefill"], rpb))
+    if args.only == "backward":
+        return single_phase(args, BackwardPhase(wl["prefill"], rpb))
     if args.only:
         wl = {args.only: wl[args.only]}
     host = {k: W.make_inputs(w) for k, w in wl.items()}
@@ -525,6 +573,16 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     if rpb.relattn_get_device_error() != 0:
         raise SystemExit("device error word set by the prologue")
+    # the backward of the prefill, timed on its own
+    bwd = BackwardPhase(wl["prefill"], rpb)
+    for _ in range(args.warmup):
+        bwd.run()
+    torch.cuda.synchronize()
+    bwd_t = timed_steps([bwd], max(2, min(args.steps, 5)), flush)["backward"]
+    torch.cuda.synchronize()
+    if rpb.relattn_get_device_error() != 0:
+        raise SystemExit("device error word set by the backward")
+    del bwd.d, bwd.dq, bwd.dk, bwd.dv, bwd.dr, bwd.out, bwd.lse, bwd.args
 
     e2e_t = e2e_steps(phases, max(1, min(args.steps, 5)), flush)
     torch.cuda.synchronize()
@@ -540,6 +598,8 @@ def gpu_arm(args):
     step_ms = max_over_ranks(step_ms, dist)
     pro_ms = max_over_ranks(sum(pro_t) / len(pro_t), dist)
     pro_gbs = pro.bytes / (pro_ms * 1e-3) / 1e9
+    bwd_ms = max_over_ranks(sum(bwd_t) / len(bwd_t), dist)
+    bwd_tf = bwd.flops / (bwd_ms * 1e-3) / 1e12
     value = ws * pre.flops / (pre_ms * 1e-3) / 1e12
     peaks, peak_kind = load_peaks()
     tf_peak = peaks["bf16_tflops"]
@@ -605,6 +665,16 @@ def gpu_arm(args):
             "roofline": {"bound": "hbm", "achieved": pro_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": pro_gbs / hbm_peak, "traffic": load_traffic("prologue"),
                          "peak_source": f"{peak_kind} HBM copy"}},
+        "backward": {
+            "value": ws * bwd_tf, "unit": "TFLOP/s", "ms": bwd_ms, "workload": pre.w.name,
+            "what": "dq, dk, dv, dr of sum(dout * out), P frozen", "flops": bwd.flops,
+            "launches": len(bwd_t) * bwd.launches,
+            "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": tf_peak,
+                         "unit": "TFLOP/s", "frac": bwd_tf / tf_peak,
+                         "traffic": load_traffic("backward"),
+                         "peak_source": f"{peak_kind} bf16 dense (burst)",
+                         "kernel": "relattn_bwd_dot_kernel + relattn_bwd_dq_kernel + "
+                                   "relattn_bwd_dkdv_kernel (mma.sync)"}},
         "e2e": {"value": ws * pre.flops / (e2e_pre * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": pre.h2d + dl.h2d + db.h2d,
                 "d2h_bytes_per_step": pre.d2h + dl.d2h + db.d2h,
@@ -646,7 +716,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched", "prologue"],
+    ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched", "prologue",
+                                       "backward"],
                     help="time one phase alone (profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:

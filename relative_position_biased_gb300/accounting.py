@@ -55,6 +55,14 @@ def flops(w: Workload, rows=None) -> int:
     return w.Hq * (4 * D * visible_pairs(w, rows) + 2 * w.r_dim * band_pairs(w, rows))
 
 
+def bwd_flops(w: Workload, rows=None) -> int:
+    """Backward: per head and visible pair the five products S, dP, dV, dK, dQ
+    (2*128 flops each, 2.5x the forward's two), and per band (i, d) pair
+    2*r_dim for dr = dR . P^T.  Recomputation beyond S is not counted."""
+    D = w.head_dim
+    return w.Hq * (10 * D * visible_pairs(w, rows) + 2 * w.r_dim * band_pairs(w, rows))
+
+
 def kv_bytes(w: Workload) -> int:
     """bf16 K and V rows visible to at least one query of each sequence."""
     tot = 0

@@ -34,8 +34,9 @@ namespace relattn {
 namespace {
 
 constexpr int BT = 64;              // query rows and keys per tile
-constexpr int NWB = 4;              // warps per CTA (16 rows or keys each)
+constexpr int NWB = 8;              // warps per CTA: 4 groups of 16 rows (or keys) x 2 halves
 constexpr int NTB = NWB * 32;
+constexpr int NGRP = 4;             // 16-row (16-key) groups per 64-row (64-key) tile
 constexpr int BSTAGES = 2;
 constexpr int RWQ = 88;             // dq kernel: R / dS window columns per warp
 constexpr int DSW = 104;            // bf16 row stride of the dS window (96 used)
@@ -112,9 +113,9 @@ __global__ void __launch_bounds__(256) relattn_bwd_dot_kernel(const BwdArgs a) {
 struct DqLayout {
   static constexpr int q = 0;                              // Q tile [64][128] swizzled
   static constexpr int dout = q + BT * 256;                // dout tile
-  static constexpr int win = dout + BT * 256;              // per-warp R / dS windows (fp32 16 x 88)
+  static constexpr int win = dout + BT * 256;              // per-group R (fp32 16 x 88) / dS windows
   static constexpr int win_bytes = 16 * RWQ * 4;
-  static constexpr int kv = win + NWB * win_bytes;         // K, V ring
+  static constexpr int kv = win + NGRP * win_bytes;        // K, V ring
   static constexpr int kv_stage = BT * 256;
   static constexpr int p = kv + 2 * BSTAGES * kv_stage;    // P slice ring
   __host__ __device__ static int p_stage(int rd_pad) { return rd_pad * (PWQ + 8) * 2; }
@@ -123,12 +124,16 @@ struct DqLayout {
   __host__ __device__ static int total(int rd_pad) { return r(rd_pad) + BT * r_stride(rd_pad); }
 };
 
+// Warp (rw, kh) takes query rows 16 rw .. 16 rw + 15 and keys 32 kh .. 32 kh + 31
+// of every key tile; the two warps of a row group share that group's R / dS
+// window and sum their partial dq / dr at the end.
 __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using L = DqLayout;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_addr(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, qq = lane & 3;
+  const int rw = warp & (NGRP - 1), kh = warp / NGRP;
 
   const int q_tile = a.q_tiles - 1 - blockIdx.x;   // longest first
   const int h = blockIdx.y, b = blockIdx.z;
@@ -185,12 +190,12 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     cp_async_commit();
   }
 
-  // per-row constants: the two rows gq, gq + 8 of this warp
+  // per-row constants: the two rows gq, gq + 8 of this group
   float cqk[2], cbias[2], lse2[2], Dr[2], srow[2];
   int pos[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const int rl = min(warp * 16 + gq + 8 * r, nrows - 1);
+    const int rl = min(rw * 16 + gq + 8 * r, nrows - 1);
     pos[r] = off + row0 + rl;
     srow[r] = log_scale(pos[r], a.inv_ln_base);
     cqk[r] = a.alpha_log2e * srow[r];
@@ -198,16 +203,17 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     lse2[r] = a.lse[(size_t)h * a.total_q + cq + row0 + rl] * kLog2e;
     Dr[r] = a.Dsum[(size_t)h * a.total_q + cq + row0 + rl];
   }
-  const int p_w0 = off + row0 + min(warp * 16, nrows - 1);
+  const int p_w0 = off + row0 + min(rw * 16, nrows - 1);
 
   float dq[16][4], dr[8][4];
 #pragma unroll
   for (int n = 0; n < 16; ++n) dq[n][0] = dq[n][1] = dq[n][2] = dq[n][3] = 0.f;
 #pragma unroll
   for (int n = 0; n < 8; ++n) dr[n][0] = dr[n][1] = dr[n][2] = dr[n][3] = 0.f;
-  float *win = reinterpret_cast<float *>(smem + L::win + warp * L::win_bytes);
-  const uint32_t win_s = sbase + L::win + warp * L::win_bytes;
-  const int arow = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);   // A-operand ldmatrix row
+  float *win = reinterpret_cast<float *>(smem + L::win + rw * L::win_bytes);
+  const uint32_t win_s = sbase + L::win + rw * L::win_bytes;
+  const int arow = rw * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);   // A-operand ldmatrix row
+  const int kb0 = 32 * kh;                                            // this warp's first key
 
   for (int it = 0; it < ntiles; ++it) {
     cp_async_wait<BSTAGES - 2>();
@@ -217,11 +223,53 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     const int st = it % BSTAGES, j0 = tile_j0(it);
     const uint32_t kb = sbase + L::kv + st * L::kv_stage;
     const uint32_t vb = sbase + L::kv + (BSTAGES + st) * L::kv_stage;
+    const bool band = is_band(j0);
+    const int cb = floor8(p_min - j0 - BT), cbw = floor8(p_w0 - j0 - BT), coloff = cbw - cb;
+    const uint32_t pb = sbase + L::p + st * L::p_stage(a.rd_pad);
 
-    // ---- S = Q K^T and dP = dout V^T (16 x 64 per warp)
-    float s[8][4], dp[8][4];
+    if (band) {
+      // the group's R window = r_rows . P[:, cbw .. cbw + 88) (fp32); warp kh
+      // computes n8 tiles [6 kh, 6 kh + 6) of the 11
+      const uint32_t rb = sbase + L::r(a.rd_pad);
+      const int rstride = L::r_stride(a.rd_pad);
+      constexpr int NH = 6;
+      const int nt0 = NH * kh;
+      float racc[NH][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < NH; ++n) racc[n][0] = racc[n][1] = racc[n][2] = racc[n][3] = 0.f;
+      for (int kk = 0; kk < a.rd_pad / 16; ++kk) {
+        uint32_t ra[4];
+        ldsm_x4_n(rb + arow * rstride + (kk * 16 + ((lane >> 4) << 3)) * 2, ra);
+        const int prow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int np = 0; np < NH / 2; ++np) {
+          const int nt = nt0 + 2 * np;
+          if (nt + 1 < RWQ / 8) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(pb + (prow * (PWQ + 8) + coloff + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
+            mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
+            mma_bf16_16816(racc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
+          } else if (nt < RWQ / 8) {
+            uint32_t b0, b1;
+            ldsm_x2_t(pb + (prow * (PWQ + 8) + coloff + nt * 8) * 2, b0, b1);
+            mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NH; ++n) {
+        const int nt = nt0 + n;
+        if (nt < RWQ / 8) {
+          *reinterpret_cast<float2 *>(&win[gq * RWQ + nt * 8 + 2 * qq]) = make_float2(racc[n][0], racc[n][1]);
+          *reinterpret_cast<float2 *>(&win[(gq + 8) * RWQ + nt * 8 + 2 * qq]) = make_float2(racc[n][2], racc[n][3]);
+        }
+      }
+    }
+
+    // ---- S = Q K^T and dP = dout V^T (16 rows x this warp's 32 keys)
+    float s[4][4], dp[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
       s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
       dp[n][0] = dp[n][1] = dp[n][2] = dp[n][3] = 0.f;
     }
@@ -231,8 +279,8 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
       ldsm_x4_n(sbase + L::q + swz(arow, 2 * kk + (lane >> 4)), qa);
       ldsm_x4_n(sbase + L::dout + swz(arow, 2 * kk + (lane >> 4)), da);
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int row = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+      for (int np = 0; np < 2; ++np) {
+        const int row = kb0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int c = 2 * kk + ((lane >> 3) & 1);
         uint32_t kf[4], vf[4];
         ldsm_x4_n(kb + swz(row, c), kf);
@@ -245,64 +293,22 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     }
 
     // ---- logits in log2 units: s_i log2e (alpha q.k + bias)
-    const bool band = is_band(j0);
-    const int cb = floor8(p_min - j0 - BT), cbw = floor8(p_w0 - j0 - BT), coloff = cbw - cb;
-    const uint32_t pb = sbase + L::p + st * L::p_stage(a.rd_pad);
     if (band) {
-      // R window = r_rows . P[:, cbw .. cbw + 88) (fp32), gathered per score
-      const uint32_t rb = sbase + L::r(a.rd_pad);
-      const int rstride = L::r_stride(a.rd_pad);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        constexpr int NH = 6;
-        const int nt0 = half ? NH : 0;
-        float racc[NH][4];
-#pragma unroll
-        for (int n = 0; n < NH; ++n) racc[n][0] = racc[n][1] = racc[n][2] = racc[n][3] = 0.f;
-        for (int kk = 0; kk < a.rd_pad / 16; ++kk) {
-          uint32_t ra[4];
-          ldsm_x4_n(rb + arow * rstride + (kk * 16 + ((lane >> 4) << 3)) * 2, ra);
-          const int prow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-          for (int np = 0; np < NH / 2; ++np) {
-            const int nt = nt0 + 2 * np;
-            if (nt + 1 < RWQ / 8) {
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4_t(pb + (prow * (PWQ + 8) + coloff + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
-              mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
-              mma_bf16_16816(racc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
-            } else if (nt < RWQ / 8) {
-              uint32_t b0, b1;
-              ldsm_x2_t(pb + (prow * (PWQ + 8) + coloff + nt * 8) * 2, b0, b1);
-              mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
-            }
-          }
-        }
-#pragma unroll
-        for (int n = 0; n < NH; ++n) {
-          const int nt = nt0 + n;
-          if (nt < RWQ / 8) {
-            *reinterpret_cast<float2 *>(&win[gq * RWQ + nt * 8 + 2 * qq]) = make_float2(racc[n][0], racc[n][1]);
-            *reinterpret_cast<float2 *>(&win[(gq + 8) * RWQ + nt * 8 + 2 * qq]) = make_float2(racc[n][2], racc[n][3]);
-          }
-        }
-      }
-      __syncwarp();
+      __syncthreads();                   // the group's window is complete
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const float *rrow = win + (gq + 8 * r) * RWQ + (pos[r] - j0 - cbw);
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < 4; ++n)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int bcol = n * 8 + 2 * qq + e;
+            const int bcol = kb0 + n * 8 + 2 * qq + e;
             s[n][2 * r + e] = fmaf(s[n][2 * r + e], cqk[r], rrow[-bcol] * cbias[r]);
           }
       }
-      __syncwarp();
     } else {
 #pragma unroll
-      for (int n = 0; n < 8; ++n) {
+      for (int n = 0; n < 4; ++n) {
         s[n][0] *= cqk[0];
         s[n][1] *= cqk[0];
         s[n][2] *= cqk[1];
@@ -316,12 +322,12 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
 #pragma unroll
     for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float x = s[n][2 * r + e];
           if (need_mask) {
-            const int j = j0 + n * 8 + 2 * qq + e;
+            const int j = j0 + kb0 + n * 8 + 2 * qq + e;
             const bool vis = j <= pos[r] && (a.window <= 0 || pos[r] - j < a.window);
             if (!vis) x = -INFINITY;
           }
@@ -329,16 +335,16 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
           s[n][2 * r + e] = p * (dp[n][2 * r + e] - Dr[r]);   // s now holds dS
         }
 
-    // ---- dq += dS K  (K with keys as the reduction dim: transposed loads)
+    // ---- dq += dS K  (this warp's keys as the reduction dim: transposed loads)
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < 2; ++kk) {
       const uint32_t a0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
       const uint32_t a1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
       const uint32_t a2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
       const uint32_t a3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
 #pragma unroll
       for (int dpi = 0; dpi < 8; ++dpi) {
-        const int row = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int row = kb0 + kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int c = 2 * dpi + (lane >> 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(kb + swz(row, c), b0, b1, b2, b3);
@@ -350,22 +356,26 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     // ---- dr += (dS sheared to [row, distance]) . P_slice^T inside the band
     if (band) {
       // window column c holds distance cbw + c; row gq + 8r, key j0 + bcol sits
-      // at column pos - j0 - bcol - cbw (always inside [0, 88) for this warp)
+      // at column pos - j0 - bcol - cbw (always inside [0, 88) for this group)
+      __syncthreads();                   // both warps of the group read their R
       __nv_bfloat16 *dsw = reinterpret_cast<__nv_bfloat16 *>(win);
-      for (int idx = lane; idx < 16 * DSW / 8; idx += 32)
+      for (int idx = 32 * kh + lane; idx < 16 * DSW / 8; idx += 64)
         reinterpret_cast<uint4 *>(dsw)[idx] = make_uint4(0u, 0u, 0u, 0u);
-      __syncwarp();
+      __syncthreads();
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         __nv_bfloat16 *drow = dsw + (gq + 8 * r) * DSW + (pos[r] - j0 - cbw);
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < 4; ++n)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) drow[-(n * 8 + 2 * qq + e)] = __float2bfloat16_rn(s[n][2 * r + e]);
+          for (int e = 0; e < 2; ++e)
+            drow[-(kb0 + n * 8 + 2 * qq + e)] = __float2bfloat16_rn(s[n][2 * r + e]);
       }
-      __syncwarp();
+      __syncthreads();
+      // warp kh takes k16 steps [3 kh, 3 kh + 3) of the window's 6
 #pragma unroll
-      for (int kk = 0; kk < 6; ++kk) {
+      for (int ks = 0; ks < 3; ++ks) {
+        const int kk = 3 * kh + ks;
         uint32_t wa[4];
         {
           const int row = (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -374,28 +384,51 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
         for (int np = 0; np < a.rd_pad / 16; ++np) {
           const int prow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
           const int pcol = coloff + kk * 16 + (((lane >> 3) & 1) << 3);
-          uint32_t b[4];
-          ldsm_x4_n(pb + (prow * (PWQ + 8) + pcol) * 2, b);
-          // (rd_pad / 16 is 1..4: unrolled by hand for the accumulator index)
-          if (np == 0) { mma_bf16_16816(dr[0], wa[0], wa[1], wa[2], wa[3], b[0], b[1]);
-                         mma_bf16_16816(dr[1], wa[0], wa[1], wa[2], wa[3], b[2], b[3]); }
-          if (np == 1) { mma_bf16_16816(dr[2], wa[0], wa[1], wa[2], wa[3], b[0], b[1]);
-                         mma_bf16_16816(dr[3], wa[0], wa[1], wa[2], wa[3], b[2], b[3]); }
-          if (np == 2) { mma_bf16_16816(dr[4], wa[0], wa[1], wa[2], wa[3], b[0], b[1]);
-                         mma_bf16_16816(dr[5], wa[0], wa[1], wa[2], wa[3], b[2], b[3]); }
-          if (np == 3) { mma_bf16_16816(dr[6], wa[0], wa[1], wa[2], wa[3], b[0], b[1]);
-                         mma_bf16_16816(dr[7], wa[0], wa[1], wa[2], wa[3], b[2], b[3]); }
+          uint32_t bq[4];
+          ldsm_x4_n(pb + (prow * (PWQ + 8) + pcol) * 2, bq);
+          // (rd_pad / 16 is 1..4: the accumulator index spelled out per case)
+          if (np == 0) { mma_bf16_16816(dr[0], wa[0], wa[1], wa[2], wa[3], bq[0], bq[1]);
+                         mma_bf16_16816(dr[1], wa[0], wa[1], wa[2], wa[3], bq[2], bq[3]); }
+          if (np == 1) { mma_bf16_16816(dr[2], wa[0], wa[1], wa[2], wa[3], bq[0], bq[1]);
+                         mma_bf16_16816(dr[3], wa[0], wa[1], wa[2], wa[3], bq[2], bq[3]); }
+          if (np == 2) { mma_bf16_16816(dr[4], wa[0], wa[1], wa[2], wa[3], bq[0], bq[1]);
+                         mma_bf16_16816(dr[5], wa[0], wa[1], wa[2], wa[3], bq[2], bq[3]); }
+          if (np == 3) { mma_bf16_16816(dr[6], wa[0], wa[1], wa[2], wa[3], bq[0], bq[1]);
+                         mma_bf16_16816(dr[7], wa[0], wa[1], wa[2], wa[3], bq[2], bq[3]); }
         }
       }
-      __syncwarp();
     }
   }
   cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- the key-half 1 warps' partial dq / dr through shared memory (the K / V ring is free)
+  float *part = reinterpret_cast<float *>(smem + L::kv);   // [4 groups][24 n8][4][32 lanes]
+  if (kh == 1) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) part[((rw * 24) + n) * 128 + c * 32 + lane] = dq[n][c];
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) part[((rw * 24) + 16 + n) * 128 + c * 32 + lane] = dr[n][c];
+  }
+  __syncthreads();
+  if (kh == 1) return;
+#pragma unroll
+  for (int n = 0; n < 16; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dq[n][c] += part[((rw * 24) + n) * 128 + c * 32 + lane];
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dr[n][c] += part[((rw * 24) + 16 + n) * 128 + c * 32 + lane];
 
   // ---- epilogue: dq = s alpha acc, dr = s acc (bf16)
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const int rl = warp * 16 + gq + 8 * r;
+    const int rl = rw * 16 + gq + 8 * r;
     if (rl >= nrows) continue;
     const size_t row = (size_t)(cq + row0 + rl) * a.Hq + h;
     const float fq = srow[r] * a.alpha;
@@ -513,11 +546,14 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
     dk[n][0] = dk[n][1] = dk[n][2] = dk[n][3] = 0.f;
     dv[n][0] = dv[n][1] = dv[n][2] = dv[n][3] = 0.f;
   }
-  const int arow = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);   // A-operand ldmatrix row
+  // warp (rw, kh): keys 16 rw .. 16 rw + 15 of the tile, query rows 32 kh .. 32 kh + 31
+  // of each query tile; the two halves' dk / dv are summed at the end
+  const int rw = warp & (NGRP - 1), kh = warp / NGRP;
+  const int arow = rw * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);     // A-operand ldmatrix row
   int jk[2];                                                             // the thread's two keys
-  jk[0] = j0 + warp * 16 + gq;
+  jk[0] = j0 + rw * 16 + gq;
   jk[1] = jk[0] + 8;
-  float *rw = reinterpret_cast<float *>(smem + L::rwin);
+  float *rwin = reinterpret_cast<float *>(smem + L::rwin);
 
   for (int it = 0; it < npairs; ++it) {
     cp_async_wait<BSTAGES - 2>();
@@ -538,10 +574,11 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
       const uint32_t rb = sb + L::s_r;
       const uint32_t pb = sb + L::s_p(a.rd_pad);
       const int rstride = L::r_stride(a.rd_pad);
+      // warp (rw, kh): rows 16 rw .. 16 rw + 15, n8 tiles [9 kh, 9 kh + 9) of the 17
 #pragma unroll
-      for (int pass = 0; pass < 3; ++pass) {
+      for (int pass = 0; pass < 2; ++pass) {
         constexpr int NH = 6;
-        const int nt0 = pass * NH;
+        const int nt0 = 9 * kh + pass * NH, nt_end = min(9 * kh + 9, PWK / 8);
         float racc[NH][4];
 #pragma unroll
         for (int n = 0; n < NH; ++n) racc[n][0] = racc[n][1] = racc[n][2] = racc[n][3] = 0.f;
@@ -552,12 +589,12 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
 #pragma unroll
           for (int np = 0; np < NH / 2; ++np) {
             const int nt = nt0 + 2 * np;
-            if (nt + 1 < PWK / 8) {
+            if (nt + 1 < nt_end) {
               uint32_t b0, b1, b2, b3;
               ldsm_x4_t(pb + (prow * (PWK + 8) + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
               mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
               mma_bf16_16816(racc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
-            } else if (nt < PWK / 8) {
+            } else if (nt < nt_end) {
               uint32_t b0, b1;
               ldsm_x2_t(pb + (prow * (PWK + 8) + nt * 8) * 2, b0, b1);
               mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
@@ -567,9 +604,9 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
 #pragma unroll
         for (int n = 0; n < NH; ++n) {
           const int nt = nt0 + n;
-          if (nt < PWK / 8) {
+          if (nt < nt_end) {
             const int c = nt * 8 + 2 * qq;
-            float *r0 = rw + (warp * 16 + gq) * RSK + c;
+            float *r0 = rwin + (rw * 16 + gq) * RSK + c;
             float *r1 = r0 + 8 * RSK;
             r0[0] = racc[n][0];
             r0[1] = racc[n][1];
@@ -583,8 +620,8 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
 
     const bool need_mask = (j0 + BT - 1 > pos0) ||
                            (a.window > 0 && j0 < pos0 + BT - 1 - a.window + 1) || (t0 + BT > Lq);
-#pragma unroll 1
-    for (int qc = 0; qc < BT; qc += 32) {
+    {
+      const int qc = 32 * kh;
       // ---- S^T = K_w Q^T and dP^T = V_w dout^T (16 keys x 32 queries)
       float st[4][4], dpt[4][4];
 #pragma unroll
@@ -623,7 +660,7 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
             float x = st[n][2 * rr + e] * a.alpha;
             if (band) {
               const int d = pos - jk[rr];
-              x += rw[il * RSK + d - cb];
+              x += rwin[il * RSK + d - cb];
             }
             x *= sc * kLog2e;
             if (need_mask) {
@@ -662,11 +699,33 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
     }
   }
   cp_async_wait<0>();
+  __syncthreads();
+
+  // ---- the second half's partial dk / dv through shared memory (the ring is free)
+  float *part = reinterpret_cast<float *>(smem + L::ring);   // [4 groups][2][16 n8][4][32 lanes]
+  if (kh == 1) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        part[((rw * 2 + 0) * 64 + n * 4 + c) * 32 + lane] = dk[n][c];
+        part[((rw * 2 + 1) * 64 + n * 4 + c) * 32 + lane] = dv[n][c];
+      }
+  }
+  __syncthreads();
+  if (kh == 1) return;
+#pragma unroll
+  for (int n = 0; n < 16; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      dk[n][c] += part[((rw * 2 + 0) * 64 + n * 4 + c) * 32 + lane];
+      dv[n][c] += part[((rw * 2 + 1) * 64 + n * 4 + c) * 32 + lane];
+    }
 
   // ---- epilogue (keys of the tile that no query sees get zeros)
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
-    const int kl = warp * 16 + gq + 8 * rr;
+    const int kl = rw * 16 + gq + 8 * rr;
     if (kl >= nkeys) continue;
     const size_t row = (size_t)(ck + j0 + kl) * a.Hkv + g;
     __nv_bfloat16 *dkd = a.dk + row * kHeadDim + 2 * qq;

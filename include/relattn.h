@@ -120,6 +120,34 @@ relattn_status relattn_decode_workspace_size(const relattn_params *params, size_
 relattn_status relattn_decode_num_splits(const relattn_params *params, int32_t *num_splits);
 
 /*
+ * Decode against a paged KV cache.  The keys of each sequence live in
+ * fixed-size pages of a pool: key p of sequence b sits at pool row
+ * block_table[b * max_pages_per_seq + p / page_size] * page_size + p % page_size
+ * of params->k / params->v (bf16 [num_pages * page_size, num_heads_kv, 128]).
+ * cu_seqlens_k keeps its meaning as cumulative key counts (Lk_b =
+ * cu_seqlens_k[b+1] - cu_seqlens_k[b]); total_k is their sum (used for
+ * planning only).  Everything else, including the split plan, the workspace
+ * (relattn_decode_workspace_size) and the results, is relattn_decode's:
+ * same arithmetic, bit-identical out / lse.  The pages give no paging
+ * scheme; this is the block-table layout of paged serving caches.
+ * Requirements: page_size a multiple of 128 (a 128-key tile stays inside a
+ * page), max_pages_per_seq * page_size >= max_seqlen_k, num_pages *
+ * page_size < 2^31, and the shapes the tcgen05 kernel takes (16-byte aligned
+ * pointers; with a bias r_dim and E multiples of 8, r_dim <= 64, E >= 64);
+ * else RELATTN_ERR_UNSUPPORTED.  A block-table entry outside [0, num_pages)
+ * makes its keys read as zero and records RELATTN_ERR_DEVICE_ARGS.
+ */
+typedef struct relattn_paged_kv {
+  const int32_t *block_table;  /* device int32 [batch, max_pages_per_seq]: pool page per block */
+  int32_t max_pages_per_seq;
+  int32_t page_size;           /* keys per page, a multiple of 128 */
+  int32_t num_pages;           /* pages in the k / v pools */
+} relattn_paged_kv;
+
+relattn_status relattn_decode_paged(const relattn_params *params, const relattn_paged_kv *kv,
+                                   void *stream);
+
+/*
  * Log-sum-exp combine of split partials (the decode combine step, exposed so
  * partials from several KV shards can be merged):
  *   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.

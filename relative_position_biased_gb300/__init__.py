@@ -33,6 +33,7 @@ EXPORTED = (
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
     "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
     "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
+    "relattn_decode_paged",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -58,6 +59,12 @@ class RelattnParams(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("num_splits", ctypes.c_int32),
     ]
+
+
+class RelattnPagedKV(ctypes.Structure):
+    """Mirror of ``relattn_paged_kv``."""
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
 
 
 class RelattnBwdParams(ctypes.Structure):
@@ -128,6 +135,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_test_skip_k_tile.restype = ctypes.c_int
         lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
         lib.relattn_test_band_ctas.restype = ctypes.c_int
+        lib.relattn_decode_paged.argtypes = [P, ctypes.POINTER(RelattnPagedKV), vp]
+        lib.relattn_decode_paged.restype = ctypes.c_int
         BP = ctypes.POINTER(RelattnBwdParams)
         lib.relattn_backward.argtypes = [BP, vp]
         lib.relattn_backward.restype = ctypes.c_int
@@ -199,6 +208,11 @@ def relattn_test_band_ctas(n: int) -> int:
 
 def relattn_status_string(status: int) -> str:
     return load_library().relattn_status_string(status).decode()
+
+
+def relattn_decode_paged(params: RelattnParams, kv: RelattnPagedKV, stream: int = 0) -> int:
+    return load_library().relattn_decode_paged(ctypes.byref(params), ctypes.byref(kv),
+                                               ctypes.c_void_p(stream))
 
 
 def relattn_backward(params: RelattnBwdParams, stream: int = 0) -> int:
@@ -328,6 +342,32 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
     _check(relattn_prologue(prm, _current_stream() if stream is None else stream),
            "relattn_prologue")
     return q_out
+
+
+def decode_paged(q, k_pool, v_pool, r, P, cu_seqlens_q, cu_seqlens_k, block_table, *,
+                 page_size: int, max_seqlen_q: int, max_seqlen_k: int, alpha: float,
+                 window: int = 0, log_scale_base: float = 0.0, num_splits: int = 0,
+                 out=None, lse=None, workspace=None, stream: Optional[int] = None):
+    """Split-KV decode against a paged KV cache: k_pool / v_pool [num_pages *
+    page_size, Hkv, 128], block_table int32 [batch, max_pages_per_seq] on the
+    device; cu_seqlens_k holds cumulative key counts.  Returns (out, lse)."""
+    out, lse = _outputs(q, out, lse)
+    total_k = int(cu_seqlens_k[-1].item())
+    prm = make_params(q, k_pool, v_pool, r, P, cu_seqlens_q, cu_seqlens_k,
+                      max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, alpha=alpha,
+                      window=window, log_scale_base=log_scale_base, out=out, lse=lse,
+                      num_splits=num_splits, total_k=total_k)
+    if workspace is None:
+        workspace = decode_workspace(prm, q.device)
+    if workspace is not None:
+        prm.workspace = workspace.data_ptr()
+        prm.workspace_bytes = workspace.numel() * workspace.element_size()
+    kv = RelattnPagedKV(block_table=block_table.data_ptr(),
+                        max_pages_per_seq=int(block_table.shape[1]), page_size=int(page_size),
+                        num_pages=int(k_pool.shape[0]) // int(page_size))
+    _check(relattn_decode_paged(prm, kv, _current_stream() if stream is None else stream),
+           "relattn_decode_paged")
+    return out, lse
 
 
 def backward(q, k, v, r, P, out, lse, dout, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int,

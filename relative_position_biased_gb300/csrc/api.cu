@@ -118,7 +118,9 @@ struct DecodePlan {
   size_t ws_bytes, lse_offset;
 };
 
-relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
+// kv_rows: rows of the K / V tensors the kernels address (total_k, or the
+// page pool's rows for paged K / V)
+relattn_status plan_decode(const relattn_params *p, DecodePlan *plan, long kv_rows = -1) {
   int sms = 0;
   relattn_status st = device_state(nullptr, nullptr, &sms);
   if (st != RELATTN_OK) return st;
@@ -126,7 +128,7 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan) {
   const int rows = p->max_seqlen_q * group;
   KernelArgs probe;
   if ((st = make_args(p, &probe)) != RELATTN_OK) return st;
-  plan->tc = tc_supported(probe, p->total_k);
+  plan->tc = tc_supported(probe, kv_rows >= 0 ? (int)kv_rows : p->total_k);
   plan->warps = decode_warps_for_rows(rows < 128 ? rows : 128);
   const int m = plan->tc ? kTcDecodeRows : plan->warps * 16;
   plan->row_blocks = (rows + m - 1) / m;
@@ -318,6 +320,46 @@ relattn_status relattn_decode(const relattn_params *p, void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = plan.tc ? cuda_status(launch_decode_tc(a, p->total_k, s))
                : cuda_status(launch_decode_mma(a, plan.warps, s));
+  if (st != RELATTN_OK) return st;
+  if (plan.splits > 1)
+    st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
+                                    p->num_heads_q, a.out, a.lse, s));
+  return st;
+}
+
+relattn_status relattn_decode_paged(const relattn_params *p, const relattn_paged_kv *kv,
+                                   void *stream) {
+  relattn_status st = validate(p, true);
+  if (st != RELATTN_OK) return st;
+  if (!kv) return RELATTN_ERR_INVALID_ARG;
+  if (kv->page_size <= 0 || kv->page_size % kTcKeyTile != 0) return RELATTN_ERR_UNSUPPORTED;
+  if (kv->num_pages <= 0 || kv->max_pages_per_seq <= 0) return RELATTN_ERR_INVALID_ARG;
+  if ((long)kv->num_pages * kv->page_size > 0x7fffffffL) return RELATTN_ERR_UNSUPPORTED;
+  if ((long)kv->max_pages_per_seq * kv->page_size < p->max_seqlen_k) return RELATTN_ERR_INVALID_ARG;
+  if (!kv->block_table || (reinterpret_cast<uintptr_t>(kv->block_table) & 3u) != 0)
+    return RELATTN_ERR_INVALID_ARG;
+  if (p->batch == 0 || p->total_q == 0) return RELATTN_OK;
+  const long pool_rows = (long)kv->num_pages * kv->page_size;
+  DecodePlan plan;
+  if ((st = plan_decode(p, &plan, pool_rows)) != RELATTN_OK) return st;
+  if (!plan.tc) return RELATTN_ERR_UNSUPPORTED;   // paged K / V: the tcgen05 kernel only
+  KernelArgs a;
+  if ((st = make_args(p, &a)) != RELATTN_OK) return st;
+  a.num_splits = plan.splits;
+  a.split_chunk = plan.chunk;
+  a.row_blocks = plan.row_blocks;
+  a.block_table = kv->block_table;
+  a.page_size = kv->page_size;
+  a.max_pages = kv->max_pages_per_seq;
+  a.num_pages = kv->num_pages;
+  if (plan.splits > 1) {
+    if (!p->workspace || p->workspace_bytes < plan.ws_bytes || !aligned16(p->workspace))
+      return RELATTN_ERR_WORKSPACE;
+    a.o_part = static_cast<float *>(p->workspace);
+    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + plan.lse_offset);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_status(launch_decode_tc(a, (int)pool_rows, s));
   if (st != RELATTN_OK) return st;
   if (plan.splits > 1)
     st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,

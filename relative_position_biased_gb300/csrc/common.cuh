@@ -42,6 +42,11 @@ struct KernelArgs {
   int band_only;                 // prefill, bias kernel: only the key tiles of the bias band
   int init_from_out;             // prefill, main kernel: start from the band's out / lse
   int sms;                       // CTAs of a persistent launch: the SM count (or a test cap)
+  // paged K / V (decode): keys at position p of sequence b sit at pool row
+  // block_table[b * max_pages + p / page_size] * page_size + p % page_size;
+  // block_table == nullptr: contiguous rows cu_seqlens_k[b] + p
+  const int32_t *block_table;
+  int page_size, max_pages, num_pages;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

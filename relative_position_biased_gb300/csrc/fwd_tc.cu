@@ -432,7 +432,18 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
             if (!run) break;
           }
           const int kg = tb + t, vg = vslot(t);        // K / V ring index across items
-          const int key = I.ck + I.p0 - tile_D(t);     // may be < 0: the tile reads zeros there
+          int key = I.ck + I.p0 - tile_D(t);           // may be < 0: the tile reads zeros there
+          if constexpr (DECODE) {
+            if (a.block_table != nullptr) {
+              // paged: the tile (128-aligned, inside one page) -> its pool rows;
+              // a page number outside the pool reads zeros and is reported
+              const int p = I.p0 - tile_D(t);
+              const int pg = a.block_table[(size_t)I.b * a.max_pages + p / a.page_size];
+              const bool ok = pg >= 0 && pg < a.num_pages;
+              if (!ok) atomicOr(a.err, kDevErrSeqlens);
+              key = ok ? pg * a.page_size + p % a.page_size : -BN;
+            }
+          }
           if (kg >= K_STAGES && !(run = mbar_wait(bar(B_K_EMPTY + kst), kph ^ 1, abort_flag, 1))) break;
           if (kg != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
             const uint32_t dst = sb + SM_K + kst * KV_STAGE_BYTES;

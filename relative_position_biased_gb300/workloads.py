@@ -174,6 +174,39 @@ def make_prologue_inputs(w: Workload, with_state: bool = False,
     return out
 
 
+def page_kv(k: torch.Tensor, v: torch.Tensor, k_lens, page_size: int, seed: int = 0,
+            spare_pages: int = 3):
+    """Scatter contiguous K / V rows into a paged pool with a shuffled page
+    order (pure layout: copies of the same bf16 rows).
+
+    Returns (k_pool, v_pool [num_pages*page_size, Hkv, D], block_table int32
+    [B, max_pages]).  Unused block-table slots hold -1; ``spare_pages`` extra
+    pages, never referenced, sit in the pool; pool rows past a sequence's end
+    inside its last page are filled with a large value so that reading them
+    by mistake shows up in the output.
+    """
+    gen = torch.Generator().manual_seed(seed + 7777)
+    pages = [(n + page_size - 1) // page_size for n in k_lens]
+    n_pages = sum(pages) + spare_pages
+    perm = torch.randperm(n_pages, generator=gen)
+    Hkv, D = k.shape[1], k.shape[2]
+    k_pool = torch.full((n_pages * page_size, Hkv, D), 1e4, dtype=k.dtype)
+    v_pool = torch.full_like(k_pool, 1e4)
+    max_pages = max(pages) if pages else 1
+    table = torch.full((len(k_lens), max(1, max_pages)), -1, dtype=torch.int32)
+    used, start = 0, 0
+    for b, n in enumerate(k_lens):
+        for i in range(pages[b]):
+            pg = int(perm[used])
+            used += 1
+            table[b, i] = pg
+            lo, hi = start + i * page_size, min(start + n, start + (i + 1) * page_size)
+            k_pool[pg * page_size: pg * page_size + (hi - lo)] = k[lo:hi]
+            v_pool[pg * page_size: pg * page_size + (hi - lo)] = v[lo:hi]
+        start += n
+    return k_pool, v_pool, table
+
+
 def cu_seqlens(lens) -> torch.Tensor:
     c = [0]
     for n in lens:

@@ -95,6 +95,22 @@ def test_combine_rejects_bad_arguments(lib):
     assert rpb.relattn_combine(264, 256, 2, 4, 2, 256, 256) == 1
 
 
+@pytest.mark.parametrize("kv_over,expect", [
+    (dict(page_size=64), 2),                  # not a multiple of 128
+    (dict(page_size=0), 2),
+    (dict(num_pages=0), 1),
+    (dict(max_pages_per_seq=0), 1),
+    (dict(block_table=None), 1),
+    (dict(block_table=(7 << 22) + 2), 1),     # not 4-byte aligned
+    (dict(max_pages_per_seq=1, page_size=128), 1),   # 1 x 128 < max_seqlen_k 200
+])
+def test_decode_paged_rejects_bad_arguments(lib, kv_over, expect):
+    kv = dict(block_table=7 << 22, max_pages_per_seq=2, page_size=128, num_pages=4)
+    kv.update(kv_over)
+    prm = _params(total_q=1, max_seqlen_q=1, max_seqlen_k=200, total_k=200)
+    assert rpb.relattn_decode_paged(prm, rpb.RelattnPagedKV(**kv)) == expect
+
+
 def _bwd_params(fwd=None, **over):
     base = dict(dout=1 << 22, dq=2 << 22, dk=3 << 22, dv=4 << 22, dr=5 << 22,
                 workspace=6 << 22, workspace_bytes=1 << 20)

@@ -17,7 +17,9 @@ state) is timed after the step, on its own, and reported under `prologue`
 in GB/s of the bytes it must move; the backward of the prefill (dq, dk, dv,
 dr from the saved out / lse) likewise under `backward`, in TFLOP/s of its
 algorithmic flops (five 128-deep products per visible pair and head, plus
-dr in the bias band).  L2 is flushed by a 256 MiB write
+dr in the bias band).  Both decodes are also timed through a paged copy of
+their K / V (128-key pages in a shuffled pool) and reported under
+`decode.paged`.  L2 is flushed by a 256 MiB write
 before every timed kernel; the flush is outside the timed events.  Before the
 flush the stream is held busy for about half a millisecond, so the host has
 queued the timed call (argument marshalling, tensor-map encoding, launch)
@@ -269,6 +271,28 @@ class ProloguePhase:
         self.rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"],
                           d["norm_k"], d["cu_seqlens_q"], d["cu_seqlens_k"], self.k_cache,
                           self.v_cache, q_out=self.q_out, conv_state_out=self.state)
+
+
+class PagedDecodePhase:
+    """A decode phase re-run against a paged copy of its K / V (128-key pages
+    in a shuffled pool, built once outside the timing)."""
+
+    def __init__(self, base, page_size, rpb):
+        self.name, self.w, self.rpb = base.name + "_paged", base.w, rpb
+        self.decode = True
+        self.base = base
+        kp, vp, table = W.page_kv(base.host["k"], base.host["v"], base.w.k_lens, page_size)
+        self.k_pool, self.v_pool, self.table = kp.cuda(), vp.cuda(), table.cuda()
+        self.page_size = page_size
+        self.launches = base.launches
+        self.bytes = base.bytes
+
+    def run(self):
+        a = self.base.args
+        self.rpb.decode_paged(a[0], self.k_pool, self.v_pool, a[3], a[4], a[5], a[6], self.table,
+                              page_size=self.page_size, total_k=sum(self.w.k_lens),
+                              out=self.base.out, lse=self.base.lse, workspace=self.base.ws,
+                              **_kw(self.w))
 
 
 class BackwardPhase:
@@ -573,6 +597,18 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     if rpb.relattn_get_device_error() != 0:
         raise SystemExit("device error word set by the prologue")
+    # both decodes again through 128-key pages of a shuffled pool
+    paged = [PagedDecodePhase(dl_p, 128, rpb) for dl_p in phases[1:]]
+    for _ in range(args.warmup):
+        for p in paged:
+            p.run()
+    torch.cuda.synchronize()
+    pg_t = timed_steps(paged, args.steps, flush)
+    torch.cuda.synchronize()
+    if rpb.relattn_get_device_error() != 0:
+        raise SystemExit("device error word set by the paged decode")
+    for p in paged:
+        del p.k_pool, p.v_pool
     # the backward of the prefill, timed on its own
     bwd = BackwardPhase(wl["prefill"], rpb)
     for _ in range(args.warmup):
@@ -598,6 +634,7 @@ def gpu_arm(args):
     step_ms = max_over_ranks(step_ms, dist)
     pro_ms = max_over_ranks(sum(pro_t) / len(pro_t), dist)
     pro_gbs = pro.bytes / (pro_ms * 1e-3) / 1e9
+    pg_ms = {p.name: max_over_ranks(sum(pg_t[p.name]) / len(pg_t[p.name]), dist) for p in paged}
     bwd_ms = max_over_ranks(sum(bwd_t) / len(bwd_t), dist)
     bwd_tf = bwd.flops / (bwd_ms * 1e-3) / 1e12
     value = ws * pre.flops / (pre_ms * 1e-3) / 1e12
@@ -657,6 +694,10 @@ def gpu_arm(args):
                          "peak_source": f"{peak_kind} HBM copy"},
             "batched": {"value": db_gbs, "unit": "GB/s", "workload": db.w.name,
                         "frac": db_gbs / hbm_peak},
+            "paged": {p.name: {"value": p.bytes / (pg_ms[p.name] * 1e-3) / 1e9, "unit": "GB/s",
+                               "ms": pg_ms[p.name], "page_size": p.page_size,
+                               "frac": p.bytes / (pg_ms[p.name] * 1e-3) / 1e9 / hbm_peak}
+                      for p in paged},
         },
         "prologue": {
             "value": ws * pro_gbs, "unit": "GB/s", "ms": pro_ms, "workload": pre.w.name,

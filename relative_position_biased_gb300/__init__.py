@@ -347,12 +347,16 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
 def decode_paged(q, k_pool, v_pool, r, P, cu_seqlens_q, cu_seqlens_k, block_table, *,
                  page_size: int, max_seqlen_q: int, max_seqlen_k: int, alpha: float,
                  window: int = 0, log_scale_base: float = 0.0, num_splits: int = 0,
-                 out=None, lse=None, workspace=None, stream: Optional[int] = None):
+                 total_k: Optional[int] = None, out=None, lse=None, workspace=None,
+                 stream: Optional[int] = None):
     """Split-KV decode against a paged KV cache: k_pool / v_pool [num_pages *
     page_size, Hkv, 128], block_table int32 [batch, max_pages_per_seq] on the
-    device; cu_seqlens_k holds cumulative key counts.  Returns (out, lse)."""
+    device; cu_seqlens_k holds cumulative key counts.  ``total_k`` (their
+    sum) sizes the split plan; when it is not given it is read back from
+    cu_seqlens_k, which waits for the stream.  Returns (out, lse)."""
     out, lse = _outputs(q, out, lse)
-    total_k = int(cu_seqlens_k[-1].item())
+    if total_k is None:
+        total_k = int(cu_seqlens_k[-1].item())
     prm = make_params(q, k_pool, v_pool, r, P, cu_seqlens_q, cu_seqlens_k,
                       max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, alpha=alpha,
                       window=window, log_scale_base=log_scale_base, out=out, lse=lse,

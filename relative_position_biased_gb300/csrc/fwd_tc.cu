@@ -417,6 +417,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           }
         }
         int c_next = I.c_start;
+        // paged decode: pool page of tile t's keys
+        auto page_of = [&](int t) {
+          return a.block_table[(size_t)I.b * a.max_pages + (I.p0 - tile_D(t)) / a.page_size];
+        };
+        int pg_next = (DECODE && a.block_table != nullptr && I.ntiles > 0) ? page_of(0) : 0;
         for (int t = 0; t < I.ntiles && run && !*abort_flag; ++t) {
           if (t < I.nb_tiles) {
             const int c_need = c_new(2 * t + 1);   // newest chunk of the tile's second half step
@@ -436,9 +441,11 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           if constexpr (DECODE) {
             if (a.block_table != nullptr) {
               // paged: the tile (128-aligned, inside one page) -> its pool rows;
-              // a page number outside the pool reads zeros and is reported
+              // a page number outside the pool reads zeros and is reported.
+              // The next tile's entry is read now, to land during this tile's waits.
               const int p = I.p0 - tile_D(t);
-              const int pg = a.block_table[(size_t)I.b * a.max_pages + p / a.page_size];
+              const int pg = pg_next;
+              if (t + 1 < I.ntiles) pg_next = page_of(t + 1);
               const bool ok = pg >= 0 && pg < a.num_pages;
               if (!ok) atomicOr(a.err, kDevErrSeqlens);
               key = ok ? pg * a.page_size + p % a.page_size : -BN;

@@ -42,6 +42,9 @@ constexpr int RWQ = 88;             // dq kernel: R / dS window columns per warp
 constexpr int DSW = 104;            // bf16 row stride of the dS window (96 used)
 constexpr int PWQ = 152;            // dq kernel: P slice columns per stage
 constexpr int PWK = 136;            // dkdv kernel: P slice / R window columns
+// bf16 row stride of a P slice: PW + pad with (PW + pad) / 8 odd, so the 8
+// rows of an ldmatrix 8x8 load fall in 8 different 16-byte bank groups
+__host__ __device__ constexpr int p_stride(int pw) { return ((pw / 8 + 1) | 1) * 8; }
 constexpr int RSK = 163;            // dkdv kernel: fp32 row stride of R (conflict-free gather)
 
 __device__ __forceinline__ int floor8(int x) { return x & ~7; }
@@ -53,11 +56,11 @@ __device__ __forceinline__ void ldsm_x4_n(uint32_t addr, uint32_t (&r)[4]) {
 // swizzled 256-byte row: 16-byte chunk c of row `row`
 __device__ __forceinline__ uint32_t swz(int row, int c) { return row * 256 + ((c ^ (row & 7)) << 4); }
 
-// P columns [cb, cb + PW) of all rd_pad channels into a [rd_pad][PW + 8] bf16
-// slice; columns outside [0, E) and channels past rd read as zero.
+// P columns [cb, cb + PW) of all rd_pad channels into a [rd_pad][p_stride(PW)]
+// bf16 slice; columns outside [0, E) and channels past rd read as zero.
 template <int PW>
 __device__ __forceinline__ void load_p_slice(const BwdArgs &a, uint32_t base, int cb, int tid) {
-  constexpr int PS = PW + 8, cpr = PW / 8;
+  constexpr int PS = p_stride(PW), cpr = PW / 8;
   for (int idx = tid; idx < a.rd_pad * cpr; idx += NTB) {
     const int c = idx / cpr, x = idx - c * cpr, col = cb + x * 8;
     const uint32_t dst = base + (c * PS + x * 8) * 2;
@@ -118,7 +121,7 @@ struct DqLayout {
   static constexpr int kv = win + NGRP * win_bytes;        // K, V ring
   static constexpr int kv_stage = BT * 256;
   static constexpr int p = kv + 2 * BSTAGES * kv_stage;    // P slice ring
-  __host__ __device__ static int p_stage(int rd_pad) { return rd_pad * (PWQ + 8) * 2; }
+  __host__ __device__ static int p_stage(int rd_pad) { return rd_pad * p_stride(PWQ) * 2; }
   __host__ __device__ static int r(int rd_pad) { return p + BSTAGES * p_stage(rd_pad); }
   __host__ __device__ static int r_stride(int rd_pad) { return (rd_pad + 8) * 2; }
   __host__ __device__ static int total(int rd_pad) { return r(rd_pad) + BT * r_stride(rd_pad); }
@@ -214,10 +217,18 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
   const uint32_t win_s = sbase + L::win + rw * L::win_bytes;
   const int arow = rw * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);   // A-operand ldmatrix row
   const int kb0 = 32 * kh;                                            // this warp's first key
+  uint32_t qa[8][4], da[8][4];   // the group's Q / dout rows as A fragments (loaded once)
 
   for (int it = 0; it < ntiles; ++it) {
     cp_async_wait<BSTAGES - 2>();
     __syncthreads();
+    if (it == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        ldsm_x4_n(sbase + L::q + swz(arow, 2 * kk + (lane >> 4)), qa[kk]);
+        ldsm_x4_n(sbase + L::dout + swz(arow, 2 * kk + (lane >> 4)), da[kk]);
+      }
+    }
     if (it + BSTAGES - 1 < ntiles) issue_tile(it + BSTAGES - 1);
     cp_async_commit();
     const int st = it % BSTAGES, j0 = tile_j0(it);
@@ -246,12 +257,12 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
           const int nt = nt0 + 2 * np;
           if (nt + 1 < RWQ / 8) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(pb + (prow * (PWQ + 8) + coloff + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
+            ldsm_x4_t(pb + (prow * p_stride(PWQ) + coloff + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
             mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
             mma_bf16_16816(racc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
           } else if (nt < RWQ / 8) {
             uint32_t b0, b1;
-            ldsm_x2_t(pb + (prow * (PWQ + 8) + coloff + nt * 8) * 2, b0, b1);
+            ldsm_x2_t(pb + (prow * p_stride(PWQ) + coloff + nt * 8) * 2, b0, b1);
             mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
           }
         }
@@ -275,9 +286,6 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     }
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      uint32_t qa[4], da[4];
-      ldsm_x4_n(sbase + L::q + swz(arow, 2 * kk + (lane >> 4)), qa);
-      ldsm_x4_n(sbase + L::dout + swz(arow, 2 * kk + (lane >> 4)), da);
 #pragma unroll
       for (int np = 0; np < 2; ++np) {
         const int row = kb0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
@@ -285,10 +293,10 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
         uint32_t kf[4], vf[4];
         ldsm_x4_n(kb + swz(row, c), kf);
         ldsm_x4_n(vb + swz(row, c), vf);
-        mma_bf16_16816(s[2 * np], qa[0], qa[1], qa[2], qa[3], kf[0], kf[1]);
-        mma_bf16_16816(s[2 * np + 1], qa[0], qa[1], qa[2], qa[3], kf[2], kf[3]);
-        mma_bf16_16816(dp[2 * np], da[0], da[1], da[2], da[3], vf[0], vf[1]);
-        mma_bf16_16816(dp[2 * np + 1], da[0], da[1], da[2], da[3], vf[2], vf[3]);
+        mma_bf16_16816(s[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kf[0], kf[1]);
+        mma_bf16_16816(s[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], kf[2], kf[3]);
+        mma_bf16_16816(dp[2 * np], da[kk][0], da[kk][1], da[kk][2], da[kk][3], vf[0], vf[1]);
+        mma_bf16_16816(dp[2 * np + 1], da[kk][0], da[kk][1], da[kk][2], da[kk][3], vf[2], vf[3]);
       }
     }
 
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
           const int prow = np * 16 + (lane & 7) + ((lane >> 4) << 3);
           const int pcol = coloff + kk * 16 + (((lane >> 3) & 1) << 3);
           uint32_t bq[4];
-          ldsm_x4_n(pb + (prow * (PWQ + 8) + pcol) * 2, bq);
+          ldsm_x4_n(pb + (prow * p_stride(PWQ) + pcol) * 2, bq);
           // (rd_pad / 16 is 1..4: the accumulator index spelled out per case)
           if (np == 0) { mma_bf16_16816(dr[0], wa[0], wa[1], wa[2], wa[3], bq[0], bq[1]);
                          mma_bf16_16816(dr[1], wa[0], wa[1], wa[2], wa[3], bq[2], bq[3]); }
@@ -461,7 +469,7 @@ struct DkvLayout {
                        s_sc = s_d + BT * 4, s_r = s_sc + BT * 4;
   __host__ __device__ static int r_stride(int rd_pad) { return (rd_pad + 8) * 2; }
   __host__ __device__ static int s_p(int rd_pad) { return s_r + BT * r_stride(rd_pad); }
-  __host__ __device__ static int stage(int rd_pad) { return s_p(rd_pad) + rd_pad * (PWK + 8) * 2; }
+  __host__ __device__ static int stage(int rd_pad) { return s_p(rd_pad) + rd_pad * p_stride(PWK) * 2; }
   __host__ __device__ static int total(int rd_pad) { return ring + BSTAGES * stage(rd_pad); }
 };
 
@@ -591,12 +599,12 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dkdv_kernel(const __grid_c
             const int nt = nt0 + 2 * np;
             if (nt + 1 < nt_end) {
               uint32_t b0, b1, b2, b3;
-              ldsm_x4_t(pb + (prow * (PWK + 8) + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
+              ldsm_x4_t(pb + (prow * p_stride(PWK) + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
               mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
               mma_bf16_16816(racc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
             } else if (nt < nt_end) {
               uint32_t b0, b1;
-              ldsm_x2_t(pb + (prow * (PWK + 8) + nt * 8) * 2, b0, b1);
+              ldsm_x2_t(pb + (prow * p_stride(PWK) + nt * 8) * 2, b0, b1);
               mma_bf16_16816(racc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
             }
           }

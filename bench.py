@@ -48,6 +48,7 @@ import statistics
 import subprocess
 import sys
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -735,6 +736,39 @@ def gpu_arm(args):
     return 0
 
 
+def splits_sweep(args):
+    """Decode time against the split count, for the heuristic's choice
+    (num_splits = 0) and fixed counts around it; one JSON line per point."""
+    import relative_position_biased_gb300 as rpb
+    rpb.build()
+    rpb.load_library()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    cases = (("decode_batched", W.decode_batched(), [0, 4, 6, 8, 12, 16, 24, 32]),
+             ("decode_batched_w4096", W.decode_batched(window=4096), [0, 4, 6, 8, 12, 16, 24]),
+             ("decode_long", W.decode_mtp_long(), [0, 38, 76, 152, 228]))
+    for name, w, counts in cases:
+        d = {k: v.cuda() for k, v in W.make_inputs(w).items()}
+        args_ = [d[k] for k in ARG_ORDER]
+        out = torch.empty_like(d["q"])
+        lse = torch.empty(w.Hq, sum(w.q_lens), dtype=torch.float32, device="cuda")
+        nbytes = A.kv_bytes(w)
+        for ns in counts:
+            prm = rpb.make_params(*args_, out=out, lse=lse, num_splits=ns, **_kw(w))
+            ws = rpb.decode_workspace(prm, "cuda")
+            _, splits = rpb.relattn_decode_num_splits(prm)
+
+            def run(ns=ns, ws=ws):
+                rpb.decode(*args_, out=out, lse=lse, workspace=ws, num_splits=ns, **_kw(w))
+            ph = types.SimpleNamespace(name=f"{name}_s{ns}", run=run)   # a phase with this split count
+            for _ in range(max(3, args.warmup)):
+                ph.run()
+            t = sorted(timed_steps([ph], args.steps, flush)[ph.name])
+            ms = t[len(t) // 2]
+            print(json.dumps({"workload": w.name, "num_splits": ns, "splits": splits,
+                              "ms_median": ms, "GBs": nbytes / (ms * 1e-3) / 1e9}), flush=True)
+    return 0
+
+
 def single_phase(args, p):
     """One phase alone (used for profiling captures): warm-up, K timed calls."""
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -760,9 +794,13 @@ def main():
     ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched", "prologue",
                                        "backward"],
                     help="time one phase alone (profiling captures)")
+    ap.add_argument("--splits-sweep", action="store_true",
+                    help="time the decodes at fixed split counts beside the heuristic's choice")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.splits_sweep:
+        return splits_sweep(args)
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)

@@ -319,6 +319,18 @@ relattn_status relattn_test_skip_k_tile(int32_t tile);
  * Process-wide; not thread-safe against concurrent launches. */
 relattn_status relattn_test_band_ctas(int32_t n);
 
+/* Test hook for the failure path of relattn_prologue; not for production use,
+ * and with no counterpart on the pages.  With tile >= 0 the staged prologue
+ * kernel's producer never issues the copies of token tile `tile` (tiles of
+ * consecutive chunk tokens, numbered from 0), so the waits of the CTA's
+ * consumer warps on that stage run out after their bounded limit (about a
+ * second): the CTA drains the copies it did issue and exits, and
+ * relattn_get_device_error() then returns RELATTN_ERR_TIMEOUT (outputs of
+ * that CTA's later tiles are undefined).  tile = -1 restores normal
+ * operation; tile < -1 -> RELATTN_ERR_INVALID_ARG.  Process-wide; not
+ * thread-safe against concurrent launches. */
+relattn_status relattn_test_prologue_skip_tile(int32_t tile);
+
 /* Human-readable name of a status code (static string). */
 const char *relattn_status_string(relattn_status status);
 

@@ -33,7 +33,7 @@ EXPORTED = (
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
     "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
     "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
-    "relattn_decode_paged",
+    "relattn_decode_paged", "relattn_test_prologue_skip_tile",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -133,6 +133,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_last_device_error_word.restype = ctypes.c_int32
         lib.relattn_test_skip_k_tile.argtypes = [ctypes.c_int32]
         lib.relattn_test_skip_k_tile.restype = ctypes.c_int
+        lib.relattn_test_prologue_skip_tile.argtypes = [ctypes.c_int32]
+        lib.relattn_test_prologue_skip_tile.restype = ctypes.c_int
         lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
         lib.relattn_test_band_ctas.restype = ctypes.c_int
         lib.relattn_decode_paged.argtypes = [P, ctypes.POINTER(RelattnPagedKV), vp]
@@ -199,6 +201,10 @@ def relattn_last_device_error_word() -> int:
 def relattn_test_skip_k_tile(tile: int) -> int:
     """Test hook: later tensor-core launches never load key tile ``tile`` (-1: off)."""
     return int(load_library().relattn_test_skip_k_tile(int(tile)))
+
+
+def relattn_test_prologue_skip_tile(tile: int) -> int:
+    return load_library().relattn_test_prologue_skip_tile(int(tile))
 
 
 def relattn_test_band_ctas(n: int) -> int:

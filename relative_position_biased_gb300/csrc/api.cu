@@ -16,6 +16,8 @@ __device__ int g_device_error;
 int g_test_skip_k_tile = -1;
 // test hook (relattn_test_band_ctas): CTA cap of the persistent band launch
 int g_test_band_ctas = 0;
+// test hook (relattn_test_prologue_skip_tile): token tile whose copies are never issued
+int g_test_prologue_skip = -1;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -447,7 +449,8 @@ relattn_status relattn_prologue(const relattn_prologue_params *p, void *stream) 
   int *err = nullptr;
   int sms = 0;
   if ((st = device_state(nullptr, &err, &sms)) != RELATTN_OK) return st;
-  return cuda_status(launch_prologue(p, err, sms, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_prologue(p, err, sms, g_test_prologue_skip,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 relattn_status relattn_get_device_error(void *stream) {
@@ -486,6 +489,12 @@ int32_t relattn_last_device_error_word(void) { return g_last_error_word; }
 relattn_status relattn_test_skip_k_tile(int32_t tile) {
   if (tile < -1) return RELATTN_ERR_INVALID_ARG;
   g_test_skip_k_tile = tile;
+  return RELATTN_OK;
+}
+
+relattn_status relattn_test_prologue_skip_tile(int32_t tile) {
+  if (tile < -1) return RELATTN_ERR_INVALID_ARG;
+  g_test_prologue_skip = tile;
   return RELATTN_OK;
 }
 

@@ -56,8 +56,9 @@ size_t bwd_dkdv_smem_bytes(int rd_pad);
 cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream);
 
 // attention prologue (prologue.cu): ShortConv + Q/K RMSNorm + KV-cache rows;
-// err = the device error word, sms = the SM count (sizes the grid).
-cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms,
+// err = the device error word, sms = the SM count (sizes the grid),
+// skip_tile = test hook (a token tile whose copies are never issued; -1 = off).
+cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms, int skip_tile,
                             cudaStream_t stream);
 
 }  // namespace relattn

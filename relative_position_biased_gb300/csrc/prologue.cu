@@ -42,6 +42,7 @@ struct PrologueArgs {
   const __nv_bfloat16 *state_in_k, *state_in_v;
   __nv_bfloat16 *state_out_k, *state_out_v;
   int *err;
+  int skip_tile;   // test hook: a token tile whose copies are never issued (-1: none)
 };
 
 __device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&x)[4]) {
@@ -387,7 +388,7 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
         info_all[st * kMaxTileTokens + lane] = make_int4(pos, ck + (Lk - Lq) - cq, ok ? 1 : 0, b);
       }
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0 && tile != a.skip_tile) {
         const int t1 = t0 + nt, h0 = max(0, t0 - kHalo);
         const uint32_t qb = (uint32_t)nt * Hq * kRow;
         const uint32_t kvb = (uint32_t)(t1 - h0) * Hkv * kRow;
@@ -520,8 +521,10 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
 
 }  // namespace
 
-cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms, cudaStream_t stream) {
+cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms, int skip_tile,
+                            cudaStream_t stream) {
   PrologueArgs a;
+  a.skip_tile = skip_tile;
   a.q = static_cast<const __nv_bfloat16 *>(p->q);
   a.k = static_cast<const __nv_bfloat16 *>(p->k);
   a.v = static_cast<const __nv_bfloat16 *>(p->v);

@@ -44,3 +44,34 @@ def test_bounded_wait_gives_up_and_context_recovers(oracle_mod):
 def test_skip_hook_rejects_bad_tile():
     assert rpb.relattn_test_skip_k_tile(-2) != rpb.RELATTN_OK
     assert rpb.relattn_test_skip_k_tile(-1) == rpb.RELATTN_OK
+
+
+def test_prologue_wait_gives_up_and_context_recovers():
+    """The staged prologue kernel: its producer leaves token tile 3 without
+    copies, so the consumer warps' bounded waits on that stage run out; the
+    CTA drains and exits, RELATTN_ERR_TIMEOUT is read back, and the next
+    call on the same context is correct."""
+    from tests.test_prologue_gpu import check, _w
+    w = _w([100, 100])                   # 25 tiles of 8 tokens (Hq 16, Hkv 2)
+    inp = W.make_prologue_inputs(w)
+    d = {k: v.cuda() for k, v in inp.items()}
+    kc = torch.zeros(200, 2, 128, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    assert rpb.relattn_get_device_error() == rpb.RELATTN_OK   # start clean
+    assert rpb.relattn_test_prologue_skip_tile(3) == rpb.RELATTN_OK
+    try:
+        rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"], d["norm_k"],
+                     d["cu_seqlens_q"], d["cu_seqlens_k"], kc, vc)
+        torch.cuda.synchronize()          # the CTAs finish (no hang)
+        st = rpb.relattn_get_device_error()
+        word = rpb.relattn_last_device_error_word()
+    finally:
+        rpb.relattn_test_prologue_skip_tile(-1)
+    assert st == rpb.RELATTN_ERR_TIMEOUT, (rpb.STATUS_NAMES.get(st, st), hex(word))
+    assert word & 2 and (word >> 8) > 0
+    check(w)                              # hook off: correct on the same context
+
+
+def test_prologue_skip_hook_rejects_bad_tile():
+    assert rpb.relattn_test_prologue_skip_tile(-2) != rpb.RELATTN_OK
+    assert rpb.relattn_test_prologue_skip_tile(-1) == rpb.RELATTN_OK

@@ -142,6 +142,12 @@ def barrier(dist):
         dist.barrier()
 
 
+def job_rate(units_per_rank: float, ms_max: float, ws: int, scale: float) -> float:
+    """Whole-job throughput: every rank processed `units_per_rank` units and
+    the slowest took `ms_max` ms (replicas, weak scaling); in units of `scale`."""
+    return ws * units_per_rank / (ms_max * 1e-3) / scale
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -638,7 +644,7 @@ def gpu_arm(args):
     pg_ms = {p.name: max_over_ranks(sum(pg_t[p.name]) / len(pg_t[p.name]), dist) for p in paged}
     bwd_ms = max_over_ranks(sum(bwd_t) / len(bwd_t), dist)
     bwd_tf = bwd.flops / (bwd_ms * 1e-3) / 1e12
-    value = ws * pre.flops / (pre_ms * 1e-3) / 1e12
+    value = job_rate(pre.flops, pre_ms, ws, 1e12)
     peaks, peak_kind = load_peaks()
     tf_peak = peaks["bf16_tflops"]
     hbm_peak = peaks["hbm_gbs"]
@@ -688,12 +694,13 @@ def gpu_arm(args):
                      "kernel": "relattn_fwd_tc_kernel<prefill, band> + relattn_fwd_tc_main_kernel "
                                "(the two launches of one prefill call)"},
         "decode": {
-            "value": dl_gbs, "unit": "GB/s", "workload": dl.w.name,
+            "value": job_rate(dl.bytes, dl_ms, ws, 1e9), "unit": "GB/s", "workload": dl.w.name,
             "roofline": {"bound": "hbm", "achieved": dl_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": dl_gbs / hbm_peak, "frac_vs_8tbs": dl_gbs / 8000.0,
                          "traffic": load_traffic("decode"),
                          "peak_source": f"{peak_kind} HBM copy"},
-            "batched": {"value": db_gbs, "unit": "GB/s", "workload": db.w.name,
+            "batched": {"value": job_rate(db.bytes, db_ms, ws, 1e9), "unit": "GB/s",
+                        "workload": db.w.name,
                         "frac": db_gbs / hbm_peak},
             "paged": {p.name: {"value": p.bytes / (pg_ms[p.name] * 1e-3) / 1e9, "unit": "GB/s",
                                "ms": pg_ms[p.name], "page_size": p.page_size,
@@ -701,14 +708,16 @@ def gpu_arm(args):
                       for p in paged},
         },
         "prologue": {
-            "value": ws * pro_gbs, "unit": "GB/s", "ms": pro_ms, "workload": pre.w.name,
+            "value": job_rate(pro.bytes, pro_ms, ws, 1e9), "unit": "GB/s", "ms": pro_ms,
+            "workload": pre.w.name,
             "what": "ShortConv k/v + RMSNorm q/k + KV-cache write + conv state out",
             "bytes": pro.bytes, "launches": args.steps * pro.launches,
             "roofline": {"bound": "hbm", "achieved": pro_gbs, "peak": hbm_peak, "unit": "GB/s",
                          "frac": pro_gbs / hbm_peak, "traffic": load_traffic("prologue"),
                          "peak_source": f"{peak_kind} HBM copy"}},
         "backward": {
-            "value": ws * bwd_tf, "unit": "TFLOP/s", "ms": bwd_ms, "workload": pre.w.name,
+            "value": job_rate(bwd.flops, bwd_ms, ws, 1e12), "unit": "TFLOP/s", "ms": bwd_ms,
+            "workload": pre.w.name,
             "what": "dq, dk, dv, dr of sum(dout * out), P frozen", "flops": bwd.flops,
             "launches": len(bwd_t) * bwd.launches,
             "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": tf_peak,
@@ -717,15 +726,15 @@ def gpu_arm(args):
                          "peak_source": f"{peak_kind} bf16 dense (burst)",
                          "kernel": "relattn_bwd_dot_kernel + relattn_bwd_dq_kernel + "
                                    "relattn_bwd_dkdv_kernel (mma.sync)"}},
-        "e2e": {"value": ws * pre.flops / (e2e_pre * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_rate(pre.flops, e2e_pre, ws, 1e12), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": pre.h2d + dl.h2d + db.h2d,
                 "d2h_bytes_per_step": pre.d2h + dl.d2h + db.d2h,
-                "decode_value": ws * dl.bytes / (e2e_dl * 1e-3) / 1e9, "decode_unit": "GB/s",
+                "decode_value": job_rate(dl.bytes, e2e_dl, ws, 1e9), "decode_unit": "GB/s",
                 "path": "pinned host buffers -> H2D -> relattn_* C ABI -> D2H out+lse",
                 "overlap": f"{e2e_steps_pipe} steps per phase; step k+1's H2D and step k-1's D2H "
                            "on two copy streams while step k computes (two device buffer sets)",
-                "serial_value": ws * pre.flops / (e2e_pre_serial * 1e-3) / 1e12,
-                "serial_decode_value": ws * dl.bytes / (e2e_dl_serial * 1e-3) / 1e9},
+                "serial_value": job_rate(pre.flops, e2e_pre_serial, ws, 1e12),
+                "serial_decode_value": job_rate(dl.bytes, e2e_dl_serial, ws, 1e9)},
         "gpu_launches": args.steps * sum(p.launches for p in phases),
         "clocks": clocks,
         "wall_s_timed_region": wall,

@@ -769,6 +769,7 @@ cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream) {
     relattn_bwd_dq_kernel<<<dim3(a.q_tiles, a.Hq, a.batch), NTB, smem, stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  if (bwd_tc_supported(a)) return launch_bwd_dkdv_tc(a, stream);
   {
     const int smem = (int)DkvLayout::total(a.rd_pad);
     cudaError_t e = cudaFuncSetAttribute(relattn_bwd_dkdv_kernel,

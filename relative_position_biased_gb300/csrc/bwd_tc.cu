@@ -1,0 +1,548 @@
+// bwd_tc.cu -- dk / dv of the relative-attention backward on tcgen05 / TMEM /
+// TMA (key-major), P frozen.
+//
+// What a CTA computes (page "SGLang and Miles Add Day-0 Support for Inkling",
+// section "Customized Efficient Kernels for Train-Inference Consistency",
+// paragraph "Relative attention"; the chain rule through the softmax): for
+// 128 keys j of one kv head and every (query head of the group, 64-row query
+// tile) that sees them,
+//     S^T = K Q^T,  dP^T = V dout^T                       (tcgen05, M = 128 keys, N = 64)
+//     P^T = exp(s_i (alpha S^T + bias) - lse_i),  dS^T = s_i alpha P^T (dP^T - D_i)
+//     dV += P^T dout,  dK += dS^T Q                        (tcgen05, A = P^T / dS^T in TMEM)
+// with bias(i, j) = [0 <= i-j < E] R[i][i-j], R = r . P.
+//
+// Roles (12 warps): warp 0 the TMA producer (K / V once, q / dout per step);
+// warp 1 the MMA issuer; warp 2 the per-step query constants (lse, D,
+// log-scale) and, for steps inside the bias band, the r rows and P columns
+// of the R window R[i][cb + c] = r_i . P[:, cb + c], which the elementwise
+// warps then compute together on warp-level MMAs into shared memory;
+// warps 4-11 two per key row (half the query columns each): they read S^T /
+// dP^T rows from TMEM,
+// gather the bias from the R window (lanes are consecutive keys, so every
+// gather is one conflict-free row of the window), and write P^T / dS^T back
+// into TMEM as bf16 for the dV / dK MMAs.  At the end they read dK / dV out.
+//
+// TMEM (512 columns): dK [0,128), dV [128,256), S^T buffers [256,320) and
+// [320,384), dP^T buffers [384,448) and [448,512); P^T / dS^T (bf16 pairs)
+// over the first 32 columns of their buffers.  S^T / dP^T of step n+1 are
+// computed while the elementwise warps work on step n.
+//
+// Every wait is bounded; a timeout sets the device error word, the roles stop,
+// the producer and the MMA issuer drain their own operations, TMEM is freed.
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace relattn {
+namespace {
+
+using namespace tc;
+
+constexpr int KT = 128;          // keys per CTA (MMA M)
+constexpr int QT = 64;           // query rows per step (MMA N of S^T, K of dV / dK)
+constexpr int QSTAGES = 2;
+constexpr int NTHR = 384;         // 4 role warps + 8 elementwise warps
+constexpr int NELEM = 256;        // elementwise threads (two per key row)
+constexpr int RWC = 200;         // R window columns (distances cb .. cb + 199)
+constexpr int RWS = 200;         // fp32 row stride of the R window
+constexpr int PSW = 216;         // bf16 row stride of the P slice (216 / 8 odd)
+
+// TMEM columns
+constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_ST = 256, TM_DP = 384;
+
+// shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t SM_K = 0;                          // 2 boxes [128 keys x 128 B]
+constexpr uint32_t SM_V = SM_K + 32768;
+constexpr uint32_t SM_Q = SM_V + 32768;               // QSTAGES x 2 boxes [64 rows x 128 B]
+constexpr uint32_t SM_DO = SM_Q + QSTAGES * 16384;
+constexpr uint32_t SM_RW = SM_DO + QSTAGES * 16384;   // R window [64][RWS] fp32
+constexpr uint32_t SM_RT = SM_RW + QT * RWS * 4;      // r tile [64][rd_pad + 8] bf16 (max 64 + 8)
+constexpr uint32_t SM_PS = SM_RT + QT * 72 * 2;       // P slice [rd_pad][PSW] bf16 (max 64 rows)
+constexpr uint32_t SM_AUX = SM_PS + 64 * PSW * 2;     // QSTAGES x {lse2, D, s*log2e, s*alpha} [64] fp32
+constexpr uint32_t SM_BAR = SM_AUX + QSTAGES * 4 * QT * 4;
+enum {
+  B_KV_FULL = 0,
+  B_Q_FULL = 1,                  // + stage
+  B_Q_EMPTY = B_Q_FULL + QSTAGES,
+  B_AUX_FULL = B_Q_EMPTY + QSTAGES,
+  B_AUX_EMPTY = B_AUX_FULL + QSTAGES,
+  B_S_FULL = B_AUX_EMPTY + QSTAGES,   // + buffer
+  B_P_FULL = B_S_FULL + 2,            // + buffer
+  B_RP_FULL = B_P_FULL + 2,           // r tile + P slice of a band step staged (aux -> elementwise)
+  B_RP_FREE = B_RP_FULL + 1,          // ... read (elementwise -> aux)
+  B_RW_DONE = B_RP_FREE + 1,          // R window written (elementwise, all warps)
+  B_RW_READ = B_RW_DONE + 1,          // R window gathered (elementwise, all warps)
+  B_DONE = B_RW_READ + 1,
+  B_DRAIN = B_DONE + 1,
+  B_COUNT = B_DRAIN + 1
+};
+constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
+constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
+constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
+constexpr uint32_t SMEM_BYTES_BWD = SM_TOTAL + 1024;
+static_assert(SMEM_BYTES_BWD <= 227 * 1024, "shared memory budget");
+
+__device__ __forceinline__ int floor8(int x) { return x & ~7; }
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test_wait(bar, parity))
+    if (clock64() - t0 > 200000000ll) return false;
+  return true;
+}
+
+// P columns [cb, cb + RWC) of all rd_pad channels -> [rd_pad][PSW] bf16;
+// columns outside [0, E) and channels past rd read as zero.  One warp.
+__device__ __forceinline__ void load_p_slice_aux(const BwdArgs &a, uint32_t base, int cb, int lane) {
+  constexpr int cpr = RWC / 8;
+  for (int idx = lane; idx < a.rd_pad * cpr; idx += 32) {
+    const int c = idx / cpr, x = idx - c * cpr, col = cb + x * 8;
+    const uint32_t dst = base + (c * PSW + x * 8) * 2;
+    const bool in_row = c < a.rd;
+    const bool whole = col >= 0 && col + 8 <= a.E;
+    const bool none = !in_row || col + 8 <= 0 || col >= a.E;
+    if (a.p_vec_ok && (whole || none)) {
+      const bool ok = in_row && whole;
+      cp_async16(dst, a.P + (ok ? (size_t)c * a.E + col : 0), ok);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c0 = col + 2 * e, c1 = c0 + 1;
+        const unsigned short lo = (in_row && c0 >= 0 && c0 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + c0]) : 0;
+        const unsigned short hi = (in_row && c1 >= 0 && c1 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + c1]) : 0;
+        w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      st_shared_v4(dst, w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NTHR, 1)
+relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
+                           const __grid_constant__ CUtensorMap map_k,
+                           const __grid_constant__ CUtensorMap map_v,
+                           const __grid_constant__ CUtensorMap map_q,
+                           const __grid_constant__ CUtensorMap map_do) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t sb = smem_addr(smem);
+  auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ------------------------------------------------------------ the CTA's keys and steps
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int cq = a.cu_q[b], ck = a.cu_k[b];
+  const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
+  if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) {
+    if (tid == 0) atomicOr(a.err, kDevErrSeqlens);
+    return;
+  }
+  const int j0 = blockIdx.x * KT;
+  const int nkeys = min(KT, Lk - j0);
+  if (nkeys <= 0) return;
+  const int off = Lk - Lq;
+  const int pos_hi = a.window > 0 ? min(Lk - 1, j0 + nkeys - 1 + a.window - 1) : Lk - 1;
+  const int t_lo = max(0, j0 - off), t_hi = min(Lq - 1, pos_hi - off);
+  const int qt_lo = t_lo / QT, n_qt = t_hi >= t_lo ? t_hi / QT - qt_lo + 1 : 0;
+  const int nsteps = a.group * n_qt;
+  const bool has_bias = a.rd > 0 && a.E > 0;
+  auto step_h = [&](int n) { return g * a.group + n / n_qt; };
+  auto step_t0 = [&](int n) { return (qt_lo + n % n_qt) * QT; };
+  auto is_band = [&](int t0) { return has_bias && (off + t0 - (j0 + KT - 1) < a.E); };
+
+  // ------------------------------------------------------------ set-up
+  if (tid == 0) {
+    mbar_init(bar(B_KV_FULL), 1);
+    for (int s = 0; s < QSTAGES; ++s) {
+      mbar_init(bar(B_Q_FULL + s), 1);
+      mbar_init(bar(B_Q_EMPTY + s), 1);
+      mbar_init(bar(B_AUX_FULL + s), 32);
+      mbar_init(bar(B_AUX_EMPTY + s), NELEM);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_S_FULL + i), 1);
+      mbar_init(bar(B_P_FULL + i), NELEM);
+    }
+    mbar_init(bar(B_RP_FULL), 32);
+    mbar_init(bar(B_RP_FREE), NELEM);
+    mbar_init(bar(B_RW_DONE), NELEM);
+    mbar_init(bar(B_RW_READ), NELEM);
+    mbar_init(bar(B_DONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SM_TMEM_SLOT, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+    prefetch_tmap(&map_q);
+    prefetch_tmap(&map_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0) {
+      bool run = true;
+      int issued = 0;
+      mbar_arrive_expect_tx(bar(B_KV_FULL), 65536);
+      tma_load_3d(sb + SM_K, &map_k, 0, g, ck + j0, bar(B_KV_FULL));
+      tma_load_3d(sb + SM_K + 16384, &map_k, 64, g, ck + j0, bar(B_KV_FULL));
+      tma_load_3d(sb + SM_V, &map_v, 0, g, ck + j0, bar(B_KV_FULL));
+      tma_load_3d(sb + SM_V + 16384, &map_v, 64, g, ck + j0, bar(B_KV_FULL));
+      for (int n = 0; n < nsteps && run; ++n) {
+        const int st = n % QSTAGES;
+        if (n >= QSTAGES &&
+            !(run = mbar_wait(bar(B_Q_EMPTY + st), ((n / QSTAGES) - 1) & 1, abort_flag, 1)))
+          break;
+        const int h = step_h(n), row = cq + step_t0(n);
+        const uint32_t dq = sb + SM_Q + st * 16384, dd = sb + SM_DO + st * 16384;
+        mbar_arrive_expect_tx(bar(B_Q_FULL + st), 32768);
+        tma_load_3d(dq, &map_q, 0, h, row, bar(B_Q_FULL + st));
+        tma_load_3d(dq + 8192, &map_q, 64, h, row, bar(B_Q_FULL + st));
+        tma_load_3d(dd, &map_do, 0, h, row, bar(B_Q_FULL + st));
+        tma_load_3d(dd + 8192, &map_do, 64, h, row, bar(B_Q_FULL + st));
+        issued = n + 1;
+      }
+      if (*abort_flag) {   // let the copies this thread issued land before the CTA exits
+        drain_wait(bar(B_KV_FULL), 0);
+        for (int m = max(0, issued - QSTAGES); m < issued; ++m)
+          drain_wait(bar(B_Q_FULL + m % QSTAGES), (m / QSTAGES) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(B_KV_FULL), 0, abort_flag, 2);
+      tc_fence_after();
+      const uint32_t id_s = idesc_bf16_f32(KT, QT, 0, 0);    // S^T: K (smem, K-major) x Q (smem, K-major)
+      const uint32_t id_o = idesc_bf16_f32(KT, 128, 0, 1);   // dV: P^T (tmem) x dout (smem, MN-major)
+      const uint64_t kd = smem_desc_sw128(sb + SM_K, 16, 1024);
+      const uint64_t vd = smem_desc_sw128(sb + SM_V, 16, 1024);
+      for (int n = 0; n <= nsteps && ok; ++n) {
+        if (n < nsteps) {
+          const int st = n % QSTAGES, buf = n & 1;
+          if (!(ok = mbar_wait(bar(B_Q_FULL + st), (n / QSTAGES) & 1, abort_flag, 3))) break;
+          tc_fence_after();
+          const uint64_t qd = smem_desc_sw128(sb + SM_Q + st * 16384, 16, 1024);
+          const uint64_t dd = smem_desc_sw128(sb + SM_DO + st * 16384, 16, 1024);
+          const uint32_t d_s = tmem + TM_ST + 64u * buf, d_p = tmem + TM_DP + 64u * buf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // 16 dims a step: 32 bytes into a 128-byte row; the second 64 dims are
+            // the second box (K / V: 16 KB on, q / dout: 8 KB on)
+            const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
+            const uint32_t bd = kk < 4 ? 2u * kk : 512u + 2u * (kk - 4);
+            mma_ss(d_s, kd + ad, qd + bd, id_s, kk > 0);
+            mma_ss(d_p, vd + ad, dd + bd, id_s, kk > 0);
+          }
+          mma_commit(bar(B_S_FULL + buf));
+        }
+        if (n >= 1) {
+          const int m = n - 1, st = m % QSTAGES, buf = m & 1;
+          if (!(ok = mbar_wait(bar(B_P_FULL + buf), (m >> 1) & 1, abort_flag, 4))) break;
+          tc_fence_after();
+          const uint32_t pa = tmem + TM_ST + 64u * buf, sa = tmem + TM_DP + 64u * buf;
+          // MN-major q / dout: 16 query rows a step (2 KB), the two 64-dim boxes 8 KB apart
+          const uint64_t om = smem_desc_sw128(sb + SM_DO + st * 16384, 8192, 1024);
+          const uint64_t qm = smem_desc_sw128(sb + SM_Q + st * 16384, 8192, 1024);
+#pragma unroll
+          for (int kq = 0; kq < QT / 16; ++kq) {
+            const uint32_t acc = (m > 0 || kq > 0) ? 1u : 0u;
+            mma_ts(tmem + TM_DV, pa + 8u * kq, om + 128u * kq, id_o, acc);
+            mma_ts(tmem + TM_DK, sa + 8u * kq, qm + 128u * kq, id_o, acc);
+          }
+          mma_commit(bar(B_Q_EMPTY + st));   // the stage's q / dout have been read
+        }
+      }
+      if (ok) {
+        mma_commit(bar(B_DONE));
+      } else {
+        // stop: wait for the MMAs already issued before tensor memory is freed
+        mma_commit(bar(B_DRAIN));
+        drain_wait(bar(B_DRAIN), 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ======================================================== per-step constants and R windows
+    // One warp, so that its only synchronisation is __syncwarp (a wait that
+    // gives up can never leave another warp stuck at a barrier).
+    int nb = 0;                          // band steps so far
+    bool run = true;
+    const int rs = (a.rd_pad + 8) * 2;   // bytes per r-tile row
+    for (int n = 0; n < nsteps && run; ++n) {
+      const int st = n % QSTAGES;
+      if (n >= QSTAGES && !(run = mbar_wait(bar(B_AUX_EMPTY + st), ((n / QSTAGES) - 1) & 1, abort_flag, 5)))
+        break;
+      const int h = step_h(n), t0 = step_t0(n);
+      float *ax = reinterpret_cast<float *>(smem + SM_AUX + st * 4 * QT * 4);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int at = lane + 32 * e, t = t0 + at;
+        const bool okr = t < Lq;
+        const size_t li = (size_t)h * a.total_q + cq + (okr ? t : 0);
+        const float sc = log_scale(off + t, a.inv_ln_base);
+        ax[at] = okr ? a.lse[li] * kLog2e : INFINITY;
+        ax[QT + at] = okr ? a.Dsum[li] : 0.f;
+        ax[2 * QT + at] = sc * kLog2e;
+        ax[3 * QT + at] = sc * a.alpha;
+      }
+      mbar_arrive(bar(B_AUX_FULL + st));
+      if (!is_band(t0)) continue;
+      if (nb > 0 && !(run = mbar_wait(bar(B_RP_FREE), (nb - 1) & 1, abort_flag, 6))) break;
+      // r rows t0 .. t0 + 63 and P columns cb .. cb + 199 of this band step (r
+      // rows past the chunk and P columns outside [0, E) read as zero)
+      const int cb = floor8(off + t0 - (j0 + KT - 1));
+      for (int idx = lane; idx < QT * (a.rd_pad / 8); idx += 32) {
+        const int row = idx / (a.rd_pad / 8), c = idx - row * (a.rd_pad / 8), tt = t0 + row;
+        const bool ok = tt < Lq && c * 8 < a.rd;
+        const __nv_bfloat16 *src = a.r + ((size_t)(cq + (tt < Lq ? tt : 0)) * a.Hq + h) * a.rd;
+        cp_async16(sb + SM_RT + row * rs + c * 16, src + (ok ? c * 8 : 0), ok);
+      }
+      load_p_slice_aux(a, sb + SM_PS, cb, lane);
+      cp_async_commit();
+      cp_async_wait<0>();
+      mbar_arrive(bar(B_RP_FULL));
+      ++nb;
+    }
+    cp_async_wait<0>();
+  } else if (warp >= 4) {
+    // ======================================================== elementwise
+    // Warp 4 + q + 4 hh (q = warp & 3) takes TMEM lanes 32 q .. 32 q + 31 (one
+    // key row a thread) and query columns 32 hh .. 32 hh + 31 of each step;
+    // its P^T / dS^T go to columns [16 hh, 16 hh + 16), which hold S^T / dP^T
+    // values this same warp has already read.
+    const int hh = (warp - 4) >> 2;
+    const int jl = 32 * (warp & 3) + lane;             // key row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int j = j0 + jl;
+    int nb = 0;
+    bool ok = true;
+    for (int n = 0; n < nsteps && ok; ++n) {
+      const int st = n % QSTAGES, buf = n & 1;
+      const int t0 = step_t0(n), pos0 = off + t0;
+      const bool band = is_band(t0);
+      const int cb = floor8(pos0 - (j0 + KT - 1));
+      if (band) {
+        // the R window of this step, R[i][c] = r_i . P[:, cb + c], computed by
+        // the 8 elementwise warps together: warp ew takes rows 16 (ew & 3) ..
+        // + 15 and n8 tiles [13 (ew >> 2), ...) of the 25
+        ok = mbar_wait(bar(B_RP_FULL), nb & 1, abort_flag, 11) &&
+             (nb == 0 || mbar_wait(bar(B_RW_READ), (nb - 1) & 1, abort_flag, 12));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const int ew = warp - 4, r0 = 16 * (ew & 3), nt_lo = 13 * (ew >> 2),
+                  nt_hi = (ew >> 2) ? RWC / 8 : 13;
+        const int gq = lane >> 2, qq = lane & 3, rs = (a.rd_pad + 8) * 2;
+        float *rwo = reinterpret_cast<float *>(smem + SM_RW);
+#pragma unroll 1
+        for (int nc = nt_lo; nc < nt_hi; nc += 5) {
+          float acc[5][4];
+#pragma unroll
+          for (int x = 0; x < 5; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+          for (int kk = 0; kk < a.rd_pad / 16; ++kk) {
+            uint32_t ra[4];
+            {
+              const int row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+              ldsm_x4(sb + SM_RT + row * rs + (kk * 16 + ((lane >> 4) << 3)) * 2, ra[0], ra[1], ra[2], ra[3]);
+            }
+            const int prow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+            for (int x = 0; x < 5; x += 2) {
+              const int nt = nc + x;
+              if (nt + 1 < nt_hi && x + 1 < 5) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(sb + SM_PS + (prow * PSW + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
+                mma_bf16_16816(acc[x], ra[0], ra[1], ra[2], ra[3], b0, b1);
+                mma_bf16_16816(acc[x + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
+              } else if (nt < nt_hi) {
+                uint32_t b0, b1;
+                ldsm_x2_t(sb + SM_PS + (prow * PSW + nt * 8) * 2, b0, b1);
+                mma_bf16_16816(acc[x], ra[0], ra[1], ra[2], ra[3], b0, b1);
+              }
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < 5; ++x) {
+            if (nc + x < nt_hi) {
+              const int c = (nc + x) * 8 + 2 * qq;
+              *reinterpret_cast<float2 *>(&rwo[(r0 + gq) * RWS + c]) = make_float2(acc[x][0], acc[x][1]);
+              *reinterpret_cast<float2 *>(&rwo[(r0 + gq + 8) * RWS + c]) = make_float2(acc[x][2], acc[x][3]);
+            }
+          }
+        }
+        mbar_arrive(bar(B_RP_FREE));     // this thread is done with the r tile / P slice
+        mbar_arrive(bar(B_RW_DONE));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_RW_DONE), nb & 1, abort_flag, 13));
+        if (!ok) break;
+      }
+      ok = mbar_wait(bar(B_S_FULL + buf), (n >> 1) & 1, abort_flag, 7) &&
+           mbar_wait(bar(B_AUX_FULL + st), (n / QSTAGES) & 1, abort_flag, 8);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const float *ax = reinterpret_cast<const float *>(smem + SM_AUX + st * 4 * QT * 4);
+      const float *rw = reinterpret_cast<const float *>(smem + SM_RW);
+      const bool need_mask = (j0 + KT - 1 > pos0) || (a.window > 0 && j0 < pos0 + QT - 1 - a.window + 1);
+      uint32_t sv[32], dv[32];
+      tmem_ld32(tmem + lane_off + TM_ST + 64u * buf + 32u * hh, sv);
+      tmem_ld32(tmem + lane_off + TM_DP + 64u * buf + 32u * hh, dv);
+      tmem_wait_ld();
+      uint32_t pk[16], dk2[16];
+#pragma unroll
+      for (int u = 0; u < 32; u += 4) {
+        const int i0 = 32 * hh + u;                    // 4 query rows of the step
+        const float4 l4 = *reinterpret_cast<const float4 *>(ax + i0);
+        const float4 d4 = *reinterpret_cast<const float4 *>(ax + QT + i0);
+        const float4 c4 = *reinterpret_cast<const float4 *>(ax + 2 * QT + i0);
+        const float4 a4 = *reinterpret_cast<const float4 *>(ax + 3 * QT + i0);
+        const float lse2[4] = {l4.x, l4.y, l4.z, l4.w}, Di[4] = {d4.x, d4.y, d4.z, d4.w};
+        const float c1[4] = {c4.x, c4.y, c4.z, c4.w}, c3[4] = {a4.x, a4.y, a4.z, a4.w};
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pos = pos0 + i0 + e;
+          float x = __uint_as_float(sv[u + e]) * a.alpha;
+          if (band) x += rw[(i0 + e) * RWS + (pos - j - cb)];
+          x *= c1[e];
+          if (need_mask) {
+            const bool vis = j <= pos && (a.window <= 0 || pos - j < a.window);
+            if (!vis) x = -INFINITY;
+          }
+          const float p = fast_exp2(x - lse2[e]);
+          pv[e] = p;
+          dsv[e] = p * (__uint_as_float(dv[u + e]) - Di[e]) * c3[e];
+        }
+        pk[(u >> 1)] = pack_bf16x2(pv[0], pv[1]);
+        pk[(u >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+        dk2[(u >> 1)] = pack_bf16x2(dsv[0], dsv[1]);
+        dk2[(u >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
+      }
+      tmem_st16(tmem + lane_off + TM_ST + 64u * buf + 16u * hh, pk);   // P^T
+      tmem_st16(tmem + lane_off + TM_DP + 64u * buf + 16u * hh, dk2);  // dS^T
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_FULL + buf));
+      mbar_arrive(bar(B_AUX_EMPTY + st));
+      if (band) {
+        mbar_arrive(bar(B_RW_READ));   // this thread has gathered from the window
+        ++nb;
+      }
+    }
+    // ---- dK / dV rows out (zeros when no query sees the keys); the TMEM
+    // loads are warp-collective, the stores only for rows inside the keys
+    if (ok && (nsteps == 0 || mbar_wait(bar(B_DONE), 0, abort_flag, 10))) {
+      tc_fence_after();
+      const size_t row = (size_t)(ck + j) * a.Hkv + g;
+      {
+        const int which = hh;                          // hh 0: dK, hh 1: dV
+        __nv_bfloat16 *dst = (which ? a.dv : a.dk) + row * kHeadDim;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          if (nsteps > 0) {
+            tmem_ld32(tmem + lane_off + (which ? TM_DV : TM_DK) + 32u * c, v);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (jl < nkeys) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
+              o.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
+              o.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
+              o.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
+              *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * q4) = o;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 bwd_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [rows, heads, 128] bf16 in boxes of 64 dims x 1 head x box_rows rows, 128-byte swizzle
+bool encode_rows(CUtensorMap *m, const void *base, int heads, int rows, int box_rows) {
+  auto fn = bwd_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const BwdArgs &a) {
+  auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!bwd_encoder()) return false;
+  if (!al(a.q) || !al(a.k) || !al(a.v) || !al(a.dout)) return false;
+  if (a.rd_pad > 64) return false;
+  return a.total_k >= KT && a.total_q >= QT;   // the TMA boxes stay inside the tensors
+}
+
+cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
+  CUtensorMap mk, mv, mq, md;
+  if (!encode_rows(&mk, a.k, a.Hkv, a.total_k, KT) || !encode_rows(&mv, a.v, a.Hkv, a.total_k, KT) ||
+      !encode_rows(&mq, a.q, a.Hq, a.total_q, QT) || !encode_rows(&md, a.dout, a.Hq, a.total_q, QT))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(relattn_bwd_dkdv_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_BWD);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int k_tiles = (a.max_k + KT - 1) / KT;
+  relattn_bwd_dkdv_tc_kernel<<<dim3(k_tiles, a.Hkv, a.batch), NTHR, SMEM_BYTES_BWD, stream>>>(a, mk, mv, mq, md);
+  return cudaGetLastError();
+}
+
+}  // namespace relattn

@@ -54,6 +54,10 @@ struct BwdArgs {
 size_t bwd_dq_smem_bytes(int rd_pad);
 size_t bwd_dkdv_smem_bytes(int rd_pad);
 cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream);
+// dk / dv on tcgen05 (bwd_tc.cu): 16-byte aligned q / k / v / dout, r_dim <= 64,
+// at least 128 keys and 64 query rows in total (the TMA boxes)
+bool bwd_tc_supported(const BwdArgs &a);
+cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream);
 
 // attention prologue (prologue.cu): ShortConv + Q/K RMSNorm + KV-cache rows;
 // err = the device error word, sms = the SM count (sizes the grid),

@@ -1040,23 +1040,30 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       // waiting for P(s)); where S(s+1) does not exist or waits for P(s) (the
       // switch to full steps), by its own commit.
       // TMEM loads / stores are warp-collective: the whole warp rescales its 32
-      // rows when any of them needs it (rows that do not are scaled by 1)
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        if (s < I.s2) {
+      // rows when any of them needs it (rows that do not are scaled by 1).
+      // Half steps: each warpgroup its half of the O columns (PV(s) waits for
+      // both warpgroups' P).  Full steps: warpgroup 0 alone, all 128 columns --
+      // the first half of PV(s) is issued as soon as warpgroup 0's P is in and
+      // writes every O column, so a rescale by warpgroup 1 could overlap it
+      // (both warpgroups take the same rescale decision for a row).
+      const bool half = s < I.s2;
+      if (__any_sync(0xffffffffu, rescale_o) && (half || wg == 0)) {
+        if (half) {
           if (s + 1 >= I.nsteps) ok = warp_wait(bar(B_PV_TAIL), n_tail0 & 1, 16);   // after PV(nsteps - 2)
           else if (s + 1 == I.s2) ok = warp_wait(bar(B_PV_SW), n_sw & 1, 16);       // after PV(s2 - 2)
           else ok = warp_wait(bar(B_S_FULL + step_kind(s + 1)), step_phase(s + 1), 16);
           if (!ok) break;
-        } else if (s > I.s2 && wg == 0) {
+        } else if (s > I.s2) {
           // both halves of PV(s-1) write every O column: wait for the second
           if (!(ok = warp_wait(bar(B_PV_F + 2 + (full_idx(s - 1) & 1)), (full_idx(s - 1) >> 1) & 1, 16))) break;
         }
         tc_fence_after();
         const float cf = rescale_o ? corr : 1.f;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
+          if (half && c >= 2) break;
           uint32_t r[32];
-          const uint32_t oaddr = tmem + lane_base + TM_O + 64u * wg + 32u * c;
+          const uint32_t oaddr = tmem + lane_base + TM_O + (half ? 64u * wg : 0u) + 32u * c;
           __syncwarp();
           tmem_ld32(oaddr, r);
           tmem_wait_ld(r);

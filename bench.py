@@ -318,8 +318,13 @@ class BackwardPhase:
         self.dq, self.dk, self.dv = (torch.empty_like(d["q"]), torch.empty_like(d["k"]),
                                      torch.empty_like(d["v"]))
         self.dr = torch.empty_like(d["r"])
-        self.ws = torch.empty(sum(w.q_lens) * w.Hq + 64, dtype=torch.float32, device="cuda")
-        self.launches = 3    # D, dq / dr, dk / dv
+        prm = rpb.RelattnBwdParams(fwd=rpb.make_params(*self.args, out=self.out, lse=self.lse,
+                                                        **_kw(w)))
+        st, nbytes = rpb.relattn_backward_workspace_size(prm)
+        if st != 0:
+            raise SystemExit("relattn_backward_workspace_size failed")
+        self.ws = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device="cuda")
+        self.launches = 4 if (w.r_dim > 0 and w.rel_extent > 0) else 3   # R, D, dq / dr, dk / dv
         self.flops = A.bwd_flops(w)
 
     def run(self):

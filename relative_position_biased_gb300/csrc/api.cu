@@ -189,8 +189,15 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
-size_t backward_workspace_bytes(const relattn_params &f) {
+// D [Hq, Tq], then (with a bias) R = r . P [Tq, Hq, E rounded up to 4] in fp32
+size_t backward_d_bytes(const relattn_params &f) {
   return ((size_t)f.num_heads_q * f.total_q * sizeof(float) + 255) / 256 * 256;
+}
+size_t backward_workspace_bytes(const relattn_params &f) {
+  size_t n = backward_d_bytes(f);
+  if (f.r_dim > 0 && f.rel_extent > 0)
+    n += (size_t)f.total_q * f.num_heads_q * ((f.rel_extent + 3) / 4 * 4) * sizeof(float);
+  return n;
 }
 
 relattn_status validate_backward(const relattn_bwd_params *p) {
@@ -419,6 +426,8 @@ relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
   a.dv = static_cast<__nv_bfloat16 *>(p->dv);
   a.dr = f.r_dim > 0 ? static_cast<__nv_bfloat16 *>(p->dr) : nullptr;
   a.Dsum = static_cast<float *>(p->workspace);
+  a.Rall = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + backward_d_bytes(f));
+  a.e_pad = (f.rel_extent + 3) / 4 * 4;
   a.err = err;
   a.batch = f.batch;
   a.total_q = f.total_q;

@@ -13,9 +13,8 @@
 //
 // Roles (12 warps): warp 0 the TMA producer (K / V once, q / dout per step);
 // warp 1 the MMA issuer; warp 2 the per-step query constants (lse, D,
-// log-scale) and, for steps inside the bias band, the r rows and P columns
-// of the R window R[i][cb + c] = r_i . P[:, cb + c], which the elementwise
-// warps then compute together on warp-level MMAs into shared memory;
+// log-scale) and, for steps inside the bias band, a TMA load of the R
+// window R[i][cb + c] = r_i . P[:, cb + c] from the R array a pre-pass wrote;
 // warps 4-11 two per key row (half the query columns each): they read S^T /
 // dP^T rows from TMEM,
 // gather the bias from the R window (lanes are consecutive keys, so every
@@ -41,12 +40,11 @@ using namespace tc;
 
 constexpr int KT = 128;          // keys per CTA (MMA M)
 constexpr int QT = 64;           // query rows per step (MMA N of S^T, K of dV / dK)
-constexpr int QSTAGES = 2;
+constexpr int QSTAGES = 3;
 constexpr int NTHR = 384;         // 4 role warps + 8 elementwise warps
 constexpr int NELEM = 256;        // elementwise threads (two per key row)
-constexpr int RWC = 200;         // R window columns (distances cb .. cb + 199)
+constexpr int RWC = 200;         // R window columns (distances cb .. cb + 199), one TMA box
 constexpr int RWS = 200;         // fp32 row stride of the R window
-constexpr int PSW = 216;         // bf16 row stride of the P slice (216 / 8 odd)
 
 // TMEM columns
 constexpr uint32_t TM_DK = 0, TM_DV = 128, TM_ST = 256, TM_DP = 384;
@@ -56,10 +54,8 @@ constexpr uint32_t SM_K = 0;                          // 2 boxes [128 keys x 128
 constexpr uint32_t SM_V = SM_K + 32768;
 constexpr uint32_t SM_Q = SM_V + 32768;               // QSTAGES x 2 boxes [64 rows x 128 B]
 constexpr uint32_t SM_DO = SM_Q + QSTAGES * 16384;
-constexpr uint32_t SM_RW = SM_DO + QSTAGES * 16384;   // R window [64][RWS] fp32
-constexpr uint32_t SM_RT = SM_RW + QT * RWS * 4;      // r tile [64][rd_pad + 8] bf16 (max 64 + 8)
-constexpr uint32_t SM_PS = SM_RT + QT * 72 * 2;       // P slice [rd_pad][PSW] bf16 (max 64 rows)
-constexpr uint32_t SM_AUX = SM_PS + 64 * PSW * 2;     // QSTAGES x {lse2, D, s*log2e, s*alpha} [64] fp32
+constexpr uint32_t SM_RW = SM_DO + QSTAGES * 16384;   // R window [64][RWS] fp32 (TMA box)
+constexpr uint32_t SM_AUX = SM_RW + QT * RWS * 4;     // QSTAGES x {lse2, D, s*log2e, s*alpha} [64] fp32
 constexpr uint32_t SM_BAR = SM_AUX + QSTAGES * 4 * QT * 4;
 enum {
   B_KV_FULL = 0,
@@ -69,10 +65,8 @@ enum {
   B_AUX_EMPTY = B_AUX_FULL + QSTAGES,
   B_S_FULL = B_AUX_EMPTY + QSTAGES,   // + buffer
   B_P_FULL = B_S_FULL + 2,            // + buffer
-  B_RP_FULL = B_P_FULL + 2,           // r tile + P slice of a band step staged (aux -> elementwise)
-  B_RP_FREE = B_RP_FULL + 1,          // ... read (elementwise -> aux)
-  B_RW_DONE = B_RP_FREE + 1,          // R window written (elementwise, all warps)
-  B_RW_READ = B_RW_DONE + 1,          // R window gathered (elementwise, all warps)
+  B_R_FULL = B_P_FULL + 2,            // R window of a band step landed (TMA)
+  B_RW_READ = B_R_FULL + 1,           // ... gathered (elementwise, all warps)
   B_DONE = B_RW_READ + 1,
   B_DRAIN = B_DONE + 1,
   B_COUNT = B_DRAIN + 1
@@ -92,39 +86,13 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-// P columns [cb, cb + RWC) of all rd_pad channels -> [rd_pad][PSW] bf16;
-// columns outside [0, E) and channels past rd read as zero.  One warp.
-__device__ __forceinline__ void load_p_slice_aux(const BwdArgs &a, uint32_t base, int cb, int lane) {
-  constexpr int cpr = RWC / 8;
-  for (int idx = lane; idx < a.rd_pad * cpr; idx += 32) {
-    const int c = idx / cpr, x = idx - c * cpr, col = cb + x * 8;
-    const uint32_t dst = base + (c * PSW + x * 8) * 2;
-    const bool in_row = c < a.rd;
-    const bool whole = col >= 0 && col + 8 <= a.E;
-    const bool none = !in_row || col + 8 <= 0 || col >= a.E;
-    if (a.p_vec_ok && (whole || none)) {
-      const bool ok = in_row && whole;
-      cp_async16(dst, a.P + (ok ? (size_t)c * a.E + col : 0), ok);
-    } else {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c0 = col + 2 * e, c1 = c0 + 1;
-        const unsigned short lo = (in_row && c0 >= 0 && c0 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + c0]) : 0;
-        const unsigned short hi = (in_row && c1 >= 0 && c1 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + c1]) : 0;
-        w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-      }
-      st_shared_v4(dst, w[0], w[1], w[2], w[3]);
-    }
-  }
-}
-
 __global__ void __launch_bounds__(NTHR, 1)
 relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
                            const __grid_constant__ CUtensorMap map_k,
                            const __grid_constant__ CUtensorMap map_v,
                            const __grid_constant__ CUtensorMap map_q,
-                           const __grid_constant__ CUtensorMap map_do) {
+                           const __grid_constant__ CUtensorMap map_do,
+                           const __grid_constant__ CUtensorMap map_r) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -167,9 +135,7 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       mbar_init(bar(B_S_FULL + i), 1);
       mbar_init(bar(B_P_FULL + i), NELEM);
     }
-    mbar_init(bar(B_RP_FULL), 32);
-    mbar_init(bar(B_RP_FREE), NELEM);
-    mbar_init(bar(B_RW_DONE), NELEM);
+    mbar_init(bar(B_R_FULL), 1);
     mbar_init(bar(B_RW_READ), NELEM);
     mbar_init(bar(B_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
@@ -185,6 +151,7 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
     prefetch_tmap(&map_v);
     prefetch_tmap(&map_q);
     prefetch_tmap(&map_do);
+    if (a.rd > 0 && a.E > 0) prefetch_tmap(&map_r);
   }
   tc_fence_before();
   __syncthreads();
@@ -281,8 +248,8 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
     // One warp, so that its only synchronisation is __syncwarp (a wait that
     // gives up can never leave another warp stuck at a barrier).
     int nb = 0;                          // band steps so far
+    int issued_r = 0;                    // (lane 0) R windows requested
     bool run = true;
-    const int rs = (a.rd_pad + 8) * 2;   // bytes per r-tile row
     for (int n = 0; n < nsteps && run; ++n) {
       const int st = n % QSTAGES;
       if (n >= QSTAGES && !(run = mbar_wait(bar(B_AUX_EMPTY + st), ((n / QSTAGES) - 1) & 1, abort_flag, 5)))
@@ -302,23 +269,19 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       }
       mbar_arrive(bar(B_AUX_FULL + st));
       if (!is_band(t0)) continue;
-      if (nb > 0 && !(run = mbar_wait(bar(B_RP_FREE), (nb - 1) & 1, abort_flag, 6))) break;
-      // r rows t0 .. t0 + 63 and P columns cb .. cb + 199 of this band step (r
-      // rows past the chunk and P columns outside [0, E) read as zero)
-      const int cb = floor8(off + t0 - (j0 + KT - 1));
-      for (int idx = lane; idx < QT * (a.rd_pad / 8); idx += 32) {
-        const int row = idx / (a.rd_pad / 8), c = idx - row * (a.rd_pad / 8), tt = t0 + row;
-        const bool ok = tt < Lq && c * 8 < a.rd;
-        const __nv_bfloat16 *src = a.r + ((size_t)(cq + (tt < Lq ? tt : 0)) * a.Hq + h) * a.rd;
-        cp_async16(sb + SM_RT + row * rs + c * 16, src + (ok ? c * 8 : 0), ok);
+      // the R window of this band step: R rows t0 .. t0 + 63 of head h,
+      // distances cb .. cb + 199 (negative distances and those past E read as
+      // zero: the box starts left of / runs past the tensor)
+      if (nb > 0 && !(run = mbar_wait(bar(B_RW_READ), (nb - 1) & 1, abort_flag, 6))) break;
+      if (lane == 0) {
+        const int cb = floor8(off + t0 - (j0 + KT - 1));
+        mbar_arrive_expect_tx(bar(B_R_FULL), QT * RWC * 4);
+        tma_load_3d(sb + SM_RW, &map_r, cb, h, cq + t0, bar(B_R_FULL));
+        issued_r = nb + 1;
       }
-      load_p_slice_aux(a, sb + SM_PS, cb, lane);
-      cp_async_commit();
-      cp_async_wait<0>();
-      mbar_arrive(bar(B_RP_FULL));
       ++nb;
     }
-    cp_async_wait<0>();
+    if (*abort_flag && lane == 0 && issued_r > 0) drain_wait(bar(B_R_FULL), (issued_r - 1) & 1);
   } else if (warp >= 4) {
     // ======================================================== elementwise
     // Warp 4 + q + 4 hh (q = warp & 3) takes TMEM lanes 32 q .. 32 q + 31 (one
@@ -336,61 +299,9 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       const int t0 = step_t0(n), pos0 = off + t0;
       const bool band = is_band(t0);
       const int cb = floor8(pos0 - (j0 + KT - 1));
-      if (band) {
-        // the R window of this step, R[i][c] = r_i . P[:, cb + c], computed by
-        // the 8 elementwise warps together: warp ew takes rows 16 (ew & 3) ..
-        // + 15 and n8 tiles [13 (ew >> 2), ...) of the 25
-        ok = mbar_wait(bar(B_RP_FULL), nb & 1, abort_flag, 11) &&
-             (nb == 0 || mbar_wait(bar(B_RW_READ), (nb - 1) & 1, abort_flag, 12));
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const int ew = warp - 4, r0 = 16 * (ew & 3), nt_lo = 13 * (ew >> 2),
-                  nt_hi = (ew >> 2) ? RWC / 8 : 13;
-        const int gq = lane >> 2, qq = lane & 3, rs = (a.rd_pad + 8) * 2;
-        float *rwo = reinterpret_cast<float *>(smem + SM_RW);
-#pragma unroll 1
-        for (int nc = nt_lo; nc < nt_hi; nc += 5) {
-          float acc[5][4];
-#pragma unroll
-          for (int x = 0; x < 5; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-          for (int kk = 0; kk < a.rd_pad / 16; ++kk) {
-            uint32_t ra[4];
-            {
-              const int row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-              ldsm_x4(sb + SM_RT + row * rs + (kk * 16 + ((lane >> 4) << 3)) * 2, ra[0], ra[1], ra[2], ra[3]);
-            }
-            const int prow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-            for (int x = 0; x < 5; x += 2) {
-              const int nt = nc + x;
-              if (nt + 1 < nt_hi && x + 1 < 5) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(sb + SM_PS + (prow * PSW + nt * 8 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
-                mma_bf16_16816(acc[x], ra[0], ra[1], ra[2], ra[3], b0, b1);
-                mma_bf16_16816(acc[x + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
-              } else if (nt < nt_hi) {
-                uint32_t b0, b1;
-                ldsm_x2_t(sb + SM_PS + (prow * PSW + nt * 8) * 2, b0, b1);
-                mma_bf16_16816(acc[x], ra[0], ra[1], ra[2], ra[3], b0, b1);
-              }
-            }
-          }
-#pragma unroll
-          for (int x = 0; x < 5; ++x) {
-            if (nc + x < nt_hi) {
-              const int c = (nc + x) * 8 + 2 * qq;
-              *reinterpret_cast<float2 *>(&rwo[(r0 + gq) * RWS + c]) = make_float2(acc[x][0], acc[x][1]);
-              *reinterpret_cast<float2 *>(&rwo[(r0 + gq + 8) * RWS + c]) = make_float2(acc[x][2], acc[x][3]);
-            }
-          }
-        }
-        mbar_arrive(bar(B_RP_FREE));     // this thread is done with the r tile / P slice
-        mbar_arrive(bar(B_RW_DONE));
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_RW_DONE), nb & 1, abort_flag, 13));
-        if (!ok) break;
-      }
       ok = mbar_wait(bar(B_S_FULL + buf), (n >> 1) & 1, abort_flag, 7) &&
-           mbar_wait(bar(B_AUX_FULL + st), (n / QSTAGES) & 1, abort_flag, 8);
+           mbar_wait(bar(B_AUX_FULL + st), (n / QSTAGES) & 1, abort_flag, 8) &&
+           (!band || mbar_wait(bar(B_R_FULL), nb & 1, abort_flag, 9));
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -527,10 +438,23 @@ bool bwd_tc_supported(const BwdArgs &a) {
 }
 
 cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
-  CUtensorMap mk, mv, mq, md;
+  CUtensorMap mk, mv, mq, md, mr;
   if (!encode_rows(&mk, a.k, a.Hkv, a.total_k, KT) || !encode_rows(&mv, a.v, a.Hkv, a.total_k, KT) ||
       !encode_rows(&mq, a.q, a.Hq, a.total_q, QT) || !encode_rows(&md, a.dout, a.Hq, a.total_q, QT))
     return cudaErrorInvalidValue;
+  mr = mk;   // (unused without a bias)
+  if (a.rd > 0 && a.E > 0) {
+    // R [Tq, Hq, e_pad] fp32 in boxes of 200 distances x 1 head x 64 rows, no swizzle
+    cuuint64_t dims[3] = {(cuuint64_t)a.E, (cuuint64_t)a.Hq, (cuuint64_t)a.total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)a.e_pad * 4, (cuuint64_t)a.Hq * a.e_pad * 4};
+    cuuint32_t box[3] = {(cuuint32_t)RWC, 1, (cuuint32_t)QT};
+    cuuint32_t es[3] = {1, 1, 1};
+    auto fn = bwd_encoder();
+    if (!fn || fn(&mr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.Rall, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   static bool attr_set[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -541,7 +465,7 @@ cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   const int k_tiles = (a.max_k + KT - 1) / KT;
-  relattn_bwd_dkdv_tc_kernel<<<dim3(k_tiles, a.Hkv, a.batch), NTHR, SMEM_BYTES_BWD, stream>>>(a, mk, mv, mq, md);
+  relattn_bwd_dkdv_tc_kernel<<<dim3(k_tiles, a.Hkv, a.batch), NTHR, SMEM_BYTES_BWD, stream>>>(a, mk, mv, mq, md, mr);
   return cudaGetLastError();
 }
 

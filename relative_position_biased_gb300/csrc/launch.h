@@ -44,6 +44,8 @@ struct BwdArgs {
   const int32_t *cu_q, *cu_k;
   __nv_bfloat16 *dq, *dk, *dv, *dr;   // dr may be null (no bias)
   float *Dsum;                 // workspace [Hq, Tq]: dout . out
+  float *Rall;                 // workspace [Tq, Hq, e_pad]: R = r . P for distances < E (bias only)
+  int e_pad;                   // row stride of Rall: E rounded up to a multiple of 4
   int *err;
   int batch, total_q, total_k, max_q, max_k, Hq, Hkv, group;
   int rd, rd_pad, E, window;

@@ -113,7 +113,7 @@ def test_decode_paged_rejects_bad_arguments(lib, kv_over, expect):
 
 def _bwd_params(fwd=None, **over):
     base = dict(dout=1 << 22, dq=2 << 22, dk=3 << 22, dv=4 << 22, dr=5 << 22,
-                workspace=6 << 22, workspace_bytes=1 << 20)
+                workspace=6 << 22, workspace_bytes=1 << 24)
     base.update(over)
     return rpb.RelattnBwdParams(fwd=fwd if fwd is not None else _params(), **base)
 
@@ -125,10 +125,16 @@ def test_backward_struct_layout_matches_header(lib):
 
 
 def test_backward_workspace_size(lib):
+    # D: 4 heads x 8 rows x 4 bytes rounded up to 256; R: 8 rows x 4 heads x 64 distances x 4 bytes
     st, n = rpb.relattn_backward_workspace_size(_bwd_params())
-    assert st == 0 and n == 256            # 4 heads x 8 rows x 4 bytes, rounded up to 256
+    assert st == 0 and n == 256 + 8 * 4 * 64 * 4
     st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(total_q=1000)))
-    assert st == 0 and n == 16128
+    assert st == 0 and n == 16128 + 1000 * 4 * 64 * 4
+    # E = 61 is padded to 64 per row; no bias: D alone
+    st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(rel_extent=61)))
+    assert st == 0 and n == 256 + 8 * 4 * 64 * 4
+    st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(r_dim=0)))
+    assert st == 0 and n == 256
 
 
 @pytest.mark.parametrize("over,fwd_over,expect", [
@@ -138,6 +144,7 @@ def test_backward_workspace_size(lib):
     (dict(dr=None), {}, 1),                 # r_dim 32 needs dr
     (dict(workspace=None), {}, 5),
     (dict(workspace_bytes=64), {}, 5),
+    (dict(workspace_bytes=1000), {}, 5),    # D fits, R does not
     (dict(), dict(r_dim=12), 2),            # r_dim not a multiple of 8
     (dict(), dict(head_dim=64), 2),
     (dict(), dict(lse=256 + 4), 1),         # lse not 16-byte aligned

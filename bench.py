@@ -74,6 +74,8 @@ KERNEL_SOURCES = {
                "relative_position_biased_gb300/csrc/common.cuh",
                "relative_position_biased_gb300/csrc/combine.cu"],
     "backward": ["relative_position_biased_gb300/csrc/bwd_mma.cu",
+                 "relative_position_biased_gb300/csrc/bwd_tc.cu",
+                 "relative_position_biased_gb300/csrc/tc_common.cuh",
                  "relative_position_biased_gb300/csrc/common.cuh"],
     "prologue": ["relative_position_biased_gb300/csrc/prologue.cu",
                  "relative_position_biased_gb300/csrc/tc_common.cuh",

@@ -189,14 +189,18 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
-// D [Hq, Tq], then (with a bias) R = r . P [Tq, Hq, E rounded up to 4] in fp32
+// D [Hq, Tq], then (with a bias) R = r . P [Tq, Hq, E rounded up to 4] and
+// the partial dq [Tq, Hq, 128], both fp32
 size_t backward_d_bytes(const relattn_params &f) {
   return ((size_t)f.num_heads_q * f.total_q * sizeof(float) + 255) / 256 * 256;
 }
+size_t backward_rall_bytes(const relattn_params &f) {
+  if (!(f.r_dim > 0 && f.rel_extent > 0)) return 0;
+  return (size_t)f.total_q * f.num_heads_q * ((f.rel_extent + 3) / 4 * 4) * sizeof(float);
+}
 size_t backward_workspace_bytes(const relattn_params &f) {
-  size_t n = backward_d_bytes(f);
-  if (f.r_dim > 0 && f.rel_extent > 0)
-    n += (size_t)f.total_q * f.num_heads_q * ((f.rel_extent + 3) / 4 * 4) * sizeof(float);
+  size_t n = backward_d_bytes(f) + backward_rall_bytes(f);
+  if (f.r_dim > 0 && f.rel_extent > 0) n += (size_t)f.total_q * f.num_heads_q * kHeadDim * sizeof(float);
   return n;
 }
 
@@ -428,6 +432,9 @@ relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
   a.Dsum = static_cast<float *>(p->workspace);
   a.Rall = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + backward_d_bytes(f));
   a.e_pad = (f.rel_extent + 3) / 4 * 4;
+  a.dq_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + backward_d_bytes(f) +
+                                        backward_rall_bytes(f));
+  a.dq_split = 0;              // (set by the launcher)
   a.err = err;
   a.batch = f.batch;
   a.total_q = f.total_q;

@@ -13,25 +13,29 @@
 //     dv_j = sum_i p(i,j) dout_i,              dr_i = s_i sum_j dl(i,j) P[:, i-j]
 // (dk, dv also summed over the query heads of a GQA group).
 //
-// Up to four launches, no atomics:
+// Up to five launches, no atomics:
 //   0. relattn_bwd_rel_kernel (with a bias, before the tcgen05 dk / dv): R = r . P
 //      for every row, head and distance below E (fp32, in the workspace), the
 //      windows that kernel loads by TMA;
 //   1. relattn_bwd_dot_kernel: D = rowsum(dout * out) (fp32, [Hq, Tq]).
-//   2. relattn_bwd_dq_kernel, query-major: a CTA takes 64 query rows of one
+//   2. dq over the keys every row of a 128-row tile sees outside the bias band
+//      (all keys without a bias), on tcgen05 (bwd_tc.cu) when the shapes allow;
+//      with a bias its fp32 result goes to the workspace.
+//   3. relattn_bwd_dq_kernel for the remaining keys (all keys without tcgen05),
+//      adding 2.'s part; it writes dq and dr: a CTA takes 64 query rows of one
 //      head and walks the key tiles they see, recomputing S (with the bias
 //      band, as the forward does) and P from the saved lse, then dP = dout V^T,
 //      dS = P (dP - D); dq += dS K in registers.  Inside the bias band dS is
 //      sheared into a per-group [row, distance] window in shared memory and
 //      dr += window . P_slice^T on the tensor cores.
-//   3. dk / dv, key-major: on tcgen05 (bwd_tc.cu) when the shapes allow, else
+//   4. dk / dv, key-major: on tcgen05 (bwd_tc.cu) when the shapes allow, else
 //      relattn_bwd_dkdv_kernel here: a CTA takes 64 keys of one kv head and
 //      walks the (query head, query tile) pairs that see them; per pair it
 //      computes the bias window R = r . P_slice once into shared memory, then
 //      per warp (16 keys) S^T, P^T, dP^T = V dout^T, dS^T, and
 //      dv += P^T dout, dk += dS^T q in registers.
-// Both recompute S and P (the forward's P is not stored).  K / V (kernel 2)
-// and q / dout / r / lse / D (kernel 3) stream through 2-stage cp.async rings.
+// All recompute S and P (the forward's P is not stored).  Here K / V (kernel 3)
+// and q / dout / r / lse / D (kernel 4) stream through 2-stage cp.async rings.
 #include "launch.h"
 
 namespace relattn {
@@ -118,9 +122,10 @@ __global__ void __launch_bounds__(256) relattn_bwd_dot_kernel(const BwdArgs a) {
 // ------------------------------------------------------------------ R = r . P for every row
 
 // Rall[(t, h)][d] = r_{t,h} . P[:, d] for d < E (fp32 accumulation of bf16
-// products, as the forward's r.P): a [Tq*Hq, r_dim] x [r_dim, E] product in
-// 128 x 128 tiles, 8 warps of 16 rows.  Both backward kernels read their bias
-// windows from it instead of recomputing them per tile.
+// products, as the forward's r.P): a [Tq*Hq, r_dim] x [r_dim, E] product. A
+// CTA keeps one 128-row r tile in shared memory and walks E in 128-distance
+// chunks, 8 warps of 16 rows.  The tcgen05 dk / dv loads its bias windows
+// from it instead of recomputing them per tile.
 constexpr int RPT = 128;
 __global__ void __launch_bounds__(256) relattn_bwd_rel_kernel(const BwdArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -129,65 +134,67 @@ __global__ void __launch_bounds__(256) relattn_bwd_rel_kernel(const BwdArgs a) {
   const int gq = lane >> 2, qq = lane & 3;
   const long rows = (long)a.total_q * a.Hq;
   const long row0 = (long)blockIdx.x * RPT;
-  const int c0 = blockIdx.y * RPT;
   const int rs = (a.rd_pad + 8) * 2;                  // bytes per r-tile row (odd 16-byte units)
   const uint32_t pbase = sbase + RPT * rs;
   const int rcs = a.rd_pad / 8;
-  for (int idx = tid; idx < RPT * rcs; idx += 256) {
+  for (int idx = tid; idx < RPT * rcs; idx += 256) {   // the r tile, once for all of E
     const int r = idx / rcs, c = idx - r * rcs;
     const bool ok = row0 + r < rows && c * 8 < a.rd;
     cp_async16(sbase + r * rs + c * 16, a.r + (ok ? (row0 + r) * a.rd + c * 8 : 0), ok);
   }
   constexpr int PS = p_stride(RPT), cpr = RPT / 8;
-  for (int idx = tid; idx < a.rd_pad * cpr; idx += 256) {
-    const int c = idx / cpr, x = idx - c * cpr, col = c0 + x * 8;
-    const uint32_t dst = pbase + (c * PS + x * 8) * 2;
-    const bool in_row = c < a.rd;
-    if (a.p_vec_ok && in_row && col + 8 <= a.E) {
-      cp_async16(dst, a.P + (size_t)c * a.E + col, true);
-    } else {
-      uint32_t w[4];
+  for (int c0 = 0; c0 < a.E; c0 += RPT) {             // 128-distance chunks of E
+    if (c0 > 0) __syncthreads();                       // the previous chunk's P slice is read
+    for (int idx = tid; idx < a.rd_pad * cpr; idx += 256) {
+      const int c = idx / cpr, x = idx - c * cpr, col = c0 + x * 8;
+      const uint32_t dst = pbase + (c * PS + x * 8) * 2;
+      const bool in_row = c < a.rd;
+      if (a.p_vec_ok && in_row && col + 8 <= a.E) {
+        cp_async16(dst, a.P + (size_t)c * a.E + col, true);
+      } else {
+        uint32_t w[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d0 = col + 2 * e, d1 = d0 + 1;
-        const unsigned short lo = (in_row && d0 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + d0]) : 0;
-        const unsigned short hi = (in_row && d1 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + d1]) : 0;
-        w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+        for (int e = 0; e < 4; ++e) {
+          const int d0 = col + 2 * e, d1 = d0 + 1;
+          const unsigned short lo = (in_row && d0 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + d0]) : 0;
+          const unsigned short hi = (in_row && d1 < a.E) ? __bfloat16_as_ushort(a.P[(size_t)c * a.E + d1]) : 0;
+          w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        st_shared_v4(dst, w[0], w[1], w[2], w[3]);
       }
-      st_shared_v4(dst, w[0], w[1], w[2], w[3]);
     }
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  float acc[16][4];
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    float acc[16][4];
 #pragma unroll
-  for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-  for (int kk = 0; kk < a.rd_pad / 16; ++kk) {
-    uint32_t ra[4];
-    ldsm_x4_n(sbase + (warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3)) * rs +
-                  (kk * 16 + ((lane >> 4) << 3)) * 2, ra);
-    const int prow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+    for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    for (int kk = 0; kk < a.rd_pad / 16; ++kk) {
+      uint32_t ra[4];
+      ldsm_x4_n(sbase + (warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3)) * rs +
+                    (kk * 16 + ((lane >> 4) << 3)) * 2, ra);
+      const int prow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(pbase + (prow * PS + np * 16 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
-      mma_bf16_16816(acc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
-      mma_bf16_16816(acc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
+      for (int np = 0; np < 8; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(pbase + (prow * PS + np * 16 + ((lane >> 4) << 3)) * 2, b0, b1, b2, b3);
+        mma_bf16_16816(acc[2 * np], ra[0], ra[1], ra[2], ra[3], b0, b1);
+        mma_bf16_16816(acc[2 * np + 1], ra[0], ra[1], ra[2], ra[3], b2, b3);
+      }
     }
-  }
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const long row = row0 + warp * 16 + gq + 8 * r;
-    if (row >= rows) continue;
-    float *dst = a.Rall + row * a.e_pad;
+    for (int r = 0; r < 2; ++r) {
+      const long row = row0 + warp * 16 + gq + 8 * r;
+      if (row >= rows) continue;
+      float *dst = a.Rall + row * a.e_pad;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int col = c0 + n * 8 + 2 * qq;
-      if (col + 1 < a.E) {
-        *reinterpret_cast<float2 *>(dst + col) = make_float2(acc[n][2 * r], acc[n][2 * r + 1]);
-      } else if (col < a.E) {
-        dst[col] = acc[n][2 * r];
+      for (int n = 0; n < 16; ++n) {
+        const int col = c0 + n * 8 + 2 * qq;
+        if (col + 1 < a.E) {
+          *reinterpret_cast<float2 *>(dst + col) = make_float2(acc[n][2 * r], acc[n][2 * r + 1]);
+        } else if (col < a.E) {
+          dst[col] = acc[n][2 * r];
+        }
       }
     }
   }
@@ -234,7 +241,14 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
   const int off = Lk - Lq, g = h / a.group;
   const int p_min = off + row0, p_max = off + row0 + nrows - 1;
   const int j_lo = a.window > 0 ? max(0, p_min - a.window + 1) : 0;
-  const int kbeg = j_lo & ~(BT - 1), kend = p_max + 1;
+  int kbeg = j_lo & ~(BT - 1);
+  if (a.dq_split) {
+    // keys every row of the enclosing 128-row tile sees outside the band are
+    // the tcgen05 dq's (relattn_bwd_dq_tc_kernel, same bound)
+    const int p0 = off + (row0 & ~127);
+    kbeg = max(kbeg, p0 - a.E + 1 > 0 ? (p0 - a.E + 1) & ~63 : 0);
+  }
+  const int kend = p_max + 1;
   const int ntiles = (kend - kbeg + BT - 1) / BT;
   auto tile_j0 = [&](int it) { return kbeg + (ntiles - 1 - it) * BT; };   // diagonal first
   const bool has_bias = a.rd > 0 && a.E > 0;
@@ -525,9 +539,17 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     const size_t row = (size_t)(cq + row0 + rl) * a.Hq + h;
     const float fq = srow[r] * a.alpha;
     __nv_bfloat16 *dst = a.dq + row * kHeadDim + 2 * qq;
+    const float *part = a.dq_split ? a.dq_part + row * kHeadDim + 2 * qq : nullptr;
 #pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(dq[n][2 * r] * fq, dq[n][2 * r + 1] * fq);
+    for (int n = 0; n < 16; ++n) {
+      float x0 = dq[n][2 * r] * fq, x1 = dq[n][2 * r + 1] * fq;
+      if (part) {
+        const float2 pp = *reinterpret_cast<const float2 *>(part + n * 8);
+        x0 += pp.x;
+        x1 += pp.y;
+      }
+      *reinterpret_cast<uint32_t *>(dst + n * 8) = pack_bf16x2(x0, x1);
+    }
     if (a.dr != nullptr) {
       __nv_bfloat16 *drd = a.dr + row * a.rd;
 #pragma unroll
@@ -840,8 +862,7 @@ cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream) {
   if (tc && a.rd > 0 && a.E > 0) {   // R = r . P for every row, read by the tcgen05 dk / dv
     const int smem = RPT * (a.rd_pad + 8) * 2 + a.rd_pad * p_stride(RPT) * 2;
     const long rows = (long)a.total_q * a.Hq;
-    const dim3 grid((unsigned)((rows + RPT - 1) / RPT), (unsigned)((a.E + RPT - 1) / RPT));
-    relattn_bwd_rel_kernel<<<grid, 256, smem, stream>>>(a);
+    relattn_bwd_rel_kernel<<<(unsigned)((rows + RPT - 1) / RPT), 256, smem, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -854,12 +875,27 @@ cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  // dq: on tcgen05 over the keys outside the bias band (all keys without a
+  // bias); the band's keys, and every key when tcgen05 is unavailable, on
+  // the warp-MMA kernel, which adds the tcgen05 part
+  const bool bias = a.rd > 0 && a.E > 0;
+  const bool tcq = tc && bwd_dq_tc_supported(a);
+  BwdArgs aq = a;
+  aq.dq_split = tcq && bias ? 1 : 0;
+  if (tcq) {
+    cudaError_t e = launch_bwd_dq_tc(aq, stream);
+    if (e != cudaSuccess) return e;
+    if (!bias && a.dr != nullptr &&   // r without an extent: dr is zero, and no kernel below writes it
+        (e = cudaMemsetAsync(a.dr, 0, (size_t)a.total_q * a.Hq * a.rd * sizeof(__nv_bfloat16), stream)) !=
+            cudaSuccess)
+      return e;
+  }
+  if (!tcq || bias) {
     const int smem = (int)DqLayout::total(a.rd_pad);
     cudaError_t e = cudaFuncSetAttribute(relattn_bwd_dq_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    relattn_bwd_dq_kernel<<<dim3(a.q_tiles, a.Hq, a.batch), NTB, smem, stream>>>(a);
+    relattn_bwd_dq_kernel<<<dim3(a.q_tiles, a.Hq, a.batch), NTB, smem, stream>>>(aq);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (tc) return launch_bwd_dkdv_tc(a, stream);

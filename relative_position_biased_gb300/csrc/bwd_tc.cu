@@ -23,8 +23,10 @@
 //
 // TMEM (512 columns): dK [0,128), dV [128,256), S^T buffers [256,320) and
 // [320,384), dP^T buffers [384,448) and [448,512); P^T / dS^T (bf16 pairs)
-// over the first 32 columns of their buffers.  S^T / dP^T of step n+1 are
-// computed while the elementwise warps work on step n.
+// over columns [0,16) and [32,48) of their buffers: each elementwise warp
+// packs its 32 query columns over the first half of the 32 it has read.
+// S^T / dP^T of step n+1 are computed while the elementwise warps work on
+// step n.
 //
 // Every wait is bounded; a timeout sets the device error word, the roles stop,
 // the producer and the MMA issuer drain their own operations, TMEM is freed.
@@ -228,8 +230,9 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
 #pragma unroll
           for (int kq = 0; kq < QT / 16; ++kq) {
             const uint32_t acc = (m > 0 || kq > 0) ? 1u : 0u;
-            mma_ts(tmem + TM_DV, pa + 8u * kq, om + 128u * kq, id_o, acc);
-            mma_ts(tmem + TM_DK, sa + 8u * kq, qm + 128u * kq, id_o, acc);
+            const uint32_t ac = 8u * kq + (kq >= 2 ? 16u : 0u);   // P^T / dS^T columns: [0,16) [32,48)
+            mma_ts(tmem + TM_DV, pa + ac, om + 128u * kq, id_o, acc);
+            mma_ts(tmem + TM_DK, sa + ac, qm + 128u * kq, id_o, acc);
           }
           mma_commit(bar(B_Q_EMPTY + st));   // the stage's q / dout have been read
         }
@@ -286,8 +289,9 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
     // ======================================================== elementwise
     // Warp 4 + q + 4 hh (q = warp & 3) takes TMEM lanes 32 q .. 32 q + 31 (one
     // key row a thread) and query columns 32 hh .. 32 hh + 31 of each step;
-    // its P^T / dS^T go to columns [16 hh, 16 hh + 16), which hold S^T / dP^T
-    // values this same warp has already read.
+    // its P^T / dS^T go to columns [32 hh, 32 hh + 16), which hold S^T / dP^T
+    // values this same warp has already read (the other warp of the row
+    // reads its own 32 columns whenever it gets there).
     const int hh = (warp - 4) >> 2;
     const int jl = 32 * (warp & 3) + lane;             // key row = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -342,8 +346,8 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
         dk2[(u >> 1)] = pack_bf16x2(dsv[0], dsv[1]);
         dk2[(u >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
       }
-      tmem_st16(tmem + lane_off + TM_ST + 64u * buf + 16u * hh, pk);   // P^T
-      tmem_st16(tmem + lane_off + TM_DP + 64u * buf + 16u * hh, dk2);  // dS^T
+      tmem_st16(tmem + lane_off + TM_ST + 64u * buf + 32u * hh, pk);   // P^T
+      tmem_st16(tmem + lane_off + TM_DP + 64u * buf + 32u * hh, dk2);  // dS^T
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + buf));
@@ -395,6 +399,287 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
   }
 }
 
+
+// ====================================================================== dq (query-major)
+//
+// For 128 query rows of one head and the 64-key steps every row of the tile
+// sees outside the bias band (j <= p0 - E for the tile's first position p0,
+// so no bias and no dr; every visible key without a bias):
+//     S = Q K^T,  dP = dout V^T                          (tcgen05, M = 128 rows, N = 64 keys)
+//     P = exp(s_i alpha S - lse_i),  dS' = s_i P (dP - D_i)
+//     dQ += dS' K                                          (tcgen05, A = dS' in TMEM)
+// and dq = alpha dQ.  Roles as in the dk / dv kernel, without the aux warp:
+// each elementwise thread owns one query row, so its constants stay in
+// registers.  TMEM: dQ [0,128), S buffers [128,192) / [192,256), dP buffers
+// [256,320) / [320,384); dS' (bf16 pairs) over columns [0,16) and [32,48) of
+// its S buffer.
+constexpr int QM = 128;          // query rows per CTA (MMA M)
+constexpr int KS = 64;           // keys per step (MMA N of S / dP, K of dQ)
+constexpr int KSTAGES = 3;
+constexpr uint32_t TQ_DQ = 0, TQ_S = 128, TQ_DP = 256;
+constexpr uint32_t SQ_Q = 0;                            // 2 boxes [128 rows x 128 B]
+constexpr uint32_t SQ_DO = SQ_Q + 32768;
+constexpr uint32_t SQ_K = SQ_DO + 32768;                // KSTAGES x 2 boxes [64 keys x 128 B]
+constexpr uint32_t SQ_V = SQ_K + KSTAGES * 16384;
+constexpr uint32_t SQ_BAR = SQ_V + KSTAGES * 16384;
+enum {
+  D_QD_FULL = 0,
+  D_KV_FULL = 1,                      // + stage
+  D_KV_EMPTY = D_KV_FULL + KSTAGES,   // + stage
+  D_S_FULL = D_KV_EMPTY + KSTAGES,    // + buffer
+  D_P_FULL = D_S_FULL + 2,            // + buffer
+  D_DONE = D_P_FULL + 2,
+  D_DRAIN = D_DONE + 1,
+  D_COUNT = D_DRAIN + 1
+};
+constexpr uint32_t SQ_TMEM_SLOT = SQ_BAR + D_COUNT * 8;
+constexpr uint32_t SQ_ABORT = SQ_TMEM_SLOT + 8;
+constexpr uint32_t SQ_TOTAL = SQ_ABORT + 8;
+constexpr uint32_t SMEM_BYTES_DQ = SQ_TOTAL + 1024;
+static_assert(SMEM_BYTES_DQ <= 227 * 1024, "shared memory budget");
+
+__global__ void __launch_bounds__(NTHR, 1)
+relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
+                         const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_do,
+                         const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t sb = smem_addr(smem);
+  auto bar = [&](int i) { return sb + SQ_BAR + 8u * i; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SQ_ABORT);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ------------------------------------------------------------ the CTA's rows and key steps
+  const int h = blockIdx.y, b = blockIdx.z, g = h / a.group;
+  const int cq = a.cu_q[b], ck = a.cu_k[b];
+  const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
+  if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) {
+    if (tid == 0) atomicOr(a.err, kDevErrSeqlens);
+    return;
+  }
+  const int row0 = (int)(gridDim.x - 1 - blockIdx.x) * QM;   // longest first
+  const int nrows = min(QM, Lq - row0);
+  if (nrows <= 0) return;
+  const int off = Lk - Lq;
+  const int p0 = off + row0, p_end = p0 + nrows - 1;
+  const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
+  const int kbeg = j_lo & ~(KS - 1);
+  const bool has_bias = a.rd > 0 && a.E > 0;
+  // without a bias every visible key; with one, the keys below the band of
+  // the tile's first row (a multiple of 64: the warp-MMA dq starts there)
+  const int kend = has_bias ? (p0 - a.E + 1 > 0 ? (p0 - a.E + 1) & ~(KS - 1) : 0) : p_end + 1;
+  const int nsteps = kend > kbeg ? (kend - kbeg + KS - 1) / KS : 0;
+
+  // ------------------------------------------------------------ set-up
+  if (tid == 0) {
+    mbar_init(bar(D_QD_FULL), 1);
+    for (int s = 0; s < KSTAGES; ++s) {
+      mbar_init(bar(D_KV_FULL + s), 1);
+      mbar_init(bar(D_KV_EMPTY + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(D_S_FULL + i), 1);
+      mbar_init(bar(D_P_FULL + i), NELEM);
+    }
+    mbar_init(bar(D_DONE), 1);
+    mbar_init(bar(D_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SQ_TMEM_SLOT, 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_q);
+    prefetch_tmap(&map_do);
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SQ_TMEM_SLOT);
+
+  if (warp == 0) {
+    // ======================================================== TMA producer
+    if (lane == 0 && nsteps > 0) {
+      bool run = true;
+      int issued = 0;
+      mbar_arrive_expect_tx(bar(D_QD_FULL), 65536);
+      tma_load_3d(sb + SQ_Q, &map_q, 0, h, cq + row0, bar(D_QD_FULL));
+      tma_load_3d(sb + SQ_Q + 16384, &map_q, 64, h, cq + row0, bar(D_QD_FULL));
+      tma_load_3d(sb + SQ_DO, &map_do, 0, h, cq + row0, bar(D_QD_FULL));
+      tma_load_3d(sb + SQ_DO + 16384, &map_do, 64, h, cq + row0, bar(D_QD_FULL));
+      for (int n = 0; n < nsteps && run; ++n) {
+        const int st = n % KSTAGES;
+        if (n >= KSTAGES &&
+            !(run = mbar_wait(bar(D_KV_EMPTY + st), ((n / KSTAGES) - 1) & 1, abort_flag, 11)))
+          break;
+        const int key = ck + kbeg + n * KS;
+        const uint32_t dk_ = sb + SQ_K + st * 16384, dv_ = sb + SQ_V + st * 16384;
+        mbar_arrive_expect_tx(bar(D_KV_FULL + st), 32768);
+        tma_load_3d(dk_, &map_k, 0, g, key, bar(D_KV_FULL + st));
+        tma_load_3d(dk_ + 8192, &map_k, 64, g, key, bar(D_KV_FULL + st));
+        tma_load_3d(dv_, &map_v, 0, g, key, bar(D_KV_FULL + st));
+        tma_load_3d(dv_ + 8192, &map_v, 64, g, key, bar(D_KV_FULL + st));
+        issued = n + 1;
+      }
+      if (*abort_flag) {   // let the copies this thread issued land before the CTA exits
+        drain_wait(bar(D_QD_FULL), 0);
+        for (int m = max(0, issued - KSTAGES); m < issued; ++m)
+          drain_wait(bar(D_KV_FULL + m % KSTAGES), (m / KSTAGES) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ======================================================== MMA issuer
+    if (lane == 0 && nsteps > 0) {
+      bool ok = mbar_wait(bar(D_QD_FULL), 0, abort_flag, 12);
+      tc_fence_after();
+      const uint32_t id_s = idesc_bf16_f32(QM, KS, 0, 0);    // S: Q (smem, K-major) x K (smem, K-major)
+      const uint32_t id_o = idesc_bf16_f32(QM, 128, 0, 1);   // dQ: dS' (tmem) x K (smem, MN-major)
+      const uint64_t qd = smem_desc_sw128(sb + SQ_Q, 16, 1024);
+      const uint64_t dd = smem_desc_sw128(sb + SQ_DO, 16, 1024);
+      for (int n = 0; n <= nsteps && ok; ++n) {
+        if (n < nsteps) {
+          const int st = n % KSTAGES, buf = n & 1;
+          if (!(ok = mbar_wait(bar(D_KV_FULL + st), (n / KSTAGES) & 1, abort_flag, 13))) break;
+          tc_fence_after();
+          const uint64_t kd = smem_desc_sw128(sb + SQ_K + st * 16384, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(sb + SQ_V + st * 16384, 16, 1024);
+          const uint32_t d_s = tmem + TQ_S + 64u * buf, d_p = tmem + TQ_DP + 64u * buf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // 16 dims a step: 32 bytes into a 128-byte row; the second 64 dims are
+            // the second box (Q / dout: 16 KB on, K / V: 8 KB on)
+            const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
+            const uint32_t bd = kk < 4 ? 2u * kk : 512u + 2u * (kk - 4);
+            mma_ss(d_s, qd + ad, kd + bd, id_s, kk > 0);
+            mma_ss(d_p, dd + ad, vd + bd, id_s, kk > 0);
+          }
+          mma_commit(bar(D_S_FULL + buf));
+        }
+        if (n >= 1) {
+          const int m = n - 1, st = m % KSTAGES, buf = m & 1;
+          if (!(ok = mbar_wait(bar(D_P_FULL + buf), (m >> 1) & 1, abort_flag, 14))) break;
+          tc_fence_after();
+          const uint32_t pa = tmem + TQ_S + 64u * buf;
+          // MN-major K: 16 keys a step (2 KB), the two 64-dim boxes 8 KB apart
+          const uint64_t km = smem_desc_sw128(sb + SQ_K + st * 16384, 8192, 1024);
+#pragma unroll
+          for (int kq = 0; kq < KS / 16; ++kq)   // dS' columns: [0,16) [32,48)
+            mma_ts(tmem + TQ_DQ, pa + 8u * kq + (kq >= 2 ? 16u : 0u), km + 128u * kq, id_o,
+                   (m > 0 || kq > 0) ? 1u : 0u);
+          mma_commit(bar(D_KV_EMPTY + st));   // the stage's K / V have been read
+        }
+      }
+      if (ok) {
+        mma_commit(bar(D_DONE));
+      } else {
+        mma_commit(bar(D_DRAIN));
+        drain_wait(bar(D_DRAIN), 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ======================================================== elementwise
+    // Warp 4 + q + 4 hh (q = warp & 3) takes TMEM lanes 32 q .. 32 q + 31 (one
+    // query row a thread) and keys 32 hh .. 32 hh + 31 of each step; its dS'
+    // goes to columns [32 hh, 32 hh + 16) of the S buffer, which hold S values
+    // this same warp has already read.
+    const int hh = (warp - 4) >> 2;
+    const int il = 32 * (warp & 3) + lane;             // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int t = row0 + il, pos = off + t;
+    const bool okr = il < nrows;
+    const size_t li = (size_t)h * a.total_q + cq + (okr ? t : 0);
+    const float srow = log_scale(pos, a.inv_ln_base);
+    const float c1 = a.alpha_log2e * srow;
+    const float lse2 = okr ? a.lse[li] * kLog2e : INFINITY;   // rows past the end: P = 0
+    const float Di = okr ? a.Dsum[li] : 0.f;
+    bool ok = true;
+    for (int n = 0; n < nsteps && ok; ++n) {
+      const int buf = n & 1, j0 = kbeg + n * KS;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(D_S_FULL + buf), (n >> 1) & 1, abort_flag, 15));
+      if (!ok) break;
+      tc_fence_after();
+      const bool need_mask = (j0 + KS - 1 > p0) || (a.window > 0 && j0 < p_end - a.window + 1);
+      uint32_t sv[32], dv[32];
+      tmem_ld32(tmem + lane_off + TQ_S + 64u * buf + 32u * hh, sv);
+      tmem_ld32(tmem + lane_off + TQ_DP + 64u * buf + 32u * hh, dv);
+      tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float d2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float x = __uint_as_float(sv[c + e]) * c1;
+          if (need_mask) {
+            const int j = j0 + 32 * hh + c + e;
+            const bool vis = j <= pos && (a.window <= 0 || pos - j < a.window);
+            if (!vis) x = -INFINITY;
+          }
+          const float p = fast_exp2(x - lse2);
+          d2[e] = p * (__uint_as_float(dv[c + e]) - Di) * srow;
+        }
+        pk[c >> 1] = pack_bf16x2(d2[0], d2[1]);
+      }
+      tmem_st16(tmem + lane_off + TQ_S + 64u * buf + 32u * hh, pk);   // dS'
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(D_P_FULL + buf));
+    }
+    // ---- dq rows out: alpha dQ, fp32 into the workspace when the band's
+    // kernel adds to it, else bf16; hh 0 takes columns 0..63, hh 1 64..127
+    if (ok && (nsteps == 0 || mbar_wait(bar(D_DONE), 0, abort_flag, 16))) {
+      tc_fence_after();
+      const size_t row = (size_t)(cq + t) * a.Hq + h;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        const int col = 64 * hh + 32 * c;
+        uint32_t v[32];
+        if (nsteps > 0) {
+          tmem_ld32(tmem + lane_off + TQ_DQ + (uint32_t)col, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (!okr) continue;
+        if (a.dq_split) {
+          float4 *dst = reinterpret_cast<float4 *>(a.dq_part + row * kHeadDim + col);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(__uint_as_float(v[4 * q4]) * a.alpha, __uint_as_float(v[4 * q4 + 1]) * a.alpha,
+                                  __uint_as_float(v[4 * q4 + 2]) * a.alpha, __uint_as_float(v[4 * q4 + 3]) * a.alpha);
+        } else {
+          __nv_bfloat16 *dst = a.dq + row * kHeadDim + col;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * a.alpha, __uint_as_float(v[8 * q4 + 1]) * a.alpha);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * a.alpha, __uint_as_float(v[8 * q4 + 3]) * a.alpha);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * a.alpha, __uint_as_float(v[8 * q4 + 5]) * a.alpha);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * a.alpha, __uint_as_float(v[8 * q4 + 7]) * a.alpha);
+            *reinterpret_cast<uint4 *>(dst + 8 * q4) = o;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
 }  // namespace
 
 namespace {
@@ -466,6 +751,29 @@ cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
   }
   const int k_tiles = (a.max_k + KT - 1) / KT;
   relattn_bwd_dkdv_tc_kernel<<<dim3(k_tiles, a.Hkv, a.batch), NTHR, SMEM_BYTES_BWD, stream>>>(a, mk, mv, mq, md, mr);
+  return cudaGetLastError();
+}
+
+bool bwd_dq_tc_supported(const BwdArgs &a) {
+  return bwd_tc_supported(a) && a.total_q >= QM && a.total_k >= KS;   // the TMA boxes stay inside
+}
+
+cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t stream) {
+  CUtensorMap mq, md, mk, mv;
+  if (!encode_rows(&mq, a.q, a.Hq, a.total_q, QM) || !encode_rows(&md, a.dout, a.Hq, a.total_q, QM) ||
+      !encode_rows(&mk, a.k, a.Hkv, a.total_k, KS) || !encode_rows(&mv, a.v, a.Hkv, a.total_k, KS))
+    return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(relattn_bwd_dq_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_DQ);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int q_tiles = (a.max_q + QM - 1) / QM;
+  relattn_bwd_dq_tc_kernel<<<dim3(q_tiles, a.Hq, a.batch), NTHR, SMEM_BYTES_DQ, stream>>>(a, mq, md, mk, mv);
   return cudaGetLastError();
 }
 

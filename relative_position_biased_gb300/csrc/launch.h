@@ -46,6 +46,9 @@ struct BwdArgs {
   float *Dsum;                 // workspace [Hq, Tq]: dout . out
   float *Rall;                 // workspace [Tq, Hq, e_pad]: R = r . P for distances < E (bias only)
   int e_pad;                   // row stride of Rall: E rounded up to a multiple of 4
+  float *dq_part;              // workspace [Tq, Hq, 128]: dq over the keys outside the bias band (fp32)
+  int dq_split;                // 1: the tcgen05 dq takes the keys outside the band and writes
+                               //    dq_part; the warp-MMA dq takes the band and adds dq_part
   int *err;
   int batch, total_q, total_k, max_q, max_k, Hq, Hkv, group;
   int rd, rd_pad, E, window;
@@ -60,6 +63,10 @@ cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream);
 // at least 128 keys and 64 query rows in total (the TMA boxes)
 bool bwd_tc_supported(const BwdArgs &a);
 cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream);
+// dq on tcgen05 (bwd_tc.cu) over the keys every row of a 128-row tile sees
+// outside the bias band (all keys without a bias); also needs 128 query rows
+bool bwd_dq_tc_supported(const BwdArgs &a);
+cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t stream);
 
 // attention prologue (prologue.cu): ShortConv + Q/K RMSNorm + KV-cache rows;
 // err = the device error word, sms = the SM count (sizes the grid),

@@ -125,14 +125,15 @@ def test_backward_struct_layout_matches_header(lib):
 
 
 def test_backward_workspace_size(lib):
-    # D: 4 heads x 8 rows x 4 bytes rounded up to 256; R: 8 rows x 4 heads x 64 distances x 4 bytes
+    # D: 4 heads x 8 rows x 4 bytes rounded up to 256; R: 8 rows x 4 heads x 64
+    # distances x 4 bytes; the partial dq: 8 rows x 4 heads x 128 x 4 bytes
     st, n = rpb.relattn_backward_workspace_size(_bwd_params())
-    assert st == 0 and n == 256 + 8 * 4 * 64 * 4
+    assert st == 0 and n == 256 + 8 * 4 * 64 * 4 + 8 * 4 * 128 * 4
     st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(total_q=1000)))
-    assert st == 0 and n == 16128 + 1000 * 4 * 64 * 4
+    assert st == 0 and n == 16128 + 1000 * 4 * 64 * 4 + 1000 * 4 * 128 * 4
     # E = 61 is padded to 64 per row; no bias: D alone
     st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(rel_extent=61)))
-    assert st == 0 and n == 256 + 8 * 4 * 64 * 4
+    assert st == 0 and n == 256 + 8 * 4 * 64 * 4 + 8 * 4 * 128 * 4
     st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(r_dim=0)))
     assert st == 0 and n == 256
 

@@ -197,3 +197,23 @@ def test_full_size_swa_prefill():
         want = do[sl].reshape(8192, 2, 8, 128).sum(axis=(0, 2))
         err = np.abs(dv[sl].sum(axis=0) - want).max()
         assert err <= 2.0 ** -7 * np.abs(dv[sl]).sum(axis=0).max(), "sum of dv"
+
+
+# dq is split: keys that every row of a 128-row query tile sees outside the
+# bias band go to the tcgen05 dq kernel, the band's keys to the warp-MMA
+# kernel, which adds the first part. These cases give the first kernel long
+# runs of keys: with and without a window and a bias, a chunk whose keys start
+# well before its queries, a short extent under long rows, many short
+# sequences, and GQA 8:1.
+@pytest.mark.parametrize("name,q_lens,k_lens,Hq,Hkv,r_dim,E,window", [
+    ("dq_nobias_long", [700], [700], 4, 2, 0, 0, 0),
+    ("dq_nobias_window", [640, 333], [640, 333], 4, 1, 0, 0, 200),
+    ("dq_chunk_prefix", [300, 129], [900, 600], 4, 2, 32, 64, 0),
+    ("dq_chunk_prefix_nobias", [300, 129], [900, 600], 4, 2, 0, 0, 0),
+    ("dq_short_extent", [777], [777], 8, 2, 16, 8, 0),
+    ("dq_window_extent", [900], [900], 4, 2, 32, 100, 333),
+    ("dq_many_short", [3, 130, 7, 129, 1, 64, 200], [3, 130, 7, 129, 1, 64, 260], 4, 2, 16, 32, 0),
+    ("dq_gqa8", [520], [520], 16, 2, 64, 200, 0),
+])
+def test_dq_split(name, q_lens, k_lens, Hq, Hkv, r_dim, E, window):
+    check(W.custom(name, q_lens, k_lens, Hq, Hkv, r_dim, E, window=window))

@@ -435,6 +435,7 @@ relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
   a.dq_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + backward_d_bytes(f) +
                                         backward_rall_bytes(f));
   a.dq_split = 0;              // (set by the launcher)
+  a.rall_ok = 0;
   a.err = err;
   a.batch = f.batch;
   a.total_q = f.total_q;

@@ -190,10 +190,12 @@ __global__ void __launch_bounds__(256) relattn_bwd_rel_kernel(const BwdArgs a) {
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
         const int col = c0 + n * 8 + 2 * qq;
+        // distances E .. e_pad - 1 (the row's padding) are written as zeros
         if (col + 1 < a.E) {
           *reinterpret_cast<float2 *>(dst + col) = make_float2(acc[n][2 * r], acc[n][2 * r + 1]);
-        } else if (col < a.E) {
-          dst[col] = acc[n][2 * r];
+        } else if (col < a.e_pad) {
+          dst[col] = col < a.E ? acc[n][2 * r] : 0.f;
+          if (col + 1 < a.e_pad) dst[col + 1] = 0.f;
         }
       }
     }
@@ -213,8 +215,12 @@ struct DqLayout {
   __host__ __device__ static int p_stage(int rd_pad) { return rd_pad * p_stride(PWQ) * 2; }
   __host__ __device__ static int r(int rd_pad) { return p + BSTAGES * p_stage(rd_pad); }
   __host__ __device__ static int r_stride(int rd_pad) { return (rd_pad + 8) * 2; }
-  __host__ __device__ static int total(int rd_pad) { return r(rd_pad) + BT * r_stride(rd_pad); }
+  // R windows loaded from the precomputed R (a ring beside K / V)
+  static constexpr int rw_stage = NGRP * win_bytes;
+  __host__ __device__ static int rw(int rd_pad) { return r(rd_pad) + BT * r_stride(rd_pad); }
+  __host__ __device__ static int total(int rd_pad) { return rw(rd_pad) + BSTAGES * rw_stage; }
 };
+static_assert(DqLayout::kv % 16 == 0 && DqLayout::win_bytes % 16 == 0, "16-byte copies");
 
 // Warp (rw, kh) takes query rows 16 rw .. 16 rw + 15 and keys 32 kh .. 32 kh + 31
 // of every key tile; the two warps of a row group share that group's R / dS
@@ -252,6 +258,7 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
   const int ntiles = (kend - kbeg + BT - 1) / BT;
   auto tile_j0 = [&](int it) { return kbeg + (ntiles - 1 - it) * BT; };   // diagonal first
   const bool has_bias = a.rd > 0 && a.E > 0;
+  const bool use_rall = has_bias && a.rall_ok;
   auto is_band = [&](int j0) { return has_bias && (p_min - (j0 + BT - 1) < a.E); };
 
   auto issue_tile = [&](int it) {
@@ -263,8 +270,24 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
       cp_async16(sbase + L::kv + st * L::kv_stage + swz(row, c), a.k + gi, ok);
       cp_async16(sbase + L::kv + (BSTAGES + st) * L::kv_stage + swz(row, c), a.v + gi, ok);
     }
-    if (is_band(j0))
+    if (is_band(j0)) {
       load_p_slice<PWQ>(a, sbase + L::p + st * L::p_stage(a.rd_pad), floor8(p_min - j0 - BT), tid);
+      if (use_rall) {
+        // each group's R window, R[row][cbw_g .. cbw_g + 88), in 16-byte pieces;
+        // cbw_g is a multiple of 8, so a piece is inside a row's [0, e_pad)
+        // (the padding past E holds zeros) or wholly outside it (zero-filled)
+        constexpr int PR = RWQ / 4;                        // pieces per row
+        for (int idx = tid; idx < NGRP * 16 * PR; idx += NTB) {
+          const int gg = idx / (16 * PR), rem = idx - gg * 16 * PR, rr = rem / PR, k = rem - rr * PR;
+          const int cbw_g = floor8(off + row0 + min(16 * gg, nrows - 1) - j0 - BT);
+          const int d = cbw_g + 4 * k;
+          const bool ok = d >= 0 && d < a.e_pad;
+          const float *src = a.Rall + ((size_t)(cq + row0 + min(16 * gg + rr, nrows - 1)) * a.Hq + h) * a.e_pad;
+          cp_async16(sbase + L::rw(a.rd_pad) + st * L::rw_stage + gg * L::win_bytes + (rr * RWQ + 4 * k) * 4,
+                     ok ? src + d : a.Rall, ok);
+        }
+      }
+    }
   };
 
   // Q, dout, r rows of the tile (rows past the end are clamped to the last one)
@@ -274,7 +297,7 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     cp_async16(sbase + L::q + swz(row, c), a.q + gi, true);
     cp_async16(sbase + L::dout + swz(row, c), a.dout + gi, true);
   }
-  if (has_bias) {
+  if (has_bias && !use_rall) {
     const int rcs = a.rd_pad / 8;
     for (int idx = tid; idx < BT * rcs; idx += NTB) {
       const int row = idx / rcs, c = idx - row * rcs;
@@ -334,7 +357,7 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     const int cb = floor8(p_min - j0 - BT), cbw = floor8(p_w0 - j0 - BT), coloff = cbw - cb;
     const uint32_t pb = sbase + L::p + st * L::p_stage(a.rd_pad);
 
-    if (band) {
+    if (band && !use_rall) {
       // the group's R window = r_rows . P[:, cbw .. cbw + 88) (fp32); warp kh
       // computes n8 tiles [6 kh, 6 kh + 6) of the 11.  (Computing it here from
       // shared-memory r and P beats gathering it from the precomputed R: that
@@ -400,10 +423,13 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
 
     // ---- logits in log2 units: s_i log2e (alpha q.k + bias)
     if (band) {
-      __syncthreads();                   // the group's window is complete
+      if (!use_rall) __syncthreads();    // the group's window is complete
+      const float *rwin = use_rall ? reinterpret_cast<const float *>(smem + L::rw(a.rd_pad) + st * L::rw_stage +
+                                                                     rw * L::win_bytes)
+                                   : win;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float *rrow = win + (gq + 8 * r) * RWQ + (pos[r] - j0 - cbw);
+        const float *rrow = rwin + (gq + 8 * r) * RWQ + (pos[r] - j0 - cbw);
 #pragma unroll
         for (int n = 0; n < 4; ++n)
 #pragma unroll
@@ -463,7 +489,7 @@ __global__ void __launch_bounds__(NTB, 1) relattn_bwd_dq_kernel(const __grid_con
     if (band) {
       // window column c holds distance cbw + c; row gq + 8r, key j0 + bcol sits
       // at column pos - j0 - bcol - cbw (always inside [0, 88) for this group)
-      __syncthreads();                   // both warps of the group read their R
+      if (!use_rall) __syncthreads();    // both warps of the group read their R
       __nv_bfloat16 *dsw = reinterpret_cast<__nv_bfloat16 *>(win);
       for (int idx = 32 * kh + lane; idx < 16 * DSW / 8; idx += 64)
         reinterpret_cast<uint4 *>(dsw)[idx] = make_uint4(0u, 0u, 0u, 0u);
@@ -882,6 +908,7 @@ cudaError_t launch_backward(const BwdArgs &a, int sms, cudaStream_t stream) {
   const bool tcq = tc && bwd_dq_tc_supported(a);
   BwdArgs aq = a;
   aq.dq_split = tcq && bias ? 1 : 0;
+  aq.rall_ok = tc && bias ? 1 : 0;       // the pre-pass above ran
   if (tcq) {
     cudaError_t e = launch_bwd_dq_tc(aq, stream);
     if (e != cudaSuccess) return e;

@@ -327,8 +327,11 @@ class BackwardPhase:
             raise SystemExit("relattn_backward_workspace_size failed")
         self.ws = torch.empty(max(1, nbytes // 4), dtype=torch.float32, device="cuda")
         # on the tcgen05 path: R, D, dq outside the band, dq / dr of the band, dk / dv
-        # (without a bias: D, dq, dk / dv)
-        self.launches = 5 if (w.r_dim > 0 and w.rel_extent > 0) else 3
+        # (without a bias: D, dq, dk / dv), and the dk / dv reduce when an even
+        # GQA group of 4 or more heads is split between two CTAs
+        group = w.Hq // w.Hkv
+        self.launches = ((5 if (w.r_dim > 0 and w.rel_extent > 0) else 3) +
+                         (1 if group >= 4 and group % 2 == 0 else 0))
         self.flops = A.bwd_flops(w)
 
     def run(self):
@@ -735,7 +738,8 @@ def gpu_arm(args):
                          "peak_source": f"{peak_kind} bf16 dense (burst)",
                          "kernel": "relattn_bwd_rel_kernel + relattn_bwd_dot_kernel + "
                                    "relattn_bwd_dq_tc_kernel + relattn_bwd_dq_kernel (band, "
-                                   "mma.sync) + relattn_bwd_dkdv_tc_kernel"}},
+                                   "mma.sync) + relattn_bwd_dkdv_tc_kernel (heads split "
+                                   "over two CTAs) + relattn_bwd_dkv_reduce_kernel"}},
         "e2e": {"value": job_rate(pre.flops, e2e_pre, ws, 1e12), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": pre.h2d + dl.h2d + db.h2d,
                 "d2h_bytes_per_step": pre.d2h + dl.d2h + db.d2h,

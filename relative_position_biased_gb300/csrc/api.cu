@@ -198,10 +198,19 @@ size_t backward_rall_bytes(const relattn_params &f) {
   if (!(f.r_dim > 0 && f.rel_extent > 0)) return 0;
   return (size_t)f.total_q * f.num_heads_q * ((f.rel_extent + 3) / 4 * 4) * sizeof(float);
 }
+size_t backward_dq_part_bytes(const relattn_params &f) {
+  if (!(f.r_dim > 0 && f.rel_extent > 0)) return 0;
+  return (size_t)f.total_q * f.num_heads_q * kHeadDim * sizeof(float);
+}
+// two fp32 halves of dk and dv when the GQA group is even and at least 4 (the
+// tcgen05 dk / dv then splits a group's query heads between two CTAs)
+size_t backward_dkv_part_bytes(const relattn_params &f) {
+  const int group = f.num_heads_kv > 0 ? f.num_heads_q / f.num_heads_kv : 0;
+  if (group < 4 || group % 2) return 0;
+  return (size_t)4 * f.total_k * f.num_heads_kv * kHeadDim * sizeof(float);
+}
 size_t backward_workspace_bytes(const relattn_params &f) {
-  size_t n = backward_d_bytes(f) + backward_rall_bytes(f);
-  if (f.r_dim > 0 && f.rel_extent > 0) n += (size_t)f.total_q * f.num_heads_q * kHeadDim * sizeof(float);
-  return n;
+  return backward_d_bytes(f) + backward_rall_bytes(f) + backward_dq_part_bytes(f) + backward_dkv_part_bytes(f);
 }
 
 relattn_status validate_backward(const relattn_bwd_params *p) {
@@ -436,6 +445,10 @@ relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
                                         backward_rall_bytes(f));
   a.dq_split = 0;              // (set by the launcher)
   a.rall_ok = 0;
+  a.dkv_part = backward_dkv_part_bytes(f) ? reinterpret_cast<float *>(
+                   static_cast<char *>(p->workspace) + backward_d_bytes(f) + backward_rall_bytes(f) +
+                   backward_dq_part_bytes(f)) : nullptr;
+  a.kv_split = 1;              // (set by the launcher)
   a.err = err;
   a.batch = f.batch;
   a.total_q = f.total_q;

@@ -32,6 +32,8 @@
 // the producer and the MMA issuer drain their own operations, TMEM is freed.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -104,7 +106,10 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ------------------------------------------------------------ the CTA's keys and steps
-  const int g = blockIdx.y, b = blockIdx.z;
+  // blockIdx.y = kv head x kv_split: with a split, CTA half `half` takes
+  // query heads [half * hpc, half * hpc + hpc) of the group
+  const int g = blockIdx.y / a.kv_split, half = blockIdx.y - g * a.kv_split, b = blockIdx.z;
+  const int hpc = a.group / a.kv_split;
   const int cq = a.cu_q[b], ck = a.cu_k[b];
   const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
   if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) {
@@ -118,9 +123,9 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
   const int pos_hi = a.window > 0 ? min(Lk - 1, j0 + nkeys - 1 + a.window - 1) : Lk - 1;
   const int t_lo = max(0, j0 - off), t_hi = min(Lq - 1, pos_hi - off);
   const int qt_lo = t_lo / QT, n_qt = t_hi >= t_lo ? t_hi / QT - qt_lo + 1 : 0;
-  const int nsteps = a.group * n_qt;
+  const int nsteps = hpc * n_qt;
   const bool has_bias = a.rd > 0 && a.E > 0;
-  auto step_h = [&](int n) { return g * a.group + n / n_qt; };
+  auto step_h = [&](int n) { return g * a.group + half * hpc + n / n_qt; };
   auto step_t0 = [&](int n) { return (qt_lo + n % n_qt) * QT; };
   auto is_band = [&](int t0) { return has_bias && (off + t0 - (j0 + KT - 1) < a.E); };
 
@@ -365,6 +370,9 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       {
         const int which = hh;                          // hh 0: dK, hh 1: dV
         __nv_bfloat16 *dst = (which ? a.dv : a.dk) + row * kHeadDim;
+        // with a split: this half's fp32 sums, added by relattn_bwd_dkv_reduce_kernel
+        float *pdst = a.kv_split > 1 ? a.dkv_part + ((size_t)(2 * half + which) * a.total_k * a.Hkv + row) * kHeadDim
+                                     : nullptr;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
@@ -375,7 +383,13 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0u;
           }
-          if (jl < nkeys) {
+          if (jl < nkeys && pdst) {
+            float4 *d4 = reinterpret_cast<float4 *>(pdst + 32 * c);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              d4[q4] = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                   __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+          } else if (jl < nkeys) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 o;
@@ -399,6 +413,20 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
   }
 }
 
+
+// dk / dv = the two halves' fp32 sums, in bf16 (a split dk / dv launch)
+__global__ void __launch_bounds__(256) relattn_bwd_dkv_reduce_kernel(const BwdArgs a) {
+  const size_t n4 = (size_t)a.total_k * a.Hkv * kHeadDim / 4;   // float4 groups per tensor
+  const float4 *p = reinterpret_cast<const float4 *>(a.dkv_part);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t which = i / n4, k = i - which * n4;            // 0: dk, 1: dv
+    const float4 x = p[which * n4 + k], y = p[(2 + which) * n4 + k];
+    uint2 o;
+    o.x = pack_bf16x2(x.x + y.x, x.y + y.y);
+    o.y = pack_bf16x2(x.z + y.z, x.w + y.w);
+    *reinterpret_cast<uint2 *>((which ? a.dv : a.dk) + 4 * k) = o;
+  }
+}
 
 // ====================================================================== dq (query-major)
 //
@@ -749,8 +777,19 @@ cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
+  // An even GQA group of at least 4 heads is split between two CTAs per key
+  // tile: twice the CTAs, half the longest one (the last wave is the ragged
+  // part of this grid), and one small reduce launch.
+  BwdArgs ak = a;
+  ak.kv_split = (a.dkv_part != nullptr && a.group >= 4 && a.group % 2 == 0) ? 2 : 1;
   const int k_tiles = (a.max_k + KT - 1) / KT;
-  relattn_bwd_dkdv_tc_kernel<<<dim3(k_tiles, a.Hkv, a.batch), NTHR, SMEM_BYTES_BWD, stream>>>(a, mk, mv, mq, md, mr);
+  relattn_bwd_dkdv_tc_kernel<<<dim3(k_tiles, a.Hkv * ak.kv_split, a.batch), NTHR, SMEM_BYTES_BWD, stream>>>(
+      ak, mk, mv, mq, md, mr);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || ak.kv_split == 1) return e;
+  const size_t n = (size_t)a.total_k * a.Hkv * kHeadDim / 2;   // float4 groups, both tensors
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8);
+  if (blocks > 0) relattn_bwd_dkv_reduce_kernel<<<blocks, 256, 0, stream>>>(ak);
   return cudaGetLastError();
 }
 

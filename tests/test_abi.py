@@ -136,6 +136,10 @@ def test_backward_workspace_size(lib):
     assert st == 0 and n == 256 + 8 * 4 * 64 * 4 + 8 * 4 * 128 * 4
     st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(r_dim=0)))
     assert st == 0 and n == 256
+    # a GQA group of 4: two fp32 halves of dk and dv, total_k x Hkv x 128 each
+    st, n = rpb.relattn_backward_workspace_size(_bwd_params(fwd=_params(num_heads_q=8, num_heads_kv=2)))
+    tk = _params().total_k
+    assert st == 0 and n == 256 + 8 * 8 * 64 * 4 + 8 * 8 * 128 * 4 + 4 * tk * 2 * 128 * 4
 
 
 @pytest.mark.parametrize("over,fwd_over,expect", [

@@ -116,7 +116,12 @@ constexpr uint32_t SM_XCH = SM_ABORT + 8;                      // row exchange [
 constexpr int kCuCache = 64;
 constexpr uint32_t SM_CU = SM_XCH + 2 * 2 * 128 * 4;            // [2][kCuCache + 1] int
 constexpr uint32_t SM_QLOADS = SM_CU + 2 * (kCuCache + 1) * 4;   // q staging loads issued
-constexpr uint32_t SM_TOTAL = SM_QLOADS + 8;
+// decode work order (batch <= kCuCache): per sequence its full / partial /
+// remaining split counts, their prefix sums, and the partial chunks by size
+constexpr uint32_t SM_ORD = SM_QLOADS + 8;
+constexpr int ORD_NF = 0, ORD_REM = kCuCache, ORD_PF = 2 * kCuCache, ORD_PZ = 3 * kCuCache + 1,
+              ORD_PTAB = 4 * kCuCache + 2, ORD_NP = 5 * kCuCache + 2, ORD_INTS = 5 * kCuCache + 4;
+constexpr uint32_t SM_TOTAL = SM_ORD + ORD_INTS * 4;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -178,7 +183,7 @@ struct Item {
   int c_start, c_first, c_last;   // r.P chunks of the band (s2 > 0)
 };
 
-template <bool DECODE>
+template <bool DECODE, bool WALK>
 __global__ void __launch_bounds__(NTHREADS, 1)
 relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
                       const __grid_constant__ CUtensorMap map_k,
@@ -204,8 +209,15 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   // running) backwards; CTA x takes items x, x + gridDim.x, ...  Every role
   // walks the same list, and the barrier phases run on across items.
   Item I{};
-  const int n_items = DECODE ? 1 : a.q_tiles * a.Hq * a.batch;
-  const int item0 = DECODE ? 0 : (int)blockIdx.x, item_step = DECODE ? 1 : (int)gridDim.x;
+  // Decode: items are (sequence, split, kv head, row block); CTAs walk them
+  // like the prefill's, in longest-first order (see load_item)
+  // (WALK = false: decode with one item per CTA, the item from blockIdx)
+  const int dec_units = DECODE ? a.Hkv * a.row_blocks : 1;
+  const int n_items = DECODE ? (WALK ? a.num_splits * dec_units * a.batch : 1) : a.q_tiles * a.Hq * a.batch;
+  const int item0 = (DECODE && !WALK) ? 0 : (int)blockIdx.x;
+  const int item_step = (DECODE && !WALK) ? 1 : (int)gridDim.x;
+  int *ord = reinterpret_cast<int *>(smem + SM_ORD);
+  const bool dec_sorted = DECODE && WALK && a.batch <= kCuCache;
   // work of the items before the current one, for barrier phases / stages
   int hb = 0, fb = 0, tb = 0, ob = 0;     // half steps, full steps, key tiles, r.P chunks
   // V-ring slots: the item's q rows take one ahead of its value tiles (TMA
@@ -243,10 +255,42 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   // -1 = inconsistent sequence lengths (reported by the caller, item skipped)
   auto load_item = [&](int idx) -> int {
     if constexpr (DECODE) {
-      I.split = blockIdx.x;
-      I.kv_head = blockIdx.y / a.row_blocks;
-      I.row0 = (blockIdx.y % a.row_blocks) * BM;
-      I.b = blockIdx.z;
+      // slot idx -> position: rounds of gridDim.x slots, every other full round
+      // reversed (a snake), over pairs (sequence, split) ordered full chunks
+      // first, then partial chunks by size, then the rest; each pair is
+      // dec_units consecutive items (kv head, row block).  Every pair is in
+      // the order, so the walk covers all items whatever the sizes.
+      int b, sp, u;
+      if constexpr (!WALK) {
+        sp = blockIdx.x;
+        u = blockIdx.y;
+        b = blockIdx.z;
+      } else if (dec_sorted) {
+        const int r = idx / item_step, c = idx - r * item_step;
+        const int pos = ((r & 1) && (r + 1) * item_step <= n_items) ? r * item_step + (item_step - 1 - c) : idx;
+        const int q = pos / dec_units;
+        u = pos - q * dec_units;
+        const int F = ord[ORD_PF + a.batch], NP = ord[ORD_NP];
+        if (q < F || q >= F + NP) {
+          const int base = q < F ? ORD_PF : ORD_PZ, qq = q < F ? q : q - F - NP;
+          b = 0;                                        // last b with prefix[b] <= qq
+          for (int i = 1; i < a.batch; ++i) b = ord[base + i] <= qq ? i : b;
+          sp = q < F ? qq - ord[ORD_PF + b]
+                     : ord[ORD_NF + b] + (ord[ORD_REM + b] > 0 ? 1 : 0) + (qq - ord[ORD_PZ + b]);
+        } else {
+          b = ord[ORD_PTAB + (q - F)];
+          sp = ord[ORD_NF + b];
+        }
+      } else {
+        sp = idx % a.num_splits;
+        const int rest = idx / a.num_splits;
+        u = rest % dec_units;
+        b = rest / dec_units;
+      }
+      I.split = sp;
+      I.kv_head = u / a.row_blocks;
+      I.row0 = (u % a.row_blocks) * BM;
+      I.b = b;
       I.h_fixed = 0;
     } else {
       const int per_x = a.Hq * a.batch;
@@ -373,12 +417,57 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   }
   tc_fence_before();
   __syncthreads();
+  if (dec_sorted) {
+    // the decode work order: sequence b's keys from the aligned start of its
+    // first row block's window, cut into splits of split_chunk keys
+    const int b = tid;
+    if (b < a.batch) {
+      const int cq = cu_s[b], ck = cu_s[kCuCache + 1 + b];
+      const int Lq = cu_s[b + 1] - cq, Lk = cu_s[kCuCache + 2 + b] - ck;
+      long vis = 0;
+      if (Lq > 0 && Lk >= Lq) {
+        const int off = Lk - Lq, rows = min(BM, Lq * a.group);
+        const int p0 = off, p_last = off + (rows - 1) / a.group;
+        const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
+        vis = (long)p_last + 1 - (j_lo & ~(BN - 1));
+      }
+      const long nf = min((long)a.num_splits, vis / a.split_chunk);
+      const long rem = nf < a.num_splits ? vis - nf * a.split_chunk : 0;
+      ord[ORD_NF + b] = (int)nf;
+      ord[ORD_REM + b] = (int)rem;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int f = 0, z = 0, np = 0;
+      for (int i = 0; i < a.batch; ++i) {
+        ord[ORD_PF + i] = f;
+        ord[ORD_PZ + i] = z;
+        const int pi = ord[ORD_REM + i] > 0 ? 1 : 0;
+        f += ord[ORD_NF + i];
+        z += a.num_splits - ord[ORD_NF + i] - pi;
+        np += pi;
+      }
+      ord[ORD_PF + a.batch] = f;
+      ord[ORD_PZ + a.batch] = z;
+      ord[ORD_NP] = np;
+    }
+    if (b < a.batch && ord[ORD_REM + b] > 0) {   // rank among the partial chunks: larger first
+      const int rb = ord[ORD_REM + b];
+      int rank = 0;
+      for (int i = 0; i < a.batch; ++i) {
+        const int ri = ord[ORD_REM + i];
+        rank += ri > rb || (ri == rb && i < b);
+      }
+      ord[ORD_PTAB + rank] = b;
+    }
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
   // TMA copies issued by the producer thread (to drain them if the CTA gives up)
   int issued_k = 0, issued_v = 0, issued_p = 0, issued_rt = 0;
   if (warp < 4) {
-  if constexpr (!DECODE) regs_dec<kRegsSupport>();
+  if constexpr (!DECODE || WALK) regs_dec<kRegsSupport>();
   if (warp == 0) {
     // ======================================================== TMA producer
     // Per tile t: the P slices its half steps need (band tiles), then K(t),
@@ -685,7 +774,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     __syncwarp();
   }
   } else {
-    if constexpr (!DECODE) regs_inc<kRegsSoftmax>();
+    if constexpr (!DECODE || WALK) regs_inc<kRegsSoftmax>();
     // ======================================================== softmax
     // Two warpgroups share the 128 rows: warpgroup wg handles the wg-th half of
     // every step's keys and O / output columns [64 wg, 64 wg + 64).  The two
@@ -1082,6 +1171,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     // ---- epilogue.  The next item's q / r rows go in first: its first MMAs
     // (r.P chunks, S) run while this item's output is written.
     const int nsteps_e = I.nsteps, tail_par = n_tail1 & 1, v_last = vslot(I.ntiles - 1) % V_STAGES;
+    const int s2_e = (DECODE && WALK) ? I.s2 : 0;
+    const int v_band_last = (DECODE && WALK) ? vslot(I.nb_tiles - 1) % V_STAGES : 0;
     const bool valid = a_row < I.nrows;
     const size_t qrow = (size_t)(I.cq + t_row) * a.Hq + h_row;
     // decode with several splits leaves fp32 partials for the combine kernel
@@ -1093,8 +1184,14 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     if (have && !q_slot) stage_item();
     if (ok && nsteps_e > 0) ok = warp_wait(bar(B_PV_TAIL + 1), tail_par, 17);
     // PV of the last step has landed: the last tile's V stage is free (the
-    // steps release every earlier one)
+    // steps release every earlier one, except, in decode, the last half-step
+    // tile when exactly one full step follows the band: its release point,
+    // the landing of S(s2 + 1), would be a step past the item's end.  A
+    // prefill CTA that walks items has band steps only.)
     if (ok && leader && nsteps_e > 0) mbar_arrive(bar(B_V_EMPTY + v_last));
+    if constexpr (DECODE && WALK) {
+      if (ok && leader && s2_e > 0 && nsteps_e == s2_e + 1) mbar_arrive(bar(B_V_EMPTY + v_band_last));
+    }
     float l_other = 0.f;
     // total row sum over both key halves
     if (ok) l_other = exchange(l, ok);
@@ -1210,7 +1307,7 @@ bool tc_supported(const KernelArgs &a, int total_k) {
 
 namespace {
 
-template <bool DECODE>
+template <bool DECODE, bool WALK>
 cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t stream) {
   TcArgs ta;
   ta.a = a;
@@ -1253,12 +1350,12 @@ cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t 
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_kernel<DECODE>,
+    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_kernel<DECODE, WALK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  relattn_fwd_tc_kernel<DECODE><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv, mp, mq, mr);
+  relattn_fwd_tc_kernel<DECODE, WALK><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv, mp, mq, mr);
   return cudaGetLastError();
 }
 
@@ -1272,11 +1369,21 @@ cudaError_t launch_prefill_tc(const KernelArgs &a, int total_k, cudaStream_t str
   if (items <= 0) return cudaSuccess;
   const long ctas = a.band_only && a.sms > 0 && items > a.sms ? (long)a.sms : items;
   if (ctas > 0x7fffffffL) return cudaErrorInvalidValue;
-  return launch_tc<false>(a, total_k, dim3((unsigned)ctas, 1, 1), stream);
+  return launch_tc<false, true>(a, total_k, dim3((unsigned)ctas, 1, 1), stream);
 }
 
 cudaError_t launch_decode_tc(const KernelArgs &a, int total_k, cudaStream_t stream) {
-  return launch_tc<true>(a, total_k, dim3(a.num_splits, a.Hkv * a.row_blocks, a.batch), stream);
+  // at most one CTA per SM, each walking items (the longest first): the next
+  // item's tiles load while the current one finishes, and the set-up is paid
+  // once per SM instead of once per (sequence, split, kv head, row block)
+  // (items that fit in one wave keep one CTA each, without the item loop's
+  // bookkeeping: about 3.5 % faster on a 1M-key decode of 152 items)
+  const long items = (long)a.num_splits * a.Hkv * a.row_blocks * a.batch;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
+  if (a.sms <= 0 || items <= a.sms)
+    return launch_tc<true, false>(a, total_k, dim3(a.num_splits, a.Hkv * a.row_blocks, a.batch), stream);
+  return launch_tc<true, true>(a, total_k, dim3((unsigned)a.sms, 1, 1), stream);
 }
 
 }  // namespace relattn

@@ -190,6 +190,45 @@ def test_decode_matches_prefill_tail():
 
 # ------------------------------------------------------------------ full-size workloads
 
+# Decode CTAs walk (sequence, split, kv head, row block) items too, the
+# longest first: full chunks, then partial chunks by size, then the rest,
+# dealt round by round with every other full round reversed. The cap makes
+# each CTA take many items, so these cases cover:
+# - empty and one-key splits;
+# - a partial last round;
+# - two row blocks;
+# - windows;
+# - more sequences than the work-order tables hold, which takes the plain order.
+
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+@pytest.mark.parametrize("splits", [0, 5])
+def test_decode_ctas_walk_many_items(band_ctas, ctas, splits):
+    band_ctas(ctas)
+    ks = [1, 4000, 130, 900, 2, 2600, 129, 1500]
+    _check(W.custom(f"dec_persist{ctas}", [1] * len(ks), ks, 16, 2, 32, 256), decode=True,
+           num_splits=splits)
+
+
+def test_decode_ctas_mtp_rows_window(band_ctas):
+    band_ctas(4)
+    ks = [3000, 40, 1200, 2048]
+    _check(W.custom("dec_persist_w", [9] * len(ks), ks, 8, 2, 32, 128, window=700), decode=True,
+           num_splits=3)
+
+
+def test_decode_ctas_row_blocks(band_ctas):
+    band_ctas(2)
+    _check(W.custom("dec_persist_g16", [16, 16], [900, 300], 16, 1, 32, 64), decode=True, num_splits=2)
+
+
+@pytest.mark.parametrize("ctas", [0, 5])
+def test_decode_many_sequences(band_ctas, ctas):
+    """70 sequences: more than the work-order tables hold (plain order)."""
+    band_ctas(ctas)
+    ks = (np.random.default_rng(11).integers(1, 700, size=70) + 1).tolist()
+    _check(W.custom(f"dec_many{ctas}", [1] * 70, ks, 4, 1, 16, 64), decode=True, num_splits=2)
+
+
 def test_workload_tiny():
     _check(W.tiny_full())
 

@@ -204,7 +204,8 @@ def test_full_size_swa_prefill():
 # kernel, which adds the first part. These cases give the first kernel long
 # runs of keys: with and without a window and a bias, a chunk whose keys start
 # well before its queries, a short extent under long rows, many short
-# sequences, and GQA 8:1.
+# sequences, GQA 8:1 and 6:1 (three heads per dk / dv CTA), an extent beyond
+# the sequence and a window below the extent (no keys outside the band).
 @pytest.mark.parametrize("name,q_lens,k_lens,Hq,Hkv,r_dim,E,window", [
     ("dq_nobias_long", [700], [700], 4, 2, 0, 0, 0),
     ("dq_nobias_window", [640, 333], [640, 333], 4, 1, 0, 0, 200),
@@ -214,6 +215,9 @@ def test_full_size_swa_prefill():
     ("dq_window_extent", [900], [900], 4, 2, 32, 100, 333),
     ("dq_many_short", [3, 130, 7, 129, 1, 64, 200], [3, 130, 7, 129, 1, 64, 260], 4, 2, 16, 32, 0),
     ("dq_gqa8", [520], [520], 16, 2, 64, 200, 0),
+    ("dq_extent_beyond_len", [300], [300], 4, 2, 32, 1024, 0),
+    ("dq_window_below_extent", [700], [700], 8, 2, 32, 256, 100),
+    ("dq_gqa6", [400], [400], 12, 2, 16, 64, 0),
 ])
 def test_dq_split(name, q_lens, k_lens, Hq, Hkv, r_dim, E, window):
     check(W.custom(name, q_lens, k_lens, Hq, Hkv, r_dim, E, window=window))

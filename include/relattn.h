@@ -217,7 +217,10 @@ int32_t relattn_last_device_error_word(void);
  * 16-byte aligned, at least relattn_backward_workspace_size() bytes) holds
  * D (4 * Hq * total_q bytes) and, with a bias, R = r . P for every row, head
  * and distance below E in fp32 (4 * total_q * Hq * E, E rounded up to 4) and
- * the part of dq from keys outside the bias band in fp32 (4 * total_q * Hq * 128).
+ * the part of dq from keys outside the bias band in fp32 (4 * total_q * Hq * 128);
+ * and, when Hq / Hkv is even and at least 4, two fp32 halves of dk and of dv
+ * (16 * total_k * Hkv * 128 bytes).  The contents are scratch: nothing is
+ * read from it before this call writes it.
  * Requirements: every pointer 16-byte aligned, r_dim a multiple of 8 (0..64).
  * Errors: RELATTN_ERR_INVALID_ARG (NULL or unaligned pointers, bad sizes),
  * RELATTN_ERR_UNSUPPORTED (head_dim != 128, r_dim not a multiple of 8 or

@@ -337,6 +337,18 @@ relattn_status relattn_test_band_ctas(int32_t n);
  * thread-safe against concurrent launches. */
 relattn_status relattn_test_prologue_skip_tile(int32_t tile);
 
+/* Test hook for the failure path of relattn_backward; not for production use,
+ * and with no counterpart on the pages.  With step >= 0 the tcgen05 backward
+ * kernels' producers never issue the copies of their step `step` (a K / V
+ * step of the dq kernel, a q / dout step of the dk / dv kernel), so the waits
+ * behind it run out after their bounded limit (about a second per wave of
+ * CTAs): each such CTA drains what it issued, frees its tensor memory and
+ * exits, and relattn_get_device_error() then returns RELATTN_ERR_TIMEOUT
+ * (the gradients are undefined).  step = -1 restores normal operation;
+ * step < -1 -> RELATTN_ERR_INVALID_ARG.  Process-wide; not thread-safe
+ * against concurrent launches. */
+relattn_status relattn_test_backward_skip_step(int32_t step);
+
 /* Human-readable name of a status code (static string). */
 const char *relattn_status_string(relattn_status status);
 

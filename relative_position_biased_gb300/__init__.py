@@ -33,7 +33,7 @@ EXPORTED = (
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
     "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
     "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
-    "relattn_decode_paged", "relattn_test_prologue_skip_tile",
+    "relattn_decode_paged", "relattn_test_prologue_skip_tile", "relattn_test_backward_skip_step",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -135,6 +135,8 @@ def load_library(path: Optional[str] = None):
         lib.relattn_test_skip_k_tile.restype = ctypes.c_int
         lib.relattn_test_prologue_skip_tile.argtypes = [ctypes.c_int32]
         lib.relattn_test_prologue_skip_tile.restype = ctypes.c_int
+        lib.relattn_test_backward_skip_step.argtypes = [ctypes.c_int32]
+        lib.relattn_test_backward_skip_step.restype = ctypes.c_int
         lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
         lib.relattn_test_band_ctas.restype = ctypes.c_int
         lib.relattn_decode_paged.argtypes = [P, ctypes.POINTER(RelattnPagedKV), vp]
@@ -205,6 +207,11 @@ def relattn_test_skip_k_tile(tile: int) -> int:
 
 def relattn_test_prologue_skip_tile(tile: int) -> int:
     return load_library().relattn_test_prologue_skip_tile(int(tile))
+
+
+def relattn_test_backward_skip_step(step: int) -> int:
+    """Test hook: the tcgen05 backward producers never load step ``step`` (-1: off)."""
+    return int(load_library().relattn_test_backward_skip_step(int(step)))
 
 
 def relattn_test_band_ctas(n: int) -> int:

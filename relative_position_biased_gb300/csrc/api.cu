@@ -18,6 +18,8 @@ int g_test_skip_k_tile = -1;
 int g_test_band_ctas = 0;
 // test hook (relattn_test_prologue_skip_tile): token tile whose copies are never issued
 int g_test_prologue_skip = -1;
+// test hook (relattn_test_backward_skip_step): step whose copies the tcgen05 backward never issues
+int g_test_bwd_skip = -1;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -449,6 +451,7 @@ relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
                    static_cast<char *>(p->workspace) + backward_d_bytes(f) + backward_rall_bytes(f) +
                    backward_dq_part_bytes(f)) : nullptr;
   a.kv_split = 1;              // (set by the launcher)
+  a.test_skip_step = g_test_bwd_skip;
   a.err = err;
   a.batch = f.batch;
   a.total_q = f.total_q;
@@ -525,6 +528,12 @@ relattn_status relattn_test_skip_k_tile(int32_t tile) {
 relattn_status relattn_test_prologue_skip_tile(int32_t tile) {
   if (tile < -1) return RELATTN_ERR_INVALID_ARG;
   g_test_prologue_skip = tile;
+  return RELATTN_OK;
+}
+
+relattn_status relattn_test_backward_skip_step(int32_t step) {
+  if (step < -1) return RELATTN_ERR_INVALID_ARG;
+  g_test_bwd_skip = step;
   return RELATTN_OK;
 }
 

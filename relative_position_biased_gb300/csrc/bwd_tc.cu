@@ -182,11 +182,13 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
           break;
         const int h = step_h(n), row = cq + step_t0(n);
         const uint32_t dq = sb + SM_Q + st * 16384, dd = sb + SM_DO + st * 16384;
-        mbar_arrive_expect_tx(bar(B_Q_FULL + st), 32768);
-        tma_load_3d(dq, &map_q, 0, h, row, bar(B_Q_FULL + st));
-        tma_load_3d(dq + 8192, &map_q, 64, h, row, bar(B_Q_FULL + st));
-        tma_load_3d(dd, &map_do, 0, h, row, bar(B_Q_FULL + st));
-        tma_load_3d(dd + 8192, &map_do, 64, h, row, bar(B_Q_FULL + st));
+        if (n != a.test_skip_step) {   // (test hook: a skipped step is never loaded)
+          mbar_arrive_expect_tx(bar(B_Q_FULL + st), 32768);
+          tma_load_3d(dq, &map_q, 0, h, row, bar(B_Q_FULL + st));
+          tma_load_3d(dq + 8192, &map_q, 64, h, row, bar(B_Q_FULL + st));
+          tma_load_3d(dd, &map_do, 0, h, row, bar(B_Q_FULL + st));
+          tma_load_3d(dd + 8192, &map_do, 64, h, row, bar(B_Q_FULL + st));
+        }
         issued = n + 1;
       }
       if (*abort_flag) {   // let the copies this thread issued land before the CTA exits
@@ -549,11 +551,13 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
           break;
         const int key = ck + kbeg + n * KS;
         const uint32_t dk_ = sb + SQ_K + st * 16384, dv_ = sb + SQ_V + st * 16384;
-        mbar_arrive_expect_tx(bar(D_KV_FULL + st), 32768);
-        tma_load_3d(dk_, &map_k, 0, g, key, bar(D_KV_FULL + st));
-        tma_load_3d(dk_ + 8192, &map_k, 64, g, key, bar(D_KV_FULL + st));
-        tma_load_3d(dv_, &map_v, 0, g, key, bar(D_KV_FULL + st));
-        tma_load_3d(dv_ + 8192, &map_v, 64, g, key, bar(D_KV_FULL + st));
+        if (n != a.test_skip_step) {   // (test hook: a skipped step is never loaded)
+          mbar_arrive_expect_tx(bar(D_KV_FULL + st), 32768);
+          tma_load_3d(dk_, &map_k, 0, g, key, bar(D_KV_FULL + st));
+          tma_load_3d(dk_ + 8192, &map_k, 64, g, key, bar(D_KV_FULL + st));
+          tma_load_3d(dv_, &map_v, 0, g, key, bar(D_KV_FULL + st));
+          tma_load_3d(dv_ + 8192, &map_v, 64, g, key, bar(D_KV_FULL + st));
+        }
         issued = n + 1;
       }
       if (*abort_flag) {   // let the copies this thread issued land before the CTA exits

@@ -49,6 +49,7 @@ struct BwdArgs {
   int rall_ok;                 // 1: Rall has been written (the band's dq loads its R windows from it)
   float *dkv_part;             // workspace [2 halves][dk, dv][Tk, Hkv, 128] fp32 (GQA groups of 4, 6, 8 ...)
   int kv_split;                // 2: two tcgen05 dk / dv CTAs per key tile, each half the group's heads
+  int test_skip_step;          // test hook: a step whose copies the tcgen05 producers never issue (-1 off)
   float *dq_part;              // workspace [Tq, Hq, 128]: dq over the keys outside the bias band (fp32)
   int dq_split;                // 1: the tcgen05 dq takes the keys outside the band and writes
                                //    dq_part; the warp-MMA dq takes the band and adds dq_part

@@ -75,3 +75,27 @@ def test_prologue_wait_gives_up_and_context_recovers():
 def test_prologue_skip_hook_rejects_bad_tile():
     assert rpb.relattn_test_prologue_skip_tile(-2) != rpb.RELATTN_OK
     assert rpb.relattn_test_prologue_skip_tile(-1) == rpb.RELATTN_OK
+
+
+def test_backward_skip_hook_times_out_and_recovers():
+    """The tcgen05 backward kernels' producers leave step 0 without copies:
+    the waits behind it run out, every CTA drains and frees its tensor memory,
+    the status is RELATTN_ERR_TIMEOUT, and the next call on the same context
+    is correct. The shape keeps each kernel to one wave of CTAs."""
+    from tests.test_backward_gpu import check as check_bwd, run_gpu as bwd_gpu
+    w = W.custom("bwd_skip", [300], [300], 4, 2, 32, 64)
+    inp = W.make_inputs(w, with_dout=True)
+    assert rpb.relattn_test_backward_skip_step(0) == rpb.RELATTN_OK
+    try:
+        with pytest.raises(AssertionError, match="RELATTN_ERR_TIMEOUT"):
+            bwd_gpu(w, inp)               # synchronises, then reads the status
+        word = rpb.relattn_last_device_error_word()
+    finally:
+        rpb.relattn_test_backward_skip_step(-1)
+    assert word & 2 and (word >> 8) > 0
+    check_bwd(w)                          # hook off: correct on the same context
+
+
+def test_backward_skip_hook_rejects_bad_step():
+    assert rpb.relattn_test_backward_skip_step(-2) != rpb.RELATTN_OK
+    assert rpb.relattn_test_backward_skip_step(-1) == rpb.RELATTN_OK

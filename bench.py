@@ -1,31 +1,40 @@
 #!/usr/bin/env python3
 """Benchmark of the relative-attention forward on GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-  1. prefill of the sliding-window workload (4 x 8192 tokens, Hq=16, Hkv=2,
-     window 4096, r_dim 64, E 1024) -- rel projection, QK^T, bias gather,
-     mask, online softmax, PV, epilogue;
-  2. split-KV decode + LSE combine of the long-context MTP verify
-     (9 query rows against 1,048,576 keys, log-scale);
-  3. split-KV decode + LSE combine of the batched decode
-     (64 sequences, 1 query row each, KV lengths U[1024, 32768]).
-`value` is the prefill throughput (TFLOP/s, algorithmic flops over the
-prefill kernel time); the decode HBM throughput (GB/s of visible K/V over the
-decode call time) is reported beside it.  The attention prologue of the
-prefill chunk (ShortConv of k / v, RMSNorm of q / k, KV-cache write, conv
-state) is timed after the step, on its own, and reported under `prologue`
-in GB/s of the bytes it must move; the backward of the prefill (dq, dk, dv,
-dr from the saved out / lse) likewise under `backward`, in TFLOP/s of its
-algorithmic flops (five 128-deep products per visible pair and head, plus
-dr in the bias band).  Both decodes are also timed through a paged copy of
-their K / V (128-key pages in a shuffled pool) and reported under
-`decode.paged`.  L2 is flushed by a 256 MiB write
-before every timed kernel; the flush is outside the timed events.  Before the
-flush the stream is held busy for about half a millisecond, so the host has
-queued the timed call (argument marshalling, tensor-map encoding, launch)
-before the device reaches it: the device-timed window holds device work only.
+One step = one pass of the whole hot path over one batch of synthetic input,
+for every workload of the benchmark set:
+  1. prefill of the full-attention varlen workload with log-scale (4
+     sequences, lengths U[16384, 65536] from seed 0, Hq=16, Hkv=2, r_dim 64,
+     E 1024) -- rel projection, QK^T, bias gather, mask, online softmax, PV,
+     epilogue.  This is the largest single-GPU prefill, and `value` is its
+     throughput (TFLOP/s, algorithmic flops over the call time);
+  2. prefill of the sliding-window workload (4 x 8192 tokens, window 4096),
+     reported under `prefill_swa` with its own roofline;
+  3. split-KV decode + LSE combine of the long-context MTP verify
+     (9 query rows against 1,048,576 keys, log-scale): `decode`;
+  4. split-KV decode + LSE combine of the batched decode (64 sequences, 1
+     query row each, KV lengths U[1024, 32768], log-scale):
+     `decode.batched`;
+  5. the same batch with a 4096-key window: `decode.batched_window`.
+Each phase is timed with CUDA events around the call on the launching
+stream; the per-phase figure is the median over the timed steps.  Decode
+throughput is GB/s of visible K/V over the call time (split kernel +
+combine).
 
-`e2e` is the same metric through the C ABI from host buffers. Every step
+The attention prologue of the SWA chunk (ShortConv of k / v, RMSNorm of q /
+k, KV-cache write, conv state) is timed after the step, on its own, and
+reported under `prologue` in GB/s of the bytes it must move; the backward of
+the SWA prefill (dq, dk, dv, dr from the saved out / lse) likewise under
+`backward`, in TFLOP/s of its algorithmic flops (five 128-deep products per
+visible pair and head, plus dr in the bias band).  Two decodes are also
+timed through a paged copy of their K / V (128-key pages in a shuffled pool)
+and reported under `decode.paged`.  L2 is flushed by a 256 MiB write before
+every timed call; the flush is outside the timed events.  Before the flush
+the stream is held busy for about half a millisecond, so the host has queued
+the timed call (argument marshalling, tensor-map encoding, launch) before
+the device reaches it: the device-timed window holds device work only.
+
+`e2e` is the headline metric through the C ABI from host buffers. Every step
 uploads its inputs from pinned host memory and reads out / lse back, and
 the timed window covers it all:
 - `value`: the copies overlap the calls, as a serving loop would run them.
@@ -64,15 +73,12 @@ METRIC = "relattn prefill TFLOP/s & decode HBM GB/s at 1 GB300; % of roofline"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+_FWD = ["relative_position_biased_gb300/csrc/fwd_tc.cu",
+        "relative_position_biased_gb300/csrc/tc_common.cuh",
+        "relative_position_biased_gb300/csrc/common.cuh"]
 KERNEL_SOURCES = {
-    "prefill": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
-                "relative_position_biased_gb300/csrc/fwd_tc_main.cu",
-                "relative_position_biased_gb300/csrc/tc_common.cuh",
-                "relative_position_biased_gb300/csrc/common.cuh"],
-    "decode": ["relative_position_biased_gb300/csrc/fwd_tc.cu",
-               "relative_position_biased_gb300/csrc/tc_common.cuh",
-               "relative_position_biased_gb300/csrc/common.cuh",
-               "relative_position_biased_gb300/csrc/combine.cu"],
+    "prefill": _FWD + ["relative_position_biased_gb300/csrc/fwd_tc_main.cu"],
+    "decode": _FWD + ["relative_position_biased_gb300/csrc/combine.cu"],
     "backward": ["relative_position_biased_gb300/csrc/bwd_mma.cu",
                  "relative_position_biased_gb300/csrc/bwd_tc.cu",
                  "relative_position_biased_gb300/csrc/tc_common.cuh",
@@ -99,15 +105,20 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def load_traffic(kind: str):
-    """dram bytes per launch from a committed ncu summary, if it is current."""
+def load_traffic(phase: str, kind: str):
+    """dram bytes per call of `phase` from a committed ncu summary, if the
+    sources of its kernels (`kind`) are unchanged since the capture."""
     try:
-        t = json.load(open(TRAFFIC_PATH)).get(kind)
+        t = json.load(open(TRAFFIC_PATH)).get(phase)
     except (OSError, ValueError):
         return None
     if not t or t.get("src_sha") != src_sha(kind):
         return None
     return t.get("bytes_per_launch")
+
+
+def median(xs):
+    return statistics.median(xs) if xs else float("nan")
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -206,9 +217,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workloads
 
+# phases of one step, in order: (name, workload); the first is the headline
 def step_workloads():
-    return {"prefill": W.swa_prefill(), "decode_long": W.decode_mtp_long(),
-            "decode_batched": W.decode_batched()}
+    return {"prefill": W.full_prefill_logscale(), "prefill_swa": W.swa_prefill(),
+            "decode_long": W.decode_mtp_long(), "decode_batched": W.decode_batched(),
+            "decode_batched_w": W.decode_batched(window=4096)}
+
+
+STEP_PHASES = ("prefill", "prefill_swa", "decode_long", "decode_batched", "decode_batched_w")
 
 
 def _kw(w):
@@ -231,6 +247,7 @@ class Phase:
         self.lse = torch.empty(self.dev["q"].shape[1], self.dev["q"].shape[0],
                                dtype=torch.float32, device="cuda")
         self.decode = w.is_decode
+        self.kind = "decode" if self.decode else "prefill"
         self.ws = None
         # prefill with a bias band: the band kernel, then the main kernel
         self.launches = 2 if (w.r_dim > 0 and w.rel_extent > 0) else 1
@@ -487,13 +504,13 @@ def reference_arm(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    w = W.swa_prefill()
+    w = step_workloads()["prefill"]
     inp = W.make_inputs(w)
     # each step: a sample of query rows sized to about a second of oracle work
-    cal = oracle_sample_rows(w, 64, seed=3)
+    cal = oracle_sample_rows(w, 16, seed=3)
     for _ in range(args.warmup):
         cdt, _, _ = time_oracle(w, inp, cal)
-    n_step = int(min(sum(w.q_lens), max(64, 64 * 1.0 / max(cdt, 1e-3))))
+    n_step = int(min(sum(w.q_lens), max(16, 16 * 1.0 / max(cdt, 1e-3))))
     dts, fl = [], 0
     t_all0 = time.perf_counter()
     for s in range(args.steps):
@@ -523,47 +540,60 @@ CPU_SAMPLE_SECONDS = 10.0   # oracle work for the cpu_baseline (bounded sample)
 
 
 def cpu_baseline(wl, host):
-    """Oracle on the host cores over a bounded sample of the prefill workload:
-    a short calibration sizes the sample to about CPU_SAMPLE_SECONDS."""
+    """Oracle on the host cores over a bounded sample of the headline prefill
+    workload: a short calibration sizes the sample to about
+    CPU_SAMPLE_SECONDS.  Beside it: every row of the MTP decode, one sequence
+    of the SWA chunk's prologue, and the last 64 rows of one SWA sequence's
+    backward."""
     w = wl["prefill"]
-    cal = oracle_sample_rows(w, 128, seed=3)
+    cal = oracle_sample_rows(w, 16, seed=3)
     cdt, _, _ = time_oracle(w, host["prefill"], cal)
-    n = int(min(sum(w.q_lens), max(128, 128 * CPU_SAMPLE_SECONDS / max(cdt, 1e-3))))
+    n = int(min(sum(w.q_lens), max(16, 16 * CPU_SAMPLE_SECONDS / max(cdt, 1e-3))))
     rows = oracle_sample_rows(w, n)
     dt, f, cores = time_oracle(w, host["prefill"], rows)
     wd = wl["decode_long"]
     drows = np.arange(sum(wd.q_lens), dtype=np.int64)   # every MTP row
     ddt, _, _ = time_oracle(wd, host["decode_long"], drows)
-    # the prologue oracle over the first sequence of the prefill chunk
+    # the prologue oracle over the first sequence of the SWA chunk
     from oracle import prologue as OP
-    wp = W.custom("prologue_sample", w.q_lens[:1], w.k_lens[:1], w.Hq, w.Hkv, 0, 0)
+    ws_ = wl["prefill_swa"]
+    wp = W.custom("prologue_sample", ws_.q_lens[:1], ws_.k_lens[:1], ws_.Hq, ws_.Hkv, 0, 0)
     pin = W.make_prologue_inputs(wp)
     t0 = time.perf_counter()
     OP.prologue(pin["q"], pin["k"], pin["v"], pin["conv_k"], pin["conv_v"], pin["norm_q"],
                 pin["norm_k"], pin["cu_seqlens_q"], pin["cu_seqlens_k"])
     pdt = time.perf_counter() - t0
     pro = {"value": A.prologue_bytes(wp) / pdt / 1e9, "unit": "GB/s",
-           "sample": f"one {wp.q_lens[0]}-row sequence x ({w.Hq} q + 2x{w.Hkv} kv) heads "
+           "sample": f"one {wp.q_lens[0]}-row sequence x ({ws_.Hq} q + 2x{ws_.Hkv} kv) heads "
                      f"({pdt:.1f} s)"}
-    # the backward oracle over the last 64 rows of the first sequence (a
+    # the backward oracle over the last 64 rows of the first SWA sequence (a
     # chunk at the end of its 8,192 keys)
     import oracle
-    T0 = w.q_lens[0]
-    wb = W.custom("bwd_sample", [64], [T0], w.Hq, w.Hkv, w.r_dim, w.rel_extent, window=w.window)
-    bin_ = W.make_inputs(w, with_dout=True)
+    T0 = ws_.q_lens[0]
+    wb = W.custom("bwd_sample", [64], [T0], ws_.Hq, ws_.Hkv, ws_.r_dim, ws_.rel_extent,
+                  window=ws_.window)
+    bin_ = W.make_inputs(ws_, with_dout=True)
     sl = slice(T0 - 64, T0)
     t0 = time.perf_counter()
     oracle.backward(bin_["q"][sl], bin_["k"][:T0], bin_["v"][:T0], bin_["r"][sl], bin_["P"],
-                    bin_["dout"][sl], [0, 64], [0, T0], alpha=w.alpha, window=w.window)
+                    bin_["dout"][sl], [0, 64], [0, T0], alpha=ws_.alpha, window=ws_.window)
     bdt = time.perf_counter() - t0
     bwd = {"value": A.bwd_flops(wb) / bdt / 1e12, "unit": "TFLOP/s",
-           "sample": f"the last 64 rows x {w.Hq} heads of one {T0}-token sequence ({bdt:.1f} s, "
-                     f"{w.Hkv} threads: one task per kv head)"}
+           "sample": f"the last 64 rows x {ws_.Hq} heads of one {T0}-token sequence ({bdt:.1f} s, "
+                     f"{ws_.Hkv} threads: one task per kv head)"}
     return {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "prologue": pro, "backward": bwd,
             "sample": f"{n} random query rows x {w.Hq} heads of {w.name} ({dt:.1f} s)",
             "decode": {"value": decode_rows_bytes(wd, drows) / ddt / 1e9, "unit": "GB/s",
                        "sample": f"all {len(drows)} query rows x {wd.Hq} heads of {wd.name} ({ddt:.1f} s)"}}
+
+
+def _roofline(bound, achieved, peak, unit, traffic, peak_kind, **extra):
+    r = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+         "frac": achieved / peak, "traffic": traffic}
+    r.update(extra)
+    r["peak_source"] = peak_kind
+    return r
 
 
 def gpu_arm(args):
@@ -578,16 +608,14 @@ def gpu_arm(args):
 
     wl = step_workloads()
     if args.only == "prologue":
-        return single_phase(args, ProloguePhase(wl["prefill"], rpb))
+        return single_phase(args, ProloguePhase(wl["prefill_swa"], rpb))
     if args.only == "backward":
-        return single_phase(args, BackwardPhase(wl["prefill"], rpb))
+        return single_phase(args, BackwardPhase(wl["prefill_swa"], rpb))
     if args.only:
-        wl = {args.only: wl[args.only]}
+        return single_phase(args, Phase(args.only, wl[args.only], W.make_inputs(wl[args.only]), rpb))
     host = {k: W.make_inputs(w) for k, w in wl.items()}
-    names = ("prefill", "decode_long", "decode_batched")
-    if args.only:
-        return single_phase(args, Phase(args.only, wl[args.only], host[args.only], rpb))
-    phases = [Phase(k, wl[k], host[k], rpb) for k in names]
+    phases = [Phase(k, wl[k], host[k], rpb) for k in STEP_PHASES]
+    ph = {p.name: p for p in phases}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
     for _ in range(args.warmup):
@@ -606,9 +634,11 @@ def gpu_arm(args):
         wall = time.perf_counter() - t0
     barrier(dist)
     clocks = clk.summary()
+    if rpb.relattn_get_device_error() != 0:
+        raise SystemExit("device error word set during the timed steps")
 
-    # the attention prologue of the prefill chunk, timed on its own
-    pro = ProloguePhase(wl["prefill"], rpb)
+    # the attention prologue of the SWA chunk, timed on its own
+    pro = ProloguePhase(wl["prefill_swa"], rpb)
     for _ in range(args.warmup):
         pro.run()
     torch.cuda.synchronize()
@@ -616,8 +646,8 @@ def gpu_arm(args):
     torch.cuda.synchronize()
     if rpb.relattn_get_device_error() != 0:
         raise SystemExit("device error word set by the prologue")
-    # both decodes again through 128-key pages of a shuffled pool
-    paged = [PagedDecodePhase(dl_p, 128, rpb) for dl_p in phases[1:]]
+    # two decodes again through 128-key pages of a shuffled pool
+    paged = [PagedDecodePhase(ph[n], 128, rpb) for n in ("decode_long", "decode_batched")]
     for _ in range(args.warmup):
         for p in paged:
             p.run()
@@ -628,8 +658,8 @@ def gpu_arm(args):
         raise SystemExit("device error word set by the paged decode")
     for p in paged:
         del p.k_pool, p.v_pool
-    # the backward of the prefill, timed on its own
-    bwd = BackwardPhase(wl["prefill"], rpb)
+    # the backward of the SWA prefill, timed on its own
+    bwd = BackwardPhase(wl["prefill_swa"], rpb)
     for _ in range(args.warmup):
         bwd.run()
     torch.cuda.synchronize()
@@ -644,36 +674,35 @@ def gpu_arm(args):
     e2e_steps_pipe = max(4, min(args.steps, 8))
     e2e_p = e2e_pipelined(phases, e2e_steps_pipe, flush)
 
-    pre, dl, db = phases
-    ms = {p.name: sum(times[p.name]) for p in phases}
-    step_ms = sum(ms.values()) / args.steps
-    pre_ms = max_over_ranks(ms["prefill"] / args.steps, dist)
-    dl_ms = max_over_ranks(ms["decode_long"] / args.steps, dist)
-    db_ms = max_over_ranks(ms["decode_batched"] / args.steps, dist)
-    step_ms = max_over_ranks(step_ms, dist)
-    pro_ms = max_over_ranks(sum(pro_t) / len(pro_t), dist)
-    pro_gbs = pro.bytes / (pro_ms * 1e-3) / 1e9
-    pg_ms = {p.name: max_over_ranks(sum(pg_t[p.name]) / len(pg_t[p.name]), dist) for p in paged}
-    bwd_ms = max_over_ranks(sum(bwd_t) / len(bwd_t), dist)
-    bwd_tf = bwd.flops / (bwd_ms * 1e-3) / 1e12
-    value = job_rate(pre.flops, pre_ms, ws, 1e12)
-    peaks, peak_kind = load_peaks()
-    tf_peak = peaks["bf16_tflops"]
-    hbm_peak = peaks["hbm_gbs"]
-    pre_tf = pre.flops / (pre_ms * 1e-3) / 1e12
-    dl_gbs = dl.bytes / (dl_ms * 1e-3) / 1e9
-    db_gbs = db.bytes / (db_ms * 1e-3) / 1e9
-    e2e_pre_serial = sum(e2e_t["prefill"]) / len(e2e_t["prefill"])
-    e2e_dl_serial = sum(e2e_t["decode_long"]) / len(e2e_t["decode_long"])
-    e2e_pre = max_over_ranks(e2e_p["prefill"], dist)
-    e2e_dl = max_over_ranks(e2e_p["decode_long"], dist)
-    e2e_pre_serial = max_over_ranks(e2e_pre_serial, dist)
-    e2e_dl_serial = max_over_ranks(e2e_dl_serial, dist)
+    # per-phase device time: the median of the timed steps, max over ranks
+    ms = {n: max_over_ranks(median(times[n]), dist) for n in STEP_PHASES}
+    step_ms = max_over_ranks(sum(median(times[n]) for n in STEP_PHASES), dist)
+    pro_ms = max_over_ranks(median(pro_t), dist)
+    pg_ms = {p.name: max_over_ranks(median(pg_t[p.name]), dist) for p in paged}
+    bwd_ms = max_over_ranks(median(bwd_t), dist)
+    e2e_ser = {n: max_over_ranks(median(e2e_t[n]), dist) for n in STEP_PHASES}
+    e2e_pipe = {n: max_over_ranks(e2e_p[n], dist) for n in STEP_PHASES}
     if rank != 0:
         return 0
+    peaks, peak_kind = load_peaks()
+    tf_peak, hbm_peak = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    tf_src = f"{peak_kind} bf16 dense (burst)"
+    hbm_src = f"{peak_kind} HBM copy"
+
+    def tflops(p):   # one GPU's rate
+        return p.flops / (ms[p.name] * 1e-3) / 1e12
+
+    def gbs(p):
+        return p.bytes / (ms[p.name] * 1e-3) / 1e9
+
+    pre, swa, dl, db, dbw = (ph[n] for n in STEP_PHASES)
+    prefill_kernels = ("relattn_fwd_tc_kernel<prefill, band> + relattn_fwd_tc_main_kernel "
+                       "(the two launches of one prefill call)")
+    pro_gbs = pro.bytes / (pro_ms * 1e-3) / 1e9
+    bwd_tf = bwd.flops / (bwd_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": job_rate(pre.flops, ms["prefill"], ws, 1e12),
         "unit": "TFLOP/s",
         "n_gpus": ws,
         "steps": args.steps,
@@ -685,35 +714,55 @@ def gpu_arm(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"{pre.w.name} + {dl.w.name} + {db.w.name}",
-            "prefill": {"batch": pre.w.batch, "seq_len": pre.w.q_lens[0], "Hq": pre.w.Hq,
+            "workload": pre.w.name,
+            "step": " + ".join(ph[n].w.name for n in STEP_PHASES),
+            "prefill": {"batch": pre.w.batch, "seq_lens": list(pre.w.q_lens), "Hq": pre.w.Hq,
                         "Hkv": pre.w.Hkv, "head_dim": 128, "r_dim": pre.w.r_dim,
                         "rel_extent": pre.w.rel_extent, "window": pre.w.window,
-                        "flops": pre.flops},
+                        "log_scale_base": pre.w.log_scale_base, "flops": pre.flops},
+            "prefill_swa": {"batch": swa.w.batch, "seq_len": swa.w.q_lens[0],
+                            "window": swa.w.window, "flops": swa.flops},
             "decode_long": {"q_rows": dl.w.q_lens[0], "kv_len": dl.w.k_lens[0],
                             "log_scale_base": dl.w.log_scale_base, "kv_bytes": dl.bytes,
                             "splits": dl.splits},
             "decode_batched": {"batch": db.w.batch, "kv_lens": "U[1024,32768]",
                                "kv_bytes": db.bytes, "splits": db.splits},
+            "decode_batched_w": {"batch": dbw.w.batch, "kv_lens": "U[1024,32768]",
+                                 "window": dbw.w.window, "kv_bytes": dbw.bytes,
+                                 "splits": dbw.splits},
+            "statistic": f"median of {args.steps} timed steps per phase",
             "l2": "flushed by a 256 MiB write before every timed call",
             "parallelism": f"replicas x{ws}",
         },
-        "phases_ms": {"prefill": pre_ms, "decode_long": dl_ms, "decode_batched": db_ms},
-        "roofline": {"bound": "tensor", "achieved": pre_tf, "peak": tf_peak,
-                     "unit": "TFLOP/s", "frac": pre_tf / tf_peak,
-                     "traffic": load_traffic("prefill"),
-                     "peak_source": f"{peak_kind} bf16 dense (burst)",
-                     "kernel": "relattn_fwd_tc_kernel<prefill, band> + relattn_fwd_tc_main_kernel "
-                               "(the two launches of one prefill call)"},
+        "phases_ms": dict(ms),
+        "roofline": _roofline("tensor", tflops(pre), tf_peak, "TFLOP/s",
+                              load_traffic("prefill_full", "prefill"), tf_src,
+                              kernel=prefill_kernels, workload=pre.w.name),
+        "prefill_swa": {
+            "value": job_rate(swa.flops, ms["prefill_swa"], ws, 1e12), "unit": "TFLOP/s",
+            "ms": ms["prefill_swa"], "workload": swa.w.name, "flops": swa.flops,
+            "roofline": _roofline("tensor", tflops(swa), tf_peak, "TFLOP/s",
+                                  load_traffic("prefill_swa", "prefill"), tf_src,
+                                  kernel=prefill_kernels)},
         "decode": {
-            "value": job_rate(dl.bytes, dl_ms, ws, 1e9), "unit": "GB/s", "workload": dl.w.name,
-            "roofline": {"bound": "hbm", "achieved": dl_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": dl_gbs / hbm_peak, "frac_vs_8tbs": dl_gbs / 8000.0,
-                         "traffic": load_traffic("decode"),
-                         "peak_source": f"{peak_kind} HBM copy"},
-            "batched": {"value": job_rate(db.bytes, db_ms, ws, 1e9), "unit": "GB/s",
-                        "workload": db.w.name,
-                        "frac": db_gbs / hbm_peak},
+            "value": job_rate(dl.bytes, ms["decode_long"], ws, 1e9), "unit": "GB/s",
+            "workload": dl.w.name, "ms": ms["decode_long"],
+            "roofline": _roofline("hbm", gbs(dl), hbm_peak, "GB/s",
+                                  load_traffic("decode_long", "decode"), hbm_src,
+                                  frac_vs_8tbs=gbs(dl) / 8000.0,
+                                  kernel="relattn_fwd_tc_kernel<decode> + relattn_combine_kernel"),
+            "batched": {"value": job_rate(db.bytes, ms["decode_batched"], ws, 1e9), "unit": "GB/s",
+                        "workload": db.w.name, "ms": ms["decode_batched"],
+                        "frac": gbs(db) / hbm_peak,
+                        "roofline": _roofline("hbm", gbs(db), hbm_peak, "GB/s",
+                                              load_traffic("decode_batched", "decode"), hbm_src,
+                                              frac_vs_8tbs=gbs(db) / 8000.0)},
+            "batched_window": {"value": job_rate(dbw.bytes, ms["decode_batched_w"], ws, 1e9),
+                               "unit": "GB/s", "workload": dbw.w.name,
+                               "ms": ms["decode_batched_w"], "frac": gbs(dbw) / hbm_peak,
+                               "roofline": _roofline("hbm", gbs(dbw), hbm_peak, "GB/s",
+                                                     load_traffic("decode_batched_w4096", "decode"),
+                                                     hbm_src, frac_vs_8tbs=gbs(dbw) / 8000.0)},
             "paged": {p.name: {"value": p.bytes / (pg_ms[p.name] * 1e-3) / 1e9, "unit": "GB/s",
                                "ms": pg_ms[p.name], "page_size": p.page_size,
                                "frac": p.bytes / (pg_ms[p.name] * 1e-3) / 1e9 / hbm_peak}
@@ -721,34 +770,38 @@ def gpu_arm(args):
         },
         "prologue": {
             "value": job_rate(pro.bytes, pro_ms, ws, 1e9), "unit": "GB/s", "ms": pro_ms,
-            "workload": pre.w.name,
+            "workload": swa.w.name,
             "what": "ShortConv k/v + RMSNorm q/k + KV-cache write + conv state out",
             "bytes": pro.bytes, "launches": args.steps * pro.launches,
-            "roofline": {"bound": "hbm", "achieved": pro_gbs, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": pro_gbs / hbm_peak, "traffic": load_traffic("prologue"),
-                         "peak_source": f"{peak_kind} HBM copy"}},
+            "roofline": _roofline("hbm", pro_gbs, hbm_peak, "GB/s",
+                                  load_traffic("prologue", "prologue"), hbm_src)},
         "backward": {
             "value": job_rate(bwd.flops, bwd_ms, ws, 1e12), "unit": "TFLOP/s", "ms": bwd_ms,
-            "workload": pre.w.name,
+            "workload": swa.w.name,
             "what": "dq, dk, dv, dr of sum(dout * out), P frozen", "flops": bwd.flops,
             "launches": len(bwd_t) * bwd.launches,
-            "roofline": {"bound": "tensor", "achieved": bwd_tf, "peak": tf_peak,
-                         "unit": "TFLOP/s", "frac": bwd_tf / tf_peak,
-                         "traffic": load_traffic("backward"),
-                         "peak_source": f"{peak_kind} bf16 dense (burst)",
-                         "kernel": "relattn_bwd_rel_kernel + relattn_bwd_dot_kernel + "
-                                   "relattn_bwd_dq_tc_kernel + relattn_bwd_dq_kernel (band, "
-                                   "mma.sync) + relattn_bwd_dkdv_tc_kernel (heads split "
-                                   "over two CTAs) + relattn_bwd_dkv_reduce_kernel"}},
-        "e2e": {"value": job_rate(pre.flops, e2e_pre, ws, 1e12), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": pre.h2d + dl.h2d + db.h2d,
-                "d2h_bytes_per_step": pre.d2h + dl.d2h + db.d2h,
-                "decode_value": job_rate(dl.bytes, e2e_dl, ws, 1e9), "decode_unit": "GB/s",
+            "roofline": _roofline("tensor", bwd_tf, tf_peak, "TFLOP/s",
+                                  load_traffic("backward", "backward"), tf_src,
+                                  kernel="relattn_bwd_rel_kernel + relattn_bwd_dot_kernel + "
+                                         "relattn_bwd_dq_tc_kernel + relattn_bwd_dq_kernel (band, "
+                                         "mma.sync) + relattn_bwd_dkdv_tc_kernel (heads split "
+                                         "over two CTAs) + relattn_bwd_dkv_reduce_kernel")},
+        "e2e": {"value": job_rate(pre.flops, e2e_pipe["prefill"], ws, 1e12), "unit": "TFLOP/s",
+                "workload": pre.w.name,
+                "h2d_bytes_per_step": sum(p.h2d for p in phases),
+                "d2h_bytes_per_step": sum(p.d2h for p in phases),
                 "path": "pinned host buffers -> H2D -> relattn_* C ABI -> D2H out+lse",
                 "overlap": f"{e2e_steps_pipe} steps per phase; step k+1's H2D and step k-1's D2H "
                            "on two copy streams while step k computes (two device buffer sets)",
-                "serial_value": job_rate(pre.flops, e2e_pre_serial, ws, 1e12),
-                "serial_decode_value": job_rate(dl.bytes, e2e_dl_serial, ws, 1e9)},
+                "serial_value": job_rate(pre.flops, e2e_ser["prefill"], ws, 1e12),
+                "phases": {n: {"value": (job_rate(ph[n].flops, e2e_pipe[n], ws, 1e12) if not ph[n].decode
+                                         else job_rate(ph[n].bytes, e2e_pipe[n], ws, 1e9)),
+                               "serial_value": (job_rate(ph[n].flops, e2e_ser[n], ws, 1e12)
+                                                if not ph[n].decode
+                                                else job_rate(ph[n].bytes, e2e_ser[n], ws, 1e9)),
+                               "unit": "GB/s" if ph[n].decode else "TFLOP/s",
+                               "h2d_bytes": ph[n].h2d, "d2h_bytes": ph[n].d2h}
+                           for n in STEP_PHASES}},
         "gpu_launches": args.steps * sum(p.launches for p in phases),
         "clocks": clocks,
         "wall_s_timed_region": wall,
@@ -799,7 +852,7 @@ def single_phase(args, p):
         p.run()
     torch.cuda.synchronize()
     t = timed_steps([p], args.steps, flush)[p.name]
-    ms = sum(t) / len(t)
+    ms = median(t)
     rate = (p.bytes / (ms * 1e-3) / 1e9, "GB/s") if p.decode else \
         (p.flops / (ms * 1e-3) / 1e12, "TFLOP/s")
     print(json.dumps({"phase": p.name, "workload": p.w.name, "ms": ms, "value": rate[0],
@@ -814,8 +867,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode_long", "decode_batched", "prologue",
-                                       "backward"],
+    ap.add_argument("--only", choices=list(STEP_PHASES) + ["prologue", "backward"],
                     help="time one phase alone (profiling captures)")
     ap.add_argument("--splits-sweep", action="store_true",
                     help="time the decodes at fixed split counts beside the heuristic's choice")

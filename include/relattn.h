@@ -179,7 +179,9 @@ relattn_status relattn_combine(const float *o_part, const float *lse_part, int32
  *     more than that for these params, the call returns RELATTN_ERR_WORKSPACE
  *     and launches nothing (pass a smaller num_splits, or use relattn_decode).
  *   - The first call on a device looks up the array's device address (with
- *     that device current).  Make that first call before any stream capture.
+ *     that device current), and so does the first call after the device's
+ *     context changes (a cudaDeviceReset loads the library's module again).
+ *     Make those calls before any stream capture.
  *   - Every call on a device shares the one array.  No contents need to carry
  *     over between calls, but two calls whose kernels can overlap on the GPU
  *     (unordered streams) race on it: order them, or use relattn_decode.
@@ -305,49 +307,57 @@ typedef struct relattn_prologue_params {
 
 relattn_status relattn_prologue(const relattn_prologue_params *params, void *stream);
 
-/* Test hook for the failure path; not for production use, and with no
- * counterpart on the pages.  With tile >= 0, every later launch of the
- * tensor-core kernels leaves key tile `tile` (the tile-th 128-key tile a CTA
- * of that kernel visits) unloaded, so the wait of the MMA issuer on it runs out after its
+/* ------------------------------------------------------------------ test hooks
+ *
+ * Declared only with RELATTN_TEST_HOOKS defined, and exported only by the
+ * test build of the library (librelattn_test.so, compiled with that macro).
+ * The product library librelattn.so has none of them: its launches run with
+ * every hook off.  None has a counterpart on the pages.  Each setting is
+ * process-wide (an atomic read by the next launches of the same library);
+ * tests set a hook, run one call, and clear it.
+ */
+#ifdef RELATTN_TEST_HOOKS
+
+/* With tile >= 0, every later launch of the forward tensor-core kernels
+ * leaves key tile `tile` (the tile-th 128-key tile a CTA of that kernel
+ * visits) unloaded, so the wait of the MMA issuer on it runs out after its
  * bounded limit (about a second): the CTA gives up, drains its own copies and
  * MMAs, frees its tensor memory and exits, and relattn_get_device_error()
  * then returns RELATTN_ERR_TIMEOUT (outputs of affected rows are undefined).
- * tile = -1 restores normal operation; tile < -1 -> RELATTN_ERR_INVALID_ARG.
- * Process-wide; not thread-safe against concurrent launches. */
+ * tile = -1 restores normal operation; tile < -1 -> RELATTN_ERR_INVALID_ARG. */
 relattn_status relattn_test_skip_k_tile(int32_t tile);
 
-/* Test hook; not for production use, and with no counterpart on the pages.
- * The bias-band launch of the two-launch prefill runs one CTA per SM, each
- * walking several work items (128 query rows of one head); with n > 0 it
- * runs at most n CTAs instead, so that small problems also take the paths
- * where a CTA moves from item to item.  Results are unchanged (only the
- * speed).  n = 0 restores the default; n < 0 -> RELATTN_ERR_INVALID_ARG.
- * Process-wide; not thread-safe against concurrent launches. */
+/* The bias-band launch of the two-launch prefill, and the walking decode
+ * launch, run one CTA per SM, each walking several work items; with n > 0
+ * they run at most n CTAs instead, so that small problems also take the
+ * paths where a CTA moves from item to item.  Results are unchanged (only
+ * the speed).  n = 0 restores the default; n < 0 -> RELATTN_ERR_INVALID_ARG. */
 relattn_status relattn_test_band_ctas(int32_t n);
 
-/* Test hook for the failure path of relattn_prologue; not for production use,
- * and with no counterpart on the pages.  With tile >= 0 the staged prologue
+/* Failure path of relattn_prologue.  With tile >= 0 the staged prologue
  * kernel's producer never issues the copies of token tile `tile` (tiles of
  * consecutive chunk tokens, numbered from 0), so the waits of the CTA's
  * consumer warps on that stage run out after their bounded limit (about a
  * second): the CTA drains the copies it did issue and exits, and
  * relattn_get_device_error() then returns RELATTN_ERR_TIMEOUT (outputs of
  * that CTA's later tiles are undefined).  tile = -1 restores normal
- * operation; tile < -1 -> RELATTN_ERR_INVALID_ARG.  Process-wide; not
- * thread-safe against concurrent launches. */
+ * operation; tile < -1 -> RELATTN_ERR_INVALID_ARG. */
 relattn_status relattn_test_prologue_skip_tile(int32_t tile);
 
-/* Test hook for the failure path of relattn_backward; not for production use,
- * and with no counterpart on the pages.  With step >= 0 the tcgen05 backward
- * kernels' producers never issue the copies of their step `step` (a K / V
- * step of the dq kernel, a q / dout step of the dk / dv kernel), so the waits
- * behind it run out after their bounded limit (about a second per wave of
- * CTAs): each such CTA drains what it issued, frees its tensor memory and
+/* Failure path of relattn_backward, one tcgen05 kernel at a time.  kernel 0
+ * is the dk / dv kernel (its step = one q / dout stage), kernel 1 the dq
+ * kernel outside the bias band (its step = one K / V stage).  With step >= 0
+ * that kernel's producer never issues the copies of its step `step`, so the
+ * waits behind it run out after their bounded limit (about a second per wave
+ * of CTAs): each such CTA drains what it issued, frees its tensor memory and
  * exits, and relattn_get_device_error() then returns RELATTN_ERR_TIMEOUT
- * (the gradients are undefined).  step = -1 restores normal operation;
- * step < -1 -> RELATTN_ERR_INVALID_ARG.  Process-wide; not thread-safe
- * against concurrent launches. */
-relattn_status relattn_test_backward_skip_step(int32_t step);
+ * with the first wait site that gave up in bits 8+ of
+ * relattn_last_device_error_word() (sites 1-10: dk / dv kernel; 11-16: dq
+ * kernel).  The gradients are then undefined.  step = -1 restores normal
+ * operation; step < -1 or another kernel -> RELATTN_ERR_INVALID_ARG. */
+relattn_status relattn_test_backward_skip_step(int32_t kernel, int32_t step);
+
+#endif /* RELATTN_TEST_HOOKS */
 
 /* Human-readable name of a status code (static string). */
 const char *relattn_status_string(relattn_status status);

@@ -10,6 +10,7 @@ fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -19,6 +20,8 @@ from . import workloads  # noqa: F401  (seeded input generators)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librelattn.so")
+# the same kernels with the relattn_test_* hooks (built beside the product library)
+TEST_LIB_PATH = os.path.join(_HERE, "librelattn_test.so")
 
 RELATTN_OK = 0
 RELATTN_ERR_TIMEOUT = 4
@@ -31,9 +34,14 @@ EXPORTED = (
     "relattn_prefill", "relattn_decode", "relattn_decode_workspace_size",
     "relattn_decode_num_splits", "relattn_combine", "relattn_get_device_error",
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
-    "relattn_last_device_error_word", "relattn_test_skip_k_tile", "relattn_test_band_ctas",
+    "relattn_last_device_error_word",
     "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
-    "relattn_decode_paged", "relattn_test_prologue_skip_tile", "relattn_test_backward_skip_step",
+    "relattn_decode_paged",
+)
+# exported by the test build only
+TEST_HOOKS = (
+    "relattn_test_skip_k_tile", "relattn_test_band_ctas", "relattn_test_prologue_skip_tile",
+    "relattn_test_backward_skip_step",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
@@ -92,8 +100,9 @@ class RelattnPrologueParams(ctypes.Structure):
     ]
 
 
-_lock = threading.Lock()
+_lock = threading.RLock()
 _lib = None
+_libs = {}    # path -> configured handle
 
 
 def build(force: bool = False) -> str:
@@ -108,12 +117,51 @@ def _open(path: str):
 
 
 def load_library(path: Optional[str] = None):
-    """Load ``librelattn.so`` (raises if it has not been built)."""
+    """Load ``librelattn.so`` (raises if it has not been built).  Inside
+    ``test_library()`` this is the test build instead."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        lib = _open(path or LIB_PATH)
+        if path is not None:
+            return _configure(path)
+        if _lib is None:
+            _lib = _configure(LIB_PATH)
+        return _lib
+
+
+def load_test_library():
+    """Load ``librelattn_test.so``: the same kernels plus the relattn_test_* hooks."""
+    with _lock:
+        lib = _configure(TEST_LIB_PATH)
+        for name in TEST_HOOKS:
+            getattr(lib, name).restype = ctypes.c_int
+        lib.relattn_test_skip_k_tile.argtypes = [ctypes.c_int32]
+        lib.relattn_test_prologue_skip_tile.argtypes = [ctypes.c_int32]
+        lib.relattn_test_backward_skip_step.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
+        return lib
+
+
+@contextlib.contextmanager
+def test_library():
+    """Route every call of this module to the test build for the duration of
+    the block (tests that set a hook run their calls inside one).  The device
+    error word and the hooks belong to the test build's own copy."""
+    global _lib
+    with _lock:
+        prev = load_library()
+        _lib = load_test_library()
+    try:
+        yield _lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _configure(path: str):
+    with _lock:
+        if path in _libs:
+            return _libs[path]
+        lib = _open(path)
         P, vp = ctypes.POINTER(RelattnParams), ctypes.c_void_p
         for name in ("relattn_prefill", "relattn_decode", "relattn_decode_noalloc"):
             f = getattr(lib, name)
@@ -131,14 +179,6 @@ def load_library(path: Optional[str] = None):
         lib.relattn_status_string.restype = ctypes.c_char_p
         lib.relattn_last_device_error_word.argtypes = []
         lib.relattn_last_device_error_word.restype = ctypes.c_int32
-        lib.relattn_test_skip_k_tile.argtypes = [ctypes.c_int32]
-        lib.relattn_test_skip_k_tile.restype = ctypes.c_int
-        lib.relattn_test_prologue_skip_tile.argtypes = [ctypes.c_int32]
-        lib.relattn_test_prologue_skip_tile.restype = ctypes.c_int
-        lib.relattn_test_backward_skip_step.argtypes = [ctypes.c_int32]
-        lib.relattn_test_backward_skip_step.restype = ctypes.c_int
-        lib.relattn_test_band_ctas.argtypes = [ctypes.c_int32]
-        lib.relattn_test_band_ctas.restype = ctypes.c_int
         lib.relattn_decode_paged.argtypes = [P, ctypes.POINTER(RelattnPagedKV), vp]
         lib.relattn_decode_paged.restype = ctypes.c_int
         BP = ctypes.POINTER(RelattnBwdParams)
@@ -150,7 +190,7 @@ def load_library(path: Optional[str] = None):
         lib.relattn_prologue.restype = ctypes.c_int
         lib.relattn_version.argtypes = []
         lib.relattn_version.restype = ctypes.c_char_p
-        _lib = lib
+        _libs[path] = lib
         return lib
 
 
@@ -201,22 +241,24 @@ def relattn_last_device_error_word() -> int:
 
 
 def relattn_test_skip_k_tile(tile: int) -> int:
-    """Test hook: later tensor-core launches never load key tile ``tile`` (-1: off)."""
-    return int(load_library().relattn_test_skip_k_tile(int(tile)))
+    """Test build: later tensor-core launches never load key tile ``tile`` (-1: off)."""
+    return int(load_test_library().relattn_test_skip_k_tile(int(tile)))
 
 
 def relattn_test_prologue_skip_tile(tile: int) -> int:
-    return load_library().relattn_test_prologue_skip_tile(int(tile))
+    """Test build: the staged prologue never copies token tile ``tile`` (-1: off)."""
+    return int(load_test_library().relattn_test_prologue_skip_tile(int(tile)))
 
 
-def relattn_test_backward_skip_step(step: int) -> int:
-    """Test hook: the tcgen05 backward producers never load step ``step`` (-1: off)."""
-    return int(load_library().relattn_test_backward_skip_step(int(step)))
+def relattn_test_backward_skip_step(kernel: int, step: int) -> int:
+    """Test build: the tcgen05 backward producer of ``kernel`` (0: dk / dv, 1:
+    dq) never loads its step ``step`` (-1: off)."""
+    return int(load_test_library().relattn_test_backward_skip_step(int(kernel), int(step)))
 
 
 def relattn_test_band_ctas(n: int) -> int:
-    """Test hook: at most ``n`` CTAs for the persistent bias-band launch (0: one per SM)."""
-    return int(load_library().relattn_test_band_ctas(int(n)))
+    """Test build: at most ``n`` CTAs for the persistent / walking launches (0: one per SM)."""
+    return int(load_test_library().relattn_test_band_ctas(int(n)))
 
 
 def relattn_status_string(status: int) -> str:

@@ -3,6 +3,11 @@
 Each ``csrc/*.cu`` translation unit is compiled in parallel with nvcc, then
 linked into a shared library next to this file.  No CMake, no torch extension
 machinery: the library exposes only the C ABI in ``include/relattn.h``.
+
+A second library, ``librelattn_test.so``, links the same kernel objects with
+``api.cu`` compiled once more under ``RELATTN_TEST_HOOKS``: it adds the
+``relattn_test_*`` entry points the failure-path tests use.  The product
+library has no test hooks.
 """
 from __future__ import annotations
 
@@ -18,6 +23,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librelattn.so")
+TEST_LIB = os.path.join(HERE, "librelattn_test.so")
+TEST_DEFINE = "-DRELATTN_TEST_HOOKS"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -43,9 +50,9 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(TEST_LIB)):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(TEST_LIB))
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
@@ -56,9 +63,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     cc = nvcc()
     srcs = _sources()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-        cmd = [cc, *_flags(extra_flags), "-c", src, "-o", obj]
+    def compile_one(job):
+        src, test = job
+        obj = os.path.join(BUILD, os.path.basename(src) + (".test.o" if test else ".o"))
+        cmd = [cc, *_flags(extra_flags), *([TEST_DEFINE] if test else []), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -66,14 +74,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             print(r.stdout + r.stderr, file=sys.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
-        objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    api = os.path.join(CSRC, "api.cu")
+    jobs = [(s_, False) for s_ in srcs] + [(api, True)]
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    prod = objs[:len(srcs)]
+    test = [o for o, s_ in zip(prod, srcs) if s_ != api] + [objs[-1]]
+    for out, group in ((LIB, prod), (TEST_LIB, test)):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = [cc, *ARCH, "-shared", "-o", tmp, *group, "-lcudart"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
     return LIB
 
 

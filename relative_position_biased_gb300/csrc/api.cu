@@ -3,6 +3,7 @@
 // relattn_get_device_error), no host fallback.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -12,18 +13,28 @@ using namespace relattn;
 namespace {
 
 __device__ int g_device_error;
-// test hook (relattn_test_skip_k_tile): K tile the tcgen05 producer never loads
-int g_test_skip_k_tile = -1;
-// test hook (relattn_test_band_ctas): CTA cap of the persistent band launch
-int g_test_band_ctas = 0;
-// test hook (relattn_test_prologue_skip_tile): token tile whose copies are never issued
-int g_test_prologue_skip = -1;
-// test hook (relattn_test_backward_skip_step): step whose copies the tcgen05 backward never issues
-int g_test_bwd_skip = -1;
+
+#ifdef RELATTN_TEST_HOOKS
+// Test build only (librelattn_test.so): settings the relattn_test_* entry
+// points change, read by the launches of the same process.
+std::atomic<int> g_test_skip_k_tile{-1};     // K tile the tcgen05 producers never load
+std::atomic<int> g_test_band_ctas{0};        // CTA cap of the persistent band / walking launches
+std::atomic<int> g_test_prologue_skip{-1};   // token tile whose prologue copies are never issued
+std::atomic<int> g_test_bwd_dkdv_skip{-1};   // step the tcgen05 dk / dv producer never loads
+std::atomic<int> g_test_bwd_dq_skip{-1};     // step the tcgen05 dq producer never loads
+#else
+// The product library has no test hooks: these are constants (every hook off).
+constexpr int g_test_skip_k_tile = -1;
+constexpr int g_test_band_ctas = 0;
+constexpr int g_test_prologue_skip = -1;
+constexpr int g_test_bwd_dkdv_skip = -1;
+constexpr int g_test_bwd_dq_skip = -1;
+#endif
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int *g_err_ptr[kMaxDevices];
+void *g_err_ctx[kMaxDevices];   // the context g_err_ptr[dev] was looked up in
 int g_sms[kMaxDevices];
 int g_last_error_word = 0;
 
@@ -31,13 +42,17 @@ relattn_status device_state(int *dev_out, int **err_out, int *sms_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RELATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_err_ptr[dev]) {
+  void *ctx = current_cu_context();
+  if (!g_err_ptr[dev] || !ctx || ctx != g_err_ctx[dev]) {
+    // first call on this device, or a new context (after cudaDeviceReset):
+    // the error word's address is looked up again in the current one
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return RELATTN_ERR_CUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return RELATTN_ERR_CUDA;
     g_err_ptr[dev] = static_cast<int *>(p);
+    g_err_ctx[dev] = current_cu_context();
     g_sms[dev] = sms;
   }
   if (dev_out) *dev_out = dev;
@@ -112,7 +127,8 @@ relattn_status make_args(const relattn_params *p, KernelArgs *a) {
   x.split_chunk = 0;
   x.q_tiles = (p->max_seqlen_q + 127) / 128;
   x.row_blocks = 1;
-  x.sms = g_test_band_ctas > 0 ? g_test_band_ctas : sms;
+  const int band_ctas = g_test_band_ctas;
+  x.sms = band_ctas > 0 ? band_ctas : sms;
   return RELATTN_OK;
 }
 
@@ -451,7 +467,8 @@ relattn_status relattn_backward(const relattn_bwd_params *p, void *stream) {
                    static_cast<char *>(p->workspace) + backward_d_bytes(f) + backward_rall_bytes(f) +
                    backward_dq_part_bytes(f)) : nullptr;
   a.kv_split = 1;              // (set by the launcher)
-  a.test_skip_step = g_test_bwd_skip;
+  a.test_skip_dkdv_step = g_test_bwd_dkdv_skip;
+  a.test_skip_dq_step = g_test_bwd_dq_skip;
   a.err = err;
   a.batch = f.batch;
   a.total_q = f.total_q;
@@ -519,6 +536,7 @@ const char *relattn_version(void) { return "relattn 0.1 sm_103a"; }
 
 int32_t relattn_last_device_error_word(void) { return g_last_error_word; }
 
+#ifdef RELATTN_TEST_HOOKS
 relattn_status relattn_test_skip_k_tile(int32_t tile) {
   if (tile < -1) return RELATTN_ERR_INVALID_ARG;
   g_test_skip_k_tile = tile;
@@ -531,9 +549,9 @@ relattn_status relattn_test_prologue_skip_tile(int32_t tile) {
   return RELATTN_OK;
 }
 
-relattn_status relattn_test_backward_skip_step(int32_t step) {
-  if (step < -1) return RELATTN_ERR_INVALID_ARG;
-  g_test_bwd_skip = step;
+relattn_status relattn_test_backward_skip_step(int32_t kernel, int32_t step) {
+  if (step < -1 || kernel < 0 || kernel > 1) return RELATTN_ERR_INVALID_ARG;
+  (kernel == 0 ? g_test_bwd_dkdv_skip : g_test_bwd_dq_skip) = step;
   return RELATTN_OK;
 }
 
@@ -542,5 +560,6 @@ relattn_status relattn_test_band_ctas(int32_t n) {
   g_test_band_ctas = n;
   return RELATTN_OK;
 }
+#endif  // RELATTN_TEST_HOOKS
 
 }  // extern "C"

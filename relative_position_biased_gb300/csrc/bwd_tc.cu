@@ -182,7 +182,7 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
           break;
         const int h = step_h(n), row = cq + step_t0(n);
         const uint32_t dq = sb + SM_Q + st * 16384, dd = sb + SM_DO + st * 16384;
-        if (n != a.test_skip_step) {   // (test hook: a skipped step is never loaded)
+        if (n != a.test_skip_dkdv_step) {   // (test hook: a skipped step is never loaded)
           mbar_arrive_expect_tx(bar(B_Q_FULL + st), 32768);
           tma_load_3d(dq, &map_q, 0, h, row, bar(B_Q_FULL + st));
           tma_load_3d(dq + 8192, &map_q, 64, h, row, bar(B_Q_FULL + st));
@@ -408,7 +408,7 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
   }
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (tid == 0 && *abort_flag) record_timeout(a.err, *abort_flag);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -416,17 +416,37 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
 }
 
 
-// dk / dv = the two halves' fp32 sums, in bf16 (a split dk / dv launch)
+// dk / dv = the two halves' fp32 sums, in bf16 (a split dk / dv launch).  A
+// warp per key row.  Only rows the split dk / dv CTAs wrote are touched: rows
+// of sequences with consistent lengths, below cu_seqlens_k[batch] (rows past
+// it, and the rows of a sequence the kernels skipped, keep their contents, as
+// on the unsplit path).
 __global__ void __launch_bounds__(256) relattn_bwd_dkv_reduce_kernel(const BwdArgs a) {
-  const size_t n4 = (size_t)a.total_k * a.Hkv * kHeadDim / 4;   // float4 groups per tensor
+  const size_t n4 = (size_t)a.total_k * a.Hkv * (kHeadDim / 4);   // float4 groups per tensor
   const float4 *p = reinterpret_cast<const float4 *>(a.dkv_part);
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n4; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t which = i / n4, k = i - which * n4;            // 0: dk, 1: dv
-    const float4 x = p[which * n4 + k], y = p[(2 + which) * n4 + k];
-    uint2 o;
-    o.x = pack_bf16x2(x.x + y.x, x.y + y.y);
-    o.y = pack_bf16x2(x.z + y.z, x.w + y.w);
-    *reinterpret_cast<uint2 *>((which ? a.dv : a.dk) + 4 * k) = o;
+  const int lane = threadIdx.x & 31;
+  const int rows = min(a.cu_k[a.batch], a.total_k);
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    int lo = 0, hi = a.batch - 1;                  // the sequence of key row r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.cu_k[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int Lq = a.cu_q[lo + 1] - a.cu_q[lo], Lk = a.cu_k[lo + 1] - a.cu_k[lo];
+    if (r < a.cu_k[lo] || Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k) continue;
+    for (int h = 0; h < a.Hkv; ++h) {
+      const size_t k = ((size_t)r * a.Hkv + h) * (kHeadDim / 4) + lane;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {                   // 0: dk, 1: dv
+        const float4 x = p[which * n4 + k], y = p[(2 + which) * n4 + k];
+        uint2 o;
+        o.x = pack_bf16x2(x.x + y.x, x.y + y.y);
+        o.y = pack_bf16x2(x.z + y.z, x.w + y.w);
+        *reinterpret_cast<uint2 *>((which ? a.dv : a.dk) + 4 * k) = o;
+      }
+    }
   }
 }
 
@@ -551,7 +571,7 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
           break;
         const int key = ck + kbeg + n * KS;
         const uint32_t dk_ = sb + SQ_K + st * 16384, dv_ = sb + SQ_V + st * 16384;
-        if (n != a.test_skip_step) {   // (test hook: a skipped step is never loaded)
+        if (n != a.test_skip_dq_step) {   // (test hook: a skipped step is never loaded)
           mbar_arrive_expect_tx(bar(D_KV_FULL + st), 32768);
           tma_load_3d(dk_, &map_k, 0, g, key, bar(D_KV_FULL + st));
           tma_load_3d(dk_ + 8192, &map_k, 64, g, key, bar(D_KV_FULL + st));
@@ -706,7 +726,7 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
   }
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (tid == 0 && *abort_flag) record_timeout(a.err, *abort_flag);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -772,14 +792,11 @@ cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(relattn_bwd_dkdv_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_BWD);
+  static std::atomic<bool> attr_set[kMaxDevicesAttr];
+  {
+    cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_bwd_dkdv_tc_kernel),
+                                      (int)SMEM_BYTES_BWD, attr_set);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
   }
   // An even GQA group of at least 4 heads is split between two CTAs per key
   // tile: twice the CTAs, half the longest one (the last wave is the ragged
@@ -791,8 +808,8 @@ cudaError_t launch_bwd_dkdv_tc(const BwdArgs &a, cudaStream_t stream) {
       ak, mk, mv, mq, md, mr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || ak.kv_split == 1) return e;
-  const size_t n = (size_t)a.total_k * a.Hkv * kHeadDim / 2;   // float4 groups, both tensors
-  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8);
+  // a warp per key row, 8 rows per CTA, grid-stride beyond 8 CTAs per SM
+  const unsigned blocks = (unsigned)std::min<size_t>(((size_t)a.total_k + 7) / 8, 152 * 8);
   if (blocks > 0) relattn_bwd_dkv_reduce_kernel<<<blocks, 256, 0, stream>>>(ak);
   return cudaGetLastError();
 }
@@ -806,14 +823,11 @@ cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t stream) {
   if (!encode_rows(&mq, a.q, a.Hq, a.total_q, QM) || !encode_rows(&md, a.dout, a.Hq, a.total_q, QM) ||
       !encode_rows(&mk, a.k, a.Hkv, a.total_k, KS) || !encode_rows(&mv, a.v, a.Hkv, a.total_k, KS))
     return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(relattn_bwd_dq_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES_DQ);
+  static std::atomic<bool> attr_set[kMaxDevicesAttr];
+  {
+    cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_bwd_dq_tc_kernel),
+                                      (int)SMEM_BYTES_DQ, attr_set);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
   }
   const int q_tiles = (a.max_q + QM - 1) / QM;
   relattn_bwd_dq_tc_kernel<<<dim3(q_tiles, a.Hq, a.batch), NTHR, SMEM_BYTES_DQ, stream>>>(a, mq, md, mk, mv);

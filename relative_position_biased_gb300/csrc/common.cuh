@@ -21,6 +21,20 @@ enum DeviceError : int {
   kDevErrTimeout = 2,   // a bounded wait gave up
 };
 
+// A bounded wait at `site` gave up: set the timeout bit and, if no site is
+// recorded yet, record this one in bits 8+ (the first CTA to report wins, so
+// the word names one real wait site rather than an OR of several).
+__device__ __forceinline__ void record_timeout(int *err, int site) {
+  int old = *reinterpret_cast<volatile int *>(err);
+  for (;;) {
+    const int want = (old >> 8) ? (old | kDevErrTimeout) : (old | kDevErrTimeout | (site << 8));
+    if (want == old) return;
+    const int seen = atomicCAS(err, old, want);
+    if (seen == old) return;
+    old = seen;
+  }
+}
+
 // Everything a kernel needs, resolved on the host from relattn_params.
 struct KernelArgs {
   const __nv_bfloat16 *q, *k, *v, *r, *P;

@@ -1243,7 +1243,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (tid == 0 && *abort_flag) record_timeout(a.err, *abort_flag);
   if (warp == 0 && lane == 0 && *abort_flag) {
     // the CTA gave up: let the producer's own copies land before shared memory
     // goes away (bounded waits, not cut short by the abort)
@@ -1346,15 +1346,10 @@ cudaError_t launch_tc(const KernelArgs &a, int total_k, dim3 grid, cudaStream_t 
     cuuint32_t br[3] = {64, 1, BM};
     if (!encode(&mq, a.q, 3, dq, sq, bq) || !encode(&mr, a.r, 3, dr, sr, br)) ta.stage_tma = 0;
   }
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_kernel<DECODE, WALK>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevicesAttr];
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_fwd_tc_kernel<DECODE, WALK>),
+                                    (int)SMEM_BYTES, attr_set);
+  if (e != cudaSuccess) return e;
   relattn_fwd_tc_kernel<DECODE, WALK><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, mk, mv, mp, mq, mr);
   return cudaGetLastError();
 }

@@ -408,7 +408,7 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort_flag) atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+  if (tid == 0 && *abort_flag) record_timeout(a.err, *abort_flag);
   if (warp == 0 && lane == 0 && *abort_flag) {
     // the CTA gave up: let the producer's own copies land before shared memory
     // goes away (bounded waits, not cut short by the abort)
@@ -467,15 +467,10 @@ cudaError_t launch_prefill_tc_main(const KernelArgs &a, int total_k, cudaStream_
   if (!encode_rows(&mq, a.q, a.Hq, a.total_q)) return cudaErrorInvalidValue;
   if (!encode_rows(&mk, a.k, a.Hkv, total_k)) return cudaErrorInvalidValue;
   if (!encode_rows(&mv, a.v, a.Hkv, total_k)) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(relattn_fwd_tc_main_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  static std::atomic<bool> attr_set[kMaxDevicesAttr];
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_fwd_tc_main_kernel),
+                                    (int)SMEM_BYTES, attr_set);
+  if (e != cudaSuccess) return e;
   relattn_fwd_tc_main_kernel<<<dim3(a.q_tiles, a.Hq / 2, a.batch), NTHREADS, SMEM_BYTES, stream>>>(
       a, mq, mk, mv);
   return cudaGetLastError();

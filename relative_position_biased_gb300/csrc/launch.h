@@ -1,9 +1,53 @@
 // launch.h -- internal launchers called by the C ABI layer (api.cu).
 #pragma once
 
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace relattn {
+
+// The calling thread's current CUDA context (a CUcontext, as an opaque key),
+// or null before the runtime has made one current.  Per-device addresses the
+// library caches (device symbols) are keyed on it: after cudaDeviceReset the
+// primary context is new, the module is loaded again and the symbols may
+// move, so a cached address is looked up again when the context changes.
+inline void *current_cu_context() {
+  static const PFN_cuCtxGetCurrent_v4000 get = []() -> PFN_cuCtxGetCurrent_v4000 {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    return nullptr;
+  }();
+  CUcontext c = nullptr;
+  if (get && get(&c) != CUDA_SUCCESS) c = nullptr;
+  return reinterpret_cast<void *>(c);
+}
+
+// Raise `func`'s dynamic shared-memory limit to `bytes` once per device.
+// `done` holds one flag per device for that kernel; the first launch on a
+// device sets the attribute under a process-wide lock, so host threads that
+// launch concurrently neither race on the flag nor skip the call.
+constexpr int kMaxDevicesAttr = 64;
+inline cudaError_t set_max_smem_once(const void *func, int bytes,
+                                     std::atomic<bool> (&done)[kMaxDevicesAttr]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesAttr)
+    return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // Query rows per decode CTA for a given row count (max_seqlen_q * group).
 int decode_warps_for_rows(int rows);
@@ -49,7 +93,8 @@ struct BwdArgs {
   int rall_ok;                 // 1: Rall has been written (the band's dq loads its R windows from it)
   float *dkv_part;             // workspace [2 halves][dk, dv][Tk, Hkv, 128] fp32 (GQA groups of 4, 6, 8 ...)
   int kv_split;                // 2: two tcgen05 dk / dv CTAs per key tile, each half the group's heads
-  int test_skip_step;          // test hook: a step whose copies the tcgen05 producers never issue (-1 off)
+  int test_skip_dkdv_step;     // test hooks: a step whose copies the tcgen05 dk / dv producer
+  int test_skip_dq_step;       //   (or the tcgen05 dq producer) never issues (-1: off)
   float *dq_part;              // workspace [Tq, Hq, 128]: dq over the keys outside the bias band (fp32)
   int dq_split;                // 1: the tcgen05 dq takes the keys outside the band and writes
                                //    dq_part; the warp-MMA dq takes the band and adds dq_part

@@ -19,7 +19,7 @@
 #include <mutex>
 
 #include "../../include/relattn.h"
-#include "common.cuh"
+#include "launch.h"
 
 namespace {
 
@@ -29,18 +29,24 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[kMaxDevices];
+void *g_scratch_ctx[kMaxDevices];   // the context g_scratch_ptr[dev] was looked up in
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device with that device current.
+// with that device current: on the first call on the device, and again
+// whenever the current context differs from the one of the last lookup (a
+// cudaDeviceReset makes a new primary context, into which the module, and the
+// array with it, is loaded again, possibly at another address).
 relattn_status scratch_for_current_device(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RELATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  void *ctx = relattn::current_cu_context();
+  if (!g_scratch_ptr[dev] || !ctx || ctx != g_scratch_ctx[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return RELATTN_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = relattn::current_cu_context();
   }
   *out = g_scratch_ptr[dev];
   return RELATTN_OK;

@@ -507,7 +507,7 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
   __syncthreads();
   if (*abort_flag) {
     if (warp == kConsumerWarps && lane == 0) {
-      atomicOr(a.err, kDevErrTimeout | (*abort_flag << 8));
+      record_timeout(a.err, *abort_flag);
       // copies still in flight: those of the last kStages tiles issued
       for (int m = max(0, issued - kStages); m < issued; ++m)
         drain_wait(full(m % kStages), (m / kStages) & 1);
@@ -556,18 +556,12 @@ cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms,
   const size_t stage_bytes = (size_t)T * a.Hq * kHeadDim * 2 + 2 * (size_t)(T + kHalo) * a.Hkv * kHeadDim * 2;
   const size_t smem = kWeightOffset + 2 * kTaps * (size_t)a.Hkv * kHeadDim * 4 + kStages * stage_bytes;
   if (rows > 0 && smem <= kPrologueMaxSmem) {
-    static bool attr_set[64] = {false};   // the attribute is set once per device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(relattn_prologue_staged_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kPrologueMaxSmem);
-      if (e != cudaSuccess) return e;
-      attr_set[dev] = true;
-    }
+    static std::atomic<bool> attr_set[kMaxDevicesAttr];   // the attribute is set once per device
+    cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_prologue_staged_kernel),
+                                      (int)kPrologueMaxSmem, attr_set);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, relattn_prologue_staged_kernel, kStagedThreads, smem);
     if (e != cudaSuccess) return e;
     const long tiles = (a.total_q + T - 1) / T;

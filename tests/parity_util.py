@@ -71,3 +71,47 @@ def compare(w: W.Workload, inp, gpu, rows=None, out_tol=OUT_TOL, lse_tol=LSE_TOL
 
 def alpha_default():
     return 1.0 / math.sqrt(W.HEAD_DIM)
+
+
+def oracle_key_range_grads(w, inp, b, j0, m):
+    """Exact dk / dv of keys [j0, j0 + m) of sequence b of a prefill workload
+    (Lq = Lk, no log-scale), from the backward oracle run on just the query
+    rows that see those keys.
+
+    With a window W, rows [j0, j0 + m + W - 1) are the only ones that see the
+    keys, and they see keys from ka = j0 - W + 1 on.  The oracle takes that
+    chunk bottom-right aligned: chunk row t sits at position
+    (qb - ka) - (qb - qa) + t = (qa + t) - ka, its original position less
+    ka, and so does every key; every distance i - j, mask and logit is the
+    original one (without a log-scale, which depends on the absolute
+    position).  One virtual sequence per query head (with
+    its kv head's keys) lets the oracle's per-(sequence, kv head) tasks run
+    in parallel; the dk / dv of a kv head are the sums over its query heads.
+    Returns (dk, dv) [m, Hkv, 128] float64.
+    """
+    import oracle
+    L, W_ = w.q_lens[b], (w.window if w.window > 0 else w.q_lens[b])
+    base = sum(w.q_lens[:b])
+    qa, qb = j0, min(L, j0 + m + W_ - 1)
+    ka = max(0, j0 - W_ + 1)
+    group = w.Hq // w.Hkv
+    qs, rs, ds, ks, vs, cq, ck = [], [], [], [], [], [0], [0]
+    for h in range(w.Hq):
+        g = h // group
+        qs.append(inp["q"][base + qa:base + qb, h:h + 1])
+        rs.append(inp["r"][base + qa:base + qb, h:h + 1])
+        ds.append(inp["dout"][base + qa:base + qb, h:h + 1])
+        ks.append(inp["k"][base + ka:base + qb, g:g + 1])
+        vs.append(inp["v"][base + ka:base + qb, g:g + 1])
+        cq.append(cq[-1] + (qb - qa))
+        ck.append(ck[-1] + (qb - ka))
+    cat = torch.cat
+    _, dk, dv, _ = oracle.backward(cat(qs), cat(ks), cat(vs), cat(rs), inp["P"], cat(ds), cq, ck,
+                                   alpha=w.alpha, window=w.window)
+    nk = qb - ka
+    dk = dk.reshape(w.Hq, nk, 128)[:, j0 - ka:j0 - ka + m]
+    dv = dv.reshape(w.Hq, nk, 128)[:, j0 - ka:j0 - ka + m]
+    # sum the query heads of each kv head -> [m, Hkv, 128]
+    dk = dk.reshape(w.Hkv, group, m, 128).sum(axis=1).transpose(1, 0, 2)
+    dv = dv.reshape(w.Hkv, group, m, 128).sum(axis=1).transpose(1, 0, 2)
+    return dk, dv

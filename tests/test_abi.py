@@ -17,9 +17,21 @@ def lib():
     return rpb.load_library()
 
 
-def _declared_functions():
+_DECL = re.compile(r"^\s*(?:const\s+)?\w+\s*\*?\s*(relattn_\w+)\s*\(", re.M)
+
+
+def _header_sections():
+    """(product declarations, test-build declarations) of include/relattn.h:
+    the test hooks are the ones inside #ifdef RELATTN_TEST_HOOKS."""
     text = open(os.path.join(ROOT, "include", "relattn.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(relattn_\w+)\s*\(", text, re.M)))
+    m = re.search(r"#ifdef RELATTN_TEST_HOOKS(.*?)#endif", text, re.S)
+    test = set(_DECL.findall(m.group(1))) if m else set()
+    prod = set(_DECL.findall(text)) - test
+    return sorted(prod), sorted(test)
+
+
+def _declared_functions():
+    return _header_sections()[0]
 
 
 def test_header_declares_the_entry_points():
@@ -29,9 +41,22 @@ def test_header_declares_the_entry_points():
 
 
 def test_library_exports_every_declared_symbol(lib):
-    for name in _declared_functions():
+    prod, test = _header_sections()
+    for name in prod:
         assert hasattr(lib, name), name
-    assert set(_declared_functions()) <= set(rpb.EXPORTED)
+    assert set(prod) == set(rpb.EXPORTED)
+    assert set(test) == set(rpb.TEST_HOOKS) and test
+
+
+def test_test_hooks_live_in_the_test_build_only(lib):
+    """The product library exports no relattn_test_* entry point; the test
+    build exports every product entry point plus the hooks."""
+    prod, test = _header_sections()
+    for name in test:
+        assert not hasattr(lib, name), name
+    tlib = rpb.load_test_library()
+    for name in prod + test:
+        assert hasattr(tlib, name), name
 
 
 def test_struct_layout_matches_header(lib):

@@ -164,17 +164,70 @@ def test_inconsistent_cu_seqlens_are_reported():
     assert rpb.relattn_get_device_error() == rpb.RELATTN_OK
 
 
+def test_split_reduce_touches_only_rows_it_wrote():
+    """GQA 4:1 (dk / dv split over two CTAs per key tile, then the reduce)
+    with K / V tensors longer than cu_seqlens_k[batch]: the rows past it keep
+    their contents, as on the unsplit path, and the rows inside match the
+    oracle."""
+    import relative_position_biased_gb300 as rpb
+    w = W.custom("bwd_pad", [100, 60], [100, 60], 8, 2, 32, 64)
+    inp = W.make_inputs(w, with_dout=True)
+    d = {k: v.cuda() for k, v in inp.items()}
+    pad = torch.randn(30, 2, 128, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    kp, vp = torch.cat([d["k"], pad]), torch.cat([d["v"], pad])
+    args = (d["q"], kp, vp, d["r"], d["P"])
+    out, lse = rpb.prefill(*args, d["cu_seqlens_q"], d["cu_seqlens_k"], **_kw(w))
+    dk, dv = torch.full_like(kp, 7.0), torch.full_like(vp, 7.0)
+    rpb.backward(*args, out, lse, d["dout"], d["cu_seqlens_q"], d["cu_seqlens_k"], dk=dk, dv=dv,
+                 **_kw(w))
+    torch.cuda.synchronize()
+    assert rpb.relattn_get_device_error() == rpb.RELATTN_OK
+    assert bool((dk[160:] == 7.0).all()) and bool((dv[160:] == 7.0).all())
+    ref = run_oracle(w, inp)
+    assert_close(dk[:160].float().cpu().double().numpy(), ref[1], "dk")
+    assert_close(dv[:160].float().cpu().double().numpy(), ref[2], "dv")
+
+
+def test_split_reduce_skips_a_sequence_the_kernels_skipped():
+    """GQA 4:1; the second sequence has Lk < Lq: the kernels skip it and
+    report it, and the reduce leaves its dk / dv rows as they were."""
+    import relative_position_biased_gb300 as rpb
+    w = W.custom("bwd_badseq", [100, 60], [100, 60], 8, 2, 32, 64)
+    inp = W.make_inputs(w, with_dout=True)
+    d = {k: v.cuda() for k, v in inp.items()}
+    args = (d["q"], d["k"], d["v"], d["r"], d["P"])
+    out, lse = rpb.prefill(*args, d["cu_seqlens_q"], d["cu_seqlens_k"], **_kw(w))
+    bad_k = torch.tensor([0, 100, 140], dtype=torch.int32, device="cuda")   # Lk 40 < Lq 60
+    dk, dv = torch.full_like(d["k"], 7.0), torch.full_like(d["v"], 7.0)
+    rpb.backward(*args, out, lse, d["dout"], d["cu_seqlens_q"], bad_k, dk=dk, dv=dv, **_kw(w))
+    torch.cuda.synchronize()
+    assert rpb.relattn_get_device_error() == 6          # RELATTN_ERR_DEVICE_ARGS
+    assert bool((dk[100:] == 7.0).all()) and bool((dv[100:] == 7.0).all())
+    w0 = W.custom("bwd_badseq0", [100], [100], 8, 2, 32, 64)
+    sub = {k: inp[k][:100] for k in ("q", "k", "v", "r", "dout")}
+    ref = run_oracle(w0, dict(sub, P=inp["P"], cu_seqlens_q=[0, 100], cu_seqlens_k=[0, 100]))
+    assert_close(dk[:100].float().cpu().double().numpy(), ref[1], "dk")
+    assert_close(dv[:100].float().cpu().double().numpy(), ref[2], "dv")
+
+
 @pytest.mark.slow
 def test_full_size_swa_prefill():
-    """4 x 8192 packed, window 4096, E 1024, r_dim 64, Hq 16 / Hkv 2.
+    """4 x 8192 packed, window 4096, E 1024, r_dim 64, Hq 16 / Hkv 2: the
+    workload the bench times, with the dq split and the dk / dv split over
+    two CTAs per key tile.
 
     dq and dr of sampled rows against the oracle on that row alone (a
     one-row chunk at the end of its sequence's keys: dq_i and dr_i depend on
-    row i only); dk and dv through two exact properties of the softmax that
-    hold at any size: the dk of a sequence sum to zero per kv head, and the dv
-    sum to the sum of the group's dout.
+    row i only).  dk and dv element by element on sampled key ranges: a
+    sequence start (band tiles near the first rows), a range across the
+    4096 boundary (band and non-band tiles, the window edge), and a sequence
+    end (keys only the last rows see), each against the oracle run on the
+    query rows that see those keys.  The softmax identities (the dk of a
+    sequence sum to zero per kv head; the dv sum to the group's dout) still
+    check every key at once.
     """
     import oracle
+    from tests.parity_util import oracle_key_range_grads
     w = W.swa_prefill()
     inp = W.make_inputs(w, with_dout=True)
     dq, dk, dv, dr = run_gpu(w, inp)
@@ -188,6 +241,11 @@ def test_full_size_swa_prefill():
                                        [0, 1], [0, i + 1], alpha=w.alpha, window=w.window)
         assert_close(dq[t:t + 1], rq, f"dq row {t}")
         assert_close(dr[t:t + 1], rr, f"dr row {t}")
+    for b, j0, m in ((1, 0, 128), (2, 4096 - 64, 128), (3, 8192 - 128, 128)):
+        rk, rv = oracle_key_range_grads(w, inp, b, j0, m)
+        sl = slice(b * 8192 + j0, b * 8192 + j0 + m)
+        assert_close(dk[sl], rk, f"dk keys {b}:{j0}+{m}")
+        assert_close(dv[sl], rv, f"dv keys {b}:{j0}+{m}")
     do = inp["dout"].double().numpy()
     for b in range(4):
         sl = slice(b * 8192, (b + 1) * 8192)

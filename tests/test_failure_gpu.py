@@ -1,12 +1,16 @@
 """Failure path of the tensor-core kernels, without faulting the GPU.
 
-A test hook makes the TMA producer leave one key tile unloaded, so the MMA
-issuer's wait on it (bounded by its clock limit, about a second) runs out.
-The CTA must give up cleanly: drain its own copies and MMAs, free its tensor
+A test hook makes a TMA producer leave one tile or step unloaded, so the
+waits behind it (bounded by a clock limit, about a second) run out.  The
+CTA must give up cleanly: drain its own copies and MMAs, free its tensor
 memory and exit; the host then reads RELATTN_ERR_TIMEOUT from the device
-error word, and the context stays usable for the next, normal call.
+error word, with the first wait site that gave up in bits 8+, and the
+context stays usable for the next, normal call.
+
+The hooks exist only in the test build of the library (librelattn_test.so);
+every test here runs its calls on that build, and the product library is
+checked to have none of them.
 """
-import numpy as np
 import pytest
 import torch
 
@@ -16,6 +20,19 @@ from relative_position_biased_gb300 import workloads as W
 from tests.parity_util import compare, run_gpu
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _test_build():
+    rpb.build()
+    with rpb.test_library():
+        yield
+
+
+def test_product_library_has_no_hooks():
+    prod = rpb.load_library(rpb.LIB_PATH)
+    for name in rpb.TEST_HOOKS:
+        assert not hasattr(prod, name), name
 
 
 def test_bounded_wait_gives_up_and_context_recovers(oracle_mod):
@@ -77,25 +94,36 @@ def test_prologue_skip_hook_rejects_bad_tile():
     assert rpb.relattn_test_prologue_skip_tile(-1) == rpb.RELATTN_OK
 
 
-def test_backward_skip_hook_times_out_and_recovers():
-    """The tcgen05 backward kernels' producers leave step 0 without copies:
-    the waits behind it run out, every CTA drains and frees its tensor memory,
-    the status is RELATTN_ERR_TIMEOUT, and the next call on the same context
-    is correct. The shape keeps each kernel to one wave of CTAs."""
+# wait sites of the two tcgen05 backward kernels (the ids their bounded waits
+# record): the dk / dv kernel 1-10, the dq kernel outside the band 11-16
+BWD_SITES = {0: range(1, 11), 1: range(11, 17)}
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_backward_skip_hook_times_out_and_recovers(kernel):
+    """One tcgen05 backward kernel's producer (kernel 0: dk / dv, 1: dq)
+    leaves its step 0 without copies: the waits behind it run out, every CTA
+    of that kernel drains and frees its tensor memory, the status is
+    RELATTN_ERR_TIMEOUT with a wait site of that kernel (the other kernel
+    runs normally), and the next call on the same context is correct.  The
+    shape keeps each kernel to one wave of CTAs."""
     from tests.test_backward_gpu import check as check_bwd, run_gpu as bwd_gpu
     w = W.custom("bwd_skip", [300], [300], 4, 2, 32, 64)
     inp = W.make_inputs(w, with_dout=True)
-    assert rpb.relattn_test_backward_skip_step(0) == rpb.RELATTN_OK
+    assert rpb.relattn_test_backward_skip_step(kernel, 0) == rpb.RELATTN_OK
     try:
         with pytest.raises(AssertionError, match="RELATTN_ERR_TIMEOUT"):
             bwd_gpu(w, inp)               # synchronises, then reads the status
         word = rpb.relattn_last_device_error_word()
     finally:
-        rpb.relattn_test_backward_skip_step(-1)
-    assert word & 2 and (word >> 8) > 0
+        rpb.relattn_test_backward_skip_step(kernel, -1)
+    assert word & 2 and (word >> 8) in BWD_SITES[kernel], hex(word)
     check_bwd(w)                          # hook off: correct on the same context
 
 
-def test_backward_skip_hook_rejects_bad_step():
-    assert rpb.relattn_test_backward_skip_step(-2) != rpb.RELATTN_OK
-    assert rpb.relattn_test_backward_skip_step(-1) == rpb.RELATTN_OK
+def test_backward_skip_hook_rejects_bad_arguments():
+    assert rpb.relattn_test_backward_skip_step(0, -2) != rpb.RELATTN_OK
+    assert rpb.relattn_test_backward_skip_step(2, 0) != rpb.RELATTN_OK
+    assert rpb.relattn_test_backward_skip_step(-1, 0) != rpb.RELATTN_OK
+    assert rpb.relattn_test_backward_skip_step(0, -1) == rpb.RELATTN_OK
+    assert rpb.relattn_test_backward_skip_step(1, -1) == rpb.RELATTN_OK

@@ -12,6 +12,8 @@ import pytest
 import torch
 
 import oracle
+from relative_position_biased_gb300 import workloads as W
+from tests import parity_util as PU
 
 ALPHA = 0.37
 
@@ -141,3 +143,20 @@ def test_softmax_invariants(kw):
         # the weights of each row sum to one
         want = x["dout"][a0:a1].reshape(a1 - a0, 2, 2, -1).sum(axis=(0, 2))
         np.testing.assert_allclose(dv[k0:k1].sum(axis=0), want, atol=1e-12)
+
+
+def test_key_range_oracle_matches_the_whole_sequence(oracle_mod):
+    """The chunked oracle of the full-size test against the oracle run on the
+    whole packed batch, on a small windowed workload with the same shape of
+    problem (several sequences, GQA, a band): the dk / dv of every sampled
+    key range must agree to fp64 rounding."""
+    w = W.custom("keyrange", [300, 260], [300, 260], 4, 2, 16, 48, window=70)
+    inp = W.make_inputs(w, with_dout=True)
+    _, dk, dv, _ = oracle_mod.backward(inp["q"], inp["k"], inp["v"], inp["r"], inp["P"],
+                                       inp["dout"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                                       alpha=w.alpha, window=w.window)
+    for b, j0, m in ((0, 0, 20), (0, 100, 37), (1, 230, 30), (1, 0, 260)):
+        rk, rv = PU.oracle_key_range_grads(w, inp, b, j0, m)
+        base = sum(w.q_lens[:b])
+        assert np.allclose(rk, dk[base + j0:base + j0 + m], rtol=1e-12, atol=1e-12)
+        assert np.allclose(rv, dv[base + j0:base + j0 + m], rtol=1e-12, atol=1e-12)

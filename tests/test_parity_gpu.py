@@ -89,13 +89,18 @@ def test_chunked_prefill_bottom_right():
 
 @pytest.fixture
 def band_ctas():
+    """The CTA cap lives in the test build of the library: the test's calls
+    run on it while the fixture is active."""
     import relative_position_biased_gb300 as rpb
 
     def set_cap(n):
         assert rpb.relattn_test_band_ctas(n) == 0
 
-    yield set_cap
-    rpb.relattn_test_band_ctas(0)
+    with rpb.test_library():
+        try:
+            yield set_cap
+        finally:
+            rpb.relattn_test_band_ctas(0)
 
 
 @pytest.mark.parametrize("ctas", [1, 3])

@@ -91,7 +91,7 @@ typedef struct relattn_params {
   float log_scale_base;        /* <= 0: off; else > 1, s(i)=max(1,ln(i+1)/ln(base))  */
   void *out;                   /* bf16 [total_q, num_heads_q, 128]                   */
   float *lse;                  /* fp32 [num_heads_q, total_q], natural log           */
-  void *workspace;             /* decode split partials (device), may be NULL        */
+  void *workspace;             /* decode scratch (device), may be NULL when none     */
   size_t workspace_bytes;
   int32_t num_splits;          /* decode: 0 = choose automatically                   */
 } relattn_params;
@@ -113,7 +113,14 @@ relattn_status relattn_prefill(const relattn_params *params, void *stream);
  */
 relattn_status relattn_decode(const relattn_params *params, void *stream);
 
-/* Workspace bytes relattn_decode needs for these params (0 when unsplit). */
+/*
+ * Workspace bytes relattn_decode needs for these params: the split partials
+ * (fp32 out and lse of every split) when the keys are cut into several
+ * splits, and, when max_seqlen_q x (num_heads_q / num_heads_kv) <= 16 and a
+ * relative bias is on, the bias of every decode row at every distance below
+ * rel_extent (fp32, total_q x num_heads_q x rel_extent).  0 when neither
+ * applies.  The workspace must be 16-byte aligned; its contents are scratch.
+ */
 relattn_status relattn_decode_workspace_size(const relattn_params *params, size_t *bytes);
 
 /* The split count relattn_decode will use for these params. */

@@ -132,10 +132,19 @@ relattn_status make_args(const relattn_params *p, KernelArgs *a) {
   return RELATTN_OK;
 }
 
+// Decode kernels: few rows per (sequence, kv head) -- the keys along the
+// MMA's M (decode_tc.cu) --, else 128-row blocks on the prefill kernel
+// (fwd_tc.cu), else the warp-MMA kernel (fwd_mma.cu) where the tcgen05
+// kernels' alignment or shape conditions fail.
+enum class DecodeKind { kMma, kRows, kKeys };
+
 struct DecodePlan {
-  bool tc;               // tcgen05 kernel (else the warp-MMA kernel)
+  DecodeKind kind;
   int warps, row_blocks, splits, chunk;
-  size_t ws_bytes, lse_offset;
+  // workspace: split partials (o, then lse at lse_offset) when splits > 1,
+  // then (few-row kernel with a bias) R of the decode rows at rel_offset
+  size_t ws_bytes, lse_offset, rel_offset;
+  bool tc() const { return kind != DecodeKind::kMma; }
 };
 
 // kv_rows: rows of the K / V tensors the kernels address (total_k, or the
@@ -148,11 +157,16 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan, long kv_ro
   const int rows = p->max_seqlen_q * group;
   KernelArgs probe;
   if ((st = make_args(p, &probe)) != RELATTN_OK) return st;
-  plan->tc = tc_supported(probe, kv_rows >= 0 ? (int)kv_rows : p->total_k);
+  const int kvr = kv_rows >= 0 ? (int)kv_rows : p->total_k;
+  plan->kind = decode_few_rows_supported(probe, kvr) ? DecodeKind::kKeys
+               : tc_supported(probe, kvr)            ? DecodeKind::kRows
+                                                     : DecodeKind::kMma;
   plan->warps = decode_warps_for_rows(rows < 128 ? rows : 128);
-  const int m = plan->tc ? kTcDecodeRows : plan->warps * 16;
+  const int m = plan->kind == DecodeKind::kKeys   ? kFewRows
+                : plan->kind == DecodeKind::kRows ? kTcDecodeRows
+                                                  : plan->warps * 16;
   plan->row_blocks = (rows + m - 1) / m;
-  const int tile = plan->tc ? kTcKeyTile : kDecodeKeyTile;
+  const int tile = plan->tc() ? kTcKeyTile : kDecodeKeyTile;
   // keys any CTA of one (sequence, kv head) may visit, from an aligned start
   long max_vis = p->max_seqlen_k;
   if (p->window > 0) {
@@ -183,15 +197,17 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan, long kv_ro
   if (splits > 65535) return RELATTN_ERR_UNSUPPORTED;
   plan->splits = (int)splits;
   plan->chunk = (int)chunk;
+  size_t end = 0;
+  plan->lse_offset = 0;
   if (plan->splits > 1) {
     const size_t rows_all = (size_t)p->total_q * p->num_heads_q;
     const size_t o_bytes = (size_t)plan->splits * rows_all * kHeadDim * sizeof(float);
     plan->lse_offset = (o_bytes + 255) / 256 * 256;
-    plan->ws_bytes = plan->lse_offset + (size_t)plan->splits * rows_all * sizeof(float);
-  } else {
-    plan->lse_offset = 0;
-    plan->ws_bytes = 0;
+    end = plan->lse_offset + (size_t)plan->splits * rows_all * sizeof(float);
   }
+  plan->rel_offset = (end + 255) / 256 * 256;
+  const size_t rel = plan->kind == DecodeKind::kKeys ? decode_rel_bytes(probe) : 0;
+  plan->ws_bytes = rel > 0 ? plan->rel_offset + rel : end;
   return RELATTN_OK;
 }
 
@@ -340,6 +356,38 @@ relattn_status relattn_decode_num_splits(const relattn_params *p, int32_t *num_s
   return RELATTN_OK;
 }
 
+// the split kernel, then the combine when there are several splits; kv_rows:
+// rows the K / V tensors hold
+relattn_status run_decode(const relattn_params *p, const DecodePlan &plan, KernelArgs &a, long kv_rows,
+                          cudaStream_t s) {
+  a.num_splits = plan.splits;
+  a.split_chunk = plan.chunk;
+  a.row_blocks = plan.row_blocks;
+  if (plan.ws_bytes > 0) {
+    if (!p->workspace || p->workspace_bytes < plan.ws_bytes || !aligned16(p->workspace))
+      return RELATTN_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(p->workspace);
+    if (plan.splits > 1) {
+      a.o_part = reinterpret_cast<float *>(ws);
+      a.lse_part = reinterpret_cast<float *>(ws + plan.lse_offset);
+    }
+    if (plan.kind == DecodeKind::kKeys && decode_rel_bytes(a) > 0)
+      a.rdec = reinterpret_cast<const float *>(ws + plan.rel_offset);
+  }
+  cudaError_t e;
+  switch (plan.kind) {
+    case DecodeKind::kKeys: e = launch_decode_few_rows(a, (int)kv_rows, s); break;
+    case DecodeKind::kRows: e = launch_decode_tc(a, (int)kv_rows, s); break;
+    default: e = launch_decode_mma(a, plan.warps, s); break;
+  }
+  relattn_status st = cuda_status(e);
+  if (st != RELATTN_OK) return st;
+  if (plan.splits > 1)
+    st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
+                                    p->num_heads_q, a.out, a.lse, s));
+  return st;
+}
+
 relattn_status relattn_decode(const relattn_params *p, void *stream) {
   relattn_status st = validate(p, true);
   if (st != RELATTN_OK) return st;
@@ -348,23 +396,7 @@ relattn_status relattn_decode(const relattn_params *p, void *stream) {
   if ((st = plan_decode(p, &plan)) != RELATTN_OK) return st;
   KernelArgs a;
   if ((st = make_args(p, &a)) != RELATTN_OK) return st;
-  a.num_splits = plan.splits;
-  a.split_chunk = plan.chunk;
-  a.row_blocks = plan.row_blocks;
-  if (plan.splits > 1) {
-    if (!p->workspace || p->workspace_bytes < plan.ws_bytes || !aligned16(p->workspace))
-      return RELATTN_ERR_WORKSPACE;
-    a.o_part = static_cast<float *>(p->workspace);
-    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + plan.lse_offset);
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = plan.tc ? cuda_status(launch_decode_tc(a, p->total_k, s))
-               : cuda_status(launch_decode_mma(a, plan.warps, s));
-  if (st != RELATTN_OK) return st;
-  if (plan.splits > 1)
-    st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
-                                    p->num_heads_q, a.out, a.lse, s));
-  return st;
+  return run_decode(p, plan, a, p->total_k, static_cast<cudaStream_t>(stream));
 }
 
 relattn_status relattn_decode_paged(const relattn_params *p, const relattn_paged_kv *kv,
@@ -382,29 +414,14 @@ relattn_status relattn_decode_paged(const relattn_params *p, const relattn_paged
   const long pool_rows = (long)kv->num_pages * kv->page_size;
   DecodePlan plan;
   if ((st = plan_decode(p, &plan, pool_rows)) != RELATTN_OK) return st;
-  if (!plan.tc) return RELATTN_ERR_UNSUPPORTED;   // paged K / V: the tcgen05 kernel only
+  if (!plan.tc()) return RELATTN_ERR_UNSUPPORTED;   // paged K / V: the tcgen05 kernels only
   KernelArgs a;
   if ((st = make_args(p, &a)) != RELATTN_OK) return st;
-  a.num_splits = plan.splits;
-  a.split_chunk = plan.chunk;
-  a.row_blocks = plan.row_blocks;
   a.block_table = kv->block_table;
   a.page_size = kv->page_size;
   a.max_pages = kv->max_pages_per_seq;
   a.num_pages = kv->num_pages;
-  if (plan.splits > 1) {
-    if (!p->workspace || p->workspace_bytes < plan.ws_bytes || !aligned16(p->workspace))
-      return RELATTN_ERR_WORKSPACE;
-    a.o_part = static_cast<float *>(p->workspace);
-    a.lse_part = reinterpret_cast<float *>(static_cast<char *>(p->workspace) + plan.lse_offset);
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = cuda_status(launch_decode_tc(a, (int)pool_rows, s));
-  if (st != RELATTN_OK) return st;
-  if (plan.splits > 1)
-    st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
-                                    p->num_heads_q, a.out, a.lse, s));
-  return st;
+  return run_decode(p, plan, a, pool_rows, static_cast<cudaStream_t>(stream));
 }
 
 relattn_status relattn_combine(const float *o_part, const float *lse_part, int32_t num_splits,

@@ -61,6 +61,9 @@ struct KernelArgs {
   // block_table == nullptr: contiguous rows cu_seqlens_k[b] + p
   const int32_t *block_table;
   int page_size, max_pages, num_pages;
+  // few-row decode (decode_tc.cu): R = r . P of every decode row and
+  // distance < E, fp32 [total_q * Hq][E] in the workspace (null without a bias)
+  const float *rdec;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -1,0 +1,770 @@
+// decode_tc.cu -- split-KV decode of relative attention for items of few query
+// rows (at most 16: one token of a GQA group of up to 16 heads, or a couple of
+// tokens of a smaller group), on 5th-generation tensor cores with the keys
+// along the MMA's M dimension.
+//
+// Same computation as the definition on the page "SGLang and Miles Add Day-0
+// Support for Inkling", section "Attention with Relative Positional
+// Embedding": x(i,j) = s(i) (alpha q_i.k_j + [0 <= i-j < E] r_i . P[:, i-j]),
+// softmax over the visible keys, PV; the keys of a sequence are cut into
+// splits whose normalised partials the LSE combine merges (page "vLLM Day-0
+// support for TML Inkling", paragraph on FA4 with sheared bias, num_splits).
+//
+// A decode item is (split, sequence, kv head): its rows are the (token,
+// head-in-group) pairs of one kv head -- 8 rows for one token of a GQA-8
+// group -- and it streams the split's keys in 128-key tiles.  With so few rows
+// the score tile is computed transposed, S^T = K Q^T: the tile's 128 keys
+// along M (TMEM lanes), the rows along N (16 columns), so the tensor core and
+// the softmax only touch real rows (the rows-along-M decode of fwd_tc.cu
+// spends 128 lanes on them).  Each softmax thread owns one key: it scales its
+// 16 scores, adds the relative bias of band tiles and masks edge tiles; the
+// per-row maximum over the tile's keys is a transposed warp reduction (lane l
+// ends with row l % 16) plus a four-warp exchange; lane l decides row l's
+// running max, which the lanes receive by shuffles; then p = 2^(x - m).  P
+// goes to shared memory as the A operand of O = P V (M = 128 with only the
+// first 16 rows real, N = 128 dims; O in TMEM, lane = row).  Each key-thread
+// keeps its share of every row's sum; the shares are reduced once per item.
+//
+// Relative bias: R = r . P for every decode row and distance below E is
+// computed beforehand (relattn_decode_rel_kernel, fp32, in the caller's
+// workspace: a few MB at most); a band tile reads R[row][p_row - j] per (key,
+// row), all sixteen loads issued before any is used.  No sheared tensor, no
+// TMEM ring, so any r_dim <= 64 and any E work.
+//
+// Warps (8; one CTA per SM walking items in a longest-first order):
+//   warp 0      TMA producer (one thread): the item's q rows (a box of group
+//               heads x tokens), then K and V tiles (3-stage rings)
+//   warp 1      TMEM allocator, MMA issuer (one thread): S^T(t) into one of
+//               two TMEM buffers, then PV(t - 1)
+//   warps 2-3   idle
+//   warps 4-7   softmax: thread = key of the tile (TMEM lane); warp 4's
+//               lanes 0-15 also own O's rows for the rescale and the epilogue
+//
+// Tensor memory: S^T buffers [0,16) and [32,48), O [128,256).  Shared memory:
+// P (16 rows x 128 keys, 4 KB; the PV MMA reads 128 rows from each 2 KB half,
+// the 112 past the real ones being whatever follows in shared memory: they
+// only feed O's padding rows), q rows (4 KB), K and V rings (3 x 32 KB each),
+// per-row constants and exchange buffers.
+//
+// Every wait is bounded; a timeout raises the CTA's abort flag and records the
+// wait site in the device error word; the CTA drains its copies and MMAs,
+// frees its tensor memory and exits.
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace relattn {
+namespace {
+
+using namespace tc;
+
+constexpr int KT = 128;                    // keys per tile (TMEM lanes of S^T)
+constexpr int NR = kFewRows;               // rows per item at most (columns of S^T)
+static_assert(NR == 16, "one 16-column chunk of S^T");
+constexpr int NSTAGE = 3;                  // K and V ring stages
+constexpr int NTHR = 256;
+constexpr float kRescale = 8.f;            // log2 units
+
+constexpr uint32_t TM_S = 0, TM_O = 128;   // S^T buffer b at 32 b; O
+constexpr uint32_t TMEM_COLS = 256;
+
+constexpr uint32_t BOX = 16384;            // [64 dims x 128 rows] bf16, 128-byte rows, 128B swizzle
+constexpr uint32_t TILE = 2 * BOX;
+constexpr uint32_t HALF16 = NR * 128;      // [64 dims (or keys) x 16 rows]: 2 KB
+constexpr uint32_t SM_P = 0;                          // P: two 2 KB halves (keys 0-63, 64-127)
+constexpr uint32_t SM_Q = SM_P + 2 * HALF16;          // q rows: two 2 KB halves (dims 0-63, 64-127)
+constexpr uint32_t SM_K = SM_Q + 2 * HALF16;          // 1024-aligned
+constexpr uint32_t SM_V = SM_K + NSTAGE * TILE;
+constexpr uint32_t SM_ROWC = SM_V + NSTAGE * TILE;    // float4 [NR]: scale, bias scale, position, R row
+constexpr uint32_t SM_RSC = SM_ROWC + NR * 16;        // float [NR]: the scales, packed
+constexpr uint32_t SM_MREF = SM_RSC + NR * 4;         // float [2][NR]: running max by tile parity
+constexpr uint32_t SM_XMAX = SM_MREF + 2 * NR * 4;    // float [2][NR][4]: tile max per warp
+constexpr uint32_t SM_AUX = SM_XMAX + 2 * NR * 16;    // float [NR][4]: row sums per warp
+// work order (batch <= kOrd): per sequence its full / partial split counts,
+// their prefix sums, the partial splits by size, and the count of partials
+constexpr int kOrd = 64;
+constexpr int ORD_NF = 0, ORD_REM = kOrd, ORD_PF = 2 * kOrd, ORD_PZ = 3 * kOrd + 1,
+              ORD_PTAB = 4 * kOrd + 2, ORD_NP = 5 * kOrd + 2, ORD_INTS = 5 * kOrd + 4;
+constexpr uint32_t SM_ORD = SM_AUX + NR * 16;
+enum {
+  B_Q_FULL = 0, B_Q_EMPTY, B_K_FULL, B_K_EMPTY = B_K_FULL + NSTAGE, B_V_FULL = B_K_EMPTY + NSTAGE,
+  B_V_EMPTY = B_V_FULL + NSTAGE, B_S_FULL = B_V_EMPTY + NSTAGE, B_S_FREE = B_S_FULL + 2,
+  B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 1, B_XCH = B_PV_DONE + 1, B_DRAIN = B_XCH + 1,
+  B_COUNT = B_DRAIN + 1
+};
+constexpr uint32_t SM_BAR = SM_ORD + ORD_INTS * 4;
+constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
+constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
+constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
+constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;      // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// the PV MMA reads 128 rows of 128 bytes from each P half's start
+static_assert(SM_P + HALF16 + BOX <= SM_TOTAL, "P operand window inside shared memory");
+
+struct DecArgs {
+  KernelArgs a;
+  int has_bias;
+  int q_bytes;       // bytes of the item's q box pair
+  int n_items;
+};
+
+// Reduction over the warp's 32 lanes of each of the 16 per-lane values, left
+// transposed: lane l gets the result for value l % 16.  Halving stages over
+// the lane bits that select the value (a lane keeps half of its values and
+// trades the other half with its partner): 16 shuffles, independent within a
+// stage, instead of 16 full-warp reductions in a chain.
+template <bool MAX>
+__device__ __forceinline__ float transpose_reduce(const float (&v)[NR], int lane) {
+  float a[NR];
+#pragma unroll
+  for (int i = 0; i < NR; ++i) a[i] = v[i];
+#pragma unroll
+  for (int w = NR / 2; w >= 1; w >>= 1) {
+    const bool hi = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const float send = hi ? a[k] : a[k + w];
+      const float keep = hi ? a[k + w] : a[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      a[k] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  const float o = __shfl_xor_sync(0xffffffffu, a[0], 16);
+  return MAX ? fmaxf(a[0], o) : a[0] + o;
+}
+
+struct Item {
+  int b, g, sp, cq, ck, nrows, p0, p_last, kbeg, ntiles;
+};
+
+__global__ void __launch_bounds__(NTHR, 1)
+relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
+                         const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v) {
+  const KernelArgs &a = da.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const uint32_t sb = smem_addr(smem);
+  auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ------------------------------------------------------------ work items
+  // An item is a (sequence, split) pair times Hkv kv heads.  With at most
+  // kOrd sequences the pairs are ordered full splits first, then the partial
+  // last splits by size, then the empty ones, and slot idx of the walk maps to
+  // a position in that order by rounds of gridDim.x slots, every other full
+  // round reversed (a snake): the longest items start first and the rounds
+  // even out.  Every role derives the same order from the same tables.
+  // Otherwise the plain order: pair = split * batch + sequence.
+  Item I{};
+  int *ord = reinterpret_cast<int *>(smem + SM_ORD);
+  const bool sorted = a.batch <= kOrd;
+  auto load_item = [&](int idx) -> int {   // 1 work, 0 nothing, -1 inconsistent lengths
+    int q, u;
+    if (sorted) {
+      const int Gd = gridDim.x, r = idx / Gd, c = idx - r * Gd;
+      const int pos = ((r & 1) && (r + 1) * Gd <= da.n_items) ? r * Gd + (Gd - 1 - c) : idx;
+      q = pos / a.Hkv;
+      u = pos - q * a.Hkv;
+      const int F = ord[ORD_PF + a.batch], NP = ord[ORD_NP];
+      if (q < F || q >= F + NP) {
+        const int base = q < F ? ORD_PF : ORD_PZ, qq = q < F ? q : q - F - NP;
+        int b = 0;                                       // last b with prefix[b] <= qq
+        for (int i = 1; i < a.batch; ++i) b = ord[base + i] <= qq ? i : b;
+        I.b = b;
+        I.sp = q < F ? qq - ord[ORD_PF + b]
+                     : ord[ORD_NF + b] + (ord[ORD_REM + b] > 0 ? 1 : 0) + (qq - ord[ORD_PZ + b]);
+      } else {
+        I.b = ord[ORD_PTAB + (q - F)];
+        I.sp = ord[ORD_NF + I.b];
+      }
+    } else {
+      q = idx / a.Hkv;
+      u = idx - q * a.Hkv;
+      I.b = q % a.batch;
+      I.sp = q / a.batch;
+    }
+    I.g = u;
+    I.cq = a.cu_q[I.b];
+    I.ck = a.cu_k[I.b];
+    const int Lq = a.cu_q[I.b + 1] - I.cq, Lk = a.cu_k[I.b + 1] - I.ck;
+    // (rows past total_q would index outputs and R out of bounds)
+    if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k || I.cq < 0 || I.cq + Lq > a.total_q) return -1;
+    if (Lq == 0) return 0;
+    I.nrows = Lq * a.group;
+    I.p0 = Lk - Lq;
+    I.p_last = I.p0 + Lq - 1;
+    const int j_lo = a.window > 0 ? max(0, I.p0 - a.window + 1) : 0;
+    const int kbase = j_lo & ~(KT - 1);
+    I.kbeg = kbase + I.sp * a.split_chunk;
+    const int kend = min(I.p_last + 1, I.kbeg + a.split_chunk);
+    I.ntiles = kend > I.kbeg ? (kend - I.kbeg + KT - 1) / KT : 0;
+    return 1;
+  };
+  const int n_items = da.n_items;
+
+  // ------------------------------------------------------------ set-up
+  // q and P start as zeros: rows past an item's real ones then score 0
+  // instead of whatever the memory held
+  for (int i = tid; i < (int)(SM_K - SM_P) / 16; i += NTHR)
+    *reinterpret_cast<uint4 *>(smem + SM_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_Q_EMPTY), 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(bar(B_K_FULL + i), 1);
+      mbar_init(bar(B_K_EMPTY + i), 1);
+      mbar_init(bar(B_V_FULL + i), 1);
+      mbar_init(bar(B_V_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_S_FULL + i), 1);
+      mbar_init(bar(B_S_FREE + i), 128);
+    }
+    mbar_init(bar(B_P_FULL), 128);
+    mbar_init(bar(B_PV_DONE), 1);
+    mbar_init(bar(B_XCH), 128);
+    mbar_init(bar(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + SM_TMEM_SLOT, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&map_q);
+    prefetch_tmap(&map_k);
+    prefetch_tmap(&map_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (sorted) {
+    // the work order: each sequence's keys from the aligned start of its
+    // window, cut into splits of split_chunk keys
+    const int b = tid;
+    if (b < a.batch) {
+      const int cq = a.cu_q[b], ck = a.cu_k[b];
+      const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
+      long vis = 0;
+      if (Lq > 0 && Lk >= Lq) {
+        const int p0 = Lk - Lq, p_last = p0 + Lq - 1;
+        const int j_lo = a.window > 0 ? max(0, p0 - a.window + 1) : 0;
+        vis = (long)p_last + 1 - (j_lo & ~(KT - 1));
+      }
+      const long nf = min((long)a.num_splits, vis / a.split_chunk);
+      ord[ORD_NF + b] = (int)nf;
+      ord[ORD_REM + b] = nf < a.num_splits ? (int)(vis - nf * a.split_chunk) : 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int f = 0, z = 0, np = 0;
+      for (int i = 0; i < a.batch; ++i) {
+        ord[ORD_PF + i] = f;
+        ord[ORD_PZ + i] = z;
+        const int pi = ord[ORD_REM + i] > 0 ? 1 : 0;
+        f += ord[ORD_NF + i];
+        z += a.num_splits - ord[ORD_NF + i] - pi;
+        np += pi;
+      }
+      ord[ORD_PF + a.batch] = f;
+      ord[ORD_PZ + a.batch] = z;
+      ord[ORD_NP] = np;
+    }
+    if (b < a.batch && ord[ORD_REM + b] > 0) {   // rank among the partial splits: larger first
+      const int rb = ord[ORD_REM + b];
+      int rank = 0;
+      for (int i = 0; i < a.batch; ++i) {
+        const int ri = ord[ORD_REM + i];
+        rank += ri > rb || (ri == rb && i < b);
+      }
+      ord[ORD_PTAB + rank] = b;
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
+  // the producer's copies, drained if the CTA gives up
+  int issued_q = 0, issued_k = 0, issued_v = 0;
+
+  if (warp == 0) {
+    // ====================================================== TMA producer
+    if (lane == 0) {
+      int T = 0, n_it = 0;
+      bool run = true;
+      for (int idx = blockIdx.x; idx < n_items && run; idx += gridDim.x) {
+        const int li = load_item(idx);
+        if (li < 0) atomicOr(a.err, kDevErrSeqlens);
+        if (li <= 0 || I.ntiles == 0) continue;
+        // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves of 64 dims
+        if (n_it > 0 && !(run = mbar_wait(bar(B_Q_EMPTY), (n_it - 1) & 1, abort_flag, 1))) break;
+        mbar_arrive_expect_tx(bar(B_Q_FULL), (uint32_t)da.q_bytes);
+        tma_load_3d(sb + SM_Q, &map_q, 0, I.g * a.group, I.cq, bar(B_Q_FULL));
+        tma_load_3d(sb + SM_Q + HALF16, &map_q, 64, I.g * a.group, I.cq, bar(B_Q_FULL));
+        issued_q = n_it + 1;
+        // paged K / V: the pool row of a 128-aligned tile inside one page
+        auto tile_row = [&](int t) -> int {
+          const int p = I.kbeg + KT * t;
+          if (a.block_table == nullptr) return I.ck + p;
+          const int pg = a.block_table[(size_t)I.b * a.max_pages + p / a.page_size];
+          if (pg < 0 || pg >= a.num_pages) {
+            atomicOr(a.err, kDevErrSeqlens);
+            return -KT;   // reads zeros
+          }
+          return pg * a.page_size + p % a.page_size;
+        };
+        for (int t = 0; t < I.ntiles && run; ++t) {
+          const int G = T + t, st = G % NSTAGE, use = G / NSTAGE;
+          const int row = tile_row(t);
+          if (G >= NSTAGE && !(run = mbar_wait(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
+          if (G != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
+            mbar_arrive_expect_tx(bar(B_K_FULL + st), TILE);
+            tma_load_3d(sb + SM_K + st * TILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
+            tma_load_3d(sb + SM_K + st * TILE + BOX, &map_k, 64, I.g, row, bar(B_K_FULL + st));
+          }
+          issued_k = G + 1;
+          if (G >= NSTAGE && !(run = mbar_wait(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
+          mbar_arrive_expect_tx(bar(B_V_FULL + st), TILE);
+          tma_load_3d(sb + SM_V + st * TILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
+          tma_load_3d(sb + SM_V + st * TILE + BOX, &map_v, 64, I.g, row, bar(B_V_FULL + st));
+          issued_v = G + 1;
+        }
+        T += I.ntiles;
+        ++n_it;
+        if (*abort_flag) run = false;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ====================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(KT, NR, 0, 0);    // S^T: K (smem) x Q (smem), both K-major
+      const uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);  // O: P (smem, K-major) x V (smem, MN-major)
+      // descriptor bases; k-step k of a 128-wide K dimension: +2 per 32 bytes
+      // inside a 128-byte row, the second 64-wide half at +16 KB in a K tile
+      // and at +2 KB in the 16-row q and P operands
+      const uint64_t qd = smem_desc_sw128(sb + SM_Q, 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(sb + SM_K, 16, 1024);
+      const uint64_t pd = smem_desc_sw128(sb + SM_P, 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(sb + SM_V, BOX, 1024);
+      auto koff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (BOX >> 4) + 2 * (k - 4)); };
+      auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
+      int T = 0, n_it = 0;
+      bool ok = true;
+      auto issue_pv = [&](int G, bool first) -> bool {
+        const int st = G % NSTAGE;
+        if (!mbar_wait(bar(B_P_FULL), G & 1, abort_flag, 4)) return false;
+        if (!mbar_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, abort_flag, 5)) return false;
+        tc_fence_after();
+        const uint64_t vd = vd0 + (uint64_t)((st * TILE) >> 4);
+        const uint32_t o = tmem + TM_O;
+        if (first) mma_ss_c<0>(o, pd + hoff(0), vd + 0, id_o);
+        else mma_ss_c<1>(o, pd + hoff(0), vd + 0, id_o);
+#pragma unroll
+        for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, pd + hoff(k), vd + 128 * k, id_o);
+        mma_commit(bar(B_PV_DONE));
+        mma_commit(bar(B_V_EMPTY + st));
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        if (load_item(idx) <= 0 || I.ntiles == 0) continue;
+        if (!(ok = mbar_wait(bar(B_Q_FULL), n_it & 1, abort_flag, 6))) break;
+        for (int t = 0; t < I.ntiles && ok; ++t) {
+          const int G = T + t, sb2 = G & 1, st = G % NSTAGE;
+          if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + sb2), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
+          if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / NSTAGE) & 1, abort_flag, 8))) break;
+          tc_fence_after();
+          const uint64_t kd = kd0 + (uint64_t)((st * TILE) >> 4);
+          const uint32_t d = tmem + TM_S + 32u * (uint32_t)sb2;
+          mma_ss_c<0>(d, kd + koff(0), qd + hoff(0), id_s);
+#pragma unroll
+          for (int k = 1; k < 8; ++k) mma_ss_c<1>(d, kd + koff(k), qd + hoff(k), id_s);
+          mma_commit(bar(B_S_FULL + sb2));
+          mma_commit(bar(B_K_EMPTY + st));
+          if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY));   // the item's q rows are read
+          if (t > 0) ok = issue_pv(G - 1, t == 1);
+        }
+        if (ok) ok = issue_pv(T + I.ntiles - 1, I.ntiles == 1);
+        T += I.ntiles;
+        ++n_it;
+      }
+      // drain: every MMA issued above has finished before TMEM is released
+      mma_commit(bar(B_DRAIN));
+      volatile int keep_waiting = 0;
+      mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 9, 400000000ll);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ======================================================== softmax
+    const int wq = warp & 3;                     // lane quarter: keys 32 wq .. 32 wq + 31
+    const int key = 32 * wq + lane;              // this thread's key of the tile (TMEM lane)
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    const bool o_owner = wq == 0;                // O rows 0..15 = lanes 0..15 of warp 4
+    const int r_own = lane & (NR - 1);           // the row this lane decides (lanes 16-31 repeat)
+    float4 *rowc = reinterpret_cast<float4 *>(smem + SM_ROWC);
+    float *rsc = reinterpret_cast<float *>(smem + SM_RSC);
+    float *mref = reinterpret_cast<float *>(smem + SM_MREF);
+    float *xmax = reinterpret_cast<float *>(smem + SM_XMAX);
+    float *aux = reinterpret_cast<float *>(smem + SM_AUX);
+    const bool has_bias = da.has_bias != 0;
+    const bool partial = a.num_splits > 1;
+    auto warp_wait = [&](uint32_t br, uint32_t parity, int site) -> bool {
+      const bool r = mbar_wait(br, parity, abort_flag, site);
+      return __all_sync(0xffffffffu, r);
+    };
+    int n_xch = 0;
+    // the 128 softmax threads meet
+    auto xch_barrier = [&]() -> bool {
+      mbar_arrive(bar(B_XCH));
+      return warp_wait(bar(B_XCH), (n_xch++) & 1, 10);
+    };
+    int T = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const int li = load_item(idx);
+      if (li <= 0) continue;
+      const int nrows = I.nrows;
+      // ---- row constants (thread = row), once every thread is done with the previous item's
+      if (!(ok = xch_barrier())) break;
+      if (key < NR) {
+        const int r = key;
+        float4 v = make_float4(0.f, 0.f, __int_as_float(0x7fffffff), __int_as_float(-1));
+        if (r < nrows) {
+          const int tau = r / a.group, hg = r - tau * a.group;
+          const int pos = I.p0 + tau;
+          const float s = log_scale(pos, a.inv_ln_base);
+          v = make_float4(a.alpha_log2e * s, kLog2e * s, __int_as_float(pos),
+                          __int_as_float((I.cq + tau) * a.Hq + I.g * a.group + hg));
+        }
+        rowc[r] = v;
+        rsc[r] = v.x;
+        mref[r] = -INFINITY;
+        mref[NR + r] = -INFINITY;
+      }
+      if (!(ok = xch_barrier())) break;
+      if (I.ntiles == 0) {
+        // an empty split of a multi-split decode: its partial contributes nothing
+        if (partial && key < nrows) {
+          const size_t qrow = (size_t)__float_as_int(rowc[key].w);
+          float *dst = a.o_part + ((size_t)I.sp * a.total_q * a.Hq + qrow) * kHeadDim;
+          for (int i = 0; i < kHeadDim; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+          a.lse_part[(size_t)I.sp * a.total_q * a.Hq + qrow] = -INFINITY;
+        }
+        continue;
+      }
+      float lp[NR];                              // this key's share of each row's sum
+#pragma unroll
+      for (int i = 0; i < NR; ++i) lp[i] = 0.f;
+      for (int t = 0; t < I.ntiles && ok; ++t) {
+        const int G = T + t, sb2 = G & 1;
+        const int j0 = I.kbeg + KT * t, j = j0 + key;
+        const bool band = has_bias && (I.p_last - j0 >= 0) && (I.p0 - (j0 + KT - 1) < a.E);
+        const bool edge = (j0 + KT - 1 > I.p0) || (a.window > 0 && j0 < I.p_last - a.window + 1);
+        // band tiles: R[row][p_row - j] for this key, every load issued before
+        // the S wait (an index outside the band reads R[0] and is discarded)
+        float rbias[NR];
+        if (band) {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float4 rc = rowc[i];
+            const int dd = __float_as_int(rc.z) - j;
+            const bool in = dd >= 0 && dd < a.E;
+            const size_t at = in ? (size_t)__float_as_int(rc.w) * a.E + dd : 0;
+            const float rv = a.rdec[at];
+            rbias[i] = in ? rv * rc.y : 0.f;
+          }
+        }
+        if (!(ok = warp_wait(bar(B_S_FULL + sb2), (G >> 1) & 1, 12))) break;
+        tc_fence_after();
+        float y[NR];
+        {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_base + TM_S + 32u * sb2, r);
+          tmem_wait_ld(r);
+#pragma unroll
+          for (int i = 0; i < NR; ++i) y[i] = __uint_as_float(r[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_S_FREE + sb2));         // this thread has read S^T(t)
+        // scale (packed row scales: 4 broadcast vector loads), bias, masks
+        {
+          const float4 *sc4 = reinterpret_cast<const float4 *>(rsc);
+#pragma unroll
+          for (int q4 = 0; q4 < NR / 4; ++q4) {
+            const float4 sv = sc4[q4];
+            y[4 * q4] *= sv.x;
+            y[4 * q4 + 1] *= sv.y;
+            y[4 * q4 + 2] *= sv.z;
+            y[4 * q4 + 3] *= sv.w;
+          }
+        }
+        if (band) {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) y[i] += rbias[i];
+        }
+        if (edge) {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const int pos = __float_as_int(rowc[i].z);
+            if (!(j <= pos && (a.window <= 0 || j > pos - a.window))) y[i] = -INFINITY;
+          }
+        }
+        // the tile's per-row maximum over this warp's keys (lane l: row l % 16),
+        // then over the four warps
+        float *xm = xmax + (t & 1) * (NR * 4);
+        {
+          const float mx = transpose_reduce<true>(y, lane);
+          if (lane < NR) xm[4 * lane + wq] = mx;
+        }
+        if (!(ok = xch_barrier())) break;
+        // lane l decides row l % 16's new running max (every warp decides the
+        // same); the lanes receive each row's by shuffles; p = 2^(y - m); this
+        // key's share of each row's sum, rescaled with the row's max
+        const float *mo = mref + (t & 1) * NR;
+        float *mn = mref + ((t + 1) & 1) * NR;
+        const float4 w4 = reinterpret_cast<const float4 *>(xm)[r_own];
+        const float mx = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w));
+        const float m_old = mo[r_own];
+        const bool upd = mx > m_old + kRescale || (m_old == -INFINITY && mx != -INFINITY);
+        const float m_new = upd ? fmaxf(m_old, mx) : m_old;
+        const float corr = !upd ? 1.f : (m_old == -INFINITY ? 0.f : fast_exp2(m_old - m_new));
+        const bool any_rescale = __any_sync(0xffffffffu, upd && t > 0 && m_old != -INFINITY);
+        const bool any_upd = __any_sync(0xffffffffu, upd);
+        if (o_owner && lane < NR) mn[r_own] = m_new;
+        const float mb = m_new == -INFINITY ? 0.f : m_new;
+        if (any_upd) {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float p = fast_exp2(y[i] - __shfl_sync(0xffffffffu, mb, i));
+            lp[i] = fmaf(lp[i], __shfl_sync(0xffffffffu, corr, i), p);
+            y[i] = p;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float p = fast_exp2(y[i] - __shfl_sync(0xffffffffu, mb, i));
+            lp[i] += p;
+            y[i] = p;
+          }
+        }
+        // the P buffer and O are free once PV(t - 1) has landed (PV of the
+        // previous tile, or the previous item's last one)
+        if (G > 0 && !(ok = warp_wait(bar(B_PV_DONE), (G - 1) & 1, 13))) break;
+        tc_fence_after();
+        if (any_rescale && o_owner) {
+          // O rows 0..31 (the lanes of warp 4) times their factor (1 past the real rows)
+          const float cf = lane < NR ? corr : 1.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            const uint32_t oaddr = tmem + lane_base + TM_O + 32u * c;
+            __syncwarp();
+            tmem_ld32(oaddr, r);
+            tmem_wait_ld(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * cf);
+            __syncwarp();
+            tmem_st32(oaddr, r);
+          }
+          tmem_wait_st();
+        }
+        // P[row][key] (bf16) into the 128-byte-swizzled K-major A operand:
+        // keys 0-63 in the first 2 KB half, 64-127 in the second
+        {
+          const uint32_t kb = (uint32_t)(key >> 6) * HALF16 + (uint32_t)((key & 7) << 1);
+          const uint32_t kc = (uint32_t)((key & 63) >> 3);
+#pragma unroll
+          for (int i = 0; i < NR; ++i)
+            *reinterpret_cast<__nv_bfloat16 *>(smem + SM_P + kb + (uint32_t)i * 128u +
+                                               ((kc ^ ((uint32_t)i & 7u)) << 4)) = __float2bfloat16_rn(y[i]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_P_FULL));
+      }
+      if (!ok) break;
+      // ---- epilogue: the row sums, then out = O / l (or the split's partial)
+      const int G_last = T + I.ntiles - 1;
+      {
+        const float sum = transpose_reduce<false>(lp, lane);
+        if (lane < NR) aux[4 * lane + wq] = sum;
+      }
+      if (!(ok = xch_barrier())) break;
+      if (!(ok = warp_wait(bar(B_PV_DONE), G_last & 1, 14))) break;
+      tc_fence_after();
+      if (o_owner) {
+        const int r = lane & (NR - 1);
+        const bool valid = lane < nrows;
+        const float4 s4 = reinterpret_cast<const float4 *>(aux)[r];
+        const float l = (s4.x + s4.y) + (s4.z + s4.w);
+        const float m = mref[(I.ntiles & 1) * NR + r];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float row_lse = (l > 0.f && m != -INFINITY) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+        const size_t qrow = valid ? (size_t)__float_as_int(rowc[r].w) : 0;
+        const size_t t_row = qrow / a.Hq, h_row = qrow - t_row * a.Hq;
+        const size_t part_row = (size_t)I.sp * a.total_q * a.Hq + qrow;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tmem + lane_base + TM_O + 32u * c, v);
+          tmem_wait_ld(v);
+          if (valid && partial) {
+            float *dst = a.o_part + part_row * kHeadDim + 32 * c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<float4 *>(dst + 4 * i) =
+                  make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                              __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+          } else if (valid) {
+            __nv_bfloat16 *dst = a.out + qrow * kHeadDim + 32 * c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 o4;
+              o4.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv);
+              o4.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
+              o4.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
+              o4.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
+              *reinterpret_cast<uint4 *>(dst + 8 * i) = o4;
+            }
+          }
+        }
+        if (valid) {
+          if (partial) a.lse_part[part_row] = row_lse;
+          else a.lse[h_row * a.total_q + t_row] = row_lse;
+        }
+      }
+      T += I.ntiles;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) record_timeout(a.err, *abort_flag);
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // the CTA gave up: let the producer's own copies land before shared memory
+    // goes away (bounded waits, not cut short by the abort)
+    volatile int keep_waiting = 0;
+    if (issued_q > 0) mbar_wait(bar(B_Q_FULL), (issued_q - 1) & 1, &keep_waiting, 15, 400000000ll);
+    for (int G = max(0, issued_k - NSTAGE); G < issued_k; ++G)
+      if (G != a.test_skip_k_tile)
+        mbar_wait(bar(B_K_FULL + G % NSTAGE), (G / NSTAGE) & 1, &keep_waiting, 15, 400000000ll);
+    for (int G = max(0, issued_v - NSTAGE); G < issued_v; ++G)
+      mbar_wait(bar(B_V_FULL + G % NSTAGE), (G / NSTAGE) & 1, &keep_waiting, 15, 400000000ll);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// R = r . P for every decode row (t, h) and distance d < E, fp32
+// [total_q * Hq][E]: a CTA takes 16 rows and 256 distances, a thread one
+// distance for the 16 rows (P reads coalesced across the threads, r rows
+// broadcast from shared memory).
+constexpr int RR = 16, RD = 256;
+__global__ void __launch_bounds__(RD) relattn_decode_rel_kernel(const KernelArgs a, float *R) {
+  __shared__ float rs[RR][64];
+  const long rows = (long)a.total_q * a.Hq;
+  const long row0 = (long)blockIdx.x * RR;
+  for (int i = threadIdx.x; i < RR * a.rd; i += RD) {
+    const int rr = i / a.rd, c = i - rr * a.rd;
+    rs[rr][c] = row0 + rr < rows ? __bfloat162float(a.r[(row0 + rr) * a.rd + c]) : 0.f;
+  }
+  __syncthreads();
+  const int d = blockIdx.y * RD + threadIdx.x;
+  if (d >= a.E) return;
+  float acc[RR];
+#pragma unroll
+  for (int i = 0; i < RR; ++i) acc[i] = 0.f;
+  for (int c = 0; c < a.rd; ++c) {
+    const float pv = __bfloat162float(a.P[(size_t)c * a.E + d]);
+#pragma unroll
+    for (int i = 0; i < RR; ++i) acc[i] = fmaf(rs[i][c], pv, acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < RR; ++i)
+    if (row0 + i < rows) R[(row0 + i) * a.E + d] = acc[i];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 dec_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
+  return fn;
+}
+
+// [rows, heads, 128] bf16 in boxes of 64 dims x box_heads heads x box_rows rows, 128B swizzle
+bool encode_heads(CUtensorMap *m, const void *base, int heads, int rows, int box_heads, int box_rows) {
+  auto fn = dec_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool decode_few_rows_supported(const KernelArgs &a, int kv_rows) {
+  auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!dec_encoder()) return false;
+  if (!al(a.q) || !al(a.k) || !al(a.v) || !al(a.out)) return false;
+  if (a.group <= 0 || a.max_q <= 0 || (long)a.group * a.max_q > NR) return false;   // one item, every row
+  if (a.max_q > a.total_q) return false;   // the q box (max_q tokens) fits the tensor
+  if (a.rd > 64) return false;             // the R pre-pass holds r rows of 64 at most
+  return kv_rows >= KT;                    // K / V boxes of 128 rows
+}
+
+size_t decode_rel_bytes(const KernelArgs &a) {
+  if (!(a.rd > 0 && a.E > 0)) return 0;
+  return (size_t)a.total_q * a.Hq * a.E * sizeof(float);
+}
+
+cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_t stream) {
+  DecArgs da;
+  da.a = a;
+  da.has_bias = a.rd > 0 && a.E > 0 && a.rdec != nullptr;
+  da.q_bytes = 2 * 64 * 2 * a.group * a.max_q;
+  const long items = (long)a.num_splits * a.batch * a.Hkv;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
+  da.n_items = (int)items;
+  if (da.has_bias) {
+    // R for the decode rows first (same stream)
+    const long rrows = (long)a.total_q * a.Hq;
+    dim3 g((unsigned)((rrows + RR - 1) / RR), (unsigned)((a.E + RD - 1) / RD));
+    relattn_decode_rel_kernel<<<g, RD, 0, stream>>>(a, const_cast<float *>(a.rdec));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap mq, mk, mv;
+  if (!encode_heads(&mq, a.q, a.Hq, a.total_q, a.group, a.max_q) ||
+      !encode_heads(&mk, a.k, a.Hkv, kv_rows, 1, KT) || !encode_heads(&mv, a.v, a.Hkv, kv_rows, 1, KT))
+    return cudaErrorInvalidValue;
+  static std::atomic<bool> attr_set[kMaxDevicesAttr];
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel),
+                                    (int)SMEM_BYTES, attr_set);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<long>(items, a.sms > 0 ? a.sms : items);
+  relattn_decode_tc_kernel<<<grid, NTHR, SMEM_BYTES, stream>>>(da, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace relattn

@@ -76,6 +76,16 @@ cudaError_t launch_prefill_tc_main(const KernelArgs &a, int total_k, cudaStream_
 // (num_splits, Hkv * row_blocks, batch); partials when num_splits > 1.
 constexpr int kTcDecodeRows = 128;
 cudaError_t launch_decode_tc(const KernelArgs &a, int total_k, cudaStream_t stream);
+// decode of few rows (decode_tc.cu): keys along the MMA's M; an item is
+// (split, sequence, kv head) and holds every row of the sequence's tokens for
+// that kv head (max_q x group <= 16).  Needs 16-byte aligned q / k / v / out
+// and at least 128 K / V rows.  With a bias it first computes R = r . P of the
+// decode rows into a.rdec (decode_rel_bytes of workspace).  Partials when
+// num_splits > 1.
+constexpr int kFewRows = 16;
+bool decode_few_rows_supported(const KernelArgs &a, int kv_rows);
+size_t decode_rel_bytes(const KernelArgs &a);
+cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_t stream);
 cudaError_t launch_decode_mma(const KernelArgs &a, int warps, cudaStream_t stream);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits,
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,

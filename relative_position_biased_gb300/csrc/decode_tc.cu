@@ -13,17 +13,24 @@
 // A decode item is (split, sequence, kv head): its rows are the (token,
 // head-in-group) pairs of one kv head -- 8 rows for one token of a GQA-8
 // group -- and it streams the split's keys in 128-key tiles.  With so few rows
-// the score tile is computed transposed, S^T = K Q^T: the tile's 128 keys
-// along M (TMEM lanes), the rows along N (16 columns), so the tensor core and
-// the softmax only touch real rows (the rows-along-M decode of fwd_tc.cu
-// spends 128 lanes on them).  Each softmax thread owns one key: it scales its
-// 16 scores, adds the relative bias of band tiles and masks edge tiles; the
-// per-row maximum over the tile's keys is a transposed warp reduction (lane l
-// ends with row l % 16) plus a four-warp exchange; lane l decides row l's
-// running max, which the lanes receive by shuffles; then p = 2^(x - m).  P
-// goes to shared memory as the A operand of O = P V (M = 128 with only the
-// first 16 rows real, N = 128 dims; O in TMEM, lane = row).  Each key-thread
-// keeps its share of every row's sum; the shares are reduced once per item.
+// both products are computed transposed, with 16 rows as the MMA's N:
+// S^T = K Q^T (the tile's 128 keys along M, i.e. TMEM lanes) and
+// O^T += V^T P^T (the 128 dims along M), so the tensor core and the softmax
+// only touch real rows (the rows-along-M decode of fwd_tc.cu spends 128 lanes
+// on them).  Each softmax thread owns one key: it scales its 16 scores, adds
+// the relative bias of band tiles and masks edge tiles; the per-row maximum
+// over the tile's keys is a transposed warp reduction (lane l ends with row
+// l % 16) plus a four-warp exchange; lane l decides row l's running max,
+// which the lanes receive by shuffles; then p = 2^(x - m), written to shared
+// memory as the B operand of the PV product.  Each key-thread keeps its share
+// of every row's sum; the shares are reduced once per item.
+//
+// Two softmax warpgroups take the item's tiles in turn (tile G of the CTA's
+// walk goes to warpgroup G % 2), each with its own running max and sum, its
+// own P buffer and its own O^T accumulator: a warpgroup has two tile periods
+// for each of its tiles, so the softmax hides behind the copies and the
+// tensor core.  At the end of the item the two partial results are merged
+// like two splits (the max of the two running maxima, each side rescaled).
 //
 // Relative bias: R = r . P for every decode row and distance below E is
 // computed beforehand (relattn_decode_rel_kernel, fp32, in the caller's
@@ -31,20 +38,19 @@
 // row), all sixteen loads issued before any is used.  No sheared tensor, no
 // TMEM ring, so any r_dim <= 64 and any E work.
 //
-// Warps (8; one CTA per SM walking items in a longest-first order):
+// Warps (10; one CTA per SM walking items in a longest-first order):
 //   warp 0      TMA producer (one thread): the item's q rows (a box of group
 //               heads x tokens), then K and V tiles (3-stage rings)
-//   warp 1      TMEM allocator, MMA issuer (one thread): S^T(t) into one of
-//               two TMEM buffers, then PV(t - 1)
-//   warps 2-3   idle
-//   warps 4-7   softmax: thread = key of the tile (TMEM lane); warp 4's
-//               lanes 0-15 also own O's rows for the rescale and the epilogue
+//   warp 1      TMEM allocator, MMA issuer (one thread): S^T(G) into the
+//               buffer of warpgroup G % 2, then O^T += V^T P^T of tile G - 1
+//   warps 2-5   softmax warpgroup 0 (even tiles), warps 6-9 warpgroup 1 (odd
+//               tiles): thread = key of the tile (TMEM lane 32 (warp % 4) +
+//               lane) for the scores, = dim of O^T for the rescale and merge
 //
-// Tensor memory: S^T buffers [0,16) and [32,48), O [128,256).  Shared memory:
-// P (16 rows x 128 keys, 4 KB; the PV MMA reads 128 rows from each 2 KB half,
-// the 112 past the real ones being whatever follows in shared memory: they
-// only feed O's padding rows), q rows (4 KB), K and V rings (3 x 32 KB each),
-// per-row constants and exchange buffers.
+// Tensor memory (64 columns): S^T of warpgroup b at 16 b, O^T of warpgroup b
+// at 32 + 16 b.  Shared memory: the two P buffers (16 rows x 128 keys, 4 KB
+// each), q rows (4 KB), K and V rings (3 x 32 KB each), the merge buffer
+// (warpgroup 1's O^T, 8 KB), per-warpgroup row constants and exchange buffers.
 //
 // Every wait is bounded; a timeout raises the CTA's abort flag and records the
 // wait site in the device error word; the CTA drains its copies and MMAs,
@@ -60,38 +66,42 @@ namespace {
 using namespace tc;
 
 constexpr int KT = 128;                    // keys per tile (TMEM lanes of S^T)
-constexpr int NR = kFewRows;               // rows per item at most (columns of S^T)
+constexpr int NR = kFewRows;               // rows per item at most (the MMAs' N)
 static_assert(NR == 16, "one 16-column chunk of S^T");
 constexpr int NSTAGE = 3;                  // K and V ring stages
-constexpr int NTHR = 256;
+constexpr int NTHR = 320;
 constexpr float kRescale = 8.f;            // log2 units
 
-constexpr uint32_t TM_S = 0, TM_O = 128;   // S^T buffer b at 32 b; O
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TM_S = 0, TM_O = 32;    // S^T / O^T of warpgroup b at + 16 b
+constexpr uint32_t TMEM_COLS = 64;
 
 constexpr uint32_t BOX = 16384;            // [64 dims x 128 rows] bf16, 128-byte rows, 128B swizzle
 constexpr uint32_t TILE = 2 * BOX;
 constexpr uint32_t HALF16 = NR * 128;      // [64 dims (or keys) x 16 rows]: 2 KB
-constexpr uint32_t SM_P = 0;                          // P: two 2 KB halves (keys 0-63, 64-127)
-constexpr uint32_t SM_Q = SM_P + 2 * HALF16;          // q rows: two 2 KB halves (dims 0-63, 64-127)
+constexpr uint32_t SM_P = 0;                          // P of warpgroup b at + 4 KB b: halves keys 0-63, 64-127
+constexpr uint32_t SM_Q = SM_P + 4 * HALF16;          // q rows: two 2 KB halves (dims 0-63, 64-127)
 constexpr uint32_t SM_K = SM_Q + 2 * HALF16;          // 1024-aligned
 constexpr uint32_t SM_V = SM_K + NSTAGE * TILE;
-constexpr uint32_t SM_ROWC = SM_V + NSTAGE * TILE;    // float4 [NR]: scale, bias scale, position, R row
-constexpr uint32_t SM_RSC = SM_ROWC + NR * 16;        // float [NR]: the scales, packed
-constexpr uint32_t SM_MREF = SM_RSC + NR * 4;         // float [2][NR]: running max by tile parity
-constexpr uint32_t SM_XMAX = SM_MREF + 2 * NR * 4;    // float [2][NR][4]: tile max per warp
-constexpr uint32_t SM_AUX = SM_XMAX + 2 * NR * 16;    // float [NR][4]: row sums per warp
+constexpr uint32_t SM_MB = SM_V + NSTAGE * TILE;      // float [NR][128]: warpgroup 1's O^T; then m, l [NR] each
+constexpr uint32_t SM_WG = SM_MB + NR * 128 * 4 + 2 * NR * 4;
+// per warpgroup: row constants and exchange buffers
+constexpr uint32_t WG_ROWC = 0;                       // float4 [NR]: scale, bias scale, position, output row
+constexpr uint32_t WG_RSC = WG_ROWC + NR * 16;        // float [NR]: the scales, packed
+constexpr uint32_t WG_MREF = WG_RSC + NR * 4;         // float [2][NR]: running max by tile parity
+constexpr uint32_t WG_XMAX = WG_MREF + 2 * NR * 4;    // float [2][NR][4]: tile max per warp
+constexpr uint32_t WG_AUX = WG_XMAX + 2 * NR * 16;    // float [NR][4]: row sums per warp
+constexpr uint32_t WG_BYTES = WG_AUX + NR * 16;
 // work order (batch <= kOrd): per sequence its full / partial split counts,
 // their prefix sums, the partial splits by size, and the count of partials
 constexpr int kOrd = 64;
 constexpr int ORD_NF = 0, ORD_REM = kOrd, ORD_PF = 2 * kOrd, ORD_PZ = 3 * kOrd + 1,
               ORD_PTAB = 4 * kOrd + 2, ORD_NP = 5 * kOrd + 2, ORD_INTS = 5 * kOrd + 4;
-constexpr uint32_t SM_ORD = SM_AUX + NR * 16;
+constexpr uint32_t SM_ORD = SM_WG + 2 * WG_BYTES;
 enum {
   B_Q_FULL = 0, B_Q_EMPTY, B_K_FULL, B_K_EMPTY = B_K_FULL + NSTAGE, B_V_FULL = B_K_EMPTY + NSTAGE,
   B_V_EMPTY = B_V_FULL + NSTAGE, B_S_FULL = B_V_EMPTY + NSTAGE, B_S_FREE = B_S_FULL + 2,
-  B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 1, B_XCH = B_PV_DONE + 1, B_DRAIN = B_XCH + 1,
-  B_COUNT = B_DRAIN + 1
+  B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2, B_XCH = B_PV_DONE + 2, B_M_FULL = B_XCH + 2,
+  B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_COUNT = B_DRAIN + 1
 };
 constexpr uint32_t SM_BAR = SM_ORD + ORD_INTS * 4;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
@@ -99,8 +109,7 @@ constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
 constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
 constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;      // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-// the PV MMA reads 128 rows of 128 bytes from each P half's start
-static_assert(SM_P + HALF16 + BOX <= SM_TOTAL, "P operand window inside shared memory");
+static_assert(SM_WG % 16 == 0 && WG_BYTES % 16 == 0, "float4 alignment");
 
 struct DecArgs {
   KernelArgs a;
@@ -208,8 +217,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   const int n_items = da.n_items;
 
   // ------------------------------------------------------------ set-up
-  // q and P start as zeros: rows past an item's real ones then score 0
-  // instead of whatever the memory held
+  // q and the P buffers start as zeros: rows past an item's real ones then
+  // score 0 instead of whatever the memory held
   for (int i = tid; i < (int)(SM_K - SM_P) / 16; i += NTHR)
     *reinterpret_cast<uint4 *>(smem + SM_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
@@ -225,10 +234,12 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_S_FULL + i), 1);
       mbar_init(bar(B_S_FREE + i), 128);
+      mbar_init(bar(B_P_FULL + i), 128);
+      mbar_init(bar(B_PV_DONE + i), 1);
+      mbar_init(bar(B_XCH + i), 128);
     }
-    mbar_init(bar(B_P_FULL), 128);
-    mbar_init(bar(B_PV_DONE), 1);
-    mbar_init(bar(B_XCH), 128);
+    mbar_init(bar(B_M_FULL), 128);
+    mbar_init(bar(B_M_FREE), 128);
     mbar_init(bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -343,31 +354,34 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   } else if (warp == 1) {
     // ====================================================== MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(KT, NR, 0, 0);    // S^T: K (smem) x Q (smem), both K-major
-      const uint32_t id_o = idesc_bf16_f32(128, 128, 0, 1);  // O: P (smem, K-major) x V (smem, MN-major)
+      const uint32_t id_s = idesc_bf16_f32(KT, NR, 0, 0);    // S^T = K Q^T: K (keys x dims), q rows, both K-major
+      const uint32_t id_o = idesc_bf16_f32(128, NR, 1, 0);   // O^T += V^T P^T: V^T dims-contiguous, P K-major
       // descriptor bases; k-step k of a 128-wide K dimension: +2 per 32 bytes
       // inside a 128-byte row, the second 64-wide half at +16 KB in a K tile
-      // and at +2 KB in the 16-row q and P operands
+      // and at +2 KB in the 16-row q and P operands; V^T: dims along M in two
+      // 64-dim boxes 16 KB apart, 16 keys (+2 KB) per k-step
       const uint64_t qd = smem_desc_sw128(sb + SM_Q, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sb + SM_K, 16, 1024);
-      const uint64_t pd = smem_desc_sw128(sb + SM_P, 16, 1024);
+      const uint64_t pd0 = smem_desc_sw128(sb + SM_P, 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(sb + SM_V, BOX, 1024);
       auto koff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (BOX >> 4) + 2 * (k - 4)); };
       auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
       int T = 0, n_it = 0;
       bool ok = true;
+      // O^T of warpgroup G % 2 (+)= V(G)^T P(G)^T; `first`: the warpgroup's first tile of the item
       auto issue_pv = [&](int G, bool first) -> bool {
-        const int st = G % NSTAGE;
-        if (!mbar_wait(bar(B_P_FULL), G & 1, abort_flag, 4)) return false;
+        const int st = G % NSTAGE, b = G & 1;
+        if (!mbar_wait(bar(B_P_FULL + b), (G >> 1) & 1, abort_flag, 4)) return false;
         if (!mbar_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, abort_flag, 5)) return false;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * TILE) >> 4);
-        const uint32_t o = tmem + TM_O;
-        if (first) mma_ss_c<0>(o, pd + hoff(0), vd + 0, id_o);
-        else mma_ss_c<1>(o, pd + hoff(0), vd + 0, id_o);
+        const uint64_t pd = pd0 + (uint64_t)((b * 2 * HALF16) >> 4);
+        const uint32_t o = tmem + TM_O + 16u * (uint32_t)b;
+        if (first) mma_ss_c<0>(o, vd + 0, pd + hoff(0), id_o);
+        else mma_ss_c<1>(o, vd + 0, pd + hoff(0), id_o);
 #pragma unroll
-        for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, pd + hoff(k), vd + 128 * k, id_o);
-        mma_commit(bar(B_PV_DONE));
+        for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, vd + 128 * k, pd + hoff(k), id_o);
+        mma_commit(bar(B_PV_DONE + b));
         mma_commit(bar(B_V_EMPTY + st));
         return true;
       };
@@ -375,21 +389,21 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         if (!(ok = mbar_wait(bar(B_Q_FULL), n_it & 1, abort_flag, 6))) break;
         for (int t = 0; t < I.ntiles && ok; ++t) {
-          const int G = T + t, sb2 = G & 1, st = G % NSTAGE;
-          if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + sb2), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
+          const int G = T + t, b = G & 1, st = G % NSTAGE;
+          if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
           if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / NSTAGE) & 1, abort_flag, 8))) break;
           tc_fence_after();
           const uint64_t kd = kd0 + (uint64_t)((st * TILE) >> 4);
-          const uint32_t d = tmem + TM_S + 32u * (uint32_t)sb2;
+          const uint32_t d = tmem + TM_S + 16u * (uint32_t)b;
           mma_ss_c<0>(d, kd + koff(0), qd + hoff(0), id_s);
 #pragma unroll
           for (int k = 1; k < 8; ++k) mma_ss_c<1>(d, kd + koff(k), qd + hoff(k), id_s);
-          mma_commit(bar(B_S_FULL + sb2));
+          mma_commit(bar(B_S_FULL + b));
           mma_commit(bar(B_K_EMPTY + st));
           if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY));   // the item's q rows are read
-          if (t > 0) ok = issue_pv(G - 1, t == 1);
+          if (t > 0) ok = issue_pv(G - 1, t - 1 < 2);
         }
-        if (ok) ok = issue_pv(T + I.ntiles - 1, I.ntiles == 1);
+        if (ok) ok = issue_pv(T + I.ntiles - 1, I.ntiles - 1 < 2);
         T += I.ntiles;
         ++n_it;
       }
@@ -399,29 +413,36 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 9, 400000000ll);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else {
     // ======================================================== softmax
-    const int wq = warp & 3;                     // lane quarter: keys 32 wq .. 32 wq + 31
-    const int key = 32 * wq + lane;              // this thread's key of the tile (TMEM lane)
+    const int wg = (warp - 2) >> 2;              // warpgroup: tiles G with G % 2 == wg
+    const int wq = warp & 3;                     // TMEM lane quarter of this warp
+    const int key = 32 * wq + lane;              // this thread's key of the tile / dim of O^T
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    const bool o_owner = wq == 0;                // O rows 0..15 = lanes 0..15 of warp 4
+    const bool row_owner = wq == 0;              // lanes 0..15 of this warp: rows 0..15
     const int r_own = lane & (NR - 1);           // the row this lane decides (lanes 16-31 repeat)
-    float4 *rowc = reinterpret_cast<float4 *>(smem + SM_ROWC);
-    float *rsc = reinterpret_cast<float *>(smem + SM_RSC);
-    float *mref = reinterpret_cast<float *>(smem + SM_MREF);
-    float *xmax = reinterpret_cast<float *>(smem + SM_XMAX);
-    float *aux = reinterpret_cast<float *>(smem + SM_AUX);
+    uint8_t *wgs = smem + SM_WG + wg * WG_BYTES;
+    float4 *rowc = reinterpret_cast<float4 *>(wgs + WG_ROWC);
+    float *rsc = reinterpret_cast<float *>(wgs + WG_RSC);
+    float *mref = reinterpret_cast<float *>(wgs + WG_MREF);
+    float *xmax = reinterpret_cast<float *>(wgs + WG_XMAX);
+    float *aux = reinterpret_cast<float *>(wgs + WG_AUX);
+    float *mbuf = reinterpret_cast<float *>(smem + SM_MB);          // [NR][128]
+    float *mbuf_m = mbuf + NR * 128, *mbuf_l = mbuf_m + NR;
+    const uint32_t s_col = tmem + lane_base + TM_S + 16u * (uint32_t)wg;
+    const uint32_t o_col = tmem + lane_base + TM_O + 16u * (uint32_t)wg;
+    const uint32_t p_buf = SM_P + (uint32_t)wg * 2 * HALF16;
     const bool has_bias = da.has_bias != 0;
     const bool partial = a.num_splits > 1;
     auto warp_wait = [&](uint32_t br, uint32_t parity, int site) -> bool {
       const bool r = mbar_wait(br, parity, abort_flag, site);
       return __all_sync(0xffffffffu, r);
     };
-    int n_xch = 0;
-    // the 128 softmax threads meet
+    int n_xch = 0, n_merge = 0;
+    // the warpgroup's 128 threads meet
     auto xch_barrier = [&]() -> bool {
-      mbar_arrive(bar(B_XCH));
-      return warp_wait(bar(B_XCH), (n_xch++) & 1, 10);
+      mbar_arrive(bar(B_XCH + wg));
+      return warp_wait(bar(B_XCH + wg), (n_xch++) & 1, 10);
     };
     int T = 0;
     bool ok = true;
@@ -429,7 +450,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       const int li = load_item(idx);
       if (li <= 0) continue;
       const int nrows = I.nrows;
-      // ---- row constants (thread = row), once every thread is done with the previous item's
+      // ---- row constants (thread = row), once the warpgroup is done with the previous item's
       if (!(ok = xch_barrier())) break;
       if (key < NR) {
         const int r = key;
@@ -449,7 +470,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       if (!(ok = xch_barrier())) break;
       if (I.ntiles == 0) {
         // an empty split of a multi-split decode: its partial contributes nothing
-        if (partial && key < nrows) {
+        if (wg == 0 && partial && key < nrows) {
           const size_t qrow = (size_t)__float_as_int(rowc[key].w);
           float *dst = a.o_part + ((size_t)I.sp * a.total_q * a.Hq + qrow) * kHeadDim;
           for (int i = 0; i < kHeadDim; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -460,8 +481,9 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       float lp[NR];                              // this key's share of each row's sum
 #pragma unroll
       for (int i = 0; i < NR; ++i) lp[i] = 0.f;
-      for (int t = 0; t < I.ntiles && ok; ++t) {
-        const int G = T + t, sb2 = G & 1;
+      int tl = 0;                                // this warpgroup's tiles of the item so far
+      for (int t = (wg - T) & 1; t < I.ntiles && ok; t += 2, ++tl) {
+        const int G = T + t;
         const int j0 = I.kbeg + KT * t, j = j0 + key;
         const bool band = has_bias && (I.p_last - j0 >= 0) && (I.p0 - (j0 + KT - 1) < a.E);
         const bool edge = (j0 + KT - 1 > I.p0) || (a.window > 0 && j0 < I.p_last - a.window + 1);
@@ -479,18 +501,18 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
             rbias[i] = in ? rv * rc.y : 0.f;
           }
         }
-        if (!(ok = warp_wait(bar(B_S_FULL + sb2), (G >> 1) & 1, 12))) break;
+        if (!(ok = warp_wait(bar(B_S_FULL + wg), (G >> 1) & 1, 12))) break;
         tc_fence_after();
         float y[NR];
         {
           uint32_t r[16];
-          tmem_ld16(tmem + lane_base + TM_S + 32u * sb2, r);
+          tmem_ld16(s_col, r);
           tmem_wait_ld(r);
 #pragma unroll
           for (int i = 0; i < NR; ++i) y[i] = __uint_as_float(r[i]);
         }
         tc_fence_before();
-        mbar_arrive(bar(B_S_FREE + sb2));         // this thread has read S^T(t)
+        mbar_arrive(bar(B_S_FREE + wg));          // this thread has read S^T(G)
         // scale (packed row scales: 4 broadcast vector loads), bias, masks
         {
           const float4 *sc4 = reinterpret_cast<const float4 *>(rsc);
@@ -516,7 +538,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         }
         // the tile's per-row maximum over this warp's keys (lane l: row l % 16),
         // then over the four warps
-        float *xm = xmax + (t & 1) * (NR * 4);
+        float *xm = xmax + (tl & 1) * (NR * 4);
         {
           const float mx = transpose_reduce<true>(y, lane);
           if (lane < NR) xm[4 * lane + wq] = mx;
@@ -525,17 +547,17 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         // lane l decides row l % 16's new running max (every warp decides the
         // same); the lanes receive each row's by shuffles; p = 2^(y - m); this
         // key's share of each row's sum, rescaled with the row's max
-        const float *mo = mref + (t & 1) * NR;
-        float *mn = mref + ((t + 1) & 1) * NR;
+        const float *mo = mref + (tl & 1) * NR;
+        float *mn = mref + ((tl + 1) & 1) * NR;
         const float4 w4 = reinterpret_cast<const float4 *>(xm)[r_own];
         const float mx = fmaxf(fmaxf(w4.x, w4.y), fmaxf(w4.z, w4.w));
         const float m_old = mo[r_own];
         const bool upd = mx > m_old + kRescale || (m_old == -INFINITY && mx != -INFINITY);
         const float m_new = upd ? fmaxf(m_old, mx) : m_old;
         const float corr = !upd ? 1.f : (m_old == -INFINITY ? 0.f : fast_exp2(m_old - m_new));
-        const bool any_rescale = __any_sync(0xffffffffu, upd && t > 0 && m_old != -INFINITY);
+        const bool any_rescale = __any_sync(0xffffffffu, upd && tl > 0 && m_old != -INFINITY);
         const bool any_upd = __any_sync(0xffffffffu, upd);
-        if (o_owner && lane < NR) mn[r_own] = m_new;
+        if (row_owner && lane < NR) mn[r_own] = m_new;
         const float mb = m_new == -INFINITY ? 0.f : m_new;
         if (any_upd) {
 #pragma unroll
@@ -552,93 +574,114 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
             y[i] = p;
           }
         }
-        // the P buffer and O are free once PV(t - 1) has landed (PV of the
-        // previous tile, or the previous item's last one)
-        if (G > 0 && !(ok = warp_wait(bar(B_PV_DONE), (G - 1) & 1, 13))) break;
+        // this warpgroup's P buffer and O^T are free once its previous tile's
+        // PV (tile G - 2: of this item, or of an earlier one) has landed
+        if (G >= 2 && !(ok = warp_wait(bar(B_PV_DONE + wg), ((G - 2) >> 1) & 1, 13))) break;
         tc_fence_after();
-        if (any_rescale && o_owner) {
-          // O rows 0..31 (the lanes of warp 4) times their factor (1 past the real rows)
-          const float cf = lane < NR ? corr : 1.f;
+        if (any_rescale) {
+          // O^T[dim][row] times the row's factor (the whole warpgroup: thread = dim)
+          uint32_t r[16];
+          tmem_ld16(o_col, r);
+          tmem_wait_ld(r);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            const uint32_t oaddr = tmem + lane_base + TM_O + 32u * c;
-            __syncwarp();
-            tmem_ld32(oaddr, r);
-            tmem_wait_ld(r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * cf);
-            __syncwarp();
-            tmem_st32(oaddr, r);
-          }
+          for (int i = 0; i < NR; ++i)
+            r[i] = __float_as_uint(__uint_as_float(r[i]) * __shfl_sync(0xffffffffu, corr, i));
+          tmem_st16(o_col, r);
           tmem_wait_st();
         }
-        // P[row][key] (bf16) into the 128-byte-swizzled K-major A operand:
+        // P[row][key] (bf16) into the 128-byte-swizzled K-major B operand:
         // keys 0-63 in the first 2 KB half, 64-127 in the second
         {
-          const uint32_t kb = (uint32_t)(key >> 6) * HALF16 + (uint32_t)((key & 7) << 1);
+          const uint32_t kb = p_buf + (uint32_t)(key >> 6) * HALF16 + (uint32_t)((key & 7) << 1);
           const uint32_t kc = (uint32_t)((key & 63) >> 3);
 #pragma unroll
           for (int i = 0; i < NR; ++i)
-            *reinterpret_cast<__nv_bfloat16 *>(smem + SM_P + kb + (uint32_t)i * 128u +
+            *reinterpret_cast<__nv_bfloat16 *>(smem + kb + (uint32_t)i * 128u +
                                                ((kc ^ ((uint32_t)i & 7u)) << 4)) = __float2bfloat16_rn(y[i]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(B_P_FULL));
+        mbar_arrive(bar(B_P_FULL + wg));
       }
       if (!ok) break;
-      // ---- epilogue: the row sums, then out = O / l (or the split's partial)
-      const int G_last = T + I.ntiles - 1;
+      // ---- this warpgroup's row sums and max; its O^T once its last PV has landed
+      const int ntl = tl;
       {
         const float sum = transpose_reduce<false>(lp, lane);
         if (lane < NR) aux[4 * lane + wq] = sum;
       }
       if (!(ok = xch_barrier())) break;
-      if (!(ok = warp_wait(bar(B_PV_DONE), G_last & 1, 14))) break;
+      if (ntl > 0) {
+        const int G_last = T + ((wg - T) & 1) + 2 * (ntl - 1);
+        if (!(ok = warp_wait(bar(B_PV_DONE + wg), (G_last >> 1) & 1, 14))) break;
+      }
       tc_fence_after();
-      if (o_owner) {
-        const int r = lane & (NR - 1);
-        const bool valid = lane < nrows;
-        const float4 s4 = reinterpret_cast<const float4 *>(aux)[r];
-        const float l = (s4.x + s4.y) + (s4.z + s4.w);
-        const float m = mref[(I.ntiles & 1) * NR + r];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const float row_lse = (l > 0.f && m != -INFINITY) ? (m + __log2f(l)) * kLn2 : -INFINITY;
-        const size_t qrow = valid ? (size_t)__float_as_int(rowc[r].w) : 0;
-        const size_t t_row = qrow / a.Hq, h_row = qrow - t_row * a.Hq;
-        const size_t part_row = (size_t)I.sp * a.total_q * a.Hq + qrow;
+      float o[NR];
+      {
+        uint32_t r[16];
+        if (ntl > 0) {
+          tmem_ld16(o_col, r);
+          tmem_wait_ld(r);
+        }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          __syncwarp();
-          tmem_ld32(tmem + lane_base + TM_O + 32u * c, v);
-          tmem_wait_ld(v);
-          if (valid && partial) {
-            float *dst = a.o_part + part_row * kHeadDim + 32 * c;
+        for (int i = 0; i < NR; ++i) o[i] = ntl > 0 ? __uint_as_float(r[i]) : 0.f;
+      }
+      const float *m_fin = mref + (ntl & 1) * NR;
+      if (wg == 1) {
+        // ---- warpgroup 1 hands its O^T, max and sums to warpgroup 0
+        if (n_merge > 0 && !(ok = warp_wait(bar(B_M_FREE), (n_merge - 1) & 1, 16))) break;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              *reinterpret_cast<float4 *>(dst + 4 * i) =
-                  make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
-                              __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
-          } else if (valid) {
-            __nv_bfloat16 *dst = a.out + qrow * kHeadDim + 32 * c;
+        for (int i = 0; i < NR; ++i) mbuf[i * 128 + key] = o[i];
+        if (row_owner && lane < NR) {
+          const float4 s4 = reinterpret_cast<const float4 *>(aux)[lane];
+          mbuf_m[lane] = m_fin[lane];
+          mbuf_l[lane] = (s4.x + s4.y) + (s4.z + s4.w);
+        }
+        mbar_arrive(bar(B_M_FULL));
+      } else {
+        // ---- warpgroup 0 merges the two halves and writes the rows
+        if (!(ok = warp_wait(bar(B_M_FULL), n_merge & 1, 17))) break;
+        // thread = dim; row i: m = max(m0, m1), each side scaled by 2^(m_side - m)
+        float lrow = 0.f, mrow = -INFINITY;   // lane i (< 16): row i's sum and max, for the lse
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 o4;
-              o4.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv);
-              o4.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
-              o4.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
-              o4.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
-              *reinterpret_cast<uint4 *>(dst + 8 * i) = o4;
-            }
+        for (int i = 0; i < NR; ++i) {
+          const float m0 = m_fin[i], m1 = mbuf_m[i];
+          const float4 s4 = reinterpret_cast<const float4 *>(aux)[i];
+          const float l0 = (s4.x + s4.y) + (s4.z + s4.w), l1 = mbuf_l[i];
+          const float m = fmaxf(m0, m1);
+          const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - m);
+          const float f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - m);
+          const float l = l0 * f0 + l1 * f1;
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          const float o1 = mbuf[i * 128 + key];
+          o[i] = ((f0 > 0.f ? o[i] * f0 : 0.f) + (f1 > 0.f ? o1 * f1 : 0.f)) * inv;
+          if (lane == i) {
+            lrow = l;
+            mrow = m;
           }
         }
-        if (valid) {
-          if (partial) a.lse_part[part_row] = row_lse;
-          else a.lse[h_row * a.total_q + t_row] = row_lse;
+        mbar_arrive(bar(B_M_FREE));
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          if (i >= nrows) break;
+          const size_t qrow = (size_t)__float_as_int(rowc[i].w);
+          if (partial)
+            a.o_part[((size_t)I.sp * a.total_q * a.Hq + qrow) * kHeadDim + key] = o[i];
+          else
+            a.out[qrow * kHeadDim + key] = __float2bfloat16_rn(o[i]);
+        }
+        if (row_owner && lane < nrows) {
+          const float row_lse = (lrow > 0.f && mrow != -INFINITY) ? (mrow + __log2f(lrow)) * kLn2 : -INFINITY;
+          const size_t qrow = (size_t)__float_as_int(rowc[lane].w);
+          if (partial) {
+            a.lse_part[(size_t)I.sp * a.total_q * a.Hq + qrow] = row_lse;
+          } else {
+            const size_t t_row = qrow / a.Hq, h_row = qrow - t_row * a.Hq;
+            a.lse[h_row * a.total_q + t_row] = row_lse;
+          }
         }
       }
+      ++n_merge;
       T += I.ntiles;
     }
   }

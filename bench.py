@@ -819,8 +819,8 @@ def splits_sweep(args):
     rpb.build()
     rpb.load_library()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    cases = (("decode_batched", W.decode_batched(), [0, 4, 6, 8, 12, 16, 24, 32]),
-             ("decode_batched_w4096", W.decode_batched(window=4096), [0, 4, 6, 8, 12, 16, 24]),
+    cases = (("decode_batched", W.decode_batched(), [0, 1, 2, 3, 4, 6, 8, 12, 16]),
+             ("decode_batched_w4096", W.decode_batched(window=4096), [0, 1, 2, 3, 4, 6, 8]),
              ("decode_long", W.decode_mtp_long(), [0, 38, 76, 152, 228]))
     for name, w, counts in cases:
         d = {k: v.cuda() for k, v in W.make_inputs(w).items()}

@@ -190,6 +190,13 @@ relattn_status plan_decode(const relattn_params *p, DecodePlan *plan, long kv_ro
     const long target = (2 * units <= sms ? 1L : 2L) * sms;
     chunk = (work + target - 1) / target;
     if (chunk < 256) chunk = 256;                       // at least 256 keys per split
+    // sliding window on the few-row kernel: when every sequence holds a full
+    // window (all units the same size) and the units about fill the SMs, one
+    // split each -- a CTA then runs at most one item, and no item boundary
+    // (each costs the length of a few tiles in that kernel) or combine is paid
+    if (plan->kind == DecodeKind::kKeys && p->window > 0 && seq_keys == (long)p->batch * max_vis &&
+        4 * units >= 3L * sms && units <= sms)
+      chunk = max_vis;
   }
   chunk = (chunk + tile - 1) / tile * tile;
   if (chunk > (max_vis + tile - 1) / tile * tile) chunk = (max_vis + tile - 1) / tile * tile;

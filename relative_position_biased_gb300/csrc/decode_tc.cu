@@ -40,7 +40,8 @@
 //
 // Warps (10; one CTA per SM walking items in a longest-first order):
 //   warp 0      TMA producer (one thread): the item's q rows (a box of group
-//               heads x tokens), then K and V tiles (3-stage rings)
+//               heads x tokens), then K and V tiles (3-stage rings); the
+//               rings run on across items
 //   warp 1      TMEM allocator, MMA issuer (one thread): S^T(G) into the
 //               buffer of warpgroup G % 2, then O^T += V^T P^T of tile G - 1
 //   warps 2-5   softmax warpgroup 0 (even tiles), warps 6-9 warpgroup 1 (odd
@@ -49,7 +50,8 @@
 //
 // Tensor memory (64 columns): S^T of warpgroup b at 16 b, O^T of warpgroup b
 // at 32 + 16 b.  Shared memory: the two P buffers (16 rows x 128 keys, 4 KB
-// each), q rows (4 KB), K and V rings (3 x 32 KB each), the merge buffer
+// each), the q rows of two items (4 KB each: the next item's load while the
+// current one runs), K and V rings (3 x 32 KB each), the merge buffer
 // (warpgroup 1's O^T, 8 KB), per-warpgroup row constants and exchange buffers.
 //
 // Every wait is bounded; a timeout raises the CTA's abort flag and records the
@@ -79,8 +81,8 @@ constexpr uint32_t BOX = 16384;            // [64 dims x 128 rows] bf16, 128-byt
 constexpr uint32_t TILE = 2 * BOX;
 constexpr uint32_t HALF16 = NR * 128;      // [64 dims (or keys) x 16 rows]: 2 KB
 constexpr uint32_t SM_P = 0;                          // P of warpgroup b at + 4 KB b: halves keys 0-63, 64-127
-constexpr uint32_t SM_Q = SM_P + 4 * HALF16;          // q rows: two 2 KB halves (dims 0-63, 64-127)
-constexpr uint32_t SM_K = SM_Q + 2 * HALF16;          // 1024-aligned
+constexpr uint32_t SM_Q = SM_P + 4 * HALF16;          // q rows of item n at + 4 KB (n % 2): halves dims 0-63, 64-127
+constexpr uint32_t SM_K = SM_Q + 4 * HALF16;          // 1024-aligned
 constexpr uint32_t SM_V = SM_K + NSTAGE * TILE;
 constexpr uint32_t SM_MB = SM_V + NSTAGE * TILE;      // float [NR][128]: warpgroup 1's O^T; then m, l [NR] each
 constexpr uint32_t SM_WG = SM_MB + NR * 128 * 4 + 2 * NR * 4;
@@ -92,13 +94,15 @@ constexpr uint32_t WG_XMAX = WG_MREF + 2 * NR * 4;    // float [2][NR][4]: tile 
 constexpr uint32_t WG_AUX = WG_XMAX + 2 * NR * 16;    // float [NR][4]: row sums per warp
 constexpr uint32_t WG_BYTES = WG_AUX + NR * 16;
 // work order (batch <= kOrd): per sequence its full / partial split counts,
-// their prefix sums, the partial splits by size, and the count of partials
+// their prefix sums, the partial splits by size, the count of partials, and
+// the sequence offsets (cu_seqlens_q / _k, read once per CTA)
 constexpr int kOrd = 64;
 constexpr int ORD_NF = 0, ORD_REM = kOrd, ORD_PF = 2 * kOrd, ORD_PZ = 3 * kOrd + 1,
-              ORD_PTAB = 4 * kOrd + 2, ORD_NP = 5 * kOrd + 2, ORD_INTS = 5 * kOrd + 4;
+              ORD_PTAB = 4 * kOrd + 2, ORD_NP = 5 * kOrd + 2, ORD_CQ = 5 * kOrd + 4,
+              ORD_CK = 6 * kOrd + 5, ORD_INTS = 7 * kOrd + 6;
 constexpr uint32_t SM_ORD = SM_WG + 2 * WG_BYTES;
 enum {
-  B_Q_FULL = 0, B_Q_EMPTY, B_K_FULL, B_K_EMPTY = B_K_FULL + NSTAGE, B_V_FULL = B_K_EMPTY + NSTAGE,
+  B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + 2, B_K_FULL = B_Q_EMPTY + 2, B_K_EMPTY = B_K_FULL + NSTAGE, B_V_FULL = B_K_EMPTY + NSTAGE,
   B_V_EMPTY = B_V_FULL + NSTAGE, B_S_FULL = B_V_EMPTY + NSTAGE, B_S_FREE = B_S_FULL + 2,
   B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2, B_XCH = B_PV_DONE + 2, B_M_FULL = B_XCH + 2,
   B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_COUNT = B_DRAIN + 1
@@ -198,9 +202,10 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       I.sp = q / a.batch;
     }
     I.g = u;
-    I.cq = a.cu_q[I.b];
-    I.ck = a.cu_k[I.b];
-    const int Lq = a.cu_q[I.b + 1] - I.cq, Lk = a.cu_k[I.b + 1] - I.ck;
+    const int *cq_t = sorted ? ord + ORD_CQ : a.cu_q, *ck_t = sorted ? ord + ORD_CK : a.cu_k;
+    I.cq = cq_t[I.b];
+    I.ck = ck_t[I.b];
+    const int Lq = cq_t[I.b + 1] - I.cq, Lk = ck_t[I.b + 1] - I.ck;
     // (rows past total_q would index outputs and R out of bounds)
     if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k || I.cq < 0 || I.cq + Lq > a.total_q) return -1;
     if (Lq == 0) return 0;
@@ -223,8 +228,10 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     *reinterpret_cast<uint4 *>(smem + SM_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (tid == 0) {
-    mbar_init(bar(B_Q_FULL), 1);
-    mbar_init(bar(B_Q_EMPTY), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_Q_FULL + i), 1);
+      mbar_init(bar(B_Q_EMPTY + i), 1);
+    }
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(bar(B_K_FULL + i), 1);
       mbar_init(bar(B_K_EMPTY + i), 1);
@@ -261,7 +268,14 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     const int b = tid;
     if (b < a.batch) {
       const int cq = a.cu_q[b], ck = a.cu_k[b];
-      const int Lq = a.cu_q[b + 1] - cq, Lk = a.cu_k[b + 1] - ck;
+      const int cq1 = a.cu_q[b + 1], ck1 = a.cu_k[b + 1];
+      ord[ORD_CQ + b + 1] = cq1;
+      ord[ORD_CK + b + 1] = ck1;
+      if (b == 0) {
+        ord[ORD_CQ] = cq;
+        ord[ORD_CK] = ck;
+      }
+      const int Lq = cq1 - cq, Lk = ck1 - ck;
       long vis = 0;
       if (Lq > 0 && Lk >= Lq) {
         const int p0 = Lk - Lq, p_last = p0 + Lq - 1;
@@ -312,11 +326,15 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         const int li = load_item(idx);
         if (li < 0) atomicOr(a.err, kDevErrSeqlens);
         if (li <= 0 || I.ntiles == 0) continue;
-        // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves of 64 dims
-        if (n_it > 0 && !(run = mbar_wait(bar(B_Q_EMPTY), (n_it - 1) & 1, abort_flag, 1))) break;
-        mbar_arrive_expect_tx(bar(B_Q_FULL), (uint32_t)da.q_bytes);
-        tma_load_3d(sb + SM_Q, &map_q, 0, I.g * a.group, I.cq, bar(B_Q_FULL));
-        tma_load_3d(sb + SM_Q + HALF16, &map_q, 64, I.g * a.group, I.cq, bar(B_Q_FULL));
+        // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves
+        // of 64 dims, in the buffer of the item's parity (the next item's rows
+        // load while the current item's last tiles run)
+        const int qb = n_it & 1;
+        if (n_it >= 2 && !(run = mbar_wait_suspend(bar(B_Q_EMPTY + qb), ((n_it >> 1) - 1) & 1, abort_flag, 1)))
+          break;
+        mbar_arrive_expect_tx(bar(B_Q_FULL + qb), (uint32_t)da.q_bytes);
+        tma_load_3d(sb + SM_Q + qb * 2 * HALF16, &map_q, 0, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
+        tma_load_3d(sb + SM_Q + qb * 2 * HALF16 + HALF16, &map_q, 64, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
         issued_q = n_it + 1;
         // paged K / V: the pool row of a 128-aligned tile inside one page
         auto tile_row = [&](int t) -> int {
@@ -332,14 +350,14 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         for (int t = 0; t < I.ntiles && run; ++t) {
           const int G = T + t, st = G % NSTAGE, use = G / NSTAGE;
           const int row = tile_row(t);
-          if (G >= NSTAGE && !(run = mbar_wait(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
+          if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
           if (G != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
             mbar_arrive_expect_tx(bar(B_K_FULL + st), TILE);
             tma_load_3d(sb + SM_K + st * TILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
             tma_load_3d(sb + SM_K + st * TILE + BOX, &map_k, 64, I.g, row, bar(B_K_FULL + st));
           }
           issued_k = G + 1;
-          if (G >= NSTAGE && !(run = mbar_wait(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
+          if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
           mbar_arrive_expect_tx(bar(B_V_FULL + st), TILE);
           tma_load_3d(sb + SM_V + st * TILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
           tma_load_3d(sb + SM_V + st * TILE + BOX, &map_v, 64, I.g, row, bar(B_V_FULL + st));
@@ -360,7 +378,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       // inside a 128-byte row, the second 64-wide half at +16 KB in a K tile
       // and at +2 KB in the 16-row q and P operands; V^T: dims along M in two
       // 64-dim boxes 16 KB apart, 16 keys (+2 KB) per k-step
-      const uint64_t qd = smem_desc_sw128(sb + SM_Q, 16, 1024);
+      const uint64_t qd0 = smem_desc_sw128(sb + SM_Q, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sb + SM_K, 16, 1024);
       const uint64_t pd0 = smem_desc_sw128(sb + SM_P, 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(sb + SM_V, BOX, 1024);
@@ -387,7 +405,9 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
-        if (!(ok = mbar_wait(bar(B_Q_FULL), n_it & 1, abort_flag, 6))) break;
+        const int qb = n_it & 1;
+        if (!(ok = mbar_wait(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
+        const uint64_t qd = qd0 + (uint64_t)((qb * 2 * HALF16) >> 4);
         for (int t = 0; t < I.ntiles && ok; ++t) {
           const int G = T + t, b = G & 1, st = G % NSTAGE;
           if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
@@ -400,7 +420,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           for (int k = 1; k < 8; ++k) mma_ss_c<1>(d, kd + koff(k), qd + hoff(k), id_s);
           mma_commit(bar(B_S_FULL + b));
           mma_commit(bar(B_K_EMPTY + st));
-          if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY));   // the item's q rows are read
+          if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY + qb));   // the item's q rows are read
           if (t > 0) ok = issue_pv(G - 1, t - 1 < 2);
         }
         if (ok) ok = issue_pv(T + I.ntiles - 1, I.ntiles - 1 < 2);
@@ -695,7 +715,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     // the CTA gave up: let the producer's own copies land before shared memory
     // goes away (bounded waits, not cut short by the abort)
     volatile int keep_waiting = 0;
-    if (issued_q > 0) mbar_wait(bar(B_Q_FULL), (issued_q - 1) & 1, &keep_waiting, 15, 400000000ll);
+    for (int n = max(0, issued_q - 2); n < issued_q; ++n)
+      mbar_wait(bar(B_Q_FULL + (n & 1)), (n >> 1) & 1, &keep_waiting, 15, 400000000ll);
     for (int G = max(0, issued_k - NSTAGE); G < issued_k; ++G)
       if (G != a.test_skip_k_tile)
         mbar_wait(bar(B_K_FULL + G % NSTAGE), (G / NSTAGE) & 1, &keep_waiting, 15, 400000000ll);
@@ -710,28 +731,56 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
 
 // R = r . P for every decode row (t, h) and distance d < E, fp32
 // [total_q * Hq][E]: a CTA takes 16 rows and 256 distances, a thread one
-// distance for the 16 rows (P reads coalesced across the threads, r rows
-// broadcast from shared memory).
+// distance for the 16 rows.  The CTA's slice of P (r_dim x 256 bf16) is first
+// staged in shared memory with 16-byte loads (scalar ones when E is not a
+// multiple of 8), all in flight together; the r rows are broadcast from
+// shared memory (zero past r_dim, and P's rows past r_dim up to the next
+// multiple of 4 are zeroed).
 constexpr int RR = 16, RD = 256;
 __global__ void __launch_bounds__(RD) relattn_decode_rel_kernel(const KernelArgs a, float *R) {
-  __shared__ float rs[RR][64];
+  __shared__ __align__(16) float rs[RR][64];
+  __shared__ __align__(16) __nv_bfloat16 ps[64][RD];
+  const int tid = threadIdx.x;
   const long rows = (long)a.total_q * a.Hq;
   const long row0 = (long)blockIdx.x * RR;
-  for (int i = threadIdx.x; i < RR * a.rd; i += RD) {
-    const int rr = i / a.rd, c = i - rr * a.rd;
-    rs[rr][c] = row0 + rr < rows ? __bfloat162float(a.r[(row0 + rr) * a.rd + c]) : 0.f;
+  const int d0 = blockIdx.y * RD, nd = min(RD, a.E - d0);
+  const int rd4 = (a.rd + 3) & ~3;
+  if ((a.E & 7) == 0 && (reinterpret_cast<uintptr_t>(a.P) & 15u) == 0) {
+    for (int k = tid; k < a.rd * (RD / 8); k += RD) {
+      const int c = k / (RD / 8), j = (k % (RD / 8)) * 8;
+      if (j < nd)
+        *reinterpret_cast<uint4 *>(&ps[c][j]) =
+            *reinterpret_cast<const uint4 *>(a.P + (size_t)c * a.E + d0 + j);
+    }
+  } else {
+    for (int k = tid; k < a.rd * RD; k += RD) {
+      const int c = k / RD, j = k % RD;
+      if (j < nd) ps[c][j] = a.P[(size_t)c * a.E + d0 + j];
+    }
+  }
+  for (int k = a.rd * RD + tid; k < rd4 * RD; k += RD) ps[k / RD][k % RD] = __float2bfloat16_rn(0.f);
+  for (int i = tid; i < RR * 64; i += RD) {
+    const int rr = i >> 6, c = i & 63;
+    rs[rr][c] = (row0 + rr < rows && c < a.rd) ? __bfloat162float(a.r[(row0 + rr) * a.rd + c]) : 0.f;
   }
   __syncthreads();
-  const int d = blockIdx.y * RD + threadIdx.x;
-  if (d >= a.E) return;
+  if (tid >= nd) return;
   float acc[RR];
 #pragma unroll
   for (int i = 0; i < RR; ++i) acc[i] = 0.f;
-  for (int c = 0; c < a.rd; ++c) {
-    const float pv = __bfloat162float(a.P[(size_t)c * a.E + d]);
+  for (int c = 0; c < rd4; c += 4) {
+    const float p0 = __bfloat162float(ps[c][tid]), p1 = __bfloat162float(ps[c + 1][tid]);
+    const float p2 = __bfloat162float(ps[c + 2][tid]), p3 = __bfloat162float(ps[c + 3][tid]);
 #pragma unroll
-    for (int i = 0; i < RR; ++i) acc[i] = fmaf(rs[i][c], pv, acc[i]);
+    for (int i = 0; i < RR; ++i) {
+      const float4 r4 = *reinterpret_cast<const float4 *>(&rs[i][c]);
+      acc[i] = fmaf(r4.x, p0, acc[i]);
+      acc[i] = fmaf(r4.y, p1, acc[i]);
+      acc[i] = fmaf(r4.z, p2, acc[i]);
+      acc[i] = fmaf(r4.w, p3, acc[i]);
+    }
   }
+  const int d = d0 + tid;
 #pragma unroll
   for (int i = 0; i < RR; ++i)
     if (row0 + i < rows) R[(row0 + i) * a.E + d] = acc[i];

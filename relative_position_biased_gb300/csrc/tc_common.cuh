@@ -81,6 +81,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same bounded wait for long waits off the issuing threads' path: each
+// probe may suspend the thread (up to about 2 us) until the phase completes,
+// so a waiting warp takes no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                  int site, long long limit_cycles = 2000000000ll) {
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity, 2000u)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit_cycles) {
+      *abort = site;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,

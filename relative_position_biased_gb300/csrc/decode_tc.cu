@@ -158,8 +158,9 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
                          const __grid_constant__ CUtensorMap map_v) {
   const KernelArgs &a = da.a;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                              ~uintptr_t(1023));
+  // 1024-aligned base, kept as an offset into the shared array so that every
+  // access below stays a shared-memory access (32-bit addresses)
+  uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(smem);
   auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);

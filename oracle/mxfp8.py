@@ -17,7 +17,8 @@ Microscaling (MX) format, read here as follows:
     is floor(log2(amax)) - 8 (8 = the exponent of the largest power of two
     E4M3 holds), clamped to [-127, 127]; an all-zero block takes -127;
     each element is x / 2^e rounded to the nearest E4M3 value, ties to even,
-    magnitudes beyond 448 saturating to 448;
+    magnitudes beyond 448 saturating to 448, the sign kept (a negative value
+    that rounds to zero is the code S=1, -0, as in IEEE rounding);
   * dequantising: element value * 2^e, exact.
 
 The MXFP8 decode reference is the fp64 forward of the relative attention on
@@ -68,8 +69,7 @@ def e4m3_encode(x):
     dhi = _POS[hi] - a
     pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi != lo) & ((hi & 1) == 0))
     code = np.where(pick_hi, hi, lo).astype(np.uint8)
-    neg = np.signbit(x) & (code != 0)
-    return np.where(neg, code | 0x80, code).astype(np.uint8)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
 
 
 def block_exponent(amax):

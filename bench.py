@@ -78,7 +78,9 @@ _FWD = ["relative_position_biased_gb300/csrc/fwd_tc.cu",
         "relative_position_biased_gb300/csrc/common.cuh"]
 KERNEL_SOURCES = {
     "prefill": _FWD + ["relative_position_biased_gb300/csrc/fwd_tc_main.cu"],
-    "decode": _FWD + ["relative_position_biased_gb300/csrc/combine.cu"],
+    "decode": _FWD + ["relative_position_biased_gb300/csrc/combine.cu",
+                      "relative_position_biased_gb300/csrc/decode_tc.cu",
+                      "relative_position_biased_gb300/csrc/mxfp8.cuh"],
     "backward": ["relative_position_biased_gb300/csrc/bwd_mma.cu",
                  "relative_position_biased_gb300/csrc/bwd_tc.cu",
                  "relative_position_biased_gb300/csrc/tc_common.cuh",
@@ -256,7 +258,11 @@ class Phase:
             self.ws = rpb.decode_workspace(prm, "cuda")
             st, splits = rpb.relattn_decode_num_splits(prm)
             self.splits = splits
-            self.launches = 1 + (1 if splits > 1 else 0)
+            # few-row items (<= 16 rows per kv head) with a bias: the decode-row
+            # bias pre-pass, then the decode; the combine when split
+            few = max(w.q_lens) * (w.Hq // w.Hkv) <= 16
+            prepass = few and w.r_dim > 0 and w.rel_extent > 0
+            self.launches = 1 + (1 if prepass else 0) + (1 if splits > 1 else 0)
         self.flops = A.flops(w)
         self.bytes = A.kv_bytes(w)
         io = A.io_bytes(w)
@@ -317,6 +323,28 @@ class PagedDecodePhase:
         a = self.base.args
         self.rpb.decode_paged(a[0], self.k_pool, self.v_pool, a[3], a[4], a[5], a[6], self.table,
                               page_size=self.page_size, total_k=sum(self.w.k_lens),
+                              out=self.base.out, lse=self.base.lse, workspace=self.base.ws,
+                              **_kw(self.w))
+
+
+class Mxfp8DecodePhase:
+    """A decode phase re-run against an MXFP8 copy of its K / V (E4M3 codes and
+    E8M0 scales per 32 dims, quantised once on the device outside the timing)."""
+
+    def __init__(self, base, rpb):
+        self.name, self.w, self.rpb = base.name + "_mxfp8", base.w, rpb
+        self.decode = True
+        self.base = base
+        a = base.args
+        self.k8, self.ks = rpb.quantize_mxfp8(a[1])
+        self.v8, self.vs = rpb.quantize_mxfp8(a[2])
+        self.launches = base.launches
+        self.bytes = A.kv_bytes_mxfp8(base.w)      # bytes the kernel must read
+        self.bytes_bf16 = base.bytes                 # the same keys in bf16
+
+    def run(self):
+        a = self.base.args
+        self.rpb.decode_mxfp8(a[0], self.k8, self.v8, self.ks, self.vs, a[3], a[4], a[5], a[6],
                               out=self.base.out, lse=self.base.lse, workspace=self.base.ws,
                               **_kw(self.w))
 
@@ -611,6 +639,10 @@ def gpu_arm(args):
         return single_phase(args, ProloguePhase(wl["prefill_swa"], rpb))
     if args.only == "backward":
         return single_phase(args, BackwardPhase(wl["prefill_swa"], rpb))
+    if args.only and args.only.endswith("_mxfp8"):
+        n = args.only[:-len("_mxfp8")]
+        mx = Mxfp8DecodePhase(Phase(n, wl[n], W.make_inputs(wl[n]), rpb), rpb)
+        return single_phase(args, mx)
     if args.only:
         return single_phase(args, Phase(args.only, wl[args.only], W.make_inputs(wl[args.only]), rpb))
     host = {k: W.make_inputs(w) for k, w in wl.items()}
@@ -658,6 +690,18 @@ def gpu_arm(args):
         raise SystemExit("device error word set by the paged decode")
     for p in paged:
         del p.k_pool, p.v_pool
+    # the two batched decodes again on an MXFP8 K / V cache
+    mx = [Mxfp8DecodePhase(ph[n], rpb) for n in ("decode_batched", "decode_batched_w")]
+    for _ in range(args.warmup):
+        for p in mx:
+            p.run()
+    torch.cuda.synchronize()
+    mx_t = timed_steps(mx, args.steps, flush)
+    torch.cuda.synchronize()
+    if rpb.relattn_get_device_error() != 0:
+        raise SystemExit("device error word set by the MXFP8 decode")
+    for p in mx:
+        del p.k8, p.v8, p.ks, p.vs
     # the backward of the SWA prefill, timed on its own
     bwd = BackwardPhase(wl["prefill_swa"], rpb)
     for _ in range(args.warmup):
@@ -679,6 +723,7 @@ def gpu_arm(args):
     step_ms = max_over_ranks(sum(median(times[n]) for n in STEP_PHASES), dist)
     pro_ms = max_over_ranks(median(pro_t), dist)
     pg_ms = {p.name: max_over_ranks(median(pg_t[p.name]), dist) for p in paged}
+    mx_ms = {p.name: max_over_ranks(median(mx_t[p.name]), dist) for p in mx}
     bwd_ms = max_over_ranks(median(bwd_t), dist)
     e2e_ser = {n: max_over_ranks(median(e2e_t[n]), dist) for n in STEP_PHASES}
     e2e_pipe = {n: max_over_ranks(e2e_p[n], dist) for n in STEP_PHASES}
@@ -767,6 +812,14 @@ def gpu_arm(args):
                                "ms": pg_ms[p.name], "page_size": p.page_size,
                                "frac": p.bytes / (pg_ms[p.name] * 1e-3) / 1e9 / hbm_peak}
                       for p in paged},
+            "mxfp8": {p.name: {"value": p.bytes / (mx_ms[p.name] * 1e-3) / 1e9, "unit": "GB/s",
+                               "ms": mx_ms[p.name], "bytes": p.bytes,
+                               "frac": p.bytes / (mx_ms[p.name] * 1e-3) / 1e9 / hbm_peak,
+                               "bf16_equivalent": p.bytes_bf16 / (mx_ms[p.name] * 1e-3) / 1e9,
+                               "what": "E4M3 K / V codes + E8M0 scales per 32 dims; q quantised "
+                                       "in the kernel, Q K^T as E4M3 products, V dequantised "
+                                       "to bf16 for P V"}
+                      for p in mx},
         },
         "prologue": {
             "value": job_rate(pro.bytes, pro_ms, ws, 1e9), "unit": "GB/s", "ms": pro_ms,
@@ -867,7 +920,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=list(STEP_PHASES) + ["prologue", "backward"],
+    ap.add_argument("--only", choices=list(STEP_PHASES) + ["prologue", "backward", "decode_batched_mxfp8",
+                                                           "decode_batched_w_mxfp8"],
                     help="time one phase alone (profiling captures)")
     ap.add_argument("--splits-sweep", action="store_true",
                     help="time the decodes at fixed split counts beside the heuristic's choice")

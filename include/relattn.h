@@ -155,6 +155,51 @@ relattn_status relattn_decode_paged(const relattn_params *params, const relattn_
                                    void *stream);
 
 /*
+ * MXFP8 K / V cache (page "SGLang and Miles Add Day-0 Support for Inkling",
+ * section "Relative Logits Optimization", paragraph "MXFP8 Support": K and V
+ * stored in MXFP8, Q K^T as an MXFP8 product, P V in bf16 with V dequantised
+ * on the fly).  The format is OCP Microscaling MXFP8: FP8 E4M3 codes (bias 7,
+ * largest finite 448, S.1111.111 NaN) and one E8M0 scale byte b = 2^(b - 127)
+ * per 32 consecutive elements of the last dimension.
+ *
+ * relattn_quantize_mxfp8: n_blocks blocks of 32 bf16 values (x, device,
+ * 16-byte aligned, contiguous) -> codes (uint8 [n_blocks * 32], 16-byte
+ * aligned) and scales (uint8 [n_blocks]).  Per block, e = floor(log2 amax) - 8
+ * clamped to [-127, 127] (-127 for an all-zero block); each code is
+ * x * 2^-e rounded to the nearest E4M3 value, ties to even, the sign kept
+ * (-0 for a negative value that rounds to zero), saturating at 448.  For a
+ * K / V cache [rows, heads, 128] the blocks are the 4 runs of 32 dims of every
+ * (row, head): scales [rows, heads, 4].  x must not overlap codes or scales.
+ * Finite inputs only.  Asynchronous on `stream`.
+ */
+relattn_status relattn_quantize_mxfp8(const void *x, int64_t n_blocks, void *codes, void *scales,
+                                      void *stream);
+
+typedef struct relattn_kv_mxfp8 {
+  const void *k;               /* uint8 E4M3 [total_k, num_heads_kv, 128], 16-byte aligned */
+  const void *v;               /* uint8 E4M3 [total_k, num_heads_kv, 128], 16-byte aligned */
+  const void *k_scale;         /* uint8 E8M0 [total_k, num_heads_kv, 4], 4-byte aligned    */
+  const void *v_scale;         /* uint8 E8M0 [total_k, num_heads_kv, 4], 4-byte aligned    */
+} relattn_kv_mxfp8;
+
+/*
+ * Decode against an MXFP8 K / V cache.  Same arguments and results as
+ * relattn_decode (params->k / params->v are ignored; kv gives the codes and
+ * scales, contiguous rows cu_seqlens_k[b] + p like relattn_decode's K / V),
+ * same split plan and workspace (relattn_decode_workspace_size of the same
+ * params).  What it computes: the relative-attention forward with q rounded
+ * through MXFP8 per 32 head dims of each row (Q K^T runs as an E4M3 x E4M3
+ * product per 32-dim block, fp32 accumulate, block scales applied in fp32),
+ * K = dequantised k codes, V = dequantised v codes (exact in bf16; P V in
+ * bf16, fp32 accumulate).  Requires max_seqlen_q x (num_heads_q /
+ * num_heads_kv) <= 16 (batched decode: one token of a GQA group up to 16, or a
+ * few tokens of a smaller one), r_dim <= 64 and total_k >= 128; else
+ * RELATTN_ERR_UNSUPPORTED.
+ */
+relattn_status relattn_decode_mxfp8(const relattn_params *params, const relattn_kv_mxfp8 *kv,
+                                    void *stream);
+
+/*
  * Log-sum-exp combine of split partials (the decode combine step, exposed so
  * partials from several KV shards can be merged):
  *   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.

@@ -24,6 +24,8 @@ LIB_PATH = os.path.join(_HERE, "librelattn.so")
 TEST_LIB_PATH = os.path.join(_HERE, "librelattn_test.so")
 
 RELATTN_OK = 0
+RELATTN_ERR_INVALID_ARG = 1
+RELATTN_ERR_UNSUPPORTED = 2
 RELATTN_ERR_TIMEOUT = 4
 STATUS_NAMES = {
     0: "RELATTN_OK", 1: "RELATTN_ERR_INVALID_ARG", 2: "RELATTN_ERR_UNSUPPORTED",
@@ -36,7 +38,7 @@ EXPORTED = (
     "relattn_status_string", "relattn_version", "relattn_decode_noalloc",
     "relattn_last_device_error_word",
     "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
-    "relattn_decode_paged",
+    "relattn_decode_paged", "relattn_decode_mxfp8", "relattn_quantize_mxfp8",
 )
 # exported by the test build only
 TEST_HOOKS = (
@@ -73,6 +75,11 @@ class RelattnPagedKV(ctypes.Structure):
     """Mirror of ``relattn_paged_kv``."""
     _fields_ = [("block_table", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
+
+
+class RelattnKvMxfp8(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class RelattnBwdParams(ctypes.Structure):
@@ -181,6 +188,10 @@ def _configure(path: str):
         lib.relattn_last_device_error_word.restype = ctypes.c_int32
         lib.relattn_decode_paged.argtypes = [P, ctypes.POINTER(RelattnPagedKV), vp]
         lib.relattn_decode_paged.restype = ctypes.c_int
+        lib.relattn_decode_mxfp8.argtypes = [P, ctypes.POINTER(RelattnKvMxfp8), vp]
+        lib.relattn_decode_mxfp8.restype = ctypes.c_int
+        lib.relattn_quantize_mxfp8.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
+        lib.relattn_quantize_mxfp8.restype = ctypes.c_int
         BP = ctypes.POINTER(RelattnBwdParams)
         lib.relattn_backward.argtypes = [BP, vp]
         lib.relattn_backward.restype = ctypes.c_int
@@ -397,6 +408,52 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
     _check(relattn_prologue(prm, _current_stream() if stream is None else stream),
            "relattn_prologue")
     return q_out
+
+
+def relattn_decode_mxfp8(params: RelattnParams, kv: RelattnKvMxfp8, stream: int = 0) -> int:
+    return load_library().relattn_decode_mxfp8(ctypes.byref(params), ctypes.byref(kv), stream)
+
+
+def relattn_quantize_mxfp8(x: int, n_blocks: int, codes: int, scales: int, stream: int = 0) -> int:
+    return load_library().relattn_quantize_mxfp8(x, n_blocks, codes, scales, stream)
+
+
+def quantize_mxfp8(x, stream: Optional[int] = None):
+    """MXFP8 of a contiguous bf16 CUDA tensor whose last dimension is a multiple
+    of 32: (codes uint8 with x's shape, scales uint8 with the last dimension
+    divided by 32)."""
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.shape[-1] % 32:
+        raise ValueError("x must be a contiguous bf16 tensor with a last dimension divisible by 32")
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(*x.shape[:-1], x.shape[-1] // 32, dtype=torch.uint8, device=x.device)
+    _check(relattn_quantize_mxfp8(x.data_ptr(), x.numel() // 32, codes.data_ptr(), scales.data_ptr(),
+                                  _current_stream() if stream is None else stream),
+           "relattn_quantize_mxfp8")
+    return codes, scales
+
+
+def decode_mxfp8(q, k8, v8, k_scale, v_scale, r, P, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int,
+                 max_seqlen_k: int, alpha: float, window: int = 0, log_scale_base: float = 0.0,
+                 num_splits: int = 0, out=None, lse=None, workspace=None, stream: Optional[int] = None):
+    """Split-KV decode against an MXFP8 K / V cache: k8 / v8 uint8 E4M3 codes
+    [total_k, Hkv, 128], k_scale / v_scale uint8 E8M0 [total_k, Hkv, 4].
+    Returns (out, lse)."""
+    out, lse = _outputs(q, out, lse)
+    prm = make_params(q, k8, v8, r, P, cu_seqlens_q, cu_seqlens_k,
+                      max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k, alpha=alpha,
+                      window=window, log_scale_base=log_scale_base, out=out, lse=lse,
+                      num_splits=num_splits)
+    if workspace is None:
+        workspace = decode_workspace(prm, q.device)
+    if workspace is not None:
+        prm.workspace = workspace.data_ptr()
+        prm.workspace_bytes = workspace.numel() * workspace.element_size()
+    kv = RelattnKvMxfp8(k=k8.data_ptr(), v=v8.data_ptr(), k_scale=k_scale.data_ptr(),
+                        v_scale=v_scale.data_ptr())
+    _check(relattn_decode_mxfp8(prm, kv, _current_stream() if stream is None else stream),
+           "relattn_decode_mxfp8")
+    return out, lse
 
 
 def decode_paged(q, k_pool, v_pool, r, P, cu_seqlens_q, cu_seqlens_k, block_table, *,

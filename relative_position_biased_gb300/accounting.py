@@ -73,6 +73,12 @@ def kv_bytes(w: Workload) -> int:
     return tot
 
 
+def kv_bytes_mxfp8(w: Workload) -> int:
+    """The same visible K and V rows stored in MXFP8: one E4M3 byte per
+    element and one E8M0 scale byte per 32 elements."""
+    return kv_bytes(w) // 2 // w.head_dim * (w.head_dim + w.head_dim // 32)
+
+
 def io_bytes(w: Workload) -> dict:
     """Bytes of every input and output tensor (for host<->device copies)."""
     Tq, Tk, D = sum(w.q_lens), sum(w.k_lens), w.head_dim

@@ -366,7 +366,7 @@ relattn_status relattn_decode_num_splits(const relattn_params *p, int32_t *num_s
 // the split kernel, then the combine when there are several splits; kv_rows:
 // rows the K / V tensors hold
 relattn_status run_decode(const relattn_params *p, const DecodePlan &plan, KernelArgs &a, long kv_rows,
-                          cudaStream_t s) {
+                          cudaStream_t s, const relattn_kv_mxfp8 *f8 = nullptr) {
   a.num_splits = plan.splits;
   a.split_chunk = plan.chunk;
   a.row_blocks = plan.row_blocks;
@@ -383,7 +383,10 @@ relattn_status run_decode(const relattn_params *p, const DecodePlan &plan, Kerne
   }
   cudaError_t e;
   switch (plan.kind) {
-    case DecodeKind::kKeys: e = launch_decode_few_rows(a, (int)kv_rows, s); break;
+    case DecodeKind::kKeys:
+      e = f8 ? launch_decode_mxfp8(a, f8->k, f8->v, f8->k_scale, f8->v_scale, (int)kv_rows, s)
+             : launch_decode_few_rows(a, (int)kv_rows, s);
+      break;
     case DecodeKind::kRows: e = launch_decode_tc(a, (int)kv_rows, s); break;
     default: e = launch_decode_mma(a, plan.warps, s); break;
   }
@@ -429,6 +432,37 @@ relattn_status relattn_decode_paged(const relattn_params *p, const relattn_paged
   a.max_pages = kv->max_pages_per_seq;
   a.num_pages = kv->num_pages;
   return run_decode(p, plan, a, pool_rows, static_cast<cudaStream_t>(stream));
+}
+
+relattn_status relattn_decode_mxfp8(const relattn_params *p, const relattn_kv_mxfp8 *kv, void *stream) {
+  if (!p || !kv) return RELATTN_ERR_INVALID_ARG;
+  // the code tensors stand in for k / v in the checks and the plan
+  relattn_params q = *p;
+  q.k = kv->k;
+  q.v = kv->v;
+  relattn_status st = validate(&q, true);
+  if (st != RELATTN_OK) return st;
+  if (q.batch == 0 || q.total_q == 0) return RELATTN_OK;
+  if (!kv->k_scale || !kv->v_scale) return RELATTN_ERR_INVALID_ARG;
+  DecodePlan plan;
+  if ((st = plan_decode(&q, &plan)) != RELATTN_OK) return st;
+  KernelArgs a;
+  if ((st = make_args(&q, &a)) != RELATTN_OK) return st;
+  if (plan.kind != DecodeKind::kKeys ||
+      !decode_mxfp8_supported(a, kv->k, kv->v, kv->k_scale, kv->v_scale, q.total_k))
+    return RELATTN_ERR_UNSUPPORTED;
+  return run_decode(&q, plan, a, q.total_k, static_cast<cudaStream_t>(stream), kv);
+}
+
+relattn_status relattn_quantize_mxfp8(const void *x, int64_t n_blocks, void *codes, void *scales,
+                                      void *stream) {
+  if (n_blocks < 0) return RELATTN_ERR_INVALID_ARG;
+  if (n_blocks == 0) return RELATTN_OK;
+  if (!x || !codes || !scales || !aligned16(x) || !aligned16(codes)) return RELATTN_ERR_INVALID_ARG;
+  if (overlaps(x, (size_t)n_blocks * 64, codes, (size_t)n_blocks * 32) ||
+      overlaps(x, (size_t)n_blocks * 64, scales, (size_t)n_blocks))
+    return RELATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_mxfp8(x, n_blocks, codes, scales, static_cast<cudaStream_t>(stream)));
 }
 
 relattn_status relattn_combine(const float *o_part, const float *lse_part, int32_t num_splits,

@@ -60,6 +60,7 @@
 #include <cudaTypedefs.h>
 
 #include "launch.h"
+#include "mxfp8.cuh"
 #include "tc_common.cuh"
 
 namespace relattn {
@@ -74,18 +75,8 @@ constexpr int NSTAGE = 3;                  // K and V ring stages
 constexpr int NTHR = 320;
 constexpr float kRescale = 8.f;            // log2 units
 
-constexpr uint32_t TM_S = 0, TM_O = 32;    // S^T / O^T of warpgroup b at + 16 b
-constexpr uint32_t TMEM_COLS = 64;
-
-constexpr uint32_t BOX = 16384;            // [64 dims x 128 rows] bf16, 128-byte rows, 128B swizzle
-constexpr uint32_t TILE = 2 * BOX;
-constexpr uint32_t HALF16 = NR * 128;      // [64 dims (or keys) x 16 rows]: 2 KB
-constexpr uint32_t SM_P = 0;                          // P of warpgroup b at + 4 KB b: halves keys 0-63, 64-127
-constexpr uint32_t SM_Q = SM_P + 4 * HALF16;          // q rows of item n at + 4 KB (n % 2): halves dims 0-63, 64-127
-constexpr uint32_t SM_K = SM_Q + 4 * HALF16;          // 1024-aligned
-constexpr uint32_t SM_V = SM_K + NSTAGE * TILE;
-constexpr uint32_t SM_MB = SM_V + NSTAGE * TILE;      // float [NR][128]: warpgroup 1's O^T; then m, l [NR] each
-constexpr uint32_t SM_WG = SM_MB + NR * 128 * 4 + 2 * NR * 4;
+constexpr uint32_t BOX = 16384;            // 128 rows of 128 bytes (64 bf16 dims or 128 fp8 dims), 128B swizzle
+constexpr uint32_t HALF16 = NR * 128;      // 16 rows of 128 bytes: 2 KB
 // per warpgroup: row constants and exchange buffers
 constexpr uint32_t WG_ROWC = 0;                       // float4 [NR]: scale, bias scale, position, output row
 constexpr uint32_t WG_RSC = WG_ROWC + NR * 16;        // float [NR]: the scales, packed
@@ -100,23 +91,53 @@ constexpr int kOrd = 64;
 constexpr int ORD_NF = 0, ORD_REM = kOrd, ORD_PF = 2 * kOrd, ORD_PZ = 3 * kOrd + 1,
               ORD_PTAB = 4 * kOrd + 2, ORD_NP = 5 * kOrd + 2, ORD_CQ = 5 * kOrd + 4,
               ORD_CK = 6 * kOrd + 5, ORD_INTS = 7 * kOrd + 6;
-constexpr uint32_t SM_ORD = SM_WG + 2 * WG_BYTES;
 enum {
   B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + 2, B_K_FULL = B_Q_EMPTY + 2, B_K_EMPTY = B_K_FULL + NSTAGE, B_V_FULL = B_K_EMPTY + NSTAGE,
   B_V_EMPTY = B_V_FULL + NSTAGE, B_S_FULL = B_V_EMPTY + NSTAGE, B_S_FREE = B_S_FULL + 2,
   B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2, B_XCH = B_PV_DONE + 2, B_M_FULL = B_XCH + 2,
   B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_COUNT = B_DRAIN + 1
 };
-constexpr uint32_t SM_BAR = SM_ORD + ORD_INTS * 4;
-constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
-constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
-constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
-constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;      // + alignment slack
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(SM_WG % 16 == 0 && WG_BYTES % 16 == 0, "float4 alignment");
+
+// Tensor- and shared-memory layout of the bf16 kernel (F8 = false) and of the
+// MXFP8 one (K / V stored as E4M3 codes with one E8M0 scale per 32 dims, q
+// quantised the same way per item, V dequantised to bf16 per tile).
+//   TMEM: S^T of warpgroup b at TM_S + SCOLS b (fp8: four 16-column blocks, one
+//   per 32 head dims, scaled in the softmax); O^T of warpgroup b at TM_O + 16 b.
+//   SMEM: the two P buffers (4 KB each), the q rows of two items (bf16: 4 KB,
+//   fp8: 2 KB each), K and V rings, (fp8) each warpgroup's bf16 V tile, the
+//   merge buffer, (fp8) the q scales of two items, per-warpgroup buffers, the
+//   work order, barriers.
+template <bool F8>
+struct Lay {
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t SCOLS = F8 ? 4 * NR : NR;
+  static constexpr uint32_t TM_O = 2 * SCOLS;
+  static constexpr uint32_t TMEM_COLS = F8 ? 256 : 64;
+  static constexpr uint32_t KTILE = F8 ? BOX : 2 * BOX;       // bytes of one K (or V) stage
+  static constexpr uint32_t QBUF = F8 ? HALF16 : 2 * HALF16;  // bytes of one item's q rows
+  static constexpr uint32_t SM_P = 0;
+  static constexpr uint32_t SM_Q = SM_P + 4 * HALF16;
+  static constexpr uint32_t SM_K = SM_Q + 4 * HALF16;
+  static constexpr uint32_t SM_V = SM_K + NSTAGE * KTILE;
+  static constexpr uint32_t SM_VB = SM_V + NSTAGE * KTILE;    // fp8: bf16 V of warpgroup b at + 2 BOX b
+  static constexpr uint32_t SM_MB = SM_VB + (F8 ? 4 * BOX : 0);   // float [NR][128]: warpgroup 1's O^T; m, l [NR]
+  static constexpr uint32_t SM_QSC = SM_MB + NR * 128 * 4 + 2 * NR * 4;  // fp8: float [2][NR][4]
+  static constexpr uint32_t SM_WG = SM_QSC + (F8 ? 2 * NR * 16 : 0);
+  static constexpr uint32_t SM_ORD = SM_WG + 2 * WG_BYTES;
+  static constexpr uint32_t SM_BAR = SM_ORD + ORD_INTS * 4;
+  static constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
+  static constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
+  static constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
+  static constexpr uint32_t SMEM_BYTES = SM_TOTAL + 1024;      // + alignment slack
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(SM_K % 1024 == 0 && SM_VB % 1024 == 0 && SM_WG % 16 == 0 && SM_QSC % 16 == 0,
+                "alignment");
+};
 
 struct DecArgs {
   KernelArgs a;
+  const uint32_t *kscale, *vscale;   // MXFP8: E8M0 scale bytes of each (row, kv head), 4 per word
+  int kv_rows;                       // rows of the K / V tensors
   int has_bias;
   int q_bytes;       // bytes of the item's q box pair
   int n_items;
@@ -151,19 +172,21 @@ struct Item {
   int b, g, sp, cq, ck, nrows, p0, p_last, kbeg, ntiles;
 };
 
+template <bool F8>
 __global__ void __launch_bounds__(NTHR, 1)
 relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
                          const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v) {
+  using L = Lay<F8>;
   const KernelArgs &a = da.a;
   extern __shared__ uint8_t smem_raw[];
   // 1024-aligned base, kept as an offset into the shared array so that every
   // access below stays a shared-memory access (32-bit addresses)
   uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_addr(smem);
-  auto bar = [&](int i) { return sb + SM_BAR + 8u * i; };
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + SM_ABORT);
+  auto bar = [&](int i) { return sb + L::SM_BAR + 8u * i; };
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::SM_ABORT);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ------------------------------------------------------------ work items
@@ -175,7 +198,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   // even out.  Every role derives the same order from the same tables.
   // Otherwise the plain order: pair = split * batch + sequence.
   Item I{};
-  int *ord = reinterpret_cast<int *>(smem + SM_ORD);
+  int *ord = reinterpret_cast<int *>(smem + L::SM_ORD);
   const bool sorted = a.batch <= kOrd;
   auto load_item = [&](int idx) -> int {   // 1 work, 0 nothing, -1 inconsistent lengths
     int q, u;
@@ -225,19 +248,19 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   // ------------------------------------------------------------ set-up
   // q and the P buffers start as zeros: rows past an item's real ones then
   // score 0 instead of whatever the memory held
-  for (int i = tid; i < (int)(SM_K - SM_P) / 16; i += NTHR)
-    *reinterpret_cast<uint4 *>(smem + SM_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = tid; i < (int)(L::SM_K - L::SM_P) / 16; i += NTHR)
+    *reinterpret_cast<uint4 *>(smem + L::SM_P + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_Q_FULL + i), 1);
-      mbar_init(bar(B_Q_EMPTY + i), 1);
+      mbar_init(bar(B_Q_EMPTY + i), F8 ? 1 + 256 : 1);   // fp8: + the softmax threads (q scales)
     }
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(bar(B_K_FULL + i), 1);
       mbar_init(bar(B_K_EMPTY + i), 1);
       mbar_init(bar(B_V_FULL + i), 1);
-      mbar_init(bar(B_V_EMPTY + i), 1);
+      mbar_init(bar(B_V_EMPTY + i), F8 ? 128 : 1);   // fp8: the dequantising warpgroup's threads
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_S_FULL + i), 1);
@@ -253,7 +276,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sb + SM_TMEM_SLOT, TMEM_COLS);
+    tmem_alloc(sb + L::SM_TMEM_SLOT, L::TMEM_COLS);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -314,13 +337,77 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     __syncthreads();
   }
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + SM_TMEM_SLOT);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::SM_TMEM_SLOT);
   // the producer's copies, drained if the CTA gives up
   int issued_q = 0, issued_k = 0, issued_v = 0;
 
   if (warp == 0) {
     // ====================================================== TMA producer
-    if (lane == 0) {
+    if constexpr (F8) {
+      // The whole warp quantises each item's q rows (MXFP8 per 32 dims) into
+      // the item's q buffer, with each (row, block) scale times the row's
+      // logit scale; lane 0 then streams the item's K / V code tiles.
+      int T = 0, n_it = 0;
+      bool run = true;
+      for (int idx = blockIdx.x; idx < n_items && run; idx += gridDim.x) {
+        const int li = load_item(idx);
+        if (li < 0 && lane == 0) atomicOr(a.err, kDevErrSeqlens);
+        if (li <= 0 || I.ntiles == 0) continue;
+        const int qb = n_it & 1;
+        if (n_it >= 2) {
+          bool okq = true;
+          if (lane == 0) okq = mbar_wait_suspend(bar(B_Q_EMPTY + qb), ((n_it >> 1) - 1) & 1, abort_flag, 1);
+          if (!__shfl_sync(0xffffffffu, okq ? 1 : 0, 0)) {
+            run = false;
+            break;
+          }
+        }
+        uint8_t *q8 = smem + L::SM_Q + qb * L::QBUF;
+        float *qsc = reinterpret_cast<float *>(smem + L::SM_QSC) + qb * NR * 4;
+        for (int pr = lane; pr < NR * 4; pr += 32) {
+          const int r = pr >> 2, blk = pr & 3;
+          uint32_t c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          float sc = 0.f;
+          if (r < I.nrows) {
+            const int tau = r / a.group, hg = r - tau * a.group;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                a.q + ((size_t)(I.cq + tau) * a.Hq + I.g * a.group + hg) * kHeadDim + 32 * blk);
+            int e;
+            quantize_block32(src, c, e);
+            sc = a.alpha_log2e * log_scale(I.p0 + tau, a.inv_ln_base) * pow2i(e);
+          }
+          // codes of dims 32 blk .. 32 blk + 31 of row r: 16-byte chunks 2 blk, 2 blk + 1
+          *reinterpret_cast<uint4 *>(q8 + r * 128 + (((2 * blk) ^ (r & 7)) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
+          *reinterpret_cast<uint4 *>(q8 + r * 128 + (((2 * blk + 1) ^ (r & 7)) << 4)) =
+              make_uint4(c[4], c[5], c[6], c[7]);
+          qsc[r * 4 + blk] = sc;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_Q_FULL + qb));
+        issued_q = n_it + 1;
+        if (lane == 0) {
+          for (int t = 0; t < I.ntiles && run; ++t) {
+            const int G = T + t, st = G % NSTAGE, use = G / NSTAGE;
+            const int row = I.ck + I.kbeg + KT * t;
+            if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
+            if (G != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
+              mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KTILE);
+              tma_load_3d(sb + L::SM_K + st * L::KTILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
+            }
+            issued_k = G + 1;
+            if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
+            mbar_arrive_expect_tx(bar(B_V_FULL + st), L::KTILE);
+            tma_load_3d(sb + L::SM_V + st * L::KTILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
+            issued_v = G + 1;
+          }
+        }
+        run = __shfl_sync(0xffffffffu, run ? 1 : 0, 0) != 0;
+        T += I.ntiles;
+        ++n_it;
+        if (*abort_flag) run = false;
+      }
+    } else if (lane == 0) {
       int T = 0, n_it = 0;
       bool run = true;
       for (int idx = blockIdx.x; idx < n_items && run; idx += gridDim.x) {
@@ -334,8 +421,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         if (n_it >= 2 && !(run = mbar_wait_suspend(bar(B_Q_EMPTY + qb), ((n_it >> 1) - 1) & 1, abort_flag, 1)))
           break;
         mbar_arrive_expect_tx(bar(B_Q_FULL + qb), (uint32_t)da.q_bytes);
-        tma_load_3d(sb + SM_Q + qb * 2 * HALF16, &map_q, 0, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
-        tma_load_3d(sb + SM_Q + qb * 2 * HALF16 + HALF16, &map_q, 64, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
+        tma_load_3d(sb + L::SM_Q + qb * L::QBUF, &map_q, 0, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
+        tma_load_3d(sb + L::SM_Q + qb * L::QBUF + HALF16, &map_q, 64, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
         issued_q = n_it + 1;
         // paged K / V: the pool row of a 128-aligned tile inside one page
         auto tile_row = [&](int t) -> int {
@@ -353,15 +440,15 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           const int row = tile_row(t);
           if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
           if (G != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
-            mbar_arrive_expect_tx(bar(B_K_FULL + st), TILE);
-            tma_load_3d(sb + SM_K + st * TILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
-            tma_load_3d(sb + SM_K + st * TILE + BOX, &map_k, 64, I.g, row, bar(B_K_FULL + st));
+            mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KTILE);
+            tma_load_3d(sb + L::SM_K + st * L::KTILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
+            tma_load_3d(sb + L::SM_K + st * L::KTILE + BOX, &map_k, 64, I.g, row, bar(B_K_FULL + st));
           }
           issued_k = G + 1;
           if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
-          mbar_arrive_expect_tx(bar(B_V_FULL + st), TILE);
-          tma_load_3d(sb + SM_V + st * TILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
-          tma_load_3d(sb + SM_V + st * TILE + BOX, &map_v, 64, I.g, row, bar(B_V_FULL + st));
+          mbar_arrive_expect_tx(bar(B_V_FULL + st), L::KTILE);
+          tma_load_3d(sb + L::SM_V + st * L::KTILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
+          tma_load_3d(sb + L::SM_V + st * L::KTILE + BOX, &map_v, 64, I.g, row, bar(B_V_FULL + st));
           issued_v = G + 1;
         }
         T += I.ntiles;
@@ -379,10 +466,13 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       // inside a 128-byte row, the second 64-wide half at +16 KB in a K tile
       // and at +2 KB in the 16-row q and P operands; V^T: dims along M in two
       // 64-dim boxes 16 KB apart, 16 keys (+2 KB) per k-step
-      const uint64_t qd0 = smem_desc_sw128(sb + SM_Q, 16, 1024);
-      const uint64_t kd0 = smem_desc_sw128(sb + SM_K, 16, 1024);
-      const uint64_t pd0 = smem_desc_sw128(sb + SM_P, 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(sb + SM_V, BOX, 1024);
+      const uint64_t qd0 = smem_desc_sw128(sb + L::SM_Q, 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(sb + L::SM_K, 16, 1024);
+      const uint64_t pd0 = smem_desc_sw128(sb + L::SM_P, 16, 1024);
+      // (fp8: the warpgroup's dequantised bf16 V tile; the K codes hold all 128 dims
+      // in one 128-byte row, 32 dims per E4M3 k-step)
+      const uint64_t vd0 = smem_desc_sw128(sb + (F8 ? L::SM_VB : L::SM_V), BOX, 1024);
+      const uint32_t id_s8 = idesc_e4m3_f32(KT, NR);
       auto koff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (BOX >> 4) + 2 * (k - 4)); };
       auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
       int T = 0, n_it = 0;
@@ -391,34 +481,42 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       auto issue_pv = [&](int G, bool first) -> bool {
         const int st = G % NSTAGE, b = G & 1;
         if (!mbar_wait(bar(B_P_FULL + b), (G >> 1) & 1, abort_flag, 4)) return false;
-        if (!mbar_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, abort_flag, 5)) return false;
+        // (fp8: P_FULL also says the warpgroup's bf16 V tile is written)
+        if (!F8 && !mbar_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, abort_flag, 5)) return false;
         tc_fence_after();
-        const uint64_t vd = vd0 + (uint64_t)((st * TILE) >> 4);
+        const uint64_t vd = vd0 + (uint64_t)(((F8 ? b * 2 * BOX : st * L::KTILE)) >> 4);
         const uint64_t pd = pd0 + (uint64_t)((b * 2 * HALF16) >> 4);
-        const uint32_t o = tmem + TM_O + 16u * (uint32_t)b;
+        const uint32_t o = tmem + L::TM_O + 16u * (uint32_t)b;
         if (first) mma_ss_c<0>(o, vd + 0, pd + hoff(0), id_o);
         else mma_ss_c<1>(o, vd + 0, pd + hoff(0), id_o);
 #pragma unroll
         for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, vd + 128 * k, pd + hoff(k), id_o);
         mma_commit(bar(B_PV_DONE + b));
-        mma_commit(bar(B_V_EMPTY + st));
+        if (!F8) mma_commit(bar(B_V_EMPTY + st));
         return true;
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         const int qb = n_it & 1;
         if (!(ok = mbar_wait(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
-        const uint64_t qd = qd0 + (uint64_t)((qb * 2 * HALF16) >> 4);
+        const uint64_t qd = qd0 + (uint64_t)((qb * L::QBUF) >> 4);
         for (int t = 0; t < I.ntiles && ok; ++t) {
           const int G = T + t, b = G & 1, st = G % NSTAGE;
           if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
           if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / NSTAGE) & 1, abort_flag, 8))) break;
           tc_fence_after();
-          const uint64_t kd = kd0 + (uint64_t)((st * TILE) >> 4);
-          const uint32_t d = tmem + TM_S + 16u * (uint32_t)b;
-          mma_ss_c<0>(d, kd + koff(0), qd + hoff(0), id_s);
+          const uint64_t kd = kd0 + (uint64_t)((st * L::KTILE) >> 4);
+          const uint32_t d = tmem + L::TM_S + L::SCOLS * (uint32_t)b;
+          if constexpr (F8) {
+            // one product per 32-dim block, each into its own 16 columns (the
+            // block scales differ, so the softmax combines them)
 #pragma unroll
-          for (int k = 1; k < 8; ++k) mma_ss_c<1>(d, kd + koff(k), qd + hoff(k), id_s);
+            for (int k = 0; k < 4; ++k) mma_f8_c<0>(d + 16u * k, kd + 2 * k, qd + 2 * k, id_s8);
+          } else {
+            mma_ss_c<0>(d, kd + koff(0), qd + hoff(0), id_s);
+#pragma unroll
+            for (int k = 1; k < 8; ++k) mma_ss_c<1>(d, kd + koff(k), qd + hoff(k), id_s);
+          }
           mma_commit(bar(B_S_FULL + b));
           mma_commit(bar(B_K_EMPTY + st));
           if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY + qb));   // the item's q rows are read
@@ -442,17 +540,17 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
     const bool row_owner = wq == 0;              // lanes 0..15 of this warp: rows 0..15
     const int r_own = lane & (NR - 1);           // the row this lane decides (lanes 16-31 repeat)
-    uint8_t *wgs = smem + SM_WG + wg * WG_BYTES;
+    uint8_t *wgs = smem + L::SM_WG + wg * WG_BYTES;
     float4 *rowc = reinterpret_cast<float4 *>(wgs + WG_ROWC);
     float *rsc = reinterpret_cast<float *>(wgs + WG_RSC);
     float *mref = reinterpret_cast<float *>(wgs + WG_MREF);
     float *xmax = reinterpret_cast<float *>(wgs + WG_XMAX);
     float *aux = reinterpret_cast<float *>(wgs + WG_AUX);
-    float *mbuf = reinterpret_cast<float *>(smem + SM_MB);          // [NR][128]
+    float *mbuf = reinterpret_cast<float *>(smem + L::SM_MB);          // [NR][128]
     float *mbuf_m = mbuf + NR * 128, *mbuf_l = mbuf_m + NR;
-    const uint32_t s_col = tmem + lane_base + TM_S + 16u * (uint32_t)wg;
-    const uint32_t o_col = tmem + lane_base + TM_O + 16u * (uint32_t)wg;
-    const uint32_t p_buf = SM_P + (uint32_t)wg * 2 * HALF16;
+    const uint32_t s_col = tmem + lane_base + L::TM_S + L::SCOLS * (uint32_t)wg;
+    const uint32_t o_col = tmem + lane_base + L::TM_O + 16u * (uint32_t)wg;
+    const uint32_t p_buf = L::SM_P + (uint32_t)wg * 2 * HALF16;
     const bool has_bias = da.has_bias != 0;
     const bool partial = a.num_splits > 1;
     auto warp_wait = [&](uint32_t br, uint32_t parity, int site) -> bool {
@@ -522,10 +620,41 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
             rbias[i] = in ? rv * rc.y : 0.f;
           }
         }
+        // fp8: this key's K and V block scales (4 E8M0 bytes each; rows past
+        // the tensor, which the copies fill with zeros, take 2^0)
+        uint32_t ksw = 0x7F7F7F7Fu, vsw = 0x7F7F7F7Fu;
+        if constexpr (F8) {
+          const int kr = I.ck + j;
+          if (kr < da.kv_rows) {
+            ksw = da.kscale[(size_t)kr * a.Hkv + I.g];
+            vsw = da.vscale[(size_t)kr * a.Hkv + I.g];
+          }
+        }
         if (!(ok = warp_wait(bar(B_S_FULL + wg), (G >> 1) & 1, 12))) break;
         tc_fence_after();
         float y[NR];
-        {
+        if constexpr (F8) {
+          // S^T of the four 32-dim blocks; y = sum_b S_b * (row scale x q block
+          // scale) * k block scale
+          const float kf0 = pow2i((int)(ksw & 0xFFu) - 127), kf1 = pow2i((int)((ksw >> 8) & 0xFFu) - 127);
+          const float kf2 = pow2i((int)((ksw >> 16) & 0xFFu) - 127), kf3 = pow2i((int)(ksw >> 24) - 127);
+          const float4 *qs4 = reinterpret_cast<const float4 *>(smem + L::SM_QSC) + (n_merge & 1) * NR;
+          uint32_t r[32];
+          tmem_ld32(s_col, r);   // blocks 0 and 1
+          tmem_wait_ld(r);
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float4 qs = qs4[i];
+            y[i] = fmaf(__uint_as_float(r[16 + i]), qs.y * kf1, __uint_as_float(r[i]) * (qs.x * kf0));
+          }
+          tmem_ld32(s_col + 32, r);   // blocks 2 and 3
+          tmem_wait_ld(r);
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float4 qs = qs4[i];
+            y[i] = fmaf(__uint_as_float(r[16 + i]), qs.w * kf3, fmaf(__uint_as_float(r[i]), qs.z * kf2, y[i]));
+          }
+        } else {
           uint32_t r[16];
           tmem_ld16(s_col, r);
           tmem_wait_ld(r);
@@ -535,7 +664,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         tc_fence_before();
         mbar_arrive(bar(B_S_FREE + wg));          // this thread has read S^T(G)
         // scale (packed row scales: 4 broadcast vector loads), bias, masks
-        {
+        if constexpr (!F8) {
           const float4 *sc4 = reinterpret_cast<const float4 *>(rsc);
 #pragma unroll
           for (int q4 = 0; q4 < NR / 4; ++q4) {
@@ -609,6 +738,30 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
             r[i] = __float_as_uint(__uint_as_float(r[i]) * __shfl_sync(0xffffffffu, corr, i));
           tmem_st16(o_col, r);
           tmem_wait_st();
+        }
+        if constexpr (F8) {
+          // this key's V codes (one 128-byte row of the stage) dequantised into
+          // the warpgroup's bf16 V tile: dims 0-63 in the first 128-byte-swizzled
+          // box, 64-127 in the second; then the stage is free for the next copy
+          const int st = G % NSTAGE;
+          if (!(ok = warp_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, 19))) break;
+          const uint8_t *v8 = smem + L::SM_V + st * L::KTILE + key * 128;
+          uint8_t *vb = smem + L::SM_VB + wg * 2 * BOX + key * 128;
+          const uint32_t sw = (uint32_t)(key & 7);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {   // 16 dims per 16-byte chunk of codes
+            const uint4 w = *reinterpret_cast<const uint4 *>(v8 + ((c ^ sw) << 4));
+            const float s = pow2i((int)((vsw >> (8 * (c >> 1))) & 0xFFu) - 127);
+            uint32_t o[8];
+            dequant4_bf16(w.x, s, o[0], o[1]);
+            dequant4_bf16(w.y, s, o[2], o[3]);
+            dequant4_bf16(w.z, s, o[4], o[5]);
+            dequant4_bf16(w.w, s, o[6], o[7]);
+            uint8_t *box = vb + (c >> 2) * BOX;
+            *reinterpret_cast<uint4 *>(box + ((((2 * c) & 7) ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(box + ((((2 * c + 1) & 7) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          mbar_arrive(bar(B_V_EMPTY + st));
         }
         // P[row][key] (bf16) into the 128-byte-swizzled K-major B operand:
         // keys 0-63 in the first 2 KB half, 64-127 in the second
@@ -702,6 +855,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           }
         }
       }
+      if constexpr (F8) mbar_arrive(bar(B_Q_EMPTY + (n_merge & 1)));   // the item's q scales are read
       ++n_merge;
       T += I.ntiles;
     }
@@ -726,7 +880,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
 
@@ -825,6 +979,16 @@ bool decode_few_rows_supported(const KernelArgs &a, int kv_rows) {
   return kv_rows >= KT;                    // K / V boxes of 128 rows
 }
 
+bool decode_mxfp8_supported(const KernelArgs &a, const void *k8, const void *v8, const void *ks,
+                            const void *vs, int kv_rows) {
+  auto al = [](const void *p, uintptr_t n) { return p && (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; };
+  if (!dec_encoder()) return false;
+  if (!al(a.q, 16) || !al(a.out, 16) || !al(k8, 16) || !al(v8, 16) || !al(ks, 4) || !al(vs, 4)) return false;
+  if (a.group <= 0 || a.max_q <= 0 || (long)a.group * a.max_q > NR) return false;
+  if (a.rd > 64 || a.block_table != nullptr) return false;
+  return kv_rows >= KT;
+}
+
 size_t decode_rel_bytes(const KernelArgs &a) {
   if (!(a.rd > 0 && a.E > 0)) return 0;
   return (size_t)a.total_q * a.Hq * a.E * sizeof(float);
@@ -833,6 +997,8 @@ size_t decode_rel_bytes(const KernelArgs &a) {
 cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_t stream) {
   DecArgs da;
   da.a = a;
+  da.kscale = da.vscale = nullptr;
+  da.kv_rows = kv_rows;
   da.has_bias = a.rd > 0 && a.E > 0 && a.rdec != nullptr;
   da.q_bytes = 2 * 64 * 2 * a.group * a.max_q;
   const long items = (long)a.num_splits * a.batch * a.Hkv;
@@ -852,11 +1018,58 @@ cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_
       !encode_heads(&mk, a.k, a.Hkv, kv_rows, 1, KT) || !encode_heads(&mv, a.v, a.Hkv, kv_rows, 1, KT))
     return cudaErrorInvalidValue;
   static std::atomic<bool> attr_set[kMaxDevicesAttr];
-  cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel),
-                                    (int)SMEM_BYTES, attr_set);
+  constexpr uint32_t smem = Lay<false>::SMEM_BYTES;
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<false>),
+                                    (int)smem, attr_set);
   if (e != cudaSuccess) return e;
   const int grid = (int)std::min<long>(items, a.sms > 0 ? a.sms : items);
-  relattn_decode_tc_kernel<<<grid, NTHR, SMEM_BYTES, stream>>>(da, mq, mk, mv);
+  relattn_decode_tc_kernel<false><<<grid, NTHR, smem, stream>>>(da, mq, mk, mv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void *v8, const void *ks,
+                                const void *vs, int kv_rows, cudaStream_t stream) {
+  DecArgs da;
+  da.a = a;
+  da.kscale = static_cast<const uint32_t *>(ks);
+  da.vscale = static_cast<const uint32_t *>(vs);
+  da.kv_rows = kv_rows;
+  da.has_bias = a.rd > 0 && a.E > 0 && a.rdec != nullptr;
+  da.q_bytes = 0;
+  const long items = (long)a.num_splits * a.batch * a.Hkv;
+  if (items <= 0) return cudaSuccess;
+  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
+  da.n_items = (int)items;
+  if (da.has_bias) {
+    const long rrows = (long)a.total_q * a.Hq;
+    dim3 g((unsigned)((rrows + RR - 1) / RR), (unsigned)((a.E + RD - 1) / RD));
+    relattn_decode_rel_kernel<<<g, RD, 0, stream>>>(a, const_cast<float *>(a.rdec));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // E4M3 codes [rows, heads, 128] in boxes of 128 dims x 1 head x 128 rows
+  auto encode_codes = [](CUtensorMap *m, const void *base, int heads, int rows) {
+    auto fn = dec_encoder();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {128, (cuuint64_t)heads * 128};
+    cuuint32_t box[3] = {128, 1, (cuuint32_t)KT};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  CUtensorMap mk, mv;
+  if (!encode_codes(&mk, k8, a.Hkv, kv_rows) || !encode_codes(&mv, v8, a.Hkv, kv_rows))
+    return cudaErrorInvalidValue;
+  static std::atomic<bool> attr_set[kMaxDevicesAttr];
+  constexpr uint32_t smem = Lay<true>::SMEM_BYTES;
+  cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<true>),
+                                    (int)smem, attr_set);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<long>(items, a.sms > 0 ? a.sms : items);
+  // (the q map is not read: the producer quantises q rows itself)
+  relattn_decode_tc_kernel<true><<<grid, NTHR, smem, stream>>>(da, mk, mk, mv);
   return cudaGetLastError();
 }
 

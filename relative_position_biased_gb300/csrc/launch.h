@@ -86,6 +86,19 @@ constexpr int kFewRows = 16;
 bool decode_few_rows_supported(const KernelArgs &a, int kv_rows);
 size_t decode_rel_bytes(const KernelArgs &a);
 cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_t stream);
+// The same decode on an MXFP8 K / V cache (decode_tc.cu): E4M3 codes k8 / v8
+// [kv_rows, Hkv, 128] (16-byte aligned) with E8M0 scales ks / vs [kv_rows,
+// Hkv, 4] (4-byte aligned); q quantised per item in the kernel, Q K^T as an
+// E4M3 product per 32-dim block, V dequantised to bf16 for P V.  Contiguous
+// K / V only.
+bool decode_mxfp8_supported(const KernelArgs &a, const void *k8, const void *v8, const void *ks,
+                            const void *vs, int kv_rows);
+cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void *v8, const void *ks,
+                                const void *vs, int kv_rows, cudaStream_t stream);
+// MXFP8 quantisation (mxfp8.cu): n_blocks blocks of 32 bf16 (x 16-byte
+// aligned) -> 32 E4M3 codes (16-byte aligned) and one E8M0 scale byte each.
+cudaError_t launch_quantize_mxfp8(const void *x, long n_blocks, void *codes, void *scales,
+                                  cudaStream_t stream);
 cudaError_t launch_decode_mma(const KernelArgs &a, int warps, cudaStream_t stream);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits,
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,

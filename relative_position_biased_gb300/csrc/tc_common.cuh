@@ -346,6 +346,23 @@ __device__ __forceinline__ void mma_ss_c(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// Instruction descriptor, kind::f8f6f4: E4M3 x E4M3 -> fp32, dense, both
+// operands K-major (A / B format fields 0 = E4M3).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                        // D format: fp32
+         | ((uint32_t)(N >> 3) << 17)     // N / 8
+         | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+// D[tmem] (+)= A[smem] * B[smem], 8-bit operands (K = 32 per instruction)
+template <int ACC>
+__device__ __forceinline__ void mma_f8_c(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 // Copy 128 rows x 32 bytes from shared memory (matrix descriptor, the same
 // format as an MMA operand's) into TMEM lanes 0..127, 8 columns from taddr.

@@ -394,7 +394,7 @@ relattn_status run_decode(const relattn_params *p, const DecodePlan &plan, Kerne
   if (st != RELATTN_OK) return st;
   if (plan.splits > 1)
     st = cuda_status(launch_combine(a.o_part, a.lse_part, plan.splits, p->total_q,
-                                    p->num_heads_q, a.out, a.lse, s));
+                                    p->num_heads_q, a.out, a.lse, s, plan.kind == DecodeKind::kKeys));
   return st;
 }
 

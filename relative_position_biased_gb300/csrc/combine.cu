@@ -27,6 +27,9 @@ relattn_combine_kernel(const float *__restrict__ o_part, const float *__restrict
   __shared__ float4 red_acc[kWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rsub = warp / RW, wi = warp % RW;
+  // launched as a programmatic dependent of the split kernel: its partials
+  // are complete and visible past this point (a plain launch returns at once)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long rows = (long)total_q * num_heads;
   const long row = (long)blockIdx.x * kRowsPerCta + rsub;
   const bool active = row < rows;
@@ -90,25 +93,33 @@ relattn_combine_kernel(const float *__restrict__ o_part, const float *__restrict
 
 template <int RW>
 cudaError_t launch_rw(const float *o_part, const float *lse_part, int num_splits, int total_q,
-                      int num_heads, __nv_bfloat16 *out, float *lse, cudaStream_t stream) {
+                      int num_heads, __nv_bfloat16 *out, float *lse, cudaStream_t stream, bool pdl) {
   constexpr int kRowsPerCta = kCombineThreads / 32 / RW;
   const long rows = (long)total_q * num_heads;
   const unsigned blocks = (unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta);
-  relattn_combine_kernel<RW><<<blocks, kCombineThreads, 0, stream>>>(o_part, lse_part, num_splits,
-                                                                     total_q, num_heads, out, lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, relattn_combine_kernel<RW>, o_part, lse_part, num_splits, total_q,
+                            num_heads, out, lse);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits, int total_q,
-                           int num_heads, __nv_bfloat16 *out, float *lse, cudaStream_t stream) {
+                           int num_heads, __nv_bfloat16 *out, float *lse, cudaStream_t stream, bool pdl) {
   const long rows = (long)total_q * num_heads;
   if (rows == 0) return cudaSuccess;
-  if (num_splits >= 64) return launch_rw<8>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream);
-  if (num_splits >= 16) return launch_rw<4>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream);
-  if (num_splits >= 4) return launch_rw<2>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream);
-  return launch_rw<1>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream);
+  if (num_splits >= 64) return launch_rw<8>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream, pdl);
+  if (num_splits >= 16) return launch_rw<4>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream, pdl);
+  if (num_splits >= 4) return launch_rw<2>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream, pdl);
+  return launch_rw<1>(o_part, lse_part, num_splits, total_q, num_heads, out, lse, stream, pdl);
 }
 
 }  // namespace relattn

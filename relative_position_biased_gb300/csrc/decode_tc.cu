@@ -38,12 +38,14 @@
 // row), all sixteen loads issued before any is used.  No sheared tensor, no
 // TMEM ring, so any r_dim <= 64 and any E work.
 //
-// Warps (10; one CTA per SM walking items in a longest-first order):
+// Warps (11; one CTA per SM walking items in a longest-first order):
 //   warp 0      TMA producer (one thread): the item's q rows (a box of group
-//               heads x tokens), then K and V tiles (3-stage rings); the
+//               heads x tokens), then K and V tiles (rings of 2-4 stages); the
 //               rings run on across items
-//   warp 1      TMEM allocator, MMA issuer (one thread): S^T(G) into the
-//               buffer of warpgroup G % 2, then O^T += V^T P^T of tile G - 1
+//   warp 1      TMEM allocator, score MMA issuer (one thread): S^T(G) into
+//               the buffer of warpgroup G % 2
+//   warp 10     P V MMA issuer (one thread): O^T += V^T P^T of tile G into
+//               warpgroup G % 2's accumulator once its P is written
 //   warps 2-5   softmax warpgroup 0 (even tiles), warps 6-9 warpgroup 1 (odd
 //               tiles): thread = key of the tile (TMEM lane 32 (warp % 4) +
 //               lane) for the scores, = dim of O^T for the rescale and merge
@@ -51,7 +53,7 @@
 // Tensor memory (64 columns): S^T of warpgroup b at 16 b, O^T of warpgroup b
 // at 32 + 16 b.  Shared memory: the two P buffers (16 rows x 128 keys, 4 KB
 // each), the q rows of two items (4 KB each: the next item's load while the
-// current one runs), K and V rings (3 x 32 KB each), the merge buffer
+// current one runs), K and V rings, the merge buffer
 // (warpgroup 1's O^T, 8 KB), per-warpgroup row constants and exchange buffers.
 //
 // Every wait is bounded; a timeout raises the CTA's abort flag and records the
@@ -71,8 +73,9 @@ using namespace tc;
 constexpr int KT = 128;                    // keys per tile (TMEM lanes of S^T)
 constexpr int NR = kFewRows;               // rows per item at most (the MMAs' N)
 static_assert(NR == 16, "one 16-column chunk of S^T");
-constexpr int NSTAGE = 3;                  // K and V ring stages
-constexpr int NTHR = 320;
+constexpr int MAXST = 4;                   // K or V ring stages at most (the layouts pick their own)
+constexpr int NTHR = 352;                  // 11 warps (roles below)
+constexpr int PV_WARP = 10;
 constexpr float kRescale = 8.f;            // log2 units
 
 constexpr uint32_t BOX = 16384;            // 128 rows of 128 bytes (64 bf16 dims or 128 fp8 dims), 128B swizzle
@@ -92,10 +95,10 @@ constexpr int ORD_NF = 0, ORD_REM = kOrd, ORD_PF = 2 * kOrd, ORD_PZ = 3 * kOrd +
               ORD_PTAB = 4 * kOrd + 2, ORD_NP = 5 * kOrd + 2, ORD_CQ = 5 * kOrd + 4,
               ORD_CK = 6 * kOrd + 5, ORD_INTS = 7 * kOrd + 6;
 enum {
-  B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + 2, B_K_FULL = B_Q_EMPTY + 2, B_K_EMPTY = B_K_FULL + NSTAGE, B_V_FULL = B_K_EMPTY + NSTAGE,
-  B_V_EMPTY = B_V_FULL + NSTAGE, B_S_FULL = B_V_EMPTY + NSTAGE, B_S_FREE = B_S_FULL + 2,
+  B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + 2, B_K_FULL = B_Q_EMPTY + 2, B_K_EMPTY = B_K_FULL + MAXST, B_V_FULL = B_K_EMPTY + MAXST,
+  B_V_EMPTY = B_V_FULL + MAXST, B_S_FULL = B_V_EMPTY + MAXST, B_S_FREE = B_S_FULL + 2,
   B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2, B_XCH = B_PV_DONE + 2, B_M_FULL = B_XCH + 2,
-  B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_COUNT = B_DRAIN + 1
+  B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_DRAIN_PV = B_DRAIN + 1, B_COUNT = B_DRAIN_PV + 1
 };
 
 // Tensor- and shared-memory layout of the bf16 kernel (F8 = false) and of the
@@ -118,8 +121,13 @@ struct Lay {
   static constexpr uint32_t SM_P = 0;
   static constexpr uint32_t SM_Q = SM_P + 4 * HALF16;
   static constexpr uint32_t SM_K = SM_Q + 4 * HALF16;
-  static constexpr uint32_t SM_V = SM_K + NSTAGE * KTILE;
-  static constexpr uint32_t SM_VB = SM_V + NSTAGE * KTILE;    // fp8: bf16 V of warpgroup b at + 2 BOX b
+  // ring stages: K is released right after its score MMA, V only after its
+  // P V MMA (bf16) or its dequantisation (fp8), so V holds its stages longer
+  // and gets more of them; at the loaded memory's ~2.5 us latency the bytes in
+  // flight, not the bandwidth, set the pace
+  static constexpr int KST = F8 ? 4 : 2, VST = 4;
+  static constexpr uint32_t SM_V = SM_K + KST * KTILE;
+  static constexpr uint32_t SM_VB = SM_V + VST * KTILE;       // fp8: bf16 V of warpgroup b at + 2 BOX b
   static constexpr uint32_t SM_MB = SM_VB + (F8 ? 4 * BOX : 0);   // float [NR][128]: warpgroup 1's O^T; m, l [NR]
   static constexpr uint32_t SM_QSC = SM_MB + NR * 128 * 4 + 2 * NR * 4;  // fp8: float [2][NR][4]
   static constexpr uint32_t SM_WG = SM_QSC + (F8 ? 2 * NR * 16 : 0);
@@ -200,7 +208,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   Item I{};
   int *ord = reinterpret_cast<int *>(smem + L::SM_ORD);
   const bool sorted = a.batch <= kOrd;
-  auto load_item = [&](int idx) -> int {   // 1 work, 0 nothing, -1 inconsistent lengths
+  auto load_item_into = [&](int idx, Item &it) -> int {   // 1 work, 0 nothing, -1 inconsistent lengths
     int q, u;
     if (sorted) {
       const int Gd = gridDim.x, r = idx / Gd, c = idx - r * Gd;
@@ -212,37 +220,38 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         const int base = q < F ? ORD_PF : ORD_PZ, qq = q < F ? q : q - F - NP;
         int b = 0;                                       // last b with prefix[b] <= qq
         for (int i = 1; i < a.batch; ++i) b = ord[base + i] <= qq ? i : b;
-        I.b = b;
-        I.sp = q < F ? qq - ord[ORD_PF + b]
+        it.b = b;
+        it.sp = q < F ? qq - ord[ORD_PF + b]
                      : ord[ORD_NF + b] + (ord[ORD_REM + b] > 0 ? 1 : 0) + (qq - ord[ORD_PZ + b]);
       } else {
-        I.b = ord[ORD_PTAB + (q - F)];
-        I.sp = ord[ORD_NF + I.b];
+        it.b = ord[ORD_PTAB + (q - F)];
+        it.sp = ord[ORD_NF + it.b];
       }
     } else {
       q = idx / a.Hkv;
       u = idx - q * a.Hkv;
-      I.b = q % a.batch;
-      I.sp = q / a.batch;
+      it.b = q % a.batch;
+      it.sp = q / a.batch;
     }
-    I.g = u;
+    it.g = u;
     const int *cq_t = sorted ? ord + ORD_CQ : a.cu_q, *ck_t = sorted ? ord + ORD_CK : a.cu_k;
-    I.cq = cq_t[I.b];
-    I.ck = ck_t[I.b];
-    const int Lq = cq_t[I.b + 1] - I.cq, Lk = ck_t[I.b + 1] - I.ck;
+    it.cq = cq_t[it.b];
+    it.ck = ck_t[it.b];
+    const int Lq = cq_t[it.b + 1] - it.cq, Lk = ck_t[it.b + 1] - it.ck;
     // (rows past total_q would index outputs and R out of bounds)
-    if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k || I.cq < 0 || I.cq + Lq > a.total_q) return -1;
+    if (Lq < 0 || Lk < Lq || Lq > a.max_q || Lk > a.max_k || it.cq < 0 || it.cq + Lq > a.total_q) return -1;
     if (Lq == 0) return 0;
-    I.nrows = Lq * a.group;
-    I.p0 = Lk - Lq;
-    I.p_last = I.p0 + Lq - 1;
-    const int j_lo = a.window > 0 ? max(0, I.p0 - a.window + 1) : 0;
+    it.nrows = Lq * a.group;
+    it.p0 = Lk - Lq;
+    it.p_last = it.p0 + Lq - 1;
+    const int j_lo = a.window > 0 ? max(0, it.p0 - a.window + 1) : 0;
     const int kbase = j_lo & ~(KT - 1);
-    I.kbeg = kbase + I.sp * a.split_chunk;
-    const int kend = min(I.p_last + 1, I.kbeg + a.split_chunk);
-    I.ntiles = kend > I.kbeg ? (kend - I.kbeg + KT - 1) / KT : 0;
+    it.kbeg = kbase + it.sp * a.split_chunk;
+    const int kend = min(it.p_last + 1, it.kbeg + a.split_chunk);
+    it.ntiles = kend > it.kbeg ? (kend - it.kbeg + KT - 1) / KT : 0;
     return 1;
   };
+  auto load_item = [&](int idx) -> int { return load_item_into(idx, I); };
   const int n_items = da.n_items;
 
   // ------------------------------------------------------------ set-up
@@ -256,7 +265,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       mbar_init(bar(B_Q_FULL + i), 1);
       mbar_init(bar(B_Q_EMPTY + i), F8 ? 1 + 256 : 1);   // fp8: + the softmax threads (q scales)
     }
-    for (int i = 0; i < NSTAGE; ++i) {
+    for (int i = 0; i < MAXST; ++i) {
       mbar_init(bar(B_K_FULL + i), 1);
       mbar_init(bar(B_K_EMPTY + i), 1);
       mbar_init(bar(B_V_FULL + i), 1);
@@ -272,6 +281,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     mbar_init(bar(B_M_FULL), 128);
     mbar_init(bar(B_M_FREE), 128);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN_PV), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -338,172 +348,172 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   }
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::SM_TMEM_SLOT);
+  // the combine after this kernel may launch (it waits for every CTA's partials)
+  asm volatile("griddepcontrol.launch_dependents;");
   // the producer's copies, drained if the CTA gives up
   int issued_q = 0, issued_k = 0, issued_v = 0;
 
   if (warp == 0) {
     // ====================================================== TMA producer
-    if constexpr (F8) {
-      // The whole warp quantises each item's q rows (MXFP8 per 32 dims) into
-      // the item's q buffer, with each (row, block) scale times the row's
-      // logit scale; lane 0 then streams the item's K / V code tiles.
-      int T = 0, n_it = 0;
-      bool run = true;
-      for (int idx = blockIdx.x; idx < n_items && run; idx += gridDim.x) {
-        const int li = load_item(idx);
-        if (li < 0 && lane == 0) atomicOr(a.err, kDevErrSeqlens);
-        if (li <= 0 || I.ntiles == 0) continue;
-        const int qb = n_it & 1;
-        if (n_it >= 2) {
-          bool okq = true;
-          if (lane == 0) okq = mbar_wait_suspend(bar(B_Q_EMPTY + qb), ((n_it >> 1) - 1) & 1, abort_flag, 1);
-          if (!__shfl_sync(0xffffffffu, okq ? 1 : 0, 0)) {
-            run = false;
-            break;
-          }
-        }
-        uint8_t *q8 = smem + L::SM_Q + qb * L::QBUF;
-        float *qsc = reinterpret_cast<float *>(smem + L::SM_QSC) + qb * NR * 4;
-        for (int pr = lane; pr < NR * 4; pr += 32) {
-          const int r = pr >> 2, blk = pr & 3;
-          uint32_t c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-          float sc = 0.f;
-          if (r < I.nrows) {
-            const int tau = r / a.group, hg = r - tau * a.group;
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                a.q + ((size_t)(I.cq + tau) * a.Hq + I.g * a.group + hg) * kHeadDim + 32 * blk);
-            int e;
-            quantize_block32(src, c, e);
-            sc = a.alpha_log2e * log_scale(I.p0 + tau, a.inv_ln_base) * pow2i(e);
-          }
-          // codes of dims 32 blk .. 32 blk + 31 of row r: 16-byte chunks 2 blk, 2 blk + 1
-          *reinterpret_cast<uint4 *>(q8 + r * 128 + (((2 * blk) ^ (r & 7)) << 4)) = make_uint4(c[0], c[1], c[2], c[3]);
-          *reinterpret_cast<uint4 *>(q8 + r * 128 + (((2 * blk + 1) ^ (r & 7)) << 4)) =
-              make_uint4(c[4], c[5], c[6], c[7]);
-          qsc[r * 4 + blk] = sc;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_Q_FULL + qb));
-        issued_q = n_it + 1;
-        if (lane == 0) {
-          for (int t = 0; t < I.ntiles && run; ++t) {
-            const int G = T + t, st = G % NSTAGE, use = G / NSTAGE;
-            const int row = I.ck + I.kbeg + KT * t;
-            if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
-            if (G != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
-              mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KTILE);
-              tma_load_3d(sb + L::SM_K + st * L::KTILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
-            }
-            issued_k = G + 1;
-            if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
-            mbar_arrive_expect_tx(bar(B_V_FULL + st), L::KTILE);
-            tma_load_3d(sb + L::SM_V + st * L::KTILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
-            issued_v = G + 1;
-          }
-        }
-        run = __shfl_sync(0xffffffffu, run ? 1 : 0, 0) != 0;
-        T += I.ntiles;
-        ++n_it;
-        if (*abort_flag) run = false;
+    // Two cursors over the CTA's tiles: the K copies run ahead as soon as a K
+    // stage is free (after its score MMA), the V copies as soon as a V stage
+    // is (after its P V MMA, or for fp8 after its dequantisation), so a late V
+    // stage never holds back the next K tile.  Each item's q rows go first
+    // (bf16: a TMA box; fp8: the whole warp quantises them).  The loop is
+    // warp-uniform: lane 0 probes the barriers and issues the copies, the
+    // decisions are broadcast.
+    Item ik{}, iv{};
+    int kidx = (int)blockIdx.x - (int)gridDim.x, vidx = kidx, kt = 0, vt = 0;
+    int GK = 0, GV = 0, n_q = 0;
+    auto next_item = [&](int &idx, Item &it) -> bool {
+      for (idx += gridDim.x; idx < n_items; idx += gridDim.x) {
+        const int li = load_item_into(idx, it);
+        if (li < 0 && lane == 0 && &it == &ik) atomicOr(a.err, kDevErrSeqlens);
+        if (li > 0 && it.ntiles > 0) return true;
       }
-    } else if (lane == 0) {
-      int T = 0, n_it = 0;
-      bool run = true;
-      for (int idx = blockIdx.x; idx < n_items && run; idx += gridDim.x) {
-        const int li = load_item(idx);
-        if (li < 0) atomicOr(a.err, kDevErrSeqlens);
-        if (li <= 0 || I.ntiles == 0) continue;
-        // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves
-        // of 64 dims, in the buffer of the item's parity (the next item's rows
-        // load while the current item's last tiles run)
-        const int qb = n_it & 1;
-        if (n_it >= 2 && !(run = mbar_wait_suspend(bar(B_Q_EMPTY + qb), ((n_it >> 1) - 1) & 1, abort_flag, 1)))
-          break;
-        mbar_arrive_expect_tx(bar(B_Q_FULL + qb), (uint32_t)da.q_bytes);
-        tma_load_3d(sb + L::SM_Q + qb * L::QBUF, &map_q, 0, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
-        tma_load_3d(sb + L::SM_Q + qb * L::QBUF + HALF16, &map_q, 64, I.g * a.group, I.cq, bar(B_Q_FULL + qb));
-        issued_q = n_it + 1;
-        // paged K / V: the pool row of a 128-aligned tile inside one page
-        auto tile_row = [&](int t) -> int {
-          const int p = I.kbeg + KT * t;
-          if (a.block_table == nullptr) return I.ck + p;
-          const int pg = a.block_table[(size_t)I.b * a.max_pages + p / a.page_size];
-          if (pg < 0 || pg >= a.num_pages) {
-            atomicOr(a.err, kDevErrSeqlens);
-            return -KT;   // reads zeros
+      return false;
+    };
+    auto ready = [&](uint32_t br, uint32_t parity) -> bool {
+      const bool r = lane == 0 ? mbar_test_wait(br, parity) : false;
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    // the pool row of tile t of item it (paged K / V: a 128-aligned tile inside one page)
+    auto tile_row = [&](const Item &it, int t) -> int {
+      const int p = it.kbeg + KT * t;
+      if (a.block_table == nullptr) return it.ck + p;
+      const int pg = a.block_table[(size_t)it.b * a.max_pages + p / a.page_size];
+      if (pg < 0 || pg >= a.num_pages) {
+        atomicOr(a.err, kDevErrSeqlens);
+        return -KT;   // reads zeros
+      }
+      return pg * a.page_size + p % a.page_size;
+    };
+    bool k_live = next_item(kidx, ik), v_live = next_item(vidx, iv), q_due = k_live;
+    long long idle_since = -1;
+    for (;;) {
+      // (lane 0's view of the abort flag, so the whole warp leaves together)
+      const bool quit = __shfl_sync(0xffffffffu, (lane == 0 && *abort_flag) ? 1 : 0, 0) != 0;
+      if (!(k_live || v_live) || quit) break;
+      bool moved = false;
+      if (k_live && q_due) {
+        const int qb = n_q & 1;
+        if (n_q < 2 || ready(bar(B_Q_EMPTY + qb), ((n_q >> 1) - 1) & 1)) {
+          if constexpr (F8) {
+            // the item's q rows, MXFP8 per 32 dims, into the K-major operand of
+            // S^T; each (row, block) scale times the row's logit scale
+            uint8_t *q8 = smem + L::SM_Q + qb * L::QBUF;
+            float *qsc = reinterpret_cast<float *>(smem + L::SM_QSC) + qb * NR * 4;
+            for (int pr = lane; pr < NR * 4; pr += 32) {
+              const int r = pr >> 2, blk = pr & 3;
+              uint32_t c[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+              float sc = 0.f;
+              if (r < ik.nrows) {
+                const int tau = r / a.group, hg = r - tau * a.group;
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    a.q + ((size_t)(ik.cq + tau) * a.Hq + ik.g * a.group + hg) * kHeadDim + 32 * blk);
+                int e;
+                quantize_block32(src, c, e);
+                sc = a.alpha_log2e * log_scale(ik.p0 + tau, a.inv_ln_base) * pow2i(e);
+              }
+              // codes of dims 32 blk .. 32 blk + 31 of row r: 16-byte chunks 2 blk, 2 blk + 1
+              *reinterpret_cast<uint4 *>(q8 + r * 128 + (((2 * blk) ^ (r & 7)) << 4)) =
+                  make_uint4(c[0], c[1], c[2], c[3]);
+              *reinterpret_cast<uint4 *>(q8 + r * 128 + (((2 * blk + 1) ^ (r & 7)) << 4)) =
+                  make_uint4(c[4], c[5], c[6], c[7]);
+              qsc[r * 4 + blk] = sc;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_Q_FULL + qb));
+          } else if (lane == 0) {
+            // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves of 64 dims
+            mbar_arrive_expect_tx(bar(B_Q_FULL + qb), (uint32_t)da.q_bytes);
+            tma_load_3d(sb + L::SM_Q + qb * L::QBUF, &map_q, 0, ik.g * a.group, ik.cq, bar(B_Q_FULL + qb));
+            tma_load_3d(sb + L::SM_Q + qb * L::QBUF + HALF16, &map_q, 64, ik.g * a.group, ik.cq,
+                        bar(B_Q_FULL + qb));
           }
-          return pg * a.page_size + p % a.page_size;
-        };
-        for (int t = 0; t < I.ntiles && run; ++t) {
-          const int G = T + t, st = G % NSTAGE, use = G / NSTAGE;
-          const int row = tile_row(t);
-          if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_K_EMPTY + st), (use - 1) & 1, abort_flag, 2))) break;
-          if (G != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
-            mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KTILE);
-            tma_load_3d(sb + L::SM_K + st * L::KTILE, &map_k, 0, I.g, row, bar(B_K_FULL + st));
-            tma_load_3d(sb + L::SM_K + st * L::KTILE + BOX, &map_k, 64, I.g, row, bar(B_K_FULL + st));
-          }
-          issued_k = G + 1;
-          if (G >= NSTAGE && !(run = mbar_wait_suspend(bar(B_V_EMPTY + st), (use - 1) & 1, abort_flag, 3))) break;
-          mbar_arrive_expect_tx(bar(B_V_FULL + st), L::KTILE);
-          tma_load_3d(sb + L::SM_V + st * L::KTILE, &map_v, 0, I.g, row, bar(B_V_FULL + st));
-          tma_load_3d(sb + L::SM_V + st * L::KTILE + BOX, &map_v, 64, I.g, row, bar(B_V_FULL + st));
-          issued_v = G + 1;
+          issued_q = ++n_q;
+          q_due = false;
+          moved = true;
         }
-        T += I.ntiles;
-        ++n_it;
-        if (*abort_flag) run = false;
+      } else if (k_live) {
+        const int st = GK % L::KST;
+        if (GK < L::KST || ready(bar(B_K_EMPTY + st), ((GK / L::KST) - 1) & 1)) {
+          if (lane == 0 && GK != a.test_skip_k_tile) {   // (test hook: a skipped tile is never loaded)
+            const int row = tile_row(ik, kt);
+            mbar_arrive_expect_tx(bar(B_K_FULL + st), L::KTILE);
+            tma_load_3d(sb + L::SM_K + st * L::KTILE, &map_k, 0, ik.g, row, bar(B_K_FULL + st));
+            if constexpr (!F8)
+              tma_load_3d(sb + L::SM_K + st * L::KTILE + BOX, &map_k, 64, ik.g, row, bar(B_K_FULL + st));
+          }
+          issued_k = ++GK;
+          if (++kt == ik.ntiles) {
+            kt = 0;
+            k_live = next_item(kidx, ik);
+            q_due = k_live;
+          }
+          moved = true;
+        }
+      }
+      if (v_live && GV < GK) {
+        const int st = GV % L::VST;
+        if (GV < L::VST || ready(bar(B_V_EMPTY + st), ((GV / L::VST) - 1) & 1)) {
+          if (lane == 0) {
+            const int row = tile_row(iv, vt);
+            mbar_arrive_expect_tx(bar(B_V_FULL + st), L::KTILE);
+            tma_load_3d(sb + L::SM_V + st * L::KTILE, &map_v, 0, iv.g, row, bar(B_V_FULL + st));
+            if constexpr (!F8)
+              tma_load_3d(sb + L::SM_V + st * L::KTILE + BOX, &map_v, 64, iv.g, row, bar(B_V_FULL + st));
+          }
+          issued_v = ++GV;
+          if (++vt == iv.ntiles) {
+            vt = 0;
+            v_live = next_item(vidx, iv);
+          }
+          moved = true;
+        }
+      }
+      // bounded: a stretch without progress longer than about a second gives
+      // up (lane 0's clock decides for the warp)
+      if (moved) {
+        idle_since = -1;
+      } else {
+        __nanosleep(64);   // back off: the softmax warps share this sub-partition
+        const long long now = clock64();
+        if (idle_since < 0) idle_since = now;
+        const bool give_up = __shfl_sync(0xffffffffu, (now - idle_since > 2000000000ll) ? 1 : 0, 0) != 0;
+        if (give_up) {
+          if (lane == 0) *abort_flag = 2;
+          break;
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ====================================================== MMA issuer
+    // ====================================================== score MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(KT, NR, 0, 0);    // S^T = K Q^T: K (keys x dims), q rows, both K-major
-      const uint32_t id_o = idesc_bf16_f32(128, NR, 1, 0);   // O^T += V^T P^T: V^T dims-contiguous, P K-major
       // descriptor bases; k-step k of a 128-wide K dimension: +2 per 32 bytes
       // inside a 128-byte row, the second 64-wide half at +16 KB in a K tile
-      // and at +2 KB in the 16-row q and P operands; V^T: dims along M in two
-      // 64-dim boxes 16 KB apart, 16 keys (+2 KB) per k-step
+      // and at +2 KB in the 16-row q and P operands (fp8: the K codes hold
+      // all 128 dims in one 128-byte row, 32 dims per E4M3 k-step); V^T:
+      // dims along M in two 64-dim boxes 16 KB apart, 16 keys (+2 KB) per k-step
       const uint64_t qd0 = smem_desc_sw128(sb + L::SM_Q, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sb + L::SM_K, 16, 1024);
-      const uint64_t pd0 = smem_desc_sw128(sb + L::SM_P, 16, 1024);
-      // (fp8: the warpgroup's dequantised bf16 V tile; the K codes hold all 128 dims
-      // in one 128-byte row, 32 dims per E4M3 k-step)
-      const uint64_t vd0 = smem_desc_sw128(sb + (F8 ? L::SM_VB : L::SM_V), BOX, 1024);
       const uint32_t id_s8 = idesc_e4m3_f32(KT, NR);
       auto koff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (BOX >> 4) + 2 * (k - 4)); };
       auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
       int T = 0, n_it = 0;
       bool ok = true;
-      // O^T of warpgroup G % 2 (+)= V(G)^T P(G)^T; `first`: the warpgroup's first tile of the item
-      auto issue_pv = [&](int G, bool first) -> bool {
-        const int st = G % NSTAGE, b = G & 1;
-        if (!mbar_wait(bar(B_P_FULL + b), (G >> 1) & 1, abort_flag, 4)) return false;
-        // (fp8: P_FULL also says the warpgroup's bf16 V tile is written)
-        if (!F8 && !mbar_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, abort_flag, 5)) return false;
-        tc_fence_after();
-        const uint64_t vd = vd0 + (uint64_t)(((F8 ? b * 2 * BOX : st * L::KTILE)) >> 4);
-        const uint64_t pd = pd0 + (uint64_t)((b * 2 * HALF16) >> 4);
-        const uint32_t o = tmem + L::TM_O + 16u * (uint32_t)b;
-        if (first) mma_ss_c<0>(o, vd + 0, pd + hoff(0), id_o);
-        else mma_ss_c<1>(o, vd + 0, pd + hoff(0), id_o);
-#pragma unroll
-        for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, vd + 128 * k, pd + hoff(k), id_o);
-        mma_commit(bar(B_PV_DONE + b));
-        if (!F8) mma_commit(bar(B_V_EMPTY + st));
-        return true;
-      };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         const int qb = n_it & 1;
         if (!(ok = mbar_wait(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
         const uint64_t qd = qd0 + (uint64_t)((qb * L::QBUF) >> 4);
         for (int t = 0; t < I.ntiles && ok; ++t) {
-          const int G = T + t, b = G & 1, st = G % NSTAGE;
+          const int G = T + t, b = G & 1, st = G % L::KST;
           if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
-          if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / NSTAGE) & 1, abort_flag, 8))) break;
+          if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / L::KST) & 1, abort_flag, 8))) break;
           tc_fence_after();
           const uint64_t kd = kd0 + (uint64_t)((st * L::KTILE) >> 4);
           const uint32_t d = tmem + L::TM_S + L::SCOLS * (uint32_t)b;
@@ -520,9 +530,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           mma_commit(bar(B_S_FULL + b));
           mma_commit(bar(B_K_EMPTY + st));
           if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY + qb));   // the item's q rows are read
-          if (t > 0) ok = issue_pv(G - 1, t - 1 < 2);
         }
-        if (ok) ok = issue_pv(T + I.ntiles - 1, I.ntiles - 1 < 2);
         T += I.ntiles;
         ++n_it;
       }
@@ -530,6 +538,44 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       mma_commit(bar(B_DRAIN));
       volatile int keep_waiting = 0;
       mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 9, 400000000ll);
+    }
+    __syncwarp();
+  } else if (warp == PV_WARP) {
+    // ====================================================== PV issuer
+    // A second issuing thread for the P V products, so the score MMAs of the
+    // next tiles and the P V MMA of a finished tile do not wait on one
+    // another's waits (each thread's commits track only its own MMAs).
+    if (lane == 0) {
+      const uint32_t id_o = idesc_bf16_f32(128, NR, 1, 0);   // O^T += V^T P^T: V^T dims-contiguous, P K-major
+      const uint64_t pd0 = smem_desc_sw128(sb + L::SM_P, 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(sb + (F8 ? L::SM_VB : L::SM_V), BOX, 1024);
+      auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
+      int T = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+        if (load_item(idx) <= 0 || I.ntiles == 0) continue;
+        for (int t = 0; t < I.ntiles && ok; ++t) {
+          // O^T of warpgroup G % 2 (+)= V(G)^T P(G)^T; the warpgroup's first tile of the item overwrites
+          const int G = T + t, st = G % L::VST, b = G & 1;
+          if (!(ok = mbar_wait(bar(B_P_FULL + b), (G >> 1) & 1, abort_flag, 4))) break;
+          // (fp8: P_FULL also says the warpgroup's bf16 V tile is written)
+          if (!F8 && !(ok = mbar_wait(bar(B_V_FULL + st), (G / L::VST) & 1, abort_flag, 5))) break;
+          tc_fence_after();
+          const uint64_t vd = vd0 + (uint64_t)(((F8 ? b * 2 * BOX : st * L::KTILE)) >> 4);
+          const uint64_t pd = pd0 + (uint64_t)((b * 2 * HALF16) >> 4);
+          const uint32_t o = tmem + L::TM_O + 16u * (uint32_t)b;
+          if (t < 2) mma_ss_c<0>(o, vd + 0, pd + hoff(0), id_o);
+          else mma_ss_c<1>(o, vd + 0, pd + hoff(0), id_o);
+#pragma unroll
+          for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, vd + 128 * k, pd + hoff(k), id_o);
+          mma_commit(bar(B_PV_DONE + b));
+          if (!F8) mma_commit(bar(B_V_EMPTY + st));
+        }
+        T += I.ntiles;
+      }
+      mma_commit(bar(B_DRAIN_PV));
+      volatile int keep_waiting = 0;
+      mbar_wait(bar(B_DRAIN_PV), 0, &keep_waiting, 9, 400000000ll);
     }
     __syncwarp();
   } else {
@@ -558,6 +604,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       return __all_sync(0xffffffffu, r);
     };
     int n_xch = 0, n_merge = 0;
+    bool r_ready = false;
     // the warpgroup's 128 threads meet
     auto xch_barrier = [&]() -> bool {
       mbar_arrive(bar(B_XCH + wg));
@@ -609,6 +656,12 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         // band tiles: R[row][p_row - j] for this key, every load issued before
         // the S wait (an index outside the band reads R[0] and is discarded)
         float rbias[NR];
+        if (band && !r_ready) {
+          // launched as a programmatic dependent of the R kernel: its rows are
+          // complete and visible past this point
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          r_ready = true;
+        }
         if (band) {
 #pragma unroll
           for (int i = 0; i < NR; ++i) {
@@ -743,8 +796,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           // this key's V codes (one 128-byte row of the stage) dequantised into
           // the warpgroup's bf16 V tile: dims 0-63 in the first 128-byte-swizzled
           // box, 64-127 in the second; then the stage is free for the next copy
-          const int st = G % NSTAGE;
-          if (!(ok = warp_wait(bar(B_V_FULL + st), (G / NSTAGE) & 1, 19))) break;
+          const int st = G % L::VST;
+          if (!(ok = warp_wait(bar(B_V_FULL + st), (G / L::VST) & 1, 19))) break;
           const uint8_t *v8 = smem + L::SM_V + st * L::KTILE + key * 128;
           uint8_t *vb = smem + L::SM_VB + wg * 2 * BOX + key * 128;
           const uint32_t sw = (uint32_t)(key & 7);
@@ -872,11 +925,11 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     volatile int keep_waiting = 0;
     for (int n = max(0, issued_q - 2); n < issued_q; ++n)
       mbar_wait(bar(B_Q_FULL + (n & 1)), (n >> 1) & 1, &keep_waiting, 15, 400000000ll);
-    for (int G = max(0, issued_k - NSTAGE); G < issued_k; ++G)
+    for (int G = max(0, issued_k - L::KST); G < issued_k; ++G)
       if (G != a.test_skip_k_tile)
-        mbar_wait(bar(B_K_FULL + G % NSTAGE), (G / NSTAGE) & 1, &keep_waiting, 15, 400000000ll);
-    for (int G = max(0, issued_v - NSTAGE); G < issued_v; ++G)
-      mbar_wait(bar(B_V_FULL + G % NSTAGE), (G / NSTAGE) & 1, &keep_waiting, 15, 400000000ll);
+        mbar_wait(bar(B_K_FULL + G % L::KST), (G / L::KST) & 1, &keep_waiting, 15, 400000000ll);
+    for (int G = max(0, issued_v - L::VST); G < issued_v; ++G)
+      mbar_wait(bar(B_V_FULL + G % L::VST), (G / L::VST) & 1, &keep_waiting, 15, 400000000ll);
   }
   if (warp == 1) {
     tc_fence_after();
@@ -893,6 +946,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
 // multiple of 4 are zeroed).
 constexpr int RR = 16, RD = 256;
 __global__ void __launch_bounds__(RD) relattn_decode_rel_kernel(const KernelArgs a, float *R) {
+  // the decode kernel may launch now: it waits for these rows before its first band tile
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ __align__(16) float rs[RR][64];
   __shared__ __align__(16) __nv_bfloat16 ps[64][RD];
   const int tid = threadIdx.x;
@@ -939,6 +994,26 @@ __global__ void __launch_bounds__(RD) relattn_decode_rel_kernel(const KernelArgs
 #pragma unroll
   for (int i = 0; i < RR; ++i)
     if (row0 + i < rows) R[(row0 + i) * a.E + d] = acc[i];
+}
+
+// Launch as a programmatic dependent of the kernel before it on the stream
+// (the decode-row R kernel): the CTAs start as soon as it lets them, and only
+// band tiles wait for its rows.  After any other kernel this is an ordinary
+// stream-ordered launch.
+template <typename K>
+cudaError_t launch_dependent(K kernel, int grid, uint32_t smem, cudaStream_t stream, const DecArgs &da,
+                             const CUtensorMap &m0, const CUtensorMap &m1, const CUtensorMap &m2) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NTHR);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, da, m0, m1, m2);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 dec_encoder() {
@@ -1022,9 +1097,8 @@ cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_
   cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<false>),
                                     (int)smem, attr_set);
   if (e != cudaSuccess) return e;
-  const int grid = (int)std::min<long>(items, a.sms > 0 ? a.sms : items);
-  relattn_decode_tc_kernel<false><<<grid, NTHR, smem, stream>>>(da, mq, mk, mv);
-  return cudaGetLastError();
+  return launch_dependent(relattn_decode_tc_kernel<false>, (int)std::min<long>(items, a.sms > 0 ? a.sms : items),
+                          smem, stream, da, mq, mk, mv);
 }
 
 cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void *v8, const void *ks,
@@ -1067,10 +1141,9 @@ cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void 
   cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<true>),
                                     (int)smem, attr_set);
   if (e != cudaSuccess) return e;
-  const int grid = (int)std::min<long>(items, a.sms > 0 ? a.sms : items);
   // (the q map is not read: the producer quantises q rows itself)
-  relattn_decode_tc_kernel<true><<<grid, NTHR, smem, stream>>>(da, mk, mk, mv);
-  return cudaGetLastError();
+  return launch_dependent(relattn_decode_tc_kernel<true>, (int)std::min<long>(items, a.sms > 0 ? a.sms : items),
+                          smem, stream, da, mk, mk, mv);
 }
 
 }  // namespace relattn

@@ -100,9 +100,11 @@ cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void 
 cudaError_t launch_quantize_mxfp8(const void *x, long n_blocks, void *codes, void *scales,
                                   cudaStream_t stream);
 cudaError_t launch_decode_mma(const KernelArgs &a, int warps, cudaStream_t stream);
+// pdl: launched as a programmatic dependent of the kernel before it on the
+// stream (which lets it launch early; the combine waits for its results)
 cudaError_t launch_combine(const float *o_part, const float *lse_part, int num_splits,
                            int total_q, int num_heads, __nv_bfloat16 *out, float *lse,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool pdl = false);
 
 // Backward pass (bwd_mma.cu): gradients of sum(dout * out) w.r.t. q, k, v, r.
 struct BwdArgs {

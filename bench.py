@@ -283,8 +283,8 @@ class ProloguePhase:
     of k / v, RMSNorm of q / k, cache write and conv state out (the sequences
     start with the chunk, so no state in)."""
 
-    def __init__(self, w, rpb):
-        self.name, self.w, self.rpb = "prologue", w, rpb
+    def __init__(self, w, rpb, mxfp8=False):
+        self.name, self.w, self.rpb = "prologue" + ("_mxfp8" if mxfp8 else ""), w, rpb
         self.decode = True   # reported in GB/s
         self.host = W.make_prologue_inputs(w)
         d = {k: v.cuda() for k, v in self.host.items()}
@@ -297,12 +297,19 @@ class ProloguePhase:
                                        device="cuda") for _ in range(2))
         self.launches = 2   # rows kernel + state kernel
         self.bytes = A.prologue_bytes(w, state_in=False, state_out=True)
+        self.mx = None
+        if mxfp8:
+            # the MXFP8 cache written as well (codes + scales: 132 bytes a 128-dim row)
+            k8 = torch.empty(Tk, w.Hkv, 128, dtype=torch.uint8, device="cuda")
+            ks = torch.empty(Tk, w.Hkv, 4, dtype=torch.uint8, device="cuda")
+            self.mx = (k8, torch.empty_like(k8), ks, torch.empty_like(ks))
+            self.bytes += 2 * sum(w.q_lens) * w.Hkv * (128 + 4)
 
     def run(self):
         d = self.dev
         self.rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"],
                           d["norm_k"], d["cu_seqlens_q"], d["cu_seqlens_k"], self.k_cache,
-                          self.v_cache, q_out=self.q_out, conv_state_out=self.state)
+                          self.v_cache, q_out=self.q_out, conv_state_out=self.state, mxfp8=self.mx)
 
 
 class PagedDecodePhase:
@@ -674,7 +681,12 @@ def gpu_arm(args):
     for _ in range(args.warmup):
         pro.run()
     torch.cuda.synchronize()
-    pro_t = timed_steps([pro], args.steps, flush)["prologue"]
+    pro_mx = ProloguePhase(wl["prefill_swa"], rpb, mxfp8=True)
+    for _ in range(args.warmup):
+        pro_mx.run()
+    torch.cuda.synchronize()
+    pro_tt = timed_steps([pro, pro_mx], args.steps, flush)
+    pro_t = pro_tt["prologue"]
     torch.cuda.synchronize()
     if rpb.relattn_get_device_error() != 0:
         raise SystemExit("device error word set by the prologue")
@@ -722,6 +734,7 @@ def gpu_arm(args):
     ms = {n: max_over_ranks(median(times[n]), dist) for n in STEP_PHASES}
     step_ms = max_over_ranks(sum(median(times[n]) for n in STEP_PHASES), dist)
     pro_ms = max_over_ranks(median(pro_t), dist)
+    pro_mx_ms = max_over_ranks(median(pro_tt["prologue_mxfp8"]), dist)
     pg_ms = {p.name: max_over_ranks(median(pg_t[p.name]), dist) for p in paged}
     mx_ms = {p.name: max_over_ranks(median(mx_t[p.name]), dist) for p in mx}
     bwd_ms = max_over_ranks(median(bwd_t), dist)
@@ -827,7 +840,11 @@ def gpu_arm(args):
             "what": "ShortConv k/v + RMSNorm q/k + KV-cache write + conv state out",
             "bytes": pro.bytes, "launches": args.steps * pro.launches,
             "roofline": _roofline("hbm", pro_gbs, hbm_peak, "GB/s",
-                                  load_traffic("prologue", "prologue"), hbm_src)},
+                                  load_traffic("prologue", "prologue"), hbm_src),
+            "mxfp8": {"ms": pro_mx_ms, "value": pro_mx.bytes / (pro_mx_ms * 1e-3) / 1e9, "unit": "GB/s",
+                      "bytes": pro_mx.bytes, "vs_bf16_only": pro_mx_ms / pro_ms,
+                      "what": "the same prologue writing the MXFP8 cache (E4M3 codes + E8M0 scales) "
+                              "beside the bf16 cache, quantise fused"}},
         "backward": {
             "value": job_rate(bwd.flops, bwd_ms, ws, 1e12), "unit": "TFLOP/s", "ms": bwd_ms,
             "workload": swa.w.name,

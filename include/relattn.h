@@ -359,6 +359,29 @@ typedef struct relattn_prologue_params {
 
 relattn_status relattn_prologue(const relattn_prologue_params *params, void *stream);
 
+/*
+ * The prologue with the MXFP8 quantise fused in (page "SGLang and Miles Add
+ * Day-0 Support for Inkling", section "Relative Logits Optimization",
+ * paragraph "MXFP8 Support": the quantisation folded into the attention
+ * prologue instead of a separate quantise-and-store step).  Same computation
+ * and arguments as relattn_prologue; each k / v cache row it writes is also
+ * stored as MXFP8 (the format of relattn_quantize_mxfp8: E4M3 codes and one
+ * E8M0 scale per 32 dims) of its bf16-rounded values, so the codes equal
+ * relattn_quantize_mxfp8 of the bf16 cache rows.  params->k_cache / v_cache
+ * may be NULL (MXFP8 cache only).  cache->k / v: uint8 [total_k,
+ * num_heads_kv, 128], 8-byte aligned; cache->k_scale / v_scale: uint8
+ * [total_k, num_heads_kv, 4]; none may overlap the k / v inputs.
+ */
+typedef struct relattn_kv_mxfp8_out {
+  void *k;
+  void *v;
+  void *k_scale;
+  void *v_scale;
+} relattn_kv_mxfp8_out;
+
+relattn_status relattn_prologue_mxfp8(const relattn_prologue_params *params,
+                                      const relattn_kv_mxfp8_out *cache, void *stream);
+
 /* ------------------------------------------------------------------ test hooks
  *
  * Declared only with RELATTN_TEST_HOOKS defined, and exported only by the

@@ -39,6 +39,7 @@ EXPORTED = (
     "relattn_last_device_error_word",
     "relattn_prologue", "relattn_backward", "relattn_backward_workspace_size",
     "relattn_decode_paged", "relattn_decode_mxfp8", "relattn_quantize_mxfp8",
+    "relattn_prologue_mxfp8",
 )
 # exported by the test build only
 TEST_HOOKS = (
@@ -199,6 +200,9 @@ def _configure(path: str):
         lib.relattn_backward_workspace_size.restype = ctypes.c_int
         lib.relattn_prologue.argtypes = [ctypes.POINTER(RelattnPrologueParams), vp]
         lib.relattn_prologue.restype = ctypes.c_int
+        lib.relattn_prologue_mxfp8.argtypes = [ctypes.POINTER(RelattnPrologueParams),
+                                               ctypes.POINTER(RelattnKvMxfp8), vp]
+        lib.relattn_prologue_mxfp8.restype = ctypes.c_int
         lib.relattn_version.argtypes = []
         lib.relattn_version.restype = ctypes.c_char_p
         _libs[path] = lib
@@ -379,13 +383,17 @@ def decode(q, k, v, r, P, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q: int, max_
 
 def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k, k_cache,
              v_cache, *, eps: float = 1e-6, q_out=None, conv_state_in=None,
-             conv_state_out=None, total_k: Optional[int] = None, stream: Optional[int] = None):
+             conv_state_out=None, total_k: Optional[int] = None, mxfp8=None,
+             stream: Optional[int] = None):
     """ShortConv + Q/K RMSNorm + KV-cache write for one chunk, on device tensors.
 
     ``conv_state_in`` / ``conv_state_out`` are ``(k_state, v_state)`` pairs of
     bf16 [batch, 3, Hkv*128] tensors, or None.  Writes ``k_cache`` / ``v_cache``
     rows in place and returns ``q_out`` (a new tensor unless given; pass
-    ``q_out=q`` to normalise in place).
+    ``q_out=q`` to normalise in place).  With ``mxfp8=(k8, v8, k_scale,
+    v_scale)`` (uint8 [total_k, Hkv, 128] codes and [total_k, Hkv, 4] scales)
+    the cache rows are also written as MXFP8 (relattn_prologue_mxfp8); the bf16
+    caches may then be None.
     """
     import torch
     if q_out is None:
@@ -400,13 +408,18 @@ def prologue(q, k, v, conv_k, conv_v, norm_q, norm_k, cu_seqlens_q, cu_seqlens_k
         norm_q=ptr(norm_q), norm_k=ptr(norm_k), eps=float(eps),
         cu_seqlens_q=ptr(cu_seqlens_q), cu_seqlens_k=ptr(cu_seqlens_k),
         batch=int(cu_seqlens_q.numel()) - 1, total_q=int(q.shape[0]),
-        total_k=int(k_cache.shape[0]) if total_k is None else int(total_k),
+        total_k=int((k_cache if k_cache is not None else mxfp8[0]).shape[0]) if total_k is None else int(total_k),
         num_heads_q=int(q.shape[1]), num_heads_kv=int(k.shape[1]), head_dim=int(q.shape[2]),
         q_out=ptr(q_out), k_cache=ptr(k_cache), v_cache=ptr(v_cache),
         conv_state_in_k=ptr(sin[0]), conv_state_in_v=ptr(sin[1]),
         conv_state_out_k=ptr(sout[0]), conv_state_out_v=ptr(sout[1]))
-    _check(relattn_prologue(prm, _current_stream() if stream is None else stream),
-           "relattn_prologue")
+    st = _current_stream() if stream is None else stream
+    if mxfp8 is None:
+        _check(relattn_prologue(prm, st), "relattn_prologue")
+    else:
+        mx = RelattnKvMxfp8(k=ptr(mxfp8[0]), v=ptr(mxfp8[1]), k_scale=ptr(mxfp8[2]), v_scale=ptr(mxfp8[3]))
+        _check(load_library().relattn_prologue_mxfp8(ctypes.byref(prm), ctypes.byref(mx), st),
+               "relattn_prologue_mxfp8")
     return q_out
 
 

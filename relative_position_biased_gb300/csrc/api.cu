@@ -274,7 +274,7 @@ relattn_status validate_backward(const relattn_bwd_params *p) {
   return RELATTN_OK;
 }
 
-relattn_status validate_prologue(const relattn_prologue_params *p) {
+relattn_status validate_prologue(const relattn_prologue_params *p, const relattn_kv_mxfp8_out *mx = nullptr) {
   if (!p) return RELATTN_ERR_INVALID_ARG;
   if (p->head_dim != kHeadDim) return RELATTN_ERR_UNSUPPORTED;
   if (p->batch < 0 || p->total_q < 0 || p->total_k < 0 || p->num_heads_q <= 0 ||
@@ -282,10 +282,24 @@ relattn_status validate_prologue(const relattn_prologue_params *p) {
     return RELATTN_ERR_INVALID_ARG;
   if (!(isfinite(p->eps) && p->eps > 0.f)) return RELATTN_ERR_INVALID_ARG;
   if (p->batch == 0) return RELATTN_OK;
-  const void *need[] = {p->q,      p->k,      p->v,      p->q_out, p->k_cache,
-                        p->v_cache, p->conv_k, p->conv_v, p->norm_q, p->norm_k};
+  const void *need[] = {p->q, p->k, p->v, p->q_out, p->conv_k, p->conv_v, p->norm_q, p->norm_k};
   for (const void *x : need)
     if (!x || !aligned(x, 16)) return RELATTN_ERR_INVALID_ARG;
+  // the bf16 cache is optional only when an MXFP8 one is written
+  const void *caches[] = {p->k_cache, p->v_cache};
+  for (const void *x : caches)
+    if (mx ? (x && !aligned(x, 16)) : (!x || !aligned(x, 16))) return RELATTN_ERR_INVALID_ARG;
+  if (mx) {
+    if (!mx->k || !mx->v || !mx->k_scale || !mx->v_scale || !aligned(mx->k, 8) || !aligned(mx->v, 8))
+      return RELATTN_ERR_INVALID_ARG;
+    const size_t codes = (size_t)p->total_k * p->num_heads_kv * kHeadDim, sc = codes / 32;
+    const size_t in_bytes = (size_t)p->total_q * p->num_heads_kv * kHeadDim * 2;
+    const void *outs8[] = {mx->k, mx->v, mx->k_scale, mx->v_scale};
+    const size_t n8[] = {codes, codes, sc, sc};
+    for (int i = 0; i < 4; ++i)
+      if (overlaps(outs8[i], n8[i], p->k, in_bytes) || overlaps(outs8[i], n8[i], p->v, in_bytes))
+        return RELATTN_ERR_INVALID_ARG;
+  }
   if (!p->cu_seqlens_q || !p->cu_seqlens_k) return RELATTN_ERR_INVALID_ARG;
   const void *states[] = {p->conv_state_in_k, p->conv_state_in_v, p->conv_state_out_k,
                           p->conv_state_out_v};
@@ -559,6 +573,19 @@ relattn_status relattn_prologue(const relattn_prologue_params *p, void *stream) 
   if ((st = device_state(nullptr, &err, &sms)) != RELATTN_OK) return st;
   return cuda_status(launch_prologue(p, err, sms, g_test_prologue_skip,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+relattn_status relattn_prologue_mxfp8(const relattn_prologue_params *p, const relattn_kv_mxfp8_out *cache,
+                                      void *stream) {
+  if (!cache) return RELATTN_ERR_INVALID_ARG;
+  relattn_status st = validate_prologue(p, cache);
+  if (st != RELATTN_OK) return st;
+  if (p->batch == 0) return RELATTN_OK;
+  int *err = nullptr;
+  int sms = 0;
+  if ((st = device_state(nullptr, &err, &sms)) != RELATTN_OK) return st;
+  return cuda_status(launch_prologue(p, err, sms, g_test_prologue_skip,
+                                     static_cast<cudaStream_t>(stream), cache));
 }
 
 relattn_status relattn_get_device_error(void *stream) {

@@ -145,7 +145,8 @@ cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t stream);
 // attention prologue (prologue.cu): ShortConv + Q/K RMSNorm + KV-cache rows;
 // err = the device error word, sms = the SM count (sizes the grid),
 // skip_tile = test hook (a token tile whose copies are never issued; -1 = off).
+// mx: an MXFP8 cache to write as well (or instead, with null bf16 caches).
 cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms, int skip_tile,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const relattn_kv_mxfp8_out *mx = nullptr);
 
 }  // namespace relattn

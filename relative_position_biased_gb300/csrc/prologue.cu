@@ -23,6 +23,7 @@
 // memory) and the separate state kernel serve head counts whose tile does
 // not fit in shared memory.
 #include "launch.h"
+#include "mxfp8.cuh"
 #include "tc_common.cuh"
 
 namespace relattn {
@@ -41,9 +42,35 @@ struct PrologueArgs {
   __nv_bfloat16 *q_out, *k_cache, *v_cache;
   const __nv_bfloat16 *state_in_k, *state_in_v;
   __nv_bfloat16 *state_out_k, *state_out_v;
+  // MXFP8 cache (null: none): E4M3 codes [total_k, Hkv, 128] and E8M0 scales
+  // [total_k, Hkv, 4] of the bf16-rounded k / v rows, written beside (or
+  // instead of, when k_cache / v_cache are null) the bf16 cache
+  uint8_t *k8, *v8, *ks8, *vs8;
   int *err;
   int skip_tile;   // test hook: a token tile whose copies are never issued (-1: none)
 };
+
+// MXFP8 of a cache row's 32-dim block spread over 32 / N lanes (N values
+// each, consecutive lanes holding consecutive dims; `mask` covers them):
+// the values are rounded to bf16 first (the bf16 cache's values), the block
+// max taken across the lanes.  c[i]: this lane's codes 4i .. 4i+3.
+template <int N>
+__device__ __forceinline__ void mx_quant_lanes(const float (&y)[N], unsigned mask, uint32_t (&c)[N / 4], int &e) {
+  float v[N];
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    v[i] = __bfloat162float(__float2bfloat16_rn(y[i]));
+    am = fmaxf(am, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 1; o < 32 / N; o <<= 1) am = fmaxf(am, __shfl_xor_sync(mask, am, o));
+  e = mx_block_exponent(am);
+  const float inv = pow2i(-e);
+#pragma unroll
+  for (int i = 0; i < N / 4; ++i)
+    c[i] = e4m3x2(v[4 * i + 1] * inv, v[4 * i] * inv) | (e4m3x2(v[4 * i + 3] * inv, v[4 * i + 2] * inv) << 16);
+}
 
 __device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&x)[4]) {
   const uint2 u = *reinterpret_cast<const uint2 *>(p);
@@ -161,10 +188,21 @@ relattn_prologue_kernel(const PrologueArgs a) {
         y[2] *= inv * g.z;
         y[3] *= inv * g.w;
       }
-      __nv_bfloat16 *dst = kind[j] == 0 ? a.q_out + ((size_t)out_row[j] * a.Hq + head[j]) * kHeadDim
-                           : (kind[j] == 1 ? a.k_cache : a.v_cache) +
-                                 ((size_t)out_row[j] * a.Hkv + head[j]) * kHeadDim;
-      store4(dst + dim, y);
+      __nv_bfloat16 *cache = kind[j] == 1 ? a.k_cache : a.v_cache;
+      if (kind[j] == 0) {
+        store4(a.q_out + ((size_t)out_row[j] * a.Hq + head[j]) * kHeadDim + dim, y);
+      } else {
+        const size_t crow = (size_t)out_row[j] * a.Hkv + head[j];
+        if (cache != nullptr) store4(cache + crow * kHeadDim + dim, y);
+        uint8_t *codes = kind[j] == 1 ? a.k8 : a.v8;
+        if (codes != nullptr) {   // (warp-uniform)
+          uint32_t c[1];
+          int e;
+          mx_quant_lanes<4>(y, 0xffffffffu, c, e);
+          *reinterpret_cast<uint32_t *>(codes + crow * kHeadDim + dim) = c[0];
+          if ((lane & 7) == 0) (kind[j] == 1 ? a.ks8 : a.vs8)[crow * 4 + (lane >> 3)] = (uint8_t)(e + 127);
+        }
+      }
     }
   }
 }
@@ -314,7 +352,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
 struct KvRow {
   float x[kTaps][8];
   const float *w;           // the lane's taps in shared memory: w[d * C + i], dims i < 8
-  __nv_bfloat16 *dst;       // the lane's 8 dims of the cache row
+  size_t crow;              // the cache row (row * Hkv + head)
   bool is_k, live;
 };
 
@@ -477,8 +515,7 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
           }
         }
         R.w = wsm + (R.is_k ? 0 : kTaps * C) + h * kHeadDim + dim;
-        R.dst = (R.is_k ? a.k_cache : a.v_cache) +
-                ((size_t)(t0 + tt + in.y) * Hkv + h) * kHeadDim + dim;
+        R.crow = (size_t)(t0 + tt + in.y) * Hkv + h;
       };
       auto conv = [&](const KvRow &R, float (&y)[8]) {
 #pragma unroll
@@ -498,7 +535,18 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
         float y[8];
         conv(A, y);
         if (A.is_k) rms_norm_half(y, gk, a.eps, hmask);
-        if (A.live) *reinterpret_cast<uint4 *>(A.dst) = pack8(y);
+        __nv_bfloat16 *cache = A.is_k ? a.k_cache : a.v_cache;
+        if (A.live && cache != nullptr) *reinterpret_cast<uint4 *>(cache + A.crow * kHeadDim + dim) = pack8(y);
+        uint8_t *codes = A.is_k ? a.k8 : a.v8;
+        if (codes != nullptr) {   // (uniform over the half-warp: one row)
+          uint32_t c[2];
+          int e;
+          mx_quant_lanes<8>(y, hmask, c, e);
+          if (A.live) {
+            *reinterpret_cast<uint2 *>(codes + A.crow * kHeadDim + dim) = make_uint2(c[0], c[1]);
+            if ((hl & 3) == 0) (A.is_k ? a.ks8 : a.vs8)[A.crow * 4 + (hl >> 2)] = (uint8_t)(e + 127);
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(empty(st));   // this warp is done with the stage
@@ -522,9 +570,13 @@ relattn_prologue_staged_kernel(const PrologueArgs a, int T) {
 }  // namespace
 
 cudaError_t launch_prologue(const relattn_prologue_params *p, int *err, int sms, int skip_tile,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const relattn_kv_mxfp8_out *mx) {
   PrologueArgs a;
   a.skip_tile = skip_tile;
+  a.k8 = mx ? static_cast<uint8_t *>(mx->k) : nullptr;
+  a.v8 = mx ? static_cast<uint8_t *>(mx->v) : nullptr;
+  a.ks8 = mx ? static_cast<uint8_t *>(mx->k_scale) : nullptr;
+  a.vs8 = mx ? static_cast<uint8_t *>(mx->v_scale) : nullptr;
   a.q = static_cast<const __nv_bfloat16 *>(p->q);
   a.k = static_cast<const __nv_bfloat16 *>(p->k);
   a.v = static_cast<const __nv_bfloat16 *>(p->v);

@@ -219,3 +219,69 @@ def test_inconsistent_cu_seqlens_are_reported_and_skipped():
 def test_full_size_swa_prefill_chunk():
     """The 4 x 8192 packed prefill chunk (16 q heads, 2 kv heads) in one call."""
     check(_w([8192] * 4), with_state_in=False)
+
+
+# ------------------------------------------------------------------ MXFP8 cache
+
+def _run_mx(w, inp, with_bf16=True):
+    import relative_position_biased_gb300 as rpb
+    d = {k: v.cuda() for k, v in inp.items()}
+    Tk = sum(w.k_lens)
+    kc = torch.full((Tk, w.Hkv, 128), SENTINEL, dtype=torch.bfloat16, device="cuda") if with_bf16 else None
+    vc = torch.full_like(kc, SENTINEL) if with_bf16 else None
+    k8 = torch.full((Tk, w.Hkv, 128), 0x55, dtype=torch.uint8, device="cuda")
+    v8 = torch.full_like(k8, 0x55)
+    ks = torch.full((Tk, w.Hkv, 4), 0x55, dtype=torch.uint8, device="cuda")
+    vs = torch.full_like(ks, 0x55)
+    rpb.prologue(d["q"], d["k"], d["v"], d["conv_k"], d["conv_v"], d["norm_q"], d["norm_k"],
+                 d["cu_seqlens_q"], d["cu_seqlens_k"], kc, vc, mxfp8=(k8, v8, ks, vs), total_k=Tk)
+    torch.cuda.synchronize()
+    st = rpb.relattn_get_device_error()
+    assert st == rpb.RELATTN_OK, rpb.STATUS_NAMES.get(st, st)
+    return kc, vc, k8, v8, ks, vs
+
+
+@pytest.mark.parametrize("q_lens,Hq,Hkv", [([3000, 2000, 1], 16, 2), ([5, 3], 512, 1), ([1] * 9, 8, 1)],
+                         ids=["staged", "register_kernel", "decode_rows"])
+def test_fused_mxfp8_cache(q_lens, Hq, Hkv):
+    """The fused MXFP8 cache: (1) exactly the quantisation of the bf16 cache
+    rows the same call writes (codes and scales, byte for byte, against the
+    MXFP8 oracle applied to those rows); (2) against the prologue oracle
+    rounded to bf16 and quantised by the MXFP8 oracle, equal in at least
+    99.9 % of the codes (the bf16 rows themselves differ from the oracle's
+    rounding in at most 0.1 %), and every dequantised value within one code
+    step; (3) rows outside the chunk untouched."""
+    from oracle import mxfp8 as M
+    w = _w(q_lens, Hq=Hq, Hkv=Hkv)
+    inp = W.make_prologue_inputs(w, with_state=True)
+    kc, vc, k8, v8, ks, vs = _run_mx(w, inp)
+    ref = run_oracle(inp, False)
+    rows = torch.from_numpy(ref["cache_rows"])
+    Tk = sum(w.k_lens)
+    untouched = torch.ones(Tk, dtype=torch.bool)
+    untouched[rows] = False
+    for cache, codes, scales, key in ((kc, k8, ks, "k_rows"), (vc, v8, vs, "v_rows")):
+        cb = cache.cpu()[rows].float().numpy()
+        c_o, s_o = M.quantize(cb)
+        assert np.array_equal(codes.cpu()[rows].numpy(), c_o), key
+        assert np.array_equal(scales.cpu()[rows].numpy(), s_o), key
+        # against the prologue oracle itself
+        rb = torch.from_numpy(ref[key]).float().bfloat16().float().numpy()
+        c_r, s_r = M.quantize(rb)
+        frac = float(np.mean(codes.cpu()[rows].numpy() == c_r))
+        assert frac >= 0.999, (key, frac)
+        dg = M.dequantize(codes.cpu()[rows].numpy(), scales.cpu()[rows].numpy())
+        dr = M.dequantize(c_r, s_r)
+        s_big = np.maximum(s_r, scales.cpu()[rows].numpy()).astype(np.int64)
+        step = np.repeat(np.ldexp(1.0, s_big - 127 - 3 + 8), 32, axis=-1)   # E4M3 spacing at the top
+        assert np.all(np.abs(dg - dr) <= step + 1e-30), key
+        assert bool((codes.cpu()[untouched] == 0x55).all()) and bool((scales.cpu()[untouched] == 0x55).all())
+
+
+def test_fused_mxfp8_without_bf16_cache():
+    w = _w([700, 64, 1])
+    inp = W.make_prologue_inputs(w, with_state=True)
+    kc, vc, k8a, v8a, ksa, vsa = _run_mx(w, inp, with_bf16=True)
+    _, _, k8b, v8b, ksb, vsb = _run_mx(w, inp, with_bf16=False)
+    for a, b in ((k8a, k8b), (v8a, v8b), (ksa, ksb), (vsa, vsb)):
+        assert torch.equal(a, b)

@@ -827,6 +827,7 @@ def gpu_arm(args):
                       for p in paged},
             "mxfp8": {p.name: {"value": p.bytes / (mx_ms[p.name] * 1e-3) / 1e9, "unit": "GB/s",
                                "ms": mx_ms[p.name], "bytes": p.bytes,
+                               "traffic": load_traffic(p.name, "decode"),
                                "frac": p.bytes / (mx_ms[p.name] * 1e-3) / 1e9 / hbm_peak,
                                "bf16_equivalent": p.bytes_bf16 / (mx_ms[p.name] * 1e-3) / 1e9,
                                "what": "E4M3 K / V codes + E8M0 scales per 32 dims; q quantised "

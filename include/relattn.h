@@ -100,6 +100,13 @@ typedef struct relattn_params {
  * Prefill / chunked prefill: any Lq_b <= Lk_b.  rows are grouped into 128-row
  * query tiles per head; key tiles outside the causal / window range are
  * skipped.  Needs no workspace.
+ *
+ * Speed depends on the shape.  The tensor-core (tcgen05) kernels take the
+ * call when q, k, v, out (and r, P with a bias) are 16-byte aligned, r_dim
+ * and rel_extent are multiples of 8, rel_extent >= 64 (or no bias), r_dim
+ * <= 64, and total_k >= 128.  Any other valid shape runs on a warp-level MMA
+ * kernel with the same results, about 2-3x slower (277 vs 662 TFLOP/s on a
+ * 4 x 8192 sliding-window prefill).
  */
 relattn_status relattn_prefill(const relattn_params *params, void *stream);
 
@@ -110,6 +117,15 @@ relattn_status relattn_prefill(const relattn_params *params, void *stream);
  * Each split writes a partial (out, lse) to the workspace and a combine kernel
  * merges them by their logsumexp.  num_splits = 0 picks the split count; the
  * chosen count is the one relattn_decode_workspace_size() sizes for.
+ *
+ * Speed depends on the shape.  Calls of at most 16 rows per kv head
+ * (max_seqlen_q x num_heads_q / num_heads_kv <= 16) take the few-row
+ * tensor-core kernel when q, k, v, out are 16-byte aligned and total_k >= 128:
+ * any r_dim <= 64 and any rel_extent.  Wider calls (e.g. a 9-token verify of
+ * a GQA-8 group) take the 128-row tensor-core kernel under the prefill's
+ * conditions above.  Any other valid shape runs on a warp-level MMA kernel
+ * with the same results, about 2x slower (2.7 vs 5.6 TB/s on a 9-row, 1M-key
+ * decode).
  */
 relattn_status relattn_decode(const relattn_params *params, void *stream);
 

@@ -133,9 +133,14 @@ relattn_status relattn_decode(const relattn_params *params, void *stream);
  * Workspace bytes relattn_decode needs for these params: the split partials
  * (fp32 out and lse of every split) when the keys are cut into several
  * splits, and, when max_seqlen_q x (num_heads_q / num_heads_kv) <= 16 and a
- * relative bias is on, the bias of every decode row at every distance below
- * rel_extent (fp32, total_q x num_heads_q x rel_extent).  0 when neither
- * applies.  The workspace must be 16-byte aligned; its contents are scratch.
+ * relative bias is on, room for the bias r . P: the larger of the bias of
+ * every decode row at every distance below rel_extent (fp32, total_q x
+ * num_heads_q x rel_extent; computed by a kernel before the decode) and, when
+ * r is 16-byte aligned with r_dim a multiple of 8 and rel_extent <= 1152,
+ * two slots per SM of one item's bias (fp32, rel_extent rounded up to 128 x
+ * the item's rows rounded up to 4; computed inside the decode kernel on the
+ * tensor cores).  0 when neither applies.  The workspace must be 16-byte
+ * aligned; its contents are scratch.
  */
 relattn_status relattn_decode_workspace_size(const relattn_params *params, size_t *bytes);
 
@@ -254,7 +259,7 @@ relattn_status relattn_combine(const float *o_part, const float *lse_part, int32
  *     over between calls, but two calls whose kernels can overlap on the GPU
  *     (unordered streams) race on it: order them, or use relattn_decode.
  */
-#define RELATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define RELATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 relattn_status relattn_decode_noalloc(const relattn_params *params, void *stream);
 
 /* Reads and clears the device error word (RELATTN_OK when clean).  Synchronises

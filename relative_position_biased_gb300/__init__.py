@@ -46,7 +46,7 @@ TEST_HOOKS = (
     "relattn_test_skip_k_tile", "relattn_test_band_ctas", "relattn_test_prologue_skip_tile",
     "relattn_test_backward_skip_step",
 )
-NOALLOC_SCRATCH_BYTES = 16 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 32 << 20   # RELATTN_NOALLOC_SCRATCH_BYTES
 
 
 class RelattnError(RuntimeError):

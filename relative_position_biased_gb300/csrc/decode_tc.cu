@@ -32,11 +32,21 @@
 // tensor core.  At the end of the item the two partial results are merged
 // like two splits (the max of the two running maxima, each side rescaled).
 //
-// Relative bias: R = r . P for every decode row and distance below E is
-// computed beforehand (relattn_decode_rel_kernel, fp32, in the caller's
-// workspace: a few MB at most); a band tile reads R[row][p_row - j] per (key,
-// row), all sixteen loads issued before any is used.  No sheared tensor, no
-// TMEM ring, so any r_dim <= 64 and any E work.
+// Relative bias, R = r . P, from one of two sources; a band tile reads R at
+// (row, p_row - j) per (key, row), all sixteen loads issued before any is used.
+//   In the kernel (bf16 K / V, r_dim a multiple of 8, E <= 1152): P^T sits in
+//   tensor memory for the whole launch (lane = distance, loaded once per CTA
+//   by the softmax warps), and for each item that reaches the band the score
+//   issuer computes R^T = P^T r^T of its rows on the tensor core (M = 128
+//   distances, N = 16 rows, one 128-distance block at a time) right after the
+//   item's q and r rows land; each softmax warpgroup copies it at the item's
+//   start into its own slot in the workspace (fp32 [distance][row]), from
+//   which its band tiles read.  The slot is private to the warpgroup, so only
+//   the warpgroup's own barrier orders the copy before the reads.
+//   Otherwise (MXFP8 K / V, other shapes): R for every decode row and
+//   distance below E is computed beforehand (relattn_decode_rel_kernel, fp32
+//   [row][E] in the workspace) and the decode is launched as its programmatic
+//   dependent.
 //
 // Warps (11; one CTA per SM walking items in a longest-first order):
 //   warp 0      TMA producer (one thread): the item's q rows (a box of group
@@ -50,10 +60,12 @@
 //               tiles): thread = key of the tile (TMEM lane 32 (warp % 4) +
 //               lane) for the scores, = dim of O^T for the rescale and merge
 //
-// Tensor memory (64 columns): S^T of warpgroup b at 16 b, O^T of warpgroup b
-// at 32 + 16 b.  Shared memory: the two P buffers (16 rows x 128 keys, 4 KB
-// each), the q rows of two items (4 KB each: the next item's load while the
-// current one runs), K and V rings, the merge buffer
+// Tensor memory (64 columns; 512 with the in-kernel R): S^T of warpgroup b at
+// 16 b, O^T of warpgroup b at 32 + 16 b; then P^T (32 columns per 128
+// distances) and the current item's R^T (16 per 128 distances).
+// Shared memory: the two P buffers (16 rows x 128 keys, 4 KB each), the q
+// rows of two items (4 KB each: the next item's load while the current one
+// runs) and their r rows (2 KB each), K and V rings, the merge buffer
 // (warpgroup 1's O^T, 8 KB), per-warpgroup row constants and exchange buffers.
 //
 // Every wait is bounded; a timeout raises the CTA's abort flag and records the
@@ -98,8 +110,16 @@ enum {
   B_Q_FULL = 0, B_Q_EMPTY = B_Q_FULL + 2, B_K_FULL = B_Q_EMPTY + 2, B_K_EMPTY = B_K_FULL + MAXST, B_V_FULL = B_K_EMPTY + MAXST,
   B_V_EMPTY = B_V_FULL + MAXST, B_S_FULL = B_V_EMPTY + MAXST, B_S_FREE = B_S_FULL + 2,
   B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2, B_XCH = B_PV_DONE + 2, B_M_FULL = B_XCH + 2,
-  B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_DRAIN_PV = B_DRAIN + 1, B_COUNT = B_DRAIN_PV + 1
+  B_M_FREE = B_M_FULL + 1, B_DRAIN = B_M_FREE + 1, B_DRAIN_PV = B_DRAIN + 1, B_R_FULL = B_DRAIN_PV + 1,
+  B_R_FREE = B_R_FULL + 1, B_PT_READY = B_R_FREE + 1, B_PT_SMEM_FULL = B_PT_READY + 1,
+  B_PT_SMEM_FREE = B_PT_SMEM_FULL + 1, B_COUNT = B_PT_SMEM_FREE + 1
 };
+// In-kernel R (bf16 kernel): tensor-memory columns past S and O.  P^T takes 32
+// columns (64 bf16 channels) per 128 distances, the R of one item 16 columns
+// (one per row) per 128 distances.
+constexpr uint32_t TM_PT = 64;
+constexpr int kRelTmemCols = 512;
+constexpr int kRelMaxBlocks = 8;   // P staged once in the V ring: 8 x (128 distances x 64 channels) bf16
 
 // Tensor- and shared-memory layout of the bf16 kernel (F8 = false) and of the
 // MXFP8 one (K / V stored as E4M3 codes with one E8M0 scale per 32 dims, q
@@ -120,7 +140,8 @@ struct Lay {
   static constexpr uint32_t QBUF = F8 ? HALF16 : 2 * HALF16;  // bytes of one item's q rows
   static constexpr uint32_t SM_P = 0;
   static constexpr uint32_t SM_Q = SM_P + 4 * HALF16;
-  static constexpr uint32_t SM_K = SM_Q + 4 * HALF16;
+  static constexpr uint32_t SM_R = SM_Q + 4 * HALF16;         // bf16: the r rows of two items (2 KB each)
+  static constexpr uint32_t SM_K = SM_R + (F8 ? 0 : 2 * HALF16);
   // ring stages: K is released right after its score MMA, V only after its
   // P V MMA (bf16) or its dequantisation (fp8), so V holds its stages longer
   // and gets more of them; at the loaded memory's ~2.5 us latency the bytes in
@@ -147,6 +168,14 @@ struct DecArgs {
   const uint32_t *kscale, *vscale;   // MXFP8: E8M0 scale bytes of each (row, kv head), 4 per word
   int kv_rows;                       // rows of the K / V tensors
   int has_bias;
+  // where the relative bias comes from: 1 = R of every decode row computed
+  // beforehand (a.rdec, [total_q * Hq][E]); 2 = computed in the kernel, per
+  // item with band tiles, into this CTA's slots (rslot)
+  int rel_mode;
+  int nt_e;          // 128-distance blocks of E
+  int rs;            // floats per distance in a slot: the item's rows, rounded up to 4
+  int r_bytes;       // bytes of the item's r box
+  float *rslot;      // per (CTA, softmax warpgroup): R^T [nt_e * 128][rs] fp32
   int q_bytes;       // bytes of the item's q box pair
   int n_items;
 };
@@ -185,7 +214,9 @@ __global__ void __launch_bounds__(NTHR, 1)
 relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
                          const __grid_constant__ CUtensorMap map_q,
                          const __grid_constant__ CUtensorMap map_k,
-                         const __grid_constant__ CUtensorMap map_v) {
+                         const __grid_constant__ CUtensorMap map_v,
+                         const __grid_constant__ CUtensorMap map_r,
+                         const __grid_constant__ CUtensorMap map_p) {
   using L = Lay<F8>;
   const KernelArgs &a = da.a;
   extern __shared__ uint8_t smem_raw[];
@@ -253,6 +284,21 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   };
   auto load_item = [&](int idx) -> int { return load_item_into(idx, I); };
   const int n_items = da.n_items;
+  // in-kernel R: tile t of an item is a band tile iff t >= first_band(it)
+  // (its oldest key is within E of the item's first row); an item computes R
+  // iff it has a band tile
+  const bool rel_tc = !F8 && da.rel_mode == 2;
+  auto first_band = [&](const Item &it) -> int {
+    const int x = it.p0 - it.kbeg - (KT - 1) - a.E;
+    return x < 0 ? 0 : x / KT + 1;
+  };
+  auto band_item = [&](const Item &it) -> bool { return rel_tc && first_band(it) < it.ntiles; };
+  // the 128-distance blocks an item's band tiles read: its distances run
+  // from p0 - (last key of its tiles) to p_last - (first key), clipped to E
+  auto r_lo = [&](const Item &it) -> int { return max(0, it.p0 - (it.kbeg + KT * it.ntiles - 1)) / KT; };
+  auto r_hi = [&](const Item &it) -> int { return min(da.nt_e - 1, (it.p_last - it.kbeg) / KT); };
+  const uint32_t tmem_cols = rel_tc ? (uint32_t)kRelTmemCols : L::TMEM_COLS;
+  const uint32_t TM_RS = TM_PT + 32u * (uint32_t)da.nt_e;   // R of the current item
 
   // ------------------------------------------------------------ set-up
   // q and the P buffers start as zeros: rows past an item's real ones then
@@ -282,17 +328,26 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     mbar_init(bar(B_M_FREE), 128);
     mbar_init(bar(B_DRAIN), 1);
     mbar_init(bar(B_DRAIN_PV), 1);
+    mbar_init(bar(B_R_FULL), 1);
+    mbar_init(bar(B_R_FREE), 256);
+    mbar_init(bar(B_PT_READY), 256);
+    mbar_init(bar(B_PT_SMEM_FULL), 1);
+    mbar_init(bar(B_PT_SMEM_FREE), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sb + L::SM_TMEM_SLOT, L::TMEM_COLS);
+    tmem_alloc(sb + L::SM_TMEM_SLOT, tmem_cols);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&map_q);
     prefetch_tmap(&map_k);
     prefetch_tmap(&map_v);
+    if (rel_tc) {
+      prefetch_tmap(&map_r);
+      prefetch_tmap(&map_p);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -352,6 +407,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   asm volatile("griddepcontrol.launch_dependents;");
   // the producer's copies, drained if the CTA gives up
   int issued_q = 0, issued_k = 0, issued_v = 0;
+  bool issued_pt = false;
 
   if (warp == 0) {
     // ====================================================== TMA producer
@@ -390,6 +446,19 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     };
     bool k_live = next_item(kidx, ik), v_live = next_item(vidx, iv), q_due = k_live;
     long long idle_since = -1;
+    // in-kernel R: P [r_dim][E] into the (still empty) V ring, 128 distances
+    // x r_dim channels per box; the V copies start once the softmax warps
+    // have moved it into tensor memory
+    bool pt_free = !rel_tc;
+    if (rel_tc) {
+      if (lane == 0) {
+        const uint32_t box = 256u * (uint32_t)a.rd;
+        mbar_arrive_expect_tx(bar(B_PT_SMEM_FULL), box * (uint32_t)da.nt_e);
+        for (int u = 0; u < da.nt_e; ++u)
+          tma_load_2d(sb + L::SM_V + box * (uint32_t)u, &map_p, KT * u, 0, bar(B_PT_SMEM_FULL));
+      }
+      issued_pt = true;
+    }
     for (;;) {
       // (lane 0's view of the abort flag, so the whole warp leaves together)
       const bool quit = __shfl_sync(0xffffffffu, (lane == 0 && *abort_flag) ? 1 : 0, 0) != 0;
@@ -426,11 +495,15 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q_FULL + qb));
           } else if (lane == 0) {
-            // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves of 64 dims
-            mbar_arrive_expect_tx(bar(B_Q_FULL + qb), (uint32_t)da.q_bytes);
+            // the item's q rows: [tokens][group heads][128 dims] as two 2 KB halves of 64 dims;
+            // with in-kernel R, an item with band tiles also brings its r rows
+            // ([tokens][group heads][64 channels], channels past r_dim read as 0)
+            const bool rb = band_item(ik);
+            mbar_arrive_expect_tx(bar(B_Q_FULL + qb), (uint32_t)(da.q_bytes + (rb ? da.r_bytes : 0)));
             tma_load_3d(sb + L::SM_Q + qb * L::QBUF, &map_q, 0, ik.g * a.group, ik.cq, bar(B_Q_FULL + qb));
             tma_load_3d(sb + L::SM_Q + qb * L::QBUF + HALF16, &map_q, 64, ik.g * a.group, ik.cq,
                         bar(B_Q_FULL + qb));
+            if (rb) tma_load_3d(sb + L::SM_R + qb * HALF16, &map_r, 0, ik.g * a.group, ik.cq, bar(B_Q_FULL + qb));
           }
           issued_q = ++n_q;
           q_due = false;
@@ -455,7 +528,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           moved = true;
         }
       }
-      if (v_live && GV < GK) {
+      if (!pt_free) pt_free = ready(bar(B_PT_SMEM_FREE), 0);
+      if (v_live && GV < GK && pt_free) {
         const int st = GV % L::VST;
         if (GV < L::VST || ready(bar(B_V_EMPTY + st), ((GV / L::VST) - 1) & 1)) {
           if (lane == 0) {
@@ -503,15 +577,49 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       const uint32_t id_s8 = idesc_e4m3_f32(KT, NR);
       auto koff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (BOX >> 4) + 2 * (k - 4)); };
       auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
-      int T = 0, n_it = 0;
+      // in-kernel R: R^T[d][row] = P^T[d] . r[row] per 128-distance block
+      // (P^T in TMEM as the A operand, the item's r rows K-major in shared memory)
+      const uint64_t rd0 = smem_desc_sw128(sb + L::SM_R, 16, 1024);
+      const int r_ksteps = a.rd_pad / 16;
+      int T = 0, n_it = 0, n_rel = 0;
       bool ok = true;
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         const int qb = n_it & 1;
         if (!(ok = mbar_wait(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
         const uint64_t qd = qd0 + (uint64_t)((qb * L::QBUF) >> 4);
+        // in-kernel R of a band item, one 128-distance block at a time ahead
+        // of the score MMAs of the tiles before the band, so that the last
+        // block goes in before S of the tile before the first band tile (or
+        // all of them before S(0) when the band starts at once)
+        const bool rb = band_item(I);
+        const int t_b = rb ? first_band(I) : I.ntiles;
+        const int u_lo = rb ? r_lo(I) : 0, n_u = rb ? r_hi(I) - u_lo + 1 : 0;
+        int r_done = 0;   // blocks issued: u_lo .. u_lo + r_done - 1
+        auto issue_r = [&](int upto) -> bool {
+          if (r_done >= upto) return true;
+          if (r_done == 0) {
+            // P^T is in TMEM (once per CTA); the previous item's R has been read out
+            if (n_rel == 0 && !mbar_wait(bar(B_PT_READY), 0, abort_flag, 21)) return false;
+            if (n_rel > 0 && !mbar_wait(bar(B_R_FREE), (n_rel - 1) & 1, abort_flag, 22)) return false;
+            tc_fence_after();
+          }
+          const uint64_t rdesc = rd0 + (uint64_t)((qb * HALF16) >> 4);
+          for (; r_done < upto; ++r_done) {
+            const uint32_t u = (uint32_t)(u_lo + r_done);
+            const uint32_t d = tmem + TM_RS + 16u * u, pa = tmem + TM_PT + 32u * u;
+            mma_ts_c<0>(d, pa, rdesc, id_s);
+            for (int k = 1; k < r_ksteps; ++k) mma_ts_c<1>(d, pa + 8u * (uint32_t)k, rdesc + 2 * k, id_s);
+          }
+          if (r_done == n_u) {
+            mma_commit(bar(B_R_FULL));
+            ++n_rel;
+          }
+          return true;
+        };
         for (int t = 0; t < I.ntiles && ok; ++t) {
           const int G = T + t, b = G & 1, st = G % L::KST;
+          if (rb && t <= t_b && !(ok = issue_r(min(n_u, max(0, n_u - (t_b - 1 - t)))))) break;
           if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
           if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / L::KST) & 1, abort_flag, 8))) break;
           tc_fence_after();
@@ -603,15 +711,67 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       const bool r = mbar_wait(br, parity, abort_flag, site);
       return __all_sync(0xffffffffu, r);
     };
-    int n_xch = 0, n_merge = 0;
+    int n_xch = 0, n_merge = 0, n_rel = 0;
     bool r_ready = false;
+    bool ok = true;
     // the warpgroup's 128 threads meet
     auto xch_barrier = [&]() -> bool {
       mbar_arrive(bar(B_XCH + wg));
       return warp_wait(bar(B_XCH + wg), (n_xch++) & 1, 10);
     };
+    // in-kernel R: this warpgroup's slot, R^T [nt_e * 128 distances][rs rows]
+    const uint32_t rslot_off = rel_tc ? ((uint32_t)blockIdx.x * 2u + (uint32_t)wg) * (uint32_t)(da.nt_e * 128 * da.rs) : 0u;
+    if (rel_tc) {
+      // P^T into TMEM, once per CTA, from the copy of P the producer put in
+      // the V ring ([r_dim][128] bf16 per block of 128 distances; distances
+      // past E read as 0): lane = distance 128 u + key of block u (warpgroup
+      // wg takes the blocks u = wg mod 2), channels as bf16 pairs over 32
+      // columns, zero past r_dim.  Then the V ring is the producer's again.
+      ok = warp_wait(bar(B_PT_SMEM_FULL), 0, 24);
+      if (ok) {
+        for (int u = wg; u < da.nt_e; u += 2) {
+          const unsigned short *src =
+              reinterpret_cast<const unsigned short *>(smem + L::SM_V + 256u * (uint32_t)a.rd * (uint32_t)u) + key;
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t lo = 2 * c < a.rd ? (uint32_t)src[(2 * c) * 128] : 0u;
+            const uint32_t hi = 2 * c + 1 < a.rd ? (uint32_t)src[(2 * c + 1) * 128] : 0u;
+            w[c] = lo | (hi << 16);
+          }
+          __syncwarp();
+          tmem_st32(tmem + lane_base + TM_PT + 32u * (uint32_t)u, w);
+        }
+        mbar_arrive(bar(B_PT_SMEM_FREE));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_PT_READY));
+      }
+    }
+    // in-kernel R: this warpgroup's copy of the current item's R into its slot
+    // (thread = distance 128 u + key, its rs rows as 16-byte stores), then the
+    // warpgroup meets so that every thread's stores precede every band read
+    auto extract_r = [&]() -> bool {
+      if (!warp_wait(bar(B_R_FULL), n_rel & 1, 23)) return false;
+      tc_fence_after();
+      // (four columns per load: the copy runs inside the tile loop, where
+      // the row sums and scores hold most registers)
+      const int u_end = r_hi(I);
+      for (int u = r_lo(I); u <= u_end; ++u) {
+        float4 *dst = reinterpret_cast<float4 *>(da.rslot + rslot_off + (uint32_t)((128 * u + key) * da.rs));
+        for (int q4 = 0; 4 * q4 < da.rs; ++q4) {
+          uint32_t v[4];
+          tmem_ld4(tmem + lane_base + TM_RS + 16u * (uint32_t)u + 4u * (uint32_t)q4, v);
+          tmem_wait_ld(v);
+          dst[q4] = make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                                __uint_as_float(v[3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_R_FREE));
+      return xch_barrier();
+    };
     int T = 0;
-    bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const int li = load_item(idx);
       if (li <= 0) continue;
@@ -648,21 +808,56 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
 #pragma unroll
       for (int i = 0; i < NR; ++i) lp[i] = 0.f;
       int tl = 0;                                // this warpgroup's tiles of the item so far
+      // in-kernel R: this warpgroup copies the item's R just before its first
+      // band tile t_w -- at the end of its tile t_w - 2, or at the top of t_w
+      // when that is its first tile of the item
+      // (copy_at: t_w while the copy is due, else -4)
+      int copy_at = -4;
+      if (band_item(I)) {
+        const int t_b = first_band(I);
+        copy_at = t_b + ((t_b - ((wg - T) & 1)) & 1);
+      }
       for (int t = (wg - T) & 1; t < I.ntiles && ok; t += 2, ++tl) {
         const int G = T + t;
         const int j0 = I.kbeg + KT * t, j = j0 + key;
         const bool band = has_bias && (I.p_last - j0 >= 0) && (I.p0 - (j0 + KT - 1) < a.E);
         const bool edge = (j0 + KT - 1 > I.p0) || (a.window > 0 && j0 < I.p_last - a.window + 1);
+        if (t == copy_at) {
+          if (!(ok = extract_r())) break;
+          copy_at = -4;
+        }
         // band tiles: R[row][p_row - j] for this key, every load issued before
         // the S wait (an index outside the band reads R[0] and is discarded)
         float rbias[NR];
-        if (band && !r_ready) {
+        if (band && !rel_tc && !r_ready) {
           // launched as a programmatic dependent of the R kernel: its rows are
           // complete and visible past this point
           asm volatile("griddepcontrol.wait;" ::: "memory");
           r_ready = true;
         }
-        if (band) {
+        if (band && rel_tc && (a.group & 3) == 0) {
+          // rows in fours of one token: one 16-byte load per four rows
+#pragma unroll
+          for (int q4 = 0; q4 < NR / 4; ++q4) {
+            const int dd = __float_as_int(rowc[4 * q4].z) - j;
+            const bool in = dd >= 0 && dd < a.E && 4 * q4 < da.rs;
+            const float4 rv =
+                *reinterpret_cast<const float4 *>(da.rslot + rslot_off + (in ? (uint32_t)(dd * da.rs + 4 * q4) : 0u));
+            rbias[4 * q4] = in ? rv.x * rowc[4 * q4].y : 0.f;
+            rbias[4 * q4 + 1] = in ? rv.y * rowc[4 * q4 + 1].y : 0.f;
+            rbias[4 * q4 + 2] = in ? rv.z * rowc[4 * q4 + 2].y : 0.f;
+            rbias[4 * q4 + 3] = in ? rv.w * rowc[4 * q4 + 3].y : 0.f;
+          }
+        } else if (band && rel_tc) {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float4 rc = rowc[i];
+            const int dd = __float_as_int(rc.z) - j;
+            const bool in = dd >= 0 && dd < a.E && i < da.rs;
+            const float rv = da.rslot[rslot_off + (in ? (uint32_t)(dd * da.rs + i) : 0u)];
+            rbias[i] = in ? rv * rc.y : 0.f;
+          }
+        } else if (band) {
 #pragma unroll
           for (int i = 0; i < NR; ++i) {
             const float4 rc = rowc[i];
@@ -829,6 +1024,10 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(B_P_FULL + wg));
+        if (t + 2 == copy_at) {
+          if (!(ok = extract_r())) break;
+          copy_at = -4;
+        }
       }
       if (!ok) break;
       // ---- this warpgroup's row sums and max; its O^T once its last PV has landed
@@ -909,6 +1108,20 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         }
       }
       if constexpr (F8) mbar_arrive(bar(B_Q_EMPTY + (n_merge & 1)));   // the item's q scales are read
+      if (band_item(I)) {
+        // a warpgroup without a band tile in the item releases its R here,
+        // after the merge hand-off: the other warpgroup's release for the
+        // previous item is in by then, so the arrivals of two items never mix.
+        // It still waits for this item's R first, so that every warpgroup
+        // takes every phase of R_FULL in turn (a parity wait that skipped a
+        // phase could pass on the one before)
+        if (copy_at >= 0) {
+          if (!(ok = warp_wait(bar(B_R_FULL), n_rel & 1, 25))) break;
+          tc_fence_before();
+          mbar_arrive(bar(B_R_FREE));
+        }
+        ++n_rel;
+      }
       ++n_merge;
       T += I.ntiles;
     }
@@ -923,6 +1136,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     // the CTA gave up: let the producer's own copies land before shared memory
     // goes away (bounded waits, not cut short by the abort)
     volatile int keep_waiting = 0;
+    if (issued_pt) mbar_wait(bar(B_PT_SMEM_FULL), 0, &keep_waiting, 15, 400000000ll);
     for (int n = max(0, issued_q - 2); n < issued_q; ++n)
       mbar_wait(bar(B_Q_FULL + (n & 1)), (n >> 1) & 1, &keep_waiting, 15, 400000000ll);
     for (int G = max(0, issued_k - L::KST); G < issued_k; ++G)
@@ -933,7 +1147,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, L::TMEM_COLS);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
@@ -996,13 +1210,14 @@ __global__ void __launch_bounds__(RD) relattn_decode_rel_kernel(const KernelArgs
     if (row0 + i < rows) R[(row0 + i) * a.E + d] = acc[i];
 }
 
-// Launch as a programmatic dependent of the kernel before it on the stream
-// (the decode-row R kernel): the CTAs start as soon as it lets them, and only
-// band tiles wait for its rows.  After any other kernel this is an ordinary
-// stream-ordered launch.
+// With pdl, launch as a programmatic dependent of the kernel before it on the
+// stream, which must be the decode-row R kernel: the CTAs start as soon as it
+// lets them, and only band tiles wait for its rows.  Otherwise an ordinary
+// stream-ordered launch (the kernel before it may be anything).
 template <typename K>
-cudaError_t launch_dependent(K kernel, int grid, uint32_t smem, cudaStream_t stream, const DecArgs &da,
-                             const CUtensorMap &m0, const CUtensorMap &m1, const CUtensorMap &m2) {
+cudaError_t launch_decode_kernel(K kernel, int grid, uint32_t smem, cudaStream_t stream, const DecArgs &da,
+                                 const CUtensorMap &m0, const CUtensorMap &m1, const CUtensorMap &m2,
+                                 const CUtensorMap &m3, const CUtensorMap &m4, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(NTHR);
@@ -1011,10 +1226,21 @@ cudaError_t launch_dependent(K kernel, int grid, uint32_t smem, cudaStream_t str
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, da, m0, m1, m2);
+  cfg.attrs = pdl ? &attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, da, m0, m1, m2, m3, m4);
 }
+
+// R = r . P of the decode rows before the decode kernel (rel_mode 1)
+cudaError_t launch_decode_rel(const KernelArgs &a, cudaStream_t stream) {
+  const long rrows = (long)a.total_q * a.Hq;
+  dim3 g((unsigned)((rrows + RR - 1) / RR), (unsigned)((a.E + RD - 1) / RD));
+  relattn_decode_rel_kernel<<<g, RD, 0, stream>>>(a, const_cast<float *>(a.rdec));
+  return cudaGetLastError();
+}
+
+// CTAs of a few-row decode launch (one per SM at most)
+long decode_grid(const KernelArgs &a, long items) { return std::min<long>(items, a.sms > 0 ? a.sms : items); }
 
 PFN_cuTensorMapEncodeTiled_v12000 dec_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
@@ -1064,9 +1290,31 @@ bool decode_mxfp8_supported(const KernelArgs &a, const void *k8, const void *v8,
   return kv_rows >= KT;
 }
 
+// In-kernel R (bf16 few-row kernel): r rows by TMA (16-byte rows and base),
+// r_dim <= 64, and P^T plus one item's R beside S and O in 512 TMEM columns
+bool decode_rel_in_kernel(const KernelArgs &a) {
+  if (!(a.rd > 0 && a.E > 0) || a.sms <= 0) return false;
+  if (a.rd % 8 != 0 || a.rd > 64 || (reinterpret_cast<uintptr_t>(a.r) & 15u) != 0) return false;
+  // P [r_dim][E] by TMA: 16-byte rows and base; all of it staged in the V ring at once
+  if (a.E % 8 != 0 || (reinterpret_cast<uintptr_t>(a.P) & 15u) != 0) return false;
+  const long nt = (a.E + 127) / 128;
+  static_assert(kRelMaxBlocks * 128 * 64 * 2 <= Lay<false>::VST * Lay<false>::KTILE, "P fits the V ring");
+  return nt <= kRelMaxBlocks && (long)TM_PT + nt * 48 <= kRelTmemCols;
+}
+
+int decode_rel_rs(const KernelArgs &a) { return (a.group * a.max_q + 3) / 4 * 4; }
+
+// workspace for either source of R: the rows of every decode row (R kernel,
+// MXFP8 decode or a shape the in-kernel path does not take), or two slots per
+// CTA (in-kernel)
 size_t decode_rel_bytes(const KernelArgs &a) {
   if (!(a.rd > 0 && a.E > 0)) return 0;
-  return (size_t)a.total_q * a.Hq * a.E * sizeof(float);
+  size_t b = (size_t)a.total_q * a.Hq * a.E * sizeof(float);
+  if (decode_rel_in_kernel(a)) {
+    const size_t slots = (size_t)a.sms * 2 * ((a.E + 127) / 128) * 128 * decode_rel_rs(a) * sizeof(float);
+    b = std::max(b, slots);
+  }
+  return b;
 }
 
 cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_t stream) {
@@ -1080,25 +1328,50 @@ cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   da.n_items = (int)items;
-  if (da.has_bias) {
-    // R for the decode rows first (same stream)
-    const long rrows = (long)a.total_q * a.Hq;
-    dim3 g((unsigned)((rrows + RR - 1) / RR), (unsigned)((a.E + RD - 1) / RD));
-    relattn_decode_rel_kernel<<<g, RD, 0, stream>>>(a, const_cast<float *>(a.rdec));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mr;
   if (!encode_heads(&mq, a.q, a.Hq, a.total_q, a.group, a.max_q) ||
       !encode_heads(&mk, a.k, a.Hkv, kv_rows, 1, KT) || !encode_heads(&mv, a.v, a.Hkv, kv_rows, 1, KT))
     return cudaErrorInvalidValue;
+  CUtensorMap mp = mq;
+  mr = mq;   // (unused unless R is computed in the kernel)
+  da.rel_mode = !da.has_bias ? 0 : decode_rel_in_kernel(a) ? 2 : 1;
+  da.nt_e = (a.E + 127) / 128;
+  da.rs = decode_rel_rs(a);
+  da.r_bytes = 128 * a.group * a.max_q;
+  da.rslot = const_cast<float *>(a.rdec);
+  if (da.rel_mode == 2) {
+    // r [total_q, Hq, r_dim] in boxes of 64 channels x group heads x max_q
+    // tokens (channels past r_dim read as 0), 128-byte swizzle
+    auto fn = dec_encoder();
+    cuuint64_t dims[3] = {(cuuint64_t)a.rd, (cuuint64_t)a.Hq, (cuuint64_t)a.total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)a.rd * 2, (cuuint64_t)a.Hq * a.rd * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)a.group, (cuuint32_t)a.max_q};
+    cuuint32_t es[3] = {1, 1, 1};
+    // P [r_dim, E] in boxes of 128 distances x r_dim channels (distances past
+    // E read as 0), no swizzle: [r_dim][128] bf16 per box
+    cuuint64_t pdims[2] = {(cuuint64_t)a.E, (cuuint64_t)a.rd};
+    cuuint64_t pstrides[1] = {(cuuint64_t)a.E * 2};
+    cuuint32_t pbox[2] = {(cuuint32_t)KT, (cuuint32_t)a.rd};
+    if (fn(&mr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16 *>(a.r), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        fn(&mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(a.P), pdims, pstrides, pbox, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      da.rel_mode = 1;
+  }
+  if (da.rel_mode == 1) {
+    // R for the decode rows first (same stream)
+    cudaError_t e = launch_decode_rel(a, stream);
+    if (e != cudaSuccess) return e;
+  }
   static std::atomic<bool> attr_set[kMaxDevicesAttr];
   constexpr uint32_t smem = Lay<false>::SMEM_BYTES;
   cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<false>),
                                     (int)smem, attr_set);
   if (e != cudaSuccess) return e;
-  return launch_dependent(relattn_decode_tc_kernel<false>, (int)std::min<long>(items, a.sms > 0 ? a.sms : items),
-                          smem, stream, da, mq, mk, mv);
+  return launch_decode_kernel(relattn_decode_tc_kernel<false>, (int)decode_grid(a, items), smem, stream, da, mq,
+                              mk, mv, mr, mp, da.rel_mode == 1);
 }
 
 cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void *v8, const void *ks,
@@ -1114,11 +1387,11 @@ cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void 
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   da.n_items = (int)items;
+  da.rel_mode = da.has_bias ? 1 : 0;
+  da.nt_e = da.rs = da.r_bytes = 0;
+  da.rslot = nullptr;
   if (da.has_bias) {
-    const long rrows = (long)a.total_q * a.Hq;
-    dim3 g((unsigned)((rrows + RR - 1) / RR), (unsigned)((a.E + RD - 1) / RD));
-    relattn_decode_rel_kernel<<<g, RD, 0, stream>>>(a, const_cast<float *>(a.rdec));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_decode_rel(a, stream);
     if (e != cudaSuccess) return e;
   }
   // E4M3 codes [rows, heads, 128] in boxes of 128 dims x 1 head x 128 rows
@@ -1141,9 +1414,10 @@ cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void 
   cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<true>),
                                     (int)smem, attr_set);
   if (e != cudaSuccess) return e;
-  // (the q map is not read: the producer quantises q rows itself)
-  return launch_dependent(relattn_decode_tc_kernel<true>, (int)std::min<long>(items, a.sms > 0 ? a.sms : items),
-                          smem, stream, da, mk, mk, mv);
+  // (the q and r maps are not read: the producer quantises q rows itself,
+  // and R comes from the R kernel)
+  return launch_decode_kernel(relattn_decode_tc_kernel<true>, (int)decode_grid(a, items), smem, stream, da, mk,
+                              mk, mv, mk, mk, da.rel_mode == 1);
 }
 
 }  // namespace relattn

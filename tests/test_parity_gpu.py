@@ -155,6 +155,19 @@ def test_decode_splits(Lq, splits):
     _check(W.custom(f"dec{Lq}", [Lq] * 4, ks, 16, 2, 32, 256), decode=True, num_splits=splits)
 
 
+# Few-row decode bias sources: in the kernel on the tensor cores (r_dim a
+# multiple of 8, rel_extent up to 1152: 9 blocks of 128 distances, r_dim and
+# E at and past the block edges), else computed by a kernel before the decode
+# (r_dim 20, rel_extent 1500).  One token per sequence (one distance per item)
+# and two (a distance per token), full and windowed keys.
+@pytest.mark.parametrize("rd,E", [(8, 1), (64, 1152), (40, 129), (24, 640), (20, 700), (64, 1500)])
+@pytest.mark.parametrize("Lq,window", [(1, 0), (2, 0), (1, 900)])
+def test_decode_bias_sources(rd, E, Lq, window):
+    ks = [2500, 1300, 129, 600 + Lq, Lq]
+    _check(W.custom(f"dec_bias{rd}_{E}", [Lq] * len(ks), ks, 16, 2, rd, E, window=window), decode=True,
+           num_splits=2)
+
+
 @pytest.mark.parametrize("window", [1, 5, 300])
 def test_decode_window(window):
     ks = [700, 1500, 300]

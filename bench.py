@@ -237,6 +237,19 @@ def _kw(w):
 ARG_ORDER = ("q", "k", "v", "r", "P", "cu_seqlens_q", "cu_seqlens_k")
 
 
+def decode_prepass(w, mxfp8):
+    """Whether a decode call of w launches the decode-row bias kernel first:
+    few-row items (<= 16 rows per kv head) with a bias, unless the bf16
+    few-row kernel computes the bias itself (r_dim a multiple of 8 and at
+    most 64, rel_extent a multiple of 8 and at most 1024)."""
+    few = max(w.q_lens) * (w.Hq // w.Hkv) <= 16
+    if not (few and w.r_dim > 0 and w.rel_extent > 0):
+        return False
+    in_kernel = (not mxfp8 and w.r_dim % 8 == 0 and w.r_dim <= 64 and w.rel_extent % 8 == 0
+                 and w.rel_extent <= 1024)
+    return not in_kernel
+
+
 class Phase:
     """One timed call of the library on device-resident inputs."""
 
@@ -258,11 +271,10 @@ class Phase:
             self.ws = rpb.decode_workspace(prm, "cuda")
             st, splits = rpb.relattn_decode_num_splits(prm)
             self.splits = splits
-            # few-row items (<= 16 rows per kv head) with a bias: the decode-row
-            # bias pre-pass, then the decode; the combine when split
-            few = max(w.q_lens) * (w.Hq // w.Hkv) <= 16
-            prepass = few and w.r_dim > 0 and w.rel_extent > 0
-            self.launches = 1 + (1 if prepass else 0) + (1 if splits > 1 else 0)
+            # the decode, the combine when split, and the decode-row bias pre-pass
+            # when the few-row kernel cannot compute the bias itself
+            self.split_launch = 1 if splits > 1 else 0
+            self.launches = 1 + self.split_launch + (1 if decode_prepass(w, mxfp8=False) else 0)
         self.flops = A.flops(w)
         self.bytes = A.kv_bytes(w)
         io = A.io_bytes(w)
@@ -345,7 +357,7 @@ class Mxfp8DecodePhase:
         a = base.args
         self.k8, self.ks = rpb.quantize_mxfp8(a[1])
         self.v8, self.vs = rpb.quantize_mxfp8(a[2])
-        self.launches = base.launches
+        self.launches = 1 + base.split_launch + (1 if decode_prepass(base.w, mxfp8=True) else 0)
         self.bytes = A.kv_bytes_mxfp8(base.w)      # bytes the kernel must read
         self.bytes_bf16 = base.bytes                 # the same keys in bf16
 

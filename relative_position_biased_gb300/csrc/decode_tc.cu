@@ -48,7 +48,17 @@
 //   [row][E] in the workspace) and the decode is launched as its programmatic
 //   dependent.
 //
-// Warps (11; one CTA per SM walking items in a longest-first order):
+// Work split: with several splits (and at most 64 sequences) the walk is
+// stream-K: the (sequence, kv head) units' tiles are laid end to end and CTA
+// c takes the range [c C, (c + 1) C), C = ceil(total / CTAs) (at least a
+// bound that keeps every unit within num_splits pieces); each piece of a unit
+// writes its partial into split slot c - (first CTA of the unit), the unit's
+// first piece marks the slots no piece fills as empty, and the combine merges
+// them.  Every CTA then streams the same number of tiles.  Otherwise each CTA
+// walks a fixed share of the (split, sequence, kv head) items in a
+// longest-first order.
+//
+// Warps (11; one CTA per SM):
 //   warp 0      TMA producer (one thread): the item's q rows (a box of group
 //               heads x tokens), then K and V tiles (rings of 2-4 stages); the
 //               rings run on across items
@@ -172,6 +182,11 @@ struct DecArgs {
   // beforehand (a.rdec, [total_q * Hq][E]); 2 = computed in the kernel, per
   // item with band tiles, into this CTA's slots (rslot)
   int rel_mode;
+  // stream-K walk (several splits, at most kOrd sequences): CTA c takes tiles
+  // [c C, (c + 1) C) of the (sequence, kv head) units laid end to end, with
+  // C = max(c_min, ceil(total tiles / CTAs)); c_min caps a unit's pieces at
+  // num_splits
+  int streamk, c_min;
   int nt_e;          // 128-distance blocks of E
   int rs;            // floats per distance in a slot: the item's rows, rounded up to 4
   int r_bytes;       // bytes of the item's r box
@@ -207,6 +222,7 @@ __device__ __forceinline__ float transpose_reduce(const float (&v)[NR], int lane
 
 struct Item {
   int b, g, sp, cq, ck, nrows, p0, p_last, kbeg, ntiles;
+  int np;   // stream-K: the pieces of the item's (sequence, kv head) unit
 };
 
 template <bool F8>
@@ -239,9 +255,26 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   Item I{};
   int *ord = reinterpret_cast<int *>(smem + L::SM_ORD);
   const bool sorted = a.batch <= kOrd;
+  const bool sk = da.streamk != 0 && sorted;
   auto load_item_into = [&](int idx, Item &it) -> int {   // 1 work, 0 nothing, -1 inconsistent lengths
     int q, u;
-    if (sorted) {
+    int t_lo = 0, t_hi = 0;
+    if (sk) {
+      // piece idx of this CTA's tile range: unit u_a + idx, the part of its
+      // tiles inside [R0, R1)
+      const int C = ord[ORD_NP], T = ord[ORD_PF + a.batch];
+      const int uu = ord[ORD_NP + 1] + idx;
+      it.b = uu / a.Hkv;
+      u = uu - it.b * a.Hkv;
+      const int U = ord[ORD_NF + it.b], P = ord[ORD_PF + it.b] + u * U;
+      const int R0 = (int)blockIdx.x * C, R1 = min(R0 + C, T);
+      t_lo = max(R0, P) - P;
+      t_hi = min(R1, P + U) - P;
+      it.sp = (int)blockIdx.x - P / C;
+      it.np = U > 0 ? (P + U - 1) / C - P / C + 1 : 0;
+      // (a unit never has more pieces than split slots: c_min sees to that)
+      if (it.sp < 0 || it.np > a.num_splits) return -1;
+    } else if (sorted) {
       const int Gd = gridDim.x, r = idx / Gd, c = idx - r * Gd;
       const int pos = ((r & 1) && (r + 1) * Gd <= da.n_items) ? r * Gd + (Gd - 1 - c) : idx;
       q = pos / a.Hkv;
@@ -277,9 +310,15 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     it.p_last = it.p0 + Lq - 1;
     const int j_lo = a.window > 0 ? max(0, it.p0 - a.window + 1) : 0;
     const int kbase = j_lo & ~(KT - 1);
+    if (sk) {
+      it.kbeg = kbase + KT * t_lo;
+      it.ntiles = max(0, t_hi - t_lo);
+      return 1;
+    }
     it.kbeg = kbase + it.sp * a.split_chunk;
     const int kend = min(it.p_last + 1, it.kbeg + a.split_chunk);
     it.ntiles = kend > it.kbeg ? (kend - it.kbeg + KT - 1) / KT : 0;
+    it.np = a.num_splits;
     return 1;
   };
   auto load_item = [&](int idx) -> int { return load_item_into(idx, I); };
@@ -372,11 +411,34 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         vis = (long)p_last + 1 - (j_lo & ~(KT - 1));
       }
       const long nf = min((long)a.num_splits, vis / a.split_chunk);
-      ord[ORD_NF + b] = (int)nf;
+      // (stream-K: the unit's tiles instead)
+      ord[ORD_NF + b] = sk ? (int)((vis + KT - 1) / KT) : (int)nf;
       ord[ORD_REM + b] = nf < a.num_splits ? (int)(vis - nf * a.split_chunk) : 0;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (sk) {
+      // stream-K: tiles before each sequence's units, the CTA's range and
+      // its first unit and piece count
+      if (tid == 0) {
+        int t = 0;
+        for (int i = 0; i < a.batch; ++i) {
+          ord[ORD_PF + i] = t;
+          t += a.Hkv * ord[ORD_NF + i];
+        }
+        ord[ORD_PF + a.batch] = t;
+        const int C = max(da.c_min, (t + (int)gridDim.x - 1) / (int)gridDim.x);
+        const int R0 = (int)blockIdx.x * C, R1 = min(R0 + C, t);
+        auto unit_of = [&](int tile) {   // the unit holding tile (tile < t)
+          int b = 0;
+          while (b + 1 < a.batch && ord[ORD_PF + b + 1] <= tile) ++b;
+          return b * a.Hkv + (tile - ord[ORD_PF + b]) / ord[ORD_NF + b];
+        };
+        const int ua = R0 < t ? unit_of(R0) : 0;
+        ord[ORD_NP] = C;
+        ord[ORD_NP + 1] = ua;
+        ord[ORD_PZ] = R0 < t ? unit_of(R1 - 1) - ua + 1 : 0;
+      }
+    } else if (tid == 0) {
       int f = 0, z = 0, np = 0;
       for (int i = 0; i < a.batch; ++i) {
         ord[ORD_PF + i] = f;
@@ -403,6 +465,9 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
   }
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::SM_TMEM_SLOT);
+  // this CTA's walk: idx = w0, w0 + wS, ... below wN (stream-K: its pieces in
+  // order; else every gridDim.x-th slot of the order)
+  const int w0 = sk ? 0 : (int)blockIdx.x, wS = sk ? 1 : (int)gridDim.x, wN = sk ? ord[ORD_PZ] : n_items;
   // the combine after this kernel may launch (it waits for every CTA's partials)
   asm volatile("griddepcontrol.launch_dependents;");
   // the producer's copies, drained if the CTA gives up
@@ -419,10 +484,10 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     // warp-uniform: lane 0 probes the barriers and issues the copies, the
     // decisions are broadcast.
     Item ik{}, iv{};
-    int kidx = (int)blockIdx.x - (int)gridDim.x, vidx = kidx, kt = 0, vt = 0;
+    int kidx = w0 - wS, vidx = kidx, kt = 0, vt = 0;
     int GK = 0, GV = 0, n_q = 0;
     auto next_item = [&](int &idx, Item &it) -> bool {
-      for (idx += gridDim.x; idx < n_items; idx += gridDim.x) {
+      for (idx += wS; idx < wN; idx += wS) {
         const int li = load_item_into(idx, it);
         if (li < 0 && lane == 0 && &it == &ik) atomicOr(a.err, kDevErrSeqlens);
         if (li > 0 && it.ntiles > 0) return true;
@@ -583,7 +648,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       const int r_ksteps = a.rd_pad / 16;
       int T = 0, n_it = 0, n_rel = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      for (int idx = w0; idx < wN && ok; idx += wS) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         const int qb = n_it & 1;
         if (!(ok = mbar_wait(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
@@ -660,7 +725,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       auto hoff = [](int k) -> uint64_t { return (uint64_t)((k < 4) ? 2 * k : (HALF16 >> 4) + 2 * (k - 4)); };
       int T = 0;
       bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      for (int idx = w0; idx < wN && ok; idx += wS) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         for (int t = 0; t < I.ntiles && ok; ++t) {
           // O^T of warpgroup G % 2 (+)= V(G)^T P(G)^T; the warpgroup's first tile of the item overwrites
@@ -772,7 +837,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       return xch_barrier();
     };
     int T = 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int idx = w0; idx < wN && ok; idx += wS) {
       const int li = load_item(idx);
       if (li <= 0) continue;
       const int nrows = I.nrows;
@@ -1100,6 +1165,11 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           const float row_lse = (lrow > 0.f && mrow != -INFINITY) ? (mrow + __log2f(lrow)) * kLn2 : -INFINITY;
           const size_t qrow = (size_t)__float_as_int(rowc[lane].w);
           if (partial) {
+            // (stream-K: the unit's first piece marks the split slots no piece
+            // of the unit fills as empty)
+            if (I.sp == 0)
+              for (int s2 = I.np; s2 < a.num_splits; ++s2)
+                a.lse_part[(size_t)s2 * a.total_q * a.Hq + qrow] = -INFINITY;
             a.lse_part[(size_t)I.sp * a.total_q * a.Hq + qrow] = row_lse;
           } else {
             const size_t t_row = qrow / a.Hq, h_row = qrow - t_row * a.Hq;
@@ -1242,6 +1312,25 @@ cudaError_t launch_decode_rel(const KernelArgs &a, cudaStream_t stream) {
 // CTAs of a few-row decode launch (one per SM at most)
 long decode_grid(const KernelArgs &a, long items) { return std::min<long>(items, a.sms > 0 ? a.sms : items); }
 
+// The walk: stream-K when the keys are cut into several splits (and the
+// sequences fit the work-order tables).  A unit (sequence, kv head) holds at
+// most U = ceil(num_splits * split_chunk / 128) tiles, and a unit of U tiles
+// meets at most ceil(U / C) + 1 ranges of C tiles, so C >= U / (num_splits - 1)
+// keeps its pieces within the num_splits partial slots.
+void set_walk(const KernelArgs &a, DecArgs &da) {
+  da.streamk = (a.num_splits > 1 && a.batch <= kOrd && a.sms > 0) ? 1 : 0;
+  da.c_min = 0;
+  if (da.streamk) {
+    const long umax = ((long)a.num_splits * a.split_chunk + KT - 1) / KT;
+    da.c_min = (int)std::max<long>(1, (umax + a.num_splits - 2) / (a.num_splits - 1));
+  }
+}
+// stream-K: one CTA per SM (the ranges even out the work); else one per item
+// up to the SM count
+int walk_grid(const KernelArgs &a, const DecArgs &da, long items) {
+  return da.streamk ? a.sms : (int)decode_grid(a, items);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 dec_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     cudaDriverEntryPointQueryResult q;
@@ -1328,6 +1417,7 @@ cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   da.n_items = (int)items;
+  set_walk(a, da);
   CUtensorMap mq, mk, mv, mr;
   if (!encode_heads(&mq, a.q, a.Hq, a.total_q, a.group, a.max_q) ||
       !encode_heads(&mk, a.k, a.Hkv, kv_rows, 1, KT) || !encode_heads(&mv, a.v, a.Hkv, kv_rows, 1, KT))
@@ -1370,7 +1460,7 @@ cudaError_t launch_decode_few_rows(const KernelArgs &a, int kv_rows, cudaStream_
   cudaError_t e = set_max_smem_once(reinterpret_cast<const void *>(relattn_decode_tc_kernel<false>),
                                     (int)smem, attr_set);
   if (e != cudaSuccess) return e;
-  return launch_decode_kernel(relattn_decode_tc_kernel<false>, (int)decode_grid(a, items), smem, stream, da, mq,
+  return launch_decode_kernel(relattn_decode_tc_kernel<false>, walk_grid(a, da, items), smem, stream, da, mq,
                               mk, mv, mr, mp, da.rel_mode == 1);
 }
 
@@ -1387,6 +1477,7 @@ cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void 
   if (items <= 0) return cudaSuccess;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   da.n_items = (int)items;
+  set_walk(a, da);
   da.rel_mode = da.has_bias ? 1 : 0;
   da.nt_e = da.rs = da.r_bytes = 0;
   da.rslot = nullptr;
@@ -1416,7 +1507,7 @@ cudaError_t launch_decode_mxfp8(const KernelArgs &a, const void *k8, const void 
   if (e != cudaSuccess) return e;
   // (the q and r maps are not read: the producer quantises q rows itself,
   // and R comes from the R kernel)
-  return launch_decode_kernel(relattn_decode_tc_kernel<true>, (int)decode_grid(a, items), smem, stream, da, mk,
+  return launch_decode_kernel(relattn_decode_tc_kernel<true>, walk_grid(a, da, items), smem, stream, da, mk,
                               mk, mv, mk, mk, da.rel_mode == 1);
 }
 

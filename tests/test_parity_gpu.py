@@ -156,16 +156,41 @@ def test_decode_splits(Lq, splits):
 
 
 # Few-row decode bias sources: in the kernel on the tensor cores (r_dim a
-# multiple of 8, rel_extent up to 1152: 9 blocks of 128 distances, r_dim and
-# E at and past the block edges), else computed by a kernel before the decode
-# (r_dim 20, rel_extent 1500).  One token per sequence (one distance per item)
-# and two (a distance per token), full and windowed keys.
-@pytest.mark.parametrize("rd,E", [(8, 1), (64, 1152), (40, 129), (24, 640), (20, 700), (64, 1500)])
+# multiple of 8 up to 64, rel_extent a multiple of 8 up to 1024: one to eight
+# blocks of 128 distances, full and partial), else computed by a kernel
+# before the decode (E = 1, r_dim 20, E = 1032 and 1500: past the eight
+# blocks).  One token per sequence (one distance per item) and two (a
+# distance per token), full and windowed keys.
+@pytest.mark.parametrize("rd,E", [(8, 64), (16, 136), (24, 640), (40, 120), (64, 1024),
+                                  (8, 1), (20, 700), (64, 1032), (64, 1500)])
 @pytest.mark.parametrize("Lq,window", [(1, 0), (2, 0), (1, 900)])
 def test_decode_bias_sources(rd, E, Lq, window):
     ks = [2500, 1300, 129, 600 + Lq, Lq]
     _check(W.custom(f"dec_bias{rd}_{E}", [Lq] * len(ks), ks, 16, 2, rd, E, window=window), decode=True,
            num_splits=2)
+
+
+# The stream-K walk of the few-row decode (several splits, at most 64
+# sequences): CTA c takes an equal range of the units' tiles laid end to end.
+# Cases: sequences without query rows between others (units of no rows), a
+# unit far longer than the others (it meets the most ranges, up to the split
+# count), CTA counts that put range boundaries on and off unit boundaries,
+# many splits over few tiles (the range size held at its lower bound), the
+# window, and two tokens per sequence.
+@pytest.mark.parametrize("ctas,splits", [(0, 2), (0, 8), (5, 3), (7, 6), (2, 16)])
+def test_decode_stream_k_ranges(band_ctas, ctas, splits):
+    band_ctas(ctas)
+    q = [1, 0, 1, 1, 0, 1, 1, 1]
+    ks = [1, 5, 9000, 130, 777, 2048, 257, 3333]
+    _check(W.custom(f"sk{ctas}_{splits}", q, ks, 16, 2, 64, 1024), decode=True, num_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [3, 5])
+def test_decode_stream_k_window_two_tokens(band_ctas, splits):
+    band_ctas(11)
+    ks = [4100, 260, 6000, 2, 1500]
+    _check(W.custom(f"skw{splits}", [2] * len(ks), ks, 16, 2, 32, 512, window=1100), decode=True,
+           num_splits=splits)
 
 
 @pytest.mark.parametrize("window", [1, 5, 300])

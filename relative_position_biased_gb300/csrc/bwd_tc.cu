@@ -323,6 +323,21 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       tmem_ld32(tmem + lane_off + TM_ST + 64u * buf + 32u * hh, sv);
       tmem_ld32(tmem + lane_off + TM_DP + 64u * buf + 32u * hh, dv);
       tmem_wait_ld();
+      // alpha S^T + bias for this thread's 32 query rows, the bias gathered
+      // from the window at once, so the window is released (and the next
+      // band step's copy can start) before the rest of the step's work
+      if (band) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int i = 32 * hh + u;
+          sv[u] = __float_as_uint(fmaf(__uint_as_float(sv[u]), a.alpha, rw[i * RWS + (pos0 + i - j - cb)]));
+        }
+        mbar_arrive(bar(B_RW_READ));   // this thread has gathered from the window
+        ++nb;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) sv[u] = __float_as_uint(__uint_as_float(sv[u]) * a.alpha);
+      }
       uint32_t pk[16], dk2[16];
 #pragma unroll
       for (int u = 0; u < 32; u += 4) {
@@ -337,9 +352,7 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int pos = pos0 + i0 + e;
-          float x = __uint_as_float(sv[u + e]) * a.alpha;
-          if (band) x += rw[(i0 + e) * RWS + (pos - j - cb)];
-          x *= c1[e];
+          float x = __uint_as_float(sv[u + e]) * c1[e];
           if (need_mask) {
             const bool vis = j <= pos && (a.window <= 0 || pos - j < a.window);
             if (!vis) x = -INFINITY;
@@ -359,10 +372,6 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + buf));
       mbar_arrive(bar(B_AUX_EMPTY + st));
-      if (band) {
-        mbar_arrive(bar(B_RW_READ));   // this thread has gathered from the window
-        ++nb;
-      }
     }
     // ---- dK / dV rows out (zeros when no query sees the keys); the TMEM
     // loads are warp-collective, the stores only for rows inside the keys

@@ -461,33 +461,39 @@ __global__ void __launch_bounds__(256) relattn_bwd_dkv_reduce_kernel(const BwdAr
 
 // ====================================================================== dq (query-major)
 //
-// For 128 query rows of one head and the 64-key steps every row of the tile
-// sees outside the bias band (j <= p0 - E for the tile's first position p0,
-// so no bias and no dr; every visible key without a bias):
-//     S = Q K^T,  dP = dout V^T                          (tcgen05, M = 128 rows, N = 64 keys)
+// For 128 query rows of one head and the 128-key steps every row of the
+// tile sees outside the bias band (j < kend, kend = p0 - E + 1 rounded down
+// to a multiple of 64 for the tile's first position p0, so no bias and no
+// dr; every visible key without a bias):
+//     S = Q K^T,  dP = dout V^T                          (tcgen05, M = 128 rows, N = 128 keys)
 //     P = exp(s_i alpha S - lse_i),  dS' = s_i P (dP - D_i)
 //     dQ += dS' K                                          (tcgen05, A = dS' in TMEM)
 // and dq = alpha dQ.  Roles as in the dk / dv kernel, without the aux warp:
 // each elementwise thread owns one query row, so its constants stay in
-// registers.  TMEM: dQ [0,128), S buffers [128,192) / [192,256), dP buffers
-// [256,320) / [320,384); dS' (bf16 pairs) over columns [0,16) and [32,48) of
-// its S buffer.
+// registers.  128-key steps: an N = 128 instruction costs about what an
+// N = 64 one does to issue, so S and dP take half the instructions per key.
+// TMEM: dQ [0,128), S buffers [128,256) / [256,384) (dS' as bf16 pairs over
+// columns [0,32) and [64,96) of its buffer: each elementwise warp packs its
+// 64 keys over the first half of the columns it has read), one dP buffer
+// [384,512): dP of step n+1 is issued once every elementwise thread has
+// loaded dP of step n (D_DP_READ), early in that thread's step.
 constexpr int QM = 128;          // query rows per CTA (MMA M)
-constexpr int KS = 64;           // keys per step (MMA N of S / dP, K of dQ)
-constexpr int KSTAGES = 3;
-constexpr uint32_t TQ_DQ = 0, TQ_S = 128, TQ_DP = 256;
+constexpr int KS = 128;          // keys per step (MMA N of S / dP, K of dQ)
+constexpr int KSTAGES = 2;
+constexpr uint32_t TQ_DQ = 0, TQ_S = 128, TQ_DP = 384;
 constexpr uint32_t SQ_Q = 0;                            // 2 boxes [128 rows x 128 B]
 constexpr uint32_t SQ_DO = SQ_Q + 32768;
-constexpr uint32_t SQ_K = SQ_DO + 32768;                // KSTAGES x 2 boxes [64 keys x 128 B]
-constexpr uint32_t SQ_V = SQ_K + KSTAGES * 16384;
-constexpr uint32_t SQ_BAR = SQ_V + KSTAGES * 16384;
+constexpr uint32_t SQ_K = SQ_DO + 32768;                // KSTAGES x 2 boxes [128 keys x 128 B]
+constexpr uint32_t SQ_V = SQ_K + KSTAGES * 32768;
+constexpr uint32_t SQ_BAR = SQ_V + KSTAGES * 32768;
 enum {
   D_QD_FULL = 0,
   D_KV_FULL = 1,                      // + stage
   D_KV_EMPTY = D_KV_FULL + KSTAGES,   // + stage
   D_S_FULL = D_KV_EMPTY + KSTAGES,    // + buffer
   D_P_FULL = D_S_FULL + 2,            // + buffer
-  D_DONE = D_P_FULL + 2,
+  D_DP_READ = D_P_FULL + 2,
+  D_DONE = D_DP_READ + 1,
   D_DRAIN = D_DONE + 1,
   D_COUNT = D_DRAIN + 1
 };
@@ -528,8 +534,9 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
   const int kbeg = j_lo & ~(KS - 1);
   const bool has_bias = a.rd > 0 && a.E > 0;
   // without a bias every visible key; with one, the keys below the band of
-  // the tile's first row (a multiple of 64: the warp-MMA dq starts there)
-  const int kend = has_bias ? (p0 - a.E + 1 > 0 ? (p0 - a.E + 1) & ~(KS - 1) : 0) : p_end + 1;
+  // the tile's first row (a multiple of 64: the warp-MMA dq starts there);
+  // keys of the last step at or past kend are masked out
+  const int kend = has_bias ? (p0 - a.E + 1 > 0 ? (p0 - a.E + 1) & ~63 : 0) : p_end + 1;
   const int nsteps = kend > kbeg ? (kend - kbeg + KS - 1) / KS : 0;
 
   // ------------------------------------------------------------ set-up
@@ -543,6 +550,7 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
       mbar_init(bar(D_S_FULL + i), 1);
       mbar_init(bar(D_P_FULL + i), NELEM);
     }
+    mbar_init(bar(D_DP_READ), NELEM);
     mbar_init(bar(D_DONE), 1);
     mbar_init(bar(D_DRAIN), 1);
     *abort_flag = 0;
@@ -579,13 +587,13 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
             !(run = mbar_wait(bar(D_KV_EMPTY + st), ((n / KSTAGES) - 1) & 1, abort_flag, 11)))
           break;
         const int key = ck + kbeg + n * KS;
-        const uint32_t dk_ = sb + SQ_K + st * 16384, dv_ = sb + SQ_V + st * 16384;
+        const uint32_t dk_ = sb + SQ_K + st * 32768, dv_ = sb + SQ_V + st * 32768;
         if (n != a.test_skip_dq_step) {   // (test hook: a skipped step is never loaded)
-          mbar_arrive_expect_tx(bar(D_KV_FULL + st), 32768);
+          mbar_arrive_expect_tx(bar(D_KV_FULL + st), 65536);
           tma_load_3d(dk_, &map_k, 0, g, key, bar(D_KV_FULL + st));
-          tma_load_3d(dk_ + 8192, &map_k, 64, g, key, bar(D_KV_FULL + st));
+          tma_load_3d(dk_ + 16384, &map_k, 64, g, key, bar(D_KV_FULL + st));
           tma_load_3d(dv_, &map_v, 0, g, key, bar(D_KV_FULL + st));
-          tma_load_3d(dv_ + 8192, &map_v, 64, g, key, bar(D_KV_FULL + st));
+          tma_load_3d(dv_ + 16384, &map_v, 64, g, key, bar(D_KV_FULL + st));
         }
         issued = n + 1;
       }
@@ -607,20 +615,27 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
       const uint64_t dd = smem_desc_sw128(sb + SQ_DO, 16, 1024);
       for (int n = 0; n <= nsteps && ok; ++n) {
         if (n < nsteps) {
+          // S(n) into buffer n & 1 (the dQ MMA of step n - 2, which read its
+          // dS', was issued before); dP(n) once dP(n - 1) has been loaded
           const int st = n % KSTAGES, buf = n & 1;
           if (!(ok = mbar_wait(bar(D_KV_FULL + st), (n / KSTAGES) & 1, abort_flag, 13))) break;
           tc_fence_after();
-          const uint64_t kd = smem_desc_sw128(sb + SQ_K + st * 16384, 16, 1024);
-          const uint64_t vd = smem_desc_sw128(sb + SQ_V + st * 16384, 16, 1024);
-          const uint32_t d_s = tmem + TQ_S + 64u * buf, d_p = tmem + TQ_DP + 64u * buf;
+          const uint64_t kd = smem_desc_sw128(sb + SQ_K + st * 32768, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(sb + SQ_V + st * 32768, 16, 1024);
+          const uint32_t d_s = tmem + TQ_S + 128u * buf, d_p = tmem + TQ_DP;
+          // 16 dims a step: 32 bytes into a 128-byte row; the second 64 dims are
+          // the second box (16 KB on for Q / dout and for K / V)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            // 16 dims a step: 32 bytes into a 128-byte row; the second 64 dims are
-            // the second box (Q / dout: 16 KB on, K / V: 8 KB on)
             const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
-            const uint32_t bd = kk < 4 ? 2u * kk : 512u + 2u * (kk - 4);
-            mma_ss(d_s, qd + ad, kd + bd, id_s, kk > 0);
-            mma_ss(d_p, dd + ad, vd + bd, id_s, kk > 0);
+            mma_ss(d_s, qd + ad, kd + ad, id_s, kk > 0);
+          }
+          if (n >= 1 && !(ok = mbar_wait(bar(D_DP_READ), (n - 1) & 1, abort_flag, 17))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
+            mma_ss(d_p, dd + ad, vd + ad, id_s, kk > 0);
           }
           mma_commit(bar(D_S_FULL + buf));
         }
@@ -628,12 +643,12 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
           const int m = n - 1, st = m % KSTAGES, buf = m & 1;
           if (!(ok = mbar_wait(bar(D_P_FULL + buf), (m >> 1) & 1, abort_flag, 14))) break;
           tc_fence_after();
-          const uint32_t pa = tmem + TQ_S + 64u * buf;
-          // MN-major K: 16 keys a step (2 KB), the two 64-dim boxes 8 KB apart
-          const uint64_t km = smem_desc_sw128(sb + SQ_K + st * 16384, 8192, 1024);
+          const uint32_t pa = tmem + TQ_S + 128u * buf;
+          // MN-major K: 16 keys a step (2 KB), the two 64-dim boxes 16 KB apart
+          const uint64_t km = smem_desc_sw128(sb + SQ_K + st * 32768, 16384, 1024);
 #pragma unroll
-          for (int kq = 0; kq < KS / 16; ++kq)   // dS' columns: [0,16) [32,48)
-            mma_ts(tmem + TQ_DQ, pa + 8u * kq + (kq >= 2 ? 16u : 0u), km + 128u * kq, id_o,
+          for (int kq = 0; kq < KS / 16; ++kq)   // dS' columns: [0,32) keys 0..63, [64,96) keys 64..127
+            mma_ts(tmem + TQ_DQ, pa + 8u * kq + (kq >= 4 ? 32u : 0u), km + 128u * kq, id_o,
                    (m > 0 || kq > 0) ? 1u : 0u);
           mma_commit(bar(D_KV_EMPTY + st));   // the stage's K / V have been read
         }
@@ -649,9 +664,9 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
   } else if (warp >= 4) {
     // ======================================================== elementwise
     // Warp 4 + q + 4 hh (q = warp & 3) takes TMEM lanes 32 q .. 32 q + 31 (one
-    // query row a thread) and keys 32 hh .. 32 hh + 31 of each step; its dS'
-    // goes to columns [32 hh, 32 hh + 16) of the S buffer, which hold S values
-    // this same warp has already read.
+    // query row a thread) and keys 64 hh .. 64 hh + 63 of each step, in two
+    // halves of 32; its dS' goes to columns [64 hh, 64 hh + 32) of the S
+    // buffer, which hold S values this same warp has already read.
     const int hh = (warp - 4) >> 2;
     const int il = 32 * (warp & 3) + lane;             // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
@@ -668,29 +683,41 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
       ok = __all_sync(0xffffffffu, mbar_wait(bar(D_S_FULL + buf), (n >> 1) & 1, abort_flag, 15));
       if (!ok) break;
       tc_fence_after();
-      const bool need_mask = (j0 + KS - 1 > p0) || (a.window > 0 && j0 < p_end - a.window + 1);
-      uint32_t sv[32], dv[32];
-      tmem_ld32(tmem + lane_off + TQ_S + 64u * buf + 32u * hh, sv);
-      tmem_ld32(tmem + lane_off + TQ_DP + 64u * buf + 32u * hh, dv);
+      const bool need_mask =
+          (j0 + KS - 1 > p0) || (a.window > 0 && j0 < p_end - a.window + 1) || (j0 + KS > kend);
+      const uint32_t sbuf = tmem + lane_off + TQ_S + 128u * buf + 64u * hh;
+      uint32_t sv[32], dv[2][32];
+      tmem_ld32(tmem + lane_off + TQ_DP + 64u * hh, dv[0]);
+      tmem_ld32(tmem + lane_off + TQ_DP + 64u * hh + 32u, dv[1]);
+      tmem_ld32(sbuf, sv);
       tmem_wait_ld();
-      uint32_t pk[16];
+      tc_fence_before();
+      mbar_arrive(bar(D_DP_READ));   // dP(n) is in registers: dP(n + 1) may be written
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float d2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float x = __uint_as_float(sv[c + e]) * c1;
-          if (need_mask) {
-            const int j = j0 + 32 * hh + c + e;
-            const bool vis = j <= pos && (a.window <= 0 || pos - j < a.window);
-            if (!vis) x = -INFINITY;
-          }
-          const float p = fast_exp2(x - lse2);
-          d2[e] = p * (__uint_as_float(dv[c + e]) - Di) * srow;
+      for (int c = 0; c < 2; ++c) {
+        if (c == 1) {
+          tmem_ld32(sbuf + 32u, sv);
+          tmem_wait_ld();
         }
-        pk[c >> 1] = pack_bf16x2(d2[0], d2[1]);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          float d2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x = __uint_as_float(sv[u + e]) * c1;
+            if (need_mask) {
+              const int j = j0 + 64 * hh + 32 * c + u + e;
+              const bool vis = j <= pos && j < kend && (a.window <= 0 || pos - j < a.window);
+              if (!vis) x = -INFINITY;
+            }
+            const float p = fast_exp2(x - lse2);
+            d2[e] = p * (__uint_as_float(dv[c][u + e]) - Di) * srow;
+          }
+          pk[u >> 1] = pack_bf16x2(d2[0], d2[1]);
+        }
+        tmem_st16(sbuf + 16u * c, pk);   // dS' over S columns this warp has read
       }
-      tmem_st16(tmem + lane_off + TQ_S + 64u * buf + 32u * hh, pk);   // dS'
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(D_P_FULL + buf));

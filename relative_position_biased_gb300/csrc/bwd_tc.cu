@@ -200,8 +200,10 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
     __syncwarp();
   } else if (warp == 1) {
     // ======================================================== MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(B_KV_FULL), 0, abort_flag, 2);
+    // The whole warp runs the issue code (descriptors stay warp-uniform); each
+    // MMA and commit is issued by one elected lane.
+    {
+      bool ok = mbar_wait_warp(bar(B_KV_FULL), 0, abort_flag, 2);
       tc_fence_after();
       const uint32_t id_s = idesc_bf16_f32(KT, QT, 0, 0);    // S^T: K (smem, K-major) x Q (smem, K-major)
       const uint32_t id_o = idesc_bf16_f32(KT, 128, 0, 1);   // dV: P^T (tmem) x dout (smem, MN-major)
@@ -210,7 +212,7 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
       for (int n = 0; n <= nsteps && ok; ++n) {
         if (n < nsteps) {
           const int st = n % QSTAGES, buf = n & 1;
-          if (!(ok = mbar_wait(bar(B_Q_FULL + st), (n / QSTAGES) & 1, abort_flag, 3))) break;
+          if (!(ok = mbar_wait_warp(bar(B_Q_FULL + st), (n / QSTAGES) & 1, abort_flag, 3))) break;
           tc_fence_after();
           const uint64_t qd = smem_desc_sw128(sb + SM_Q + st * 16384, 16, 1024);
           const uint64_t dd = smem_desc_sw128(sb + SM_DO + st * 16384, 16, 1024);
@@ -221,14 +223,14 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
             // the second box (K / V: 16 KB on, q / dout: 8 KB on)
             const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
             const uint32_t bd = kk < 4 ? 2u * kk : 512u + 2u * (kk - 4);
-            mma_ss(d_s, kd + ad, qd + bd, id_s, kk > 0);
-            mma_ss(d_p, vd + ad, dd + bd, id_s, kk > 0);
+            mma_ss_e(d_s, kd + ad, qd + bd, id_s, kk > 0);
+            mma_ss_e(d_p, vd + ad, dd + bd, id_s, kk > 0);
           }
-          mma_commit(bar(B_S_FULL + buf));
+          mma_commit_e(bar(B_S_FULL + buf));
         }
         if (n >= 1) {
           const int m = n - 1, st = m % QSTAGES, buf = m & 1;
-          if (!(ok = mbar_wait(bar(B_P_FULL + buf), (m >> 1) & 1, abort_flag, 4))) break;
+          if (!(ok = mbar_wait_warp(bar(B_P_FULL + buf), (m >> 1) & 1, abort_flag, 4))) break;
           tc_fence_after();
           const uint32_t pa = tmem + TM_ST + 64u * buf, sa = tmem + TM_DP + 64u * buf;
           // MN-major q / dout: 16 query rows a step (2 KB), the two 64-dim boxes 8 KB apart
@@ -238,17 +240,17 @@ relattn_bwd_dkdv_tc_kernel(const __grid_constant__ BwdArgs a,
           for (int kq = 0; kq < QT / 16; ++kq) {
             const uint32_t acc = (m > 0 || kq > 0) ? 1u : 0u;
             const uint32_t ac = 8u * kq + (kq >= 2 ? 16u : 0u);   // P^T / dS^T columns: [0,16) [32,48)
-            mma_ts(tmem + TM_DV, pa + ac, om + 128u * kq, id_o, acc);
-            mma_ts(tmem + TM_DK, sa + ac, qm + 128u * kq, id_o, acc);
+            mma_ts_e(tmem + TM_DV, pa + ac, om + 128u * kq, id_o, acc);
+            mma_ts_e(tmem + TM_DK, sa + ac, qm + 128u * kq, id_o, acc);
           }
-          mma_commit(bar(B_Q_EMPTY + st));   // the stage's q / dout have been read
+          mma_commit_e(bar(B_Q_EMPTY + st));   // the stage's q / dout have been read
         }
       }
       if (ok) {
-        mma_commit(bar(B_DONE));
+        mma_commit_e(bar(B_DONE));
       } else {
         // stop: wait for the MMAs already issued before tensor memory is freed
-        mma_commit(bar(B_DRAIN));
+        mma_commit_e(bar(B_DRAIN));
         drain_wait(bar(B_DRAIN), 0);
       }
     }
@@ -606,8 +608,10 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
     __syncwarp();
   } else if (warp == 1) {
     // ======================================================== MMA issuer
-    if (lane == 0 && nsteps > 0) {
-      bool ok = mbar_wait(bar(D_QD_FULL), 0, abort_flag, 12);
+    // The whole warp runs the issue code (descriptors stay warp-uniform); each
+    // MMA and commit is issued by one elected lane.
+    if (nsteps > 0) {
+      bool ok = mbar_wait_warp(bar(D_QD_FULL), 0, abort_flag, 12);
       tc_fence_after();
       const uint32_t id_s = idesc_bf16_f32(QM, KS, 0, 0);    // S: Q (smem, K-major) x K (smem, K-major)
       const uint32_t id_o = idesc_bf16_f32(QM, 128, 0, 1);   // dQ: dS' (tmem) x K (smem, MN-major)
@@ -618,7 +622,7 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
           // S(n) into buffer n & 1 (the dQ MMA of step n - 2, which read its
           // dS', was issued before); dP(n) once dP(n - 1) has been loaded
           const int st = n % KSTAGES, buf = n & 1;
-          if (!(ok = mbar_wait(bar(D_KV_FULL + st), (n / KSTAGES) & 1, abort_flag, 13))) break;
+          if (!(ok = mbar_wait_warp(bar(D_KV_FULL + st), (n / KSTAGES) & 1, abort_flag, 13))) break;
           tc_fence_after();
           const uint64_t kd = smem_desc_sw128(sb + SQ_K + st * 32768, 16, 1024);
           const uint64_t vd = smem_desc_sw128(sb + SQ_V + st * 32768, 16, 1024);
@@ -628,35 +632,35 @@ relattn_bwd_dq_tc_kernel(const __grid_constant__ BwdArgs a,
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
-            mma_ss(d_s, qd + ad, kd + ad, id_s, kk > 0);
+            mma_ss_e(d_s, qd + ad, kd + ad, id_s, kk > 0);
           }
-          if (n >= 1 && !(ok = mbar_wait(bar(D_DP_READ), (n - 1) & 1, abort_flag, 17))) break;
+          if (n >= 1 && !(ok = mbar_wait_warp(bar(D_DP_READ), (n - 1) & 1, abort_flag, 17))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t ad = kk < 4 ? 2u * kk : 1024u + 2u * (kk - 4);
-            mma_ss(d_p, dd + ad, vd + ad, id_s, kk > 0);
+            mma_ss_e(d_p, dd + ad, vd + ad, id_s, kk > 0);
           }
-          mma_commit(bar(D_S_FULL + buf));
+          mma_commit_e(bar(D_S_FULL + buf));
         }
         if (n >= 1) {
           const int m = n - 1, st = m % KSTAGES, buf = m & 1;
-          if (!(ok = mbar_wait(bar(D_P_FULL + buf), (m >> 1) & 1, abort_flag, 14))) break;
+          if (!(ok = mbar_wait_warp(bar(D_P_FULL + buf), (m >> 1) & 1, abort_flag, 14))) break;
           tc_fence_after();
           const uint32_t pa = tmem + TQ_S + 128u * buf;
           // MN-major K: 16 keys a step (2 KB), the two 64-dim boxes 16 KB apart
           const uint64_t km = smem_desc_sw128(sb + SQ_K + st * 32768, 16384, 1024);
 #pragma unroll
           for (int kq = 0; kq < KS / 16; ++kq)   // dS' columns: [0,32) keys 0..63, [64,96) keys 64..127
-            mma_ts(tmem + TQ_DQ, pa + 8u * kq + (kq >= 4 ? 32u : 0u), km + 128u * kq, id_o,
+            mma_ts_e(tmem + TQ_DQ, pa + 8u * kq + (kq >= 4 ? 32u : 0u), km + 128u * kq, id_o,
                    (m > 0 || kq > 0) ? 1u : 0u);
-          mma_commit(bar(D_KV_EMPTY + st));   // the stage's K / V have been read
+          mma_commit_e(bar(D_KV_EMPTY + st));   // the stage's K / V have been read
         }
       }
       if (ok) {
-        mma_commit(bar(D_DONE));
+        mma_commit_e(bar(D_DONE));
       } else {
-        mma_commit(bar(D_DRAIN));
+        mma_commit_e(bar(D_DRAIN));
         drain_wait(bar(D_DRAIN), 0);
       }
     }

@@ -62,9 +62,10 @@
 //   warp 0      TMA producer (one thread): the item's q rows (a box of group
 //               heads x tokens), then K and V tiles (rings of 2-4 stages); the
 //               rings run on across items
-//   warp 1      TMEM allocator, score MMA issuer (one thread): S^T(G) into
-//               the buffer of warpgroup G % 2
-//   warp 10     P V MMA issuer (one thread): O^T += V^T P^T of tile G into
+//   warp 1      TMEM allocator, score MMA issuer (the warp runs the issue
+//               code, an elected lane issues): S^T(G) into the buffer of
+//               warpgroup G % 2
+//   warp 10     P V MMA issuer (likewise): O^T += V^T P^T of tile G into
 //               warpgroup G % 2's accumulator once its P is written
 //   warps 2-5   softmax warpgroup 0 (even tiles), warps 6-9 warpgroup 1 (odd
 //               tiles): thread = key of the tile (TMEM lane 32 (warp % 4) +
@@ -630,7 +631,9 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     __syncwarp();
   } else if (warp == 1) {
     // ====================================================== score MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue code (descriptors stay warp-uniform); each
+    // MMA and commit is issued by one elected lane.
+    {
       const uint32_t id_s = idesc_bf16_f32(KT, NR, 0, 0);    // S^T = K Q^T: K (keys x dims), q rows, both K-major
       // descriptor bases; k-step k of a 128-wide K dimension: +2 per 32 bytes
       // inside a 128-byte row, the second 64-wide half at +16 KB in a K tile
@@ -651,7 +654,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
       for (int idx = w0; idx < wN && ok; idx += wS) {
         if (load_item(idx) <= 0 || I.ntiles == 0) continue;
         const int qb = n_it & 1;
-        if (!(ok = mbar_wait(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
+        if (!(ok = mbar_wait_warp(bar(B_Q_FULL + qb), (n_it >> 1) & 1, abort_flag, 6))) break;
         const uint64_t qd = qd0 + (uint64_t)((qb * L::QBUF) >> 4);
         // in-kernel R of a band item, one 128-distance block at a time ahead
         // of the score MMAs of the tiles before the band, so that the last
@@ -665,19 +668,19 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
           if (r_done >= upto) return true;
           if (r_done == 0) {
             // P^T is in TMEM (once per CTA); the previous item's R has been read out
-            if (n_rel == 0 && !mbar_wait(bar(B_PT_READY), 0, abort_flag, 21)) return false;
-            if (n_rel > 0 && !mbar_wait(bar(B_R_FREE), (n_rel - 1) & 1, abort_flag, 22)) return false;
+            if (n_rel == 0 && !mbar_wait_warp(bar(B_PT_READY), 0, abort_flag, 21)) return false;
+            if (n_rel > 0 && !mbar_wait_warp(bar(B_R_FREE), (n_rel - 1) & 1, abort_flag, 22)) return false;
             tc_fence_after();
           }
           const uint64_t rdesc = rd0 + (uint64_t)((qb * HALF16) >> 4);
           for (; r_done < upto; ++r_done) {
             const uint32_t u = (uint32_t)(u_lo + r_done);
             const uint32_t d = tmem + TM_RS + 16u * u, pa = tmem + TM_PT + 32u * u;
-            mma_ts_c<0>(d, pa, rdesc, id_s);
-            for (int k = 1; k < r_ksteps; ++k) mma_ts_c<1>(d, pa + 8u * (uint32_t)k, rdesc + 2 * k, id_s);
+            mma_ts_e<0>(d, pa, rdesc, id_s);
+            for (int k = 1; k < r_ksteps; ++k) mma_ts_e<1>(d, pa + 8u * (uint32_t)k, rdesc + 2 * k, id_s);
           }
           if (r_done == n_u) {
-            mma_commit(bar(B_R_FULL));
+            mma_commit_e(bar(B_R_FULL));
             ++n_rel;
           }
           return true;
@@ -685,8 +688,8 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         for (int t = 0; t < I.ntiles && ok; ++t) {
           const int G = T + t, b = G & 1, st = G % L::KST;
           if (rb && t <= t_b && !(ok = issue_r(min(n_u, max(0, n_u - (t_b - 1 - t)))))) break;
-          if (G >= 2 && !(ok = mbar_wait(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
-          if (!(ok = mbar_wait(bar(B_K_FULL + st), (G / L::KST) & 1, abort_flag, 8))) break;
+          if (G >= 2 && !(ok = mbar_wait_warp(bar(B_S_FREE + b), ((G >> 1) - 1) & 1, abort_flag, 7))) break;
+          if (!(ok = mbar_wait_warp(bar(B_K_FULL + st), (G / L::KST) & 1, abort_flag, 8))) break;
           tc_fence_after();
           const uint64_t kd = kd0 + (uint64_t)((st * L::KTILE) >> 4);
           const uint32_t d = tmem + L::TM_S + L::SCOLS * (uint32_t)b;
@@ -694,21 +697,21 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
             // one product per 32-dim block, each into its own 16 columns (the
             // block scales differ, so the softmax combines them)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_f8_c<0>(d + 16u * k, kd + 2 * k, qd + 2 * k, id_s8);
+            for (int k = 0; k < 4; ++k) mma_f8_e<0>(d + 16u * k, kd + 2 * k, qd + 2 * k, id_s8);
           } else {
-            mma_ss_c<0>(d, kd + koff(0), qd + hoff(0), id_s);
+            mma_ss_e<0>(d, kd + koff(0), qd + hoff(0), id_s);
 #pragma unroll
-            for (int k = 1; k < 8; ++k) mma_ss_c<1>(d, kd + koff(k), qd + hoff(k), id_s);
+            for (int k = 1; k < 8; ++k) mma_ss_e<1>(d, kd + koff(k), qd + hoff(k), id_s);
           }
-          mma_commit(bar(B_S_FULL + b));
-          mma_commit(bar(B_K_EMPTY + st));
-          if (t == I.ntiles - 1) mma_commit(bar(B_Q_EMPTY + qb));   // the item's q rows are read
+          mma_commit_e(bar(B_S_FULL + b));
+          mma_commit_e(bar(B_K_EMPTY + st));
+          if (t == I.ntiles - 1) mma_commit_e(bar(B_Q_EMPTY + qb));   // the item's q rows are read
         }
         T += I.ntiles;
         ++n_it;
       }
       // drain: every MMA issued above has finished before TMEM is released
-      mma_commit(bar(B_DRAIN));
+      mma_commit_e(bar(B_DRAIN));
       volatile int keep_waiting = 0;
       mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 9, 400000000ll);
     }
@@ -717,8 +720,9 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     // ====================================================== PV issuer
     // A second issuing thread for the P V products, so the score MMAs of the
     // next tiles and the P V MMA of a finished tile do not wait on one
-    // another's waits (each thread's commits track only its own MMAs).
-    if (lane == 0) {
+    // another's waits (each issuing lane's commits track only its own MMAs).
+    // The whole warp runs it; an elected lane issues.
+    {
       const uint32_t id_o = idesc_bf16_f32(128, NR, 1, 0);   // O^T += V^T P^T: V^T dims-contiguous, P K-major
       const uint64_t pd0 = smem_desc_sw128(sb + L::SM_P, 16, 1024);
       const uint64_t vd0 = smem_desc_sw128(sb + (F8 ? L::SM_VB : L::SM_V), BOX, 1024);
@@ -730,23 +734,23 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
         for (int t = 0; t < I.ntiles && ok; ++t) {
           // O^T of warpgroup G % 2 (+)= V(G)^T P(G)^T; the warpgroup's first tile of the item overwrites
           const int G = T + t, st = G % L::VST, b = G & 1;
-          if (!(ok = mbar_wait(bar(B_P_FULL + b), (G >> 1) & 1, abort_flag, 4))) break;
+          if (!(ok = mbar_wait_warp(bar(B_P_FULL + b), (G >> 1) & 1, abort_flag, 4))) break;
           // (fp8: P_FULL also says the warpgroup's bf16 V tile is written)
-          if (!F8 && !(ok = mbar_wait(bar(B_V_FULL + st), (G / L::VST) & 1, abort_flag, 5))) break;
+          if (!F8 && !(ok = mbar_wait_warp(bar(B_V_FULL + st), (G / L::VST) & 1, abort_flag, 5))) break;
           tc_fence_after();
           const uint64_t vd = vd0 + (uint64_t)(((F8 ? b * 2 * BOX : st * L::KTILE)) >> 4);
           const uint64_t pd = pd0 + (uint64_t)((b * 2 * HALF16) >> 4);
           const uint32_t o = tmem + L::TM_O + 16u * (uint32_t)b;
-          if (t < 2) mma_ss_c<0>(o, vd + 0, pd + hoff(0), id_o);
-          else mma_ss_c<1>(o, vd + 0, pd + hoff(0), id_o);
+          if (t < 2) mma_ss_e<0>(o, vd + 0, pd + hoff(0), id_o);
+          else mma_ss_e<1>(o, vd + 0, pd + hoff(0), id_o);
 #pragma unroll
-          for (int k = 1; k < 8; ++k) mma_ss_c<1>(o, vd + 128 * k, pd + hoff(k), id_o);
-          mma_commit(bar(B_PV_DONE + b));
-          if (!F8) mma_commit(bar(B_V_EMPTY + st));
+          for (int k = 1; k < 8; ++k) mma_ss_e<1>(o, vd + 128 * k, pd + hoff(k), id_o);
+          mma_commit_e(bar(B_PV_DONE + b));
+          if (!F8) mma_commit_e(bar(B_V_EMPTY + st));
         }
         T += I.ntiles;
       }
-      mma_commit(bar(B_DRAIN_PV));
+      mma_commit_e(bar(B_DRAIN_PV));
       volatile int keep_waiting = 0;
       mbar_wait(bar(B_DRAIN_PV), 0, &keep_waiting, 9, 400000000ll);
     }

@@ -26,7 +26,8 @@
 //               after PV).  In the band-only prefill it also loads each
 //               item's q rows (into a K-ring slot ahead of the item's tiles)
 //               and r rows (into the r tile)
-//   warp 1      TMEM allocator; MMA issuer (one thread):  S = Q K^T (Q in
+//   warp 1      TMEM allocator; MMA issuer (the warp runs the issue code,
+//               an elected lane issues):  S = Q K^T (Q in
 //               TMEM; in the band-only prefill copied there from its K-ring
 //               slot with tcgen05.cp), R_chunk = r P_slice (both operands from
 //               shared memory), O += P V (P in TMEM)
@@ -566,7 +567,9 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
     __syncwarp();
   } else if (warp == 1) {
     // ======================================================== MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue code (descriptors stay warp-uniform); each
+    // MMA, copy and commit is issued by one elected lane.
+    {
       const uint32_t id_h = idesc_bf16_f32(BM, HN, 0, 0);       // half S: Q(tmem) x K(smem, K-major)
       const uint32_t id_f = idesc_bf16_f32(BM, BN, 0, 0);       // full S
       const uint32_t id_o = idesc_bf16_f32(BM, 128, 0, 1);      // O: P(tmem) x V(smem, MN-major)
@@ -586,105 +589,105 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       // is free again.  Every S MMA that read the previous q has landed.
       auto copy_q = [&](int vq) -> bool {
         const int st = vq % V_STAGES;
-        if (!mbar_wait(bar(B_V_FULL + st), (vq / V_STAGES) & 1, abort_flag, 6)) return false;
+        if (!mbar_wait_warp(bar(B_V_FULL + st), (vq / V_STAGES) & 1, abort_flag, 6)) return false;
         tc_fence_after();
         const uint64_t qd = kd0 + (uint64_t)((SM_V - SM_K + st * KV_STAGE_BYTES) >> 4);
-        tmem_cp_128x256b(tmem + TM_Q + 0, qd + 0);
-        tmem_cp_128x256b(tmem + TM_Q + 8, qd + 2);
-        tmem_cp_128x256b(tmem + TM_Q + 16, qd + 4);
-        tmem_cp_128x256b(tmem + TM_Q + 24, qd + 6);
-        tmem_cp_128x256b(tmem + TM_Q + 32, qd + 1024);
-        tmem_cp_128x256b(tmem + TM_Q + 40, qd + 1026);
-        tmem_cp_128x256b(tmem + TM_Q + 48, qd + 1028);
-        tmem_cp_128x256b(tmem + TM_Q + 56, qd + 1030);
-        mma_commit(bar(B_V_EMPTY + st));
+        tmem_cp_128x256b_e(tmem + TM_Q + 0, qd + 0);
+        tmem_cp_128x256b_e(tmem + TM_Q + 8, qd + 2);
+        tmem_cp_128x256b_e(tmem + TM_Q + 16, qd + 4);
+        tmem_cp_128x256b_e(tmem + TM_Q + 24, qd + 6);
+        tmem_cp_128x256b_e(tmem + TM_Q + 32, qd + 1024);
+        tmem_cp_128x256b_e(tmem + TM_Q + 40, qd + 1026);
+        tmem_cp_128x256b_e(tmem + TM_Q + 48, qd + 1028);
+        tmem_cp_128x256b_e(tmem + TM_Q + 56, qd + 1030);
+        mma_commit_e(bar(B_V_EMPTY + st));
         return true;
       };
       bool q_in = false;   // the current item's q rows are already in TMEM
       auto issue_r = [&](int c) -> bool {
         if (!rt_ready) {
-          if (!mbar_wait(bar(B_RT_FULL), n_rt & 1, abort_flag, 7)) return false;
+          if (!mbar_wait_warp(bar(B_RT_FULL), n_rt & 1, abort_flag, 7)) return false;
           rt_ready = true;
         }
         const int o = chunk_idx(c);
         const int st = o % P_STAGES;
-        if (!mbar_wait(bar(B_PS_FULL + st), (o / P_STAGES) & 1, abort_flag, 8)) return false;
+        if (!mbar_wait_warp(bar(B_PS_FULL + st), (o / P_STAGES) & 1, abort_flag, 8)) return false;
         tc_fence_after();
         const uint32_t d = tmem + TM_R + 64u * (uint32_t)(o % 3);
         const uint64_t pd = pd0 + (uint64_t)((st * 8192) >> 4);
-        mma_ss_c<0>(d, rd0, pd, id_r);
-        if (r_ksteps > 1) mma_ss_c<1>(d, rd0 + 2, pd + 128, id_r);
-        if (r_ksteps > 2) mma_ss_c<1>(d, rd0 + 4, pd + 256, id_r);
-        if (r_ksteps > 3) mma_ss_c<1>(d, rd0 + 6, pd + 384, id_r);
-        mma_commit(bar(B_R_FULL + o % 3));
+        mma_ss_e<0>(d, rd0, pd, id_r);
+        if (r_ksteps > 1) mma_ss_e<1>(d, rd0 + 2, pd + 128, id_r);
+        if (r_ksteps > 2) mma_ss_e<1>(d, rd0 + 4, pd + 256, id_r);
+        if (r_ksteps > 3) mma_ss_e<1>(d, rd0 + 6, pd + 384, id_r);
+        mma_commit_e(bar(B_R_FULL + o % 3));
         // the item's last chunk: once it lands the r tile may take the next item's rows
-        if (q_slot && c == I.c_last) mma_commit(bar(B_RT_EMPTY));   // its landing also frees P stage st (softmax arrives)
+        if (q_slot && c == I.c_last) mma_commit_e(bar(B_RT_EMPTY));   // its landing also frees P stage st (softmax arrives)
         return true;
       };
       auto issue_s = [&](int s) -> bool {
         const int t = tb + step_tile(s), st = t % K_STAGES;
-        if (!mbar_wait(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9)) return false;
+        if (!mbar_wait_warp(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9)) return false;
         tc_fence_after();
         const uint32_t qa = tmem + TM_Q;
         const uint64_t kd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
         // k-step k: dims 16k..16k+15 -> box k/4, 32 bytes per step inside the row
         if (s < I.s2) {
           const uint32_t d = tmem + TM_H + 64u * (uint32_t)(s & 1);
-          mma_ts_c<0>(d, qa + 0, kd + 0, id_h);
-          mma_ts_c<1>(d, qa + 8, kd + 2, id_h);
-          mma_ts_c<1>(d, qa + 16, kd + 4, id_h);
-          mma_ts_c<1>(d, qa + 24, kd + 6, id_h);
-          mma_ts_c<1>(d, qa + 32, kd + 1024, id_h);
-          mma_ts_c<1>(d, qa + 40, kd + 1026, id_h);
-          mma_ts_c<1>(d, qa + 48, kd + 1028, id_h);
-          mma_ts_c<1>(d, qa + 56, kd + 1030, id_h);
+          mma_ts_e<0>(d, qa + 0, kd + 0, id_h);
+          mma_ts_e<1>(d, qa + 8, kd + 2, id_h);
+          mma_ts_e<1>(d, qa + 16, kd + 4, id_h);
+          mma_ts_e<1>(d, qa + 24, kd + 6, id_h);
+          mma_ts_e<1>(d, qa + 32, kd + 1024, id_h);
+          mma_ts_e<1>(d, qa + 40, kd + 1026, id_h);
+          mma_ts_e<1>(d, qa + 48, kd + 1028, id_h);
+          mma_ts_e<1>(d, qa + 56, kd + 1030, id_h);
         } else {
           const uint32_t d = tmem + TM_S + 128u * (uint32_t)(full_idx(s) & 1);
-          mma_ts_c<0>(d, qa + 0, kd + 0, id_f);
-          mma_ts_c<1>(d, qa + 8, kd + 2, id_f);
-          mma_ts_c<1>(d, qa + 16, kd + 4, id_f);
-          mma_ts_c<1>(d, qa + 24, kd + 6, id_f);
-          mma_ts_c<1>(d, qa + 32, kd + 1024, id_f);
-          mma_ts_c<1>(d, qa + 40, kd + 1026, id_f);
-          mma_ts_c<1>(d, qa + 48, kd + 1028, id_f);
-          mma_ts_c<1>(d, qa + 56, kd + 1030, id_f);
+          mma_ts_e<0>(d, qa + 0, kd + 0, id_f);
+          mma_ts_e<1>(d, qa + 8, kd + 2, id_f);
+          mma_ts_e<1>(d, qa + 16, kd + 4, id_f);
+          mma_ts_e<1>(d, qa + 24, kd + 6, id_f);
+          mma_ts_e<1>(d, qa + 32, kd + 1024, id_f);
+          mma_ts_e<1>(d, qa + 40, kd + 1026, id_f);
+          mma_ts_e<1>(d, qa + 48, kd + 1028, id_f);
+          mma_ts_e<1>(d, qa + 56, kd + 1030, id_f);
         }
         // one commit per S group: its landing also tells the softmax warps that
         // the K stage was read (for the tile's last S) and that every MMA
         // issued before it, PV(s - 2) included, has finished
-        mma_commit(bar(B_S_FULL + step_kind(s)));
+        mma_commit_e(bar(B_S_FULL + step_kind(s)));
         return true;
       };
       // O += P V; k-step k = 16 keys = 2048 bytes of the MN-major V tile
       auto issue_pv = [&](int s) -> bool {
         const int t = vslot(step_tile(s)), st = t % V_STAGES;
-        if (!mbar_wait(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5)) return false;
+        if (!mbar_wait_warp(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5)) return false;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
         const uint32_t o = tmem + TM_O;
         if (s < I.s2) {
           const uint32_t pa = tmem + TM_H + 64u * (uint32_t)(s & 1);
-          if (s > 0) mma_ts_c<1>(o, pa + 0, vd + 0, id_o);
-          else mma_ts_c<0>(o, pa + 0, vd + 0, id_o);
-          mma_ts_c<1>(o, pa + 8, vd + 128, id_o);
-          mma_ts_c<1>(o, pa + 16, vd + 256, id_o);
-          mma_ts_c<1>(o, pa + 24, vd + 384, id_o);
+          if (s > 0) mma_ts_e<1>(o, pa + 0, vd + 0, id_o);
+          else mma_ts_e<0>(o, pa + 0, vd + 0, id_o);
+          mma_ts_e<1>(o, pa + 8, vd + 128, id_o);
+          mma_ts_e<1>(o, pa + 16, vd + 256, id_o);
+          mma_ts_e<1>(o, pa + 24, vd + 384, id_o);
         } else {
           // two halves, one per warpgroup's P (keys 0..63 / 64..127), each
           // issued as soon as that warpgroup's P is in
           const int par = full_idx(s) & 1, ph = (full_idx(s) >> 1) & 1;
           for (int h = 0; h < 2; ++h) {
-            if (!mbar_wait(bar(B_P_HALF + 2 * h + par), ph, abort_flag, 11)) return false;
+            if (!mbar_wait_warp(bar(B_P_HALF + 2 * h + par), ph, abort_flag, 11)) return false;
             tc_fence_after();
             const uint32_t pa = tmem + TM_P + 32u * h;
             const uint64_t vh = vd + 512 * h;
-            if (s > 0 || h > 0) mma_ts_c<1>(o, pa + 0, vh + 0, id_o);
-            else mma_ts_c<0>(o, pa + 0, vh + 0, id_o);
-            mma_ts_c<1>(o, pa + 8, vh + 128, id_o);
-            mma_ts_c<1>(o, pa + 16, vh + 256, id_o);
-            mma_ts_c<1>(o, pa + 24, vh + 384, id_o);
+            if (s > 0 || h > 0) mma_ts_e<1>(o, pa + 0, vh + 0, id_o);
+            else mma_ts_e<0>(o, pa + 0, vh + 0, id_o);
+            mma_ts_e<1>(o, pa + 8, vh + 128, id_o);
+            mma_ts_e<1>(o, pa + 16, vh + 256, id_o);
+            mma_ts_e<1>(o, pa + 24, vh + 384, id_o);
             // this half of the P buffer is free again once this lands
-            mma_commit(bar(B_PV_F + 2 * h + par));
+            mma_commit_e(bar(B_PV_F + 2 * h + par));
           }
         }
         // In the band, PV(s) completion is learnt from the landing of S(s + 2)
@@ -692,9 +695,9 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         // such S follows without waiting for P: the last two steps, and the step
         // before the first full step (whose S is issued after the last half
         // step's PV).  Full steps commit PV_F above.
-        if (s == I.nsteps - 2) mma_commit(bar(B_PV_TAIL));
-        if (s == I.nsteps - 1) mma_commit(bar(B_PV_TAIL + 1));
-        if (I.s2 < I.nsteps && s == I.s2 - 2) mma_commit(bar(B_PV_SW));
+        if (s == I.nsteps - 2) mma_commit_e(bar(B_PV_TAIL));
+        if (s == I.nsteps - 1) mma_commit_e(bar(B_PV_TAIL + 1));
+        if (I.s2 < I.nsteps && s == I.s2 - 2) mma_commit_e(bar(B_PV_SW));
         return true;
       };
       for (int idx = item0; idx < n_items && ok; idx += item_step) {
@@ -708,7 +711,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         if (q_in) q_in = false;
         else ok = copy_q(vb);
       } else {
-        ok = mbar_wait(bar(B_Q_READY), n_it & 1, abort_flag, 6);
+        ok = mbar_wait_warp(bar(B_Q_READY), n_it & 1, abort_flag, 6);
         tc_fence_after();
       }
       rt_ready = false;
@@ -728,10 +731,10 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           if (!switch_next && s + 1 < I.nsteps && !(ok = issue_s(s + 1))) break;
           if (s + 1 < I.s2) {
             const int c = c_new(s + 1);
-            if (!(ok = mbar_wait(bar(B_R_FREE), (hb + s) & 1, abort_flag, 10))) break;
+            if (!(ok = mbar_wait_warp(bar(B_R_FREE), (hb + s) & 1, abort_flag, 10))) break;
             if (c >= I.c_start && !(ok = issue_r(c))) break;
           }
-          if (!(ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11))) break;
+          if (!(ok = mbar_wait_warp(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11))) break;
           tc_fence_after();
           if (!(ok = issue_pv(s))) break;
           if (switch_next) {
@@ -742,7 +745,7 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
           // ---- full step: S(s+2) into the buffer of S(s) as soon as the
           // softmax has read it, then PV(s)
           if (s + 2 < I.nsteps) {
-            if (!(ok = mbar_wait(bar(B_S_READ + (full_idx(s) & 1)), (full_idx(s) >> 1) & 1, abort_flag, 19))) break;
+            if (!(ok = mbar_wait_warp(bar(B_S_READ + (full_idx(s) & 1)), (full_idx(s) >> 1) & 1, abort_flag, 19))) break;
             tc_fence_after();
             if (!(ok = issue_s(s + 2))) break;
           }
@@ -754,20 +757,20 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
         // once the last S has landed nothing reads q: the next item's q rows
         // go in now, ahead of this step's PV (if the producer has issued them
         // already; else at the next item's start)
-        if (*q_loads > n_it + 1) {
-          ok = mbar_wait(bar(B_S_FULL + step_kind(s)), step_phase(s), abort_flag, 13);
+        if (__shfl_sync(0xffffffffu, *q_loads, 0) > n_it + 1) {
+          ok = mbar_wait_warp(bar(B_S_FULL + step_kind(s)), step_phase(s), abort_flag, 13);
           tc_fence_after();
           if (ok) ok = copy_q(vb + I.ntiles + q_slot);
           q_in = ok;
         }
-        if (ok) ok = mbar_wait(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11);
+        if (ok) ok = mbar_wait_warp(bar(B_P_FULL + step_kind(s)), step_phase(s), abort_flag, 11);
         tc_fence_after();
         if (ok) ok = issue_pv(s);
       }
       finish_item();
       }
       // drain: every MMA issued above has finished before TMEM is released
-      mma_commit(bar(B_DRAIN));
+      mma_commit_e(bar(B_DRAIN));
       volatile int keep_waiting = 0;
       mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 12, 400000000ll);
     }

@@ -8,8 +8,9 @@
 // heads share every K/V tile and every mask.  Warp roles:
 //   warp 0      TMA producer (one thread): the two Q tiles once, then K and V
 //               tiles of 128 keys (2- and 3-stage rings)
-//   warp 1      TMEM allocator; MMA issuer (one thread): S_w = Q_w K^T (both
-//               operands in shared memory), O_w += P_w V (P_w in TMEM)
+//   warp 1      TMEM allocator; MMA issuer (the whole warp runs the issue
+//               code, an elected lane issues): S_w = Q_w K^T (both operands in
+//               shared memory), O_w += P_w V (P_w in TMEM)
 //   warps 2-3   idle
 //   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1: thread = row,
 //               all 128 keys of a tile
@@ -185,7 +186,9 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
       __syncwarp();
     } else if (warp == 1) {
       // ====================================================== MMA issuer
-      if (lane == 0) {
+      // The whole warp runs this (descriptors stay warp-uniform); each MMA and
+      // commit is issued by one elected lane.
+      {
         const uint32_t id_s = idesc_bf16_f32(BM, BN, 0, 0);     // S: Q (smem, K-major) x K (smem, K-major)
         const uint32_t id_o = idesc_bf16_f32(BM, 128, 0, 1);    // O: P (tmem) x V (smem, MN-major)
         // descriptor bases: +2 per 32 bytes of a 128-byte row, +1024 per 16 KB
@@ -193,39 +196,39 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
         const uint64_t qd0 = smem_desc_sw128(sb + SM_Q, 16, 1024);
         const uint64_t kd0 = smem_desc_sw128(sb + SM_K, 16, 1024);
         const uint64_t vd0 = smem_desc_sw128(sb + SM_V, BOX_BYTES, 1024);
-        bool ok = mbar_wait(bar(B_Q_FULL), 0, abort_flag, 23);
+        bool ok = mbar_wait_warp(bar(B_Q_FULL), 0, abort_flag, 23);
         auto issue_s = [&](int w, int i) -> bool {   // S_w of main tile i
           const int ks = i % K_STAGES;
-          if (w == 0 && !mbar_wait(bar(B_K_FULL + ks), (i / K_STAGES) & 1, abort_flag, 24)) return false;
+          if (w == 0 && !mbar_wait_warp(bar(B_K_FULL + ks), (i / K_STAGES) & 1, abort_flag, 24)) return false;
           const uint64_t qd = qd0 + (uint64_t)(w * (TILE_BYTES >> 4));
           const uint64_t kd = kd0 + (uint64_t)(ks * (TILE_BYTES >> 4));
           const uint32_t d = tmem + TM_S + 128u * (uint32_t)w;
-          mma_ss_c<0>(d, qd + 0, kd + 0, id_s);
-          mma_ss_c<1>(d, qd + 2, kd + 2, id_s);
-          mma_ss_c<1>(d, qd + 4, kd + 4, id_s);
-          mma_ss_c<1>(d, qd + 6, kd + 6, id_s);
-          mma_ss_c<1>(d, qd + 1024, kd + 1024, id_s);
-          mma_ss_c<1>(d, qd + 1026, kd + 1026, id_s);
-          mma_ss_c<1>(d, qd + 1028, kd + 1028, id_s);
-          mma_ss_c<1>(d, qd + 1030, kd + 1030, id_s);
-          mma_commit(bar(B_S_FULL + w));
+          mma_ss_e<0>(d, qd + 0, kd + 0, id_s);
+          mma_ss_e<1>(d, qd + 2, kd + 2, id_s);
+          mma_ss_e<1>(d, qd + 4, kd + 4, id_s);
+          mma_ss_e<1>(d, qd + 6, kd + 6, id_s);
+          mma_ss_e<1>(d, qd + 1024, kd + 1024, id_s);
+          mma_ss_e<1>(d, qd + 1026, kd + 1026, id_s);
+          mma_ss_e<1>(d, qd + 1028, kd + 1028, id_s);
+          mma_ss_e<1>(d, qd + 1030, kd + 1030, id_s);
+          mma_commit_e(bar(B_S_FULL + w));
           return true;
         };
         auto issue_pv = [&](int w, int i) -> bool {   // O_w += P_w V of main tile i
           const int vs = i % V_STAGES;
-          if (w == 0 && !mbar_wait(bar(B_V_FULL + vs), (i / V_STAGES) & 1, abort_flag, 25)) return false;
+          if (w == 0 && !mbar_wait_warp(bar(B_V_FULL + vs), (i / V_STAGES) & 1, abort_flag, 25)) return false;
           const uint64_t vd = vd0 + (uint64_t)(vs * (TILE_BYTES >> 4));
           const uint32_t o = tmem + TM_O + 128u * (uint32_t)w, pa = tmem + TM_S + 128u * (uint32_t)w;
-          if (i > 0 || a.init_from_out) mma_ts_c<1>(o, pa + 0, vd + 0, id_o);
-          else mma_ts_c<0>(o, pa + 0, vd + 0, id_o);
-          mma_ts_c<1>(o, pa + 8, vd + 128, id_o);
-          mma_ts_c<1>(o, pa + 16, vd + 256, id_o);
-          mma_ts_c<1>(o, pa + 24, vd + 384, id_o);
-          mma_ts_c<1>(o, pa + 32, vd + 512, id_o);
-          mma_ts_c<1>(o, pa + 40, vd + 640, id_o);
-          mma_ts_c<1>(o, pa + 48, vd + 768, id_o);
-          mma_ts_c<1>(o, pa + 56, vd + 896, id_o);
-          if (i == n_main - 1) mma_commit(bar(B_PV_TAIL + w));
+          if (i > 0 || a.init_from_out) mma_ts_e<1>(o, pa + 0, vd + 0, id_o);
+          else mma_ts_e<0>(o, pa + 0, vd + 0, id_o);
+          mma_ts_e<1>(o, pa + 8, vd + 128, id_o);
+          mma_ts_e<1>(o, pa + 16, vd + 256, id_o);
+          mma_ts_e<1>(o, pa + 24, vd + 384, id_o);
+          mma_ts_e<1>(o, pa + 32, vd + 512, id_o);
+          mma_ts_e<1>(o, pa + 40, vd + 640, id_o);
+          mma_ts_e<1>(o, pa + 48, vd + 768, id_o);
+          mma_ts_e<1>(o, pa + 56, vd + 896, id_o);
+          if (i == n_main - 1) mma_commit_e(bar(B_PV_TAIL + w));
           return true;
         };
         if (ok) ok = issue_s(0, 0);
@@ -234,14 +237,14 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
         // issued to read: the tensor core runs them in order
         for (int i = 0; i < n_main && ok; ++i) {
           for (int w = 0; w < 2 && ok; ++w) {
-            if (!(ok = mbar_wait(bar(B_P_FULL + w), i & 1, abort_flag, 26))) break;
+            if (!(ok = mbar_wait_warp(bar(B_P_FULL + w), i & 1, abort_flag, 26))) break;
             tc_fence_after();
             if (!(ok = issue_pv(w, i))) break;
             if (i + 1 < n_main) ok = issue_s(w, i + 1);
           }
         }
         // drain: every MMA issued above has finished before TMEM is released
-        mma_commit(bar(B_DRAIN));
+        mma_commit_e(bar(B_DRAIN));
         volatile int keep_waiting = 0;
         mbar_wait(bar(B_DRAIN), 0, &keep_waiting, 27, 400000000ll);
       }

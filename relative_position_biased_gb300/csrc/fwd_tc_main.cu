@@ -53,7 +53,7 @@ constexpr uint32_t SM_V = SM_K + K_STAGES * TILE_BYTES;
 constexpr uint32_t SM_BAR = SM_V + V_STAGES * TILE_BYTES;
 constexpr int B_Q_FULL = 0, B_K_FULL = 1, B_K_EMPTY = B_K_FULL + K_STAGES, B_V_FULL = B_K_EMPTY + K_STAGES,
               B_V_EMPTY = B_V_FULL + V_STAGES, B_S_FULL = B_V_EMPTY + V_STAGES, B_P_FULL = B_S_FULL + 2,
-              B_PV_TAIL = B_P_FULL + 2, B_DRAIN = B_PV_TAIL + 2, B_COUNT = B_DRAIN + 1;
+              B_P_HALF = B_P_FULL + 2, B_PV_TAIL = B_P_HALF + 2, B_DRAIN = B_PV_TAIL + 2, B_COUNT = B_DRAIN + 1;
 constexpr uint32_t SM_TMEM_SLOT = SM_BAR + B_COUNT * 8;
 constexpr uint32_t SM_ABORT = SM_TMEM_SLOT + 8;
 constexpr uint32_t SM_TOTAL = SM_ABORT + 8;
@@ -133,6 +133,7 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(B_S_FULL + w), 1);
       mbar_init(bar(B_P_FULL + w), 128);
+      mbar_init(bar(B_P_HALF + w), 128);
       mbar_init(bar(B_PV_TAIL + w), 1);
     }
     mbar_init(bar(B_DRAIN), 1);
@@ -214,9 +215,13 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
           mma_commit_e(bar(B_S_FULL + w));
           return true;
         };
-        auto issue_pv = [&](int w, int i) -> bool {   // O_w += P_w V of main tile i
+        // O_w += P_w V of main tile i, keys 0..63 once the softmax has written
+        // that half of P, keys 64..127 once it has written all of it
+        auto issue_pv = [&](int w, int i) -> bool {
           const int vs = i % V_STAGES;
           if (w == 0 && !mbar_wait_warp(bar(B_V_FULL + vs), (i / V_STAGES) & 1, abort_flag, 25)) return false;
+          if (!mbar_wait_warp(bar(B_P_HALF + w), i & 1, abort_flag, 30)) return false;
+          tc_fence_after();
           const uint64_t vd = vd0 + (uint64_t)(vs * (TILE_BYTES >> 4));
           const uint32_t o = tmem + TM_O + 128u * (uint32_t)w, pa = tmem + TM_S + 128u * (uint32_t)w;
           if (i > 0 || a.init_from_out) mma_ts_e<1>(o, pa + 0, vd + 0, id_o);
@@ -224,6 +229,8 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
           mma_ts_e<1>(o, pa + 8, vd + 128, id_o);
           mma_ts_e<1>(o, pa + 16, vd + 256, id_o);
           mma_ts_e<1>(o, pa + 24, vd + 384, id_o);
+          if (!mbar_wait_warp(bar(B_P_FULL + w), i & 1, abort_flag, 26)) return false;
+          tc_fence_after();
           mma_ts_e<1>(o, pa + 32, vd + 512, id_o);
           mma_ts_e<1>(o, pa + 40, vd + 640, id_o);
           mma_ts_e<1>(o, pa + 48, vd + 768, id_o);
@@ -237,8 +244,6 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
         // issued to read: the tensor core runs them in order
         for (int i = 0; i < n_main && ok; ++i) {
           for (int w = 0; w < 2 && ok; ++w) {
-            if (!(ok = mbar_wait_warp(bar(B_P_FULL + w), i & 1, abort_flag, 26))) break;
-            tc_fence_after();
             if (!(ok = issue_pv(w, i))) break;
             if (i + 1 < n_main) ok = issue_s(w, i + 1);
           }
@@ -328,37 +333,53 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
 #pragma unroll
         for (int k = 0; k < 128; ++k) x[k] = (k >= kmin && k <= kmax) ? x[k] : -INFINITY;
       }
+      // P (bf16 pairs) of keys 32c .. 32c + 31 over S_w columns [16c, 16c + 16)
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      auto p_chunk = [&](int c, float mu) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float y0, y1;
+          ffma2(y0, y1, x[32 * c + 2 * k], x[32 * c + 2 * k + 1], cqk, cqk, -mu, -mu);
+          const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+          ffma2(acc[2 * (k & 1)], acc[2 * (k & 1) + 1], e0, e1, 1.f, 1.f, acc[2 * (k & 1)], acc[2 * (k & 1) + 1]);
+          pk[k] = pack_bf16x2(e0, e1);
+        }
+        __syncwarp();
+        tmem_st16(sbuf + 16u * (uint32_t)c, pk);
+      };
+      // Where every row of the warp has a running max, the first half of P is
+      // computed against it before the tile's own max is known: that max only
+      // decides whether the running max moves (a rare rescale), and a warp in
+      // which some row's does recomputes the half.  The values are the same as
+      // computing the max first.
+      const bool spec = __all_sync(0xffffffffu, m_ref != -INFINITY);
+      if (spec) {
+        p_chunk(0, m_ref);
+        p_chunk(1, m_ref);
+      }
       const float mx = row_max(x) * cqk;
       float corr = 1.f;
-      bool rescale_o = false;
+      bool rescale_o = false, moved = false;
       if (mx > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mx != -INFINITY)) {
         const float m_new = fmaxf(m_ref, mx);
         corr = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - m_new);
         rescale_o = (m_ref != -INFINITY) && (i > 0 || a.init_from_out);
         l *= corr;
         m_ref = m_new;
+        moved = true;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P (bf16 pairs) over the first 64 columns of S_w, 32 keys at a time
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!spec || __any_sync(0xffffffffu, moved)) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float y0, y1;
-          ffma2(y0, y1, x[32 * c + 2 * k], x[32 * c + 2 * k + 1], cqk, cqk, -m_use, -m_use);
-          const float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
-          ffma2(acc[2 * (k & 1)], acc[2 * (k & 1) + 1], e0, e1, 1.f, 1.f, acc[2 * (k & 1)], acc[2 * (k & 1) + 1]);
-          pk[k] = pack_bf16x2(e0, e1);
-        }
-        __syncwarp();
-        tmem_st16(sbuf + 16u * c, pk);
+        for (int k = 0; k < 4; ++k) acc[k] = 0.f;
+        p_chunk(0, m_use);
+        p_chunk(1, m_use);
       }
-      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       // O_w is touched only when a row of this warp needs a rescale; PV_w(i-1)
       // has finished (S_w(i) was issued after it).  TMEM loads / stores are
-      // warp-collective: the whole warp rescales (rows that need not: by 1)
+      // warp-collective: the whole warp rescales (rows that need not: by 1).
+      // It happens before the first half of P is handed over: PV_w(i) starts then.
       if (__any_sync(0xffffffffu, rescale_o)) {
         const float cf = rescale_o ? corr : 1.f;
 #pragma unroll
@@ -373,6 +394,12 @@ relattn_fwd_tc_main_kernel(const __grid_constant__ KernelArgs a,
           tmem_st32(obuf + 32u * c, r);
         }
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(B_P_HALF + w));
+      p_chunk(2, m_use);
+      p_chunk(3, m_use);
+      l += (acc[0] + acc[1]) + (acc[2] + acc[3]);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_P_FULL + w));

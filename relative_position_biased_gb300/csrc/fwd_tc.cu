@@ -626,7 +626,9 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       };
       auto issue_s = [&](int s) -> bool {
         const int t = tb + step_tile(s), st = t % K_STAGES;
-        if (!mbar_wait_warp(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9)) return false;
+        // (the second half step of a tile uses the K tile the first one waited for)
+        if (!(s < I.s2 && (s & 1)) && !mbar_wait_warp(bar(B_K_FULL + st), (t / K_STAGES) & 1, abort_flag, 9))
+          return false;
         tc_fence_after();
         const uint32_t qa = tmem + TM_Q;
         const uint64_t kd = kd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
@@ -661,7 +663,8 @@ relattn_fwd_tc_kernel(const __grid_constant__ TcArgs ta,
       // O += P V; k-step k = 16 keys = 2048 bytes of the MN-major V tile
       auto issue_pv = [&](int s) -> bool {
         const int t = vslot(step_tile(s)), st = t % V_STAGES;
-        if (!mbar_wait_warp(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5)) return false;
+        if (!(s < I.s2 && (s & 1)) && !mbar_wait_warp(bar(B_V_FULL + st), (t / V_STAGES) & 1, abort_flag, 5))
+          return false;
         tc_fence_after();
         const uint64_t vd = vd0 + (uint64_t)((st * KV_STAGE_BYTES) >> 4) + (uint64_t)(step_kh(s) * 8);
         const uint32_t o = tmem + TM_O;

@@ -718,7 +718,7 @@ relattn_decode_tc_kernel(const __grid_constant__ DecArgs da,
     __syncwarp();
   } else if (warp == PV_WARP) {
     // ====================================================== PV issuer
-    // A second issuing warp for the P V products, so the score MMAs of the
+    // A second issuing thread for the P V products, so the score MMAs of the
     // next tiles and the P V MMA of a finished tile do not wait on one
     // another's waits (each issuing lane's commits track only its own MMAs).
     // The whole warp runs it; an elected lane issues.

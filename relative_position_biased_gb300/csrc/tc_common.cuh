@@ -376,7 +376,7 @@ __device__ __forceinline__ void mma_f8_c(uint32_t d_tmem, uint64_t a_desc, uint6
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 // Copy 128 rows x 32 bytes from shared memory (matrix descriptor, the same
 // format as an MMA operand's) into TMEM lanes 0..127, 8 columns from taddr.
-// Asynchronous; ordered with the issuing lane's tcgen05.mma before and after.
+// Asynchronous; ordered with the issuing thread's tcgen05.mma before and after.
 __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;\n" ::"r"(taddr), "l"(sdesc) : "memory");
 }
